@@ -1,0 +1,215 @@
+"""CPU oracle of the capacity-bounded MoE layer forward.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``. The library never imports it, and it
+imports nothing from the library.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C, fp32, fixed evaluation
+order; see its header for the steps and the passages they follow). This module
+compiles it with gcc and wraps it with ctypes; the only Python-side logic is
+array marshalling and the slot layout bookkeeping of ``route()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so next to the source (gcc, OpenMP, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-ffp-contract=off", "-fno-fast-math",
+               "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        L.oracle_exp.argtypes = [f32]
+        L.oracle_exp.restype = f32
+        L.oracle_capacity.argtypes = [i64, i64, i64, i64, i64]
+        L.oracle_capacity.restype = i64
+        L.oracle_router.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+        L.oracle_router.restype = i32
+        L.oracle_select_layout.argtypes = [i32, i32, i32, i64, i32, P, P, P, P, P, P, P, P, P, P]
+        L.oracle_select_layout.restype = i32
+        L.oracle_ffn_routes.argtypes = [i32, P, P, i32, i32, P, P, P, P, P, P]
+        L.oracle_ffn_routes.restype = i32
+        L.oracle_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
+        L.oracle_combine.restype = i32
+        L.oracle_forward_tokens.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P]
+        L.oracle_forward_tokens.restype = i32
+        L.oracle_num_threads.restype = i32
+        L.oracle_set_num_threads.argtypes = [i32]
+        _lib = L
+    return _lib
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    lib().oracle_set_num_threads(int(n))
+
+
+def exp_f32(v: np.ndarray) -> np.ndarray:
+    L = lib()
+    v = np.asarray(v, dtype=np.float32).ravel()
+    return np.array([L.oracle_exp(float(a)) for a in v], dtype=np.float32)
+
+
+def capacity(N: int, K: int, E: int, cap_num: int, cap_den: int) -> int:
+    return int(lib().oracle_capacity(N, K, E, cap_num, cap_den))
+
+
+def router(x_bits: np.ndarray, wr: np.ndarray, bias: Optional[np.ndarray], K: int,
+           renorm: bool = True, want_probs: bool = False, want_logits: bool = False):
+    """Returns (topk_ids [N,K] i32, topk_p [N,K] f32, probs [N,E] or None, logits or None)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    wr = np.ascontiguousarray(wr, dtype=np.float32)
+    N, H = x_bits.shape
+    E = wr.shape[1]
+    ids = np.empty((N, K), dtype=np.int32)
+    p = np.empty((N, K), dtype=np.float32)
+    probs = np.empty((N, E), dtype=np.float32) if want_probs else None
+    logits = np.empty((N, E), dtype=np.float32) if want_logits else None
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    rc = lib().oracle_router(N, H, E, K, int(bool(renorm)), _p(x_bits), _p(wr), _p(b), _p(ids),
+                             _p(p), _p(probs), _p(logits))
+    if rc != 0:
+        raise RuntimeError("oracle_router failed: %d" % rc)
+    return ids, p, probs, logits
+
+
+@dataclass
+class Layout:
+    cap: int
+    cpad: int
+    keep: np.ndarray             # [N,K] u8
+    expert_counts: np.ndarray    # [E]
+    kept_counts: np.ndarray      # [E]
+    sorted_slot_ids: np.ndarray  # [E*cpad]
+    expert_ids: np.ndarray       # [E*cpad/bm]
+    block_start: np.ndarray      # [E]
+    num_tokens_post_padded: int
+    token_routes: np.ndarray     # [N,K]
+
+
+def select_layout(topk_ids: np.ndarray, topk_p: np.ndarray, E: int, cap: int, bm: int) -> Layout:
+    topk_ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    topk_p = np.ascontiguousarray(topk_p, dtype=np.float32)
+    N, K = topk_ids.shape
+    cpad = (cap + bm - 1) // bm * bm
+    keep = np.empty((N, K), dtype=np.uint8)
+    ec = np.empty(E, dtype=np.int32)
+    kc = np.empty(E, dtype=np.int32)
+    ssi = np.empty(max(E * cpad, 1), dtype=np.int32)
+    eid = np.empty(max(E * cpad // bm, 1), dtype=np.int32)
+    bs = np.empty(E, dtype=np.int32)
+    ntpp = np.zeros(1, dtype=np.int32)
+    tr = np.empty((N, K), dtype=np.int32)
+    rc = lib().oracle_select_layout(N, E, K, cap, bm, _p(topk_ids), _p(topk_p), _p(keep), _p(ec),
+                                    _p(kc), _p(ssi), _p(eid), _p(bs), _p(ntpp), _p(tr))
+    if rc != 0:
+        raise RuntimeError("oracle_select_layout failed: %d" % rc)
+    return Layout(cap, cpad, keep, ec, kc, ssi[:E * cpad], eid[:E * cpad // bm], bs,
+                  int(ntpp[0]), tr)
+
+
+class ExpertWeights:
+    """Per-expert bf16 weight blocks held as pointer tables for the C side.
+
+    wg[e], wu[e]: [H,I] bit patterns; wd[e]: [I,H]. Experts not present are
+    null pointers (using one is a caller error)."""
+
+    def __init__(self, E: int, wg: Dict[int, np.ndarray], wu: Dict[int, np.ndarray],
+                 wd: Dict[int, np.ndarray]):
+        self._keep = []
+        PT = ctypes.c_void_p * E
+        self.wg, self.wu, self.wd = PT(), PT(), PT()
+        for table, src in ((self.wg, wg), (self.wu, wu), (self.wd, wd)):
+            for e, a in src.items():
+                a = np.ascontiguousarray(a, dtype=np.uint16)
+                self._keep.append(a)
+                table[e] = a.ctypes.data
+
+
+def ffn_routes(tokens: Sequence[int], experts: Sequence[int], x_bits: np.ndarray,
+               W: ExpertWeights, H: int, I: int, want_h: bool = False):
+    """FFN output o [n,H] (and activation a [n,I]) of the given (token, expert) pairs."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    experts = np.ascontiguousarray(experts, dtype=np.int32)
+    n = len(tokens)
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    o = np.empty((n, H), dtype=np.float32)
+    h = np.empty((n, I), dtype=np.float32) if want_h else None
+    rc = lib().oracle_ffn_routes(n, _p(tokens), _p(experts), H, I, _p(x_bits), W.wg, W.wu, W.wd,
+                                 _p(h), _p(o))
+    if rc != 0:
+        raise RuntimeError("oracle_ffn_routes failed: %d" % rc)
+    return (o, h) if want_h else o
+
+
+def combine(t0: int, t1: int, keep: np.ndarray, topk_p: np.ndarray, o_routes: np.ndarray) -> np.ndarray:
+    keep = np.ascontiguousarray(keep, dtype=np.uint8)
+    topk_p = np.ascontiguousarray(topk_p, dtype=np.float32)
+    o_routes = np.ascontiguousarray(o_routes, dtype=np.float32)
+    K = keep.shape[1]
+    H = o_routes.shape[-1]
+    y = np.empty((t1 - t0, H), dtype=np.float32)
+    lib().oracle_combine(t0, t1, K, H, _p(keep), _p(topk_p), _p(o_routes), _p(y))
+    return y
+
+
+def forward_tokens(t0: int, t1: int, x_bits: np.ndarray, W: ExpertWeights, H: int, I: int,
+                   topk_ids: np.ndarray, topk_p: np.ndarray, keep: np.ndarray) -> np.ndarray:
+    """Layer output y [t1-t0, H] (fp32) for tokens [t0, t1)."""
+    K = topk_ids.shape[1]
+    y = np.empty((max(t1 - t0, 0), H), dtype=np.float32)
+    rc = lib().oracle_forward_tokens(t0, t1, K, H, I, _p(np.ascontiguousarray(x_bits, dtype=np.uint16)),
+                                     W.wg, W.wu, W.wd,
+                                     _p(np.ascontiguousarray(topk_ids, dtype=np.int32)),
+                                     _p(np.ascontiguousarray(topk_p, dtype=np.float32)),
+                                     _p(np.ascontiguousarray(keep, dtype=np.uint8)), _p(y))
+    if rc != 0:
+        raise RuntimeError("oracle_forward_tokens failed: %d" % rc)
+    return y
+
+
+@dataclass
+class Routing:
+    topk_ids: np.ndarray
+    topk_p: np.ndarray
+    layout: Layout
+
+
+def route(x_bits: np.ndarray, wr: np.ndarray, bias: Optional[np.ndarray], E: int, K: int,
+          cap_num: int, cap_den: int, bm: int, renorm: bool = True) -> Routing:
+    """Steps 1-4: router, capacity, selection and layout for all tokens."""
+    N = x_bits.shape[0]
+    ids, p, _, _ = router(x_bits, wr, bias, K, renorm)
+    cap = capacity(N, K, E, cap_num, cap_den)
+    return Routing(ids, p, select_layout(ids, p, E, cap, bm))

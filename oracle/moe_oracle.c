@@ -1,0 +1,358 @@
+/*
+ * Plain, slow CPU oracle of the capacity-bounded MoE layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this file; the library path never does. It shares
+ * no code, header or constant table with the CUDA library.
+ *
+ * Steps, in the order the pages give them:
+ *   1. router: logits -> softmax -> top-K -> renormalise
+ *      (router precedes dispatch: "Permute-Free Grouped GEMM for MoE (bf16,
+ *      gfx950)", section 1 "Motivation"; the captured region "starts after
+ *      routing": "feat(cuda-graphs): capture fixed-capacity MoE execution",
+ *      "What does this PR do?")
+ *   2. source capacity ceil(N*K*F/E) ("feat(cuda-graphs) ...", "Design notes")
+ *   3. drop-and-pad: each expert keeps at most `capacity` routes, chosen by
+ *      routing probability; unused slots carry no probability (same section)
+ *   4. route-list layout: expert-sorted, block-padded sorted_slot_ids with
+ *      sentinel N, expert_ids (-1 for blocks without a kept route),
+ *      block_start, num_tokens_post_padded, token_routes ("Permute-Free ...",
+ *      section 4 "Data structures")
+ *   5. expert FFN on kept routes: FC1 on the gathered row, SwiGLU
+ *      silu(gate)*up, FC2 ("Permute-Free ...", section 3 "End-to-end flow")
+ *   6. gather-combine: each token sums its kept routes weighted by routing
+ *      probability ("Permute-Free ...", section 2 "Core idea")
+ *
+ * Floating point: fp32 throughout, as the library's contract states (fp32
+ * accumulation). Every output element is produced by one thread in a fixed
+ * order, so results do not depend on the OpenMP thread count. Build with
+ * -ffp-contract=off so that no a*b+c is fused except where fmaf() is written.
+ *
+ * Parity pins (tests/test_oracle_pins.py): capacity worked values, invariants
+ * of the layout, brute-force selection by rank counting, a dense fp64
+ * reference on tiny inputs, exp against the C library, top-K against a stable
+ * sort, and reductions to a plain SwiGLU MLP (E=1,K=1) and to a dense softmax
+ * mixture (K=E).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+static float bits_to_f32(uint32_t u) {
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* fp32 exp used by the router softmax.                                      */
+/* Cody-Waite argument reduction v = n*ln2 + r with n = rint(v*log2(e)), the */
+/* constant ln 2 split in two fp32 parts (hi = ln 2 rounded to fp32, lo = the */
+/* remainder rounded to fp32), then the degree-7 Taylor polynomial of e^r in  */
+/* Horner form with fma, then scaling by 2^n through the exponent bits.       */
+/* Domain used by the softmax: v <= 0. v < -87 returns +0.                    */
+/* ------------------------------------------------------------------------ */
+float oracle_exp(float v) {
+  if (v < -87.0f) return 0.0f;
+  const float log2e = (float)(1.0 / M_LN2);
+  const float ln2_hi = (float)M_LN2;
+  const float ln2_lo = (float)(M_LN2 - (double)ln2_hi);
+  float n = rintf(v * log2e);
+  float r = fmaf(-n, ln2_hi, v);
+  r = fmaf(-n, ln2_lo, r);
+  /* 1/k! for k = 7 .. 0, each rounded from double to fp32 */
+  float p = (float)(1.0 / 5040.0);
+  p = fmaf(p, r, (float)(1.0 / 720.0));
+  p = fmaf(p, r, (float)(1.0 / 120.0));
+  p = fmaf(p, r, (float)(1.0 / 24.0));
+  p = fmaf(p, r, (float)(1.0 / 6.0));
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  int ni = (int)n;
+  float scale = bits_to_f32((uint32_t)(ni + 127) << 23);
+  return p * scale;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 1: router.                                                           */
+/* logits l[t,e] = (sum over h ascending of x[t,h]*Wr[h,e], one fp32 fma per */
+/*   term) + b[e];                                                           */
+/* p = softmax(l): m = max_e l, z_e = exp(l_e - m), s = sum of z_e in        */
+/*   ascending e, p_e = z_e / s;                                             */
+/* top-K: K times take the largest p_e not yet taken, ties to the lower e;   */
+/* renormalise (renorm=1): d = sum of the K chosen p in pick order,          */
+/*   p'_k = p_k / d; renorm=0 keeps p'_k = p_k.                              */
+/* probs_out (optional, [N,E]) receives p; logits_out (optional) receives l. */
+/* ------------------------------------------------------------------------ */
+int oracle_router(int N, int H, int E, int K, int renorm, const uint16_t* x, const float* wr,
+                  const float* bias, int32_t* topk_ids, float* topk_p, float* probs_out,
+                  float* logits_out) {
+  if (N < 0 || H <= 0 || E <= 0 || K <= 0 || K > E) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < N; ++t) {
+    float* l = (float*)malloc(sizeof(float) * (size_t)E);
+    float* p = (float*)malloc(sizeof(float) * (size_t)E);
+    char* taken = (char*)calloc((size_t)E, 1);
+    if (!l || !p || !taken) {
+#pragma omp atomic write
+      bad = 1;
+      free(l); free(p); free(taken);
+      continue;
+    }
+    for (int e = 0; e < E; ++e) {
+      float acc = 0.0f;
+      for (int h = 0; h < H; ++h) acc = fmaf(bf16_to_f32(x[(size_t)t * H + h]), wr[(size_t)h * E + e], acc);
+      l[e] = acc + (bias ? bias[e] : 0.0f);
+    }
+    float m = l[0];
+    for (int e = 1; e < E; ++e) if (l[e] > m) m = l[e];
+    float s = 0.0f;
+    for (int e = 0; e < E; ++e) {
+      p[e] = oracle_exp(l[e] - m);
+      s = s + p[e];
+    }
+    for (int e = 0; e < E; ++e) p[e] = p[e] / s;
+    if (probs_out) memcpy(probs_out + (size_t)t * E, p, sizeof(float) * (size_t)E);
+    if (logits_out) memcpy(logits_out + (size_t)t * E, l, sizeof(float) * (size_t)E);
+    float d = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || p[e] > p[best]) best = e; /* strict '>' keeps the lower e on ties */
+      }
+      taken[best] = 1;
+      topk_ids[(size_t)t * K + k] = best;
+      topk_p[(size_t)t * K + k] = p[best];
+      d = d + p[best];
+    }
+    if (renorm)
+      for (int k = 0; k < K; ++k) topk_p[(size_t)t * K + k] = topk_p[(size_t)t * K + k] / d;
+    free(l); free(p); free(taken);
+  }
+  return bad ? -2 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 2: source capacity ceil(N*K*F/E) with F = cap_num/cap_den, in exact  */
+/* integer arithmetic.                                                       */
+/* ------------------------------------------------------------------------ */
+int64_t oracle_capacity(int64_t N, int64_t K, int64_t E, int64_t cap_num, int64_t cap_den) {
+  if (E <= 0 || cap_den <= 0 || N < 0 || K < 0 || cap_num < 0) return -1;
+  int64_t num = N * K * cap_num;
+  int64_t den = E * cap_den;
+  return (num + den - 1) / den;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Steps 3 and 4: drop-and-pad selection, then the route-list layout.        */
+/* For each expert e: the routes (t,k) with topk_ids[t,k] == e, ordered by   */
+/* (p' descending, t ascending); the first `cap` are kept, the rest dropped. */
+/* Layout with Cpad = roundup(cap, bm): expert e owns slots                  */
+/* [e*Cpad, (e+1)*Cpad); its kept tokens fill the first slots in ascending t; */
+/* the other slots hold the sentinel N.                                      */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  float p;
+  int32_t t;
+  int32_t r; /* route index t*K + k */
+} route_key;
+
+static int cmp_prob_desc_token_asc(const void* a, const void* b) {
+  const route_key* x = (const route_key*)a;
+  const route_key* y = (const route_key*)b;
+  if (x->p > y->p) return -1;
+  if (x->p < y->p) return 1;
+  return (x->t > y->t) - (x->t < y->t);
+}
+
+static int cmp_token_asc(const void* a, const void* b) {
+  const route_key* x = (const route_key*)a;
+  const route_key* y = (const route_key*)b;
+  return (x->t > y->t) - (x->t < y->t);
+}
+
+int oracle_select_layout(int N, int E, int K, int64_t cap, int bm, const int32_t* topk_ids,
+                         const float* topk_p, uint8_t* keep, int32_t* expert_counts,
+                         int32_t* kept_counts, int32_t* sorted_slot_ids, int32_t* expert_ids,
+                         int32_t* block_start, int32_t* num_tokens_post_padded,
+                         int32_t* token_routes) {
+  if (N < 0 || E <= 0 || K <= 0 || cap < 0 || bm <= 0) return -1;
+  const int64_t cpad = (cap + bm - 1) / bm * bm;
+  const int64_t R = (int64_t)N * K;
+  for (int64_t r = 0; r < R; ++r) { keep[r] = 0; token_routes[r] = -1; }
+  for (int64_t s = 0; s < (int64_t)E * cpad; ++s) sorted_slot_ids[s] = N;
+  route_key* buf = (route_key*)malloc(sizeof(route_key) * (size_t)(R > 0 ? R : 1));
+  if (!buf) return -2;
+  for (int e = 0; e < E; ++e) {
+    int64_t n = 0;
+    for (int64_t r = 0; r < R; ++r)
+      if (topk_ids[r] == e) { buf[n].p = topk_p[r]; buf[n].t = (int32_t)(r / K); buf[n].r = (int32_t)r; ++n; }
+    expert_counts[e] = (int32_t)n;
+    qsort(buf, (size_t)n, sizeof(route_key), cmp_prob_desc_token_asc);
+    int64_t kept = n < cap ? n : cap;
+    kept_counts[e] = (int32_t)kept;
+    qsort(buf, (size_t)kept, sizeof(route_key), cmp_token_asc); /* kept ones in ascending t */
+    for (int64_t j = 0; j < kept; ++j) {
+      int64_t slot = (int64_t)e * cpad + j;
+      sorted_slot_ids[slot] = buf[j].t;
+      keep[buf[j].r] = 1;
+      token_routes[buf[j].r] = (int32_t)slot;
+    }
+    block_start[e] = (int32_t)((int64_t)e * cpad / bm);
+  }
+  const int64_t nblocks = (int64_t)E * cpad / bm;
+  for (int64_t b = 0; b < nblocks; ++b) {
+    int64_t e = b / (cpad / bm);
+    int64_t first = b * bm - e * cpad; /* first slot of the block within expert e */
+    expert_ids[b] = (first < kept_counts[e]) ? (int32_t)e : -1;
+  }
+  *num_tokens_post_padded = (int32_t)((int64_t)E * cpad);
+  free(buf);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 5: expert FFN for one route: token row x[t], expert e.               */
+/*   g_i = sum_h x_h*Wg[e,h,i], u_i = sum_h x_h*Wu[e,h,i] (ascending h),     */
+/*   a_i = silu(g_i)*u_i with silu(v) = v/(1+exp(-v)),                       */
+/*   o_j = sum_i a_i*Wd[e,i,j] (ascending i).                                */
+/* wg/wu point at expert e's [H,I] block, wd at its [I,H] block (bf16 bits). */
+/* h_out (optional, [I]) receives a; o_out ([H]) receives o.                 */
+/* ------------------------------------------------------------------------ */
+static void ffn_one(int H, int I, const uint16_t* xrow, const uint16_t* wg, const uint16_t* wu,
+                    const uint16_t* wd, float* g, float* u, float* h_out, float* o_out) {
+  for (int i = 0; i < I; ++i) { g[i] = 0.0f; u[i] = 0.0f; }
+  for (int h = 0; h < H; ++h) {
+    const float xv = bf16_to_f32(xrow[h]);
+    const uint16_t* wgr = wg + (size_t)h * I;
+    const uint16_t* wur = wu + (size_t)h * I;
+    for (int i = 0; i < I; ++i) {
+      g[i] = g[i] + xv * bf16_to_f32(wgr[i]);
+      u[i] = u[i] + xv * bf16_to_f32(wur[i]);
+    }
+  }
+  for (int i = 0; i < I; ++i) {
+    const float s = g[i] / (1.0f + expf(-g[i]));
+    g[i] = s * u[i]; /* g now holds the activation a */
+    if (h_out) h_out[i] = g[i];
+  }
+  for (int j = 0; j < H; ++j) o_out[j] = 0.0f;
+  for (int i = 0; i < I; ++i) {
+    const float a = g[i];
+    const uint16_t* wdr = wd + (size_t)i * H;
+    for (int j = 0; j < H; ++j) o_out[j] = o_out[j] + a * bf16_to_f32(wdr[j]);
+  }
+}
+
+/* FFN for a list of (token, expert) pairs. Expert weights are addressed via
+ * per-expert pointer tables so callers can hold only the experts they need.
+ * h_out: [n,I] or NULL; o_out: [n,H]. */
+int oracle_ffn_routes(int n, const int32_t* tokens, const int32_t* experts, int H, int I,
+                      const uint16_t* x, const uint16_t* const* wg, const uint16_t* const* wu,
+                      const uint16_t* const* wd, float* h_out, float* o_out) {
+  int bad = 0;
+#pragma omp parallel
+  {
+    float* g = (float*)malloc(sizeof(float) * (size_t)I);
+    float* u = (float*)malloc(sizeof(float) * (size_t)I);
+    if (!g || !u) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int j = 0; j < n; ++j) {
+        const int e = experts[j];
+        ffn_one(H, I, x + (size_t)tokens[j] * H, wg[e], wu[e], wd[e], g, u,
+                h_out ? h_out + (size_t)j * I : NULL, o_out + (size_t)j * H);
+      }
+    }
+    free(g); free(u);
+  }
+  return bad ? -2 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 6: gather-combine for tokens t in [t0, t1):                          */
+/*   y[t] = sum over k = 0..K-1 with keep[t,k] of p'[t,k] * o_route[t,k],    */
+/* fp32, in k order; a token with no kept route gives y = 0.                 */
+/* o_routes: [(t1-t0)*K, H] rows, the FFN output of route (t,k) (rows of     */
+/* dropped routes are ignored).                                              */
+/* ------------------------------------------------------------------------ */
+int oracle_combine(int t0, int t1, int K, int H, const uint8_t* keep, const float* topk_p,
+                   const float* o_routes, float* y) {
+#pragma omp parallel for schedule(static)
+  for (int t = t0; t < t1; ++t) {
+    float* yr = y + (size_t)(t - t0) * H;
+    for (int j = 0; j < H; ++j) yr[j] = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      const size_t r = (size_t)t * K + k;
+      if (!keep[r]) continue;
+      const float w = topk_p[r];
+      const float* orow = o_routes + ((size_t)(t - t0) * K + k) * H;
+      for (int j = 0; j < H; ++j) yr[j] = yr[j] + w * orow[j];
+    }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Whole forward for tokens [t0, t1) given the routing of all N tokens:      */
+/* FFN of every kept route of those tokens, then the combine.                */
+/* ------------------------------------------------------------------------ */
+int oracle_forward_tokens(int t0, int t1, int K, int H, int I, const uint16_t* x,
+                          const uint16_t* const* wg, const uint16_t* const* wu,
+                          const uint16_t* const* wd, const int32_t* topk_ids,
+                          const float* topk_p, const uint8_t* keep, float* y) {
+  const int nt = t1 - t0;
+  if (nt <= 0) return 0;
+  float* o = (float*)calloc((size_t)nt * K * H, sizeof(float));
+  int32_t* tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)nt * K);
+  int32_t* ex = (int32_t*)malloc(sizeof(int32_t) * (size_t)nt * K);
+  int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)nt * K);
+  if (!o || !tok || !ex || !pos) { free(o); free(tok); free(ex); free(pos); return -2; }
+  int n = 0;
+  for (int t = t0; t < t1; ++t)
+    for (int k = 0; k < K; ++k) {
+      const size_t r = (size_t)t * K + k;
+      if (!keep[r]) continue;
+      tok[n] = t; ex[n] = topk_ids[r]; pos[n] = (t - t0) * K + k; ++n;
+    }
+  float* on = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1) * H);
+  if (!on) { free(o); free(tok); free(ex); free(pos); return -2; }
+  int rc = oracle_ffn_routes(n, tok, ex, H, I, x, wg, wu, wd, NULL, on);
+  for (int j = 0; j < n; ++j) memcpy(o + (size_t)pos[j] * H, on + (size_t)j * H, sizeof(float) * (size_t)H);
+  if (rc == 0) rc = oracle_combine(t0, t1, K, H, keep, topk_p, o, y);
+  free(on); free(o); free(tok); free(ex); free(pos);
+  return rc;
+}
