@@ -1,0 +1,189 @@
+/*
+ * moe.h: C ABI of the capacity-bounded Mixture-of-Experts layer forward on a
+ * single NVIDIA GB300 (sm_103a).
+ *
+ * Data flow, one stream, no host synchronisation, no allocation:
+ *
+ *   moe_route_align : x . W_r (+ b) -> softmax -> top-K -> renormalise
+ *                     -> per-expert counts -> drop-and-pad selection
+ *                     -> expert-sorted, block-padded route list
+ *   moe_ffn_forward : FC1 gather-GEMM (rows of x gathered by sorted_slot_ids
+ *                     inside the tile load) with SwiGLU in its epilogue, then
+ *                     FC2 grouped GEMM over the same slots
+ *   moe_combine     : each token sums its kept routes, weighted by the
+ *                     renormalised routing probability
+ *
+ * Sources ("the pages"):
+ *  [FC]  "feat(cuda-graphs): capture fixed-capacity MoE execution", NVIDIA-NeMo
+ *        Automodel #2932: Design notes (capacity, drop-and-pad, constant
+ *        per-expert row counts), What does this PR do (captured boundary).
+ *  [PF]  "Permute-Free Grouped GEMM for MoE (bf16, gfx950)", ROCm
+ *        TransformerEngine #694: section 2 Core idea (gather-in-GEMM,
+ *        contention-free gather-combine), section 3 End-to-end flow, section 4
+ *        Data structures (sorted_slot_ids, expert_ids, block_start,
+ *        num_tokens_post_padded, token_routes), section 5 Kernels.
+ *  [BK]  "[4/5] feat: capture the FFN experts at bucketed padded shapes",
+ *        vllm-project/afd-plugin #335: What this adds (a grouped GEMM takes
+ *        its grouping from a device-side count vector).
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are DEVICE pointers owned by the caller, allocated
+ *    to the static sizes given below. The library never allocates, frees,
+ *    synchronises, or reads device data on the host, so every call may be
+ *    captured in a CUDA graph ([PF] section 6 "CUDA-graph capturable").
+ *  - Row-major layouts; bf16 tensors are passed as `const void*` holding IEEE
+ *    bfloat16 values. Pointers to bf16 tensors must be 16-byte aligned.
+ *  - Return 0 on success, a negative MOE_ERR_* code otherwise. Invalid
+ *    arguments are rejected before any launch; unsupported shapes fail closed
+ *    (never a silent fallback), as [FC] Changelog / Known limitations does.
+ *  - `stream` is the CUDA stream all work is queued on (0 = legacy default).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)       /* null pointer, misaligned pointer, bad field */
+#define MOE_ERR_UNSUPPORTED_SHAPE (-2) /* shape outside what the kernels implement */
+#define MOE_ERR_WORKSPACE (-3)         /* workspace missing or smaller than required */
+#define MOE_ERR_CUDA (-4)              /* a CUDA launch or driver call failed */
+#define MOE_ERR_DEVICE (-5)            /* a kernel recorded an error (moe_device_error) */
+
+/* Layer shape and routing policy.
+ *  n_tokens  N   tokens in the batch (0 allowed: every call is a no-op)
+ *  hidden    H   model width; multiple of 128
+ *  n_experts E   1..256
+ *  top_k     K   1..min(E,16) experts per token
+ *  inter     I   SwiGLU intermediate width per expert; multiple of 128
+ *  cap_num/cap_den  capacity factor F = cap_num/cap_den (> 0); the source
+ *                capacity is cap = ceil(N*K*F/E) ([FC] Design notes)
+ *  block_m   bm  padding granularity of the route list: 16, 32, 64 or 128
+ *  renorm    1 = renormalise the K chosen probabilities to sum to 1, 0 = keep
+ *                the softmax probabilities */
+typedef struct moe_config {
+  int32_t n_tokens;
+  int32_t hidden;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t inter;
+  int32_t cap_num;
+  int32_t cap_den;
+  int32_t block_m;
+  int32_t renorm;
+} moe_config_t;
+
+/* Routing metadata written by moe_route_align ([PF] section 4). All device
+ * pointers, caller-allocated. With Cpad = roundup(cap, bm) and
+ * S = E*Cpad = moe_max_slots():
+ *  topk_ids        [N,K] i32  chosen experts, in descending probability
+ *  topk_p          [N,K] f32  renormalised routing probabilities p'
+ *  keep            [N,K] u8   1 if the route holds a slot, 0 if dropped
+ *  expert_counts   [E]   i32  routes per expert before capacity
+ *  kept_counts     [E]   i32  min(expert_counts, cap): the device-side count
+ *                             vector the GEMMs take their grouping from ([BK])
+ *  sorted_slot_ids [S]   i32  slot -> token row; expert e owns slots
+ *                             [e*Cpad, (e+1)*Cpad), kept tokens first in
+ *                             ascending token order, the rest hold the
+ *                             sentinel N (a gather of row N reads zeros)
+ *  expert_ids      [S/bm] i32 expert owning each bm-slot block, -1 for a block
+ *                             holding no kept route
+ *  block_start     [E]   i32  first block of expert e (slots start at
+ *                             block_start[e]*bm)
+ *  num_tokens_post_padded [1] i32  padded extent S, as a device scalar
+ *  token_routes    [N,K] i32  inverse map: slot of route (t,k), -1 if dropped */
+typedef struct moe_routes {
+  int32_t* topk_ids;
+  float* topk_p;
+  uint8_t* keep;
+  int32_t* expert_counts;
+  int32_t* kept_counts;
+  int32_t* sorted_slot_ids;
+  int32_t* expert_ids;
+  int32_t* block_start;
+  int32_t* num_tokens_post_padded;
+  int32_t* token_routes;
+} moe_routes_t;
+
+/* Host-side size queries (no GPU work). Negative on an invalid config. */
+int64_t moe_capacity(const moe_config_t* cfg);    /* cap = ceil(N*K*F/E) */
+int64_t moe_max_slots(const moe_config_t* cfg);   /* S = E*roundup(cap,bm) */
+int64_t moe_max_blocks(const moe_config_t* cfg);  /* S / bm */
+/* Bytes of scratch moe_route_align needs (0 when N == 0). */
+int64_t moe_route_workspace_bytes(const moe_config_t* cfg);
+
+/* Router, per-expert scan, drop-and-pad selection and route-list layout.
+ *  x        [N,H] bf16 token activations
+ *  w_router [H,E] f32 router weight; logits l[t,e] = sum_h x[t,h]*W_r[h,e]
+ *           accumulated in ascending h with one fp32 fma per term, then + b[e]
+ *  bias     [E]   f32 per-expert logit bias, or NULL for none
+ *  out      routing metadata (every field required)
+ *  workspace/ws_bytes  device scratch of at least moe_route_workspace_bytes
+ * Softmax uses the library's own fp32 exp (Cody-Waite reduction, degree-7
+ * Taylor polynomial); top-K ties go to the lower expert id; capacity keeps,
+ * per expert, the routes with the highest p', ties to the lower token index
+ * ([FC] Design notes: "selected by routing probability"). Results are
+ * bit-identical from run to run. */
+int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_router,
+                    const float* bias, const moe_routes_t* out, void* workspace,
+                    size_t ws_bytes, cudaStream_t stream);
+
+/* FC1 gather-GEMM + SwiGLU ([PF] section 2 and 3).
+ *  x    [N,H] bf16; row sorted_slot_ids[s] of x feeds slot s
+ *  w13  [E,2I,H] bf16 packed expert weights (moe_pack_w13): rows [0,I) of
+ *       expert e are W_gate[e]^T, rows [I,2I) are W_up[e]^T
+ *  h    [S,I] bf16 output, h[s,:] = silu(x_s W_gate[e]) * (x_s W_up[e]) for
+ *       s in expert e's slots; fp32 accumulation. Rows of slots at or past
+ *       roundup(kept_counts[e],16) within an expert are not written; rows of
+ *       padding slots below that bound are written as 0. */
+int moe_fc1_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                    const void* w13, void* h, cudaStream_t stream);
+
+/* FC2 grouped GEMM ([PF] section 3: FC2 reads its rows by route position).
+ *  h    [S,I] bf16 from moe_fc1_forward
+ *  w2   [E,H,I] bf16 packed (moe_pack_w2): row j of expert e is W_down[e][:,j]
+ *  o    [S,H] bf16 output, o[s,:] = h[s,:] W_down[e]; same written-row rule as h */
+int moe_fc2_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* h,
+                    const void* w2, void* o, cudaStream_t stream);
+
+/* moe_fc1_forward followed by moe_fc2_forward on the same stream. */
+int moe_ffn_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                    const void* w13, const void* w2, void* h, void* o, cudaStream_t stream);
+
+/* Contention-free gather-combine ([PF] section 2 and 5 "route_gather_combine").
+ *  o  [S,H] bf16 expert outputs;  y [N,H] bf16 output:
+ *  y[t,:] = sum over k with token_routes[t,k] >= 0 of topk_p[t,k]*o[token_routes[t,k],:]
+ *  in fp32, in k order. Dropped routes contribute nothing; a token with every
+ *  route dropped gets y = 0. Each output row is written by one CTA; no atomics. */
+int moe_combine(const moe_config_t* cfg, const moe_routes_t* routes, const void* o, void* y,
+                cudaStream_t stream);
+
+/* One-time weight packing into the K-major layouts the GEMMs read.
+ *  w_gate, w_up [E,H,I] bf16 (x . W_gate[e] is [N,I]);  w13 [E,2I,H] bf16
+ *  w_down       [E,I,H] bf16;                          w2  [E,H,I] bf16 */
+int moe_pack_w13(const moe_config_t* cfg, const void* w_gate, const void* w_up, void* w13,
+                 cudaStream_t stream);
+int moe_pack_w2(const moe_config_t* cfg, const void* w_down, void* w2, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int status);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t moe_launch_count(void);
+
+/* Reads and clears the device error word of the current device. Kernels set
+ * it (instead of trapping) when a bounded wait runs out. Synchronises the
+ * device: call outside of timed regions and outside stream capture.
+ * *out receives the word (0 = no error). Returns MOE_OK or MOE_ERR_CUDA. */
+int moe_device_error(uint32_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,237 @@
+"""Capacity-bounded Mixture-of-Experts layer forward for NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/moe.h`` (``libmoe.so``,
+built in-tree by ``_build.build()``). The binding only marshals arguments:
+every step of the layer runs in the library's CUDA kernels. PyTorch is used
+for device memory and streams. If the library is missing, every call raises;
+there is no fallback path.
+
+Typical use (all tensors on one CUDA device)::
+
+    cfg = Config(n_tokens=N, hidden=H, n_experts=E, top_k=K, inter=I,
+                 cap_num=5, cap_den=4, block_m=32)
+    routes = alloc_routes(cfg, device)
+    ws = alloc_workspace(cfg, device)
+    pack_w13(cfg, w_gate, w_up, w13); pack_w2(cfg, w_down, w2)   # once
+    route_align(cfg, x, w_router, bias, routes, ws)
+    ffn_forward(cfg, routes, x, w13, w2, h, o)
+    combine(cfg, routes, o, y)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = [
+    "Config", "Routes", "MoEError", "lib", "library_path", "alloc_routes", "alloc_workspace",
+    "alloc_buffers", "capacity", "max_slots", "max_blocks", "route_workspace_bytes",
+    "route_align", "fc1_forward", "fc2_forward", "ffn_forward", "combine", "pack_w13",
+    "pack_w2", "status_string", "launch_count", "device_error", "forward",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libmoe.so")
+_lib = None
+
+MOE_OK = 0
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__("%s failed: %d (%s)" % (fn, status, status_string(status)))
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    """Mirror of moe_config_t."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "n_tokens", "hidden", "n_experts", "top_k", "inter", "cap_num", "cap_den", "block_m",
+        "renorm")]
+
+    def __init__(self, n_tokens, hidden, n_experts, top_k, inter, cap_num=1, cap_den=1,
+                 block_m=32, renorm=1):
+        super().__init__(n_tokens, hidden, n_experts, top_k, inter, cap_num, cap_den, block_m,
+                         renorm)
+
+
+class _RoutesC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "topk_ids", "topk_p", "keep", "expert_counts", "kept_counts", "sorted_slot_ids",
+        "expert_ids", "block_start", "num_tokens_post_padded", "token_routes")]
+
+
+class Routes:
+    """Routing metadata tensors (device), allocated to the static bounds."""
+    FIELDS = _RoutesC._fields_
+
+    def __init__(self, **tensors):
+        for name, _ in self.FIELDS:
+            setattr(self, name, tensors[name])
+
+    def c(self) -> _RoutesC:
+        return _RoutesC(*[getattr(self, n).data_ptr() for n, _ in self.FIELDS])
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libmoe.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libmoe.so is not built (run __graft_entry__.build() or "
+                               "python -m mixture_experts_routing_gb300._build)")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        CP = ctypes.POINTER(Config)
+        RP = ctypes.POINTER(_RoutesC)
+        for name in ("moe_capacity", "moe_max_slots", "moe_max_blocks", "moe_route_workspace_bytes"):
+            getattr(L, name).argtypes = [CP]
+            getattr(L, name).restype = I64
+        L.moe_route_align.argtypes = [CP, P, P, P, RP, P, SZ, P]
+        L.moe_fc1_forward.argtypes = [CP, RP, P, P, P, P]
+        L.moe_fc2_forward.argtypes = [CP, RP, P, P, P, P]
+        L.moe_ffn_forward.argtypes = [CP, RP, P, P, P, P, P, P]
+        L.moe_combine.argtypes = [CP, RP, P, P, P]
+        L.moe_pack_w13.argtypes = [CP, P, P, P, P]
+        L.moe_pack_w2.argtypes = [CP, P, P, P]
+        for name in ("moe_route_align", "moe_fc1_forward", "moe_fc2_forward", "moe_ffn_forward",
+                     "moe_combine", "moe_pack_w13", "moe_pack_w2"):
+            getattr(L, name).restype = I32
+        L.moe_status_string.argtypes = [I32]
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_launch_count.argtypes = []
+        L.moe_launch_count.restype = ctypes.c_uint64
+        L.moe_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        L.moe_device_error.restype = I32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != MOE_OK:
+        raise MoEError(fn, status)
+
+
+def _q(fn: str, cfg: Config) -> int:
+    v = getattr(lib(), fn)(ctypes.byref(cfg))
+    if v < 0:
+        raise MoEError(fn, int(v))
+    return int(v)
+
+
+def capacity(cfg: Config) -> int:
+    return _q("moe_capacity", cfg)
+
+
+def max_slots(cfg: Config) -> int:
+    return _q("moe_max_slots", cfg)
+
+
+def max_blocks(cfg: Config) -> int:
+    return _q("moe_max_blocks", cfg)
+
+
+def route_workspace_bytes(cfg: Config) -> int:
+    return _q("moe_route_workspace_bytes", cfg)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def alloc_routes(cfg: Config, device) -> Routes:
+    import torch
+    N, K, E = max(cfg.n_tokens, 1), cfg.top_k, cfg.n_experts  # >= 1 row: non-null pointers
+    S, B = max_slots(cfg), max_blocks(cfg)
+    i32 = dict(dtype=torch.int32, device=device)
+    return Routes(
+        topk_ids=torch.empty((N, K), **i32), topk_p=torch.empty((N, K), dtype=torch.float32, device=device),
+        keep=torch.empty((N, K), dtype=torch.uint8, device=device),
+        expert_counts=torch.empty(E, **i32), kept_counts=torch.empty(E, **i32),
+        sorted_slot_ids=torch.empty(max(S, 1), **i32), expert_ids=torch.empty(max(B, 1), **i32),
+        block_start=torch.empty(E, **i32), num_tokens_post_padded=torch.empty(1, **i32),
+        token_routes=torch.empty((N, K), **i32))
+
+
+def alloc_workspace(cfg: Config, device):
+    import torch
+    return torch.empty(max(route_workspace_bytes(cfg), 256), dtype=torch.uint8, device=device)
+
+
+def alloc_buffers(cfg: Config, device):
+    """h [S,I], o [S,H] and y [N,H] bf16 buffers for one forward."""
+    import torch
+    S = max(max_slots(cfg), 1)
+    bf = dict(dtype=torch.bfloat16, device=device)
+    return (torch.empty((S, cfg.inter), **bf), torch.empty((S, cfg.hidden), **bf),
+            torch.empty((max(cfg.n_tokens, 1), cfg.hidden), **bf))
+
+
+def route_align(cfg: Config, x, w_router, bias, routes: Routes, workspace, stream=None) -> None:
+    rc = lib().moe_route_align(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias),
+                               ctypes.byref(routes.c()), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("moe_route_align", rc)
+
+
+def fc1_forward(cfg: Config, routes: Routes, x, w13, h, stream=None) -> None:
+    _check("moe_fc1_forward", lib().moe_fc1_forward(ctypes.byref(cfg), ctypes.byref(routes.c()),
+                                                    _ptr(x), _ptr(w13), _ptr(h), _stream(stream)))
+
+
+def fc2_forward(cfg: Config, routes: Routes, h, w2, o, stream=None) -> None:
+    _check("moe_fc2_forward", lib().moe_fc2_forward(ctypes.byref(cfg), ctypes.byref(routes.c()),
+                                                    _ptr(h), _ptr(w2), _ptr(o), _stream(stream)))
+
+
+def ffn_forward(cfg: Config, routes: Routes, x, w13, w2, h, o, stream=None) -> None:
+    _check("moe_ffn_forward", lib().moe_ffn_forward(ctypes.byref(cfg), ctypes.byref(routes.c()),
+                                                    _ptr(x), _ptr(w13), _ptr(w2), _ptr(h), _ptr(o),
+                                                    _stream(stream)))
+
+
+def combine(cfg: Config, routes: Routes, o, y, stream=None) -> None:
+    _check("moe_combine", lib().moe_combine(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(o),
+                                            _ptr(y), _stream(stream)))
+
+
+def pack_w13(cfg: Config, w_gate, w_up, w13, stream=None) -> None:
+    _check("moe_pack_w13", lib().moe_pack_w13(ctypes.byref(cfg), _ptr(w_gate), _ptr(w_up),
+                                              _ptr(w13), _stream(stream)))
+
+
+def pack_w2(cfg: Config, w_down, w2, stream=None) -> None:
+    _check("moe_pack_w2", lib().moe_pack_w2(ctypes.byref(cfg), _ptr(w_down), _ptr(w2),
+                                            _stream(stream)))
+
+
+def forward(cfg: Config, x, w_router, bias, w13, w2, routes: Routes, workspace, h, o, y,
+            stream=None) -> None:
+    """The whole layer: route_align, ffn_forward, combine (three C calls)."""
+    route_align(cfg, x, w_router, bias, routes, workspace, stream)
+    ffn_forward(cfg, routes, x, w13, w2, h, o, stream)
+    combine(cfg, routes, o, y, stream)
+
+
+def launch_count() -> int:
+    return int(lib().moe_launch_count())
+
+
+def device_error() -> int:
+    v = ctypes.c_uint32(0)
+    _check("moe_device_error", lib().moe_device_error(ctypes.byref(v)))
+    return int(v.value)

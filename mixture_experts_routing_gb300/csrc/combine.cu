@@ -1,0 +1,113 @@
+// Contention-free gather-combine and the one-time weight packing transposes.
+//
+// Combine: "Permute-Free Grouped GEMM for MoE (bf16, gfx950)", section 2 Core
+// idea and section 5 (route_gather_combine): each output token pulls its own
+// routes through the token_routes inverse map and reduces them in registers,
+// instead of expert outputs being scattered with atomics. One CTA per token
+// row; 16-byte vector loads and stores; fp32 accumulation in k order.
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kCombineThreads = 128;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  // round-to-nearest-even; values are finite
+  uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  ua = (ua + 0x7FFFu + ((ua >> 16) & 1u)) >> 16;
+  ub = (ub + 0x7FFFu + ((ub >> 16) & 1u)) >> 16;
+  return ua | (ub << 16);
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+    const uint16_t* __restrict__ o, const int32_t* __restrict__ token_routes,
+    const float* __restrict__ topk_p, uint16_t* __restrict__ y, int N, int H, int K) {
+  const int t = blockIdx.x;
+  int slot[KMAX];
+  float w[KMAX];
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    slot[k] = (k < K) ? token_routes[(size_t)t * K + k] : -1;
+    w[k] = (k < K) ? topk_p[(size_t)t * K + k] : 0.0f;
+  }
+  const int nv = H / 8;
+  for (int v = threadIdx.x; v < nv; v += kCombineThreads) {
+    uint4 in[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (slot[k] >= 0) in[k] = __ldg(reinterpret_cast<const uint4*>(o + (size_t)slot[k] * H) + v);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (slot[k] < 0) continue;
+      float f[8];
+      bf16x8_to_f32(in[k], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(w[k], f[i], acc[i]);
+    }
+    uint4 out;
+    out.x = pack_bf16x2(acc[0], acc[1]);
+    out.y = pack_bf16x2(acc[2], acc[3]);
+    out.z = pack_bf16x2(acc[4], acc[5]);
+    out.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(y + (size_t)t * H)[v] = out;
+  }
+}
+
+__global__ void transpose_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int R,
+                                 int C, int64_t in_es, int64_t out_es, int64_t out_off) {
+  __shared__ uint16_t tile[32][33];
+  const int e = blockIdx.z;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const uint16_t* src = in + (size_t)e * in_es;
+  uint16_t* dst = out + (size_t)e * out_es + out_off;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < R && c < C) tile[i][threadIdx.x] = src[(size_t)r * C + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < R && c < C) dst[(size_t)c * R + r] = tile[threadIdx.x][i];
+  }
+}
+
+}  // namespace
+
+int launch_combine(const CombineArgs& a, cudaStream_t s) {
+  if (a.N <= 0) return 0;
+  if (a.K <= 2)
+    combine_kernel<2><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
+  else if (a.K <= 4)
+    combine_kernel<4><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
+  else if (a.K <= 8)
+    combine_kernel<8><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
+  else
+    combine_kernel<16><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? 1 : -(int)err;
+}
+
+int launch_transpose(const uint16_t* in, uint16_t* out, int E, int R, int C, int64_t in_es,
+                     int64_t out_es, int64_t out_off, cudaStream_t s) {
+  if (E <= 0 || R <= 0 || C <= 0) return 0;
+  dim3 grid((C + 31) / 32, (R + 31) / 32, E);
+  transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(in, out, R, C, in_es, out_es, out_off);
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? 1 : -(int)err;
+}
+
+}  // namespace moe

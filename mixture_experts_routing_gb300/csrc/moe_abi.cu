@@ -1,0 +1,279 @@
+// C ABI of the library (declared in include/moe.h): argument checks, workspace
+// carving, and the launch sequence of each entry point. No allocation, no
+// host synchronisation, no device-to-host reads (except moe_device_error, which
+// is documented as a synchronising diagnostic).
+#include <atomic>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// Device error word: kernels OR flags into it instead of trapping.
+__device__ uint32_t g_moe_error_word;
+
+uint32_t* error_word_ptr() {
+  static std::mutex mu;
+  static uint32_t* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t roundup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+// Fields valid and shape inside what the kernels implement.
+int check_cfg(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->n_tokens < 0 || c->hidden <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->inter <= 0 ||
+      c->cap_den <= 0 || c->cap_num < 0 || (c->renorm != 0 && c->renorm != 1) ||
+      c->top_k > c->n_experts)
+    return MOE_ERR_INVALID_ARG;
+  if (c->block_m != 16 && c->block_m != 32 && c->block_m != 64 && c->block_m != 128)
+    return MOE_ERR_INVALID_ARG;
+  if (c->cap_num == 0) return MOE_ERR_UNSUPPORTED_SHAPE;  // dropless mode: not in this build
+  if (c->hidden % 128 != 0 || c->inter % 128 != 0 || c->n_experts > moe::kMaxExperts ||
+      c->top_k > moe::kMaxTopK || c->n_tokens > moe::kMaxTokens)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int64_t cap = ((int64_t)c->n_tokens * c->top_k * c->cap_num + (int64_t)c->n_experts * c->cap_den - 1) /
+                      ((int64_t)c->n_experts * c->cap_den);
+  const int64_t S = (int64_t)c->n_experts * roundup(cap, c->block_m);
+  if (S > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int64_t cap_of(const moe_config_t* c) {
+  return ((int64_t)c->n_tokens * c->top_k * c->cap_num + (int64_t)c->n_experts * c->cap_den - 1) /
+         ((int64_t)c->n_experts * c->cap_den);
+}
+
+int64_t cpad_of(const moe_config_t* c) { return roundup(cap_of(c), c->block_m); }
+
+struct WsLayout {
+  size_t logits, chunk_rank, chunk_counts, chunk_off, expert_off, route_list, total;
+};
+
+WsLayout ws_layout(const moe_config_t* c) {
+  WsLayout w{};
+  const int64_t N = c->n_tokens, E = c->n_experts, K = c->top_k;
+  const int64_t C = (N + moe::kTokensPerChunk - 1) / moe::kTokensPerChunk;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  w.logits = take((size_t)(N * E) * 4);
+  w.chunk_rank = take((size_t)(N * K) * 4);
+  w.chunk_counts = take((size_t)(C * E) * 4);
+  w.chunk_off = take((size_t)(C * E) * 4);
+  w.expert_off = take((size_t)(E + 1) * 4);
+  w.route_list = take((size_t)(N * K) * 4);
+  w.total = off;
+  return w;
+}
+
+bool routes_complete(const moe_routes_t* r) {
+  return r && r->topk_ids && r->topk_p && r->keep && r->expert_counts && r->kept_counts &&
+         r->sorted_slot_ids && r->expert_ids && r->block_start && r->num_tokens_post_padded &&
+         r->token_routes;
+}
+
+int finish(int launched) {
+  if (launched < 0) return MOE_ERR_CUDA;
+  g_launches.fetch_add((uint64_t)launched, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t moe_capacity(const moe_config_t* cfg) {
+  const int rc = check_cfg(cfg);
+  return rc != MOE_OK ? rc : cap_of(cfg);
+}
+
+int64_t moe_max_slots(const moe_config_t* cfg) {
+  const int rc = check_cfg(cfg);
+  return rc != MOE_OK ? rc : (int64_t)cfg->n_experts * cpad_of(cfg);
+}
+
+int64_t moe_max_blocks(const moe_config_t* cfg) {
+  const int rc = check_cfg(cfg);
+  return rc != MOE_OK ? rc : (int64_t)cfg->n_experts * cpad_of(cfg) / cfg->block_m;
+}
+
+int64_t moe_route_workspace_bytes(const moe_config_t* cfg) {
+  const int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  return (int64_t)ws_layout(cfg).total;
+}
+
+int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_router,
+                    const float* bias, const moe_routes_t* out, void* workspace, size_t ws_bytes,
+                    cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!routes_complete(out)) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_tokens > 0 && (!x || !w_router || !aligned16(x))) return MOE_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(cfg);
+  if (!workspace || ws_bytes < w.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  moe::RouteArgs a{};
+  a.N = cfg->n_tokens;
+  a.H = cfg->hidden;
+  a.E = cfg->n_experts;
+  a.K = cfg->top_k;
+  a.renorm = cfg->renorm;
+  a.bm = cfg->block_m;
+  a.cap = cap_of(cfg);
+  a.cpad = cpad_of(cfg);
+  a.x = static_cast<const uint16_t*>(x);
+  a.wr = w_router;
+  a.bias = bias;
+  a.topk_ids = out->topk_ids;
+  a.topk_p = out->topk_p;
+  a.keep = out->keep;
+  a.expert_counts = out->expert_counts;
+  a.kept_counts = out->kept_counts;
+  a.sorted_slot_ids = out->sorted_slot_ids;
+  a.expert_ids = out->expert_ids;
+  a.block_start = out->block_start;
+  a.ntpp = out->num_tokens_post_padded;
+  a.token_routes = out->token_routes;
+  a.ws.logits = reinterpret_cast<float*>(ws + w.logits);
+  a.ws.chunk_rank = reinterpret_cast<int32_t*>(ws + w.chunk_rank);
+  a.ws.chunk_counts = reinterpret_cast<int32_t*>(ws + w.chunk_counts);
+  a.ws.chunk_off = reinterpret_cast<int32_t*>(ws + w.chunk_off);
+  a.ws.expert_off = reinterpret_cast<int32_t*>(ws + w.expert_off);
+  a.ws.route_list = reinterpret_cast<int32_t*>(ws + w.route_list);
+  return finish(moe::launch_route(a, stream));
+}
+
+static int gemm_common(const moe_config_t* cfg, const moe_routes_t* routes, const void* act,
+                       const void* w, void* out, int fc1, cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!routes || !routes->sorted_slot_ids || !routes->kept_counts || !routes->block_start)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->n_tokens == 0) return MOE_OK;
+  if (!act || !w || !out || !aligned16(act) || !aligned16(w) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  uint32_t* err = error_word_ptr();
+  if (!err) return MOE_ERR_CUDA;
+  moe::GemmArgs a{};
+  a.fc1 = fc1;
+  a.N = cfg->n_tokens;
+  a.H = cfg->hidden;
+  a.E = cfg->n_experts;
+  a.I = cfg->inter;
+  a.bm = cfg->block_m;
+  a.cpad = cpad_of(cfg);
+  a.act = act;
+  a.w = w;
+  a.out = out;
+  a.act_rows = fc1 ? cfg->n_tokens : (int64_t)cfg->n_experts * a.cpad;
+  a.sorted_slot_ids = routes->sorted_slot_ids;
+  a.kept_counts = routes->kept_counts;
+  a.block_start = routes->block_start;
+  a.err = err;
+  return finish(moe::launch_gemm(a, stream));
+}
+
+int moe_fc1_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                    const void* w13, void* h, cudaStream_t stream) {
+  return gemm_common(cfg, routes, x, w13, h, 1, stream);
+}
+
+int moe_fc2_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* h,
+                    const void* w2, void* o, cudaStream_t stream) {
+  return gemm_common(cfg, routes, h, w2, o, 0, stream);
+}
+
+int moe_ffn_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                    const void* w13, const void* w2, void* h, void* o, cudaStream_t stream) {
+  const int rc = moe_fc1_forward(cfg, routes, x, w13, h, stream);
+  if (rc != MOE_OK) return rc;
+  return moe_fc2_forward(cfg, routes, h, w2, o, stream);
+}
+
+int moe_combine(const moe_config_t* cfg, const moe_routes_t* routes, const void* o, void* y,
+                cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!routes || !routes->token_routes || !routes->topk_p) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_tokens == 0) return MOE_OK;
+  if (!o || !y || !aligned16(o) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  moe::CombineArgs a{};
+  a.N = cfg->n_tokens;
+  a.H = cfg->hidden;
+  a.K = cfg->top_k;
+  a.o = static_cast<const uint16_t*>(o);
+  a.token_routes = routes->token_routes;
+  a.topk_p = routes->topk_p;
+  a.y = static_cast<uint16_t*>(y);
+  return finish(moe::launch_combine(a, stream));
+}
+
+int moe_pack_w13(const moe_config_t* cfg, const void* w_gate, const void* w_up, void* w13,
+                 cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!w_gate || !w_up || !w13) return MOE_ERR_INVALID_ARG;
+  const int E = cfg->n_experts, H = cfg->hidden, I = cfg->inter;
+  const int64_t in_es = (int64_t)H * I, out_es = 2 * (int64_t)H * I;
+  int l1 = moe::launch_transpose(static_cast<const uint16_t*>(w_gate), static_cast<uint16_t*>(w13),
+                                 E, H, I, in_es, out_es, 0, stream);
+  if (l1 < 0) return MOE_ERR_CUDA;
+  int l2 = moe::launch_transpose(static_cast<const uint16_t*>(w_up), static_cast<uint16_t*>(w13), E,
+                                 H, I, in_es, out_es, (int64_t)I * H, stream);
+  if (l2 < 0) return MOE_ERR_CUDA;
+  return finish(l1 + l2);
+}
+
+int moe_pack_w2(const moe_config_t* cfg, const void* w_down, void* w2, cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!w_down || !w2) return MOE_ERR_INVALID_ARG;
+  const int E = cfg->n_experts, H = cfg->hidden, I = cfg->inter;
+  return finish(moe::launch_transpose(static_cast<const uint16_t*>(w_down), static_cast<uint16_t*>(w2),
+                                      E, I, H, (int64_t)I * H, (int64_t)I * H, 0, stream));
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA launch or driver error";
+    case MOE_ERR_DEVICE: return "device-side error recorded";
+    default: return "unknown status";
+  }
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_device_error(uint32_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  uint32_t v = 0, zero = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_moe_error_word, sizeof v) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_moe_error_word, &zero, sizeof zero) != cudaSuccess) return MOE_ERR_CUDA;
+  *out = v;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// Internal launch interface between the C ABI (moe_abi.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kTokensPerChunk = 64;   // tokens per router CTA = one scan chunk
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 16;
+constexpr int kMaxTokens = 24576;     // select kernel stages one expert's routes in smem
+
+struct RouteWs {
+  float* logits;          // [N,E]
+  int32_t* chunk_rank;    // [N,K] rank of route among same-expert routes of its chunk
+  int32_t* chunk_counts;  // [C,E]
+  int32_t* chunk_off;     // [C,E] routes of expert e in chunks before c
+  int32_t* expert_off;    // [E+1] exclusive scan of expert_counts
+  int32_t* route_list;    // [N*K] route indices grouped by expert, ascending token
+};
+
+struct RouteArgs {
+  int N, H, E, K, renorm, bm;
+  int64_t cap, cpad;
+  const uint16_t* x;
+  const float* wr;
+  const float* bias;
+  int32_t* topk_ids;
+  float* topk_p;
+  uint8_t* keep;
+  int32_t* expert_counts;
+  int32_t* kept_counts;
+  int32_t* sorted_slot_ids;
+  int32_t* expert_ids;
+  int32_t* block_start;
+  int32_t* ntpp;
+  int32_t* token_routes;
+  RouteWs ws;
+};
+
+// Returns the number of kernels launched (>= 0) or a negative cudaError_t.
+int launch_route(const RouteArgs& a, cudaStream_t s);
+
+struct GemmArgs {
+  int fc1;               // 1: FC1 gather + SwiGLU epilogue; 0: FC2 plain epilogue
+  int N, H, E, I, bm;
+  int64_t cpad;
+  const void* act;       // FC1: x [N,H]; FC2: h [S,I]
+  const void* w;         // FC1: w13 [E,2I,H]; FC2: w2 [E,H,I]
+  void* out;             // FC1: h [S,I]; FC2: o [S,H]
+  int64_t act_rows;      // rows of act (N for FC1, S for FC2)
+  const int32_t* sorted_slot_ids;
+  const int32_t* kept_counts;
+  const int32_t* block_start;
+  uint32_t* err;
+};
+
+int launch_gemm(const GemmArgs& a, cudaStream_t s);
+
+struct CombineArgs {
+  int N, H, K;
+  const uint16_t* o;
+  const int32_t* token_routes;
+  const float* topk_p;
+  uint16_t* y;
+};
+
+int launch_combine(const CombineArgs& a, cudaStream_t s);
+
+// out[e*out_es + out_off + c*R + r] = in[e*in_es + r*C + c], bf16.
+int launch_transpose(const uint16_t* in, uint16_t* out, int E, int R, int C, int64_t in_es,
+                     int64_t out_es, int64_t out_off, cudaStream_t s);
+
+}  // namespace moe

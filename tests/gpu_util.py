@@ -1,0 +1,183 @@
+"""Shared set-up for the GPU parity tests: seeded inputs on the device, the
+library's forward through the C ABI, and tolerance checks against the oracle."""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+import mixture_experts_routing_gb300 as moe
+import oracle
+import synth
+import synth.gpu
+
+# BF16 outputs against the fp32 oracle: max-abs error and relative Frobenius error.
+TOL_MAX_ABS = 2e-2
+TOL_REL_FRO = 1e-2
+
+
+def bf16_dev(bits: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, what: str) -> None:
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    if ref.size == 0:
+        return
+    err = np.abs(got - ref).max()
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert err <= TOL_MAX_ABS and rel <= TOL_REL_FRO, "%s: max-abs %.3g rel-fro %.3g" % (what, err, rel)
+
+
+def assert_close_intermediate(got: np.ndarray, ref: np.ndarray, what: str) -> None:
+    """Tolerance for the bf16 intermediates h and o (the stated max-abs 2e-2
+    applies to the layer output y). Each element is rounded to bf16 once
+    (error <= 2^-8 of its magnitude); o also inherits h's rounding through a
+    sum of I random-signed terms, a few 0.1 % of the row's RMS. Bound:
+    |got-ref| <= 2^-7*|ref| + 0.02*rms(ref), and relative Frobenius <= 1e-2."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    if ref.size == 0:
+        return
+    d = np.abs(got - ref)
+    rms = np.sqrt(np.mean(ref ** 2))
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    worst = (d - 2.0 ** -7 * np.abs(ref)).max() / max(rms, 1e-30)
+    assert rel <= TOL_REL_FRO and worst <= 0.02, "%s: rel-fro %.3g, excess %.3g rms" % (what, rel, worst)
+
+
+class Problem:
+    """One workload's inputs on the device plus the library's buffers."""
+
+    def __init__(self, w: synth.Workload, bm: int = 32, dev="cuda:0", host_weights: bool = True,
+                 bias: Optional[np.ndarray] = None, renorm: int = 1, x_bits: Optional[np.ndarray] = None,
+                 with_ffn: bool = True):
+        self.w, self.bm, self.dev = w, bm, torch.device(dev)
+        N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
+        self.cfg = moe.Config(N, H, E, K, I, w.cap_num, w.cap_den, block_m=bm, renorm=renorm)
+        self.x_bits = (x_bits if x_bits is not None
+                       else synth.normal_bf16_bits(w.seed, synth.STREAM["x"], 0, N * H, w.x_std).reshape(N, H))
+        self.wr = synth.normal_f32(w.seed, synth.STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E)
+        if bias is None and w.zipf_s is not None:
+            bias = synth.zipf_bias(w.seed, E, w.zipf_s)
+        self.bias = bias
+        self.x = bf16_dev(self.x_bits, self.dev) if N > 0 else torch.empty((1, H), dtype=torch.bfloat16, device=self.dev)
+        self.wr_d = torch.from_numpy(self.wr).to(self.dev)
+        self.bias_d = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).to(self.dev)
+        bf = dict(dtype=torch.bfloat16, device=self.dev)
+        self.host_w: Dict[str, Dict[int, np.ndarray]] = {"wg": {}, "wu": {}, "wd": {}}
+        self.with_ffn = with_ffn
+        self.routes = moe.alloc_routes(self.cfg, self.dev)
+        self.ws = moe.alloc_workspace(self.cfg, self.dev)
+        if not with_ffn:
+            return
+        wg = torch.empty((E, H, I), **bf)
+        wu = torch.empty((E, H, I), **bf)
+        wd = torch.empty((E, I, H), **bf)
+        if host_weights:
+            hw = synth.make_host_inputs(w)
+            for k in ("wg", "wu", "wd"):
+                self.host_w[k] = hw[k]
+            wg.copy_(bf16_dev(np.stack([hw["wg"][e] for e in range(E)]), self.dev))
+            wu.copy_(bf16_dev(np.stack([hw["wu"][e] for e in range(E)]), self.dev))
+            wd.copy_(bf16_dev(np.stack([hw["wd"][e] for e in range(E)]), self.dev))
+        else:
+            synth.gpu.fill(wg, w.seed, synth.STREAM["wg"], w.w_std)
+            synth.gpu.fill(wu, w.seed, synth.STREAM["wu"], w.w_std)
+            synth.gpu.fill(wd, w.seed, synth.STREAM["wd"], w.w_std)
+        self.w13 = torch.empty((E, 2 * I, H), **bf)
+        self.w2 = torch.empty((E, H, I), **bf)
+        moe.pack_w13(self.cfg, wg, wu, self.w13)
+        moe.pack_w2(self.cfg, wd, self.w2)
+        del wg, wu, wd
+        self.h, self.o, self.y = moe.alloc_buffers(self.cfg, self.dev)
+        # poison outputs so unwritten rows show up
+        for t in (self.h, self.o, self.y):
+            t.fill_(float("nan"))
+
+    def run(self) -> None:
+        if not self.with_ffn:
+            moe.route_align(self.cfg, self.x, self.wr_d, self.bias_d, self.routes, self.ws)
+            torch.cuda.synchronize()
+            return
+        moe.forward(self.cfg, self.x, self.wr_d, self.bias_d, self.w13, self.w2, self.routes,
+                    self.ws, self.h, self.o, self.y)
+        torch.cuda.synchronize()
+        assert moe.device_error() == 0
+
+    def expert_weights(self, experts) -> oracle.ExpertWeights:
+        w, E, H, I = self.w, self.w.n_experts, self.w.hidden, self.w.inter
+        for e in experts:
+            if e not in self.host_w["wg"]:
+                self.host_w["wg"][e] = synth.normal_bf16_bits(w.seed, synth.STREAM["wg"], e * H * I, H * I, w.w_std).reshape(H, I)
+                self.host_w["wu"][e] = synth.normal_bf16_bits(w.seed, synth.STREAM["wu"], e * H * I, H * I, w.w_std).reshape(H, I)
+                self.host_w["wd"][e] = synth.normal_bf16_bits(w.seed, synth.STREAM["wd"], e * I * H, I * H, w.w_std).reshape(I, H)
+        return oracle.ExpertWeights(E, self.host_w["wg"], self.host_w["wu"], self.host_w["wd"])
+
+    def oracle_routing(self) -> oracle.Routing:
+        w = self.w
+        return oracle.route(self.x_bits, self.wr, self.bias, w.n_experts, w.top_k, w.cap_num,
+                            w.cap_den, self.bm, renorm=bool(self.cfg.renorm))
+
+    def routes_np(self) -> dict:
+        N = self.w.n_tokens
+        out = {n: getattr(self.routes, n).cpu().numpy() for n, _ in moe.Routes.FIELDS}
+        for n in ("topk_ids", "topk_p", "keep", "token_routes"):
+            out[n] = out[n][:N]
+        return out
+
+
+def assert_routing_equal(P: Problem, R: oracle.Routing) -> None:
+    g = P.routes_np()
+    L = R.layout
+    S = L.num_tokens_post_padded
+    assert np.array_equal(g["topk_ids"], R.topk_ids), "topk_ids"
+    assert np.array_equal(g["topk_p"].view(np.int32), R.topk_p.view(np.int32)), "topk_p bits"
+    assert np.array_equal(g["keep"], L.keep), "keep"
+    assert np.array_equal(g["expert_counts"], L.expert_counts), "expert_counts"
+    assert np.array_equal(g["kept_counts"], L.kept_counts), "kept_counts"
+    assert np.array_equal(g["sorted_slot_ids"][:S], L.sorted_slot_ids), "sorted_slot_ids"
+    assert np.array_equal(g["expert_ids"][:len(L.expert_ids)], L.expert_ids), "expert_ids"
+    assert np.array_equal(g["block_start"], L.block_start), "block_start"
+    assert int(g["num_tokens_post_padded"][0]) == S, "num_tokens_post_padded"
+    assert np.array_equal(g["token_routes"], L.token_routes), "token_routes"
+
+
+def check_expert_slots(P: Problem, R: oracle.Routing, experts) -> None:
+    """h and o of every kept slot of the given experts against the oracle FFN,
+    and zeros in the padding rows below the 16-row granule."""
+    L = R.layout
+    H, I = P.w.hidden, P.w.inter
+    W = P.expert_weights(experts)
+    h = P.h.float().cpu().numpy()
+    o = P.o.float().cpu().numpy()
+    for e in experts:
+        base, kept = e * L.cpad, int(L.kept_counts[e])
+        if kept == 0:
+            continue
+        toks = L.sorted_slot_ids[base:base + kept]
+        o_ref, h_ref = oracle.ffn_routes(toks, [e] * kept, P.x_bits, W, H, I, want_h=True)
+        assert_close_intermediate(h[base:base + kept], h_ref, "h of expert %d" % e)
+        assert_close_intermediate(o[base:base + kept], o_ref, "o of expert %d" % e)
+        pad_end = base + (kept + 15) // 16 * 16
+        assert np.all(h[base + kept:pad_end] == 0) and np.all(o[base + kept:pad_end] == 0)
+
+
+def check_combine_property(P: Problem, R: oracle.Routing) -> None:
+    """y[t] equals the fp64 gather-combine of the library's own o rows."""
+    o = P.o.float().cpu().numpy().astype(np.float64)
+    y = P.y.float().cpu().numpy()
+    tr = R.layout.token_routes
+    p = R.topk_p.astype(np.float64)
+    ref = np.zeros(y.shape)
+    mag = np.zeros(y.shape)
+    for k in range(tr.shape[1]):
+        m = tr[:, k] >= 0
+        ref[m] += p[m, k:k + 1] * o[tr[m, k]]
+        mag[m] += np.abs(p[m, k:k + 1] * o[tr[m, k]])
+    # bf16 rounding of the output (half an ulp: 2^-8 relative) plus fp32 accumulation
+    assert np.all(np.abs(y - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * mag + 1e-30)

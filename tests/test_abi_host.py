@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/moe.h declares, answers size queries, and rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_routing_gb300 as moe
+import oracle
+import synth
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\**\s+\**(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mixture_experts_routing_gb300 import _build
+    _build.build()
+    return moe.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_route_align", "moe_ffn_forward", "moe_combine", "moe_fc1_forward",
+              "moe_fc2_forward", "moe_pack_w13", "moe_pack_w2", "moe_route_workspace_bytes",
+              "moe_max_slots", "moe_capacity", "moe_status_string", "moe_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def _cfg(w, bm=32):
+    return moe.Config(w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter, w.cap_num, w.cap_den,
+                      block_m=bm)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_small", "qwen3_30b", "dsv3"])
+@pytest.mark.parametrize("bm", [16, 32, 64, 128])
+def test_size_queries_match_oracle_capacity(L, name, bm):
+    w = synth.WORKLOADS[name]
+    cfg = _cfg(w, bm)
+    cap = oracle.capacity(w.n_tokens, w.top_k, w.n_experts, w.cap_num, w.cap_den)
+    assert moe.capacity(cfg) == cap
+    cpad = -(-cap // bm) * bm
+    assert moe.max_slots(cfg) == w.n_experts * cpad
+    assert moe.max_blocks(cfg) == w.n_experts * cpad // bm
+    assert moe.route_workspace_bytes(cfg) >= 4 * w.n_tokens * w.n_experts
+
+
+def test_invalid_configs_fail_closed(L):
+    good = dict(n_tokens=64, hidden=128, n_experts=8, top_k=2, inter=128, cap_num=1, cap_den=1,
+                block_m=32)
+    bad_fields = [("n_tokens", -1), ("hidden", 0), ("n_experts", 0), ("top_k", 0), ("top_k", 9),
+                  ("cap_den", 0), ("block_m", 8), ("block_m", 48)]
+    for k, v in bad_fields:
+        c = moe.Config(**dict(good, **{k: v}))
+        assert L.moe_max_slots(ctypes.byref(c)) == -1, (k, v)
+    unsupported = [("hidden", 192), ("inter", 64), ("n_experts", 300), ("n_tokens", 10 ** 6),
+                   ("cap_num", 0)]
+    for k, v in unsupported:
+        c = moe.Config(**dict(good, **{k: v}, top_k=2))
+        assert L.moe_max_slots(ctypes.byref(c)) == -2, (k, v)
+    assert L.moe_max_slots(None) == -1
+
+
+def test_entry_points_reject_bad_arguments_before_launch(L):
+    cfg = moe.Config(64, 128, 8, 2, 128, 1, 1, block_m=32)
+    empty = moe._RoutesC()
+    # missing routes
+    assert L.moe_route_align(ctypes.byref(cfg), 16, 16, None, ctypes.byref(empty), 256, 1 << 20,
+                             None) == -1
+    full = moe._RoutesC(*([256] * 10))
+    # null x / router weight
+    assert L.moe_route_align(ctypes.byref(cfg), None, 16, None, ctypes.byref(full), 256, 1 << 20,
+                             None) == -1
+    # misaligned x
+    assert L.moe_route_align(ctypes.byref(cfg), 18, 16, None, ctypes.byref(full), 256, 1 << 20,
+                             None) == -1
+    # workspace missing / too small
+    assert L.moe_route_align(ctypes.byref(cfg), 16, 16, None, ctypes.byref(full), None, 1 << 20,
+                             None) == -3
+    need = moe.route_workspace_bytes(cfg)
+    assert L.moe_route_align(ctypes.byref(cfg), 16, 16, None, ctypes.byref(full), 256, need - 1,
+                             None) == -3
+    # GEMMs and combine: null / misaligned operands
+    assert L.moe_fc1_forward(ctypes.byref(cfg), ctypes.byref(full), None, 256, 256, None) == -1
+    assert L.moe_fc2_forward(ctypes.byref(cfg), ctypes.byref(full), 256, 264, 256, None) == -1
+    assert L.moe_combine(ctypes.byref(cfg), ctypes.byref(full), 256, None, None) == -1
+    assert L.moe_combine(ctypes.byref(cfg), None, 256, 256, None) == -1
+    assert L.moe_pack_w13(ctypes.byref(cfg), None, 256, 256, None) == -1
+    assert L.moe_pack_w2(ctypes.byref(cfg), 256, None, None) == -1
+    bad = moe.Config(64, 100, 8, 2, 128, 1, 1, block_m=32)
+    assert L.moe_combine(ctypes.byref(bad), ctypes.byref(full), 256, 256, None) == -2
+
+
+def test_status_strings(L):
+    assert moe.status_string(0) == "ok"
+    assert "unsupported" in moe.status_string(-2)
+    assert moe.status_string(12345) == "unknown status"
