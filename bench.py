@@ -1,0 +1,474 @@
+#!/usr/bin/env python3
+"""MoE-layer forward benchmark on GB300.
+
+One step = one forward of the whole layer over one batch of synthetic tokens:
+moe_route_align (router, scan, drop-and-pad select, route-list layout), FC1
+gather-GEMM + SwiGLU, FC2 grouped GEMM, gather-combine, each a C-ABI call.
+
+Default workload: the DeepSeek-V3-shaped layer (N=4096 tokens, H=7168,
+E=256, top-8, I=2048, F=1.25, ~22.5 GB of bf16 expert weights), the largest
+workload that fits one GPU. Its inputs exceed L2, so no flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle, on the host cores
+
+Under torchrun each rank is an independent replica with its own batch (weak
+scaling, no collective on the data path); value = tokens of all ranks / the
+slowest rank's time. Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer fwd tokens/s on 1 GB300; grouped-GEMM TFLOPS as % of BF16 peak"
+UNIT = "tokens/s"
+
+
+# ----------------------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dsv3")
+    ap.add_argument("--block-m", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-experts", type=int, default=48,
+                    help="experts whose FFN the CPU baseline runs (bounded sample)")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Max of a float over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "_source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["mixture_experts_routing_gb300/csrc/gemm.cu",
+                "mixture_experts_routing_gb300/csrc/ptx.cuh"]
+
+
+def ncu_traffic(kernel: str, workload: str, units: float):
+    """DRAM bytes per launch from the committed ncu summary, scaled by the
+    launch's units; None when absent or when the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("workload") != workload:
+        return None
+    if d.get("source_hash") != source_hash(d.get("sources", GEMM_SOURCES)):
+        return None
+    return d["dram_bytes_per_unit"] * units
+
+
+# ----------------------------------------------------------------------------- work model
+def work_model(w, kept_counts):
+    """Algorithmic bytes and flops per launch of each kernel, from the
+    per-expert kept counts of this batch."""
+    import numpy as np
+    N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
+    kc = np.asarray(kept_counts, dtype=np.int64)
+    kept = int(kc.sum())
+    active = int((kc > 0).sum())
+    rows = int(((kc + 15) // 16 * 16).sum())  # slots the GEMMs compute (16-row granule)
+    m = {}
+    m["fc1"] = {"flops": 2.0 * kept * H * 2 * I,
+                "bytes": active * 2.0 * I * H * 2 + N * H * 2 + rows * I * 2,
+                "units": active, "unit": "active expert"}
+    m["fc2"] = {"flops": 2.0 * kept * I * H,
+                "bytes": active * 1.0 * H * I * 2 + rows * I * 2 + rows * H * 2,
+                "units": active, "unit": "active expert"}
+    m["combine"] = {"flops": 2.0 * kept * H, "bytes": kept * H * 2.0 + N * H * 2 + N * K * 8,
+                    "units": N, "unit": "token"}
+    m["route"] = {"flops": 2.0 * N * H * E, "bytes": N * H * 2.0 + H * E * 4 + N * E * 8 + N * K * 24,
+                  "units": N, "unit": "token"}
+    m["_kept"], m["_active"], m["_rows"] = kept, active, rows
+    return m
+
+
+def roofline_for(name, model, ms, peaks, workload):
+    """Roofline object of one kernel: bound, achieved, peak, frac, traffic."""
+    d = model[name]
+    sec = ms / 1e3
+    hbm = peaks["hbm_gbs"]
+    tensor = peaks["bf16_tflops"]
+    alu = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12  # fp32 FMA pipes
+    if name == "route":
+        t_c, peak_c = d["flops"] / (alu * 1e12), alu
+    else:
+        t_c, peak_c = d["flops"] / (tensor * 1e12), tensor
+    t_m = d["bytes"] / (hbm * 1e9)
+    src = peaks["_source"]
+    if t_m >= t_c:
+        ach = d["bytes"] / sec / 1e9
+        r = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+             "peak_source": src}
+    else:
+        ach = d["flops"] / sec / 1e12
+        r = {"bound": "alu" if name == "route" else "tensor", "achieved": ach, "peak": peak_c,
+             "unit": "TFLOP/s", "frac": ach / peak_c, "peak_source": src}
+    tr = ncu_traffic("moe_gemm_kernel:" + name, workload, d["units"]) if name in ("fc1", "fc2") else None
+    r["traffic"] = tr
+    r["kernel"] = name
+    r["ms"] = ms
+    r["algorithmic_bytes"] = d["bytes"]
+    r["algorithmic_flops"] = d["flops"]
+    return r
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def time_oracle_sample(w, x_bits, wr, bias, bm, n_experts_sample, seed_experts=0):
+    """The oracle, as it stands, on a bounded sample of one step: routing of
+    every token, expert FFN of `n_experts_sample` experts' kept routes
+    (extrapolated to all kept routes by route count), combine of every token.
+    Returns (tokens/s, description, seconds of CPU work, threads)."""
+    import numpy as np
+    import oracle
+    import synth
+    N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
+    t0 = time.perf_counter()
+    R = oracle.route(x_bits, wr, bias, E, K, w.cap_num, w.cap_den, bm)
+    t_route = time.perf_counter() - t0
+    L = R.layout
+    kept_total = int(L.kept_counts.sum())
+    cand = [e for e in range(E) if L.kept_counts[e] > 0]
+    rng = np.random.default_rng(seed_experts)
+    sample = sorted(rng.choice(cand, size=min(n_experts_sample, len(cand)), replace=False).tolist())
+    wg = {e: synth.normal_bf16_bits(w.seed, synth.STREAM["wg"], e * H * I, H * I, w.w_std).reshape(H, I) for e in sample}
+    wu = {e: synth.normal_bf16_bits(w.seed, synth.STREAM["wu"], e * H * I, H * I, w.w_std).reshape(H, I) for e in sample}
+    wd = {e: synth.normal_bf16_bits(w.seed, synth.STREAM["wd"], e * I * H, I * H, w.w_std).reshape(I, H) for e in sample}
+    W = oracle.ExpertWeights(E, wg, wu, wd)
+    toks, exps = [], []
+    for e in sample:
+        base = e * L.cpad
+        k = int(L.kept_counts[e])
+        toks += L.sorted_slot_ids[base:base + k].tolist()
+        exps += [e] * k
+    t0 = time.perf_counter()
+    oracle.ffn_routes(toks, exps, x_bits, W, H, I)
+    t_ffn = time.perf_counter() - t0
+    o_zero = np.zeros((N * K, H), dtype=np.float32)
+    t0 = time.perf_counter()
+    oracle.combine(0, N, L.keep, R.topk_p, o_zero)
+    t_comb = time.perf_counter() - t0
+    t_full = t_route + t_ffn * kept_total / max(len(toks), 1) + t_comb
+    desc = ("routing of all %d tokens + expert FFN of %d/%d experts (%d of %d kept routes, "
+            "time extrapolated by route count) + combine of all tokens"
+            % (N, len(sample), len(cand), len(toks), kept_total))
+    return N / t_full, desc, t_route + t_ffn + t_comb, oracle.num_threads()
+
+
+def host_inputs(w, rank_seed):
+    import synth
+    N, H, E = w.n_tokens, w.hidden, w.n_experts
+    x_bits = synth.normal_bf16_bits(rank_seed, synth.STREAM["x"], 0, N * H, w.x_std).reshape(N, H)
+    wr = synth.normal_f32(w.seed, synth.STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E)
+    bias = synth.zipf_bias(w.seed, E, w.zipf_s) if w.zipf_s is not None else None
+    return x_bits, wr, bias
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    import synth
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[args.workload]
+    x_bits, wr, bias = host_inputs(w, w.seed)
+    n_exp = max(1, min(4, args.cpu_experts))
+    for _ in range(args.warmup):
+        time_oracle_sample(w, x_bits, wr, bias, args.block_m, n_exp)
+    vals, secs = [], 0.0
+    t_start = time.perf_counter()
+    for i in range(args.steps):
+        v, desc, s, cores = time_oracle_sample(w, x_bits, wr, bias, args.block_m, n_exp, seed_experts=i)
+        vals.append(v)
+        secs += s
+    wall = time.perf_counter() - t_start
+    value = len(vals) / sum(1.0 / v for v in vals)  # tokens over total extrapolated time
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.n_tokens / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": w.name, "description": w.note, "block_m": args.block_m,
+                                        "parallelism": "single host, OpenMP"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "per step: " + desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(out))
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import mixture_experts_routing_gb300 as moe
+    import synth
+    import synth.gpu
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    w = synth.WORKLOADS[args.workload]
+    N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
+    cfg = moe.Config(N, H, E, K, I, w.cap_num, w.cap_den, block_m=args.block_m)
+    peaks = load_peaks()
+
+    # inputs: this rank's batch (seed = rank), shared weights
+    rank_seed = w.seed + rank
+    x_bits, wr_h, bias_h = host_inputs(w, rank_seed)
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    wr = torch.from_numpy(wr_h).to(dev)
+    bias = None if bias_h is None else torch.from_numpy(bias_h).to(dev)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    w13 = torch.empty((E, 2 * I, H), **bf)
+    w2 = torch.empty((E, H, I), **bf)
+    tmp = torch.empty((E, H, I), **bf)
+    synth.gpu.fill(tmp, w.seed, synth.STREAM["wg"], w.w_std)
+    wu = torch.empty((E, H, I), **bf)
+    synth.gpu.fill(wu, w.seed, synth.STREAM["wu"], w.w_std)
+    moe.pack_w13(cfg, tmp, wu, w13)
+    del wu
+    tmp = tmp.view(E, I, H)
+    synth.gpu.fill(tmp, w.seed, synth.STREAM["wd"], w.w_std)
+    moe.pack_w2(cfg, tmp, w2)
+    torch.cuda.synchronize()
+    del tmp
+    torch.cuda.empty_cache()
+    routes = moe.alloc_routes(cfg, dev)
+    ws = moe.alloc_workspace(cfg, dev)
+    h, o, y = moe.alloc_buffers(cfg, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    names = ("route", "fc1", "fc2", "combine")
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        moe.route_align(cfg, x, wr, bias, routes, ws, stream)
+        if evs is not None:
+            evs[1].record(stream)
+        moe.fc1_forward(cfg, routes, x, w13, h, stream)
+        if evs is not None:
+            evs[2].record(stream)
+        moe.fc2_forward(cfg, routes, h, w2, o, stream)
+        if evs is not None:
+            evs[3].record(stream)
+        moe.combine(cfg, routes, o, y, stream)
+        if evs is not None:
+            evs[4].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- device-timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index).start()
+    time.sleep(0.3)  # let the sampler start before the timed work
+    launches0 = moe.launch_count()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    launches = moe.launch_count() - launches0
+    barrier(dist, dev)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(start.elapsed_time(end), dist, dev)
+    per_kernel = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                  for j, n in enumerate(names)}
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+    kept_counts = routes.kept_counts.cpu().numpy()
+
+    # ---- end to end: pinned host x in, host y out, every step
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y[:N], non_blocking=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y[:N], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+
+    model = work_model(w, kept_counts)
+    dom = max(("fc1", "fc2", "combine", "route"), key=lambda n: per_kernel[n])
+    roof = roofline_for(dom, model, per_kernel[dom], peaks, w.name)
+    kernels = {n: roofline_for(n, model, per_kernel[n], peaks, w.name) for n in names}
+    gemm_ms = per_kernel["fc1"] + per_kernel["fc2"]
+    gemm_flops = model["fc1"]["flops"] + model["fc2"]["flops"]
+    issued = 2.0 * 3 * H * I * E * moe.capacity(cfg)
+
+    tokens = N * world * args.steps
+    value = tokens / (ms_total / 1e3)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.note, "tokens_per_step_per_gpu": N,
+                   "block_m": args.block_m, "capacity": moe.capacity(cfg),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (%.1f GB of expert weights); no flush"
+                         % ((w13.numel() + w2.numel()) * 2 / 1e9)},
+        "gpu_launches": launches,
+        "e2e": {"value": N * world * args.steps / (ms_e2e / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": N * H * 2, "d2h_bytes_per_step": N * H * 2},
+        "roofline": roof,
+        "grouped_gemm": {"ms": gemm_ms, "tflops_useful": gemm_flops / (gemm_ms / 1e3) / 1e12,
+                         "pct_bf16_peak": gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                         "tflops_issued_capacity_shape": issued / (gemm_ms / 1e3) / 1e12,
+                         "kept_routes": model["_kept"], "active_experts": model["_active"]},
+        "kernels_ms": per_kernel,
+        "kernels": {n: {k: v for k, v in kernels[n].items() if k in ("bound", "achieved", "unit", "frac")}
+                    for n in names},
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, secs, cores = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m, args.cpu_experts)
+        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": desc, "cpu_seconds": secs}
+    if rank == 0:
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

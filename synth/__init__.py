@@ -121,8 +121,49 @@ def _cos2pi_f32(u: np.ndarray) -> np.ndarray:
     return np.where(neg, -v, v)
 
 
+_HERE = __import__("os").path.dirname(__import__("os").path.abspath(__file__))
+_CLIB = None
+
+
+def build_host(force: bool = False) -> str:
+    """Compile the C twin (synth_host.c) with gcc; returns the library path."""
+    import os
+    import subprocess
+    src = os.path.join(_HERE, "synth_host.c")
+    so = os.path.join(_HERE, "libsynth_host.so")
+    if force or not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(src):
+        tmp = so + ".tmp.%d" % os.getpid()
+        subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+                        "-fPIC", "-shared", src, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, so)
+    return so
+
+
+def _clib():
+    global _CLIB
+    if _CLIB is None:
+        import ctypes
+        L = ctypes.CDLL(build_host())
+        for name in ("synth_normal_f32", "synth_normal_bf16"):
+            f = getattr(L, name)
+            f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
+                          ctypes.c_uint32, ctypes.c_float]
+            f.restype = None
+        _CLIB = L
+    return _CLIB
+
+
 def normal_f32(seed: int, stream: int, start: int, count: int, std: float = 1.0) -> np.ndarray:
-    """fp32 values ``z_i * std`` for counter indices ``start .. start+count-1``."""
+    """fp32 values ``z_i * std`` for counter indices ``start .. start+count-1``
+    (computed by the C twin; ``normal_f32_numpy`` is the same definition)."""
+    out = np.empty(count, dtype=np.float32)
+    if count:
+        _clib().synth_normal_f32(out.ctypes.data, count, start, seed, stream, float(std))
+    return out
+
+
+def normal_f32_numpy(seed: int, stream: int, start: int, count: int, std: float = 1.0) -> np.ndarray:
+    """The generator definition in numpy (slow; pins the C and CUDA twins)."""
     idx = np.arange(start, start + count, dtype=np.uint64)
     out = np.empty(count, dtype=np.float32)
     chunk = 1 << 16
@@ -149,7 +190,10 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 
 
 def normal_bf16_bits(seed: int, stream: int, start: int, count: int, std: float = 1.0) -> np.ndarray:
-    return f32_to_bf16_bits(normal_f32(seed, stream, start, count, std))
+    out = np.empty(count, dtype=np.uint16)
+    if count:
+        _clib().synth_normal_bf16(out.ctypes.data, count, start, seed, stream, float(std))
+    return out
 
 
 def zipf_bias(seed: int, n_experts: int, s: float) -> np.ndarray:
@@ -200,6 +244,10 @@ WORKLOADS = {
                           note="Qwen3-30B-A3B-shaped layer: N=8192, H=2048, E=128, top-8, I=768, F=1.0, Zipf(1.0) router bias"),
     "dsv3": Workload("dsv3", 4096, 7168, 256, 8, 2048, 5, 4, w_std=0.006,
                      note="DeepSeek-V3-shaped layer: N=4096, H=7168, E=256, top-8, I=2048, F=1.25, balanced router"),
+    # profiling case: the DeepSeek-V3 shapes with 16 experts and N scaled so that
+    # each expert sees the same ~128 routes; 1.4 GB of weights (above L2)
+    "dsv3_e16": Workload("dsv3_e16", 256, 7168, 16, 8, 2048, 5, 4, w_std=0.006,
+                         note="DeepSeek-V3 shapes with 16 experts, N=256 (ncu profiling case)"),
     "dropless": Workload("dropless", 16384, 4096, 64, 6, 1408, 0, 1, zipf_s=0.8,
                          note="dropless bucketed layer: H=4096, E=64, top-6, I=1408, N swept 128..16384, Zipf(0.8)",
                          sweep=tuple(2 ** k for k in range(7, 15))),

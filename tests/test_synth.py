@@ -1,5 +1,6 @@
 """Host side of the seeded input generator (no MoE arithmetic here)."""
 import numpy as np
+import pytest
 from scipy import stats
 
 import synth
@@ -11,6 +12,16 @@ def test_counter_based_slices_agree():
     assert np.array_equal(full[1234:1234 + 777], part)
     assert not np.array_equal(synth.normal_f32(0, 3, 0, 100), synth.normal_f32(0, 2, 0, 100))
     assert not np.array_equal(synth.normal_f32(1, 2, 0, 100), synth.normal_f32(0, 2, 0, 100))
+
+
+@pytest.mark.parametrize("seed,stream,start,count,std", [
+    (0, 0, 0, 200_000, 1.0), (0, 2, 123_456_789, 50_000, 0.02), (3, 4, 10 ** 11, 50_000, 0.006)])
+def test_c_twin_matches_numpy_definition(seed, stream, start, count, std):
+    ref = synth.normal_f32_numpy(seed, stream, start, count, std)
+    assert np.array_equal(synth.normal_f32(seed, stream, start, count, std).view(np.uint32),
+                          ref.view(np.uint32))
+    assert np.array_equal(synth.normal_bf16_bits(seed, stream, start, count, std),
+                          synth.f32_to_bf16_bits(ref))
 
 
 def test_normal_statistics():
