@@ -171,6 +171,35 @@ int moe_pack_w13(const moe_config_t* cfg, const void* w_gate, const void* w_up, 
                  cudaStream_t stream);
 int moe_pack_w2(const moe_config_t* cfg, const void* w_down, void* w2, cudaStream_t stream);
 
+/* Size of the library's built-in route scratch used by moe_route_align_noalloc. */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* moe_route_align for callers that cannot allocate device memory. No page
+ * describes this call; it exists for users of this library. Some callers run
+ * where cudaMalloc is unavailable or forbidden: a custom op or plugin inside
+ * another runtime that owns every device allocation and hands the plugin no
+ * allocator; a latency-bound serving loop that bans allocator calls, because
+ * cudaMalloc may synchronise the device and stall every stream; a deployment
+ * that fixes its memory budget before the first request. They cannot provide
+ * the workspace moe_route_align asks for, so this variant uses an 8 MiB
+ * scratch array built into the library instead (every GPU that loads the
+ * library holds it until the process exits). Arguments and results are those
+ * of moe_route_align, without workspace/ws_bytes.
+ *  - Returns MOE_ERR_WORKSPACE, without launching anything, when
+ *    moe_route_workspace_bytes(cfg) exceeds MOE_NOALLOC_SCRATCH_BYTES (for
+ *    example N*E*4 bytes of logits alone above 8 MiB).
+ *  - The first call on each device looks up the scratch array's device
+ *    address (with that device current); make that first call before any
+ *    stream capture on the device.
+ *  - All calls on a device share the one scratch array and it keeps the last
+ *    call's contents; nothing in it needs to start at zero, because every
+ *    word the kernels read is written earlier in the same call. Calls whose
+ *    work overlaps on the GPU (different streams, or different threads without
+ *    ordering) race on that array: order them on one stream.
+ *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. */
+int moe_route_align_noalloc(const moe_config_t* cfg, const void* x, const float* w_router,
+                            const float* bias, const moe_routes_t* out, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(int status);
 

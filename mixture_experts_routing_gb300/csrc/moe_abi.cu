@@ -277,3 +277,39 @@ int moe_device_error(uint32_t* out) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moe_route_align_noalloc: moe_route_align with a scratch array built into the
+// library, for callers that cannot allocate device memory (see moe.h).
+namespace {
+
+static __device__ __align__(256) uint8_t g_route_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_route_scratch on the current device, looked up once per
+// device (the host-side name is only a stand-in, not a device address).
+uint8_t* route_scratch_ptr() {
+  static std::mutex mu;
+  static uint8_t* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return nullptr;
+    ptrs[dev] = static_cast<uint8_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" int moe_route_align_noalloc(const moe_config_t* cfg, const void* x,
+                                       const float* w_router, const float* bias,
+                                       const moe_routes_t* out, cudaStream_t stream) {
+  const int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (ws_layout(cfg).total > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  uint8_t* scratch = route_scratch_ptr();
+  if (!scratch) return MOE_ERR_CUDA;
+  return moe_route_align(cfg, x, w_router, bias, out, scratch, MOE_NOALLOC_SCRATCH_BYTES, stream);
+}
