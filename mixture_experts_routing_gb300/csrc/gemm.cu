@@ -112,32 +112,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_s;
 
   if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
-      const int a_row0 = e * p.a_rows_per_expert + f * p.f_rows;
-      const uint32_t tx = (uint32_t)p.n_acc * kATileBytes + (uint32_t)n_eff * 128u;
-      for (int kt = 0; kt < p.k_tiles; ++kt) {
-        const int s = kt % p.stages;
-        const uint32_t u = (uint32_t)(kt / p.stages);
-        if (kt >= p.stages &&
-            !mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty))
-          break;
-        const uint32_t fb = smem_u32(&full_bar[s]);
+    // Lane 0 arms the stage barrier and loads the weight tiles; then every
+    // lane of the warp issues its share of the B-operand copies, so the many
+    // small row gathers of FC1 do not serialise on one thread.
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    const int a_row0 = e * p.a_rows_per_expert + f * p.f_rows;
+    const uint32_t tx = (uint32_t)p.n_acc * kATileBytes + (uint32_t)n_eff * 128u;
+    for (int kt = 0; kt < p.k_tiles; ++kt) {
+      const int s = kt % p.stages;
+      const uint32_t u = (uint32_t)(kt / p.stages);
+      int ok = 1;
+      if (lane == 0 && kt >= p.stages)
+        ok = mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      const uint32_t fb = smem_u32(&full_bar[s]);
+      const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
+      const int kx = kt * kBK;
+      if (lane == 0) {
         mbar_arrive_expect_tx(fb, tx);
-        const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
-        const int kx = kt * kBK;
         tma_load_2d(st, &tmA, kx, a_row0, fb, pol_w);
         if (p.n_acc == 2) tma_load_2d(st + kATileBytes, &tmA, kx, a_row0 + p.a_second_off, fb, pol_w);
-        const uint32_t b = st + p.b_off;
-        if (p.fc1) {
-          for (int q = 0; q < n_eff; q += 4)
-            tma_gather4(b + (uint32_t)q * 128u, &tmB, kx, rows_s[q], rows_s[q + 1], rows_s[q + 2],
-                        rows_s[q + 3], fb, pol_x);
-        } else {
-          for (int q = 0; q < n_eff; q += 16)
-            tma_load_2d(b + (uint32_t)q * 128u, &tmB, kx, slot0 + q, fb, pol_x);
-        }
+      }
+      __syncwarp();
+      const uint32_t b = st + p.b_off;
+      if (p.fc1) {
+        for (int q = lane * 4; q < n_eff; q += 128)
+          tma_gather4(b + (uint32_t)q * 128u, &tmB, kx, rows_s[q], rows_s[q + 1], rows_s[q + 2],
+                      rows_s[q + 3], fb, pol_x);
+      } else {
+        for (int q = lane * 16; q < n_eff; q += 512)
+          tma_load_2d(b + (uint32_t)q * 128u, &tmB, kx, slot0 + q, fb, pol_x);
       }
     }
   } else if (warp == 1) {
