@@ -332,9 +332,19 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2) return -1;
   const size_t dyn = (size_t)p.stages * p.stage_bytes + 1024;
-  cudaError_t err =
-      cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-  if (err != cudaSuccess) return -(int)err;
+  cudaError_t err = cudaSuccess;
+  {
+    // raise the kernel's dynamic shared-memory limit once per device
+    static int set_for[64] = {};
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return -(int)err;
+    if (dev < 0 || dev >= 64 || !set_for[dev]) {
+      err = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBudget);
+      if (err != cudaSuccess) return -(int)err;
+      if (dev >= 0 && dev < 64) set_for[dev] = 1;
+    }
+  }
   const int64_t grid = (int64_t)a.E * p.f_tiles * p.n_tok_tiles;
   moe_gemm_kernel<<<(unsigned)grid, kThreads, dyn, s>>>(tmA, tmB, p);
   err = cudaGetLastError();

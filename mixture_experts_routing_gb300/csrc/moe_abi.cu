@@ -61,7 +61,7 @@ int64_t cap_of(const moe_config_t* c) {
 int64_t cpad_of(const moe_config_t* c) { return roundup(cap_of(c), c->block_m); }
 
 struct WsLayout {
-  size_t logits, chunk_rank, chunk_counts, chunk_off, expert_off, route_list, total;
+  size_t logits, chunk_counts, chunk_lofs, chunk_routes, total;
 };
 
 WsLayout ws_layout(const moe_config_t* c) {
@@ -75,11 +75,9 @@ WsLayout ws_layout(const moe_config_t* c) {
     return at;
   };
   w.logits = take((size_t)(N * E) * 4);
-  w.chunk_rank = take((size_t)(N * K) * 4);
   w.chunk_counts = take((size_t)(C * E) * 4);
-  w.chunk_off = take((size_t)(C * E) * 4);
-  w.expert_off = take((size_t)(E + 1) * 4);
-  w.route_list = take((size_t)(N * K) * 4);
+  w.chunk_lofs = take((size_t)(C * E) * 4);
+  w.chunk_routes = take((size_t)(N * K) * 4);
   w.total = off;
   return w;
 }
@@ -154,11 +152,9 @@ int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_route
   a.ntpp = out->num_tokens_post_padded;
   a.token_routes = out->token_routes;
   a.ws.logits = reinterpret_cast<float*>(ws + w.logits);
-  a.ws.chunk_rank = reinterpret_cast<int32_t*>(ws + w.chunk_rank);
   a.ws.chunk_counts = reinterpret_cast<int32_t*>(ws + w.chunk_counts);
-  a.ws.chunk_off = reinterpret_cast<int32_t*>(ws + w.chunk_off);
-  a.ws.expert_off = reinterpret_cast<int32_t*>(ws + w.expert_off);
-  a.ws.route_list = reinterpret_cast<int32_t*>(ws + w.route_list);
+  a.ws.chunk_lofs = reinterpret_cast<int32_t*>(ws + w.chunk_lofs);
+  a.ws.chunk_routes = reinterpret_cast<int32_t*>(ws + w.chunk_routes);
   return finish(moe::launch_route(a, stream));
 }
 

@@ -13,11 +13,9 @@ constexpr int kMaxTokens = 24576;     // select kernel stages one expert's route
 
 struct RouteWs {
   float* logits;          // [N,E]
-  int32_t* chunk_rank;    // [N,K] rank of route among same-expert routes of its chunk
-  int32_t* chunk_counts;  // [C,E]
-  int32_t* chunk_off;     // [C,E] routes of expert e in chunks before c
-  int32_t* expert_off;    // [E+1] exclusive scan of expert_counts
-  int32_t* route_list;    // [N*K] route indices grouped by expert, ascending token
+  int32_t* chunk_counts;  // [C,E] routes of expert e in chunk c
+  int32_t* chunk_lofs;    // [C,E] offset of expert e's routes in chunk c's sorted list
+  int32_t* chunk_routes;  // [N*K] per chunk: route indices sorted by expert, token order kept
 };
 
 struct RouteArgs {

@@ -5,15 +5,15 @@
 //                     one sequential fma chain, so the logits (and hence the
 //                     top-K indices) are bit-reproducible.
 //  R2 router_topk   : one warp per token: softmax with our own fp32 exp, K rounds
-//                     of warp-shuffle argmax on a packed (p, ~e) key, renormalise;
-//                     the CTA also counts its chunk's routes per expert and ranks
-//                     each route among its chunk's same-expert routes.
-//  R3 route_scan    : per-expert exclusive scan over chunks (counts, offsets).
-//  R3 route_scatter : route list grouped by expert, ascending token order.
-//  R4 route_select  : one CTA per expert: radix select of the `cap` highest
-//                     renormalised probabilities (ties to the lower token), then
-//                     the block-padded layout of sorted_slot_ids / expert_ids /
-//                     token_routes.
+//                     of warp argmax (max of the p bits, then min of the expert
+//                     ids at that max), renormalise; then the CTA sorts its
+//                     64-token chunk's routes by expert (stable) and records
+//                     per-expert counts and offsets (the scan's first level).
+//  R3+R4 route_select: one CTA per expert: exclusive scan of the expert's chunk
+//                     counts, gather of its routes in token order, radix select
+//                     of the `cap` highest renormalised probabilities (ties to
+//                     the lower token), then the block-padded layout of
+//                     sorted_slot_ids / expert_ids / token_routes.
 // Route-list contract: "Permute-Free Grouped GEMM for MoE (bf16, gfx950)",
 // section 4 Data structures and section 5 Kernels (route_list_scan,
 // route_list_align). Capacity and drop-and-pad: "feat(cuda-graphs): capture
@@ -24,10 +24,6 @@
 
 namespace moe {
 namespace {
-
-__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
-  return __uint_as_float((uint32_t)b << 16);
-}
 
 // fp32 exp: Cody-Waite reduction v = n ln2 + r (ln 2 split into an fp32 head
 // and an fp32 tail), degree-7 Taylor polynomial of e^r in Horner form with
@@ -54,95 +50,163 @@ __device__ __forceinline__ float route_exp(float v) {
 }
 
 // ---------------------------------------------------------------- R1
-constexpr int LBM = 64, LBN = 64, LBK = 16;  // 256 threads, 4x4 outputs each
+// CTA tile BM tokens x BN experts, TM x TN outputs per thread (TN = 8 is two
+// groups of 4 columns, BN/2 apart, for conflict-free 16-byte shared loads),
+// BK = 32 contraction elements per stage, a 4-stage cp.async ring for x (bf16
+// rows, converted once per stage into a transposed fp32 tile) and W_r (fp32).
+// Each output is still one fma chain in ascending h. (Chosen by measurement
+// among 8 tile shapes: 64x128 with 4x8 per thread was fastest on both the
+// Qwen3-30B and DeepSeek-V3 router shapes.)
+constexpr int LBK = 32, LSTAGES = 4;
 
-__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
-                                                            const float* __restrict__ wr,
-                                                            const float* __restrict__ bias,
-                                                            float* __restrict__ logits, int N,
-                                                            int H, int E) {
-  __shared__ __align__(16) float As[2][LBK][LBM];
-  __shared__ __align__(16) float Bs[2][LBK][LBN];
-  const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;
-  const int m0 = blockIdx.y * LBM, n0 = blockIdx.x * LBN;
-  const int a_row = tid >> 2, a_col = (tid & 3) * 4;
-  const int b_row = tid >> 4, b_col = (tid & 15) * 4;
-  float acc[4][4];
+__device__ __forceinline__ void cpa16(uint32_t dst, const void* src, uint32_t n) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cpa4(uint32_t dst, const void* src, uint32_t n) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+
+template <int BM, int BN, int TM, int TN>
+constexpr size_t router_smem_bytes() {
+  return (size_t)LSTAGES * BM * LBK * 2 + (size_t)LSTAGES * LBK * BN * 4 + (size_t)LBK * BM * 4;
+}
+
+template <int BM, int BN, int TM, int TN>
+__global__ void __launch_bounds__((BM / TM) * (BN / TN)) router_logits_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
+    float* __restrict__ logits, int N, int H, int E, int wr_vec4) {
+  constexpr int NT = (BM / TM) * (BN / TN);
+  extern __shared__ __align__(16) uint8_t rsm[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                    // [S][BM][BK] bf16
+  float* bs = reinterpret_cast<float*>(rsm + LSTAGES * BM * LBK * 2);  // [S][BK][BN]
+  float* as = bs + LSTAGES * LBK * BN;                                  // [BK][BM]
+  const int tid = threadIdx.x, tx = tid % (BN / TN), ty = tid / (BN / TN);
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  float acc[TM][TN];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-  float ra[4], rb[4];
-  auto load = [&](int k0) {
-    const int t = m0 + a_row;
-    if (t < N) {
-      const uint2 v = *reinterpret_cast<const uint2*>(x + (size_t)t * H + k0 + a_col);
-      ra[0] = bf16_to_f32((uint16_t)(v.x & 0xFFFFu));
-      ra[1] = bf16_to_f32((uint16_t)(v.x >> 16));
-      ra[2] = bf16_to_f32((uint16_t)(v.y & 0xFFFFu));
-      ra[3] = bf16_to_f32((uint16_t)(v.y >> 16));
-    } else {
-      ra[0] = ra[1] = ra[2] = ra[3] = 0.0f;
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+  const int KT = H / LBK;
+  auto col_of = [&](int j) { return (j / 4) * (BN / 2) * (TN / 8) + tx * 4 + (j % 4); };
+  auto issue = [&](int kt) {
+    if (kt < KT) {
+      const int slot = kt % LSTAGES, k0 = kt * LBK;
+      for (int c = tid; c < BM * LBK / 8; c += NT) {
+        const int row = c / (LBK / 8), q = c % (LBK / 8);
+        const int t = m0 + row;
+        const bool ok = t < N;
+        cpa16((uint32_t)__cvta_generic_to_shared(xs + (size_t)slot * BM * LBK + row * LBK + q * 8),
+              x + (size_t)(ok ? t : 0) * H + k0 + q * 8, ok ? 16u : 0u);
+      }
+      float* bsl = bs + (size_t)slot * LBK * BN;
+      if (wr_vec4) {
+        for (int c = tid; c < LBK * BN / 4; c += NT) {
+          const int k = c / (BN / 4), q = c % (BN / 4);
+          const int e = n0 + q * 4;
+          const bool ok = e < E;
+          cpa16((uint32_t)__cvta_generic_to_shared(bsl + k * BN + q * 4),
+                wr + (size_t)(k0 + k) * E + (ok ? e : 0), ok ? 16u : 0u);
+        }
+      } else {
+        for (int c = tid; c < LBK * BN; c += NT) {
+          const int k = c / BN, q = c % BN;
+          const int e = n0 + q;
+          const bool ok = e < E;
+          cpa4((uint32_t)__cvta_generic_to_shared(bsl + k * BN + q),
+               wr + (size_t)(k0 + k) * E + (ok ? e : 0), ok ? 4u : 0u);
+        }
+      }
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  for (int st = 0; st < LSTAGES - 1; ++st) issue(st);
+  for (int kt = 0; kt < KT; ++kt) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(LSTAGES - 2) : "memory");
+    __syncthreads();  // stage kt landed; every thread is done with stage kt-1 and with `as`
+    issue(kt + LSTAGES - 1);
+    const uint16_t* xsl = xs + (size_t)(kt % LSTAGES) * BM * LBK;
+    for (int c = tid; c < BM * LBK / 8; c += NT) {
+      const int m = c % BM, q = c / BM;
+      const uint4 v = *reinterpret_cast<const uint4*>(xsl + m * LBK + q * 8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = n0 + b_col + j;
-      rb[j] = (e < E) ? wr[(size_t)(k0 + b_row) * E + e] : 0.0f;
+      for (int i = 0; i < 4; ++i) {
+        as[(q * 8 + 2 * i) * BM + m] = __uint_as_float(w[i] << 16);
+        as[(q * 8 + 2 * i + 1) * BM + m] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
     }
-  };
-  auto store = [&](int buf) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) As[buf][a_col + j][a_row] = ra[j];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) Bs[buf][b_row][b_col + j] = rb[j];
-  };
-  load(0);
-  store(0);
-  __syncthreads();
-  int buf = 0;
-  for (int k0 = 0; k0 < H; k0 += LBK) {
-    const bool more = k0 + LBK < H;
-    if (more) load(k0 + LBK);
+    __syncthreads();
+    const float* bsl = bs + (size_t)(kt % LSTAGES) * LBK * BN;
 #pragma unroll
     for (int kk = 0; kk < LBK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[4] = {b.x, b.y, b.z, b.w};
+      float av[TM], bv[TN];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < TM; i += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(&as[kk * BM + ty * TM + i]);
+        av[i] = q.x; av[i + 1] = q.y; av[i + 2] = q.z; av[i + 3] = q.w;
+      }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+      for (int j = 0; j < TN; j += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(&bsl[kk * BN + col_of(j)]);
+        bv[j] = q.x; bv[j + 1] = q.y; bv[j + 2] = q.z; bv[j + 3] = q.w;
+      }
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
     }
-    if (more) store(buf ^ 1);
-    __syncthreads();
-    buf ^= 1;
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = m0 + ty * 4 + i;
+  for (int i = 0; i < TM; ++i) {
+    const int t = m0 + ty * TM + i;
     if (t >= N) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = n0 + tx * 4 + j;
+    for (int j = 0; j < TN; ++j) {
+      const int e = n0 + col_of(j);
       if (e < E) logits[(size_t)t * E + e] = __fadd_rn(acc[i][j], bias ? bias[e] : 0.0f);
     }
   }
 }
 
+template <int BM, int BN, int TM, int TN>
+cudaError_t launch_router_logits(const RouteArgs& a, int vec4, cudaStream_t s) {
+  constexpr size_t smem = router_smem_bytes<BM, BN, TM, TN>();
+  static int set_for[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || !set_for[dev]) {
+    err = cudaFuncSetAttribute(router_logits_kernel<BM, BN, TM, TN>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) set_for[dev] = 1;
+  }
+  dim3 g((a.E + BN - 1) / BN, (a.N + BM - 1) / BM);
+  router_logits_kernel<BM, BN, TM, TN><<<g, (BM / TM) * (BN / TN), smem, s>>>(
+      a.x, a.wr, a.bias, a.ws.logits, a.N, a.H, a.E, vec4);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- R2
-constexpr int kTopkWarps = 16;
+// One warp per token (32 warps, 64 tokens per CTA = one chunk). After the
+// chunk's top-K, the CTA sorts its routes by expert (stable, so each expert's
+// routes stay in token order) and records per-expert counts and offsets.
+constexpr int kTopkWarps = 32;
 
 __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
     const float* __restrict__ logits, int N, int E, int K, int renorm, int32_t* __restrict__ topk_ids,
-    float* __restrict__ topk_p, int32_t* __restrict__ chunk_rank,
-    int32_t* __restrict__ chunk_counts) {
+    float* __restrict__ topk_p, int32_t* __restrict__ chunk_counts,
+    int32_t* __restrict__ chunk_lofs, int32_t* __restrict__ chunk_routes) {
   __shared__ float zbuf[kTopkWarps][kMaxExperts];
   __shared__ int32_t ids_s[kTokensPerChunk * kMaxTopK];
   __shared__ int32_t hist[kMaxExperts];
+  __shared__ int32_t offs[kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * kTokensPerChunk;
+  const int c = blockIdx.x;
+  const int t0 = c * kTokensPerChunk;
   const int nt = min(kTokensPerChunk, N - t0);
   constexpr int PER = kMaxExperts / 32;
   for (int tl = warp; tl < nt; tl += kTopkWarps) {
@@ -174,27 +238,28 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < PER; ++j) v[j] = __fdiv_rn(v[j], s);
+    // K picks of the largest p, ties to the lower e: warp max of the p bit
+    // pattern (p >= 0, so bits order like values), then warp min of the expert
+    // ids holding that maximum.
     uint32_t taken = 0;
     float d = 0.0f, my_p = 0.0f;
     int my_id = 0;
     for (int k = 0; k < K; ++k) {
-      unsigned long long best = 0ull;
+      uint32_t best = 0;
 #pragma unroll
       for (int j = 0; j < PER; ++j) {
         const int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u)) {
-          const unsigned long long key =
-              ((unsigned long long)__float_as_uint(v[j]) << 32) | (0xFFFFFFFFu - (uint32_t)e);
-          best = key > best ? key : best;
-        }
+        if (e < E && !((taken >> j) & 1u)) best = max(best, __float_as_uint(v[j]));
       }
+      const uint32_t pmax = __reduce_max_sync(0xFFFFFFFFu, best);
+      uint32_t mine = 0xFFFFFFFFu;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        best = other > best ? other : best;
+      for (int j = PER - 1; j >= 0; --j) {
+        const int e = lane + 32 * j;
+        if (e < E && !((taken >> j) & 1u) && __float_as_uint(v[j]) == pmax) mine = (uint32_t)e;
       }
-      const int eb = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
-      const float pb = __uint_as_float((uint32_t)(best >> 32));
+      const int eb = (int)__reduce_min_sync(0xFFFFFFFFu, mine);
+      const float pb = __uint_as_float(pmax);
       if ((eb & 31) == lane) taken |= 1u << (eb >> 5);
       d = __fadd_rn(d, pb);  // pick order
       if (lane == k) { my_id = eb; my_p = pb; }
@@ -205,65 +270,44 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
       topk_p[(size_t)t * K + lane] = renorm ? __fdiv_rn(my_p, d) : my_p;
     }
   }
+  // stable counting sort of the chunk's routes by expert
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  for (int r = threadIdx.x; r < nt * K; r += blockDim.x) {
-    const int tl = r / K;
-    const int e = ids_s[r];
-    int cnt = 0;
-    for (int r2 = 0; r2 < tl * K; ++r2) cnt += (ids_s[r2] == e);
-    chunk_rank[(size_t)t0 * K + r] = cnt;
-    atomicAdd(&hist[e], 1);
-  }
+  const int nr = nt * K;
+  for (int r = threadIdx.x; r < nr; r += blockDim.x) atomicAdd(&hist[ids_s[r]], 1);
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    chunk_counts[(size_t)blockIdx.x * E + e] = hist[e];
-}
-
-// ---------------------------------------------------------------- R3
-__global__ void route_scan_kernel(const int32_t* __restrict__ chunk_counts,
-                                  int32_t* __restrict__ chunk_off,
-                                  int32_t* __restrict__ expert_counts,
-                                  int32_t* __restrict__ expert_off, int C, int E) {
-  __shared__ int32_t tot[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  if (warp == 0) {
     int run = 0;
-    for (int c = 0; c < C; ++c) {
-      const int v = chunk_counts[(size_t)c * E + e];
-      chunk_off[(size_t)c * E + e] = run;
-      run += v;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int h = (e < E) ? hist[e] : 0;
+      int incl = h;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (e < E) offs[e] = run + incl - h;
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    tot[e] = run;
-    expert_counts[e] = run;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int e = 0; e < E; ++e) {
-      expert_off[e] = acc;
-      acc += tot[e];
-    }
-    expert_off[E] = acc;
+  for (int r = threadIdx.x; r < nr; r += blockDim.x) {
+    const int e = ids_s[r];
+    const int tl = r / K;
+    int rank = 0;
+    for (int r2 = 0; r2 < tl * K; ++r2) rank += (ids_s[r2] == e);  // earlier tokens only
+    chunk_routes[(size_t)t0 * K + offs[e] + rank] = t0 * K + r;
   }
-}
-
-__global__ void route_scatter_kernel(const int32_t* __restrict__ topk_ids,
-                                     const int32_t* __restrict__ chunk_rank,
-                                     const int32_t* __restrict__ chunk_off,
-                                     const int32_t* __restrict__ expert_off,
-                                     int32_t* __restrict__ route_list, int N, int K, int E) {
-  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= (int64_t)N * K) return;
-  const int t = (int)(r / K);
-  const int c = t / kTokensPerChunk;
-  const int e = topk_ids[r];
-  if (e < 0 || e >= E) return;
-  const int64_t pos = (int64_t)expert_off[e] + chunk_off[(size_t)c * E + e] + chunk_rank[r];
-  if (pos >= 0 && pos < (int64_t)N * K) route_list[pos] = (int32_t)r;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    chunk_counts[(size_t)c * E + e] = hist[e];
+    chunk_lofs[(size_t)c * E + e] = offs[e];
+  }
 }
 
 // ---------------------------------------------------------------- R4
 constexpr int kSelThreads = 1024;
+constexpr int kMaxChunks = kMaxTokens / kTokensPerChunk;
 
 // Exclusive scan of v over the CTA (kSelThreads threads, all must call).
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
@@ -291,55 +335,81 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
   return warp_tot[warp] + incl - v;
 }
 
+// One CTA per expert: assemble the expert's routes in token order from the
+// chunk tables, select the `cap` highest p' (ties to the lower token) and
+// write the expert's part of the route-list layout.
 __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
-    const int32_t* __restrict__ expert_counts, const int32_t* __restrict__ expert_off,
-    const int32_t* __restrict__ route_list, const float* __restrict__ topk_p, int N, int E, int K,
-    int cap, int cpad, int bm, uint8_t* __restrict__ keep, int32_t* __restrict__ kept_counts,
-    int32_t* __restrict__ sorted_slot_ids, int32_t* __restrict__ expert_ids,
-    int32_t* __restrict__ block_start, int32_t* __restrict__ ntpp,
-    int32_t* __restrict__ token_routes) {
+    const int32_t* __restrict__ chunk_counts, const int32_t* __restrict__ chunk_lofs,
+    const int32_t* __restrict__ chunk_routes, const float* __restrict__ topk_p, int N, int E, int K,
+    int cap, int cpad, int bm, uint8_t* __restrict__ keep, int32_t* __restrict__ expert_counts,
+    int32_t* __restrict__ kept_counts, int32_t* __restrict__ sorted_slot_ids,
+    int32_t* __restrict__ expert_ids, int32_t* __restrict__ block_start,
+    int32_t* __restrict__ ntpp, int32_t* __restrict__ token_routes) {
   extern __shared__ uint32_t dyn[];
   __shared__ int32_t hist[256];
   __shared__ int32_t warp_tot[32];
+  __shared__ int32_t s_cnt[kMaxChunks];
+  __shared__ int32_t s_pos[kMaxChunks];
   __shared__ uint32_t s_prefix;
   __shared__ int32_t s_remaining;
+  __shared__ int32_t s_total;
   const int e = blockIdx.x;
-  const int tid = threadIdx.x;
-  // a token picks each expert at most once, so n <= N; the clamps only guard
-  // the staging buffers and the route list
-  const int n = min(max(expert_counts[e], 0), N);
-  const int off = min(max(expert_off[e], 0), N * K - n);
-  uint32_t* keys = dyn;                                  // p' bits, list order
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = (N + kTokensPerChunk - 1) / kTokensPerChunk;
+  uint32_t* keys = dyn;                                  // p' bits, token order
   int32_t* rids = reinterpret_cast<int32_t*>(dyn + N);   // route index t*K+k
-  for (int i = tid; i < n; i += kSelThreads) {
-    const int r = route_list[off + i];
-    rids[i] = r;
-    keys[i] = __float_as_uint(topk_p[r]);
+  // column e of the chunk tables -> positions in the expert's list
+  const int cnt = (tid < C) ? min(max(chunk_counts[(size_t)tid * E + e], 0), kTokensPerChunk) : 0;
+  const int pos0 = block_exclusive_scan(cnt, warp_tot);
+  if (tid < C) { s_cnt[tid] = cnt; s_pos[tid] = pos0; }
+  if (tid == C - 1) s_total = pos0 + cnt;
+  if (C == 0 && tid == 0) s_total = 0;
+  __syncthreads();
+  const int n = min(s_total, N);
+  for (int cc = warp; cc < C; cc += kSelThreads / 32) {
+    const int lo = min(max(chunk_lofs[(size_t)cc * E + e], 0), kTokensPerChunk * K);
+    const int64_t chunk_base = (int64_t)cc * kTokensPerChunk * K;
+    const int m = (int)min((int64_t)min(s_cnt[cc], kTokensPerChunk * K - lo),
+                           (int64_t)N * K - chunk_base - lo);
+    const int at = s_pos[cc];
+    for (int i = lane; i < m; i += 32) {
+      if (at + i >= n) break;
+      int r = chunk_routes[chunk_base + lo + i];
+      if ((unsigned)r >= (unsigned)(N * K)) r = 0;  // never taken when the tables agree
+      rids[at + i] = r;
+      keys[at + i] = __float_as_uint(topk_p[r]);
+    }
   }
   __syncthreads();
   const bool select = n > cap;
   uint32_t thr = 0;
   int needed = 0;
   if (select) {
-    // k-th largest key (k = cap), 8 bits at a time from the top
+    // the cap-th largest key, 8 bits at a time from the top; histogram bins
+    // are filled with warp-aggregated atomics (a hot expert's keys crowd a
+    // few bins)
     uint32_t prefix = 0, mask = 0;
     int remaining = cap;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
       __syncthreads();
-      for (int i = tid; i < n; i += kSelThreads) {
-        const uint32_t k = keys[i];
-        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+      for (int base = warp * 32; base < n; base += kSelThreads) {
+        const int i = base + lane;
+        const uint32_t k = (i < n) ? keys[i] : 0u;
+        const bool cand = (i < n) && ((k & mask) == prefix);
+        const int bin = cand ? (int)((k >> shift) & 255u) : -1;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
+        if (cand && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
       }
       __syncthreads();
       if (tid == 0) {
-        int cum = 0, d = 255;
-        for (; d > 0; --d) {
-          if (cum + hist[d] >= remaining) break;
-          cum += hist[d];
+        int cum = 0, dg = 255;
+        for (; dg > 0; --dg) {
+          if (cum + hist[dg] >= remaining) break;
+          cum += hist[dg];
         }
         s_remaining = remaining - cum;
-        s_prefix = prefix | ((uint32_t)d << shift);
+        s_prefix = prefix | ((uint32_t)dg << shift);
       }
       __syncthreads();
       remaining = s_remaining;
@@ -349,7 +419,7 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     thr = prefix;
     needed = remaining;  // how many keys equal to thr are kept (lowest tokens first)
   }
-  // each thread owns a contiguous run of the list, so scans follow list order
+  // each thread owns a contiguous run of the list, so scans follow token order
   const int ipt = (n + kSelThreads - 1) / kSelThreads;
   const int i0 = min(n, tid * ipt), i1 = min(n, i0 + ipt);
   int ties = 0;
@@ -391,12 +461,13 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     }
   }
   const int kept_e = select ? cap : n;
-  for (int s = kept_e + tid; s < cpad; s += kSelThreads) sorted_slot_ids[base + s] = N;
+  for (int sl = kept_e + tid; sl < cpad; sl += kSelThreads) sorted_slot_ids[base + sl] = N;
   const int nb = cpad / bm;
   for (int b = tid; b < nb; b += kSelThreads)
     expert_ids[(size_t)e * nb + b] = (b * bm < kept_e) ? e : -1;
   if (tid == 0) {
     block_start[e] = e * nb;
+    expert_counts[e] = n;
     kept_counts[e] = kept_e;
     if (e == 0) *ntpp = E * cpad;
   }
@@ -408,33 +479,35 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   int launched = 0;
   const int C = (a.N + kTokensPerChunk - 1) / kTokensPerChunk;
   if (a.N > 0) {
-    dim3 g1((a.E + LBN - 1) / LBN, (a.N + LBM - 1) / LBM);
-    router_logits_kernel<<<g1, 256, 0, s>>>(a.x, a.wr, a.bias, a.ws.logits, a.N, a.H, a.E);
+    const int vec4 = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 15u) == 0);
+    const cudaError_t e1 = (a.E > 64) ? launch_router_logits<64, 128, 4, 8>(a, vec4, s)
+                                      : launch_router_logits<64, 64, 4, 4>(a, vec4, s);
+    if (e1 != cudaSuccess) return -(int)e1;
     ++launched;
     router_topk_kernel<<<C, kTopkWarps * 32, 0, s>>>(a.ws.logits, a.N, a.E, a.K, a.renorm,
-                                                     a.topk_ids, a.topk_p, a.ws.chunk_rank,
-                                                     a.ws.chunk_counts);
-    ++launched;
-  }
-  route_scan_kernel<<<1, 256, 0, s>>>(a.ws.chunk_counts, a.ws.chunk_off, a.expert_counts,
-                                      a.ws.expert_off, C, a.E);
-  ++launched;
-  if (a.N > 0) {
-    const int64_t R = (int64_t)a.N * a.K;
-    route_scatter_kernel<<<(unsigned)((R + 255) / 256), 256, 0, s>>>(
-        a.topk_ids, a.ws.chunk_rank, a.ws.chunk_off, a.ws.expert_off, a.ws.route_list, a.N, a.K,
-        a.E);
+                                                     a.topk_ids, a.topk_p, a.ws.chunk_counts,
+                                                     a.ws.chunk_lofs, a.ws.chunk_routes);
     ++launched;
   }
   const size_t dyn = (size_t)a.N * 8;
-  cudaError_t err = cudaFuncSetAttribute(route_select_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-  if (err != cudaSuccess) return -(int)err;
+  cudaError_t err = cudaSuccess;
+  {
+    // raise the kernel's dynamic shared-memory limit once per device
+    static int set_for[64] = {};
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return -(int)err;
+    if (dev < 0 || dev >= 64 || !set_for[dev]) {
+      err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxTokens * 8);
+      if (err != cudaSuccess) return -(int)err;
+      if (dev >= 0 && dev < 64) set_for[dev] = 1;
+    }
+  }
   const int cap = (int)(a.cap < a.N ? a.cap : a.N);
   route_select_kernel<<<a.E, kSelThreads, dyn, s>>>(
-      a.expert_counts, a.ws.expert_off, a.ws.route_list, a.topk_p, a.N, a.E, a.K, cap,
-      (int)a.cpad, a.bm, a.keep, a.kept_counts, a.sorted_slot_ids, a.expert_ids, a.block_start,
-      a.ntpp, a.token_routes);
+      a.ws.chunk_counts, a.ws.chunk_lofs, a.ws.chunk_routes, a.topk_p, a.N, a.E, a.K, cap,
+      (int)a.cpad, a.bm, a.keep, a.expert_counts, a.kept_counts, a.sorted_slot_ids, a.expert_ids,
+      a.block_start, a.ntpp, a.token_routes);
   ++launched;
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;
