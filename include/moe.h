@@ -97,7 +97,11 @@ typedef struct moe_config {
  *  block_start     [E]   i32  first block of expert e (slots start at
  *                             block_start[e]*bm)
  *  num_tokens_post_padded [1] i32  padded extent S, as a device scalar
- *  token_routes    [N,K] i32  inverse map: slot of route (t,k), -1 if dropped */
+ *  token_routes    [N,K] i32  inverse map: slot of route (t,k), -1 if dropped
+ *  gemm_sched      [4]   i32  work counters of the expert GEMMs' tile scheduler;
+ *                             zeroed by moe_route_align and left zeroed by every
+ *                             GEMM call (a routes object serves one stream at a
+ *                             time: GEMM calls sharing it must not overlap) */
 typedef struct moe_routes {
   int32_t* topk_ids;
   float* topk_p;
@@ -109,6 +113,7 @@ typedef struct moe_routes {
   int32_t* block_start;
   int32_t* num_tokens_post_padded;
   int32_t* token_routes;
+  int32_t* gemm_sched;
 } moe_routes_t;
 
 /* Host-side size queries (no GPU work). Negative on an invalid config. */

@@ -58,7 +58,7 @@ class Config(ctypes.Structure):
 class _RoutesC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "topk_ids", "topk_p", "keep", "expert_counts", "kept_counts", "sorted_slot_ids",
-        "expert_ids", "block_start", "num_tokens_post_padded", "token_routes")]
+        "expert_ids", "block_start", "num_tokens_post_padded", "token_routes", "gemm_sched")]
 
 
 class Routes:
@@ -164,7 +164,7 @@ def alloc_routes(cfg: Config, device) -> Routes:
         expert_counts=torch.empty(E, **i32), kept_counts=torch.empty(E, **i32),
         sorted_slot_ids=torch.empty(max(S, 1), **i32), expert_ids=torch.empty(max(B, 1), **i32),
         block_start=torch.empty(E, **i32), num_tokens_post_padded=torch.empty(1, **i32),
-        token_routes=torch.empty((N, K), **i32))
+        token_routes=torch.empty((N, K), **i32), gemm_sched=torch.zeros(4, **i32))
 
 
 def alloc_workspace(cfg: Config, device):

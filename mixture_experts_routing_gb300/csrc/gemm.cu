@@ -11,25 +11,31 @@
 //  x[sorted_slot_ids[s], :], copied row by row (16-byte cp.async, 128 threads)
 //  straight into the 128-byte-swizzled operand buffer; no permuted copy of x is
 //  written. (A TMA tile::gather4 of the same rows measured 2x slower overall:
-//  one 512-byte gather per ~80 cycles per SM.) Two
-//  accumulators per CTA, gate rows and up rows of the same 128 features; the
-//  epilogue reads both from TMEM and writes h = silu(gate) * up (SwiGLU as the
-//  FC1 epilogue rather than a separate pass).
+//  one 512-byte gather per ~80 cycles per SM.) Two accumulators per tile, gate
+//  rows and up rows of the same 128 features; the epilogue reads both from TMEM
+//  and writes h = silu(gate) * up (SwiGLU as the FC1 epilogue rather than a
+//  separate pass).
 //  FC2 (route space, same section 3): B rows are h[s, :] for a contiguous slot
-//  range, fetched by tiled TMA loads; up to two 128-row output tiles per CTA
-//  share one B stage.
+//  range, fetched by tiled TMA loads; up to two 128-row output tiles share one
+//  B stage.
 //
 // The grouping comes from device-side vectors only (kept_counts, block_start:
 // "[4/5] feat: capture the FFN experts at bucketed padded shapes", What this
-// adds): the grid is the static bound E x feature tiles x slot tiles and a CTA
-// whose slot tile lies past its expert's kept count exits at once, so nothing
-// is read back to the host and the launch is graph-capturable.
+// adds): the tile list is the static bound E x feature tiles x slot tiles and a
+// tile past its expert's kept count is skipped, so nothing is read back to the
+// host and the launch is graph-capturable.
 //
-// Warp roles (192 threads): warp 0 = TMA producer (weight tiles; FC2's B
+// Persistent: one CTA per SM takes tiles from a global counter (dynamic
+// scheduling: tiles of a skewed routing differ a lot in size) and publishes
+// each tile id to its other warps through a small shared-memory queue. The
+// operand ring runs across tile boundaries, so the weight stream keeps going
+// while the epilogue of the previous tile drains TMEM and stores. The last CTA
+// to finish resets the counter, so the next launch finds it at zero.
+// Warp roles (320 threads): warp 0 = TMA producer (weight tiles; FC2's B
 // tiles), warp 1 = TMEM allocator and single-thread UMMA issuer, warps 2-5 =
-// FC1's B-row gatherers during the main loop, then the epilogue (warp w reads
-// TMEM lanes 32*(w%4) .. 32*(w%4)+31). Operand stages form a ring guarded by
-// full/empty mbarriers; UMMA completion is signalled with tcgen05.commit.
+// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31), warps 6-9 = FC1's B-row
+// gatherers. Stages are guarded by full/empty mbarriers, the accumulator by
+// tmem_full / tmem_empty; UMMA completion is signalled with tcgen05.commit.
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
@@ -43,12 +49,15 @@ constexpr int kBK = 64;           // contraction elements per stage (128 B of bf
 constexpr int kTileM = 128;       // weight rows per accumulator (UMMA M)
 constexpr int kMaxTileN = 256;    // slots per tile (UMMA N)
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;  // 16 KiB
 constexpr uint32_t kSmemBudget = 225 * 1024;
-constexpr int kGatherThreads = 128;  // warps 2-5
+constexpr int kGatherThreads = 128;  // warps 6-9
 constexpr int kGatherDepth = 2;      // cp.async groups in flight per gather thread
+constexpr int kStageRowElems = 64;   // epilogue staging row: up to 2 x 32 features (bf16)
+constexpr uint32_t kEpiStageBytes = 4u * 16u * kStageRowElems * 2u;  // 4 warps x 16 rows
+constexpr int kTileQ = 4;            // depth of the tile-id queue
 
 struct GemmParams {
   int fc1;
@@ -59,24 +68,49 @@ struct GemmParams {
   int f_rows;
   int f_tiles;
   int n_tok_tiles;
+  int n_tiles;
   int tile_n;
   int bm;
   int out_ld;
   int stages;
   uint32_t stage_bytes;
   uint32_t b_off;
+  uint32_t epi_off;      // offset of the epilogue staging buffer from the aligned smem base
   const uint16_t* act;   // FC1: x [act_rows, act_ld] for the row gather
   int act_ld;
   int act_rows;
   const int32_t* sorted_slot_ids;
   const int32_t* kept_counts;
   const int32_t* block_start;
+  int32_t* sched;        // [2]: next tile to hand out, CTAs finished
   uint16_t* out;
   uint32_t* err;
 };
 
-__device__ __forceinline__ uint16_t f32_to_bf16(float v) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+struct Tile {
+  int e, f, rows, n_eff, slot0;
+};
+
+// Decodes tile index t (slot tile fastest, then feature tile, then expert);
+// false when the tile holds no kept slot.
+__device__ __forceinline__ bool tile_at(const GemmParams& p, int t, Tile& T) {
+  const int jt = t % p.n_tok_tiles;
+  t /= p.n_tok_tiles;
+  T.f = t % p.f_tiles;
+  T.e = t / p.f_tiles;
+  T.rows = min(p.tile_n, p.kept_counts[T.e] - jt * p.tile_n);
+  if (T.rows <= 0) return false;
+  T.n_eff = (T.rows + 15) & ~15;
+  T.slot0 = p.block_start[T.e] * p.bm + jt * p.tile_n;
+  return true;
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float v) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -85,109 +119,263 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t accum_bar;
+  __shared__ __align__(8) uint64_t tmem_full_bar;
+  __shared__ __align__(8) uint64_t tmem_empty_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int32_t rows_s[kMaxTileN];
+  __shared__ volatile int gather_abort;  // set by a gatherer whose wait ran out
+  __shared__ int32_t tile_q[kTileQ];
+  __shared__ __align__(8) uint64_t tq_full[kTileQ];
+  __shared__ __align__(8) uint64_t tq_empty[kTileQ];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int idx = blockIdx.x;
-  const int jt = idx % p.n_tok_tiles;
-  idx /= p.n_tok_tiles;
-  const int f = idx % p.f_tiles;
-  const int e = idx / p.f_tiles;
-  const int rows = min(p.tile_n, p.kept_counts[e] - jt * p.tile_n);
-  if (rows <= 0) return;  // uniform over the CTA: nothing allocated or armed yet
-  const int n_eff = (rows + 15) & ~15;
-  const int slot0 = p.block_start[e] * p.bm + jt * p.tile_n;
-  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
 
   if (threadIdx.x == 0) {
+    gather_abort = 0;
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), p.fc1 ? 1 + kGatherThreads : 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
-    mbar_init(smem_u32(&accum_bar), 1);
+    mbar_init(smem_u32(&tmem_full_bar), 1);
+    mbar_init(smem_u32(&tmem_empty_bar), 4);  // one arrive per epilogue warp
+    for (int i = 0; i < kTileQ; ++i) {
+      mbar_init(smem_u32(&tq_full[i]), 1);
+      // consumers: the UMMA thread, the 4 epilogue warps, the 4 gather warps (FC1)
+      mbar_init(smem_u32(&tq_empty[i]), p.fc1 ? 9 : 5);
+    }
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     if (!p.fc1) tma_prefetch_desc(&tmB);
   }
-  if (warp >= 2 && p.fc1)
-    for (int i = threadIdx.x - 64; i < n_eff; i += kGatherThreads)
-      rows_s[i] = p.sorted_slot_ids[slot0 + i];
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
+  // Pops the next tile id (lane 0 waits, the warp gets the value); -1 ends.
+  auto pop_tile = [&](uint32_t& qi, uint32_t code) -> int {
+    const int slot = (int)(qi % kTileQ);
+    int t = -1;
+    if (lane == 0) {
+      if (mbar_wait(smem_u32(&tq_full[slot]), (qi / kTileQ) & 1u, p.err, code)) t = tile_q[slot];
+      mbar_arrive(smem_u32(&tq_empty[slot]));
+    }
+    ++qi;
+    return __shfl_sync(0xFFFFFFFFu, t, 0);
+  };
+
   if (warp == 0) {
-    // Lane 0 arms the stage barrier and loads the weight tiles; for FC2 every
-    // lane then issues its share of the B-operand tile loads.
+    // ---------------------------------------------------------------- TMA producer
+    // Also the scheduler: takes the next non-empty tile from the global counter
+    // and publishes it to the other roles.
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
-    const int a_row0 = e * p.a_rows_per_expert + f * p.f_rows;
-    const uint32_t tx = (uint32_t)p.n_acc * kATileBytes + (p.fc1 ? 0u : (uint32_t)n_eff * 128u);
-    for (int kt = 0; kt < p.k_tiles; ++kt) {
-      const int s = kt % p.stages;
-      const uint32_t u = (uint32_t)(kt / p.stages);
-      int ok = 1;
-      if (lane == 0 && kt >= p.stages)
-        ok = mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty);
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) break;
-      const uint32_t fb = smem_u32(&full_bar[s]);
-      const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
-      const int kx = kt * kBK;
+    uint32_t gk = 0;  // k-steps issued by this CTA, across tiles
+    for (uint32_t qi = 0;; ++qi) {
+      int t = -1;
       if (lane == 0) {
-        mbar_arrive_expect_tx(fb, tx);
-        tma_load_2d(st, &tmA, kx, a_row0, fb, pol_w);
-        if (p.n_acc == 2) tma_load_2d(st + kATileBytes, &tmA, kx, a_row0 + p.a_second_off, fb, pol_w);
+        Tile T0;
+        do {
+          t = atomicAdd(&p.sched[0], 1);
+        } while (t < p.n_tiles && !tile_at(p, t, T0));
+        if (t >= p.n_tiles) t = -1;
+        const int slot = (int)(qi % kTileQ);
+        if (qi >= (uint32_t)kTileQ &&
+            !mbar_wait(smem_u32(&tq_empty[slot]), ((qi / kTileQ) - 1u) & 1u, p.err, kErrWaitEmpty))
+          t = -1;
+        tile_q[slot] = t;
+        mbar_arrive(smem_u32(&tq_full[slot]));
       }
-      __syncwarp();
-      if (!p.fc1) {
-        const uint32_t b = st + p.b_off;
-        for (int q = lane * 16; q < n_eff; q += 512)
-          tma_load_2d(b + (uint32_t)q * 128u, &tmB, kx, slot0 + q, fb, pol_x);
+      t = __shfl_sync(0xFFFFFFFFu, t, 0);
+      if (t < 0) break;
+      Tile T;
+      tile_at(p, t, T);
+      const int a_row0 = T.e * p.a_rows_per_expert + T.f * p.f_rows;
+      const uint32_t tx =
+          (uint32_t)p.n_acc * kATileBytes + (p.fc1 ? 0u : (uint32_t)T.n_eff * 128u);
+      bool ok = true;
+      for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
+        const int s = (int)(gk % (uint32_t)p.stages);
+        const uint32_t u = gk / (uint32_t)p.stages;
+        int w = 1;
+        if (lane == 0 && gk >= (uint32_t)p.stages)
+          w = mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty);
+        if (!__shfl_sync(0xFFFFFFFFu, w, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full_bar[s]);
+        const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
+        const int kx = kt * kBK;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, tx);
+          tma_load_2d(st, &tmA, kx, a_row0, fb, pol_w);
+          if (p.n_acc == 2)
+            tma_load_2d(st + kATileBytes, &tmA, kx, a_row0 + p.a_second_off, fb, pol_w);
+        }
+        __syncwarp();
+        if (!p.fc1) {
+          const uint32_t b = st + p.b_off;
+          for (int q = lane * 16; q < T.n_eff; q += 512)
+            tma_load_2d(b + (uint32_t)q * 128u, &tmB, kx, T.slot0 + q, fb, pol_x);
+        }
+      }
+      if (!ok) break;
+    }
+    if (lane == 0) {
+      // every CTA has made its last fetch before counting itself finished, so
+      // the last one to finish may reset the counter for the next launch
+      __threadfence();
+      if (atomicAdd(&p.sched[1], 1) == (int)gridDim.x - 1) {
+        atomicExch(&p.sched[0], 0);
+        atomicExch(&p.sched[1], 0);
+        __threadfence();
       }
     }
   } else if (warp == 1) {
+    // ---------------------------------------------------------------- UMMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kTileM, n_eff);
-      for (int kt = 0; kt < p.k_tiles; ++kt) {
-        const int s = kt % p.stages;
-        const uint32_t u = (uint32_t)(kt / p.stages);
-        if (!mbar_wait(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) break;
-        tc_fence_after();
-        const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint32_t acc = (kt | kk) != 0;
-          const uint64_t bdesc = sdesc_sw128(st + p.b_off + (uint32_t)kk * 32u);
-          umma_bf16(tmem, sdesc_sw128(st + (uint32_t)kk * 32u), bdesc, idesc, acc);
-          if (p.n_acc == 2)
-            umma_bf16(tmem + 256u, sdesc_sw128(st + kATileBytes + (uint32_t)kk * 32u), bdesc, idesc,
-                      acc);
-        }
-        umma_commit(smem_u32(&empty_bar[s]));
-      }
-      umma_commit(smem_u32(&accum_bar));
-    }
-  } else {
-    if (p.fc1) {
-      // FC1 B operand: row r of the stage holds x[rows_s[r], kx .. kx+63],
-      // 16-byte chunk c at r*128 + ((c ^ (r%8)) * 16) (the 128-byte swizzle
-      // the UMMA descriptor expects); sentinel rows are zero-filled. Each
-      // thread keeps kGatherDepth copy groups in flight, then makes a stage's
-      // writes visible to the tensor core's async proxy and arrives.
-      const int gt = threadIdx.x - 64;
-      const int nchunks = n_eff * 8;
-      int kt = 0;
-      for (; kt < p.k_tiles; ++kt) {
-        const int s = kt % p.stages;
-        const uint32_t u = (uint32_t)(kt / p.stages);
-        if (kt >= p.stages &&
-            !mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty))
+      uint32_t gk = 0, tc = 0, qi = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = (int)(qi % kTileQ);
+        int t = -1;
+        if (mbar_wait(smem_u32(&tq_full[slot]), (qi / kTileQ) & 1u, p.err, kErrWaitFull))
+          t = tile_q[slot];
+        mbar_arrive(smem_u32(&tq_empty[slot]));
+        ++qi;
+        if (t < 0) break;
+        Tile T;
+        tile_at(p, t, T);
+        if (tc > 0 &&
+            !mbar_wait(smem_u32(&tmem_empty_bar), (tc - 1) & 1u, p.err, kErrWaitAccum)) {
+          ok = false;
           break;
+        }
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(kTileM, T.n_eff);
+        for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
+          const int s = (int)(gk % (uint32_t)p.stages);
+          const uint32_t u = gk / (uint32_t)p.stages;
+          if (!mbar_wait(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t acc = (kt | kk) != 0;
+            const uint64_t bdesc = sdesc_sw128(st + p.b_off + (uint32_t)kk * 32u);
+            umma_bf16(tmem, sdesc_sw128(st + (uint32_t)kk * 32u), bdesc, idesc, acc);
+            if (p.n_acc == 2)
+              umma_bf16(tmem + 256u, sdesc_sw128(st + kATileBytes + (uint32_t)kk * 32u), bdesc,
+                        idesc, acc);
+          }
+          umma_commit(smem_u32(&empty_bar[s]));
+        }
+        umma_commit(smem_u32(&tmem_full_bar));  // also after an abort: tracks issued MMAs
+        ++tc;
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t stg_u = sbase + p.epi_off + (uint32_t)(warp - 2) * 16u * kStageRowElems * 2u;
+    uint32_t tc = 0, qi = 0;
+    for (;;) {
+      const int t = pop_tile(qi, kErrWaitAccum);
+      if (t < 0) break;
+      Tile T;
+      tile_at(p, t, T);
+      // lane 0 waits for the whole warp, so the warp-collective TMEM loads
+      // below are reached by all lanes or by none
+      int w = 1;
+      if (lane == 0) w = mbar_wait(smem_u32(&tmem_full_bar), tc & 1u, p.err, kErrWaitAccum);
+      ++tc;
+      if (!__shfl_sync(0xFFFFFFFFu, w, 0)) break;
+      tc_fence_after();
+      const int nseg = p.fc1 ? 1 : p.n_acc;  // 32-feature segments per staged row
+      const int feat0 = p.fc1 ? T.f * kTileM + q * 32 : T.f * p.f_rows + q * 32;
+      for (int c0 = 0; c0 < T.n_eff; c0 += 16) {
+        uint32_t v0[16], v1[16];
+        tmem_ld16(tl + (uint32_t)c0, v0);
+        if (p.n_acc == 2) tmem_ld16(tl + 256u + (uint32_t)c0, v1);
+        tmem_ld_wait();
+        // lane = feature; stage [16 slots][32 or 64 features] as bf16
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float a;
+          if (p.fc1) {
+            const float g = __uint_as_float(v0[i]);
+            a = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[i]);
+          } else {
+            a = __uint_as_float(v0[i]);
+          }
+          const uint32_t at = stg_u + (uint32_t)(i * kStageRowElems + lane) * 2u;
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(at), "h"((unsigned short)bf16_bits(a)) : "memory");
+          if (!p.fc1 && p.n_acc == 2)
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(at + 64u),
+                         "h"((unsigned short)bf16_bits(__uint_as_float(v1[i])))
+                         : "memory");
+        }
+        __syncwarp();
+        // 16 rows x nseg segments of 64 bytes, 4 x 16-byte chunks each
+        const int chunks = 16 * nseg * 4;
+        for (int ch = lane; ch < chunks; ch += 32) {
+          const int row = ch / (nseg * 4), rem = ch % (nseg * 4);
+          const int seg = rem / 4, part = rem % 4;
+          uint4 val;
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                       : "r"(stg_u + (uint32_t)(row * kStageRowElems + seg * 32 + part * 8) * 2u)
+                       : "memory");
+          uint16_t* dst =
+              p.out + (size_t)(T.slot0 + c0 + row) * p.out_ld + feat0 + seg * kTileM + part * 8;
+          *reinterpret_cast<uint4*>(dst) = val;
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar));
+    }
+  } else if (p.fc1) {
+    // ---------------------------------------------------------------- FC1 row gather
+    // Row r of a stage holds x[rows_s[r], kx .. kx+63]: 16-byte chunk c at
+    // r*128 + ((c ^ (r%8)) * 16), the 128-byte swizzle the UMMA descriptor
+    // expects; sentinel rows are zero-filled. Each thread keeps kGatherDepth
+    // copy groups in flight, then makes a stage's writes visible to the tensor
+    // core's async proxy and arrives.
+    // Every gather thread walks the same tiles and meets the others at the
+    // named barrier of each tile; a thread whose wait runs out raises
+    // gather_abort, and all threads read it right after the next barrier, so
+    // they leave together and none is left waiting at a barrier.
+    const int gt = threadIdx.x - 192;
+    uint32_t gk = 0, qi = 0;
+    for (;;) {
+      const int t = pop_tile(qi, kErrWaitFull);
+      if (t < 0) break;
+      Tile T;
+      tile_at(p, t, T);
+      named_bar_sync(1, kGatherThreads);  // the previous tile's rows_s is no longer read
+      if (gather_abort) break;
+      for (int i = gt; i < T.n_eff; i += kGatherThreads)
+        rows_s[i] = p.sorted_slot_ids[T.slot0 + i];
+      named_bar_sync(1, kGatherThreads);
+      const int nchunks = T.n_eff * 8;
+      for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
+        const int s = (int)(gk % (uint32_t)p.stages);
+        const uint32_t u = gk / (uint32_t)p.stages;
+        if (gather_abort) break;
+        if (gk >= (uint32_t)p.stages &&
+            !mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty)) {
+          gather_abort = 1;
+          break;
+        }
         const uint32_t b = sbase + (uint32_t)s * p.stage_bytes + p.b_off;
         const int kx = kt * kBK;
         for (int j = gt; j < nchunks; j += kGatherThreads) {
@@ -199,55 +387,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                       valid ? 16u : 0u);
         }
         cp_async_commit();
-        if (kt >= kGatherDepth) {
+        if (gk >= (uint32_t)kGatherDepth) {
           cp_async_wait<kGatherDepth>();
           fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&full_bar[(kt - kGatherDepth) % p.stages]));
-        }
-      }
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      for (int j = kt > kGatherDepth ? kt - kGatherDepth : 0; j < kt; ++j)
-        mbar_arrive(smem_u32(&full_bar[j % p.stages]));
-    }
-    const int q = warp & 3;
-    if (mbar_wait(smem_u32(&accum_bar), 0u, p.err, kErrWaitAccum)) {
-      tc_fence_after();
-      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-      if (p.fc1) {
-        const int feat = f * kTileM + q * 32 + lane;
-        for (int c0 = 0; c0 < n_eff; c0 += 16) {
-          uint32_t g[16], u[16];
-          tmem_ld16(tl + (uint32_t)c0, g);
-          tmem_ld16(tl + 256u + (uint32_t)c0, u);
-          tmem_ld_wait();
-          uint16_t* o = p.out + (size_t)(slot0 + c0) * p.out_ld + feat;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float gv = __uint_as_float(g[i]);
-            const float uv = __uint_as_float(u[i]);
-            const float a = gv / (1.0f + __expf(-gv)) * uv;
-            o[(size_t)i * p.out_ld] = f32_to_bf16(a);
-          }
-        }
-      } else {
-        const int feat = f * p.f_rows + q * 32 + lane;
-        for (int c0 = 0; c0 < n_eff; c0 += 16) {
-          uint32_t v0[16], v1[16];
-          tmem_ld16(tl + (uint32_t)c0, v0);
-          if (p.n_acc == 2) tmem_ld16(tl + 256u + (uint32_t)c0, v1);
-          tmem_ld_wait();
-          uint16_t* o = p.out + (size_t)(slot0 + c0) * p.out_ld + feat;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[(size_t)i * p.out_ld] = f32_to_bf16(__uint_as_float(v0[i]));
-          if (p.n_acc == 2) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              o[(size_t)i * p.out_ld + kTileM] = f32_to_bf16(__uint_as_float(v1[i]));
-          }
+          mbar_arrive(smem_u32(&full_bar[(gk - kGatherDepth) % (uint32_t)p.stages]));
         }
       }
     }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (uint32_t j = gk > (uint32_t)kGatherDepth ? gk - kGatherDepth : 0u; j < gk; ++j)
+      mbar_arrive(smem_u32(&full_bar[j % (uint32_t)p.stages]));
   }
   tc_fence_before();
   __syncthreads();
@@ -283,6 +433,23 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// SM count of the current device, with the kernel's shared-memory opt-in set
+// up once per device.
+int device_sms(cudaError_t* err) {
+  static int sms[64] = {};
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && sms[dev] > 0) return sms[dev];
+  int n = 0;
+  if ((*err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return 0;
+  if ((*err = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kSmemBudget)) != cudaSuccess)
+    return 0;
+  if (dev >= 0 && dev < 64) sms[dev] = n;
+  return n;
 }
 
 }  // namespace
@@ -326,27 +493,20 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   p.n_tok_tiles = (int)((a.cpad + kMaxTileN - 1) / kMaxTileN);
   const int64_t per = (a.cpad + p.n_tok_tiles - 1) / p.n_tok_tiles;
   p.tile_n = (int)((per + 15) / 16 * 16);
+  p.n_tiles = a.E * p.f_tiles * p.n_tok_tiles;
   p.b_off = (uint32_t)p.n_acc * kATileBytes;
   p.stage_bytes = p.b_off + (((uint32_t)p.tile_n * 128u + 1023u) & ~1023u);
-  p.stages = (int)((kSmemBudget - 1024u) / p.stage_bytes);
+  p.stages = (int)((kSmemBudget - 1024u - kEpiStageBytes) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2) return -1;
-  const size_t dyn = (size_t)p.stages * p.stage_bytes + 1024;
+  p.epi_off = (uint32_t)p.stages * p.stage_bytes;
+  const size_t dyn = (size_t)p.epi_off + kEpiStageBytes + 1024;
   cudaError_t err = cudaSuccess;
-  {
-    // raise the kernel's dynamic shared-memory limit once per device
-    static int set_for[64] = {};
-    int dev = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return -(int)err;
-    if (dev < 0 || dev >= 64 || !set_for[dev]) {
-      err = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBudget);
-      if (err != cudaSuccess) return -(int)err;
-      if (dev >= 0 && dev < 64) set_for[dev] = 1;
-    }
-  }
-  const int64_t grid = (int64_t)a.E * p.f_tiles * p.n_tok_tiles;
-  moe_gemm_kernel<<<(unsigned)grid, kThreads, dyn, s>>>(tmA, tmB, p);
+  const int sms = device_sms(&err);
+  if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
+  const int grid = p.n_tiles < sms ? p.n_tiles : sms;
+  p.sched = a.sched;
+  moe_gemm_kernel<<<grid, kThreads, dyn, s>>>(tmA, tmB, p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;
   return 1;

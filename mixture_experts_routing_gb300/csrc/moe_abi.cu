@@ -61,7 +61,7 @@ int64_t cap_of(const moe_config_t* c) {
 int64_t cpad_of(const moe_config_t* c) { return roundup(cap_of(c), c->block_m); }
 
 struct WsLayout {
-  size_t logits, chunk_counts, chunk_lofs, chunk_routes, total;
+  size_t logits, chunk_counts, chunk_lofs, chunk_routes, chunk_keys, total;
 };
 
 WsLayout ws_layout(const moe_config_t* c) {
@@ -78,6 +78,7 @@ WsLayout ws_layout(const moe_config_t* c) {
   w.chunk_counts = take((size_t)(C * E) * 4);
   w.chunk_lofs = take((size_t)(C * E) * 4);
   w.chunk_routes = take((size_t)(N * K) * 4);
+  w.chunk_keys = take((size_t)(N * K) * 4);
   w.total = off;
   return w;
 }
@@ -85,7 +86,7 @@ WsLayout ws_layout(const moe_config_t* c) {
 bool routes_complete(const moe_routes_t* r) {
   return r && r->topk_ids && r->topk_p && r->keep && r->expert_counts && r->kept_counts &&
          r->sorted_slot_ids && r->expert_ids && r->block_start && r->num_tokens_post_padded &&
-         r->token_routes;
+         r->token_routes && r->gemm_sched;
 }
 
 int finish(int launched) {
@@ -151,10 +152,12 @@ int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_route
   a.block_start = out->block_start;
   a.ntpp = out->num_tokens_post_padded;
   a.token_routes = out->token_routes;
+  a.gemm_sched = out->gemm_sched;
   a.ws.logits = reinterpret_cast<float*>(ws + w.logits);
   a.ws.chunk_counts = reinterpret_cast<int32_t*>(ws + w.chunk_counts);
   a.ws.chunk_lofs = reinterpret_cast<int32_t*>(ws + w.chunk_lofs);
   a.ws.chunk_routes = reinterpret_cast<int32_t*>(ws + w.chunk_routes);
+  a.ws.chunk_keys = reinterpret_cast<uint32_t*>(ws + w.chunk_keys);
   return finish(moe::launch_route(a, stream));
 }
 
@@ -162,7 +165,8 @@ static int gemm_common(const moe_config_t* cfg, const moe_routes_t* routes, cons
                        const void* w, void* out, int fc1, cudaStream_t stream) {
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
-  if (!routes || !routes->sorted_slot_ids || !routes->kept_counts || !routes->block_start)
+  if (!routes || !routes->sorted_slot_ids || !routes->kept_counts || !routes->block_start ||
+      !routes->gemm_sched)
     return MOE_ERR_INVALID_ARG;
   if (cfg->n_tokens == 0) return MOE_OK;
   if (!act || !w || !out || !aligned16(act) || !aligned16(w) || !aligned16(out))
@@ -184,6 +188,7 @@ static int gemm_common(const moe_config_t* cfg, const moe_routes_t* routes, cons
   a.sorted_slot_ids = routes->sorted_slot_ids;
   a.kept_counts = routes->kept_counts;
   a.block_start = routes->block_start;
+  a.sched = routes->gemm_sched + (fc1 ? 0 : 2);
   a.err = err;
   return finish(moe::launch_gemm(a, stream));
 }

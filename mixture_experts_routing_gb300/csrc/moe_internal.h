@@ -16,6 +16,7 @@ struct RouteWs {
   int32_t* chunk_counts;  // [C,E] routes of expert e in chunk c
   int32_t* chunk_lofs;    // [C,E] offset of expert e's routes in chunk c's sorted list
   int32_t* chunk_routes;  // [N*K] per chunk: route indices sorted by expert, token order kept
+  uint32_t* chunk_keys;   // [N*K] the renormalised probability bits of those routes
 };
 
 struct RouteArgs {
@@ -34,6 +35,7 @@ struct RouteArgs {
   int32_t* block_start;
   int32_t* ntpp;
   int32_t* token_routes;
+  int32_t* gemm_sched;
   RouteWs ws;
 };
 
@@ -51,6 +53,7 @@ struct GemmArgs {
   const int32_t* sorted_slot_ids;
   const int32_t* kept_counts;
   const int32_t* block_start;
+  int32_t* sched;        // [2]: next tile, finished CTAs (this GEMM's pair of gemm_sched)
   uint32_t* err;
 };
 

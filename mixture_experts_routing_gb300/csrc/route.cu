@@ -199,9 +199,11 @@ constexpr int kTopkWarps = 32;
 __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
     const float* __restrict__ logits, int N, int E, int K, int renorm, int32_t* __restrict__ topk_ids,
     float* __restrict__ topk_p, int32_t* __restrict__ chunk_counts,
-    int32_t* __restrict__ chunk_lofs, int32_t* __restrict__ chunk_routes) {
+    int32_t* __restrict__ chunk_lofs, int32_t* __restrict__ chunk_routes,
+    uint32_t* __restrict__ chunk_keys) {
   __shared__ float zbuf[kTopkWarps][kMaxExperts];
   __shared__ int32_t ids_s[kTokensPerChunk * kMaxTopK];
+  __shared__ uint32_t pk_s[kTokensPerChunk * kMaxTopK];
   __shared__ int32_t hist[kMaxExperts];
   __shared__ int32_t offs[kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -266,8 +268,10 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
       if (lane == 0) ids_s[tl * K + k] = eb;
     }
     if (lane < K) {
+      const float pr = renorm ? __fdiv_rn(my_p, d) : my_p;
       topk_ids[(size_t)t * K + lane] = my_id;
-      topk_p[(size_t)t * K + lane] = renorm ? __fdiv_rn(my_p, d) : my_p;
+      topk_p[(size_t)t * K + lane] = pr;
+      pk_s[tl * K + lane] = __float_as_uint(pr);
     }
   }
   // stable counting sort of the chunk's routes by expert
@@ -298,6 +302,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
     int rank = 0;
     for (int r2 = 0; r2 < tl * K; ++r2) rank += (ids_s[r2] == e);  // earlier tokens only
     chunk_routes[(size_t)t0 * K + offs[e] + rank] = t0 * K + r;
+    chunk_keys[(size_t)t0 * K + offs[e] + rank] = pk_s[r];
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     chunk_counts[(size_t)c * E + e] = hist[e];
@@ -340,11 +345,13 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
 // write the expert's part of the route-list layout.
 __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     const int32_t* __restrict__ chunk_counts, const int32_t* __restrict__ chunk_lofs,
-    const int32_t* __restrict__ chunk_routes, const float* __restrict__ topk_p, int N, int E, int K,
+    const int32_t* __restrict__ chunk_routes, const uint32_t* __restrict__ chunk_keys, int N,
+    int E, int K,
     int cap, int cpad, int bm, uint8_t* __restrict__ keep, int32_t* __restrict__ expert_counts,
     int32_t* __restrict__ kept_counts, int32_t* __restrict__ sorted_slot_ids,
     int32_t* __restrict__ expert_ids, int32_t* __restrict__ block_start,
-    int32_t* __restrict__ ntpp, int32_t* __restrict__ token_routes) {
+    int32_t* __restrict__ ntpp, int32_t* __restrict__ token_routes,
+    int32_t* __restrict__ gemm_sched) {
   extern __shared__ uint32_t dyn[];
   __shared__ int32_t hist[256];
   __shared__ int32_t warp_tot[32];
@@ -377,7 +384,7 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
       int r = chunk_routes[chunk_base + lo + i];
       if ((unsigned)r >= (unsigned)(N * K)) r = 0;  // never taken when the tables agree
       rids[at + i] = r;
-      keys[at + i] = __float_as_uint(topk_p[r]);
+      keys[at + i] = chunk_keys[chunk_base + lo + i];
     }
   }
   __syncthreads();
@@ -402,14 +409,30 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
         if (cand && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
       }
       __syncthreads();
-      if (tid == 0) {
-        int cum = 0, dg = 255;
-        for (; dg > 0; --dg) {
-          if (cum + hist[dg] >= remaining) break;
-          cum += hist[dg];
+      if (warp == 0) {
+        // digit holding the remaining-th largest key: lane l owns bins
+        // 255-8l .. 248-8l (descending); a warp scan of the lane sums finds
+        // the lane, a short walk finds the bin
+        int h[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { h[j] = hist[255 - 8 * lane - j]; sum += h[j]; }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += u;
         }
-        s_remaining = remaining - cum;
-        s_prefix = prefix | ((uint32_t)dg << shift);
+        const int before = incl - sum;
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, before < remaining && incl >= remaining);
+        if (hit != 0u && lane == __ffs(hit) - 1) {
+          int cum = before, j = 0;
+          for (; j < 7; ++j) {
+            if (cum + h[j] >= remaining) break;
+            cum += h[j];
+          }
+          s_remaining = remaining - cum;
+          s_prefix = prefix | ((uint32_t)(255 - 8 * lane - j) << shift);
+        }
       }
       __syncthreads();
       remaining = s_remaining;
@@ -469,7 +492,10 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     block_start[e] = e * nb;
     expert_counts[e] = n;
     kept_counts[e] = kept_e;
-    if (e == 0) *ntpp = E * cpad;
+    if (e == 0) {
+      *ntpp = E * cpad;
+      for (int i = 0; i < 4; ++i) gemm_sched[i] = 0;
+    }
   }
 }
 
@@ -486,7 +512,8 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
     ++launched;
     router_topk_kernel<<<C, kTopkWarps * 32, 0, s>>>(a.ws.logits, a.N, a.E, a.K, a.renorm,
                                                      a.topk_ids, a.topk_p, a.ws.chunk_counts,
-                                                     a.ws.chunk_lofs, a.ws.chunk_routes);
+                                                     a.ws.chunk_lofs, a.ws.chunk_routes,
+                                                     a.ws.chunk_keys);
     ++launched;
   }
   const size_t dyn = (size_t)a.N * 8;
@@ -505,9 +532,9 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   }
   const int cap = (int)(a.cap < a.N ? a.cap : a.N);
   route_select_kernel<<<a.E, kSelThreads, dyn, s>>>(
-      a.ws.chunk_counts, a.ws.chunk_lofs, a.ws.chunk_routes, a.topk_p, a.N, a.E, a.K, cap,
+      a.ws.chunk_counts, a.ws.chunk_lofs, a.ws.chunk_routes, a.ws.chunk_keys, a.N, a.E, a.K, cap,
       (int)a.cpad, a.bm, a.keep, a.expert_counts, a.kept_counts, a.sorted_slot_ids, a.expert_ids,
-      a.block_start, a.ntpp, a.token_routes);
+      a.block_start, a.ntpp, a.token_routes, a.gemm_sched);
   ++launched;
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;

@@ -81,7 +81,7 @@ def test_entry_points_reject_bad_arguments_before_launch(L):
     # missing routes
     assert L.moe_route_align(ctypes.byref(cfg), 16, 16, None, ctypes.byref(empty), 256, 1 << 20,
                              None) == -1
-    full = moe._RoutesC(*([256] * 10))
+    full = moe._RoutesC(*([256] * len(moe._RoutesC._fields_)))
     # null x / router weight
     assert L.moe_route_align(ctypes.byref(cfg), None, 16, None, ctypes.byref(full), 256, 1 << 20,
                              None) == -1
