@@ -31,11 +31,13 @@
 // operand ring runs across tile boundaries, so the weight stream keeps going
 // while the epilogue of the previous tile drains TMEM and stores. The last CTA
 // to finish resets the counter, so the next launch finds it at zero.
-// Warp roles (320 threads): warp 0 = TMA producer (weight tiles; FC2's B
-// tiles), warp 1 = TMEM allocator and single-thread UMMA issuer, warps 2-5 =
-// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31), warps 6-9 = FC1's B-row
-// gatherers. Stages are guarded by full/empty mbarriers, the accumulator by
-// tmem_full / tmem_empty; UMMA completion is signalled with tcgen05.commit.
+// Warp roles (448 threads): warp 0 = TMA producer (weight tiles; FC2's B
+// tiles), warp 1 = TMEM allocator and single-thread UMMA issuer, warps 2-9 =
+// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31; two warps per lane
+// quarter take alternate 16-column chunks, halving the time TMEM stays
+// occupied), warps 10-13 = FC1's B-row gatherers. Stages are guarded by
+// full/empty mbarriers, the accumulator by tmem_full / tmem_empty; UMMA
+// completion is signalled with tcgen05.commit.
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
@@ -49,14 +51,16 @@ constexpr int kBK = 64;           // contraction elements per stage (128 B of bf
 constexpr int kTileM = 128;       // weight rows per accumulator (UMMA M)
 constexpr int kMaxTileN = 256;    // slots per tile (UMMA N)
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kEpiWarps = 8;         // warps 2-9
+constexpr int kGatherWarp0 = 10;     // warps 10-13
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;  // 16 KiB
 constexpr uint32_t kSmemBudget = 225 * 1024;
-constexpr int kGatherThreads = 128;  // warps 6-9
+constexpr int kGatherThreads = 128;  // warps 10-13
 constexpr int kGatherDepth = 2;      // cp.async groups in flight per gather thread
 constexpr int kStageRowElems = 64;   // epilogue staging row: up to 2 x 32 features (bf16)
-constexpr uint32_t kEpiStageBytes = 4u * 16u * kStageRowElems * 2u;  // 4 warps x 16 rows
+constexpr uint32_t kEpiStageBytes = kEpiWarps * 16u * kStageRowElems * 2u;  // per warp 16 rows
 constexpr int kTileQ = 4;            // depth of the tile-id queue
 
 struct GemmParams {
@@ -139,11 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     mbar_init(smem_u32(&tmem_full_bar), 1);
-    mbar_init(smem_u32(&tmem_empty_bar), 4);  // one arrive per epilogue warp
+    mbar_init(smem_u32(&tmem_empty_bar), kEpiWarps);  // one arrive per epilogue warp
     for (int i = 0; i < kTileQ; ++i) {
       mbar_init(smem_u32(&tq_full[i]), 1);
-      // consumers: the UMMA thread, the 4 epilogue warps, the 4 gather warps (FC1)
-      mbar_init(smem_u32(&tq_empty[i]), p.fc1 ? 9 : 5);
+      // consumers: the UMMA thread, the epilogue warps, the 4 gather warps (FC1)
+      mbar_init(smem_u32(&tq_empty[i]), 1 + kEpiWarps + (p.fc1 ? 4 : 0));
     }
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
@@ -281,9 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++tc;
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;  // which of the two warps of this lane quarter
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t stg_u = sbase + p.epi_off + (uint32_t)(warp - 2) * 16u * kStageRowElems * 2u;
     uint32_t tc = 0, qi = 0;
@@ -301,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int nseg = p.fc1 ? 1 : p.n_acc;  // 32-feature segments per staged row
       const int feat0 = p.fc1 ? T.f * kTileM + q * 32 : T.f * p.f_rows + q * 32;
-      for (int c0 = 0; c0 < T.n_eff; c0 += 16) {
+      for (int c0 = half * 16; c0 < T.n_eff; c0 += 32) {
         uint32_t v0[16], v1[16];
         tmem_ld16(tl + (uint32_t)c0, v0);
         if (p.n_acc == 2) tmem_ld16(tl + 256u + (uint32_t)c0, v1);
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // named barrier of each tile; a thread whose wait runs out raises
     // gather_abort, and all threads read it right after the next barrier, so
     // they leave together and none is left waiting at a barrier.
-    const int gt = threadIdx.x - 192;
+    const int gt = threadIdx.x - kGatherWarp0 * 32;
     uint32_t gk = 0, qi = 0;
     for (;;) {
       const int t = pop_tile(qi, kErrWaitFull);
