@@ -213,3 +213,125 @@ def route(x_bits: np.ndarray, wr: np.ndarray, bias: Optional[np.ndarray], E: int
     ids, p, _, _ = router(x_bits, wr, bias, K, renorm)
     cap = capacity(N, K, E, cap_num, cap_den)
     return Routing(ids, p, select_layout(ids, p, E, cap, bm))
+
+
+# ---------------------------------------------------------------- dropless variant + backward
+def _bind_backward(L):
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    if getattr(L, "_bwd_bound", False):
+        return L
+    L.oracle_dropless_extent.argtypes = [i64, i64, i64, i32, P, i32, i32]
+    L.oracle_dropless_extent.restype = i64
+    L.oracle_dropless_layout.argtypes = [i32, i32, i32, i32, P, i32, i32, i64, P, P, P, P, P, P, P,
+                                         P]
+    L.oracle_dropless_layout.restype = i32
+    L.oracle_bwd_routes.argtypes = [i32, P, P, P, i32, i32, P, P, P, P, P, P, P, P, P, P]
+    L.oracle_bwd_routes.restype = i32
+    L.oracle_wgrad_expert.argtypes = [i32, P, i32, i32, P, P, P, P, P, P, P, P]
+    L.oracle_wgrad_expert.restype = i32
+    L._bwd_bound = True
+    return L
+
+
+def dropless_extent(count: int, R: int, E: int, bm: int, ladder_num, ladder_den: int) -> int:
+    L = _bind_backward(lib())
+    lad = np.ascontiguousarray(ladder_num, dtype=np.int32)
+    return int(L.oracle_dropless_extent(count, R, E, bm, _p(lad), len(lad), ladder_den))
+
+
+def dropless_s_max(N: int, K: int, E: int, bm: int, ladder_num, ladder_den: int) -> int:
+    """Static slot bound: R + E * (top rung + bm)."""
+    R = N * K
+    top = dropless_extent(0, R, E, bm, [max(ladder_num)], ladder_den) if len(ladder_num) else 0
+    return R + E * (top + bm)
+
+
+@dataclass
+class DroplessLayout:
+    expert_counts: np.ndarray
+    extents: np.ndarray
+    block_start: np.ndarray
+    sorted_slot_ids: np.ndarray   # [s_max]
+    expert_ids: np.ndarray        # [s_max / bm]
+    num_tokens_post_padded: int
+    token_routes: np.ndarray      # [N, K]
+
+
+def dropless_layout(topk_ids: np.ndarray, E: int, bm: int, ladder_num, ladder_den: int) -> DroplessLayout:
+    L = _bind_backward(lib())
+    topk_ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    N, K = topk_ids.shape
+    lad = np.ascontiguousarray(ladder_num, dtype=np.int32)
+    s_max = dropless_s_max(N, K, E, bm, lad, ladder_den)
+    ec, ex, bs = (np.empty(E, np.int32) for _ in range(3))
+    ssi = np.empty(s_max, np.int32)
+    eid = np.empty(s_max // bm, np.int32)
+    ntpp = np.zeros(1, np.int32)
+    tr = np.empty((N, K), np.int32)
+    rc = L.oracle_dropless_layout(N, E, K, bm, _p(lad), len(lad), ladder_den, s_max, _p(topk_ids),
+                                  _p(ec), _p(ex), _p(bs), _p(ssi), _p(eid), _p(ntpp), _p(tr))
+    if rc != 0:
+        raise RuntimeError("oracle_dropless_layout failed: %d" % rc)
+    return DroplessLayout(ec, ex, bs, ssi, eid, int(ntpp[0]), tr)
+
+
+def bwd_routes(tokens, experts, probs, x_bits, dy_bits, W: ExpertWeights, H: int, I: int):
+    """Per-route backward: (dprob [n], dxr [n,H], dg [n,I], du [n,I], aw [n,I])."""
+    L = _bind_backward(lib())
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    experts = np.ascontiguousarray(experts, dtype=np.int32)
+    probs = np.ascontiguousarray(probs, dtype=np.float32)
+    n = len(tokens)
+    out = dict(dprob=np.empty(n, np.float32), dxr=np.empty((n, H), np.float32),
+               dg=np.empty((n, I), np.float32), du=np.empty((n, I), np.float32),
+               aw=np.empty((n, I), np.float32))
+    rc = L.oracle_bwd_routes(n, _p(tokens), _p(experts), _p(probs), H, I,
+                             _p(np.ascontiguousarray(x_bits, dtype=np.uint16)),
+                             _p(np.ascontiguousarray(dy_bits, dtype=np.uint16)), W.wg, W.wu, W.wd,
+                             _p(out["dprob"]), _p(out["dxr"]), _p(out["dg"]), _p(out["du"]),
+                             _p(out["aw"]))
+    if rc != 0:
+        raise RuntimeError("oracle_bwd_routes failed: %d" % rc)
+    return out
+
+
+def wgrad_expert(tokens, x_bits, dy_bits, aw, dg, du, H: int, I: int):
+    """(dWd [I,H], dWg [H,I], dWu [H,I]) of one expert from its routes in slot order."""
+    L = _bind_backward(lib())
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    n = len(tokens)
+    dwd = np.empty((I, H), np.float32)
+    dwg = np.empty((H, I), np.float32)
+    dwu = np.empty((H, I), np.float32)
+    L.oracle_wgrad_expert(n, _p(tokens), H, I, _p(np.ascontiguousarray(x_bits, dtype=np.uint16)),
+                          _p(np.ascontiguousarray(dy_bits, dtype=np.uint16)),
+                          _p(np.ascontiguousarray(aw, dtype=np.float32)),
+                          _p(np.ascontiguousarray(dg, dtype=np.float32)),
+                          _p(np.ascontiguousarray(du, dtype=np.float32)), _p(dwd), _p(dwg), _p(dwu))
+    return dwd, dwg, dwu
+
+
+def backward_all(x_bits, dy_bits, W: ExpertWeights, H: int, I: int, E: int, topk_ids, topk_p,
+                 token_routes):
+    """Whole expert-path backward: dX [N,H], dprob [N,K], dW per expert (dicts).
+    Routes are processed in slot order per expert (token_routes gives the slot)."""
+    N, K = topk_ids.shape
+    r = np.nonzero(token_routes.ravel() >= 0)[0]
+    tok, kk = r // K, r % K
+    ex = topk_ids.ravel()[r]
+    pr = topk_p.ravel()[r]
+    out = bwd_routes(tok, ex, pr, x_bits, dy_bits, W, H, I)
+    dX = np.zeros((N, H), np.float32)
+    for k in range(K):  # k order
+        m = kk == k
+        dX[tok[m]] = dX[tok[m]] + out["dxr"][m]
+    dprob = np.zeros((N, K), np.float32)
+    dprob[tok, kk] = out["dprob"]
+    slots = token_routes.ravel()[r]
+    dW = {}
+    for e in range(E):
+        sel = np.nonzero(ex == e)[0]
+        sel = sel[np.argsort(slots[sel], kind="stable")]
+        dW[e] = wgrad_expert(tok[sel], x_bits, dy_bits, out["aw"][sel], out["dg"][sel],
+                             out["du"][sel], H, I)
+    return dX, dprob, dW

@@ -22,17 +22,27 @@
  *      silu(gate)*up, FC2 ("Permute-Free ...", section 3 "End-to-end flow")
  *   6. gather-combine: each token sums its kept routes weighted by routing
  *      probability ("Permute-Free ...", section 2 "Core idea")
+ * Dropless, bucketed variant and backward (second half of the file):
+ *   7. dropless layout: per-expert extents from a ladder of multiples of the
+ *      expected rows ("[4/5] feat: capture the FFN experts at bucketed padded
+ *      shapes", What this adds)
+ *   8. expert-path backward given dY: FC2 data gradient, SwiGLU backward with
+ *      the activation recomputed from gate and up, routing-weight gradient,
+ *      FC1 data gradient reduced per token, weight gradients in slot order
+ *      ("Permute-Free ...", sections 3, 5 and 6)
  *
  * Floating point: fp32 throughout, as the library's contract states (fp32
  * accumulation). Every output element is produced by one thread in a fixed
  * order, so results do not depend on the OpenMP thread count. Build with
  * -ffp-contract=off so that no a*b+c is fused except where fmaf() is written.
  *
- * Parity pins (tests/test_oracle_pins.py): capacity worked values, invariants
- * of the layout, brute-force selection by rank counting, a dense fp64
- * reference on tiny inputs, exp against the C library, top-K against a stable
- * sort, and reductions to a plain SwiGLU MLP (E=1,K=1) and to a dense softmax
- * mixture (K=E).
+ * Parity pins (tests/test_oracle_pins.py, tests/test_oracle_backward_pins.py):
+ * capacity worked values, invariants of both layouts, hand-worked layouts,
+ * brute-force selection by rank counting, a dense fp64 reference on tiny
+ * inputs, exp against the C library, top-K against a stable sort, reductions
+ * to a plain SwiGLU MLP (E=1,K=1) and to a dense softmax mixture (K=E),
+ * central finite differences of an fp64 forward for every backward output.
+ * tests/test_oracle_mutations.py plants mistakes here and checks a pin fails.
  */
 #include <math.h>
 #include <stdint.h>
@@ -355,4 +365,187 @@ int oracle_forward_tokens(int t0, int t1, int K, int H, int I, const uint16_t* x
   if (rc == 0) rc = oracle_combine(t0, t1, K, H, keep, topk_p, o, y);
   free(on); free(o); free(tok); free(ex); free(pos);
   return rc;
+}
+
+/* ======================================================================== */
+/* Dropless, bucketed variant ("[4/5] feat: capture the FFN experts at      */
+/* bucketed padded shapes", What this adds: a ladder of buckets built as    */
+/* multiples of the expected item size; an item takes the smallest bucket   */
+/* that holds it, and runs unpadded when none does).                        */
+/* Per expert: rung_j = roundup(ceil(num_j*R / (den*E)), bm) with R = N*K;  */
+/* extent_e = the smallest rung >= count_e, else roundup(count_e, bm).      */
+/* Nothing is dropped. Expert e's slots start at the exclusive scan of the  */
+/* extents; its tokens fill them in ascending t, the rest hold sentinel N.  */
+/* Slots past the total up to s_max hold N, their blocks -1.                */
+/* ======================================================================== */
+int64_t oracle_dropless_extent(int64_t count, int64_t R, int64_t E, int bm, const int32_t* ladder_num,
+                               int ladder_len, int ladder_den) {
+  for (int j = 0; j < ladder_len; ++j) {
+    const int64_t num = (int64_t)ladder_num[j] * R;
+    const int64_t den = (int64_t)ladder_den * E;
+    int64_t rung = (num + den - 1) / den;
+    rung = (rung + bm - 1) / bm * bm;
+    if (count <= rung) return rung;
+  }
+  return (count + bm - 1) / bm * bm;
+}
+
+int oracle_dropless_layout(int N, int E, int K, int bm, const int32_t* ladder_num, int ladder_len,
+                           int ladder_den, int64_t s_max, const int32_t* topk_ids,
+                           int32_t* expert_counts, int32_t* extents, int32_t* block_start,
+                           int32_t* sorted_slot_ids, int32_t* expert_ids,
+                           int32_t* num_tokens_post_padded, int32_t* token_routes) {
+  const int64_t R = (int64_t)N * K;
+  for (int e = 0; e < E; ++e) expert_counts[e] = 0;
+  for (int64_t r = 0; r < R; ++r) expert_counts[topk_ids[r]] += 1;
+  int64_t base = 0;
+  for (int e = 0; e < E; ++e) {
+    extents[e] = (int32_t)oracle_dropless_extent(expert_counts[e], R, E, bm, ladder_num, ladder_len,
+                                                 ladder_den);
+    block_start[e] = (int32_t)(base / bm);
+    base += extents[e];
+  }
+  if (base > s_max) return -3;
+  *num_tokens_post_padded = (int32_t)base;
+  for (int64_t s = 0; s < s_max; ++s) sorted_slot_ids[s] = N;
+  for (int64_t b = 0; b < s_max / bm; ++b) expert_ids[b] = -1;
+  for (int e = 0; e < E; ++e) {
+    const int64_t b0 = (int64_t)block_start[e] * bm;
+    int64_t j = 0;
+    for (int t = 0; t < N; ++t) /* ascending token order */
+      for (int k = 0; k < K; ++k)
+        if (topk_ids[(int64_t)t * K + k] == e) {
+          sorted_slot_ids[b0 + j] = t;
+          token_routes[(int64_t)t * K + k] = (int32_t)(b0 + j);
+          ++j;
+        }
+    for (int64_t b = 0; b < extents[e] / bm; ++b)
+      expert_ids[b0 / bm + b] = (b * bm < expert_counts[e]) ? e : -1;
+  }
+  return 0;
+}
+
+/* ======================================================================== */
+/* Backward of the expert path for one route (token t, expert e, weight p'): */
+/* the vector-Jacobian product of y[t] += p' * o with o = a . Wd[e],        */
+/* a = silu(g)*u, g = x_t . Wg[e], u = x_t . Wu[e], given dY[t]:            */
+/*   dA0_i = sum_j dY_j * Wd[e,i,j]        (FC2 data gradient, route space) */
+/*   dprob = sum_i a_i * dA0_i             (gradient of the routing weight) */
+/*   dA = p' * dA0                                                          */
+/*   dg_i = dA_i * u_i * s_i * (1 + g_i*(1 - s_i)),  s = sigmoid(g)         */
+/*   du_i = dA_i * silu(g_i)                                                */
+/*   dXr_h = sum_i dg_i*Wg[e,h,i] + du_i*Wu[e,h,i]                          */
+/* SwiGLU is recomputed from g and u ("Permute-Free ...", section 6: "swiglu */
+/* is just an op", recomputed in the backward). fp32, fixed orders.          */
+/* Outputs (any may be NULL): dprob, dxr [H], dg [I], du [I], aw [I] = p'*a. */
+/* ======================================================================== */
+static void bwd_one(int H, int I, float p, const uint16_t* xrow, const uint16_t* dyrow,
+                    const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, float* g, float* u,
+                    float* da0, float* dprob, float* dxr, float* dg_out, float* du_out,
+                    float* aw_out) {
+  for (int i = 0; i < I; ++i) { g[i] = 0.0f; u[i] = 0.0f; }
+  for (int h = 0; h < H; ++h) {
+    const float xv = bf16_to_f32(xrow[h]);
+    for (int i = 0; i < I; ++i) {
+      g[i] = g[i] + xv * bf16_to_f32(wg[(size_t)h * I + i]);
+      u[i] = u[i] + xv * bf16_to_f32(wu[(size_t)h * I + i]);
+    }
+  }
+  for (int i = 0; i < I; ++i) {
+    float acc = 0.0f;
+    const uint16_t* wdr = wd + (size_t)i * H;
+    for (int j = 0; j < H; ++j) acc = acc + bf16_to_f32(dyrow[j]) * bf16_to_f32(wdr[j]);
+    da0[i] = acc;
+  }
+  float dp = 0.0f;
+  for (int i = 0; i < I; ++i) {
+    const float s = 1.0f / (1.0f + expf(-g[i]));
+    const float silu = g[i] * s;
+    const float a = silu * u[i];
+    dp = dp + a * da0[i];
+    const float dA = p * da0[i];
+    const float dgi = dA * u[i] * s * (1.0f + g[i] * (1.0f - s));
+    const float dui = dA * silu;
+    if (aw_out) aw_out[i] = p * a;
+    da0[i] = dgi; /* reuse: da0 now holds dg */
+    u[i] = dui;   /* reuse: u now holds du */
+  }
+  if (dprob) *dprob = dp;
+  if (dg_out) memcpy(dg_out, da0, sizeof(float) * (size_t)I);
+  if (du_out) memcpy(du_out, u, sizeof(float) * (size_t)I);
+  if (dxr) {
+    for (int h = 0; h < H; ++h) {
+      float acc = 0.0f;
+      const uint16_t* wgr = wg + (size_t)h * I;
+      const uint16_t* wur = wu + (size_t)h * I;
+      for (int i = 0; i < I; ++i)
+        acc = acc + da0[i] * bf16_to_f32(wgr[i]) + u[i] * bf16_to_f32(wur[i]);
+      dxr[h] = acc;
+    }
+  }
+}
+
+/* Backward for a list of n routes (token, expert, p'). Per route outputs as in
+ * bwd_one, stored row-wise; NULL skips an output. */
+int oracle_bwd_routes(int n, const int32_t* tokens, const int32_t* experts, const float* probs, int H,
+                      int I, const uint16_t* x, const uint16_t* dy, const uint16_t* const* wg,
+                      const uint16_t* const* wu, const uint16_t* const* wd, float* dprob,
+                      float* dxr, float* dg, float* du, float* aw) {
+  int bad = 0;
+#pragma omp parallel
+  {
+    float* g = (float*)malloc(sizeof(float) * (size_t)I);
+    float* u = (float*)malloc(sizeof(float) * (size_t)I);
+    float* d = (float*)malloc(sizeof(float) * (size_t)I);
+    if (!g || !u || !d) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int r = 0; r < n; ++r) {
+        const int e = experts[r];
+        const int t = tokens[r];
+        bwd_one(H, I, probs[r], x + (size_t)t * H, dy + (size_t)t * H, wg[e], wu[e], wd[e], g, u, d,
+                dprob ? dprob + r : NULL, dxr ? dxr + (size_t)r * H : NULL,
+                dg ? dg + (size_t)r * I : NULL, du ? du + (size_t)r * I : NULL,
+                aw ? aw + (size_t)r * I : NULL);
+      }
+    }
+    free(g); free(u); free(d);
+  }
+  return bad ? -2 : 0;
+}
+
+/* Weight gradients of one expert from its routes in ascending slot order:
+ *   dWd[i,j] = sum_s aw_s[i] * dY[t_s, j]     (aw = p' * a)
+ *   dWg[h,i] = sum_s x[t_s, h] * dg_s[i],  dWu[h,i] = sum_s x[t_s, h] * du_s[i]
+ * n routes; rows of aw/dg/du [n, I]; outputs fp32 (any may be NULL). */
+int oracle_wgrad_expert(int n, const int32_t* tokens, int H, int I, const uint16_t* x,
+                        const uint16_t* dy, const float* aw, const float* dg, const float* du,
+                        float* dwd /*[I,H]*/, float* dwg /*[H,I]*/, float* dwu /*[H,I]*/) {
+  if (dwd) {
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < I; ++i)
+      for (int j = 0; j < H; ++j) {
+        float acc = 0.0f;
+        for (int s = 0; s < n; ++s)
+          acc = acc + aw[(size_t)s * I + i] * bf16_to_f32(dy[(size_t)tokens[s] * H + j]);
+        dwd[(size_t)i * H + j] = acc;
+      }
+  }
+  if (dwg || dwu) {
+#pragma omp parallel for schedule(static)
+    for (int h = 0; h < H; ++h)
+      for (int i = 0; i < I; ++i) {
+        float ag = 0.0f, au = 0.0f;
+        for (int s = 0; s < n; ++s) {
+          const float xv = bf16_to_f32(x[(size_t)tokens[s] * H + h]);
+          ag = ag + xv * dg[(size_t)s * I + i];
+          au = au + xv * du[(size_t)s * I + i];
+        }
+        if (dwg) dwg[(size_t)h * I + i] = ag;
+        if (dwu) dwu[(size_t)h * I + i] = au;
+      }
+  }
+  return 0;
 }

@@ -1,0 +1,63 @@
+"""The pins catch plausible mistakes: each case plants one mistake in a
+temporary copy of the oracle's C source, builds it, and requires that a pin
+fails against it. (Mistakes are planted in the oracle, on the CPU.)"""
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_backward_pins as bp
+import test_oracle_pins as fp
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
+
+MUTATIONS = [
+    ("top-K ties to the higher expert", "p[e] > p[best]) best = e;", "p[e] >= p[best]) best = e;",
+     lambda: fp.test_router_hand_worked_cases()),
+    ("capacity rounded down", "return (num + den - 1) / den;", "return num / den;",
+     lambda: fp.test_capacity_worked_values()),
+    ("selection ignores the probability", "if (x->p > y->p) return -1;\n  if (x->p < y->p) return 1;",
+     "", lambda: [fp.test_selection_matches_brute_force_rank(s) for s in range(6)]),
+    ("kept tokens laid out in probability order",
+     "    qsort(buf, (size_t)kept, sizeof(route_key), cmp_token_asc); /* kept ones in ascending t */\n",
+     "", lambda: fp.test_layout_hand_worked("layout_prob_k2.txt")),
+    ("silu without its gate factor", "const float s = g[i] / (1.0f + expf(-g[i]));",
+     "const float s = 1.0f / (1.0f + expf(-g[i]));",
+     lambda: fp.test_single_expert_top1_is_plain_swiglu_mlp()),
+    ("renormalisation skipped", "topk_p[(size_t)t * K + k] = topk_p[(size_t)t * K + k] / d;",
+     "topk_p[(size_t)t * K + k] = topk_p[(size_t)t * K + k];",
+     lambda: fp.test_router_matches_fp64_library_routines(37, 64, 8, 2, False)),
+    ("SwiGLU backward loses the derivative term", "(1.0f + g[i] * (1.0f - s))", "(1.0f)",
+     lambda: bp.test_backward_matches_central_differences(0)),
+    ("dprob taken from the weighted gradient", "dp = dp + a * da0[i];", "dp = dp + a * p * da0[i];",
+     lambda: bp.test_backward_matches_central_differences(1)),
+    ("dW_down without the routing weight", "if (aw_out) aw_out[i] = p * a;",
+     "if (aw_out) aw_out[i] = a;", lambda: bp.test_weight_gradients_match_fp64_closed_form()),
+    ("dropless extent ignores the ladder", "    if (count <= rung) return rung;", "",
+     lambda: bp.test_dropless_layout_hand_worked()),
+]
+
+
+@pytest.mark.parametrize("name,old,new,pin", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pin_fails_on_planted_mistake(name, old, new, pin, monkeypatch):
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation site must be unique: " + name
+    tmp = tempfile.mkdtemp(prefix="oracle_mut_")
+    try:
+        c = os.path.join(tmp, "moe_oracle.c")
+        so = os.path.join(tmp, "liboracle.so")
+        open(c, "w").write(src.replace(old, new))
+        subprocess.run(["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-ffp-contract=off", "-fopenmp",
+                        "-fPIC", "-shared", c, "-o", so, "-lm"], check=True)
+        monkeypatch.setattr(oracle, "_SRC", c)
+        monkeypatch.setattr(oracle, "_LIB", so)
+        monkeypatch.setattr(oracle, "_lib", None)
+        with pytest.raises(AssertionError):
+            pin()
+    finally:
+        oracle._lib = None
+        shutil.rmtree(tmp, ignore_errors=True)
