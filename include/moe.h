@@ -62,11 +62,19 @@ extern "C" {
  *  n_experts E   1..256
  *  top_k     K   1..min(E,16) experts per token
  *  inter     I   SwiGLU intermediate width per expert; multiple of 128
- *  cap_num/cap_den  capacity factor F = cap_num/cap_den (> 0); the source
- *                capacity is cap = ceil(N*K*F/E) ([FC] Design notes)
+ *  cap_num/cap_den  capacity factor F = cap_num/cap_den; the source
+ *                capacity is cap = ceil(N*K*F/E) ([FC] Design notes).
+ *                cap_num = 0 selects the dropless, bucketed layout: no route
+ *                is dropped and expert e's slot region has the extent of the
+ *                smallest ladder rung that holds its route count ([BK] What
+ *                this adds), or its count rounded up to bm if none does
  *  block_m   bm  padding granularity of the route list: 16, 32, 64 or 128
  *  renorm    1 = renormalise the K chosen probabilities to sum to 1, 0 = keep
- *                the softmax probabilities */
+ *                the softmax probabilities
+ *  ladder_len, ladder_den, ladder_num (dropless only; ladder_len 0..16)
+ *                rung j = roundup(ceil(ladder_num[j]*N*K / (ladder_den*E)), bm):
+ *                multiples ladder_num[j]/ladder_den of the expected rows per
+ *                expert; ladder_num is a host array, ascending, positive */
 typedef struct moe_config {
   int32_t n_tokens;
   int32_t hidden;
@@ -77,6 +85,9 @@ typedef struct moe_config {
   int32_t cap_den;
   int32_t block_m;
   int32_t renorm;
+  int32_t ladder_len;
+  int32_t ladder_den;
+  const int32_t* ladder_num;
 } moe_config_t;
 
 /* Routing metadata written by moe_route_align ([PF] section 4). All device
@@ -117,8 +128,10 @@ typedef struct moe_routes {
 } moe_routes_t;
 
 /* Host-side size queries (no GPU work). Negative on an invalid config. */
-int64_t moe_capacity(const moe_config_t* cfg);    /* cap = ceil(N*K*F/E) */
-int64_t moe_max_slots(const moe_config_t* cfg);   /* S = E*roundup(cap,bm) */
+int64_t moe_capacity(const moe_config_t* cfg);    /* cap = ceil(N*K*F/E); N when dropless */
+/* S = E*roundup(cap,bm); dropless: N*K + E*(top rung + bm), the static bound of
+ * the padded extent (the real extent is num_tokens_post_padded) */
+int64_t moe_max_slots(const moe_config_t* cfg);
 int64_t moe_max_blocks(const moe_config_t* cfg);  /* S / bm */
 /* Bytes of scratch moe_route_align needs (0 when N == 0). */
 int64_t moe_route_workspace_bytes(const moe_config_t* cfg);

@@ -47,12 +47,17 @@ class Config(ctypes.Structure):
     """Mirror of moe_config_t."""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_tokens", "hidden", "n_experts", "top_k", "inter", "cap_num", "cap_den", "block_m",
-        "renorm")]
+        "renorm", "ladder_len", "ladder_den")] + [("ladder_num", ctypes.POINTER(ctypes.c_int32))]
 
     def __init__(self, n_tokens, hidden, n_experts, top_k, inter, cap_num=1, cap_den=1,
-                 block_m=32, renorm=1):
+                 block_m=32, renorm=1, ladder=None, ladder_den=1):
+        """cap_num=0 selects the dropless layout; ladder: rung multipliers
+        (numerators over ladder_den) of the expected rows per expert."""
+        lad = list(ladder or [])
+        self._ladder = (ctypes.c_int32 * max(len(lad), 1))(*lad)
         super().__init__(n_tokens, hidden, n_experts, top_k, inter, cap_num, cap_den, block_m,
-                         renorm)
+                         renorm, len(lad), ladder_den,
+                         ctypes.cast(self._ladder, ctypes.POINTER(ctypes.c_int32)))
 
 
 class _RoutesC(ctypes.Structure):

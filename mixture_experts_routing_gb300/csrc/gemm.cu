@@ -56,10 +56,12 @@ constexpr int kEpiWarps = 8;         // warps 2-9
 constexpr int kGatherWarp0 = 10;     // warps 10-13
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;  // 16 KiB
-constexpr uint32_t kSmemBudget = 225 * 1024;
+// dynamic shared memory opt-in; with the kernel's ~3.3 KB of static shared
+// memory the CTA stays under the 227 KB per-block limit
+constexpr uint32_t kSmemBudget = 223 * 1024;
 constexpr int kGatherThreads = 128;  // warps 10-13
 constexpr int kGatherDepth = 2;      // cp.async groups in flight per gather thread
-constexpr int kStageRowElems = 64;   // epilogue staging row: up to 2 x 32 features (bf16)
+constexpr int kStageRowElems = 32;   // epilogue staging row: 32 features (bf16)
 constexpr uint32_t kEpiStageBytes = kEpiWarps * 16u * kStageRowElems * 2u;  // per warp 16 rows
 constexpr int kTileQ = 4;            // depth of the tile-id queue
 
@@ -71,9 +73,7 @@ struct GemmParams {
   int a_second_off;
   int f_rows;
   int f_tiles;
-  int n_tok_tiles;
-  int n_tiles;
-  int tile_n;
+  int E;
   int bm;
   int out_ld;
   int stages;
@@ -95,18 +95,51 @@ struct Tile {
   int e, f, rows, n_eff, slot0;
 };
 
-// Decodes tile index t (slot tile fastest, then feature tile, then expert);
-// false when the tile holds no kept slot.
-__device__ __forceinline__ bool tile_at(const GemmParams& p, int t, Tile& T) {
-  const int jt = t % p.n_tok_tiles;
-  t /= p.n_tok_tiles;
-  T.f = t % p.f_tiles;
-  T.e = t / p.f_tiles;
-  T.rows = min(p.tile_n, p.kept_counts[T.e] - jt * p.tile_n);
-  if (T.rows <= 0) return false;
+// Dense tile list: expert e owns tiles [tpre[e], tpre[e+1]); each of its
+// ntt = ceil(kept/256) slot tiles holds ttn[e] slots (kept split evenly,
+// rounded up to 16), times f_tiles feature tiles. Built once per CTA.
+__device__ __forceinline__ void build_tile_list(const GemmParams& p, int32_t* tpre, int32_t* ttn,
+                                                int lane) {
+  int run = 0;
+  for (int e0 = 0; e0 < p.E; e0 += 32) {
+    const int e = e0 + lane;
+    int tiles = 0;
+    if (e < p.E) {
+      const int kept = max(p.kept_counts[e], 0);
+      const int ntt = (kept + kMaxTileN - 1) / kMaxTileN;
+      ttn[e] = ntt ? ((kept + ntt - 1) / ntt + 15) & ~15 : 0;
+      tiles = ntt * p.f_tiles;
+    }
+    int incl = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (e < p.E) tpre[e] = run + incl - tiles;
+    run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+  if (lane == 0) tpre[p.E] = run;
+}
+
+// Decodes tile index t (slot tile fastest, then feature tile, within expert).
+__device__ __forceinline__ void tile_at(const GemmParams& p, const int32_t* tpre,
+                                        const int32_t* ttn, int t, Tile& T) {
+  int lo = 0, hi = p.E - 1;  // last e with tpre[e] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tpre[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  T.e = lo;
+  const int local = t - tpre[lo];
+  const int tn = ttn[lo];
+  const int kept = p.kept_counts[lo];
+  const int ntt = (kept + kMaxTileN - 1) / kMaxTileN;
+  const int jt = local % ntt;
+  T.f = local / ntt;
+  T.rows = min(tn, kept - jt * tn);
   T.n_eff = (T.rows + 15) & ~15;
-  T.slot0 = p.block_start[T.e] * p.bm + jt * p.tile_n;
-  return true;
+  T.slot0 = p.block_start[lo] * p.bm + jt * tn;
 }
 
 __device__ __forceinline__ uint32_t bf16_bits(float v) {
@@ -128,6 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ int32_t rows_s[kMaxTileN];
   __shared__ volatile int gather_abort;  // set by a gatherer whose wait ran out
+  __shared__ int32_t tpre[kMaxExperts + 1];
+  __shared__ int32_t ttn[kMaxExperts];
   __shared__ int32_t tile_q[kTileQ];
   __shared__ __align__(8) uint64_t tq_full[kTileQ];
   __shared__ __align__(8) uint64_t tq_empty[kTileQ];
@@ -154,8 +189,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!p.fc1) tma_prefetch_desc(&tmB);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+  if (warp == 0) build_tile_list(p, tpre, ttn, lane);
   tc_fence_before();
   __syncthreads();
+  const int n_tiles = tpre[p.E];
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
@@ -181,11 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t qi = 0;; ++qi) {
       int t = -1;
       if (lane == 0) {
-        Tile T0;
-        do {
-          t = atomicAdd(&p.sched[0], 1);
-        } while (t < p.n_tiles && !tile_at(p, t, T0));
-        if (t >= p.n_tiles) t = -1;
+        t = atomicAdd(&p.sched[0], 1);
+        if (t >= n_tiles) t = -1;
         const int slot = (int)(qi % kTileQ);
         if (qi >= (uint32_t)kTileQ &&
             !mbar_wait(smem_u32(&tq_empty[slot]), ((qi / kTileQ) - 1u) & 1u, p.err, kErrWaitEmpty))
@@ -196,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       t = __shfl_sync(0xFFFFFFFFu, t, 0);
       if (t < 0) break;
       Tile T;
-      tile_at(p, t, T);
+      tile_at(p, tpre, ttn, t, T);
       const int a_row0 = T.e * p.a_rows_per_expert + T.f * p.f_rows;
       const uint32_t tx =
           (uint32_t)p.n_acc * kATileBytes + (p.fc1 ? 0u : (uint32_t)T.n_eff * 128u);
@@ -253,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++qi;
         if (t < 0) break;
         Tile T;
-        tile_at(p, t, T);
+        tile_at(p, tpre, ttn, t, T);
         if (tc > 0 &&
             !mbar_wait(smem_u32(&tmem_empty_bar), (tc - 1) & 1u, p.err, kErrWaitAccum)) {
           ok = false;
@@ -296,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = pop_tile(qi, kErrWaitAccum);
       if (t < 0) break;
       Tile T;
-      tile_at(p, t, T);
+      tile_at(p, tpre, ttn, t, T);
       // lane 0 waits for the whole warp, so the warp-collective TMEM loads
       // below are reached by all lanes or by none
       int w = 1;
@@ -304,46 +338,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++tc;
       if (!__shfl_sync(0xFFFFFFFFu, w, 0)) break;
       tc_fence_after();
-      const int nseg = p.fc1 ? 1 : p.n_acc;  // 32-feature segments per staged row
       const int feat0 = p.fc1 ? T.f * kTileM + q * 32 : T.f * p.f_rows + q * 32;
       for (int c0 = half * 16; c0 < T.n_eff; c0 += 32) {
         uint32_t v0[16], v1[16];
         tmem_ld16(tl + (uint32_t)c0, v0);
         if (p.n_acc == 2) tmem_ld16(tl + 256u + (uint32_t)c0, v1);
         tmem_ld_wait();
-        // lane = feature; stage [16 slots][32 or 64 features] as bf16
+        // lane = feature; stage [16 slots][32 features] as bf16 and write the
+        // rows with 16-byte stores; FC2's second accumulator follows the first
+        for (int seg = 0; seg < (p.fc1 ? 1 : p.n_acc); ++seg) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float a;
-          if (p.fc1) {
-            const float g = __uint_as_float(v0[i]);
-            a = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[i]);
-          } else {
-            a = __uint_as_float(v0[i]);
-          }
-          const uint32_t at = stg_u + (uint32_t)(i * kStageRowElems + lane) * 2u;
-          asm volatile("st.shared.b16 [%0], %1;" ::"r"(at), "h"((unsigned short)bf16_bits(a)) : "memory");
-          if (!p.fc1 && p.n_acc == 2)
-            asm volatile("st.shared.b16 [%0], %1;" ::"r"(at + 64u),
-                         "h"((unsigned short)bf16_bits(__uint_as_float(v1[i])))
+          for (int i = 0; i < 16; ++i) {
+            float a;
+            if (p.fc1) {
+              const float g = __uint_as_float(v0[i]);
+              a = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[i]);
+            } else {
+              a = __uint_as_float(seg == 0 ? v0[i] : v1[i]);
+            }
+            const uint32_t at = stg_u + (uint32_t)(i * kStageRowElems + lane) * 2u;
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(at), "h"((unsigned short)bf16_bits(a))
                          : "memory");
+          }
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 2; ++it) {  // 16 rows x 4 chunks of 16 bytes
+            const int ch = lane + it * 32;
+            const int row = ch >> 2, part = ch & 3;
+            uint4 val;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                         : "r"(stg_u + (uint32_t)(row * kStageRowElems + part * 8) * 2u)
+                         : "memory");
+            uint16_t* dst = p.out + (size_t)(T.slot0 + c0 + row) * p.out_ld + feat0 +
+                            seg * kTileM + part * 8;
+            *reinterpret_cast<uint4*>(dst) = val;
+          }
+          __syncwarp();
         }
-        __syncwarp();
-        // 16 rows x nseg segments of 64 bytes, 4 x 16-byte chunks each
-        const int chunks = 16 * nseg * 4;
-        for (int ch = lane; ch < chunks; ch += 32) {
-          const int row = ch / (nseg * 4), rem = ch % (nseg * 4);
-          const int seg = rem / 4, part = rem % 4;
-          uint4 val;
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                       : "r"(stg_u + (uint32_t)(row * kStageRowElems + seg * 32 + part * 8) * 2u)
-                       : "memory");
-          uint16_t* dst =
-              p.out + (size_t)(T.slot0 + c0 + row) * p.out_ld + feat0 + seg * kTileM + part * 8;
-          *reinterpret_cast<uint4*>(dst) = val;
-        }
-        __syncwarp();
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar));
@@ -365,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = pop_tile(qi, kErrWaitFull);
       if (t < 0) break;
       Tile T;
-      tile_at(p, t, T);
+      tile_at(p, tpre, ttn, t, T);
       named_bar_sync(1, kGatherThreads);  // the previous tile's rows_s is no longer read
       if (gather_abort) break;
       for (int i = gt; i < T.n_eff; i += kGatherThreads)
@@ -451,8 +483,10 @@ int device_sms(cudaError_t* err) {
   if ((*err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return 0;
   if ((*err = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kSmemBudget)) != cudaSuccess)
+                                   (int)kSmemBudget)) != cudaSuccess) {
+    cudaGetLastError();  // reported here; do not leave it for a later launch to report
     return 0;
+  }
   if (dev >= 0 && dev < 64) sms[dev] = n;
   return n;
 }
@@ -460,7 +494,7 @@ int device_sms(cudaError_t* err) {
 }  // namespace
 
 int launch_gemm(const GemmArgs& a, cudaStream_t s) {
-  if (a.cpad <= 0 || a.N <= 0) return 0;
+  if (a.max_rows <= 0 || a.N <= 0) return 0;
   GemmParams p{};
   p.fc1 = a.fc1;
   p.bm = a.bm;
@@ -472,7 +506,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   p.act = static_cast<const uint16_t*>(a.act);
   p.act_ld = a.fc1 ? a.H : a.I;
   p.act_rows = a.fc1 ? a.N : 0;
-  const int64_t S = (int64_t)a.E * a.cpad;
+  const int64_t S = a.s_max;
   CUtensorMap tmA, tmB;
   if (a.fc1) {
     p.n_acc = 2;
@@ -495,12 +529,14 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
     if (!make_map(&tmA, a.w, (uint64_t)a.I, (uint64_t)a.E * a.H, kBK, kTileM)) return -1;
     if (!make_map(&tmB, a.act, (uint64_t)a.I, (uint64_t)S, kBK, 16)) return -1;
   }
-  p.n_tok_tiles = (int)((a.cpad + kMaxTileN - 1) / kMaxTileN);
-  const int64_t per = (a.cpad + p.n_tok_tiles - 1) / p.n_tok_tiles;
-  p.tile_n = (int)((per + 15) / 16 * 16);
-  p.n_tiles = a.E * p.f_tiles * p.n_tok_tiles;
+  p.E = a.E;
+  // stage size for the largest slot tile any expert can have
+  const int64_t rows_cap = a.max_rows < kMaxTileN ? a.max_rows : kMaxTileN;
+  const int tile_cap = (int)((rows_cap + 15) / 16 * 16);
+  const int64_t grid_bound =
+      (int64_t)p.f_tiles * ((a.max_total + kMaxTileN - 1) / kMaxTileN + a.E);
   p.b_off = (uint32_t)p.n_acc * kATileBytes;
-  p.stage_bytes = p.b_off + (((uint32_t)p.tile_n * 128u + 1023u) & ~1023u);
+  p.stage_bytes = p.b_off + (((uint32_t)tile_cap * 128u + 1023u) & ~1023u);
   p.stages = (int)((kSmemBudget - 1024u - kEpiStageBytes) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2) return -1;
@@ -509,7 +545,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   cudaError_t err = cudaSuccess;
   const int sms = device_sms(&err);
   if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
-  const int grid = p.n_tiles < sms ? p.n_tiles : sms;
+  const int grid = (int)(grid_bound < sms ? grid_bound : sms);
   p.sched = a.sched;
   moe_gemm_kernel<<<grid, kThreads, dyn, s>>>(tmA, tmB, p);
   err = cudaGetLastError();

@@ -42,23 +42,60 @@ int check_cfg(const moe_config_t* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->block_m != 16 && c->block_m != 32 && c->block_m != 64 && c->block_m != 128)
     return MOE_ERR_INVALID_ARG;
-  if (c->cap_num == 0) return MOE_ERR_UNSUPPORTED_SHAPE;  // dropless mode: not in this build
+  if (c->cap_num == 0) {  // dropless: the ladder must be well formed
+    if (c->ladder_len < 0 || c->ladder_len > moe::kMaxLadder) return MOE_ERR_INVALID_ARG;
+    if (c->ladder_len > 0) {
+      if (!c->ladder_num || c->ladder_den <= 0) return MOE_ERR_INVALID_ARG;
+      for (int j = 0; j < c->ladder_len; ++j)
+        if (c->ladder_num[j] <= 0 || (j > 0 && c->ladder_num[j] <= c->ladder_num[j - 1]))
+          return MOE_ERR_INVALID_ARG;
+    }
+  }
   if (c->hidden % 128 != 0 || c->inter % 128 != 0 || c->n_experts > moe::kMaxExperts ||
       c->top_k > moe::kMaxTopK || c->n_tokens > moe::kMaxTokens)
     return MOE_ERR_UNSUPPORTED_SHAPE;
-  const int64_t cap = ((int64_t)c->n_tokens * c->top_k * c->cap_num + (int64_t)c->n_experts * c->cap_den - 1) /
-                      ((int64_t)c->n_experts * c->cap_den);
-  const int64_t S = (int64_t)c->n_experts * roundup(cap, c->block_m);
+  int64_t S = 0;
+  if (c->cap_num == 0) {
+    const int64_t R = (int64_t)c->n_tokens * c->top_k;
+    int64_t top = 0;
+    if (c->ladder_len > 0) {
+      const int64_t num = (int64_t)c->ladder_num[c->ladder_len - 1] * R;
+      const int64_t den = (int64_t)c->ladder_den * c->n_experts;
+      top = roundup((num + den - 1) / den, c->block_m);
+    }
+    S = roundup(R + (int64_t)c->n_experts * (top + c->block_m), c->block_m);
+  } else {
+    const int64_t cap =
+        ((int64_t)c->n_tokens * c->top_k * c->cap_num + (int64_t)c->n_experts * c->cap_den - 1) /
+        ((int64_t)c->n_experts * c->cap_den);
+    S = (int64_t)c->n_experts * roundup(cap, c->block_m);
+  }
   if (S > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
 
+bool dropless_of(const moe_config_t* c) { return c->cap_num == 0; }
+
 int64_t cap_of(const moe_config_t* c) {
+  if (dropless_of(c)) return c->n_tokens;
   return ((int64_t)c->n_tokens * c->top_k * c->cap_num + (int64_t)c->n_experts * c->cap_den - 1) /
          ((int64_t)c->n_experts * c->cap_den);
 }
 
 int64_t cpad_of(const moe_config_t* c) { return roundup(cap_of(c), c->block_m); }
+
+// Slot rows of the route list and of the slot-space buffers.
+int64_t slots_of(const moe_config_t* c) {
+  if (!dropless_of(c)) return (int64_t)c->n_experts * cpad_of(c);
+  const int64_t R = (int64_t)c->n_tokens * c->top_k;
+  int64_t top = 0;
+  if (c->ladder_len > 0) {
+    const int64_t num = (int64_t)c->ladder_num[c->ladder_len - 1] * R;
+    const int64_t den = (int64_t)c->ladder_den * c->n_experts;
+    top = roundup((num + den - 1) / den, c->block_m);
+  }
+  return roundup(R + (int64_t)c->n_experts * (top + c->block_m), c->block_m);
+}
 
 struct WsLayout {
   size_t logits, chunk_counts, chunk_lofs, chunk_routes, chunk_keys, total;
@@ -106,12 +143,12 @@ int64_t moe_capacity(const moe_config_t* cfg) {
 
 int64_t moe_max_slots(const moe_config_t* cfg) {
   const int rc = check_cfg(cfg);
-  return rc != MOE_OK ? rc : (int64_t)cfg->n_experts * cpad_of(cfg);
+  return rc != MOE_OK ? rc : slots_of(cfg);
 }
 
 int64_t moe_max_blocks(const moe_config_t* cfg) {
   const int rc = check_cfg(cfg);
-  return rc != MOE_OK ? rc : (int64_t)cfg->n_experts * cpad_of(cfg) / cfg->block_m;
+  return rc != MOE_OK ? rc : slots_of(cfg) / cfg->block_m;
 }
 
 int64_t moe_route_workspace_bytes(const moe_config_t* cfg) {
@@ -139,6 +176,11 @@ int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_route
   a.bm = cfg->block_m;
   a.cap = cap_of(cfg);
   a.cpad = cpad_of(cfg);
+  a.dropless = dropless_of(cfg);
+  a.ladder.len = a.dropless ? cfg->ladder_len : 0;
+  a.ladder.den = cfg->ladder_den > 0 ? cfg->ladder_den : 1;
+  for (int j = 0; j < a.ladder.len; ++j) a.ladder.num[j] = cfg->ladder_num[j];
+  a.s_max = slots_of(cfg);
   a.x = static_cast<const uint16_t*>(x);
   a.wr = w_router;
   a.bias = bias;
@@ -180,11 +222,14 @@ static int gemm_common(const moe_config_t* cfg, const moe_routes_t* routes, cons
   a.E = cfg->n_experts;
   a.I = cfg->inter;
   a.bm = cfg->block_m;
-  a.cpad = cpad_of(cfg);
+  a.max_rows = dropless_of(cfg) ? cfg->n_tokens : cap_of(cfg);
+  if (a.max_rows > cfg->n_tokens) a.max_rows = cfg->n_tokens;
+  a.max_total = (int64_t)cfg->n_tokens * cfg->top_k;
+  a.s_max = slots_of(cfg);
   a.act = act;
   a.w = w;
   a.out = out;
-  a.act_rows = fc1 ? cfg->n_tokens : (int64_t)cfg->n_experts * a.cpad;
+  a.act_rows = fc1 ? cfg->n_tokens : a.s_max;
   a.sorted_slot_ids = routes->sorted_slot_ids;
   a.kept_counts = routes->kept_counts;
   a.block_start = routes->block_start;

@@ -19,9 +19,19 @@ struct RouteWs {
   uint32_t* chunk_keys;   // [N*K] the renormalised probability bits of those routes
 };
 
+constexpr int kMaxLadder = 16;
+
+struct Ladder {  // dropless padding rungs: multiples num[j]/den of the expected rows
+  int len, den;
+  int num[kMaxLadder];
+};
+
 struct RouteArgs {
   int N, H, E, K, renorm, bm;
-  int64_t cap, cpad;
+  int64_t cap, cpad;     // capacity mode
+  int dropless;          // 1: keep every route, extents from the ladder
+  Ladder ladder;
+  int64_t s_max;         // slots the caller allocated (static bound)
   const uint16_t* x;
   const float* wr;
   const float* bias;
@@ -45,7 +55,9 @@ int launch_route(const RouteArgs& a, cudaStream_t s);
 struct GemmArgs {
   int fc1;               // 1: FC1 gather + SwiGLU epilogue; 0: FC2 plain epilogue
   int N, H, E, I, bm;
-  int64_t cpad;
+  int64_t max_rows;      // upper bound of kept routes per expert
+  int64_t max_total;     // upper bound of kept routes over all experts
+  int64_t s_max;         // rows of the slot-space buffers (h, o)
   const void* act;       // FC1: x [N,H]; FC2: h [S,I]
   const void* w;         // FC1: w13 [E,2I,H]; FC2: w2 [E,H,I]
   void* out;             // FC1: h [S,I]; FC2: o [S,H]

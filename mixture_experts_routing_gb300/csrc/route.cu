@@ -347,7 +347,8 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     const int32_t* __restrict__ chunk_counts, const int32_t* __restrict__ chunk_lofs,
     const int32_t* __restrict__ chunk_routes, const uint32_t* __restrict__ chunk_keys, int N,
     int E, int K,
-    int cap, int cpad, int bm, uint8_t* __restrict__ keep, int32_t* __restrict__ expert_counts,
+    int cap, int cpad, int bm, int dropless, Ladder ladder, int s_max,
+    uint8_t* __restrict__ keep, int32_t* __restrict__ expert_counts,
     int32_t* __restrict__ kept_counts, int32_t* __restrict__ sorted_slot_ids,
     int32_t* __restrict__ expert_ids, int32_t* __restrict__ block_start,
     int32_t* __restrict__ ntpp, int32_t* __restrict__ token_routes,
@@ -360,6 +361,9 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
   __shared__ uint32_t s_prefix;
   __shared__ int32_t s_remaining;
   __shared__ int32_t s_total;
+  __shared__ int32_t s_base;      // first slot of this expert
+  __shared__ int32_t s_extent;    // slots of this expert
+  __shared__ int32_t s_all;       // dropless: total padded extent
   const int e = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = (N + kTokensPerChunk - 1) / kTokensPerChunk;
@@ -373,6 +377,35 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
   if (C == 0 && tid == 0) s_total = 0;
   __syncthreads();
   const int n = min(s_total, N);
+  int base = e * cpad, extent = cpad;  // capacity mode: fixed regions
+  if (dropless) {
+    // every expert's count (column sums of the chunk table), its extent from
+    // the ladder, and the exclusive scan of the extents up to this expert
+    __syncthreads();
+    const long long R = (long long)N * K;
+    int ext = 0;
+    if (tid < E) {
+      int cnt_e = 0;
+      for (int c2 = 0; c2 < C; ++c2) cnt_e += chunk_counts[(size_t)c2 * E + tid];
+      ext = -1;
+      for (int j = 0; j < ladder.len && ext < 0; ++j) {
+        const long long num = (long long)ladder.num[j] * R, den = (long long)ladder.den * E;
+        long long rung = (num + den - 1) / den;
+        rung = (rung + bm - 1) / bm * bm;
+        if (cnt_e <= rung) ext = (int)rung;
+      }
+      if (ext < 0) ext = (cnt_e + bm - 1) / bm * bm;
+    }
+    const int before = block_exclusive_scan(ext, warp_tot);
+    if (tid == e) {
+      s_base = before;
+      s_extent = ext;
+    }
+    if (tid == E - 1) s_all = before + ext;
+    __syncthreads();
+    base = s_base;
+    extent = s_extent;
+  }
   for (int cc = warp; cc < C; cc += kSelThreads / 32) {
     const int lo = min(max(chunk_lofs[(size_t)cc * E + e], 0), kTokensPerChunk * K);
     const int64_t chunk_base = (int64_t)cc * kTokensPerChunk * K;
@@ -463,7 +496,6 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
   int pos = block_exclusive_scan(kept_local, warp_tot);
   // second pass: same keep decisions, now writing the layout
   tie_rank = tie_base;
-  const int base = e * cpad;
   for (int i = i0; i < i1; ++i) {
     bool kp = true;
     if (select) {
@@ -484,18 +516,24 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     }
   }
   const int kept_e = select ? cap : n;
-  for (int sl = kept_e + tid; sl < cpad; sl += kSelThreads) sorted_slot_ids[base + sl] = N;
-  const int nb = cpad / bm;
+  for (int sl = kept_e + tid; sl < extent; sl += kSelThreads) sorted_slot_ids[base + sl] = N;
+  const int nb = extent / bm;
   for (int b = tid; b < nb; b += kSelThreads)
-    expert_ids[(size_t)e * nb + b] = (b * bm < kept_e) ? e : -1;
+    expert_ids[(size_t)base / bm + b] = (b * bm < kept_e) ? e : -1;
+  if (dropless && e == E - 1) {
+    // slots past the padded total up to the allocated bound: sentinel / -1
+    for (int sl = s_all + tid; sl < s_max; sl += kSelThreads) sorted_slot_ids[sl] = N;
+    for (int b = s_all / bm + tid; b < s_max / bm; b += kSelThreads) expert_ids[b] = -1;
+  }
   if (tid == 0) {
-    block_start[e] = e * nb;
+    block_start[e] = base / bm;
     expert_counts[e] = n;
     kept_counts[e] = kept_e;
     if (e == 0) {
-      *ntpp = E * cpad;
+      if (!dropless) *ntpp = E * cpad;
       for (int i = 0; i < 4; ++i) gemm_sched[i] = 0;
     }
+    if (dropless && e == E - 1) *ntpp = s_all;
   }
 }
 
@@ -533,7 +571,8 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   const int cap = (int)(a.cap < a.N ? a.cap : a.N);
   route_select_kernel<<<a.E, kSelThreads, dyn, s>>>(
       a.ws.chunk_counts, a.ws.chunk_lofs, a.ws.chunk_routes, a.ws.chunk_keys, a.N, a.E, a.K, cap,
-      (int)a.cpad, a.bm, a.keep, a.expert_counts, a.kept_counts, a.sorted_slot_ids, a.expert_ids,
+      (int)a.cpad, a.bm, a.dropless, a.ladder, (int)a.s_max, a.keep, a.expert_counts,
+      a.kept_counts, a.sorted_slot_ids, a.expert_ids,
       a.block_start, a.ntpp, a.token_routes, a.gemm_sched);
   ++launched;
   err = cudaGetLastError();

@@ -228,6 +228,8 @@ class Workload:
     seed: int = 0
     note: str = ""
     sweep: tuple = field(default=())
+    ladder: tuple = field(default=())   # dropless: rung multipliers (numerators)
+    ladder_den: int = 1
 
     def with_tokens(self, n: int) -> "Workload":
         d = dict(self.__dict__)
@@ -250,7 +252,8 @@ WORKLOADS = {
                          note="DeepSeek-V3 shapes with 16 experts, N=256 (ncu profiling case)"),
     "dropless": Workload("dropless", 16384, 4096, 64, 6, 1408, 0, 1, zipf_s=0.8,
                          note="dropless bucketed layer: H=4096, E=64, top-6, I=1408, N swept 128..16384, Zipf(0.8)",
-                         sweep=tuple(2 ** k for k in range(7, 15))),
+                         sweep=tuple(2 ** k for k in range(7, 15)),
+                         ladder=(2, 3, 4, 5, 6, 8), ladder_den=4),
 }
 
 

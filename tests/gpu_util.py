@@ -58,7 +58,8 @@ class Problem:
                  with_ffn: bool = True):
         self.w, self.bm, self.dev = w, bm, torch.device(dev)
         N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
-        self.cfg = moe.Config(N, H, E, K, I, w.cap_num, w.cap_den, block_m=bm, renorm=renorm)
+        self.cfg = moe.Config(N, H, E, K, I, w.cap_num, w.cap_den, block_m=bm, renorm=renorm,
+                              ladder=list(w.ladder), ladder_den=w.ladder_den)
         self.x_bits = (x_bits if x_bits is not None
                        else synth.normal_bf16_bits(w.seed, synth.STREAM["x"], 0, N * H, w.x_std).reshape(N, H))
         self.wr = synth.normal_f32(w.seed, synth.STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E)
@@ -120,6 +121,8 @@ class Problem:
 
     def oracle_routing(self) -> oracle.Routing:
         w = self.w
+        if w.cap_num == 0:
+            return dropless_routing(self)
         return oracle.route(self.x_bits, self.wr, self.bias, w.n_experts, w.top_k, w.cap_num,
                             w.cap_den, self.bm, renorm=bool(self.cfg.renorm))
 
@@ -131,10 +134,22 @@ class Problem:
         return out
 
 
+def dropless_routing(P: "Problem") -> oracle.Routing:
+    """Router plus the dropless, bucketed layout, in the shape of oracle.Layout
+    (slot arrays over the whole allocated bound)."""
+    w = P.w
+    ids, p, _, _ = oracle.router(P.x_bits, P.wr, P.bias, w.top_k, renorm=bool(P.cfg.renorm))
+    D = oracle.dropless_layout(ids, w.n_experts, P.bm, list(w.ladder), w.ladder_den)
+    keep = np.ones(ids.shape, np.uint8)
+    L = oracle.Layout(w.n_tokens, 0, keep, D.expert_counts, D.expert_counts, D.sorted_slot_ids,
+                      D.expert_ids, D.block_start, D.num_tokens_post_padded, D.token_routes)
+    return oracle.Routing(ids, p, L)
+
+
 def assert_routing_equal(P: Problem, R: oracle.Routing) -> None:
     g = P.routes_np()
     L = R.layout
-    S = L.num_tokens_post_padded
+    S = len(L.sorted_slot_ids)
     assert np.array_equal(g["topk_ids"], R.topk_ids), "topk_ids"
     assert np.array_equal(g["topk_p"].view(np.int32), R.topk_p.view(np.int32)), "topk_p bits"
     assert np.array_equal(g["keep"], L.keep), "keep"
@@ -143,7 +158,7 @@ def assert_routing_equal(P: Problem, R: oracle.Routing) -> None:
     assert np.array_equal(g["sorted_slot_ids"][:S], L.sorted_slot_ids), "sorted_slot_ids"
     assert np.array_equal(g["expert_ids"][:len(L.expert_ids)], L.expert_ids), "expert_ids"
     assert np.array_equal(g["block_start"], L.block_start), "block_start"
-    assert int(g["num_tokens_post_padded"][0]) == S, "num_tokens_post_padded"
+    assert int(g["num_tokens_post_padded"][0]) == L.num_tokens_post_padded, "num_tokens_post_padded"
     assert np.array_equal(g["token_routes"], L.token_routes), "token_routes"
 
 
@@ -156,7 +171,7 @@ def check_expert_slots(P: Problem, R: oracle.Routing, experts) -> None:
     h = P.h.float().cpu().numpy()
     o = P.o.float().cpu().numpy()
     for e in experts:
-        base, kept = e * L.cpad, int(L.kept_counts[e])
+        base, kept = int(L.block_start[e]) * P.bm, int(L.kept_counts[e])
         if kept == 0:
             continue
         toks = L.sorted_slot_ids[base:base + kept]

@@ -67,8 +67,7 @@ def test_invalid_configs_fail_closed(L):
     for k, v in bad_fields:
         c = moe.Config(**dict(good, **{k: v}))
         assert L.moe_max_slots(ctypes.byref(c)) == -1, (k, v)
-    unsupported = [("hidden", 192), ("inter", 64), ("n_experts", 300), ("n_tokens", 10 ** 6),
-                   ("cap_num", 0)]
+    unsupported = [("hidden", 192), ("inter", 64), ("n_experts", 300), ("n_tokens", 10 ** 6)]
     for k, v in unsupported:
         c = moe.Config(**dict(good, **{k: v}, top_k=2))
         assert L.moe_max_slots(ctypes.byref(c)) == -2, (k, v)
@@ -109,3 +108,24 @@ def test_status_strings(L):
     assert moe.status_string(0) == "ok"
     assert "unsupported" in moe.status_string(-2)
     assert moe.status_string(12345) == "unknown status"
+
+
+@pytest.mark.parametrize("N", [128, 1000, 16384])
+def test_dropless_sizes_match_oracle_bound(L, N):
+    ladder = [2, 3, 4, 5, 6, 8]  # 0.5x .. 2x of the expected rows per expert
+    cfg = moe.Config(N, 4096, 64, 6, 1408, 0, 1, block_m=32, ladder=ladder, ladder_den=4)
+    assert moe.capacity(cfg) == N
+    want = oracle.dropless_s_max(N, 6, 64, 32, ladder, 4)
+    assert moe.max_slots(cfg) == -(-want // 32) * 32
+    assert moe.max_blocks(cfg) * 32 == moe.max_slots(cfg)
+
+
+def test_dropless_ladder_validation(L):
+    base = dict(n_tokens=64, hidden=128, n_experts=8, top_k=2, inter=128, cap_num=0, cap_den=1)
+    ok = moe.Config(**base, ladder=[1, 2, 4], ladder_den=2)
+    assert L.moe_max_slots(ctypes.byref(ok)) > 0
+    for lad, den in (([4, 2], 2), ([0, 1], 2), ([1, 2], 0), (list(range(1, 18)), 1)):
+        c = moe.Config(**base, ladder=lad, ladder_den=den)
+        assert L.moe_max_slots(ctypes.byref(c)) == -1, (lad, den)
+    no_ladder = moe.Config(**base)
+    assert moe.max_slots(no_ladder) == 64 * 2 + 8 * 32
