@@ -174,6 +174,17 @@ int moe_fc2_forward(const moe_config_t* cfg, const moe_routes_t* routes, const v
 int moe_ffn_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
                     const void* w13, const void* w2, void* h, void* o, cudaStream_t stream);
 
+/* Training forward: moe_ffn_forward that also saves FC1's pre-activations for
+ * moe_ffn_backward ("Permute-Free Grouped GEMM for MoE (bf16, gfx950)",
+ * section 5: the FC1 kernel optionally writes the 2F pre-activation).
+ *  preact [S,2I] bf16 output: columns [0,I) hold g = x_s W_gate[e], columns
+ *         [I,2I) hold u = x_s W_up[e] (fp32 accumulation rounded to bf16); same
+ *         written-row rule as h. Required (non-NULL) when N > 0.
+ * Other arguments and outputs as moe_ffn_forward. */
+int moe_ffn_forward_train(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                          const void* w13, const void* w2, void* h, void* o, void* preact,
+                          cudaStream_t stream);
+
 /* Contention-free gather-combine ([PF] section 2 and 5 "route_gather_combine").
  *  o  [S,H] bf16 expert outputs;  y [N,H] bf16 output:
  *  y[t,:] = sum over k with token_routes[t,k] >= 0 of topk_p[t,k]*o[token_routes[t,k],:]
@@ -188,6 +199,35 @@ int moe_combine(const moe_config_t* cfg, const moe_routes_t* routes, const void*
 int moe_pack_w13(const moe_config_t* cfg, const void* w_gate, const void* w_up, void* w13,
                  cudaStream_t stream);
 int moe_pack_w2(const moe_config_t* cfg, const void* w_down, void* w2, cudaStream_t stream);
+
+/* Bytes of scratch moe_ffn_backward needs: about S*(2 + 6I + 2H) bytes plus
+ * S*I/8 for the dprob partials (S = moe_max_slots). */
+int64_t moe_backward_workspace_bytes(const moe_config_t* cfg);
+
+/* Backward of the expert path y = sum_k p'_k FFN_e(x) for a given dY
+ * ("Permute-Free Grouped GEMM for MoE (bf16, gfx950)", section 3 End-to-end
+ * flow, backward, and section 5 Kernels: FC2 dgrad with the SwiGLU backward
+ * in its epilogue, FC1 dgrad, FC1's input gradient reduced by the
+ * gather-combine, weight gradients contracted over the token slots). Works in
+ * both layouts; dropped routes contribute nothing.
+ *  x, w13, w2  as in the forward;  preact [S,2I] bf16 from moe_ffn_forward_train
+ *  dy     [N,H] bf16 gradient of y
+ *  dx     [N,H] bf16 output: the gradient of y with respect to x through the
+ *         experts, dX[t] = sum over kept k of (dg W_gate[e]^T + du W_up[e]^T)
+ *         (the router's path is not included)
+ *  dw13   [E,2I,H] f32 output, the gradient of the packed w13 (rows [0,I):
+ *         dW_gate[e]^T, rows [I,2I): dW_up[e]^T); zero for an expert with no
+ *         kept route
+ *  dw2    [E,H,I] f32 output, the gradient of the packed w2 (dW_down[e]^T)
+ *  dprob  [N,K] f32 output: dL/dp'[t,k] = <silu(g) u, dY[t] W_down[e]^T> for a
+ *         kept route, 0 for a dropped one
+ *  workspace/ws_bytes  device scratch of at least moe_backward_workspace_bytes
+ * fp32 accumulation everywhere; dPre = [dg | du], p' a and the per-route input
+ * gradients are bf16 intermediates in the workspace. Outputs are overwritten. */
+int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                     const void* w13, const void* w2, const void* preact, const void* dy,
+                     void* dx, float* dw13, float* dw2, float* dprob, void* workspace,
+                     size_t ws_bytes, cudaStream_t stream);
 
 /* Size of the library's built-in route scratch used by moe_route_align_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)

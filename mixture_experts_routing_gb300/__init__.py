@@ -28,6 +28,7 @@ __all__ = [
     "alloc_buffers", "capacity", "max_slots", "max_blocks", "route_workspace_bytes",
     "route_align", "fc1_forward", "fc2_forward", "ffn_forward", "combine", "pack_w13",
     "pack_w2", "status_string", "launch_count", "device_error", "forward",
+    "ffn_forward_train", "backward_workspace_bytes", "alloc_backward_workspace", "ffn_backward",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -93,7 +94,8 @@ def lib():
         P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
         CP = ctypes.POINTER(Config)
         RP = ctypes.POINTER(_RoutesC)
-        for name in ("moe_capacity", "moe_max_slots", "moe_max_blocks", "moe_route_workspace_bytes"):
+        for name in ("moe_capacity", "moe_max_slots", "moe_max_blocks", "moe_route_workspace_bytes",
+                     "moe_backward_workspace_bytes"):
             getattr(L, name).argtypes = [CP]
             getattr(L, name).restype = I64
         L.moe_route_align.argtypes = [CP, P, P, P, RP, P, SZ, P]
@@ -101,10 +103,13 @@ def lib():
         L.moe_fc2_forward.argtypes = [CP, RP, P, P, P, P]
         L.moe_ffn_forward.argtypes = [CP, RP, P, P, P, P, P, P]
         L.moe_combine.argtypes = [CP, RP, P, P, P]
+        L.moe_ffn_forward_train.argtypes = [CP, RP, P, P, P, P, P, P, P]
+        L.moe_ffn_backward.argtypes = [CP, RP, P, P, P, P, P, P, P, P, P, P, SZ, P]
         L.moe_pack_w13.argtypes = [CP, P, P, P, P]
         L.moe_pack_w2.argtypes = [CP, P, P, P]
         for name in ("moe_route_align", "moe_fc1_forward", "moe_fc2_forward", "moe_ffn_forward",
-                     "moe_combine", "moe_pack_w13", "moe_pack_w2"):
+                     "moe_combine", "moe_pack_w13", "moe_pack_w2", "moe_ffn_forward_train",
+                     "moe_ffn_backward"):
             getattr(L, name).restype = I32
         L.moe_status_string.argtypes = [I32]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -146,6 +151,10 @@ def max_blocks(cfg: Config) -> int:
 
 def route_workspace_bytes(cfg: Config) -> int:
     return _q("moe_route_workspace_bytes", cfg)
+
+
+def backward_workspace_bytes(cfg: Config) -> int:
+    return _q("moe_backward_workspace_bytes", cfg)
 
 
 def _ptr(t) -> Optional[int]:
@@ -207,6 +216,30 @@ def ffn_forward(cfg: Config, routes: Routes, x, w13, w2, h, o, stream=None) -> N
     _check("moe_ffn_forward", lib().moe_ffn_forward(ctypes.byref(cfg), ctypes.byref(routes.c()),
                                                     _ptr(x), _ptr(w13), _ptr(w2), _ptr(h), _ptr(o),
                                                     _stream(stream)))
+
+
+def ffn_forward_train(cfg: Config, routes: Routes, x, w13, w2, h, o, preact, stream=None) -> None:
+    """ffn_forward that also writes FC1's pre-activations preact [S,2I] (g | u)."""
+    _check("moe_ffn_forward_train",
+           lib().moe_ffn_forward_train(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(x),
+                                       _ptr(w13), _ptr(w2), _ptr(h), _ptr(o), _ptr(preact),
+                                       _stream(stream)))
+
+
+def alloc_backward_workspace(cfg: Config, device):
+    import torch
+    return torch.empty(max(backward_workspace_bytes(cfg), 256), dtype=torch.uint8, device=device)
+
+
+def ffn_backward(cfg: Config, routes: Routes, x, w13, w2, preact, dy, dx, dw13, dw2, dprob,
+                 workspace, stream=None) -> None:
+    """Expert-path backward: dx [N,H] bf16, dw13 [E,2I,H] f32, dw2 [E,H,I] f32,
+    dprob [N,K] f32 (outputs overwritten)."""
+    _check("moe_ffn_backward",
+           lib().moe_ffn_backward(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(x), _ptr(w13),
+                                  _ptr(w2), _ptr(preact), _ptr(dy), _ptr(dx), _ptr(dw13),
+                                  _ptr(dw2), _ptr(dprob), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def combine(cfg: Config, routes: Routes, o, y, stream=None) -> None:

@@ -67,6 +67,70 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   }
 }
 
+// Backward of the combine ("Permute-Free Grouped GEMM for MoE (bf16, gfx950)",
+// section 3: FC1's input gradient is reduced per token by the same
+// gather-combine): dX[t] = sum_k dXr[token_routes[t,k]] with unit weights, the
+// routing probability having been applied inside the FC2 dgrad. Threads
+// 0..K-1 also reduce dprob[t,k] from the slot's per-32-feature partials.
+template <int KMAX>
+__global__ void __launch_bounds__(kCombineThreads) combine_bwd_kernel(
+    const uint16_t* __restrict__ dxr, const float* __restrict__ part, int n_part,
+    const int32_t* __restrict__ token_routes, uint16_t* __restrict__ dx,
+    float* __restrict__ dprob, int N, int H, int K) {
+  const int t = blockIdx.x;
+  int slot[KMAX];
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) slot[k] = (k < K) ? token_routes[(size_t)t * K + k] : -1;
+  if (threadIdx.x < K) {
+    const int sl = token_routes[(size_t)t * K + threadIdx.x];
+    float acc = 0.0f;
+    if (sl >= 0)
+      for (int j = 0; j < n_part; ++j) acc += part[(size_t)sl * n_part + j];
+    dprob[(size_t)t * K + threadIdx.x] = acc;
+  }
+  const int nv = H / 8;
+  for (int v = threadIdx.x; v < nv; v += kCombineThreads) {
+    uint4 in[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (slot[k] >= 0) in[k] = __ldg(reinterpret_cast<const uint4*>(dxr + (size_t)slot[k] * H) + v);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (slot[k] < 0) continue;
+      float f[8];
+      bf16x8_to_f32(in[k], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+    }
+    uint4 out;
+    out.x = pack_bf16x2(acc[0], acc[1]);
+    out.y = pack_bf16x2(acc[2], acc[3]);
+    out.z = pack_bf16x2(acc[4], acc[5]);
+    out.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(dx + (size_t)t * H)[v] = out;
+  }
+}
+
+// slot_route[s]: the route t*K+k that slot s holds (token_routes[t,k] == s),
+// -1 for a padding slot. Block 0 also zeroes the backward GEMMs' counters.
+__global__ void slot_route_kernel(const int32_t* __restrict__ sorted_slot_ids,
+                                  const int32_t* __restrict__ token_routes, int N, int K,
+                                  int64_t s_max, int32_t* __restrict__ slot_route,
+                                  int32_t* __restrict__ sched_zero, int n_zero) {
+  if (blockIdx.x == 0 && (int)threadIdx.x < n_zero) sched_zero[threadIdx.x] = 0;
+  const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= s_max) return;
+  const int t = sorted_slot_ids[s];
+  int r = -1;
+  if (t >= 0 && t < N)
+    for (int k = 0; k < K; ++k)
+      if (token_routes[(size_t)t * K + k] == (int32_t)s) r = t * K + k;
+  slot_route[s] = r;
+}
+
 __global__ void transpose_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int R,
                                  int C, int64_t in_es, int64_t out_es, int64_t out_off) {
   __shared__ uint16_t tile[32][33];
@@ -97,6 +161,38 @@ int launch_combine(const CombineArgs& a, cudaStream_t s) {
     combine_kernel<8><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
   else
     combine_kernel<16><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? 1 : -(int)err;
+}
+
+int launch_combine_bwd(const uint16_t* dxr, const float* part, int n_part,
+                       const int32_t* token_routes, int N, int H, int K, uint16_t* dx,
+                       float* dprob, cudaStream_t s) {
+  if (N <= 0) return 0;
+#define MOE_COMBINE_BWD(KM)                                                                  \
+  combine_bwd_kernel<KM><<<N, kCombineThreads, 0, s>>>(dxr, part, n_part, token_routes, dx, \
+                                                        dprob, N, H, K)
+  if (K <= 2)
+    MOE_COMBINE_BWD(2);
+  else if (K <= 4)
+    MOE_COMBINE_BWD(4);
+  else if (K <= 8)
+    MOE_COMBINE_BWD(8);
+  else
+    MOE_COMBINE_BWD(16);
+#undef MOE_COMBINE_BWD
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? 1 : -(int)err;
+}
+
+int launch_slot_route(const int32_t* sorted_slot_ids, const int32_t* token_routes, int N, int K,
+                      int64_t s_max, int32_t* slot_route, int32_t* sched_zero, int n_zero,
+                      cudaStream_t s) {
+  if (s_max <= 0) return 0;
+  const int threads = 256;
+  const int64_t blocks = (s_max + threads - 1) / threads;
+  slot_route_kernel<<<(unsigned)blocks, threads, 0, s>>>(sorted_slot_ids, token_routes, N, K, s_max,
+                                                         slot_route, sched_zero, n_zero);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }

@@ -43,6 +43,7 @@
 
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace moe {
 namespace {
@@ -66,7 +67,9 @@ constexpr uint32_t kEpiStageBytes = kEpiWarps * 16u * kStageRowElems * 2u;  // p
 constexpr int kTileQ = 4;            // depth of the tile-id queue
 
 struct GemmParams {
-  int fc1;
+  int mode;              // GemmMode
+  int gather_b;          // B rows gathered from act by sorted_slot_ids (FC1, dgrad of FC2)
+  int a_mn;              // A read MN-major (the dgrads: the packed weights used transposed)
   int n_acc;
   int k_tiles;
   int a_rows_per_expert;
@@ -88,6 +91,12 @@ struct GemmParams {
   const int32_t* block_start;
   int32_t* sched;        // [2]: next tile to hand out, CTAs finished
   uint16_t* out;
+  uint16_t* out2;        // FC1: pre-activations [S,2I] or null; FC2 dgrad: p'*a [S,I]
+  const uint16_t* aux;   // FC2 dgrad: pre-activations [S,2I]
+  const int32_t* slot_route;  // FC2 dgrad: route of each slot, -1 for padding
+  const float* topk_p;        // FC2 dgrad: p' per route
+  float* part;                // FC2 dgrad: dprob partials [S, I/32]
+  int inter;                  // I
   uint32_t* err;
 };
 
@@ -146,6 +155,108 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float((uint32_t)b << 16);
+}
+
+// Writes a 16-slot x 32-feature block to a bf16 row-major matrix: lane l holds
+// feature l of slots 0..15 in v; dst points at (slot 0, feature 0), ld is the
+// row stride in elements. Staged through this warp's 1 KiB buffer so that each
+// row goes out as four 16-byte stores.
+__device__ __forceinline__ void store_rows16(uint32_t stg_u, int lane, const float (&v)[16],
+                                             uint16_t* dst, int ld) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t at = stg_u + (uint32_t)(i * kStageRowElems + lane) * 2u;
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(at), "h"((unsigned short)bf16_bits(v[i]))
+                 : "memory");
+  }
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {  // 16 rows x 4 chunks of 16 bytes
+    const int ch = lane + it * 32;
+    const int row = ch >> 2, part = ch & 3;
+    uint4 val;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                 : "r"(stg_u + (uint32_t)(row * kStageRowElems + part * 8) * 2u)
+                 : "memory");
+    *reinterpret_cast<uint4*>(dst + (size_t)row * ld + part * 8) = val;
+  }
+  __syncwarp();
+}
+
+// Epilogue of the FC2 dgrad for 16 slots (registers) x 32 features (lanes).
+// dA0[s,i] = dY[t_s] . W_down[e][i,:] arrives in v; with g, u the saved
+// pre-activations and p' the slot's routing probability:
+//   a = silu(g) u,  dprob part = sum_i a dA0,  dA = p' dA0,
+//   dg = dA u sigma(g) (1 + g (1 - sigma(g))),  du = dA silu(g),  aw = p' a.
+// dg and du go to dPre (gate columns, then up columns), aw to out2, and the
+// 32-feature partial sum of a dA0 of each slot to part[s, f*4 + q]. Padding
+// slots get zeros.
+__device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const Tile& T, int c0,
+                                                      int feat0, int q, int lane, uint32_t stg_u,
+                                                      const uint32_t (&v)[16]) {
+  const int I = p.inter;
+  const int ld2 = 2 * I;
+  float pl = 0.0f;
+  if (lane < 16 && c0 + lane < T.rows) {
+    const int r = p.slot_route[T.slot0 + c0 + lane];
+    if (r >= 0) pl = p.topk_p[r];
+  }
+  float dg[16], du[16], aw[16], dp[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float pj = __shfl_sync(0xFFFFFFFFu, pl, j);
+    const bool valid = c0 + j < T.rows;
+    const size_t row = (size_t)(T.slot0 + c0 + j) * ld2;
+    const float g = valid ? bf16_to_f32(p.aux[row + feat0 + lane]) : 0.0f;
+    const float u = valid ? bf16_to_f32(p.aux[row + I + feat0 + lane]) : 0.0f;
+    const float da0 = valid ? __uint_as_float(v[j]) : 0.0f;
+    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+    const float silu = g * sg;
+    const float a = silu * u;
+    dp[j] = a * da0;
+    const float dA = pj * da0;
+    dg[j] = dA * u * sg * (1.0f + g * (1.0f - sg));
+    du[j] = dA * silu;
+    aw[j] = pj * a;
+  }
+  const size_t row0 = (size_t)(T.slot0 + c0);
+  store_rows16(stg_u, lane, dg, p.out + row0 * ld2 + feat0, ld2);
+  store_rows16(stg_u, lane, du, p.out + row0 * ld2 + I + feat0, ld2);
+  store_rows16(stg_u, lane, aw, p.out2 + row0 * I + feat0, I);
+  // sum dp over the 32 lanes for each of the 16 slots, halving the values
+  // held per lane at each exchange: afterwards lanes 2m and 2m+1 hold slot m
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const bool hi = lane & 16;
+    const float send = hi ? dp[j] : dp[j + 8];
+    dp[j] = (hi ? dp[j + 8] : dp[j]) + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool hi = lane & 8;
+    const float send = hi ? dp[j] : dp[j + 4];
+    dp[j] = (hi ? dp[j + 4] : dp[j]) + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const bool hi = lane & 4;
+    const float send = hi ? dp[j] : dp[j + 2];
+    dp[j] = (hi ? dp[j + 2] : dp[j]) + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+  }
+  {
+    const bool hi = lane & 2;
+    const float send = hi ? dp[0] : dp[1];
+    dp[0] = (hi ? dp[1] : dp[0]) + __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+  }
+  dp[0] += __shfl_xor_sync(0xFFFFFFFFu, dp[0], 1);
+  const int m = lane >> 1;
+  if ((lane & 1) == 0 && c0 + m < T.rows)
+    p.part[(row0 + m) * (size_t)(I / 32) + T.f * 4 + q] = dp[0];
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -174,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     gather_abort = 0;
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), p.fc1 ? 1 + kGatherThreads : 1);
+      mbar_init(smem_u32(&full_bar[s]), p.gather_b ? 1 + kGatherThreads : 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     mbar_init(smem_u32(&tmem_full_bar), 1);
@@ -182,11 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kTileQ; ++i) {
       mbar_init(smem_u32(&tq_full[i]), 1);
       // consumers: the UMMA thread, the epilogue warps, the 4 gather warps (FC1)
-      mbar_init(smem_u32(&tq_empty[i]), 1 + kEpiWarps + (p.fc1 ? 4 : 0));
+      mbar_init(smem_u32(&tq_empty[i]), 1 + kEpiWarps + (p.gather_b ? 4 : 0));
     }
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
-    if (!p.fc1) tma_prefetch_desc(&tmB);
+    if (!p.gather_b) tma_prefetch_desc(&tmB);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
   if (warp == 0) build_tile_list(p, tpre, ttn, lane);
@@ -231,9 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t < 0) break;
       Tile T;
       tile_at(p, tpre, ttn, t, T);
-      const int a_row0 = T.e * p.a_rows_per_expert + T.f * p.f_rows;
+      // K-major A: rows e*a_rows_per_expert + f*f_rows, k along the row.
+      // MN-major A: the weight matrix read transposed; its rows are k
+      // (e*a_rows_per_expert + k) and the tile's 128 features are two 64-wide
+      // column boxes per accumulator.
+      const int a_row0 = T.e * p.a_rows_per_expert + (p.a_mn ? 0 : T.f * p.f_rows);
+      const int a_col0 = T.f * p.f_rows;
       const uint32_t tx =
-          (uint32_t)p.n_acc * kATileBytes + (p.fc1 ? 0u : (uint32_t)T.n_eff * 128u);
+          (uint32_t)p.n_acc * kATileBytes + (p.gather_b ? 0u : (uint32_t)T.n_eff * 128u);
       bool ok = true;
       for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
         const int s = (int)(gk % (uint32_t)p.stages);
@@ -250,12 +366,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kx = kt * kBK;
         if (lane == 0) {
           mbar_arrive_expect_tx(fb, tx);
-          tma_load_2d(st, &tmA, kx, a_row0, fb, pol_w);
-          if (p.n_acc == 2)
-            tma_load_2d(st + kATileBytes, &tmA, kx, a_row0 + p.a_second_off, fb, pol_w);
+          if (p.a_mn) {
+            for (int ac = 0; ac < p.n_acc; ++ac)
+              for (int c = 0; c < 2; ++c)
+                tma_load_2d(st + (uint32_t)ac * kATileBytes + (uint32_t)c * 8192u, &tmA,
+                            a_col0 + ac * kTileM + c * 64, a_row0 + kx, fb, pol_w);
+          } else {
+            tma_load_2d(st, &tmA, kx, a_row0, fb, pol_w);
+            if (p.n_acc == 2)
+              tma_load_2d(st + kATileBytes, &tmA, kx, a_row0 + p.a_second_off, fb, pol_w);
+          }
         }
         __syncwarp();
-        if (!p.fc1) {
+        if (!p.gather_b) {
           const uint32_t b = st + p.b_off;
           for (int q = lane * 16; q < T.n_eff; q += 512)
             tma_load_2d(b + (uint32_t)q * 128u, &tmB, kx, T.slot0 + q, fb, pol_x);
@@ -294,7 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16_f32(kTileM, T.n_eff);
+        const uint32_t idesc = idesc_bf16_f32(kTileM, T.n_eff) | (p.a_mn ? kIdescAMnMajor : 0u);
+        // one UMMA k-step (16 elements) advances 32 bytes along a K-major row,
+        // or 16 rows of 128 bytes in an MN-major tile
+        const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
         for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
           const int s = (int)(gk % (uint32_t)p.stages);
           const uint32_t u = gk / (uint32_t)p.stages;
@@ -308,10 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t acc = (kt | kk) != 0;
             const uint64_t bdesc = sdesc_sw128(st + p.b_off + (uint32_t)kk * 32u);
-            umma_bf16(tmem, sdesc_sw128(st + (uint32_t)kk * 32u), bdesc, idesc, acc);
-            if (p.n_acc == 2)
-              umma_bf16(tmem + 256u, sdesc_sw128(st + kATileBytes + (uint32_t)kk * 32u), bdesc,
-                        idesc, acc);
+            const uint32_t a0 = st + (uint32_t)kk * a_kstep;
+            umma_bf16(tmem, p.a_mn ? sdesc_sw128_mn(a0) : sdesc_sw128(a0), bdesc, idesc, acc);
+            if (p.n_acc == 2) {
+              const uint32_t a1 = a0 + kATileBytes;
+              umma_bf16(tmem + 256u, p.a_mn ? sdesc_sw128_mn(a1) : sdesc_sw128(a1), bdesc, idesc,
+                        acc);
+            }
           }
           umma_commit(smem_u32(&empty_bar[s]));
         }
@@ -338,50 +467,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++tc;
       if (!__shfl_sync(0xFFFFFFFFu, w, 0)) break;
       tc_fence_after();
-      const int feat0 = p.fc1 ? T.f * kTileM + q * 32 : T.f * p.f_rows + q * 32;
+      const int feat0 = T.f * p.f_rows + q * 32;  // first feature of this lane quarter
       for (int c0 = half * 16; c0 < T.n_eff; c0 += 32) {
         uint32_t v0[16], v1[16];
         tmem_ld16(tl + (uint32_t)c0, v0);
         if (p.n_acc == 2) tmem_ld16(tl + 256u + (uint32_t)c0, v1);
         tmem_ld_wait();
-        // lane = feature; stage [16 slots][32 features] as bf16 and write the
-        // rows with 16-byte stores; FC2's second accumulator follows the first
-        for (int seg = 0; seg < (p.fc1 ? 1 : p.n_acc); ++seg) {
+        const size_t row0 = (size_t)(T.slot0 + c0);  // slot of register 0
+        if (p.mode == kModeFc1) {
+          float hv[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float a;
-            if (p.fc1) {
-              const float g = __uint_as_float(v0[i]);
-              a = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[i]);
-            } else {
-              a = __uint_as_float(seg == 0 ? v0[i] : v1[i]);
-            }
-            const uint32_t at = stg_u + (uint32_t)(i * kStageRowElems + lane) * 2u;
-            asm volatile("st.shared.b16 [%0], %1;" ::"r"(at), "h"((unsigned short)bf16_bits(a))
-                         : "memory");
+            const float g = __uint_as_float(v0[i]);
+            hv[i] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[i]);
           }
-          __syncwarp();
+          store_rows16(stg_u, lane, hv, p.out + row0 * p.out_ld + feat0, p.out_ld);
+          if (p.out2) {  // pre-activations for the backward: gate, then up
+            float gv[16], uv[16];
 #pragma unroll
-          for (int it = 0; it < 2; ++it) {  // 16 rows x 4 chunks of 16 bytes
-            const int ch = lane + it * 32;
-            const int row = ch >> 2, part = ch & 3;
-            uint4 val;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                         : "r"(stg_u + (uint32_t)(row * kStageRowElems + part * 8) * 2u)
-                         : "memory");
-            uint16_t* dst = p.out + (size_t)(T.slot0 + c0 + row) * p.out_ld + feat0 +
-                            seg * kTileM + part * 8;
-            *reinterpret_cast<uint4*>(dst) = val;
+            for (int i = 0; i < 16; ++i) {
+              gv[i] = __uint_as_float(v0[i]);
+              uv[i] = __uint_as_float(v1[i]);
+            }
+            const int ld2 = 2 * p.inter;
+            store_rows16(stg_u, lane, gv, p.out2 + row0 * ld2 + feat0, ld2);
+            store_rows16(stg_u, lane, uv, p.out2 + row0 * ld2 + p.inter + feat0, ld2);
           }
-          __syncwarp();
+        } else if (p.mode == kModeDgrad2) {
+          swiglu_backward_chunk(p, T, c0, feat0, q, lane, stg_u, v0);
+        } else {
+          for (int seg = 0; seg < p.n_acc; ++seg) {
+            float ov[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = __uint_as_float(seg == 0 ? v0[i] : v1[i]);
+            store_rows16(stg_u, lane, ov, p.out + row0 * p.out_ld + feat0 + seg * kTileM,
+                         p.out_ld);
+          }
         }
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar));
     }
-  } else if (p.fc1) {
-    // ---------------------------------------------------------------- FC1 row gather
+  } else if (p.gather_b) {
+    // ---------------------------------------------------------------- B row gather
     // Row r of a stage holds x[rows_s[r], kx .. kx+63]: 16-byte chunk c at
     // r*128 + ((c ^ (r%8)) * 16), the 128-byte swizzle the UMMA descriptor
     // expects; sentinel rows are zero-filled. Each thread keeps kGatherDepth
@@ -444,34 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }();
-  return fn;
-}
-
-// 2-D bf16 tensor [rows, cols] row-major, 128-byte swizzled boxes of
-// box_cols x box_rows; out-of-bounds elements read as zero.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-              uint32_t box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // SM count of the current device, with the kernel's shared-memory opt-in set
 // up once per device.
 int device_sms(cudaError_t* err) {
@@ -496,38 +596,75 @@ int device_sms(cudaError_t* err) {
 int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.max_rows <= 0 || a.N <= 0) return 0;
   GemmParams p{};
-  p.fc1 = a.fc1;
+  p.mode = a.mode;
+  p.gather_b = a.mode == kModeFc1 || a.mode == kModeDgrad2;
+  p.a_mn = a.mode == kModeDgrad2 || a.mode == kModeDgrad1;
   p.bm = a.bm;
   p.sorted_slot_ids = a.sorted_slot_ids;
   p.kept_counts = a.kept_counts;
   p.block_start = a.block_start;
   p.out = static_cast<uint16_t*>(a.out);
+  p.out2 = static_cast<uint16_t*>(a.out2);
+  p.aux = static_cast<const uint16_t*>(a.aux);
+  p.slot_route = a.slot_route;
+  p.topk_p = a.topk_p;
+  p.part = a.part;
+  p.inter = a.I;
   p.err = a.err;
   p.act = static_cast<const uint16_t*>(a.act);
-  p.act_ld = a.fc1 ? a.H : a.I;
-  p.act_rows = a.fc1 ? a.N : 0;
+  p.act_rows = p.gather_b ? a.N : 0;
   const int64_t S = a.s_max;
+  const uint64_t E = (uint64_t)a.E;
   CUtensorMap tmA, tmB;
-  if (a.fc1) {
-    p.n_acc = 2;
-    p.k_tiles = a.H / kBK;
-    p.a_rows_per_expert = 2 * a.I;
-    p.a_second_off = a.I;
-    p.f_rows = kTileM;
-    p.f_tiles = a.I / kTileM;
-    p.out_ld = a.I;
-    if (!make_map(&tmA, a.w, (uint64_t)a.H, (uint64_t)a.E * 2 * a.I, kBK, kTileM)) return -1;
-    tmB = tmA;  // unused: FC1 gathers its B rows with cp.async
-  } else {
-    p.n_acc = (a.H % (2 * kTileM) == 0) ? 2 : 1;
-    p.k_tiles = a.I / kBK;
-    p.a_rows_per_expert = a.H;
-    p.a_second_off = kTileM;
-    p.f_rows = kTileM * p.n_acc;
-    p.f_tiles = a.H / p.f_rows;
-    p.out_ld = a.H;
-    if (!make_map(&tmA, a.w, (uint64_t)a.I, (uint64_t)a.E * a.H, kBK, kTileM)) return -1;
-    if (!make_map(&tmB, a.act, (uint64_t)a.I, (uint64_t)S, kBK, 16)) return -1;
+  switch (a.mode) {
+    case kModeFc1:  // A = w13 rows [E*2I, H]; B gathered from x [N, H]
+      p.n_acc = 2;
+      p.k_tiles = a.H / kBK;
+      p.a_rows_per_expert = 2 * a.I;
+      p.a_second_off = a.I;
+      p.f_rows = kTileM;
+      p.f_tiles = a.I / kTileM;
+      p.out_ld = a.I;
+      p.act_ld = a.H;
+      if (!make_map(&tmA, a.w, (uint64_t)a.H, E * 2 * a.I, kBK, kTileM)) return -1;
+      tmB = tmA;  // unused: B rows are gathered with cp.async
+      break;
+    case kModeFc2:  // A = w2 rows [E*H, I]; B = h [S, I]
+      p.n_acc = (a.H % (2 * kTileM) == 0) ? 2 : 1;
+      p.k_tiles = a.I / kBK;
+      p.a_rows_per_expert = a.H;
+      p.a_second_off = kTileM;
+      p.f_rows = kTileM * p.n_acc;
+      p.f_tiles = a.H / p.f_rows;
+      p.out_ld = a.H;
+      p.act_ld = a.I;
+      if (!make_map(&tmA, a.w, (uint64_t)a.I, E * a.H, kBK, kTileM)) return -1;
+      if (!make_map(&tmB, a.act, (uint64_t)a.I, (uint64_t)S, kBK, 16)) return -1;
+      break;
+    case kModeDgrad2:  // A[i, h] = w2[e][h][i] (MN-major, K = H); B gathered from dY [N, H]
+      p.n_acc = 1;
+      p.k_tiles = a.H / kBK;
+      p.a_rows_per_expert = a.H;
+      p.f_rows = kTileM;
+      p.f_tiles = a.I / kTileM;
+      p.out_ld = 2 * a.I;
+      p.act_ld = a.H;
+      if (!make_map(&tmA, a.w, (uint64_t)a.I, E * a.H, 64, kBK)) return -1;
+      tmB = tmA;
+      break;
+    case kModeDgrad1:  // A[h, k] = w13[e][k][h] (MN-major, K = 2I); B = dPre [S, 2I]
+      p.n_acc = (a.H % (2 * kTileM) == 0) ? 2 : 1;
+      p.k_tiles = 2 * a.I / kBK;
+      p.a_rows_per_expert = 2 * a.I;
+      p.f_rows = kTileM * p.n_acc;
+      p.f_tiles = a.H / p.f_rows;
+      p.out_ld = a.H;
+      p.act_ld = 2 * a.I;
+      if (!make_map(&tmA, a.w, (uint64_t)a.H, E * 2 * a.I, 64, kBK)) return -1;
+      if (!make_map(&tmB, a.act, (uint64_t)(2 * a.I), (uint64_t)S, kBK, 16)) return -1;
+      break;
+    default:
+      return -1;
   }
   p.E = a.E;
   // stage size for the largest slot tile any expert can have

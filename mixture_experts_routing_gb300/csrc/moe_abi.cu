@@ -120,6 +120,32 @@ WsLayout ws_layout(const moe_config_t* c) {
   return w;
 }
 
+// Backward scratch: slot -> route map, the backward GEMMs' tile counters, the
+// dprob partials, dPre = [dg | du], aw = p' a and the per-slot input gradient.
+struct BwdLayout {
+  size_t slot_route, sched, part, dpre, aw, dxr, total;
+};
+
+BwdLayout bwd_layout(const moe_config_t* c) {
+  BwdLayout w{};
+  const int64_t S = c->n_tokens > 0 ? slots_of(c) : 0;
+  const int64_t H = c->hidden, I = c->inter;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  w.slot_route = take((size_t)S * 4);
+  w.sched = take(8 * 4);
+  w.part = take((size_t)(S * (I / 32)) * 4);
+  w.dpre = take((size_t)(S * 2 * I) * 2);
+  w.aw = take((size_t)(S * I) * 2);
+  w.dxr = take((size_t)(S * H) * 2);
+  w.total = off;
+  return w;
+}
+
 bool routes_complete(const moe_routes_t* r) {
   return r && r->topk_ids && r->topk_p && r->keep && r->expert_counts && r->kept_counts &&
          r->sorted_slot_ids && r->expert_ids && r->block_start && r->num_tokens_post_padded &&
@@ -203,20 +229,9 @@ int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_route
   return finish(moe::launch_route(a, stream));
 }
 
-static int gemm_common(const moe_config_t* cfg, const moe_routes_t* routes, const void* act,
-                       const void* w, void* out, int fc1, cudaStream_t stream) {
-  int rc = check_cfg(cfg);
-  if (rc != MOE_OK) return rc;
-  if (!routes || !routes->sorted_slot_ids || !routes->kept_counts || !routes->block_start ||
-      !routes->gemm_sched)
-    return MOE_ERR_INVALID_ARG;
-  if (cfg->n_tokens == 0) return MOE_OK;
-  if (!act || !w || !out || !aligned16(act) || !aligned16(w) || !aligned16(out))
-    return MOE_ERR_INVALID_ARG;
-  uint32_t* err = error_word_ptr();
-  if (!err) return MOE_ERR_CUDA;
-  moe::GemmArgs a{};
-  a.fc1 = fc1;
+// Shape fields and routing pointers common to every expert-GEMM launch.
+static void gemm_base(const moe_config_t* cfg, const moe_routes_t* routes, uint32_t* err,
+                      moe::GemmArgs& a) {
   a.N = cfg->n_tokens;
   a.H = cfg->hidden;
   a.E = cfg->n_experts;
@@ -226,31 +241,62 @@ static int gemm_common(const moe_config_t* cfg, const moe_routes_t* routes, cons
   if (a.max_rows > cfg->n_tokens) a.max_rows = cfg->n_tokens;
   a.max_total = (int64_t)cfg->n_tokens * cfg->top_k;
   a.s_max = slots_of(cfg);
-  a.act = act;
-  a.w = w;
-  a.out = out;
-  a.act_rows = fc1 ? cfg->n_tokens : a.s_max;
   a.sorted_slot_ids = routes->sorted_slot_ids;
   a.kept_counts = routes->kept_counts;
   a.block_start = routes->block_start;
-  a.sched = routes->gemm_sched + (fc1 ? 0 : 2);
   a.err = err;
+}
+
+static bool gemm_routes_ok(const moe_routes_t* routes) {
+  return routes && routes->sorted_slot_ids && routes->kept_counts && routes->block_start &&
+         routes->gemm_sched;
+}
+
+static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* act,
+                      const void* w, void* out, void* preact, int fc1, cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!gemm_routes_ok(routes)) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_tokens == 0) return MOE_OK;
+  if (!act || !w || !out || !aligned16(act) || !aligned16(w) || !aligned16(out) ||
+      !aligned16(preact))
+    return MOE_ERR_INVALID_ARG;
+  uint32_t* err = error_word_ptr();
+  if (!err) return MOE_ERR_CUDA;
+  moe::GemmArgs a{};
+  gemm_base(cfg, routes, err, a);
+  a.mode = fc1 ? moe::kModeFc1 : moe::kModeFc2;
+  a.act = act;
+  a.w = w;
+  a.out = out;
+  a.out2 = fc1 ? preact : nullptr;
+  a.act_rows = fc1 ? cfg->n_tokens : a.s_max;
+  a.sched = routes->gemm_sched + (fc1 ? 0 : 2);
   return finish(moe::launch_gemm(a, stream));
 }
 
 int moe_fc1_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
                     const void* w13, void* h, cudaStream_t stream) {
-  return gemm_common(cfg, routes, x, w13, h, 1, stream);
+  return fc_forward(cfg, routes, x, w13, h, nullptr, 1, stream);
 }
 
 int moe_fc2_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* h,
                     const void* w2, void* o, cudaStream_t stream) {
-  return gemm_common(cfg, routes, h, w2, o, 0, stream);
+  return fc_forward(cfg, routes, h, w2, o, nullptr, 0, stream);
 }
 
 int moe_ffn_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
                     const void* w13, const void* w2, void* h, void* o, cudaStream_t stream) {
   const int rc = moe_fc1_forward(cfg, routes, x, w13, h, stream);
+  if (rc != MOE_OK) return rc;
+  return moe_fc2_forward(cfg, routes, h, w2, o, stream);
+}
+
+int moe_ffn_forward_train(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                          const void* w13, const void* w2, void* h, void* o, void* preact,
+                          cudaStream_t stream) {
+  if (cfg && cfg->n_tokens > 0 && !preact) return MOE_ERR_INVALID_ARG;
+  const int rc = fc_forward(cfg, routes, x, w13, h, preact, 1, stream);
   if (rc != MOE_OK) return rc;
   return moe_fc2_forward(cfg, routes, h, w2, o, stream);
 }
@@ -296,6 +342,115 @@ int moe_pack_w2(const moe_config_t* cfg, const void* w_down, void* w2, cudaStrea
   const int E = cfg->n_experts, H = cfg->hidden, I = cfg->inter;
   return finish(moe::launch_transpose(static_cast<const uint16_t*>(w_down), static_cast<uint16_t*>(w2),
                                       E, I, H, (int64_t)I * H, (int64_t)I * H, 0, stream));
+}
+
+int64_t moe_backward_workspace_bytes(const moe_config_t* cfg) {
+  const int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  return (int64_t)bwd_layout(cfg).total;
+}
+
+int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                     const void* w13, const void* w2, const void* preact, const void* dy,
+                     void* dx, float* dw13, float* dw2, float* dprob, void* workspace,
+                     size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!routes_complete(routes)) return MOE_ERR_INVALID_ARG;
+  if (!dw13 || !dw2 || !aligned16(dw13) || !aligned16(dw2)) return MOE_ERR_INVALID_ARG;
+  const BwdLayout L = bwd_layout(cfg);
+  if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  if (cfg->n_tokens > 0 &&
+      (!x || !w13 || !w2 || !preact || !dy || !dx || !dprob || !aligned16(x) ||
+       !aligned16(w13) || !aligned16(w2) || !aligned16(preact) || !aligned16(dy) ||
+       !aligned16(dx)))
+    return MOE_ERR_INVALID_ARG;
+  uint32_t* err = error_word_ptr();
+  if (!err) return MOE_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* slot_route = reinterpret_cast<int32_t*>(ws + L.slot_route);
+  int32_t* sched = reinterpret_cast<int32_t*>(ws + L.sched);
+  float* part = reinterpret_cast<float*>(ws + L.part);
+  void* dpre = ws + L.dpre;
+  void* aw = ws + L.aw;
+  void* dxr = ws + L.dxr;
+  const int N = cfg->n_tokens, H = cfg->hidden, E = cfg->n_experts, I = cfg->inter,
+            K = cfg->top_k;
+  const int64_t S = slots_of(cfg);
+  int launched = 0;
+  auto add = [&](int l) {
+    if (l < 0) return false;
+    launched += l;
+    return true;
+  };
+  // 1. slot -> route map (p' and dprob of each slot); zeroes the counters
+  if (!add(moe::launch_slot_route(routes->sorted_slot_ids, routes->token_routes, N, K,
+                                  N > 0 ? S : 0, slot_route, sched, 8, stream)))
+    return finish(-1);
+  if (N > 0) {
+    // 2. FC2 dgrad with the SwiGLU backward: dPre, aw = p' a, dprob partials
+    moe::GemmArgs g{};
+    gemm_base(cfg, routes, err, g);
+    g.mode = moe::kModeDgrad2;
+    g.act = dy;
+    g.w = w2;
+    g.out = dpre;
+    g.out2 = aw;
+    g.aux = preact;
+    g.slot_route = slot_route;
+    g.topk_p = routes->topk_p;
+    g.part = part;
+    g.act_rows = N;
+    g.sched = sched + 0;
+    if (!add(moe::launch_gemm(g, stream))) return finish(-1);
+    // 3. FC1 dgrad: dXr[s] = dg W_gate^T + du W_up^T
+    moe::GemmArgs d{};
+    gemm_base(cfg, routes, err, d);
+    d.mode = moe::kModeDgrad1;
+    d.act = dpre;
+    d.w = w13;
+    d.out = dxr;
+    d.act_rows = S;
+    d.sched = sched + 2;
+    if (!add(moe::launch_gemm(d, stream))) return finish(-1);
+    // 4. per-token reduction: dX (unit weights) and dprob
+    if (!add(moe::launch_combine_bwd(static_cast<const uint16_t*>(dxr), part, I / 32,
+                                     routes->token_routes, N, H, K, static_cast<uint16_t*>(dx),
+                                     dprob, stream)))
+      return finish(-1);
+  }
+  // 5. weight gradients (zero for an expert without kept slots, and for N = 0)
+  moe::WgradArgs wg{};
+  wg.N = N;
+  wg.H = H;
+  wg.E = E;
+  wg.I = I;
+  wg.bm = cfg->block_m;
+  wg.s_max = S > 0 ? S : 1;
+  wg.x = x;
+  wg.dy = dy;
+  wg.sorted_slot_ids = routes->sorted_slot_ids;
+  wg.kept_counts = routes->kept_counts;
+  wg.block_start = routes->block_start;
+  wg.err = err;
+  if (N > 0) {
+    wg.dw13 = 0;
+    wg.slot_mat = aw;
+    wg.sched = sched + 4;
+    wg.out = dw2;
+    if (!add(moe::launch_wgrad(wg, stream))) return finish(-1);
+    wg.dw13 = 1;
+    wg.slot_mat = dpre;
+    wg.sched = sched + 6;
+    wg.out = dw13;
+    if (!add(moe::launch_wgrad(wg, stream))) return finish(-1);
+  } else {
+    const size_t n13 = (size_t)E * 2 * I * H * 4, n2 = (size_t)E * H * I * 4;
+    if (cudaMemsetAsync(dw13, 0, n13, stream) != cudaSuccess ||
+        cudaMemsetAsync(dw2, 0, n2, stream) != cudaSuccess)
+      return finish(-1);
+  }
+  return finish(launched);
 }
 
 const char* moe_status_string(int status) {

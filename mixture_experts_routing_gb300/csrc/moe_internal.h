@@ -52,16 +52,29 @@ struct RouteArgs {
 // Returns the number of kernels launched (>= 0) or a negative cudaError_t.
 int launch_route(const RouteArgs& a, cudaStream_t s);
 
+enum GemmMode {
+  kModeFc1 = 0,     // FC1: B = rows of x gathered by slot, SwiGLU epilogue
+  kModeFc2 = 1,     // FC2: B = h rows by slot (TMA), plain epilogue
+  kModeDgrad2 = 2,  // dgrad of FC2: A = w2 read MN-major, B = rows of dY gathered by
+                    // slot, SwiGLU-backward epilogue
+  kModeDgrad1 = 3,  // dgrad of FC1: A = w13 read MN-major, B = dPre rows by slot (TMA)
+};
+
 struct GemmArgs {
-  int fc1;               // 1: FC1 gather + SwiGLU epilogue; 0: FC2 plain epilogue
+  int mode;              // GemmMode
   int N, H, E, I, bm;
   int64_t max_rows;      // upper bound of kept routes per expert
   int64_t max_total;     // upper bound of kept routes over all experts
   int64_t s_max;         // rows of the slot-space buffers (h, o)
-  const void* act;       // FC1: x [N,H]; FC2: h [S,I]
-  const void* w;         // FC1: w13 [E,2I,H]; FC2: w2 [E,H,I]
-  void* out;             // FC1: h [S,I]; FC2: o [S,H]
-  int64_t act_rows;      // rows of act (N for FC1, S for FC2)
+  const void* act;       // FC1: x [N,H]; FC2: h [S,I]; dgrad2: dY [N,H]; dgrad1: dPre [S,2I]
+  const void* w;         // FC1, dgrad1: w13 [E,2I,H]; FC2, dgrad2: w2 [E,H,I]
+  void* out;             // FC1: h [S,I]; FC2: o [S,H]; dgrad2: dPre [S,2I]; dgrad1: dXr [S,H]
+  void* out2;            // FC1: pre-activations [S,2I] or null; dgrad2: p'*a [S,I]
+  const void* aux;       // dgrad2: pre-activations [S,2I]
+  const int32_t* slot_route;  // dgrad2: route of each slot (-1 padding)
+  const float* topk_p;        // dgrad2
+  float* part;                // dgrad2: dprob partials [S, I/32]
+  int64_t act_rows;      // rows of act (N when gathered, else S)
   const int32_t* sorted_slot_ids;
   const int32_t* kept_counts;
   const int32_t* block_start;
@@ -70,6 +83,35 @@ struct GemmArgs {
 };
 
 int launch_gemm(const GemmArgs& a, cudaStream_t s);
+
+struct WgradArgs {
+  int dw13;              // 1: dW13 [E,2I,H] from dPre and x; 0: dW2 [E,H,I] from aw and dY
+  int N, H, E, I, bm;
+  int64_t s_max;
+  const void* slot_mat;  // dW13: dPre [S,2I]; dW2: aw [S,I]
+  const void* x;         // [N,H]
+  const void* dy;        // [N,H]
+  const int32_t* sorted_slot_ids;
+  const int32_t* kept_counts;
+  const int32_t* block_start;
+  int32_t* sched;        // [2]
+  float* out;
+  uint32_t* err;
+};
+
+int launch_wgrad(const WgradArgs& a, cudaStream_t s);
+
+// Backward helpers (combine.cu).
+// slot_route[s] = route t*K+k held by slot s, -1 for padding; also zeroes
+// sched_zero[0..n_zero).
+int launch_slot_route(const int32_t* sorted_slot_ids, const int32_t* token_routes, int N, int K,
+                      int64_t s_max, int32_t* slot_route, int32_t* sched_zero, int n_zero,
+                      cudaStream_t s);
+// dX[t] = sum_k dXr[token_routes[t,k]] (fp32, k order) and
+// dprob[t,k] = sum_j part[token_routes[t,k], j] (j order; 0 for a dropped route).
+int launch_combine_bwd(const uint16_t* dxr, const float* part, int n_part,
+                       const int32_t* token_routes, int N, int H, int K, uint16_t* dx,
+                       float* dprob, cudaStream_t s);
 
 struct CombineArgs {
   int N, H, K;

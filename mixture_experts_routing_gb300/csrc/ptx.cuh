@@ -153,6 +153,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: bf16 x bf16 -> f32, both operands K-major.
+// MN-major operand in 128-byte-swizzled tiles of 64 MN elements x 8 K rows:
+// the leading byte offset steps between 64-element MN chunks (each chunk holds
+// 64 K rows of 128 bytes: 8192 bytes), the stride byte offset between 8-row K
+// groups (1024 bytes).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(8192u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// instruction-descriptor bits: A (bit 15) or B (bit 16) read MN-major
+constexpr uint32_t kIdescAMnMajor = 1u << 15;
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);

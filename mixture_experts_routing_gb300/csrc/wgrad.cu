@@ -1,0 +1,406 @@
+// Expert weight gradients on the 5th-generation tensor cores.
+//
+// For each expert e, over its kept slots s (token t_s = sorted_slot_ids[s]):
+//   dW2[e][h][i]  = sum_s dY[t_s, h] * aw[s, i]        aw = p' * silu(g) * u
+//   dW13[e][k][h] = sum_s dPre[s, k] * x[t_s, h]        dPre = [dg | du]
+// ("Permute-Free Grouped GEMM for MoE (bf16, gfx950)", section 5, the
+// weight-gradient kernel: the contraction runs over the token slots, one owner
+// per output tile, fp32 output). dW2 and dW13 have the packed layouts of w2
+// [E,H,I] and w13 [E,2I,H], so they update the packed weights directly.
+//
+// Both operands have the slot as their contraction index and their feature
+// dimension contiguous in memory, so both are read MN-major: stage tiles are
+// 64 slots (K) x 64-feature chunks, 128 bytes per row with the 128-byte
+// swizzle. One operand is slot-indexed (aw or dPre rows: TMA boxes), the other
+// is token-indexed (rows of dY or x picked through sorted_slot_ids: 16-byte
+// cp.async by four gather warps, padding rows zero-filled), as in the forward's
+// gather-in-GEMM.
+//
+// The UMMA M dimension is always the output's contiguous dimension (i for dW2,
+// h for dW13), so TMEM lane = output column and every epilogue store of one
+// accumulator column is 32 consecutive floats. Tiles are 128 x 256 with two
+// TMEM accumulators (512 columns), so the epilogue of one tile overlaps the
+// MMAs of the next. An expert's last k-chunk issues only the 16-slot k-steps
+// that hold kept slots (rows up to roundup(kept,16) are written by the FC2
+// dgrad, zeros for padding); an expert with no kept slot gets zero tiles
+// written without any MMA.
+//
+// Persistent CTAs with a dynamic tile scheduler (global counter, shared-memory
+// tile queue, last CTA resets the counter), as in the forward GEMMs.
+#include <cudaTypedefs.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWM = 128;              // UMMA M: output-contiguous features per tile
+constexpr int kWN = 256;              // UMMA N
+constexpr int kWK = 64;               // slots per stage
+constexpr int kWThreads = 448;
+constexpr int kWEpiWarps = 8;         // warps 2-9
+constexpr int kWGatherWarp0 = 10;     // warps 10-13
+constexpr int kWGatherThreads = 128;
+constexpr int kWGatherDepth = 2;
+constexpr int kWMaxStages = 8;
+constexpr uint32_t kWABytes = kWM * kWK * 2;  // 16 KiB: 2 chunks of 64 features
+constexpr uint32_t kWBBytes = kWN * kWK * 2;  // 32 KiB: 4 chunks
+constexpr uint32_t kWStageBytes = kWABytes + kWBBytes;
+constexpr uint32_t kWSmemBudget = 223 * 1024;
+constexpr uint32_t kWTmemCols = 512;
+constexpr int kWTileQ = 4;
+
+struct WgradParams {
+  int E, m_total, n_total, m_tiles, n_tiles, bm, stages;
+  int tile_n;            // UMMA N: 256, or 128 when n_total is not a multiple of 256
+  int a_gather;          // 1: A from gathered token rows (dW13: x), B slot rows (dPre)
+                         // 0: A slot rows (aw), B from gathered token rows (dW2: dY)
+  const uint16_t* act;   // token-indexed operand [act_rows, act_ld]
+  int act_ld, act_rows;
+  const int32_t* sorted_slot_ids;
+  const int32_t* kept_counts;
+  const int32_t* block_start;
+  int32_t* sched;        // [2]
+  float* out;            // [E, n_total, m_total]
+  uint32_t* err;
+};
+
+struct WTile {
+  int e, m0, n0, kept, slot0;
+};
+
+__device__ __forceinline__ void wtile_at(const WgradParams& p, int t, WTile& T) {
+  const int per = p.m_tiles * p.n_tiles;
+  T.e = t / per;
+  const int r = t - T.e * per;
+  T.m0 = (r % p.m_tiles) * kWM;
+  T.n0 = (r / p.m_tiles) * p.tile_n;
+  T.kept = max(p.kept_counts[T.e], 0);
+  T.slot0 = p.block_start[T.e] * p.bm;
+}
+
+__device__ __forceinline__ void named_bar_sync_w(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    moe_wgrad_kernel(const __grid_constant__ CUtensorMap tmD, const WgradParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kWMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kWMaxStages];
+  __shared__ __align__(8) uint64_t tmem_full_bar[2];
+  __shared__ __align__(8) uint64_t tmem_empty_bar[2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int gather_abort;
+  __shared__ int32_t tile_q[kWTileQ];
+  __shared__ __align__(8) uint64_t tq_full[kWTileQ];
+  __shared__ __align__(8) uint64_t tq_empty[kWTileQ];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int n_tiles = p.E * p.m_tiles * p.n_tiles;
+  // the slot-indexed operand: A (aw) when B is gathered, else B (dPre)
+  const uint32_t d_off = p.a_gather ? kWABytes : 0u;
+  const int d_chunks = p.a_gather ? p.tile_n / 64 : kWM / 64;
+  const uint32_t g_off = p.a_gather ? 0u : kWABytes;
+  const int g_chunks = p.a_gather ? kWM / 64 : p.tile_n / 64;
+
+  if (threadIdx.x == 0) {
+    gather_abort = 0;
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1 + kWGatherThreads);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tmem_full_bar[b]), 1);
+      mbar_init(smem_u32(&tmem_empty_bar[b]), kWEpiWarps);
+    }
+    for (int i = 0; i < kWTileQ; ++i) {
+      mbar_init(smem_u32(&tq_full[i]), 1);
+      mbar_init(smem_u32(&tq_empty[i]), 1 + kWEpiWarps + 4);
+    }
+    mbar_fence_init();
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), kWTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  auto pop_tile = [&](uint32_t& qi, uint32_t code) -> int {
+    const int slot = (int)(qi % kWTileQ);
+    int t = -1;
+    if (lane == 0) {
+      if (mbar_wait(smem_u32(&tq_full[slot]), (qi / kWTileQ) & 1u, p.err, code)) t = tile_q[slot];
+      mbar_arrive(smem_u32(&tq_empty[slot]));
+    }
+    ++qi;
+    return __shfl_sync(0xFFFFFFFFu, t, 0);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ scheduler + TMA producer
+    const uint64_t pol = policy_evict_last();
+    uint32_t gk = 0;
+    for (uint32_t qi = 0;; ++qi) {
+      int t = -1;
+      if (lane == 0) {
+        t = atomicAdd(&p.sched[0], 1);
+        if (t >= n_tiles) t = -1;
+        const int slot = (int)(qi % kWTileQ);
+        if (qi >= (uint32_t)kWTileQ &&
+            !mbar_wait(smem_u32(&tq_empty[slot]), ((qi / kWTileQ) - 1u) & 1u, p.err, kErrWaitEmpty))
+          t = -1;
+        tile_q[slot] = t;
+        mbar_arrive(smem_u32(&tq_full[slot]));
+      }
+      t = __shfl_sync(0xFFFFFFFFu, t, 0);
+      if (t < 0) break;
+      WTile T;
+      wtile_at(p, t, T);
+      const int chunks = (T.kept + kWK - 1) / kWK;
+      const int dcol0 = p.a_gather ? T.n0 : T.m0;
+      bool ok = true;
+      for (int kt = 0; kt < chunks; ++kt, ++gk) {
+        const int s = (int)(gk % (uint32_t)p.stages);
+        const uint32_t u = gk / (uint32_t)p.stages;
+        int w = 1;
+        if (lane == 0 && gk >= (uint32_t)p.stages)
+          w = mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty);
+        if (!__shfl_sync(0xFFFFFFFFu, w, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&full_bar[s]);
+          const uint32_t st = sbase + (uint32_t)s * kWStageBytes + d_off;
+          mbar_arrive_expect_tx(fb, (uint32_t)d_chunks * 8192u);
+          for (int c = 0; c < d_chunks; ++c)
+            tma_load_2d(st + (uint32_t)c * 8192u, &tmD, dcol0 + c * 64, T.slot0 + kt * kWK, fb,
+                        pol);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+    }
+    if (lane == 0) {
+      __threadfence();
+      if (atomicAdd(&p.sched[1], 1) == (int)gridDim.x - 1) {
+        atomicExch(&p.sched[0], 0);
+        atomicExch(&p.sched[1], 0);
+        __threadfence();
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kWM, p.tile_n) | kIdescAMnMajor | kIdescBMnMajor;
+      uint32_t gk = 0, tc = 0, qi = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = (int)(qi % kWTileQ);
+        int t = -1;
+        if (mbar_wait(smem_u32(&tq_full[slot]), (qi / kWTileQ) & 1u, p.err, kErrWaitFull))
+          t = tile_q[slot];
+        mbar_arrive(smem_u32(&tq_empty[slot]));
+        ++qi;
+        if (t < 0) break;
+        WTile T;
+        wtile_at(p, t, T);
+        if (T.kept == 0) continue;  // zero tile: the epilogue writes it without TMEM
+        const uint32_t b = tc & 1u;
+        if (tc >= 2 && !mbar_wait(smem_u32(&tmem_empty_bar[b]), ((tc >> 1) - 1u) & 1u, p.err,
+                                  kErrWaitAccum))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * (uint32_t)kWN;
+        const int chunks = (T.kept + kWK - 1) / kWK;
+        for (int kt = 0; kt < chunks; ++kt, ++gk) {
+          const int s = (int)(gk % (uint32_t)p.stages);
+          const uint32_t u = gk / (uint32_t)p.stages;
+          if (!mbar_wait(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + (uint32_t)s * kWStageBytes;
+          const int rem = T.kept - kt * kWK;
+          const int ksub = rem >= kWK ? kWK / 16 : (rem + 15) / 16;
+          for (int kk = 0; kk < ksub; ++kk)
+            umma_bf16(d, sdesc_sw128_mn(st + (uint32_t)kk * 2048u),
+                      sdesc_sw128_mn(st + kWABytes + (uint32_t)kk * 2048u), idesc,
+                      (kt | kk) != 0);
+          umma_commit(smem_u32(&empty_bar[s]));
+        }
+        umma_commit(smem_u32(&tmem_full_bar[b]));  // also after an abort: tracks issued MMAs
+        ++tc;
+      }
+    }
+  } else if (warp < 2 + kWEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    // warp w reads TMEM lanes 32*(w%4)..+31 (output rows m0+32q..+31) and the
+    // 16-column chunks c0 = 16*half, +32, ...; each column store is 32
+    // consecutive floats.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint32_t tc = 0, qi = 0;
+    for (;;) {
+      const int t = pop_tile(qi, kErrWaitAccum);
+      if (t < 0) break;
+      WTile T;
+      wtile_at(p, t, T);
+      float* dst = p.out + ((size_t)T.e * p.n_total + T.n0) * p.m_total + T.m0 + q * 32 + lane;
+      if (T.kept == 0) {
+        for (int c = half * 16; c < p.tile_n; c += 32)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[(size_t)(c + j) * p.m_total] = 0.0f;
+        continue;
+      }
+      const uint32_t b = tc & 1u;
+      int w = 1;
+      if (lane == 0) w = mbar_wait(smem_u32(&tmem_full_bar[b]), (tc >> 1) & 1u, p.err, kErrWaitAccum);
+      ++tc;
+      if (!__shfl_sync(0xFFFFFFFFu, w, 0)) break;
+      tc_fence_after();
+      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + b * (uint32_t)kWN;
+      for (int c = half * 16; c < p.tile_n; c += 32) {
+        uint32_t v[16];
+        tmem_ld16(tl + (uint32_t)c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) dst[(size_t)(c + j) * p.m_total] = __uint_as_float(v[j]);
+      }
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar[b]));
+    }
+  } else {
+    // ------------------------------------------------------------ token-row gather
+    // Stage row r (slot slot0 + 64kt + r) of 64-feature chunk c holds
+    // act[t, col0 + 64c .. +63] for t = sorted_slot_ids[slot]: 16-byte unit j
+    // at c*8192 + r*128 + ((j ^ (r%8)) * 16). Slots past the kept count and
+    // sentinel tokens are zero-filled. Abort protocol as in the forward's
+    // gather: every thread meets the others at the named barrier of each tile.
+    const int gt = threadIdx.x - kWGatherWarp0 * 32;
+    const int units = g_chunks * 8;  // 16-byte units per slot row
+    uint32_t gk = 0, qi = 0;
+    for (;;) {
+      const int t = pop_tile(qi, kErrWaitFull);
+      if (t < 0) break;
+      WTile T;
+      wtile_at(p, t, T);
+      named_bar_sync_w(1, kWGatherThreads);
+      if (gather_abort) break;
+      const int gcol0 = p.a_gather ? T.m0 : T.n0;
+      const int chunks = (T.kept + kWK - 1) / kWK;
+      for (int kt = 0; kt < chunks; ++kt, ++gk) {
+        const int s = (int)(gk % (uint32_t)p.stages);
+        const uint32_t u = gk / (uint32_t)p.stages;
+        if (gather_abort) break;
+        if (gk >= (uint32_t)p.stages &&
+            !mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty)) {
+          gather_abort = 1;
+          break;
+        }
+        const uint32_t g = sbase + (uint32_t)s * kWStageBytes + g_off;
+        for (int idx = gt; idx < kWK * units; idx += kWGatherThreads) {
+          const int r = idx / units, cu = idx - r * units;
+          const int c = cu >> 3, j = cu & 7;
+          const int ks = kt * kWK + r;
+          const int tok = ks < T.kept ? p.sorted_slot_ids[T.slot0 + ks] : -1;
+          const bool valid = (unsigned)tok < (unsigned)p.act_rows;
+          const uint16_t* src =
+              p.act + (size_t)(valid ? tok : 0) * p.act_ld + gcol0 + c * 64 + j * 8;
+          cp_async_16(g + (uint32_t)c * 8192u + (uint32_t)r * 128u + ((uint32_t)(j ^ (r & 7)) << 4),
+                      src, valid ? 16u : 0u);
+        }
+        cp_async_commit();
+        if (gk >= (uint32_t)kWGatherDepth) {
+          cp_async_wait<kWGatherDepth>();
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&full_bar[(gk - kWGatherDepth) % (uint32_t)p.stages]));
+        }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (uint32_t j = gk > (uint32_t)kWGatherDepth ? gk - kWGatherDepth : 0u; j < gk; ++j)
+      mbar_arrive(smem_u32(&full_bar[j % (uint32_t)p.stages]));
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kWTmemCols);
+  }
+}
+
+int wgrad_sms(cudaError_t* err) {
+  static int sms[64] = {};
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && sms[dev] > 0) return sms[dev];
+  int n = 0;
+  if ((*err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return 0;
+  if ((*err = cudaFuncSetAttribute(moe_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kWSmemBudget)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (dev >= 0 && dev < 64) sms[dev] = n;
+  return n;
+}
+
+}  // namespace
+
+int launch_wgrad(const WgradArgs& a, cudaStream_t s) {
+  if (a.E <= 0) return 0;
+  WgradParams p{};
+  p.E = a.E;
+  p.bm = a.bm;
+  p.sorted_slot_ids = a.sorted_slot_ids;
+  p.kept_counts = a.kept_counts;
+  p.block_start = a.block_start;
+  p.sched = a.sched;
+  p.out = a.out;
+  p.err = a.err;
+  CUtensorMap tmD;
+  if (a.dw13) {
+    // M = h (x gathered), N = k over 2I (dPre rows)
+    p.a_gather = 1;
+    p.m_total = a.H;
+    p.n_total = 2 * a.I;
+    p.act = static_cast<const uint16_t*>(a.x);
+    p.act_ld = a.H;
+    if (!make_map(&tmD, a.slot_mat, (uint64_t)(2 * a.I), (uint64_t)a.s_max, 64, kWK)) return -1;
+  } else {
+    // M = i (aw rows), N = h (dY gathered)
+    p.a_gather = 0;
+    p.m_total = a.I;
+    p.n_total = a.H;
+    p.act = static_cast<const uint16_t*>(a.dy);
+    p.act_ld = a.H;
+    if (!make_map(&tmD, a.slot_mat, (uint64_t)a.I, (uint64_t)a.s_max, 64, kWK)) return -1;
+  }
+  p.act_rows = a.N;
+  p.tile_n = (p.n_total % kWN == 0) ? kWN : 128;
+  if (p.m_total % kWM != 0 || p.n_total % p.tile_n != 0) return -1;
+  p.m_tiles = p.m_total / kWM;
+  p.n_tiles = p.n_total / p.tile_n;
+  p.stages = (int)((kWSmemBudget - 1024u) / kWStageBytes);
+  if (p.stages > kWMaxStages) p.stages = kWMaxStages;
+  const size_t dyn = (size_t)p.stages * kWStageBytes + 1024;
+  cudaError_t err = cudaSuccess;
+  const int sms = wgrad_sms(&err);
+  if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
+  const int64_t tiles = (int64_t)p.E * p.m_tiles * p.n_tiles;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  moe_wgrad_kernel<<<grid, kWThreads, dyn, s>>>(tmD, p);
+  err = cudaGetLastError();
+  return err == cudaSuccess ? 1 : -(int)err;
+}
+
+}  // namespace moe

@@ -196,3 +196,55 @@ def check_combine_property(P: Problem, R: oracle.Routing) -> None:
         mag[m] += np.abs(p[m, k:k + 1] * o[tr[m, k]])
     # bf16 rounding of the output (half an ulp: 2^-8 relative) plus fp32 accumulation
     assert np.all(np.abs(y - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * mag + 1e-30)
+
+
+def assert_close_grad(got: np.ndarray, ref: np.ndarray, what: str) -> None:
+    """fp32 gradients of large magnitude: relative Frobenius <= 1e-2 and
+    max-abs <= 2e-2 * max(1, max|ref|)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    if ref.size == 0:
+        return
+    err = np.abs(got - ref).max()
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    bound = TOL_MAX_ABS * max(1.0, np.abs(ref).max())
+    assert rel <= TOL_REL_FRO and err <= bound, "%s: max-abs %.3g (bound %.3g) rel-fro %.3g" % (
+        what, err, bound, rel)
+
+
+class Backward:
+    """Training forward (saving the pre-activations) and the expert-path
+    backward of a Problem for a seeded dY, through the C ABI."""
+
+    def __init__(self, P: Problem, dy_std: float = 1.0):
+        w, dev = P.w, P.dev
+        N, H, E, I, K = w.n_tokens, w.hidden, w.n_experts, w.inter, w.top_k
+        S = max(moe.max_slots(P.cfg), 1)
+        self.P = P
+        self.dy_bits = synth.normal_bf16_bits(w.seed, synth.STREAM["dy"], 0, N * H, dy_std).reshape(N, H)
+        self.dy = bf16_dev(self.dy_bits, dev) if N > 0 else torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.preact = torch.full((S, 2 * I), float("nan"), **bf)
+        self.dx = torch.full((max(N, 1), H), float("nan"), **bf)
+        self.dw13 = torch.full((E, 2 * I, H), float("nan"), dtype=torch.float32, device=dev)
+        self.dw2 = torch.full((E, H, I), float("nan"), dtype=torch.float32, device=dev)
+        self.dprob = torch.full((max(N, 1), K), float("nan"), dtype=torch.float32, device=dev)
+        self.ws = moe.alloc_backward_workspace(P.cfg, dev)
+        self.ws.fill_(0xFF)  # NaN bit patterns where a kernel reads before writing
+
+    def run(self) -> None:
+        P = self.P
+        moe.route_align(P.cfg, P.x, P.wr_d, P.bias_d, P.routes, P.ws)
+        moe.ffn_forward_train(P.cfg, P.routes, P.x, P.w13, P.w2, P.h, P.o, self.preact)
+        moe.combine(P.cfg, P.routes, P.o, P.y)
+        moe.ffn_backward(P.cfg, P.routes, P.x, P.w13, P.w2, self.preact, self.dy, self.dx,
+                         self.dw13, self.dw2, self.dprob, self.ws)
+        torch.cuda.synchronize()
+        assert moe.device_error() == 0
+
+    def weight_grads(self, e: int):
+        """(dWd [I,H], dWg [H,I], dWu [H,I]) of expert e in the oracle's layout."""
+        I = self.P.w.inter
+        d13 = self.dw13[e].cpu().numpy()
+        return self.dw2[e].cpu().numpy().T, d13[:I].T, d13[I:].T
