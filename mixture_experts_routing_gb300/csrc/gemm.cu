@@ -257,10 +257,6 @@ __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const
     p.part[(row0 + m) * (size_t)(I / 32) + T.f * 4 + q] = dp[0];
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
@@ -270,8 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t tmem_full_bar;
   __shared__ __align__(8) uint64_t tmem_empty_bar;
   __shared__ uint32_t tmem_base_s;
-  __shared__ int32_t rows_s[kMaxTileN];
-  __shared__ volatile int gather_abort;  // set by a gatherer whose wait ran out
   __shared__ int32_t tpre[kMaxExperts + 1];
   __shared__ int32_t ttn[kMaxExperts];
   __shared__ int32_t tile_q[kTileQ];
@@ -283,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = (raw + 1023u) & ~1023u;
 
   if (threadIdx.x == 0) {
-    gather_abort = 0;
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), p.gather_b ? 1 + kGatherThreads : 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
@@ -310,13 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Pops the next tile id (lane 0 waits, the warp gets the value); -1 ends.
   auto pop_tile = [&](uint32_t& qi, uint32_t code) -> int {
     const int slot = (int)(qi % kTileQ);
-    int t = -1;
-    if (lane == 0) {
-      if (mbar_wait(smem_u32(&tq_full[slot]), (qi / kTileQ) & 1u, p.err, code)) t = tile_q[slot];
-      mbar_arrive(smem_u32(&tq_empty[slot]));
-    }
+    const bool ok = mbar_wait_warp(smem_u32(&tq_full[slot]), (qi / kTileQ) & 1u, p.err, code);
+    const int t = ok ? tile_q[slot] : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&tq_empty[slot]));
     ++qi;
-    return __shfl_sync(0xFFFFFFFFu, t, 0);
+    return t;
   };
 
   if (warp == 0) {
@@ -327,14 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_x = policy_evict_last();
     uint32_t gk = 0;  // k-steps issued by this CTA, across tiles
     for (uint32_t qi = 0;; ++qi) {
+      const int slot = (int)(qi % kTileQ);
+      const bool free_ok =
+          qi < (uint32_t)kTileQ ||
+          mbar_wait_warp(smem_u32(&tq_empty[slot]), ((qi / kTileQ) - 1u) & 1u, p.err, kErrWaitEmpty);
       int t = -1;
       if (lane == 0) {
-        t = atomicAdd(&p.sched[0], 1);
+        if (free_ok) t = atomicAdd(&p.sched[0], 1);
         if (t >= n_tiles) t = -1;
-        const int slot = (int)(qi % kTileQ);
-        if (qi >= (uint32_t)kTileQ &&
-            !mbar_wait(smem_u32(&tq_empty[slot]), ((qi / kTileQ) - 1u) & 1u, p.err, kErrWaitEmpty))
-          t = -1;
         tile_q[slot] = t;
         mbar_arrive(smem_u32(&tq_full[slot]));
       }
@@ -354,10 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
         const int s = (int)(gk % (uint32_t)p.stages);
         const uint32_t u = gk / (uint32_t)p.stages;
-        int w = 1;
-        if (lane == 0 && gk >= (uint32_t)p.stages)
-          w = mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty);
-        if (!__shfl_sync(0xFFFFFFFFu, w, 0)) {
+        if (gk >= (uint32_t)p.stages &&
+            !mbar_wait_warp(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty)) {
           ok = false;
           break;
         }
@@ -398,37 +388,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- UMMA issuer
-    if (lane == 0) {
-      uint32_t gk = 0, tc = 0, qi = 0;
+    // The whole warp walks the tiles and takes the waits; lane 0 issues.
+    uint32_t gk = 0, tc = 0, qi = 0;
+    for (;;) {
+      const int t = pop_tile(qi, kErrWaitFull);
+      if (t < 0) break;
+      Tile T;
+      tile_at(p, tpre, ttn, t, T);
+      if (tc > 0 && !mbar_wait_warp(smem_u32(&tmem_empty_bar), (tc - 1) & 1u, p.err, kErrWaitAccum))
+        break;
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(kTileM, T.n_eff) | (p.a_mn ? kIdescAMnMajor : 0u);
+      // one UMMA k-step (16 elements) advances 32 bytes along a K-major row,
+      // or 16 rows of 128 bytes in an MN-major tile
+      const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
       bool ok = true;
-      while (ok) {
-        const int slot = (int)(qi % kTileQ);
-        int t = -1;
-        if (mbar_wait(smem_u32(&tq_full[slot]), (qi / kTileQ) & 1u, p.err, kErrWaitFull))
-          t = tile_q[slot];
-        mbar_arrive(smem_u32(&tq_empty[slot]));
-        ++qi;
-        if (t < 0) break;
-        Tile T;
-        tile_at(p, tpre, ttn, t, T);
-        if (tc > 0 &&
-            !mbar_wait(smem_u32(&tmem_empty_bar), (tc - 1) & 1u, p.err, kErrWaitAccum)) {
+      for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
+        const int s = (int)(gk % (uint32_t)p.stages);
+        const uint32_t u = gk / (uint32_t)p.stages;
+        if (!mbar_wait_warp(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16_f32(kTileM, T.n_eff) | (p.a_mn ? kIdescAMnMajor : 0u);
-        // one UMMA k-step (16 elements) advances 32 bytes along a K-major row,
-        // or 16 rows of 128 bytes in an MN-major tile
-        const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
-        for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
-          const int s = (int)(gk % (uint32_t)p.stages);
-          const uint32_t u = gk / (uint32_t)p.stages;
-          if (!mbar_wait(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (lane == 0) {
           const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -444,9 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit(smem_u32(&empty_bar[s]));
         }
-        umma_commit(smem_u32(&tmem_full_bar));  // also after an abort: tracks issued MMAs
-        ++tc;
+        __syncwarp();
       }
+      if (lane == 0) umma_commit(smem_u32(&tmem_full_bar));  // also after an abort
+      __syncwarp();
+      ++tc;
+      if (!ok) break;
     }
   } else if (warp < 2 + kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
@@ -460,12 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t < 0) break;
       Tile T;
       tile_at(p, tpre, ttn, t, T);
-      // lane 0 waits for the whole warp, so the warp-collective TMEM loads
-      // below are reached by all lanes or by none
-      int w = 1;
-      if (lane == 0) w = mbar_wait(smem_u32(&tmem_full_bar), tc & 1u, p.err, kErrWaitAccum);
+      // the warp's vote: the warp-collective TMEM loads below are reached by
+      // all lanes or by none
+      const bool w = mbar_wait_warp(smem_u32(&tmem_full_bar), tc & 1u, p.err, kErrWaitAccum);
       ++tc;
-      if (!__shfl_sync(0xFFFFFFFFu, w, 0)) break;
+      if (!w) break;
       tc_fence_after();
       const int feat0 = T.f * p.f_rows + q * 32;  // first feature of this lane quarter
       for (int c0 = half * 16; c0 < T.n_eff; c0 += 32) {
@@ -510,47 +495,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (p.gather_b) {
     // ---------------------------------------------------------------- B row gather
-    // Row r of a stage holds x[rows_s[r], kx .. kx+63]: 16-byte chunk c at
-    // r*128 + ((c ^ (r%8)) * 16), the 128-byte swizzle the UMMA descriptor
-    // expects; sentinel rows are zero-filled. Each thread keeps kGatherDepth
-    // copy groups in flight, then makes a stage's writes visible to the tensor
-    // core's async proxy and arrives.
-    // Every gather thread walks the same tiles and meets the others at the
-    // named barrier of each tile; a thread whose wait runs out raises
-    // gather_abort, and all threads read it right after the next barrier, so
-    // they leave together and none is left waiting at a barrier.
+    // Row r of a stage holds act[sorted_slot_ids[slot0 + r], kx .. kx+63]:
+    // 16-byte chunk c at r*128 + ((c ^ (r%8)) * 16), the 128-byte swizzle the
+    // UMMA descriptor expects; sentinel rows are zero-filled. Thread gt copies
+    // chunk c = gt%8 of rows r = gt/8 + 16i (i < n_eff/16) of every stage; it
+    // looks its rows' token offsets up once per tile, so each copy is one
+    // address add and one cp.async. Each thread keeps kGatherDepth copy groups
+    // in flight, then makes a stage's writes visible to the tensor core's async
+    // proxy and arrives. Waits end in a warp vote, so a warp leaves together
+    // when one runs out.
     const int gt = threadIdx.x - kGatherWarp0 * 32;
+    const int c = gt & 7, rb = gt >> 3;
+    const uint32_t dst0 = (uint32_t)rb * 128u + ((uint32_t)(c ^ (rb & 7)) << 4);
     uint32_t gk = 0, qi = 0;
-    for (;;) {
+    bool ok = true;
+    while (ok) {
       const int t = pop_tile(qi, kErrWaitFull);
       if (t < 0) break;
       Tile T;
       tile_at(p, tpre, ttn, t, T);
-      named_bar_sync(1, kGatherThreads);  // the previous tile's rows_s is no longer read
-      if (gather_abort) break;
-      for (int i = gt; i < T.n_eff; i += kGatherThreads)
-        rows_s[i] = p.sorted_slot_ids[T.slot0 + i];
-      named_bar_sync(1, kGatherThreads);
-      const int nchunks = T.n_eff * 8;
+      const int n_i = T.n_eff >> 4;
+      uint32_t off[16];
+      uint32_t vmask = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        off[i] = 0;
+        if (i < n_i) {
+          const int tok = p.sorted_slot_ids[T.slot0 + rb + 16 * i];
+          if ((unsigned)tok < (unsigned)p.act_rows) {
+            off[i] = (uint32_t)tok * (uint32_t)p.act_ld + (uint32_t)(c * 8);
+            vmask |= 1u << i;
+          }
+        }
+      }
       for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
         const int s = (int)(gk % (uint32_t)p.stages);
         const uint32_t u = gk / (uint32_t)p.stages;
-        if (gather_abort) break;
         if (gk >= (uint32_t)p.stages &&
-            !mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty)) {
-          gather_abort = 1;
+            !mbar_wait_warp(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty)) {
+          ok = false;
           break;
         }
-        const uint32_t b = sbase + (uint32_t)s * p.stage_bytes + p.b_off;
-        const int kx = kt * kBK;
-        for (int j = gt; j < nchunks; j += kGatherThreads) {
-          const int r = j >> 3, c = j & 7;
-          const int tok = rows_s[r];
-          const bool valid = (unsigned)tok < (unsigned)p.act_rows;
-          const uint16_t* src = p.act + (size_t)(valid ? tok : 0) * p.act_ld + kx + c * 8;
-          cp_async_16(b + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4), src,
-                      valid ? 16u : 0u);
-        }
+        const uint32_t b = sbase + (uint32_t)s * p.stage_bytes + p.b_off + dst0;
+        const uint16_t* src = p.act + kt * kBK;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < n_i) cp_async_16(b + (uint32_t)i * 2048u, src + off[i], ((vmask >> i) & 1u) << 4);
         cp_async_commit();
         if (gk >= (uint32_t)kGatherDepth) {
           cp_async_wait<kGatherDepth>();

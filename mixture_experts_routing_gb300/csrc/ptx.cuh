@@ -64,6 +64,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   }
 }
 
+// mbar_wait taken by every lane of a warp, with the warp's vote as the
+// result, so the warp takes one path afterwards. (A wait taken by one lane
+// while the others stand at a warp-synchronous shuffle ran the row-gather
+// loops up to 1.8x slower.)
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t* err,
+                                               uint32_t code) {
+  const bool ok = mbar_wait(bar, parity, err, code);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

@@ -81,10 +81,6 @@ __device__ __forceinline__ void wtile_at(const WgradParams& p, int t, WTile& T) 
   T.slot0 = p.block_start[T.e] * p.bm;
 }
 
-__device__ __forceinline__ void named_bar_sync_w(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 __global__ void __launch_bounds__(kWThreads, 1)
     moe_wgrad_kernel(const __grid_constant__ CUtensorMap tmD, const WgradParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -93,7 +89,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
   __shared__ __align__(8) uint64_t tmem_full_bar[2];
   __shared__ __align__(8) uint64_t tmem_empty_bar[2];
   __shared__ uint32_t tmem_base_s;
-  __shared__ volatile int gather_abort;
   __shared__ int32_t tile_q[kWTileQ];
   __shared__ __align__(8) uint64_t tq_full[kWTileQ];
   __shared__ __align__(8) uint64_t tq_empty[kWTileQ];
@@ -108,7 +103,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const int g_chunks = p.a_gather ? kWM / 64 : p.tile_n / 64;
 
   if (threadIdx.x == 0) {
-    gather_abort = 0;
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1 + kWGatherThreads);
       mbar_init(smem_u32(&empty_bar[s]), 1);
@@ -132,13 +126,12 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
   auto pop_tile = [&](uint32_t& qi, uint32_t code) -> int {
     const int slot = (int)(qi % kWTileQ);
-    int t = -1;
-    if (lane == 0) {
-      if (mbar_wait(smem_u32(&tq_full[slot]), (qi / kWTileQ) & 1u, p.err, code)) t = tile_q[slot];
-      mbar_arrive(smem_u32(&tq_empty[slot]));
-    }
+    const bool ok = mbar_wait_warp(smem_u32(&tq_full[slot]), (qi / kWTileQ) & 1u, p.err, code);
+    const int t = ok ? tile_q[slot] : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&tq_empty[slot]));
     ++qi;
-    return __shfl_sync(0xFFFFFFFFu, t, 0);
+    return t;
   };
 
   if (warp == 0) {
@@ -146,14 +139,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const uint64_t pol = policy_evict_last();
     uint32_t gk = 0;
     for (uint32_t qi = 0;; ++qi) {
+      const int slot = (int)(qi % kWTileQ);
+      const bool free_ok =
+          qi < (uint32_t)kWTileQ ||
+          mbar_wait_warp(smem_u32(&tq_empty[slot]), ((qi / kWTileQ) - 1u) & 1u, p.err, kErrWaitEmpty);
       int t = -1;
       if (lane == 0) {
-        t = atomicAdd(&p.sched[0], 1);
+        if (free_ok) t = atomicAdd(&p.sched[0], 1);
         if (t >= n_tiles) t = -1;
-        const int slot = (int)(qi % kWTileQ);
-        if (qi >= (uint32_t)kWTileQ &&
-            !mbar_wait(smem_u32(&tq_empty[slot]), ((qi / kWTileQ) - 1u) & 1u, p.err, kErrWaitEmpty))
-          t = -1;
         tile_q[slot] = t;
         mbar_arrive(smem_u32(&tq_full[slot]));
       }
@@ -167,10 +160,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
       for (int kt = 0; kt < chunks; ++kt, ++gk) {
         const int s = (int)(gk % (uint32_t)p.stages);
         const uint32_t u = gk / (uint32_t)p.stages;
-        int w = 1;
-        if (lane == 0 && gk >= (uint32_t)p.stages)
-          w = mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty);
-        if (!__shfl_sync(0xFFFFFFFFu, w, 0)) {
+        if (gk >= (uint32_t)p.stages &&
+            !mbar_wait_warp(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty)) {
           ok = false;
           break;
         }
@@ -196,36 +187,32 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kWM, p.tile_n) | kIdescAMnMajor | kIdescBMnMajor;
-      uint32_t gk = 0, tc = 0, qi = 0;
+    // The whole warp walks the tiles and takes the waits; lane 0 issues.
+    const uint32_t idesc = idesc_bf16_f32(kWM, p.tile_n) | kIdescAMnMajor | kIdescBMnMajor;
+    uint32_t gk = 0, tc = 0, qi = 0;
+    for (;;) {
+      const int t = pop_tile(qi, kErrWaitFull);
+      if (t < 0) break;
+      WTile T;
+      wtile_at(p, t, T);
+      if (T.kept == 0) continue;  // zero tile: the epilogue writes it without TMEM
+      const uint32_t b = tc & 1u;
+      if (tc >= 2 && !mbar_wait_warp(smem_u32(&tmem_empty_bar[b]), ((tc >> 1) - 1u) & 1u, p.err,
+                                     kErrWaitAccum))
+        break;
+      tc_fence_after();
+      const uint32_t d = tmem + b * (uint32_t)kWN;
+      const int chunks = (T.kept + kWK - 1) / kWK;
       bool ok = true;
-      while (ok) {
-        const int slot = (int)(qi % kWTileQ);
-        int t = -1;
-        if (mbar_wait(smem_u32(&tq_full[slot]), (qi / kWTileQ) & 1u, p.err, kErrWaitFull))
-          t = tile_q[slot];
-        mbar_arrive(smem_u32(&tq_empty[slot]));
-        ++qi;
-        if (t < 0) break;
-        WTile T;
-        wtile_at(p, t, T);
-        if (T.kept == 0) continue;  // zero tile: the epilogue writes it without TMEM
-        const uint32_t b = tc & 1u;
-        if (tc >= 2 && !mbar_wait(smem_u32(&tmem_empty_bar[b]), ((tc >> 1) - 1u) & 1u, p.err,
-                                  kErrWaitAccum))
+      for (int kt = 0; kt < chunks; ++kt, ++gk) {
+        const int s = (int)(gk % (uint32_t)p.stages);
+        const uint32_t u = gk / (uint32_t)p.stages;
+        if (!mbar_wait_warp(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) {
+          ok = false;
           break;
+        }
         tc_fence_after();
-        const uint32_t d = tmem + b * (uint32_t)kWN;
-        const int chunks = (T.kept + kWK - 1) / kWK;
-        for (int kt = 0; kt < chunks; ++kt, ++gk) {
-          const int s = (int)(gk % (uint32_t)p.stages);
-          const uint32_t u = gk / (uint32_t)p.stages;
-          if (!mbar_wait(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (lane == 0) {
           const uint32_t st = sbase + (uint32_t)s * kWStageBytes;
           const int rem = T.kept - kt * kWK;
           const int ksub = rem >= kWK ? kWK / 16 : (rem + 15) / 16;
@@ -235,9 +222,12 @@ __global__ void __launch_bounds__(kWThreads, 1)
                       (kt | kk) != 0);
           umma_commit(smem_u32(&empty_bar[s]));
         }
-        umma_commit(smem_u32(&tmem_full_bar[b]));  // also after an abort: tracks issued MMAs
-        ++tc;
+        __syncwarp();
       }
+      if (lane == 0) umma_commit(smem_u32(&tmem_full_bar[b]));  // also after an abort
+      __syncwarp();
+      ++tc;
+      if (!ok) break;
     }
   } else if (warp < 2 + kWEpiWarps) {
     // ------------------------------------------------------------ epilogue
@@ -260,10 +250,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
         continue;
       }
       const uint32_t b = tc & 1u;
-      int w = 1;
-      if (lane == 0) w = mbar_wait(smem_u32(&tmem_full_bar[b]), (tc >> 1) & 1u, p.err, kErrWaitAccum);
+      const bool w =
+          mbar_wait_warp(smem_u32(&tmem_full_bar[b]), (tc >> 1) & 1u, p.err, kErrWaitAccum);
       ++tc;
-      if (!__shfl_sync(0xFFFFFFFFu, w, 0)) break;
+      if (!w) break;
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + b * (uint32_t)kWN;
       for (int c = half * 16; c < p.tile_n; c += 32) {
@@ -281,40 +271,54 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // Stage row r (slot slot0 + 64kt + r) of 64-feature chunk c holds
     // act[t, col0 + 64c .. +63] for t = sorted_slot_ids[slot]: 16-byte unit j
     // at c*8192 + r*128 + ((j ^ (r%8)) * 16). Slots past the kept count and
-    // sentinel tokens are zero-filled. Abort protocol as in the forward's
-    // gather: every thread meets the others at the named barrier of each tile.
-    const int gt = threadIdx.x - kWGatherWarp0 * 32;
-    const int units = g_chunks * 8;  // 16-byte units per slot row
+    // sentinel tokens are zero-filled. A warp copies whole rows (lane = 16-byte
+    // unit; rpi = 32/units rows per instruction): warp g owns rows
+    // rpi*g + sub + 4*rpi*i, and lane j < 16 holds the token of the warp's j-th
+    // row, loaded one stage ahead and broadcast with a shuffle. Waits end in a
+    // warp vote, so a warp leaves together when one runs out.
+    const int gw = warp - kWGatherWarp0;
+    const int units = g_chunks * 8;     // 16-byte units per row: 16 or 32
+    const int rpi = 32 / units;         // rows per warp instruction: 2 or 1
+    const int sub = lane / units;
+    const int uc = lane % units;
+    const int c = uc >> 3, jj = uc & 7;
+    const int n_ins = 16 / rpi;         // instructions per stage
+    const int my_row = rpi * gw + (lane % rpi) + 4 * rpi * (lane / rpi);  // lane < 16
     uint32_t gk = 0, qi = 0;
-    for (;;) {
+    bool ok = true;
+    while (ok) {
       const int t = pop_tile(qi, kErrWaitFull);
       if (t < 0) break;
       WTile T;
       wtile_at(p, t, T);
-      named_bar_sync_w(1, kWGatherThreads);
-      if (gather_abort) break;
-      const int gcol0 = p.a_gather ? T.m0 : T.n0;
+      const int gcol0 = (p.a_gather ? T.m0 : T.n0) + c * 64 + jj * 8;
       const int chunks = (T.kept + kWK - 1) / kWK;
+      auto token_of = [&](int kt) -> int {
+        const int ks = kt * kWK + my_row;
+        return (lane < 16 && kt < chunks && ks < T.kept) ? p.sorted_slot_ids[T.slot0 + ks] : -1;
+      };
+      int nxt = token_of(0);
       for (int kt = 0; kt < chunks; ++kt, ++gk) {
+        const int cur = nxt;
+        nxt = token_of(kt + 1);
         const int s = (int)(gk % (uint32_t)p.stages);
         const uint32_t u = gk / (uint32_t)p.stages;
-        if (gather_abort) break;
         if (gk >= (uint32_t)p.stages &&
-            !mbar_wait(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty)) {
-          gather_abort = 1;
+            !mbar_wait_warp(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty)) {
+          ok = false;
           break;
         }
-        const uint32_t g = sbase + (uint32_t)s * kWStageBytes + g_off;
-        for (int idx = gt; idx < kWK * units; idx += kWGatherThreads) {
-          const int r = idx / units, cu = idx - r * units;
-          const int c = cu >> 3, j = cu & 7;
-          const int ks = kt * kWK + r;
-          const int tok = ks < T.kept ? p.sorted_slot_ids[T.slot0 + ks] : -1;
-          const bool valid = (unsigned)tok < (unsigned)p.act_rows;
-          const uint16_t* src =
-              p.act + (size_t)(valid ? tok : 0) * p.act_ld + gcol0 + c * 64 + j * 8;
-          cp_async_16(g + (uint32_t)c * 8192u + (uint32_t)r * 128u + ((uint32_t)(j ^ (r & 7)) << 4),
-                      src, valid ? 16u : 0u);
+        const uint32_t g = sbase + (uint32_t)s * kWStageBytes + g_off + (uint32_t)c * 8192u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (i < n_ins) {
+            const int tok = __shfl_sync(0xFFFFFFFFu, cur, i * rpi + sub);
+            const int r = rpi * gw + sub + 4 * rpi * i;
+            const bool valid = (unsigned)tok < (unsigned)p.act_rows;
+            const uint16_t* src = p.act + (size_t)(valid ? tok : 0) * p.act_ld + gcol0;
+            cp_async_16(g + (uint32_t)r * 128u + ((uint32_t)(jj ^ (r & 7)) << 4), src,
+                        valid ? 16u : 0u);
+          }
         }
         cp_async_commit();
         if (gk >= (uint32_t)kWGatherDepth) {
