@@ -61,7 +61,6 @@ constexpr uint32_t kATileBytes = kTileM * kBK * 2;  // 16 KiB
 // memory the CTA stays under the 227 KB per-block limit
 constexpr uint32_t kSmemBudget = 223 * 1024;
 constexpr int kGatherThreads = 128;  // warps 10-13
-constexpr int kGatherDepth = 2;      // cp.async groups in flight per gather thread
 constexpr int kStageRowElems = 32;   // epilogue staging row: 32 features (bf16)
 constexpr uint32_t kEpiStageBytes = kEpiWarps * 16u * kStageRowElems * 2u;  // per warp 16 rows
 constexpr int kTileQ = 4;            // depth of the tile-id queue
@@ -412,6 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         if (lane == 0) {
+          // B rows written by cp.async (generic proxy) are read by the tensor core
+          if (p.gather_b) fence_proxy_async_smem();
           const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -500,10 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // UMMA descriptor expects; sentinel rows are zero-filled. Thread gt copies
     // chunk c = gt%8 of rows r = gt/8 + 16i (i < n_eff/16) of every stage; it
     // looks its rows' token offsets up once per tile, so each copy is one
-    // address add and one cp.async. Each thread keeps kGatherDepth copy groups
-    // in flight, then makes a stage's writes visible to the tensor core's async
-    // proxy and arrives. Waits end in a warp vote, so a warp leaves together
-    // when one runs out.
+    // address add and one cp.async. A thread does not wait for its copies: the
+    // stage's full barrier receives its arrival when they complete
+    // (cp.async.mbarrier.arrive.noinc), so the gather runs as many stages ahead
+    // as the ring holds; the UMMA thread fences the generic-proxy writes
+    // against its async-proxy operand reads after the barrier. Waits end in a
+    // warp vote, so a warp leaves together when one runs out.
     const int gt = threadIdx.x - kGatherWarp0 * 32;
     const int c = gt & 7, rb = gt >> 3;
     const uint32_t dst0 = (uint32_t)rb * 128u + ((uint32_t)(c ^ (rb & 7)) << 4);
@@ -541,18 +544,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           if (i < n_i) cp_async_16(b + (uint32_t)i * 2048u, src + off[i], ((vmask >> i) & 1u) << 4);
-        cp_async_commit();
-        if (gk >= (uint32_t)kGatherDepth) {
-          cp_async_wait<kGatherDepth>();
-          fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&full_bar[(gk - kGatherDepth) % (uint32_t)p.stages]));
-        }
+        cp_async_mbar_arrive_noinc(smem_u32(&full_bar[s]));
       }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (uint32_t j = gk > (uint32_t)kGatherDepth ? gk - kGatherDepth : 0u; j < gk; ++j)
-      mbar_arrive(smem_u32(&full_bar[j % (uint32_t)p.stages]));
+    cp_async_wait_all();
   }
   tc_fence_before();
   __syncthreads();

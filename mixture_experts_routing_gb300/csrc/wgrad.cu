@@ -43,7 +43,6 @@ constexpr int kWThreads = 448;
 constexpr int kWEpiWarps = 8;         // warps 2-9
 constexpr int kWGatherWarp0 = 10;     // warps 10-13
 constexpr int kWGatherThreads = 128;
-constexpr int kWGatherDepth = 2;
 constexpr int kWMaxStages = 8;
 constexpr uint32_t kWABytes = kWM * kWK * 2;  // 16 KiB: 2 chunks of 64 features
 constexpr uint32_t kWBBytes = kWN * kWK * 2;  // 32 KiB: 4 chunks
@@ -213,6 +212,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
         tc_fence_after();
         if (lane == 0) {
+          fence_proxy_async_smem();  // gathered rows: cp.async (generic proxy) writes
           const uint32_t st = sbase + (uint32_t)s * kWStageBytes;
           const int rem = T.kept - kt * kWK;
           const int ksub = rem >= kWK ? kWK / 16 : (rem + 15) / 16;
@@ -274,8 +274,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // sentinel tokens are zero-filled. A warp copies whole rows (lane = 16-byte
     // unit; rpi = 32/units rows per instruction): warp g owns rows
     // rpi*g + sub + 4*rpi*i, and lane j < 16 holds the token of the warp's j-th
-    // row, loaded one stage ahead and broadcast with a shuffle. Waits end in a
-    // warp vote, so a warp leaves together when one runs out.
+    // row, loaded one stage ahead and broadcast with a shuffle. The full
+    // barrier receives each thread's arrival when its copies complete
+    // (cp.async.mbarrier.arrive.noinc); the UMMA thread fences them against
+    // its async-proxy reads. Waits end in a warp vote, so a warp leaves
+    // together when one runs out.
     const int gw = warp - kWGatherWarp0;
     const int units = g_chunks * 8;     // 16-byte units per row: 16 or 32
     const int rpi = 32 / units;         // rows per warp instruction: 2 or 1
@@ -320,18 +323,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         valid ? 16u : 0u);
           }
         }
-        cp_async_commit();
-        if (gk >= (uint32_t)kWGatherDepth) {
-          cp_async_wait<kWGatherDepth>();
-          fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&full_bar[(gk - kWGatherDepth) % (uint32_t)p.stages]));
-        }
+        cp_async_mbar_arrive_noinc(smem_u32(&full_bar[s]));
       }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (uint32_t j = gk > (uint32_t)kWGatherDepth ? gk - kWGatherDepth : 0u; j < gk; ++j)
-      mbar_arrive(smem_u32(&full_bar[j % (uint32_t)p.stages]));
+    cp_async_wait_all();
   }
   tc_fence_before();
   __syncthreads();
