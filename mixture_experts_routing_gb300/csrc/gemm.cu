@@ -50,7 +50,7 @@ namespace {
 
 constexpr int kBK = 64;           // contraction elements per stage (128 B of bf16)
 constexpr int kTileM = 128;       // weight rows per accumulator (UMMA M)
-constexpr int kMaxTileN = 256;    // slots per tile (UMMA N)
+constexpr int kMaxTileN = 256;    // slots per tile (UMMA N), at most
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 448;
 constexpr int kEpiWarps = 8;         // warps 2-9
@@ -64,12 +64,16 @@ constexpr int kGatherThreads = 128;  // warps 10-13
 constexpr int kStageRowElems = 32;   // epilogue staging row: 32 features (bf16)
 constexpr uint32_t kEpiStageBytes = kEpiWarps * 16u * kStageRowElems * 2u;  // per warp 16 rows
 constexpr int kTileQ = 4;            // depth of the tile-id queue
+constexpr uint32_t kPsBytes = kEpiWarps * 16 * 4;  // FC2 dgrad: 16 p' values per epilogue warp
 
 struct GemmParams {
-  int mode;              // GemmMode
-  int gather_b;          // B rows gathered from act by sorted_slot_ids (FC1, dgrad of FC2)
-  int a_mn;              // A read MN-major (the dgrads: the packed weights used transposed)
-  int n_acc;
+  int n_acc;             // accumulators per tile: FC1 gate + up; otherwise two 128-feature
+                         // tiles (the last feature tile may hold one: Tile::nacc)
+  int pair_feats;        // the two accumulators are feature tiles (not gate/up)
+  int m_total;           // features of the output (ragged last tile when pair_feats)
+  int max_tn;            // slots per tile, at most (128 or 256)
+  uint32_t acc_off;      // TMEM columns between a tile's two accumulators
+  uint32_t buf_stride;   // TMEM columns of one accumulator buffer
   int k_tiles;
   int a_rows_per_expert;
   int a_second_off;
@@ -82,6 +86,8 @@ struct GemmParams {
   uint32_t stage_bytes;
   uint32_t b_off;
   uint32_t epi_off;      // offset of the epilogue staging buffer from the aligned smem base
+  uint32_t ps_off;       // FC2 dgrad: offset of the epilogue warps' p' slots
+  int n_buf;             // accumulators in flight: 2 when a tile uses 256 TMEM columns, else 1
   const uint16_t* act;   // FC1: x [act_rows, act_ld] for the row gather
   int act_ld;
   int act_rows;
@@ -92,20 +98,20 @@ struct GemmParams {
   uint16_t* out;
   uint16_t* out2;        // FC1: pre-activations [S,2I] or null; FC2 dgrad: p'*a [S,I]
   const uint16_t* aux;   // FC2 dgrad: pre-activations [S,2I]
-  const int32_t* slot_route;  // FC2 dgrad: route of each slot, -1 for padding
-  const float* topk_p;        // FC2 dgrad: p' per route
+  const float* slot_prob;     // FC2 dgrad: p' of each slot's route, 0 for padding
   float* part;                // FC2 dgrad: dprob partials [S, I/32]
   int inter;                  // I
   uint32_t* err;
 };
 
 struct Tile {
-  int e, f, rows, n_eff, slot0;
+  int e, f, rows, n_eff, slot0, nacc;
 };
 
 // Dense tile list: expert e owns tiles [tpre[e], tpre[e+1]); each of its
 // ntt = ceil(kept/256) slot tiles holds ttn[e] slots (kept split evenly,
-// rounded up to 16), times f_tiles feature tiles. Built once per CTA.
+// rounded up to 16, at most max_tn), times f_tiles feature tiles. Built once
+// per CTA.
 __device__ __forceinline__ void build_tile_list(const GemmParams& p, int32_t* tpre, int32_t* ttn,
                                                 int lane) {
   int run = 0;
@@ -114,7 +120,7 @@ __device__ __forceinline__ void build_tile_list(const GemmParams& p, int32_t* tp
     int tiles = 0;
     if (e < p.E) {
       const int kept = max(p.kept_counts[e], 0);
-      const int ntt = (kept + kMaxTileN - 1) / kMaxTileN;
+      const int ntt = (kept + p.max_tn - 1) / p.max_tn;
       ttn[e] = ntt ? ((kept + ntt - 1) / ntt + 15) & ~15 : 0;
       tiles = ntt * p.f_tiles;
     }
@@ -142,12 +148,13 @@ __device__ __forceinline__ void tile_at(const GemmParams& p, const int32_t* tpre
   const int local = t - tpre[lo];
   const int tn = ttn[lo];
   const int kept = p.kept_counts[lo];
-  const int ntt = (kept + kMaxTileN - 1) / kMaxTileN;
+  const int ntt = (kept + p.max_tn - 1) / p.max_tn;
   const int jt = local % ntt;
   T.f = local / ntt;
   T.rows = min(tn, kept - jt * tn);
   T.n_eff = (T.rows + 15) & ~15;
   T.slot0 = p.block_start[lo] * p.bm + jt * tn;
+  T.nacc = (p.pair_feats && T.f * p.f_rows + kTileM >= p.m_total) ? 1 : p.n_acc;
 }
 
 __device__ __forceinline__ uint32_t bf16_bits(float v) {
@@ -185,46 +192,68 @@ __device__ __forceinline__ void store_rows16(uint32_t stg_u, int lane, const flo
   __syncwarp();
 }
 
+// Pre-activations of 16 slots (c0..c0+15 of the tile) for this lane's feature:
+// gate in the low half, up in the high half of each word; 0 past the kept rows.
+__device__ __forceinline__ void load_preact16(const GemmParams& p, const Tile& T, int c0, int f,
+                                              uint32_t (&gu)[16]) {
+  const int ld2 = 2 * p.inter;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    gu[j] = 0u;
+    if (c0 + j < T.rows) {
+      const uint16_t* r = p.aux + (size_t)(T.slot0 + c0 + j) * ld2 + f;
+      gu[j] = (uint32_t)r[0] | ((uint32_t)r[p.inter] << 16);
+    }
+  }
+}
+
+// p' of slot c0 + lane of the tile for lanes 0..15 (0 past the kept rows).
+__device__ __forceinline__ float load_slot_prob(const GemmParams& p, const Tile& T, int c0, int lane) {
+  return (lane < 16 && c0 + lane < T.rows) ? p.slot_prob[T.slot0 + c0 + lane] : 0.0f;
+}
+
 // Epilogue of the FC2 dgrad for 16 slots (registers) x 32 features (lanes).
 // dA0[s,i] = dY[t_s] . W_down[e][i,:] arrives in v; with g, u the saved
-// pre-activations and p' the slot's routing probability:
+// pre-activations (gu) and p' the slot's routing probability (ps):
 //   a = silu(g) u,  dprob part = sum_i a dA0,  dA = p' dA0,
 //   dg = dA u sigma(g) (1 + g (1 - sigma(g))),  du = dA silu(g),  aw = p' a.
 // dg and du go to dPre (gate columns, then up columns), aw to out2, and the
-// 32-feature partial sum of a dA0 of each slot to part[s, f*4 + q]. Padding
-// slots get zeros.
+// 32-feature partial sum of a dA0 of each slot to part[s, feat0/32]. Padding
+// slots get zeros (their dA0, g, u and p' are 0).
 __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const Tile& T, int c0,
-                                                      int feat0, int q, int lane, uint32_t stg_u,
-                                                      const uint32_t (&v)[16]) {
+                                                      int feat0, int lane, uint32_t stg_u,
+                                                      const uint32_t (&v)[16],
+                                                      const uint32_t (&gu)[16], const float* ps) {
   const int I = p.inter;
   const int ld2 = 2 * I;
-  float pl = 0.0f;
-  if (lane < 16 && c0 + lane < T.rows) {
-    const int r = p.slot_route[T.slot0 + c0 + lane];
-    if (r >= 0) pl = p.topk_p[r];
-  }
-  float dg[16], du[16], aw[16], dp[16];
+  const size_t row0 = (size_t)(T.slot0 + c0);
+  float o[16], dp[16];
+  // dg
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const float pj = __shfl_sync(0xFFFFFFFFu, pl, j);
-    const bool valid = c0 + j < T.rows;
-    const size_t row = (size_t)(T.slot0 + c0 + j) * ld2;
-    const float g = valid ? bf16_to_f32(p.aux[row + feat0 + lane]) : 0.0f;
-    const float u = valid ? bf16_to_f32(p.aux[row + I + feat0 + lane]) : 0.0f;
-    const float da0 = valid ? __uint_as_float(v[j]) : 0.0f;
+    const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
     const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
-    const float silu = g * sg;
-    const float a = silu * u;
-    dp[j] = a * da0;
-    const float dA = pj * da0;
-    dg[j] = dA * u * sg * (1.0f + g * (1.0f - sg));
-    du[j] = dA * silu;
-    aw[j] = pj * a;
+    const float da0 = __uint_as_float(v[j]);
+    dp[j] = g * sg * u * da0;
+    o[j] = ps[c0 + j] * da0 * u * sg * (1.0f + g * (1.0f - sg));
   }
-  const size_t row0 = (size_t)(T.slot0 + c0);
-  store_rows16(stg_u, lane, dg, p.out + row0 * ld2 + feat0, ld2);
-  store_rows16(stg_u, lane, du, p.out + row0 * ld2 + I + feat0, ld2);
-  store_rows16(stg_u, lane, aw, p.out2 + row0 * I + feat0, I);
+  store_rows16(stg_u, lane, o, p.out + row0 * ld2 + feat0, ld2);
+  // du
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float g = __uint_as_float(gu[j] << 16);
+    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+    o[j] = ps[c0 + j] * __uint_as_float(v[j]) * g * sg;
+  }
+  store_rows16(stg_u, lane, o, p.out + row0 * ld2 + I + feat0, ld2);
+  // aw
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
+    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+    o[j] = ps[c0 + j] * (g * sg * u);
+  }
+  store_rows16(stg_u, lane, o, p.out2 + row0 * I + feat0, I);
   // sum dp over the 32 lanes for each of the 16 slots, halving the values
   // held per lane at each exchange: afterwards lanes 2m and 2m+1 hold slot m
 #pragma unroll
@@ -253,17 +282,21 @@ __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const
   dp[0] += __shfl_xor_sync(0xFFFFFFFFu, dp[0], 1);
   const int m = lane >> 1;
   if ((lane & 1) == 0 && c0 + m < T.rows)
-    p.part[(row0 + m) * (size_t)(I / 32) + T.f * 4 + q] = dp[0];
+    p.part[(row0 + m) * (size_t)(I / 32) + feat0 / 32] = dp[0];
 }
 
+// One instantiation per GemmMode, so each carries only its own code path.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
+  constexpr bool kGatherB = kMode == kModeFc1 || kMode == kModeDgrad2;
+  constexpr bool kAMn = kMode == kModeDgrad2 || kMode == kModeDgrad1;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t tmem_full_bar;
-  __shared__ __align__(8) uint64_t tmem_empty_bar;
+  __shared__ __align__(8) uint64_t tmem_full_bar[2];
+  __shared__ __align__(8) uint64_t tmem_empty_bar[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ int32_t tpre[kMaxExperts + 1];
   __shared__ int32_t ttn[kMaxExperts];
@@ -277,19 +310,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), p.gather_b ? 1 + kGatherThreads : 1);
+      mbar_init(smem_u32(&full_bar[s]), kGatherB ? 1 + kGatherThreads : 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
-    mbar_init(smem_u32(&tmem_full_bar), 1);
-    mbar_init(smem_u32(&tmem_empty_bar), kEpiWarps);  // one arrive per epilogue warp
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tmem_full_bar[b]), 1);
+      mbar_init(smem_u32(&tmem_empty_bar[b]), kEpiWarps);  // one arrive per epilogue warp
+    }
     for (int i = 0; i < kTileQ; ++i) {
       mbar_init(smem_u32(&tq_full[i]), 1);
       // consumers: the UMMA thread, the epilogue warps, the 4 gather warps (FC1)
-      mbar_init(smem_u32(&tq_empty[i]), 1 + kEpiWarps + (p.gather_b ? 4 : 0));
+      mbar_init(smem_u32(&tq_empty[i]), 1 + kEpiWarps + (kGatherB ? 4 : 0));
     }
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
-    if (!p.gather_b) tma_prefetch_desc(&tmB);
+    if (!kGatherB) tma_prefetch_desc(&tmB);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
   if (warp == 0) build_tile_list(p, tpre, ttn, lane);
@@ -337,10 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // MN-major A: the weight matrix read transposed; its rows are k
       // (e*a_rows_per_expert + k) and the tile's 128 features are two 64-wide
       // column boxes per accumulator.
-      const int a_row0 = T.e * p.a_rows_per_expert + (p.a_mn ? 0 : T.f * p.f_rows);
+      const int a_row0 = T.e * p.a_rows_per_expert + (kAMn ? 0 : T.f * p.f_rows);
       const int a_col0 = T.f * p.f_rows;
       const uint32_t tx =
-          (uint32_t)p.n_acc * kATileBytes + (p.gather_b ? 0u : (uint32_t)T.n_eff * 128u);
+          (uint32_t)T.nacc * kATileBytes + (kGatherB ? 0u : (uint32_t)T.n_eff * 128u);
       bool ok = true;
       for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
         const int s = (int)(gk % (uint32_t)p.stages);
@@ -355,19 +390,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kx = kt * kBK;
         if (lane == 0) {
           mbar_arrive_expect_tx(fb, tx);
-          if (p.a_mn) {
-            for (int ac = 0; ac < p.n_acc; ++ac)
+          if (kAMn) {
+            for (int ac = 0; ac < T.nacc; ++ac)
               for (int c = 0; c < 2; ++c)
                 tma_load_2d(st + (uint32_t)ac * kATileBytes + (uint32_t)c * 8192u, &tmA,
                             a_col0 + ac * kTileM + c * 64, a_row0 + kx, fb, pol_w);
           } else {
             tma_load_2d(st, &tmA, kx, a_row0, fb, pol_w);
-            if (p.n_acc == 2)
+            if (T.nacc == 2)
               tma_load_2d(st + kATileBytes, &tmA, kx, a_row0 + p.a_second_off, fb, pol_w);
           }
         }
         __syncwarp();
-        if (!p.gather_b) {
+        if (!kGatherB) {
           const uint32_t b = st + p.b_off;
           for (int q = lane * 16; q < T.n_eff; q += 512)
             tma_load_2d(b + (uint32_t)q * 128u, &tmB, kx, T.slot0 + q, fb, pol_x);
@@ -394,13 +429,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t < 0) break;
       Tile T;
       tile_at(p, tpre, ttn, t, T);
-      if (tc > 0 && !mbar_wait_warp(smem_u32(&tmem_empty_bar), (tc - 1) & 1u, p.err, kErrWaitAccum))
+      // accumulator buffer: two in flight when one tile uses 256 columns
+      const uint32_t ab = tc % (uint32_t)p.n_buf, au = tc / (uint32_t)p.n_buf;
+      if (au > 0 &&
+          !mbar_wait_warp(smem_u32(&tmem_empty_bar[ab]), (au - 1) & 1u, p.err, kErrWaitAccum))
         break;
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16_f32(kTileM, T.n_eff) | (p.a_mn ? kIdescAMnMajor : 0u);
+      const uint32_t dacc = tmem + ab * p.buf_stride;
+      const uint32_t idesc = idesc_bf16_f32(kTileM, T.n_eff) | (kAMn ? kIdescAMnMajor : 0u);
       // one UMMA k-step (16 elements) advances 32 bytes along a K-major row,
       // or 16 rows of 128 bytes in an MN-major tile
-      const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
+      constexpr uint32_t a_kstep = kAMn ? 2048u : 32u;
       bool ok = true;
       for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
         const int s = (int)(gk % (uint32_t)p.stages);
@@ -412,25 +451,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (lane == 0) {
           // B rows written by cp.async (generic proxy) are read by the tensor core
-          if (p.gather_b) fence_proxy_async_smem();
+          if (kGatherB) fence_proxy_async_smem();
           const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t acc = (kt | kk) != 0;
             const uint64_t bdesc = sdesc_sw128(st + p.b_off + (uint32_t)kk * 32u);
             const uint32_t a0 = st + (uint32_t)kk * a_kstep;
-            umma_bf16(tmem, p.a_mn ? sdesc_sw128_mn(a0) : sdesc_sw128(a0), bdesc, idesc, acc);
-            if (p.n_acc == 2) {
+            umma_bf16(dacc, kAMn ? sdesc_sw128_mn(a0) : sdesc_sw128(a0), bdesc, idesc, acc);
+            if (T.nacc == 2) {
               const uint32_t a1 = a0 + kATileBytes;
-              umma_bf16(tmem + 256u, p.a_mn ? sdesc_sw128_mn(a1) : sdesc_sw128(a1), bdesc, idesc,
-                        acc);
+              umma_bf16(dacc + p.acc_off, kAMn ? sdesc_sw128_mn(a1) : sdesc_sw128(a1), bdesc,
+                        idesc, acc);
             }
           }
           umma_commit(smem_u32(&empty_bar[s]));
         }
         __syncwarp();
       }
-      if (lane == 0) umma_commit(smem_u32(&tmem_full_bar));  // also after an abort
+      if (lane == 0) umma_commit(smem_u32(&tmem_full_bar[ab]));  // also after an abort
       __syncwarp();
       ++tc;
       if (!ok) break;
@@ -441,60 +480,96 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;  // which of the two warps of this lane quarter
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t stg_u = sbase + p.epi_off + (uint32_t)(warp - 2) * 16u * kStageRowElems * 2u;
+    // FC2 dgrad: this warp's 16 p' values of the current chunk
+    float* ps_w = reinterpret_cast<float*>(smem_raw + (sbase - smem_u32(smem_raw)) + p.ps_off) +
+                  (warp - 2) * 16;
     uint32_t tc = 0, qi = 0;
     for (;;) {
       const int t = pop_tile(qi, kErrWaitAccum);
       if (t < 0) break;
       Tile T;
       tile_at(p, tpre, ttn, t, T);
+      const uint32_t ab = tc % (uint32_t)p.n_buf, au = tc / (uint32_t)p.n_buf;
+      const int feat0 = T.f * p.f_rows + q * 32;  // first feature of this lane quarter
+      const int nch = (T.n_eff - half * 16 + 31) / 32;  // this warp's 16-slot chunks
+      uint32_t gu_next[16];
+      float p_next = 0.0f;
+      if (kMode == kModeDgrad2 && nch > 0) {
+        // before the accumulator is ready: the first chunk's pre-activations
+        // and p' (lane j < 16 holds slot j's) into registers
+        load_preact16(p, T, half * 16, feat0 + lane, gu_next);
+        p_next = load_slot_prob(p, T, half * 16, lane);
+      }
       // the warp's vote: the warp-collective TMEM loads below are reached by
       // all lanes or by none
-      const bool w = mbar_wait_warp(smem_u32(&tmem_full_bar), tc & 1u, p.err, kErrWaitAccum);
+      const bool w = mbar_wait_warp(smem_u32(&tmem_full_bar[ab]), au & 1u, p.err, kErrWaitAccum);
       ++tc;
       if (!w) break;
       tc_fence_after();
-      const int feat0 = T.f * p.f_rows + q * 32;  // first feature of this lane quarter
-      for (int c0 = half * 16; c0 < T.n_eff; c0 += 32) {
-        uint32_t v0[16], v1[16];
-        tmem_ld16(tl + (uint32_t)c0, v0);
-        if (p.n_acc == 2) tmem_ld16(tl + 256u + (uint32_t)c0, v1);
-        tmem_ld_wait();
-        const size_t row0 = (size_t)(T.slot0 + c0);  // slot of register 0
-        if (p.mode == kModeFc1) {
-          float hv[16];
+      const uint32_t ta = tl + ab * p.buf_stride;
+      if constexpr (kMode == kModeDgrad2) {
+        // chunks of accumulator 0, then of accumulator 1; the next chunk's
+        // operands load under this chunk's math
+        const int total = T.nacc * nch;
+        for (int it = 0; it < total; ++it) {
+          const int a = it / nch, c0 = half * 16 + 32 * (it - a * nch);
+          uint32_t gu[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float g = __uint_as_float(v0[i]);
-            hv[i] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[i]);
+          for (int j = 0; j < 16; ++j) gu[j] = gu_next[j];
+          const float p_cur = p_next;
+          if (it + 1 < total) {
+            const int a2 = (it + 1) / nch, c2 = half * 16 + 32 * (it + 1 - a2 * nch);
+            load_preact16(p, T, c2, feat0 + a2 * kTileM + lane, gu_next);
+            p_next = load_slot_prob(p, T, c2, lane);
           }
-          store_rows16(stg_u, lane, hv, p.out + row0 * p.out_ld + feat0, p.out_ld);
-          if (p.out2) {  // pre-activations for the backward: gate, then up
-            float gv[16], uv[16];
+          uint32_t v[16];
+          tmem_ld16(ta + (uint32_t)a * p.acc_off + (uint32_t)c0, v);
+          tmem_ld_wait();
+          if (lane < 16) ps_w[lane] = p_cur;
+          __syncwarp();
+          swiglu_backward_chunk(p, T, c0, feat0 + a * kTileM, lane, stg_u, v, gu, ps_w - c0);
+        }
+      } else {
+        for (int c0 = half * 16; c0 < T.n_eff; c0 += 32) {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(ta + (uint32_t)c0, v0);
+          if (T.nacc == 2) tmem_ld16(ta + p.acc_off + (uint32_t)c0, v1);
+          tmem_ld_wait();
+          const size_t row0 = (size_t)(T.slot0 + c0);  // slot of register 0
+          if constexpr (kMode == kModeFc1) {
+            float hv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              gv[i] = __uint_as_float(v0[i]);
-              uv[i] = __uint_as_float(v1[i]);
+              const float g = __uint_as_float(v0[i]);
+              hv[i] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[i]);
             }
-            const int ld2 = 2 * p.inter;
-            store_rows16(stg_u, lane, gv, p.out2 + row0 * ld2 + feat0, ld2);
-            store_rows16(stg_u, lane, uv, p.out2 + row0 * ld2 + p.inter + feat0, ld2);
-          }
-        } else if (p.mode == kModeDgrad2) {
-          swiglu_backward_chunk(p, T, c0, feat0, q, lane, stg_u, v0);
-        } else {
-          for (int seg = 0; seg < p.n_acc; ++seg) {
-            float ov[16];
+            store_rows16(stg_u, lane, hv, p.out + row0 * p.out_ld + feat0, p.out_ld);
+            if (p.out2) {  // pre-activations for the backward: gate, then up
+              float gv[16], uv[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) ov[i] = __uint_as_float(seg == 0 ? v0[i] : v1[i]);
-            store_rows16(stg_u, lane, ov, p.out + row0 * p.out_ld + feat0 + seg * kTileM,
-                         p.out_ld);
+              for (int i = 0; i < 16; ++i) {
+                gv[i] = __uint_as_float(v0[i]);
+                uv[i] = __uint_as_float(v1[i]);
+              }
+              const int ld2 = 2 * p.inter;
+              store_rows16(stg_u, lane, gv, p.out2 + row0 * ld2 + feat0, ld2);
+              store_rows16(stg_u, lane, uv, p.out2 + row0 * ld2 + p.inter + feat0, ld2);
+            }
+          } else {
+            for (int seg = 0; seg < T.nacc; ++seg) {
+              float ov[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) ov[i] = __uint_as_float(seg == 0 ? v0[i] : v1[i]);
+              store_rows16(stg_u, lane, ov, p.out + row0 * p.out_ld + feat0 + seg * kTileM,
+                           p.out_ld);
+            }
           }
         }
       }
       tc_fence_before();
-      if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar));
+      if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar[ab]));
     }
-  } else if (p.gather_b) {
+  } else if (kGatherB) {
     // ---------------------------------------------------------------- B row gather
     // Row r of a stage holds act[sorted_slot_ids[slot0 + r], kx .. kx+63]:
     // 16-byte chunk c at r*128 + ((c ^ (r%8)) * 16), the 128-byte swizzle the
@@ -557,8 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// SM count of the current device, with the kernel's shared-memory opt-in set
-// up once per device.
+template <int kMode>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(moe_gemm_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSmemBudget);
+}
+
+// SM count of the current device, with every instantiation's shared-memory
+// opt-in set up once per device.
 int device_sms(cudaError_t* err) {
   static int sms[64] = {};
   int dev = 0;
@@ -567,8 +648,10 @@ int device_sms(cudaError_t* err) {
   int n = 0;
   if ((*err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return 0;
-  if ((*err = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kSmemBudget)) != cudaSuccess) {
+  if ((*err = set_smem_attr<kModeFc1>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeFc2>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeDgrad2>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeDgrad1>()) != cudaSuccess) {
     cudaGetLastError();  // reported here; do not leave it for a later launch to report
     return 0;
   }
@@ -581,9 +664,7 @@ int device_sms(cudaError_t* err) {
 int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.max_rows <= 0 || a.N <= 0) return 0;
   GemmParams p{};
-  p.mode = a.mode;
-  p.gather_b = a.mode == kModeFc1 || a.mode == kModeDgrad2;
-  p.a_mn = a.mode == kModeDgrad2 || a.mode == kModeDgrad1;
+  const bool gather_b = a.mode == kModeFc1 || a.mode == kModeDgrad2;
   p.bm = a.bm;
   p.sorted_slot_ids = a.sorted_slot_ids;
   p.kept_counts = a.kept_counts;
@@ -591,19 +672,21 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   p.out = static_cast<uint16_t*>(a.out);
   p.out2 = static_cast<uint16_t*>(a.out2);
   p.aux = static_cast<const uint16_t*>(a.aux);
-  p.slot_route = a.slot_route;
-  p.topk_p = a.topk_p;
+  p.slot_prob = a.slot_prob;
   p.part = a.part;
   p.inter = a.I;
   p.err = a.err;
   p.act = static_cast<const uint16_t*>(a.act);
-  p.act_rows = p.gather_b ? a.N : 0;
+  p.act_rows = gather_b ? a.N : 0;
   const int64_t S = a.s_max;
   const uint64_t E = (uint64_t)a.E;
   CUtensorMap tmA, tmB;
+  p.max_tn = kMaxTileN;
   switch (a.mode) {
-    case kModeFc1:  // A = w13 rows [E*2I, H]; B gathered from x [N, H]
+    case kModeFc1:  // A = w13 rows [E*2I, H] (gate and up accumulators); B gathered from x
       p.n_acc = 2;
+      p.pair_feats = 0;
+      p.m_total = a.I;
       p.k_tiles = a.H / kBK;
       p.a_rows_per_expert = 2 * a.I;
       p.a_second_off = a.I;
@@ -614,20 +697,26 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       if (!make_map(&tmA, a.w, (uint64_t)a.H, E * 2 * a.I, kBK, kTileM)) return -1;
       tmB = tmA;  // unused: B rows are gathered with cp.async
       break;
-    case kModeFc2:  // A = w2 rows [E*H, I]; B = h [S, I]
-      p.n_acc = (a.H % (2 * kTileM) == 0) ? 2 : 1;
+    case kModeFc2:  // A = w2 rows [E*H, I], two 128-row feature tiles; B = h [S, I]
+      p.n_acc = 2;
+      p.pair_feats = 1;
+      p.m_total = a.H;
       p.k_tiles = a.I / kBK;
       p.a_rows_per_expert = a.H;
       p.a_second_off = kTileM;
-      p.f_rows = kTileM * p.n_acc;
-      p.f_tiles = a.H / p.f_rows;
+      p.f_rows = 2 * kTileM;
+      p.f_tiles = (a.H + 2 * kTileM - 1) / (2 * kTileM);
       p.out_ld = a.H;
       p.act_ld = a.I;
       if (!make_map(&tmA, a.w, (uint64_t)a.I, E * a.H, kBK, kTileM)) return -1;
       if (!make_map(&tmB, a.act, (uint64_t)a.I, (uint64_t)S, kBK, 16)) return -1;
       break;
     case kModeDgrad2:  // A[i, h] = w2[e][h][i] (MN-major, K = H); B gathered from dY [N, H]
+      // one 128-feature accumulator per tile, two tiles in flight in TMEM, so
+      // the SwiGLU-backward epilogue overlaps the next tile's MMAs
       p.n_acc = 1;
+      p.pair_feats = 1;
+      p.m_total = a.I;
       p.k_tiles = a.H / kBK;
       p.a_rows_per_expert = a.H;
       p.f_rows = kTileM;
@@ -638,11 +727,13 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       tmB = tmA;
       break;
     case kModeDgrad1:  // A[h, k] = w13[e][k][h] (MN-major, K = 2I); B = dPre [S, 2I]
-      p.n_acc = (a.H % (2 * kTileM) == 0) ? 2 : 1;
+      p.n_acc = 2;
+      p.pair_feats = 1;
+      p.m_total = a.H;
       p.k_tiles = 2 * a.I / kBK;
       p.a_rows_per_expert = 2 * a.I;
-      p.f_rows = kTileM * p.n_acc;
-      p.f_tiles = a.H / p.f_rows;
+      p.f_rows = 2 * kTileM;
+      p.f_tiles = (a.H + 2 * kTileM - 1) / (2 * kTileM);
       p.out_ld = a.H;
       p.act_ld = 2 * a.I;
       if (!make_map(&tmA, a.w, (uint64_t)a.H, E * 2 * a.I, 64, kBK)) return -1;
@@ -653,23 +744,32 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   }
   p.E = a.E;
   // stage size for the largest slot tile any expert can have
-  const int64_t rows_cap = a.max_rows < kMaxTileN ? a.max_rows : kMaxTileN;
+  const int64_t rows_cap = a.max_rows < p.max_tn ? a.max_rows : p.max_tn;
   const int tile_cap = (int)((rows_cap + 15) / 16 * 16);
   const int64_t grid_bound =
-      (int64_t)p.f_tiles * ((a.max_total + kMaxTileN - 1) / kMaxTileN + a.E);
+      (int64_t)p.f_tiles * ((a.max_total + p.max_tn - 1) / p.max_tn + a.E);
   p.b_off = (uint32_t)p.n_acc * kATileBytes;
   p.stage_bytes = p.b_off + (((uint32_t)tile_cap * 128u + 1023u) & ~1023u);
-  p.stages = (int)((kSmemBudget - 1024u - kEpiStageBytes) / p.stage_bytes);
+  p.stages = (int)((kSmemBudget - 1024u - kEpiStageBytes - kPsBytes) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2) return -1;
   p.epi_off = (uint32_t)p.stages * p.stage_bytes;
-  const size_t dyn = (size_t)p.epi_off + kEpiStageBytes + 1024;
+  p.ps_off = p.epi_off + kEpiStageBytes;
+  p.acc_off = (uint32_t)p.max_tn;
+  p.buf_stride = (uint32_t)(p.n_acc * p.max_tn);
+  p.n_buf = 2 * p.buf_stride <= kTmemCols ? 2 : 1;
+  const size_t dyn = (size_t)p.ps_off + kPsBytes + 1024;
   cudaError_t err = cudaSuccess;
   const int sms = device_sms(&err);
   if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
   const int grid = (int)(grid_bound < sms ? grid_bound : sms);
   p.sched = a.sched;
-  moe_gemm_kernel<<<grid, kThreads, dyn, s>>>(tmA, tmB, p);
+  switch (a.mode) {
+    case kModeFc1: moe_gemm_kernel<kModeFc1><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
+    case kModeFc2: moe_gemm_kernel<kModeFc2><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
+    case kModeDgrad2: moe_gemm_kernel<kModeDgrad2><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
+    default: moe_gemm_kernel<kModeDgrad1><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
+  }
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;
   return 1;

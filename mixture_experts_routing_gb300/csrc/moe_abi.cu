@@ -120,10 +120,10 @@ WsLayout ws_layout(const moe_config_t* c) {
   return w;
 }
 
-// Backward scratch: slot -> route map, the backward GEMMs' tile counters, the
+// Backward scratch: p' of each slot, the backward GEMMs' tile counters, the
 // dprob partials, dPre = [dg | du], aw = p' a and the per-slot input gradient.
 struct BwdLayout {
-  size_t slot_route, sched, part, dpre, aw, dxr, total;
+  size_t slot_prob, sched, part, dpre, aw, dxr, total;
 };
 
 BwdLayout bwd_layout(const moe_config_t* c) {
@@ -136,7 +136,7 @@ BwdLayout bwd_layout(const moe_config_t* c) {
     off += (bytes + 255) / 256 * 256;
     return at;
   };
-  w.slot_route = take((size_t)S * 4);
+  w.slot_prob = take((size_t)S * 4);
   w.sched = take(8 * 4);
   w.part = take((size_t)(S * (I / 32)) * 4);
   w.dpre = take((size_t)(S * 2 * I) * 2);
@@ -368,7 +368,7 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
   uint32_t* err = error_word_ptr();
   if (!err) return MOE_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int32_t* slot_route = reinterpret_cast<int32_t*>(ws + L.slot_route);
+  float* slot_prob = reinterpret_cast<float*>(ws + L.slot_prob);
   int32_t* sched = reinterpret_cast<int32_t*>(ws + L.sched);
   float* part = reinterpret_cast<float*>(ws + L.part);
   void* dpre = ws + L.dpre;
@@ -383,9 +383,9 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
     launched += l;
     return true;
   };
-  // 1. slot -> route map (p' and dprob of each slot); zeroes the counters
-  if (!add(moe::launch_slot_route(routes->sorted_slot_ids, routes->token_routes, N, K,
-                                  N > 0 ? S : 0, slot_route, sched, 8, stream)))
+  // 1. p' of each slot; zeroes the counters
+  if (!add(moe::launch_slot_route(routes->sorted_slot_ids, routes->token_routes, routes->topk_p,
+                                  N, K, N > 0 ? S : 0, slot_prob, sched, 8, stream)))
     return finish(-1);
   if (N > 0) {
     // 2. FC2 dgrad with the SwiGLU backward: dPre, aw = p' a, dprob partials
@@ -397,8 +397,7 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
     g.out = dpre;
     g.out2 = aw;
     g.aux = preact;
-    g.slot_route = slot_route;
-    g.topk_p = routes->topk_p;
+    g.slot_prob = slot_prob;
     g.part = part;
     g.act_rows = N;
     g.sched = sched + 0;

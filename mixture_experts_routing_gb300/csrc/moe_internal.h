@@ -71,8 +71,7 @@ struct GemmArgs {
   void* out;             // FC1: h [S,I]; FC2: o [S,H]; dgrad2: dPre [S,2I]; dgrad1: dXr [S,H]
   void* out2;            // FC1: pre-activations [S,2I] or null; dgrad2: p'*a [S,I]
   const void* aux;       // dgrad2: pre-activations [S,2I]
-  const int32_t* slot_route;  // dgrad2: route of each slot (-1 padding)
-  const float* topk_p;        // dgrad2
+  const float* slot_prob;     // dgrad2: p' of each slot's route (0 padding)
   float* part;                // dgrad2: dprob partials [S, I/32]
   int64_t act_rows;      // rows of act (N when gathered, else S)
   const int32_t* sorted_slot_ids;
@@ -102,11 +101,11 @@ struct WgradArgs {
 int launch_wgrad(const WgradArgs& a, cudaStream_t s);
 
 // Backward helpers (combine.cu).
-// slot_route[s] = route t*K+k held by slot s, -1 for padding; also zeroes
-// sched_zero[0..n_zero).
-int launch_slot_route(const int32_t* sorted_slot_ids, const int32_t* token_routes, int N, int K,
-                      int64_t s_max, int32_t* slot_route, int32_t* sched_zero, int n_zero,
-                      cudaStream_t s);
+// slot_prob[s] = topk_p of the route t*K+k held by slot s, 0 for padding;
+// also zeroes sched_zero[0..n_zero).
+int launch_slot_route(const int32_t* sorted_slot_ids, const int32_t* token_routes,
+                      const float* topk_p, int N, int K, int64_t s_max, float* slot_prob,
+                      int32_t* sched_zero, int n_zero, cudaStream_t s);
 // dX[t] = sum_k dXr[token_routes[t,k]] (fp32, k order) and
 // dprob[t,k] = sum_j part[token_routes[t,k], j] (j order; 0 for a dropped route).
 int launch_combine_bwd(const uint16_t* dxr, const float* part, int n_part,

@@ -36,7 +36,7 @@
 namespace moe {
 namespace {
 
-constexpr int kWM = 128;              // UMMA M: output-contiguous features per tile
+constexpr int kWM = 128;              // UMMA M: output-contiguous features per accumulator
 constexpr int kWN = 256;              // UMMA N
 constexpr int kWK = 64;               // slots per stage
 constexpr int kWThreads = 448;
@@ -44,8 +44,8 @@ constexpr int kWEpiWarps = 8;         // warps 2-9
 constexpr int kWGatherWarp0 = 10;     // warps 10-13
 constexpr int kWGatherThreads = 128;
 constexpr int kWMaxStages = 8;
-constexpr uint32_t kWABytes = kWM * kWK * 2;  // 16 KiB: 2 chunks of 64 features
-constexpr uint32_t kWBBytes = kWN * kWK * 2;  // 32 KiB: 4 chunks
+constexpr uint32_t kWABytes = 2 * kWM * kWK * 2;  // 32 KiB: two accumulators' A, 4 chunks
+constexpr uint32_t kWBBytes = kWN * kWK * 2;      // 32 KiB: 4 chunks
 constexpr uint32_t kWStageBytes = kWABytes + kWBBytes;
 constexpr uint32_t kWSmemBudget = 223 * 1024;
 constexpr uint32_t kWTmemCols = 512;
@@ -54,6 +54,8 @@ constexpr int kWTileQ = 4;
 struct WgradParams {
   int E, m_total, n_total, m_tiles, n_tiles, bm, stages;
   int tile_n;            // UMMA N: 256, or 128 when n_total is not a multiple of 256
+  uint32_t buf_stride;   // TMEM columns of one accumulator buffer (2 x tile_n)
+  int n_buf;             // accumulator buffers in flight (2 when 2 x buf_stride fits)
   int a_gather;          // 1: A from gathered token rows (dW13: x), B slot rows (dPre)
                          // 0: A slot rows (aw), B from gathered token rows (dW2: dY)
   const uint16_t* act;   // token-indexed operand [act_rows, act_ld]
@@ -67,14 +69,15 @@ struct WgradParams {
 };
 
 struct WTile {
-  int e, m0, n0, kept, slot0;
+  int e, m0, n0, kept, slot0, nacc;  // nacc: 128-row accumulators (the last M tile may hold one)
 };
 
 __device__ __forceinline__ void wtile_at(const WgradParams& p, int t, WTile& T) {
   const int per = p.m_tiles * p.n_tiles;
   T.e = t / per;
   const int r = t - T.e * per;
-  T.m0 = (r % p.m_tiles) * kWM;
+  T.m0 = (r % p.m_tiles) * 2 * kWM;
+  T.nacc = T.m0 + kWM < p.m_total ? 2 : 1;
   T.n0 = (r / p.m_tiles) * p.tile_n;
   T.kept = max(p.kept_counts[T.e], 0);
   T.slot0 = p.block_start[T.e] * p.bm;
@@ -95,11 +98,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int n_tiles = p.E * p.m_tiles * p.n_tiles;
-  // the slot-indexed operand: A (aw) when B is gathered, else B (dPre)
+  // the slot-indexed operand: A (aw) when B is gathered, else B (dPre); an
+  // A side holds 2 chunks of 64 features per accumulator
   const uint32_t d_off = p.a_gather ? kWABytes : 0u;
-  const int d_chunks = p.a_gather ? p.tile_n / 64 : kWM / 64;
   const uint32_t g_off = p.a_gather ? 0u : kWABytes;
-  const int g_chunks = p.a_gather ? kWM / 64 : p.tile_n / 64;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       wtile_at(p, t, T);
       const int chunks = (T.kept + kWK - 1) / kWK;
       const int dcol0 = p.a_gather ? T.n0 : T.m0;
+      const int d_chunks = p.a_gather ? p.tile_n / 64 : 2 * T.nacc;
       bool ok = true;
       for (int kt = 0; kt < chunks; ++kt, ++gk) {
         const int s = (int)(gk % (uint32_t)p.stages);
@@ -195,12 +198,12 @@ __global__ void __launch_bounds__(kWThreads, 1)
       WTile T;
       wtile_at(p, t, T);
       if (T.kept == 0) continue;  // zero tile: the epilogue writes it without TMEM
-      const uint32_t b = tc & 1u;
-      if (tc >= 2 && !mbar_wait_warp(smem_u32(&tmem_empty_bar[b]), ((tc >> 1) - 1u) & 1u, p.err,
-                                     kErrWaitAccum))
+      const uint32_t b = tc % (uint32_t)p.n_buf, bu = tc / (uint32_t)p.n_buf;
+      if (bu > 0 && !mbar_wait_warp(smem_u32(&tmem_empty_bar[b]), (bu - 1u) & 1u, p.err,
+                                    kErrWaitAccum))
         break;
       tc_fence_after();
-      const uint32_t d = tmem + b * (uint32_t)kWN;
+      const uint32_t d = tmem + b * p.buf_stride;
       const int chunks = (T.kept + kWK - 1) / kWK;
       bool ok = true;
       for (int kt = 0; kt < chunks; ++kt, ++gk) {
@@ -216,10 +219,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
           const uint32_t st = sbase + (uint32_t)s * kWStageBytes;
           const int rem = T.kept - kt * kWK;
           const int ksub = rem >= kWK ? kWK / 16 : (rem + 15) / 16;
-          for (int kk = 0; kk < ksub; ++kk)
-            umma_bf16(d, sdesc_sw128_mn(st + (uint32_t)kk * 2048u),
-                      sdesc_sw128_mn(st + kWABytes + (uint32_t)kk * 2048u), idesc,
-                      (kt | kk) != 0);
+          for (int kk = 0; kk < ksub; ++kk) {
+            const uint64_t bdesc = sdesc_sw128_mn(st + kWABytes + (uint32_t)kk * 2048u);
+            for (int a = 0; a < T.nacc; ++a)
+              umma_bf16(d + (uint32_t)(a * p.tile_n),
+                        sdesc_sw128_mn(st + (uint32_t)a * 16384u + (uint32_t)kk * 2048u), bdesc,
+                        idesc, (kt | kk) != 0);
+          }
           umma_commit(smem_u32(&empty_bar[s]));
         }
         __syncwarp();
@@ -244,24 +250,28 @@ __global__ void __launch_bounds__(kWThreads, 1)
       wtile_at(p, t, T);
       float* dst = p.out + ((size_t)T.e * p.n_total + T.n0) * p.m_total + T.m0 + q * 32 + lane;
       if (T.kept == 0) {
-        for (int c = half * 16; c < p.tile_n; c += 32)
+        for (int a = 0; a < T.nacc; ++a)
+          for (int c = half * 16; c < p.tile_n; c += 32)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dst[(size_t)(c + j) * p.m_total] = 0.0f;
+            for (int j = 0; j < 16; ++j) dst[(size_t)(c + j) * p.m_total + a * kWM] = 0.0f;
         continue;
       }
-      const uint32_t b = tc & 1u;
+      const uint32_t b = tc % (uint32_t)p.n_buf, bu = tc / (uint32_t)p.n_buf;
       const bool w =
-          mbar_wait_warp(smem_u32(&tmem_full_bar[b]), (tc >> 1) & 1u, p.err, kErrWaitAccum);
+          mbar_wait_warp(smem_u32(&tmem_full_bar[b]), bu & 1u, p.err, kErrWaitAccum);
       ++tc;
       if (!w) break;
       tc_fence_after();
-      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + b * (uint32_t)kWN;
-      for (int c = half * 16; c < p.tile_n; c += 32) {
-        uint32_t v[16];
-        tmem_ld16(tl + (uint32_t)c, v);
-        tmem_ld_wait();
+      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + b * p.buf_stride;
+      for (int a = 0; a < T.nacc; ++a) {
+        for (int c = half * 16; c < p.tile_n; c += 32) {
+          uint32_t v[16];
+          tmem_ld16(tl + (uint32_t)(a * p.tile_n + c), v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) dst[(size_t)(c + j) * p.m_total] = __uint_as_float(v[j]);
+          for (int j = 0; j < 16; ++j)
+            dst[(size_t)(c + j) * p.m_total + a * kWM] = __uint_as_float(v[j]);
+        }
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar[b]));
@@ -280,13 +290,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // its async-proxy reads. Waits end in a warp vote, so a warp leaves
     // together when one runs out.
     const int gw = warp - kWGatherWarp0;
-    const int units = g_chunks * 8;     // 16-byte units per row: 16 or 32
-    const int rpi = 32 / units;         // rows per warp instruction: 2 or 1
-    const int sub = lane / units;
-    const int uc = lane % units;
-    const int c = uc >> 3, jj = uc & 7;
-    const int n_ins = 16 / rpi;         // instructions per stage
-    const int my_row = rpi * gw + (lane % rpi) + 4 * rpi * (lane / rpi);  // lane < 16
     uint32_t gk = 0, qi = 0;
     bool ok = true;
     while (ok) {
@@ -294,6 +297,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (t < 0) break;
       WTile T;
       wtile_at(p, t, T);
+      const int g_chunks = p.a_gather ? 2 * T.nacc : p.tile_n / 64;
+      const int units = g_chunks * 8;     // 16-byte units per row: 16 or 32
+      const int rpi = 32 / units;         // rows per warp instruction: 2 or 1
+      const int sub = lane / units;
+      const int uc = lane % units;
+      const int c = uc >> 3, jj = uc & 7;
+      const int n_ins = 16 / rpi;         // instructions per stage
+      const int my_row = rpi * gw + (lane % rpi) + 4 * rpi * (lane / rpi);  // lane < 16
       const int gcol0 = (p.a_gather ? T.m0 : T.n0) + c * 64 + jj * 8;
       const int chunks = (T.kept + kWK - 1) / kWK;
       auto token_of = [&](int kt) -> int {
@@ -387,8 +398,10 @@ int launch_wgrad(const WgradArgs& a, cudaStream_t s) {
   p.act_rows = a.N;
   p.tile_n = (p.n_total % kWN == 0) ? kWN : 128;
   if (p.m_total % kWM != 0 || p.n_total % p.tile_n != 0) return -1;
-  p.m_tiles = p.m_total / kWM;
+  p.m_tiles = (p.m_total + 2 * kWM - 1) / (2 * kWM);
   p.n_tiles = p.n_total / p.tile_n;
+  p.buf_stride = (uint32_t)(2 * p.tile_n);
+  p.n_buf = 2 * p.buf_stride <= kWTmemCols ? 2 : 1;
   p.stages = (int)((kWSmemBudget - 1024u) / kWStageBytes);
   if (p.stages > kWMaxStages) p.stages = kWMaxStages;
   const size_t dyn = (size_t)p.stages * kWStageBytes + 1024;
