@@ -11,6 +11,9 @@ workload that fits one GPU. Its inputs exceed L2, so no flush is needed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle, on the host cores
+    python bench.py --workload dropless    # training step of the dropless,
+                                           # bucketed layer (forward + backward),
+                                           # swept over N = 128 .. 16384
 
 Under torchrun each rank is an independent replica with its own batch (weak
 scaling, no collective on the data path); value = tokens of all ranks / the
@@ -32,6 +35,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer fwd tokens/s on 1 GB300; grouped-GEMM TFLOPS as % of BF16 peak"
+METRIC_TRAIN = ("MoE-layer fwd+bwd tokens/s on 1 GB300 (dropless bucketed layer, dX/dW backward); "
+                "TFLOPS as % of BF16 peak")
 UNIT = "tokens/s"
 
 
@@ -281,19 +286,31 @@ def run_reference(args):
         return 0
     w = synth.WORKLOADS[args.workload]
     x_bits, wr, bias = host_inputs(w, w.seed)
-    n_exp = max(1, min(4, args.cpu_experts))
-    for _ in range(args.warmup):
-        time_oracle_sample(w, x_bits, wr, bias, args.block_m, n_exp)
+    train = w.cap_num == 0
+    if train:  # dropless training step: routing + expert-path backward on a route sample
+        dy_bits = synth.normal_bf16_bits(w.seed, synth.STREAM["dy"], 0, w.n_tokens * w.hidden,
+                                         1.0).reshape(w.n_tokens, w.hidden)
+
+        def sample(i):
+            return time_oracle_train_sample(w, x_bits, dy_bits, wr, bias, args.block_m, n_routes=1024,
+                                            seed=i)
+    else:
+        n_exp = max(1, min(4, args.cpu_experts))
+
+        def sample(i):
+            return time_oracle_sample(w, x_bits, wr, bias, args.block_m, n_exp, seed_experts=i)
+    for i in range(args.warmup):
+        sample(i)
     vals, secs = [], 0.0
     t_start = time.perf_counter()
     for i in range(args.steps):
-        v, desc, s, cores = time_oracle_sample(w, x_bits, wr, bias, args.block_m, n_exp, seed_experts=i)
+        v, desc, s, cores = sample(i)
         vals.append(v)
         secs += s
     wall = time.perf_counter() - t_start
     value = len(vals) / sum(1.0 / v for v in vals)  # tokens over total extrapolated time
     out = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_TRAIN if train else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.n_tokens / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": {"workload": w.name, "description": w.note, "block_m": args.block_m,
@@ -463,10 +480,240 @@ def run_ours(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- training step (dropless)
+def time_oracle_train_sample(w, x_bits, dy_bits, wr, bias, bm, n_routes=4096, seed=0):
+    """The oracle's routing of every token plus the expert-path backward of a
+    bounded sample of routes (forward recompute, dX row, dW contributions),
+    extrapolated to all routes by route count."""
+    import numpy as np
+    import oracle
+    import synth
+    N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
+    t0 = time.perf_counter()
+    ids, p, _, _ = oracle.router(x_bits, wr, bias, K, renorm=True)
+    t_route = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    r = rng.choice(N * K, size=min(n_routes, N * K), replace=False)
+    tok, ex = (r // K).astype(np.int32), ids.ravel()[r].astype(np.int32)
+    pr = p.ravel()[r]
+    exps = sorted(set(ex.tolist()))
+    wg = {e: synth.normal_bf16_bits(w.seed, synth.STREAM["wg"], e * H * I, H * I, w.w_std).reshape(H, I) for e in exps}
+    wu = {e: synth.normal_bf16_bits(w.seed, synth.STREAM["wu"], e * H * I, H * I, w.w_std).reshape(H, I) for e in exps}
+    wd = {e: synth.normal_bf16_bits(w.seed, synth.STREAM["wd"], e * I * H, I * H, w.w_std).reshape(I, H) for e in exps}
+    W = oracle.ExpertWeights(E, wg, wu, wd)
+    t0 = time.perf_counter()
+    out = oracle.bwd_routes(tok, ex, pr, x_bits, dy_bits, W, H, I)
+    e0 = exps[0]
+    sel = ex == e0
+    oracle.wgrad_expert(tok[sel], x_bits, dy_bits, out["aw"][sel], out["dg"][sel], out["du"][sel], H, I)
+    t_bwd = time.perf_counter() - t0
+    t_full = t_route + t_bwd * (N * K) / len(r)
+    desc = ("routing of all %d tokens + expert-path backward (recomputed forward, dX, dprob, "
+            "dW) of %d of %d routes, time extrapolated by route count" % (N, len(r), N * K))
+    return N / t_full, desc, t_route + t_bwd, oracle.num_threads()
+
+
+def run_ours_train(args):
+    import numpy as np
+    import torch
+
+    import mixture_experts_routing_gb300 as moe
+    import synth
+    import synth.gpu
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    base = synth.WORKLOADS[args.workload]
+    peaks = load_peaks()
+    H, E, K, I = base.hidden, base.n_experts, base.top_k, base.inter
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    # weights, packed once (random-init, the layer's shapes)
+    cfg0 = moe.Config(base.n_tokens, H, E, K, I, 0, 1, block_m=args.block_m, ladder=list(base.ladder),
+                      ladder_den=base.ladder_den)
+    w13 = torch.empty((E, 2 * I, H), **bf)
+    w2 = torch.empty((E, H, I), **bf)
+    tmp = torch.empty((E, H, I), **bf)
+    synth.gpu.fill(tmp, base.seed, synth.STREAM["wg"], base.w_std)
+    wu = torch.empty((E, H, I), **bf)
+    synth.gpu.fill(wu, base.seed, synth.STREAM["wu"], base.w_std)
+    moe.pack_w13(cfg0, tmp, wu, w13)
+    del wu
+    tmp = tmp.view(E, I, H)
+    synth.gpu.fill(tmp, base.seed, synth.STREAM["wd"], base.w_std)
+    moe.pack_w2(cfg0, tmp, w2)
+    del tmp
+    dw13 = torch.empty((E, 2 * I, H), dtype=torch.float32, device=dev)
+    dw2 = torch.empty((E, H, I), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def setup(N):
+        w = base.with_tokens(N)
+        cfg = moe.Config(N, H, E, K, I, 0, 1, block_m=args.block_m, ladder=list(base.ladder),
+                         ladder_den=base.ladder_den)
+        x_bits, wr_h, bias_h = host_inputs(w, w.seed + rank)
+        dy_bits = synth.normal_bf16_bits(w.seed + rank, synth.STREAM["dy"], 0, N * H, 1.0).reshape(N, H)
+        S = moe.max_slots(cfg)
+        st = dict(w=w, cfg=cfg, x_bits=x_bits, dy_bits=dy_bits, wr_h=wr_h, bias_h=bias_h,
+                  x=torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(dev),
+                  dy=torch.from_numpy(dy_bits.view(np.int16)).view(torch.bfloat16).to(dev),
+                  wr=torch.from_numpy(wr_h).to(dev),
+                  bias=None if bias_h is None else torch.from_numpy(bias_h).to(dev),
+                  routes=moe.alloc_routes(cfg, dev), ws=moe.alloc_workspace(cfg, dev),
+                  bws=moe.alloc_backward_workspace(cfg, dev),
+                  preact=torch.empty((S, 2 * I), **bf), dx=torch.empty((N, H), **bf),
+                  dprob=torch.empty((N, K), dtype=torch.float32, device=dev))
+        st["h"], st["o"], st["y"] = moe.alloc_buffers(cfg, dev)
+        return st
+
+    def step(st, evs=None):
+        c, r = st["cfg"], st["routes"]
+        if evs is not None:
+            evs[0].record(stream)
+        moe.route_align(c, st["x"], st["wr"], st["bias"], r, st["ws"], stream)
+        if evs is not None:
+            evs[1].record(stream)
+        moe.ffn_forward_train(c, r, st["x"], w13, w2, st["h"], st["o"], st["preact"], stream)
+        if evs is not None:
+            evs[2].record(stream)
+        moe.combine(c, r, st["o"], st["y"], stream)
+        if evs is not None:
+            evs[3].record(stream)
+        moe.ffn_backward(c, r, st["x"], w13, w2, st["preact"], st["dy"], st["dx"], dw13, dw2,
+                         st["dprob"], st["bws"], stream)
+        if evs is not None:
+            evs[4].record(stream)
+
+    def time_steps(st, steps):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist, dev)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(steps):
+            step(st, evs[i])
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist, dev)
+        per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
+               for j, n in enumerate(("route", "ffn_forward", "combine", "ffn_backward"))}
+        return max_over_ranks(a.elapsed_time(b), dist, dev) / steps, per
+
+    # ---- sweep over N (the curve), then the headline at N = base.n_tokens
+    sweep = {}
+    for N in base.sweep:
+        if N == base.n_tokens:
+            continue
+        st = setup(N)
+        for _ in range(max(args.warmup, 3)):
+            step(st)
+        ms, per = time_steps(st, max(3, min(args.steps, 10)))
+        R = N * K
+        sweep[str(N)] = {"ms_per_step": ms, "tokens_per_s": N * world / (ms / 1e3),
+                         "tflops": 18.0 * R * H * I / (ms / 1e3) / 1e12,
+                         "fwd_ms": per["route"] + per["ffn_forward"] + per["combine"],
+                         "bwd_ms": per["ffn_backward"]}
+        del st
+        torch.cuda.empty_cache()
+    st = setup(base.n_tokens)
+    N = base.n_tokens
+    for _ in range(max(args.warmup, 3)):
+        step(st)
+    torch.cuda.synchronize()
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    clocks = ClockSampler(dev.index).start()
+    time.sleep(0.3)
+    launches0 = moe.launch_count()
+    ms, per = time_steps(st, args.steps)
+    launches = moe.launch_count() - launches0
+    clk = clocks.stop()
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+    R = N * K
+    sweep[str(N)] = {"ms_per_step": ms, "tokens_per_s": N * world / (ms / 1e3),
+                     "tflops": 18.0 * R * H * I / (ms / 1e3) / 1e12,
+                     "fwd_ms": per["route"] + per["ffn_forward"] + per["combine"],
+                     "bwd_ms": per["ffn_backward"]}
+
+    # ---- end to end: x and dY in from pinned host memory, y, dX and dprob out
+    xh = torch.from_numpy(st["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    dyh = torch.from_numpy(st["dy_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
+    dxh = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
+    dph = torch.empty((N, K), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        st["x"].copy_(xh, non_blocking=True)
+        st["dy"].copy_(dyh, non_blocking=True)
+        step(st)
+        yh.copy_(st["y"][:N], non_blocking=True)
+        dxh.copy_(st["dx"], non_blocking=True)
+        dph.copy_(st["dprob"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
+
+    bwd_flops = 12.0 * R * H * I
+    ach = bwd_flops / (per["ffn_backward"] / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"], "traffic": None, "peak_source": peaks["_source"],
+            "kernel": "ffn_backward (FC2 dgrad + SwiGLU backward, FC1 dgrad, dX/dprob "
+                      "gather-combine, dW2 and dW13 weight gradients)",
+            "ms": per["ffn_backward"], "algorithmic_flops": bwd_flops}
+    value = N * world / (ms / 1e3)
+    out = {
+        "metric": METRIC_TRAIN, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": base.name, "description": base.note, "tokens_per_step_per_gpu": N,
+                   "block_m": args.block_m, "ladder": [list(base.ladder), base.ladder_den],
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (%.2f GB of expert weights, %.2f GB of fp32 weight "
+                         "gradients); no flush" % ((w13.numel() + w2.numel()) * 2 / 1e9,
+                                                   (dw13.numel() + dw2.numel()) * 4 / 1e9)},
+        "gpu_launches": launches,
+        "e2e": {"value": N * world / (ms_e2e / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2 + N * K * 4},
+        "roofline": roof,
+        "tflops_fwd_bwd": 18.0 * R * H * I / (ms / 1e3) / 1e12,
+        "pct_bf16_peak_fwd_bwd": 18.0 * R * H * I / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+        "calls_ms": per,
+        "sweep": sweep,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, secs, cores = time_oracle_train_sample(st["w"], st["x_bits"], st["dy_bits"],
+                                                        st["wr_h"], st["bias_h"], args.block_m)
+        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": desc, "cpu_seconds": secs}
+    if rank == 0:
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    import synth
+    if synth.WORKLOADS[args.workload].cap_num == 0:
+        return run_ours_train(args)
     return run_ours(args)
 
 
