@@ -229,6 +229,8 @@ def _bind_backward(L):
     L.oracle_bwd_routes.restype = i32
     L.oracle_wgrad_expert.argtypes = [i32, P, i32, i32, P, P, P, P, P, P, P, P]
     L.oracle_wgrad_expert.restype = i32
+    L.oracle_router_backward.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
+    L.oracle_router_backward.restype = i32
     L._bwd_bound = True
     return L
 
@@ -335,3 +337,27 @@ def backward_all(x_bits, dy_bits, W: ExpertWeights, H: int, I: int, E: int, topk
         dW[e] = wgrad_expert(tok[sel], x_bits, dy_bits, out["aw"][sel], out["dg"][sel],
                              out["du"][sel], H, I)
     return dX, dprob, dW
+
+
+def router_backward(x_bits, wr, bias, K: int, dprob, renorm: bool = True, want_dx: bool = True,
+                    want_dwr: bool = True):
+    """Router backward for a given dprob [N,K] (d loss / d p'): the forward
+    router (probabilities and chosen experts) is recomputed by the oracle.
+    Returns dict(dlogits [N,E], dwr [H,E], dbias [E], dx [N,H] (router path),
+    topk_ids, probs)."""
+    L = _bind_backward(lib())
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    wr = np.ascontiguousarray(wr, dtype=np.float32)
+    N, H = x_bits.shape
+    E = wr.shape[1]
+    ids, _, probs, _ = router(x_bits, wr, bias, K, renorm=renorm, want_probs=True)
+    dprob = np.ascontiguousarray(dprob, dtype=np.float32)
+    out = dict(dlogits=np.empty((N, E), np.float32), dbias=np.empty(E, np.float32),
+               dwr=np.empty((H, E), np.float32) if want_dwr else None,
+               dx=np.empty((N, H), np.float32) if want_dx else None, topk_ids=ids, probs=probs)
+    rc = L.oracle_router_backward(N, H, E, K, int(bool(renorm)), _p(x_bits), _p(wr), _p(probs),
+                                  _p(ids), _p(dprob), _p(out["dlogits"]), _p(out["dwr"]),
+                                  _p(out["dbias"]), _p(out["dx"]))
+    if rc != 0:
+        raise RuntimeError("oracle_router_backward failed: %d" % rc)
+    return out

@@ -549,3 +549,72 @@ int oracle_wgrad_expert(int n, const int32_t* tokens, int H, int I, const uint16
   }
   return 0;
 }
+
+/* ======================================================================== */
+/* Router backward: the gradient of the routing probabilities p' (dprob,    */
+/* [N,K], d loss / d p'[t,k]) through top-K renormalisation and the softmax */
+/* to the logits, then to W_r, the bias and x. The chosen set is the one of */
+/* the forward (top-K selection is piecewise constant). Per token t, with   */
+/* p = softmax(l) and the chosen experts e_k:                               */
+/*   renorm:  d = sum_k p[e_k],  p'_k = p[e_k]/d,                           */
+/*            g[e_k] = (dprob_k - sum_j dprob_j p'_j) / d                   */
+/*   no renorm: g[e_k] = dprob_k;   g[e] = 0 for experts not chosen         */
+/*   dl[e] = p[e] * (g[e] - sum_j g[e_j] p[e_j])                            */
+/* and dWr[h,e] = sum_t x[t,h] dl[t,e], dbias[e] = sum_t dl[t,e],           */
+/* dx[t,h] = sum_e dl[t,e] Wr[h,e]. probs [N,E] from oracle_router.         */
+/* Outputs may be NULL except dlogits.                                      */
+/* ======================================================================== */
+int oracle_router_backward(int N, int H, int E, int K, int renorm, const uint16_t* x,
+                           const float* wr, const float* probs, const int32_t* topk_ids,
+                           const float* dprob, float* dlogits, float* dwr, float* dbias,
+                           float* dx) {
+  if (N < 0 || H <= 0 || E <= 0 || K <= 0 || K > E || K > 16 || !dlogits) return -1;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < N; ++t) {
+    const float* p = probs + (size_t)t * E;
+    const int32_t* ids = topk_ids + (size_t)t * K;
+    const float* dp = dprob + (size_t)t * K;
+    float* dl = dlogits + (size_t)t * E;
+    float gk[16];
+    if (renorm) {
+      float d = 0.0f;
+      for (int k = 0; k < K; ++k) d = d + p[ids[k]];
+      float c = 0.0f;
+      for (int k = 0; k < K; ++k) c = c + dp[k] * (p[ids[k]] / d);
+      for (int k = 0; k < K; ++k) gk[k] = (dp[k] - c) / d;
+    } else {
+      for (int k = 0; k < K; ++k) gk[k] = dp[k];
+    }
+    float s = 0.0f;
+    for (int k = 0; k < K; ++k) s = s + gk[k] * p[ids[k]];
+    for (int e = 0; e < E; ++e) dl[e] = -p[e] * s;
+    for (int k = 0; k < K; ++k) dl[ids[k]] = p[ids[k]] * (gk[k] - s);
+  }
+  if (dwr) {
+#pragma omp parallel for schedule(static)
+    for (int h = 0; h < H; ++h)
+      for (int e = 0; e < E; ++e) {
+        float acc = 0.0f;
+        for (int t = 0; t < N; ++t)
+          acc = acc + bf16_to_f32(x[(size_t)t * H + h]) * dlogits[(size_t)t * E + e];
+        dwr[(size_t)h * E + e] = acc;
+      }
+  }
+  if (dbias) {
+    for (int e = 0; e < E; ++e) {
+      float acc = 0.0f;
+      for (int t = 0; t < N; ++t) acc = acc + dlogits[(size_t)t * E + e];
+      dbias[e] = acc;
+    }
+  }
+  if (dx) {
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < N; ++t)
+      for (int h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int e = 0; e < E; ++e) acc = acc + dlogits[(size_t)t * E + e] * wr[(size_t)h * E + e];
+        dx[(size_t)t * H + h] = acc;
+      }
+  }
+  return 0;
+}

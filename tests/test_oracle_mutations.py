@@ -12,6 +12,7 @@ import pytest
 import oracle
 import test_oracle_backward_pins as bp
 import test_oracle_pins as fp
+import test_oracle_router_backward_pins as rb
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
 
@@ -39,6 +40,13 @@ MUTATIONS = [
      "if (aw_out) aw_out[i] = a;", lambda: bp.test_weight_gradients_match_fp64_closed_form()),
     ("dropless extent ignores the ladder", "    if (count <= rung) return rung;", "",
      lambda: bp.test_dropless_layout_hand_worked()),
+    ("router backward skips the renormalisation term", "gk[k] = (dp[k] - c) / d;",
+     "gk[k] = dp[k] / d;", lambda: rb.test_router_backward_matches_central_differences(0, True)),
+    ("router backward skips the softmax normaliser", "dl[ids[k]] = p[ids[k]] * (gk[k] - s);",
+     "dl[ids[k]] = p[ids[k]] * gk[k];", lambda: rb.test_router_backward_matches_central_differences(1, False)),
+    ("router dx with the weight transposed", "acc = acc + dlogits[(size_t)t * E + e] * wr[(size_t)h * E + e];",
+     "acc = acc + dlogits[(size_t)t * E + e] * wr[(size_t)e * H + h];",
+     lambda: rb.test_router_backward_matches_central_differences(2, True)),
 ]
 
 
