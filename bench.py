@@ -565,7 +565,10 @@ def run_ours_train(args):
                   routes=moe.alloc_routes(cfg, dev), ws=moe.alloc_workspace(cfg, dev),
                   bws=moe.alloc_backward_workspace(cfg, dev),
                   preact=torch.empty((S, 2 * I), **bf), dx=torch.empty((N, H), **bf),
-                  dprob=torch.empty((N, K), dtype=torch.float32, device=dev))
+                  dprob=torch.empty((N, K), dtype=torch.float32, device=dev),
+                  rws=moe.alloc_router_backward_workspace(cfg, dev),
+                  dwr=torch.empty((H, E), dtype=torch.float32, device=dev),
+                  dbias=torch.empty(E, dtype=torch.float32, device=dev))
         st["h"], st["o"], st["y"] = moe.alloc_buffers(cfg, dev)
         return st
 
@@ -586,9 +589,13 @@ def run_ours_train(args):
                          st["dprob"], st["bws"], stream)
         if evs is not None:
             evs[4].record(stream)
+        moe.router_backward(c, r, st["x"], st["wr"], st["bias"], st["dprob"], st["dx"], st["dwr"],
+                            st["dbias"], st["rws"], stream)
+        if evs is not None:
+            evs[5].record(stream)
 
     def time_steps(st, steps):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(dist, dev)
         torch.cuda.synchronize()
@@ -599,7 +606,8 @@ def run_ours_train(args):
         torch.cuda.synchronize()
         barrier(dist, dev)
         per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
-               for j, n in enumerate(("route", "ffn_forward", "combine", "ffn_backward"))}
+               for j, n in enumerate(("route", "ffn_forward", "combine", "ffn_backward",
+                                      "router_backward"))}
         return max_over_ranks(a.elapsed_time(b), dist, dev) / steps, per
 
     # ---- sweep over N (the curve), then the headline at N = base.n_tokens
@@ -615,7 +623,7 @@ def run_ours_train(args):
         sweep[str(N)] = {"ms_per_step": ms, "tokens_per_s": N * world / (ms / 1e3),
                          "tflops": 18.0 * R * H * I / (ms / 1e3) / 1e12,
                          "fwd_ms": per["route"] + per["ffn_forward"] + per["combine"],
-                         "bwd_ms": per["ffn_backward"]}
+                         "bwd_ms": per["ffn_backward"] + per["router_backward"]}
         del st
         torch.cuda.empty_cache()
     st = setup(base.n_tokens)
@@ -637,7 +645,7 @@ def run_ours_train(args):
     sweep[str(N)] = {"ms_per_step": ms, "tokens_per_s": N * world / (ms / 1e3),
                      "tflops": 18.0 * R * H * I / (ms / 1e3) / 1e12,
                      "fwd_ms": per["route"] + per["ffn_forward"] + per["combine"],
-                     "bwd_ms": per["ffn_backward"]}
+                     "bwd_ms": per["ffn_backward"] + per["router_backward"]}
 
     # ---- end to end: x and dY in from pinned host memory, y, dX and dprob out
     xh = torch.from_numpy(st["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()

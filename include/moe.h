@@ -229,6 +229,34 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
                      void* dx, float* dw13, float* dw2, float* dprob, void* workspace,
                      size_t ws_bytes, cudaStream_t stream);
 
+/* Bytes of scratch moe_router_backward needs: N*E*4 for the logit gradient
+ * plus the per-split partial sums of dW_r (about two CTA tiles per SM). */
+int64_t moe_router_backward_workspace_bytes(const moe_config_t* cfg);
+
+/* Router backward: the gradient of the routing probabilities p' (dprob, e.g.
+ * from moe_ffn_backward) through top-K renormalisation and the softmax to the
+ * logits, then to the router weight, the bias and x. The chosen experts are
+ * those in routes->topk_ids (moe_route_align of the same x, W_r, bias): top-K
+ * selection is piecewise constant, so it passes no gradient. The pages'
+ * routing probabilities carry a gradient to the router ("Permute-Free Grouped
+ * GEMM for MoE (bf16, gfx950)", section 6: the SwiGLU backward optionally
+ * computes the route-prob grad); this call continues that gradient. Per token,
+ * with p = softmax(l) recomputed exactly as moe_route_align computes it:
+ *   renorm: d = sum_k p[e_k], c = sum_k dprob_k p'_k, g_k = (dprob_k - c)/d
+ *   else:   g_k = dprob_k;   s = sum_k g_k p[e_k]
+ *   dl[e] = p[e] (g[e] - s)   (g = 0 for the experts not chosen)
+ *  x, w_router, bias   the forward's inputs (bias may be NULL)
+ *  dprob      [N,K] f32 d loss / d p'
+ *  dx         [N,H] bf16, in/out: dx += dl . W_r^T, summed in fp32 and rounded
+ *             to bf16 once (add the router's path to the experts' dX)
+ *  dw_router  [H,E] f32 output: sum_t x[t,:]^T dl[t,:]
+ *  dbias      [E] f32 output sum_t dl[t,:], or NULL
+ * Outputs other than dx are overwritten. fp32 throughout; deterministic. */
+int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                        const float* w_router, const float* bias, const float* dprob, void* dx,
+                        float* dw_router, float* dbias, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream);
+
 /* Size of the library's built-in route scratch used by moe_route_align_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 

@@ -29,6 +29,7 @@ __all__ = [
     "route_align", "fc1_forward", "fc2_forward", "ffn_forward", "combine", "pack_w13",
     "pack_w2", "status_string", "launch_count", "device_error", "forward",
     "ffn_forward_train", "backward_workspace_bytes", "alloc_backward_workspace", "ffn_backward",
+    "router_backward_workspace_bytes", "alloc_router_backward_workspace", "router_backward",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -95,7 +96,7 @@ def lib():
         CP = ctypes.POINTER(Config)
         RP = ctypes.POINTER(_RoutesC)
         for name in ("moe_capacity", "moe_max_slots", "moe_max_blocks", "moe_route_workspace_bytes",
-                     "moe_backward_workspace_bytes"):
+                     "moe_backward_workspace_bytes", "moe_router_backward_workspace_bytes"):
             getattr(L, name).argtypes = [CP]
             getattr(L, name).restype = I64
         L.moe_route_align.argtypes = [CP, P, P, P, RP, P, SZ, P]
@@ -105,11 +106,12 @@ def lib():
         L.moe_combine.argtypes = [CP, RP, P, P, P]
         L.moe_ffn_forward_train.argtypes = [CP, RP, P, P, P, P, P, P, P]
         L.moe_ffn_backward.argtypes = [CP, RP, P, P, P, P, P, P, P, P, P, P, SZ, P]
+        L.moe_router_backward.argtypes = [CP, RP, P, P, P, P, P, P, P, P, SZ, P]
         L.moe_pack_w13.argtypes = [CP, P, P, P, P]
         L.moe_pack_w2.argtypes = [CP, P, P, P]
         for name in ("moe_route_align", "moe_fc1_forward", "moe_fc2_forward", "moe_ffn_forward",
                      "moe_combine", "moe_pack_w13", "moe_pack_w2", "moe_ffn_forward_train",
-                     "moe_ffn_backward"):
+                     "moe_ffn_backward", "moe_router_backward"):
             getattr(L, name).restype = I32
         L.moe_status_string.argtypes = [I32]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -240,6 +242,27 @@ def ffn_backward(cfg: Config, routes: Routes, x, w13, w2, preact, dy, dx, dw13, 
                                   _ptr(w2), _ptr(preact), _ptr(dy), _ptr(dx), _ptr(dw13),
                                   _ptr(dw2), _ptr(dprob), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def router_backward_workspace_bytes(cfg: Config) -> int:
+    return _q("moe_router_backward_workspace_bytes", cfg)
+
+
+def alloc_router_backward_workspace(cfg: Config, device):
+    import torch
+    return torch.empty(max(router_backward_workspace_bytes(cfg), 256), dtype=torch.uint8, device=device)
+
+
+def router_backward(cfg: Config, routes: Routes, x, w_router, bias, dprob, dx, dw_router, dbias,
+                    workspace, stream=None) -> None:
+    """Router backward: dx += dl . W_r^T (bf16, in place), dw_router [H,E] f32 and
+    dbias [E] f32 (or None) overwritten."""
+    _check("moe_router_backward",
+           lib().moe_router_backward(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(x),
+                                     _ptr(w_router), _ptr(bias), _ptr(dprob), _ptr(dx),
+                                     _ptr(dw_router), _ptr(dbias), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
 
 
 def combine(cfg: Config, routes: Routes, o, y, stream=None) -> None:

@@ -452,6 +452,63 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
   return finish(launched);
 }
 
+static void router_bwd_layout(const moe_config_t* c, size_t* dl_off, size_t* part_off,
+                              size_t* total) {
+  const int64_t N = c->n_tokens, H = c->hidden, E = c->n_experts;
+  const int splits = N > 0 ? moe::router_bwd_splits((int)N, (int)H, (int)E) : 0;
+  *dl_off = 0;
+  *part_off = (size_t)((N * E * 4 + 255) / 256 * 256);
+  *total = *part_off + (size_t)((splits * H * E * 4 + 255) / 256 * 256);
+}
+
+int64_t moe_router_backward_workspace_bytes(const moe_config_t* cfg) {
+  const int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  size_t a, b, t;
+  router_bwd_layout(cfg, &a, &b, &t);
+  return (int64_t)t;
+}
+
+int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                        const float* w_router, const float* bias, const float* dprob, void* dx,
+                        float* dw_router, float* dbias, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!routes || !routes->topk_ids || !w_router || !dw_router) return MOE_ERR_INVALID_ARG;
+  size_t dl_off, part_off, total;
+  router_bwd_layout(cfg, &dl_off, &part_off, &total);
+  if (cfg->n_tokens > 0 && (!workspace || ws_bytes < total || !aligned16(workspace)))
+    return MOE_ERR_WORKSPACE;
+  if (cfg->n_tokens > 0 && (!x || !dprob || !dx || !aligned16(x)))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->n_tokens == 0) {  // no token: zero gradients
+    if (cudaMemsetAsync(dw_router, 0, (size_t)cfg->hidden * cfg->n_experts * 4, stream) !=
+            cudaSuccess ||
+        (dbias && cudaMemsetAsync(dbias, 0, (size_t)cfg->n_experts * 4, stream) != cudaSuccess))
+      return finish(-1);
+    return MOE_OK;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  moe::RouterBwdArgs a{};
+  a.N = cfg->n_tokens;
+  a.H = cfg->hidden;
+  a.E = cfg->n_experts;
+  a.K = cfg->top_k;
+  a.renorm = cfg->renorm;
+  a.x = static_cast<const uint16_t*>(x);
+  a.wr = w_router;
+  a.bias = bias;
+  a.topk_ids = routes->topk_ids;
+  a.dprob = dprob;
+  a.dl = reinterpret_cast<float*>(ws + dl_off);
+  a.part = reinterpret_cast<float*>(ws + part_off);
+  a.dwr = dw_router;
+  a.dbias = dbias;
+  a.dx = static_cast<uint16_t*>(dx);
+  return finish(moe::launch_router_backward(a, stream));
+}
+
 const char* moe_status_string(int status) {
   switch (status) {
     case MOE_OK: return "ok";

@@ -100,6 +100,25 @@ struct WgradArgs {
 
 int launch_wgrad(const WgradArgs& a, cudaStream_t s);
 
+// Router backward (route.cu): logits recomputed into dl, dl = d loss / d logits
+// from dprob, then dW_r (split over tokens, partials in part), dbias, and
+// dx += dl . W_r^T (bf16 in/out).
+struct RouterBwdArgs {
+  int N, H, E, K, renorm;
+  const uint16_t* x;
+  const float* wr;
+  const float* bias;
+  const int32_t* topk_ids;
+  const float* dprob;
+  float* dl;        // [N,E] workspace
+  float* part;      // [splits,H,E] workspace
+  float* dwr;       // [H,E]
+  float* dbias;     // [E] or null
+  uint16_t* dx;     // [N,H] bf16, accumulated
+};
+int router_bwd_splits(int N, int H, int E);
+int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s);
+
 // Backward helpers (combine.cu).
 // slot_prob[s] = topk_p of the route t*K+k held by slot s, 0 for padding;
 // also zeroes sched_zero[0..n_zero).

@@ -18,6 +18,7 @@
 // section 4 Data structures and section 5 Kernels (route_list_scan,
 // route_list_align). Capacity and drop-and-pad: "feat(cuda-graphs): capture
 // fixed-capacity MoE execution", Design notes.
+#include <cuda_bf16.h>
 #include <math.h>
 
 #include "moe_internal.h"
@@ -537,6 +538,271 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
   }
 }
 
+
+// ---------------------------------------------------------------- router backward
+// The gradient of the routing probabilities p' (dprob [N,K]) through top-K
+// renormalisation and the softmax to the logits, with the chosen experts of
+// the forward held fixed (the selection is piecewise constant). One warp per
+// token recomputes p exactly as the forward does (same exp, ascending-e sum,
+// IEEE divide), then, with the chosen experts e_k:
+//   renorm: d = sum_k p[e_k], c = sum_k dprob_k p[e_k]/d, g_k = (dprob_k - c)/d
+//   else:   g_k = dprob_k
+//   s = sum_k g_k p[e_k];  dl[e] = p[e] (g[e] - s), g[e] = 0 for the others.
+// dl overwrites the logits.
+constexpr int kDlWarps = 8;
+
+__global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
+    float* __restrict__ ld, int N, int E, int K, int renorm, const int32_t* __restrict__ topk_ids,
+    const float* __restrict__ dprob) {
+  __shared__ float pbuf[kDlWarps][kMaxExperts];
+  __shared__ float gk_s[kDlWarps][kMaxTopK];
+  __shared__ int32_t id_s[kDlWarps][kMaxTopK];
+  __shared__ float s_s[kDlWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kDlWarps + warp;
+  if (t >= N) return;
+  constexpr int PER = kMaxExperts / 32;
+  float* l = ld + (size_t)t * E;
+  float v[PER];
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = (e < E) ? l[e] : -INFINITY;
+    m = fmaxf(m, v[j]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    if (e < E) {
+      v[j] = route_exp(__fsub_rn(v[j], m));
+      pbuf[warp][e] = v[j];
+    }
+  }
+  __syncwarp();
+  float sum = 0.0f;
+  if (lane == 0)
+    for (int e = 0; e < E; ++e) sum = __fadd_rn(sum, pbuf[warp][e]);  // ascending e
+  sum = __shfl_sync(0xFFFFFFFFu, sum, 0);
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = __fdiv_rn(v[j], sum);
+    if (e < E) pbuf[warp][e] = v[j];
+  }
+  if (lane < K) id_s[warp][lane] = topk_ids[(size_t)t * K + lane];
+  __syncwarp();
+  if (lane == 0) {
+    float d = 0.0f, c = 0.0f, sg = 0.0f;
+    if (renorm) {
+      for (int k = 0; k < K; ++k) d = __fadd_rn(d, pbuf[warp][id_s[warp][k]]);
+      for (int k = 0; k < K; ++k)
+        c = __fadd_rn(c, __fmul_rn(dprob[(size_t)t * K + k], __fdiv_rn(pbuf[warp][id_s[warp][k]], d)));
+    }
+    for (int k = 0; k < K; ++k) {
+      const float dp = dprob[(size_t)t * K + k];
+      const float g = renorm ? __fdiv_rn(__fsub_rn(dp, c), d) : dp;
+      gk_s[warp][k] = g;
+      sg = __fadd_rn(sg, __fmul_rn(g, pbuf[warp][id_s[warp][k]]));
+    }
+    s_s[warp] = sg;
+  }
+  __syncwarp();
+  const float sg = s_s[warp];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    if (e >= E) continue;
+    float g = 0.0f;
+    for (int k = 0; k < K; ++k)
+      if (id_s[warp][k] == e) g = gk_s[warp][k];
+    l[e] = __fmul_rn(v[j], __fsub_rn(g, sg));
+  }
+}
+
+// dW_r[h,e] = sum_t x[t,h] dl[t,e] over the tokens of one split (64 x 64 CTA
+// tile, 4 x 4 per thread, 32 tokens per stage, the next stage's loads held in
+// registers while this stage is computed); partial sums of split z go to
+// part + z*H*E, each a sequential sum over ascending t within the split.
+// (vec: H a multiple of 4 and E a multiple of 4, so a thread's 4 columns are
+// one 8-byte x load and one 16-byte dl load.)
+constexpr int kRbTile = 64, kDwK = 32;
+
+__global__ void __launch_bounds__(256) router_dwr_kernel(const uint16_t* __restrict__ x,
+                                                         const float* __restrict__ dl, int N, int H,
+                                                         int E, int t_per_split, int vec,
+                                                         float* __restrict__ part) {
+  __shared__ __align__(16) float as[2][kDwK][kRbTile];
+  __shared__ __align__(16) float bs[2][kDwK][kRbTile];
+  const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+  const int e0 = blockIdx.x * kRbTile, h0 = blockIdx.y * kRbTile;
+  const int ta = blockIdx.z * t_per_split, tb = min(N, ta + t_per_split);
+  // this thread's loads of each 32 x 64 stage tile: rows lk and lk + 16, 4 columns
+  const int lk = tid / 16, lc = (tid % 16) * 4;
+  float ra[2][4], rb[2][4];
+  auto fetch = [&](int t0) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int t = t0 + lk + 16 * r;
+      const bool ok = t < tb;
+      if (vec) {
+        uint2 xv = make_uint2(0u, 0u);
+        float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok && h0 + lc < H) xv = *reinterpret_cast<const uint2*>(x + (size_t)t * H + h0 + lc);
+        if (ok && e0 + lc < E) dv = *reinterpret_cast<const float4*>(dl + (size_t)t * E + e0 + lc);
+        ra[r][0] = __uint_as_float(xv.x << 16);
+        ra[r][1] = __uint_as_float(xv.x & 0xFFFF0000u);
+        ra[r][2] = __uint_as_float(xv.y << 16);
+        ra[r][3] = __uint_as_float(xv.y & 0xFFFF0000u);
+        rb[r][0] = dv.x; rb[r][1] = dv.y; rb[r][2] = dv.z; rb[r][3] = dv.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          ra[r][j] = (ok && h0 + lc + j < H)
+                         ? __uint_as_float((uint32_t)x[(size_t)t * H + h0 + lc + j] << 16) : 0.0f;
+          rb[r][j] = (ok && e0 + lc + j < E) ? dl[(size_t)t * E + e0 + lc + j] : 0.0f;
+        }
+      }
+    }
+  };
+  float acc[4][4] = {};
+  if (ta < tb) fetch(ta);
+  int buf = 0;
+  for (int t0 = ta; t0 < tb; t0 += kDwK, buf ^= 1) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      *reinterpret_cast<float4*>(&as[buf][lk + 16 * r][lc]) =
+          make_float4(ra[r][0], ra[r][1], ra[r][2], ra[r][3]);
+      *reinterpret_cast<float4*>(&bs[buf][lk + 16 * r][lc]) =
+          make_float4(rb[r][0], rb[r][1], rb[r][2], rb[r][3]);
+    }
+    __syncthreads();
+    if (t0 + kDwK < tb) fetch(t0 + kDwK);  // next stage's loads overlap this stage's math
+#pragma unroll
+    for (int k = 0; k < kDwK; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(&as[buf][k][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&bs[buf][k][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+    }
+  }
+  float* out = part + (size_t)blockIdx.z * H * E;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int h = h0 + ty * 4 + i;
+    if (h >= H) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) out[(size_t)h * E + e] = acc[i][j];
+    }
+  }
+}
+
+// dW_r = sum of the splits' partials in split order.
+__global__ void router_dwr_reduce_kernel(const float* __restrict__ part, int splits, int64_t n,
+                                         float* __restrict__ dwr) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float acc = 0.0f;
+  for (int z = 0; z < splits; ++z) acc = __fadd_rn(acc, part[(size_t)z * n + i]);
+  dwr[i] = acc;
+}
+
+// dbias[e] = sum_t dl[t,e]: each of 256 threads sums a strided set of tokens
+// in ascending order, then a fixed-order tree over the threads.
+__global__ void __launch_bounds__(256) router_dbias_kernel(const float* __restrict__ dl, int N,
+                                                           int E, float* __restrict__ dbias) {
+  __shared__ float red[256];
+  const int e = blockIdx.x;
+  float acc = 0.0f;
+  for (int t = threadIdx.x; t < N; t += 256) acc = __fadd_rn(acc, dl[(size_t)t * E + e]);
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) red[threadIdx.x] = __fadd_rn(red[threadIdx.x], red[threadIdx.x + w]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) dbias[e] = red[0];
+}
+
+// dx[t,h] += sum_e dl[t,e] W_r[h,e] (fp32, rounded to bf16 once). 64 tokens x
+// 64 rows of W_r per CTA; both operands are staged 64 experts at a time as
+// rows (e contiguous, padded to 68 floats), and a thread takes 4 tokens x 4
+// rows of W_r (tx + 16j: the 8 threads of a quarter-warp hit 8 different
+// 16-byte bank groups), reading 16 bytes (4 experts) of each row per step:
+// 8 loads per 64 fma.
+constexpr int kDxE = 64, kDxPad = kDxE + 4;
+
+__global__ void __launch_bounds__(256) router_dx_kernel(const float* __restrict__ dl,
+                                                        const float* __restrict__ wr, int N, int H,
+                                                        int E, int vec4, uint16_t* __restrict__ dx) {
+  __shared__ __align__(16) float ds[kRbTile][kDxPad];
+  __shared__ __align__(16) float ws_[kRbTile][kDxPad];
+  const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+  const int h0 = blockIdx.x * kRbTile, t0 = blockIdx.y * kRbTile;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < E; k0 += kDxE) {
+    const int ke = min(kDxE, E - k0);
+    for (int i = tid; i < kRbTile * (kDxE / 4); i += 256) {
+      const int r = i / (kDxE / 4), q = (i % (kDxE / 4)) * 4;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (vec4) {  // E a multiple of 4, 16-byte rows
+        if (q < ke && t0 + r < N) a = *reinterpret_cast<const float4*>(dl + (size_t)(t0 + r) * E + k0 + q);
+        if (q < ke && h0 + r < H) b = *reinterpret_cast<const float4*>(wr + (size_t)(h0 + r) * E + k0 + q);
+      } else {
+        float av[4] = {0.f, 0.f, 0.f, 0.f}, bv[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < 4; ++j) {
+          if (q + j >= ke) break;
+          if (t0 + r < N) av[j] = dl[(size_t)(t0 + r) * E + k0 + q + j];
+          if (h0 + r < H) bv[j] = wr[(size_t)(h0 + r) * E + k0 + q + j];
+        }
+        a = make_float4(av[0], av[1], av[2], av[3]);
+        b = make_float4(bv[0], bv[1], bv[2], bv[3]);
+      }
+      *reinterpret_cast<float4*>(&ds[r][q]) = a;
+      *reinterpret_cast<float4*>(&ws_[r][q]) = b;
+    }
+    __syncthreads();
+    for (int k = 0; k < ke; k += 4) {
+      float4 a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(&ds[ty * 4 + i][k]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = *reinterpret_cast<const float4*>(&ws_[tx + 16 * j][k]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = __fmaf_rn(a[i].x, b[j].x, acc[i][j]);
+          acc[i][j] = __fmaf_rn(a[i].y, b[j].y, acc[i][j]);
+          acc[i][j] = __fmaf_rn(a[i].z, b[j].z, acc[i][j]);
+          acc[i][j] = __fmaf_rn(a[i].w, b[j].w, acc[i][j]);
+        }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= N) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int h = h0 + tx + 16 * j;
+      if (h >= H) continue;
+      uint16_t* q = dx + (size_t)t * H + h;
+      const float v = __fadd_rn(__uint_as_float((uint32_t)*q << 16), acc[i][j]);
+      *q = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+  }
+}
+
 }  // namespace
 
 int launch_route(const RouteArgs& a, cudaStream_t s) {
@@ -578,6 +844,55 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;
   return launched;
+}
+
+int router_bwd_splits(int N, int H, int E) {
+  const int tiles = ((E + kRbTile - 1) / kRbTile) * ((H + kRbTile - 1) / kRbTile);
+  int splits = (2 * 152 + tiles - 1) / tiles;  // about two CTAs per SM
+  const int max_splits = (N + 255) / 256;      // at least 256 tokens per split
+  if (splits > max_splits) splits = max_splits;
+  return splits < 1 ? 1 : splits;
+}
+
+int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
+  if (a.N <= 0) return 0;
+  int launched = 0;
+  // logits recomputed exactly as the forward (into the dl buffer)
+  RouteArgs r{};
+  r.N = a.N;
+  r.H = a.H;
+  r.E = a.E;
+  r.x = a.x;
+  r.wr = a.wr;
+  r.bias = a.bias;
+  r.ws.logits = a.dl;
+  const int vec4 = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 15u) == 0);
+  cudaError_t err = (a.E > 64) ? launch_router_logits<64, 128, 4, 8>(r, vec4, s)
+                               : launch_router_logits<64, 64, 4, 4>(r, vec4, s);
+  if (err != cudaSuccess) return -(int)err;
+  ++launched;
+  router_dlogits_kernel<<<(a.N + kDlWarps - 1) / kDlWarps, kDlWarps * 32, 0, s>>>(
+      a.dl, a.N, a.E, a.K, a.renorm, a.topk_ids, a.dprob);
+  ++launched;
+  const int splits = router_bwd_splits(a.N, a.H, a.E);
+  const int tps = ((a.N + splits - 1) / splits + kDwK - 1) / kDwK * kDwK;
+  dim3 g1((a.E + kRbTile - 1) / kRbTile, (a.H + kRbTile - 1) / kRbTile, splits);
+  const int dw_vec = (a.H % 4 == 0) && (a.E % 4 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(a.x) & 7u) == 0);
+  router_dwr_kernel<<<g1, 256, 0, s>>>(a.x, a.dl, a.N, a.H, a.E, tps, dw_vec, a.part);
+  ++launched;
+  const int64_t n = (int64_t)a.H * a.E;
+  router_dwr_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.part, splits, n, a.dwr);
+  ++launched;
+  if (a.dbias) {
+    router_dbias_kernel<<<a.E, 256, 0, s>>>(a.dl, a.N, a.E, a.dbias);
+    ++launched;
+  }
+  dim3 g2((a.H + kRbTile - 1) / kRbTile, (a.N + kRbTile - 1) / kRbTile);
+  router_dx_kernel<<<g2, 256, 0, s>>>(a.dl, a.wr, a.N, a.H, a.E, vec4, a.dx);
+  ++launched;
+  err = cudaGetLastError();
+  return err == cudaSuccess ? launched : -(int)err;
 }
 
 }  // namespace moe
