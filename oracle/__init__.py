@@ -51,11 +51,12 @@ def lib():
         L.oracle_router.restype = i32
         L.oracle_select_layout.argtypes = [i32, i32, i32, i64, i32, P, P, P, P, P, P, P, P, P, P]
         L.oracle_select_layout.restype = i32
-        L.oracle_ffn_routes.argtypes = [i32, P, P, i32, i32, P, P, P, P, P, P]
+        L.oracle_ffn_routes.argtypes = [i32, P, P, i32, i32, P, P, P, P, i32, P, P, P]
         L.oracle_ffn_routes.restype = i32
         L.oracle_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
         L.oracle_combine.restype = i32
-        L.oracle_forward_tokens.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P]
+        L.oracle_forward_tokens.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32, i32,
+                                            P]
         L.oracle_forward_tokens.restype = i32
         L.oracle_num_threads.restype = i32
         L.oracle_set_num_threads.argtypes = [i32]
@@ -157,25 +158,34 @@ class ExpertWeights:
                 table[e] = a.ctypes.data
 
 
+ACT_SILU, ACT_GELU = 0, 1
+
+
 def ffn_routes(tokens: Sequence[int], experts: Sequence[int], x_bits: np.ndarray,
-               W: ExpertWeights, H: int, I: int, want_h: bool = False):
-    """FFN output o [n,H] (and activation a [n,I]) of the given (token, expert) pairs."""
+               W: ExpertWeights, H: int, I: int, want_h: bool = False, act: int = ACT_SILU,
+               scales: Optional[np.ndarray] = None):
+    """FFN output o [n,H] (and activation a [n,I]) of the given (token, expert)
+    pairs; act: 0 silu, 1 gelu; scales [n]: per-route factor of the activation
+    (p' when the routing probability is applied in the activation)."""
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     experts = np.ascontiguousarray(experts, dtype=np.int32)
     n = len(tokens)
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     o = np.empty((n, H), dtype=np.float32)
     h = np.empty((n, I), dtype=np.float32) if want_h else None
+    sc = None if scales is None else np.ascontiguousarray(scales, dtype=np.float32)
     rc = lib().oracle_ffn_routes(n, _p(tokens), _p(experts), H, I, _p(x_bits), W.wg, W.wu, W.wd,
-                                 _p(h), _p(o))
+                                 int(act), _p(sc), _p(h), _p(o))
     if rc != 0:
         raise RuntimeError("oracle_ffn_routes failed: %d" % rc)
     return (o, h) if want_h else o
 
 
-def combine(t0: int, t1: int, keep: np.ndarray, topk_p: np.ndarray, o_routes: np.ndarray) -> np.ndarray:
+def combine(t0: int, t1: int, keep: np.ndarray, topk_p: Optional[np.ndarray],
+            o_routes: np.ndarray) -> np.ndarray:
+    """topk_p None: unit weights."""
     keep = np.ascontiguousarray(keep, dtype=np.uint8)
-    topk_p = np.ascontiguousarray(topk_p, dtype=np.float32)
+    topk_p = None if topk_p is None else np.ascontiguousarray(topk_p, dtype=np.float32)
     o_routes = np.ascontiguousarray(o_routes, dtype=np.float32)
     K = keep.shape[1]
     H = o_routes.shape[-1]
@@ -185,15 +195,18 @@ def combine(t0: int, t1: int, keep: np.ndarray, topk_p: np.ndarray, o_routes: np
 
 
 def forward_tokens(t0: int, t1: int, x_bits: np.ndarray, W: ExpertWeights, H: int, I: int,
-                   topk_ids: np.ndarray, topk_p: np.ndarray, keep: np.ndarray) -> np.ndarray:
-    """Layer output y [t1-t0, H] (fp32) for tokens [t0, t1)."""
+                   topk_ids: np.ndarray, topk_p: np.ndarray, keep: np.ndarray, act: int = ACT_SILU,
+                   prob_in_act: bool = False) -> np.ndarray:
+    """Layer output y [t1-t0, H] (fp32) for tokens [t0, t1); act 0 silu, 1 gelu;
+    prob_in_act: p' multiplies the activation and the combine uses unit weights."""
     K = topk_ids.shape[1]
     y = np.empty((max(t1 - t0, 0), H), dtype=np.float32)
     rc = lib().oracle_forward_tokens(t0, t1, K, H, I, _p(np.ascontiguousarray(x_bits, dtype=np.uint16)),
                                      W.wg, W.wu, W.wd,
                                      _p(np.ascontiguousarray(topk_ids, dtype=np.int32)),
                                      _p(np.ascontiguousarray(topk_p, dtype=np.float32)),
-                                     _p(np.ascontiguousarray(keep, dtype=np.uint8)), _p(y))
+                                     _p(np.ascontiguousarray(keep, dtype=np.uint8)), int(act),
+                                     int(bool(prob_in_act)), _p(y))
     if rc != 0:
         raise RuntimeError("oracle_forward_tokens failed: %d" % rc)
     return y
@@ -225,7 +238,7 @@ def _bind_backward(L):
     L.oracle_dropless_layout.argtypes = [i32, i32, i32, i32, P, i32, i32, i64, P, P, P, P, P, P, P,
                                          P]
     L.oracle_dropless_layout.restype = i32
-    L.oracle_bwd_routes.argtypes = [i32, P, P, P, i32, i32, P, P, P, P, P, P, P, P, P, P]
+    L.oracle_bwd_routes.argtypes = [i32, P, P, P, i32, i32, i32, P, P, P, P, P, P, P, P, P, P]
     L.oracle_bwd_routes.restype = i32
     L.oracle_wgrad_expert.argtypes = [i32, P, i32, i32, P, P, P, P, P, P, P, P]
     L.oracle_wgrad_expert.restype = i32
@@ -277,7 +290,8 @@ def dropless_layout(topk_ids: np.ndarray, E: int, bm: int, ladder_num, ladder_de
     return DroplessLayout(ec, ex, bs, ssi, eid, int(ntpp[0]), tr)
 
 
-def bwd_routes(tokens, experts, probs, x_bits, dy_bits, W: ExpertWeights, H: int, I: int):
+def bwd_routes(tokens, experts, probs, x_bits, dy_bits, W: ExpertWeights, H: int, I: int,
+               act: int = ACT_SILU):
     """Per-route backward: (dprob [n], dxr [n,H], dg [n,I], du [n,I], aw [n,I])."""
     L = _bind_backward(lib())
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
@@ -287,7 +301,7 @@ def bwd_routes(tokens, experts, probs, x_bits, dy_bits, W: ExpertWeights, H: int
     out = dict(dprob=np.empty(n, np.float32), dxr=np.empty((n, H), np.float32),
                dg=np.empty((n, I), np.float32), du=np.empty((n, I), np.float32),
                aw=np.empty((n, I), np.float32))
-    rc = L.oracle_bwd_routes(n, _p(tokens), _p(experts), _p(probs), H, I,
+    rc = L.oracle_bwd_routes(n, _p(tokens), _p(experts), _p(probs), H, I, int(act),
                              _p(np.ascontiguousarray(x_bits, dtype=np.uint16)),
                              _p(np.ascontiguousarray(dy_bits, dtype=np.uint16)), W.wg, W.wu, W.wd,
                              _p(out["dprob"]), _p(out["dxr"]), _p(out["dg"]), _p(out["du"]),
@@ -314,7 +328,7 @@ def wgrad_expert(tokens, x_bits, dy_bits, aw, dg, du, H: int, I: int):
 
 
 def backward_all(x_bits, dy_bits, W: ExpertWeights, H: int, I: int, E: int, topk_ids, topk_p,
-                 token_routes):
+                 token_routes, act: int = ACT_SILU):
     """Whole expert-path backward: dX [N,H], dprob [N,K], dW per expert (dicts).
     Routes are processed in slot order per expert (token_routes gives the slot)."""
     N, K = topk_ids.shape
@@ -322,7 +336,7 @@ def backward_all(x_bits, dy_bits, W: ExpertWeights, H: int, I: int, E: int, topk
     tok, kk = r // K, r % K
     ex = topk_ids.ravel()[r]
     pr = topk_p.ravel()[r]
-    out = bwd_routes(tok, ex, pr, x_bits, dy_bits, W, H, I)
+    out = bwd_routes(tok, ex, pr, x_bits, dy_bits, W, H, I, act=act)
     dX = np.zeros((N, H), np.float32)
     for k in range(K):  # k order
         m = kk == k

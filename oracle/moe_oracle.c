@@ -18,8 +18,9 @@
  *      sentinel N, expert_ids (-1 for blocks without a kept route),
  *      block_start, num_tokens_post_padded, token_routes ("Permute-Free ...",
  *      section 4 "Data structures")
- *   5. expert FFN on kept routes: FC1 on the gathered row, SwiGLU
- *      silu(gate)*up, FC2 ("Permute-Free ...", section 3 "End-to-end flow")
+ *   5. expert FFN on kept routes: FC1 on the gathered row, the gated
+ *      activation act(gate)*up (silu or gelu; optionally times p'), FC2
+ *      ("Permute-Free ...", section 3 "End-to-end flow")
  *   6. gather-combine: each token sums its kept routes weighted by routing
  *      probability ("Permute-Free ...", section 2 "Core idea")
  * Dropless, bucketed variant and backward (second half of the file):
@@ -253,15 +254,40 @@ int oracle_select_layout(int N, int E, int K, int64_t cap, int bm, const int32_t
 }
 
 /* ------------------------------------------------------------------------ */
+/* Gated activations of the expert FFN, act(gate) * up ("Permute-Free       */
+/* Grouped GEMM for MoE (bf16, gfx950)", section 3: act(gate)*up; section 8: */
+/* silu and gelu). act 0: silu(v) = v * sigma(v) = v / (1 + exp(-v)).        */
+/* act 1: gelu(v) = v * Phi(v) = 0.5 v (1 + erf(v / sqrt 2)), the exact form.*/
+/* act_grad is the derivative: silu' = sigma(v) (1 + v (1 - sigma(v))),      */
+/* gelu' = Phi(v) + v phi(v), phi(v) = exp(-v^2/2) / sqrt(2 pi).             */
+/* ------------------------------------------------------------------------ */
+static float act_fn(int act, float v) {
+  if (act == 1) return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+  return v / (1.0f + expf(-v));
+}
+
+static float act_grad(int act, float v) {
+  if (act == 1) {
+    const float cdf = 0.5f * (1.0f + erff(v * 0.70710678118654752f));
+    const float pdf = expf(-0.5f * v * v) * 0.39894228040143268f;
+    return cdf + v * pdf;
+  }
+  const float sg = 1.0f / (1.0f + expf(-v));
+  return sg * (1.0f + v * (1.0f - sg));
+}
+
+/* ------------------------------------------------------------------------ */
 /* Step 5: expert FFN for one route: token row x[t], expert e.               */
 /*   g_i = sum_h x_h*Wg[e,h,i], u_i = sum_h x_h*Wu[e,h,i] (ascending h),     */
-/*   a_i = silu(g_i)*u_i with silu(v) = v/(1+exp(-v)),                       */
+/*   a_i = act(g_i)*u_i*scale (scale = p' when the routing probability is    */
+/*   applied in the activation, else 1),                                     */
 /*   o_j = sum_i a_i*Wd[e,i,j] (ascending i).                                */
 /* wg/wu point at expert e's [H,I] block, wd at its [I,H] block (bf16 bits). */
 /* h_out (optional, [I]) receives a; o_out ([H]) receives o.                 */
 /* ------------------------------------------------------------------------ */
 static void ffn_one(int H, int I, const uint16_t* xrow, const uint16_t* wg, const uint16_t* wu,
-                    const uint16_t* wd, float* g, float* u, float* h_out, float* o_out) {
+                    const uint16_t* wd, int act, float scale, float* g, float* u, float* h_out,
+                    float* o_out) {
   for (int i = 0; i < I; ++i) { g[i] = 0.0f; u[i] = 0.0f; }
   for (int h = 0; h < H; ++h) {
     const float xv = bf16_to_f32(xrow[h]);
@@ -273,8 +299,7 @@ static void ffn_one(int H, int I, const uint16_t* xrow, const uint16_t* wg, cons
     }
   }
   for (int i = 0; i < I; ++i) {
-    const float s = g[i] / (1.0f + expf(-g[i]));
-    g[i] = s * u[i]; /* g now holds the activation a */
+    g[i] = act_fn(act, g[i]) * u[i] * scale; /* g now holds the activation a */
     if (h_out) h_out[i] = g[i];
   }
   for (int j = 0; j < H; ++j) o_out[j] = 0.0f;
@@ -287,10 +312,12 @@ static void ffn_one(int H, int I, const uint16_t* xrow, const uint16_t* wg, cons
 
 /* FFN for a list of (token, expert) pairs. Expert weights are addressed via
  * per-expert pointer tables so callers can hold only the experts they need.
- * h_out: [n,I] or NULL; o_out: [n,H]. */
+ * act: gated activation (0 silu, 1 gelu); scales: [n] per-route factor of the
+ * activation, or NULL for 1. h_out: [n,I] or NULL; o_out: [n,H]. */
 int oracle_ffn_routes(int n, const int32_t* tokens, const int32_t* experts, int H, int I,
                       const uint16_t* x, const uint16_t* const* wg, const uint16_t* const* wu,
-                      const uint16_t* const* wd, float* h_out, float* o_out) {
+                      const uint16_t* const* wd, int act, const float* scales, float* h_out,
+                      float* o_out) {
   int bad = 0;
 #pragma omp parallel
   {
@@ -303,8 +330,9 @@ int oracle_ffn_routes(int n, const int32_t* tokens, const int32_t* experts, int 
 #pragma omp for schedule(dynamic, 1)
       for (int j = 0; j < n; ++j) {
         const int e = experts[j];
-        ffn_one(H, I, x + (size_t)tokens[j] * H, wg[e], wu[e], wd[e], g, u,
-                h_out ? h_out + (size_t)j * I : NULL, o_out + (size_t)j * H);
+        ffn_one(H, I, x + (size_t)tokens[j] * H, wg[e], wu[e], wd[e], act,
+                scales ? scales[j] : 1.0f, g, u, h_out ? h_out + (size_t)j * I : NULL,
+                o_out + (size_t)j * H);
       }
     }
     free(g); free(u);
@@ -315,7 +343,8 @@ int oracle_ffn_routes(int n, const int32_t* tokens, const int32_t* experts, int 
 /* ------------------------------------------------------------------------ */
 /* Step 6: gather-combine for tokens t in [t0, t1):                          */
 /*   y[t] = sum over k = 0..K-1 with keep[t,k] of p'[t,k] * o_route[t,k],    */
-/* fp32, in k order; a token with no kept route gives y = 0.                 */
+/* fp32, in k order; a token with no kept route gives y = 0. topk_p NULL:    */
+/* unit weights (the probability was applied in the activation).             */
 /* o_routes: [(t1-t0)*K, H] rows, the FFN output of route (t,k) (rows of     */
 /* dropped routes are ignored).                                              */
 /* ------------------------------------------------------------------------ */
@@ -328,7 +357,7 @@ int oracle_combine(int t0, int t1, int K, int H, const uint8_t* keep, const floa
     for (int k = 0; k < K; ++k) {
       const size_t r = (size_t)t * K + k;
       if (!keep[r]) continue;
-      const float w = topk_p[r];
+      const float w = topk_p ? topk_p[r] : 1.0f;
       const float* orow = o_routes + ((size_t)(t - t0) * K + k) * H;
       for (int j = 0; j < H; ++j) yr[j] = yr[j] + w * orow[j];
     }
@@ -343,27 +372,32 @@ int oracle_combine(int t0, int t1, int K, int H, const uint8_t* keep, const floa
 int oracle_forward_tokens(int t0, int t1, int K, int H, int I, const uint16_t* x,
                           const uint16_t* const* wg, const uint16_t* const* wu,
                           const uint16_t* const* wd, const int32_t* topk_ids,
-                          const float* topk_p, const uint8_t* keep, float* y) {
+                          const float* topk_p, const uint8_t* keep, int act, int prob_in_act,
+                          float* y) {
   const int nt = t1 - t0;
   if (nt <= 0) return 0;
   float* o = (float*)calloc((size_t)nt * K * H, sizeof(float));
   int32_t* tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)nt * K);
   int32_t* ex = (int32_t*)malloc(sizeof(int32_t) * (size_t)nt * K);
   int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)nt * K);
-  if (!o || !tok || !ex || !pos) { free(o); free(tok); free(ex); free(pos); return -2; }
+  float* sc = (float*)malloc(sizeof(float) * (size_t)nt * K);
+  if (!o || !tok || !ex || !pos || !sc) {
+    free(o); free(tok); free(ex); free(pos); free(sc);
+    return -2;
+  }
   int n = 0;
   for (int t = t0; t < t1; ++t)
     for (int k = 0; k < K; ++k) {
       const size_t r = (size_t)t * K + k;
       if (!keep[r]) continue;
-      tok[n] = t; ex[n] = topk_ids[r]; pos[n] = (t - t0) * K + k; ++n;
+      tok[n] = t; ex[n] = topk_ids[r]; pos[n] = (t - t0) * K + k; sc[n] = topk_p[r]; ++n;
     }
   float* on = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1) * H);
-  if (!on) { free(o); free(tok); free(ex); free(pos); return -2; }
-  int rc = oracle_ffn_routes(n, tok, ex, H, I, x, wg, wu, wd, NULL, on);
+  if (!on) { free(o); free(tok); free(ex); free(pos); free(sc); return -2; }
+  int rc = oracle_ffn_routes(n, tok, ex, H, I, x, wg, wu, wd, act, prob_in_act ? sc : NULL, NULL, on);
   for (int j = 0; j < n; ++j) memcpy(o + (size_t)pos[j] * H, on + (size_t)j * H, sizeof(float) * (size_t)H);
-  if (rc == 0) rc = oracle_combine(t0, t1, K, H, keep, topk_p, o, y);
-  free(on); free(o); free(tok); free(ex); free(pos);
+  if (rc == 0) rc = oracle_combine(t0, t1, K, H, keep, prob_in_act ? NULL : topk_p, o, y);
+  free(on); free(o); free(tok); free(ex); free(pos); free(sc);
   return rc;
 }
 
@@ -428,18 +462,19 @@ int oracle_dropless_layout(int N, int E, int K, int bm, const int32_t* ladder_nu
 /* ======================================================================== */
 /* Backward of the expert path for one route (token t, expert e, weight p'): */
 /* the vector-Jacobian product of y[t] += p' * o with o = a . Wd[e],        */
-/* a = silu(g)*u, g = x_t . Wg[e], u = x_t . Wu[e], given dY[t]:            */
+/* a = act(g)*u, g = x_t . Wg[e], u = x_t . Wu[e], given dY[t] (the same   */
+/* whether p' multiplies in the combine or in the activation):              */
 /*   dA0_i = sum_j dY_j * Wd[e,i,j]        (FC2 data gradient, route space) */
 /*   dprob = sum_i a_i * dA0_i             (gradient of the routing weight) */
 /*   dA = p' * dA0                                                          */
-/*   dg_i = dA_i * u_i * s_i * (1 + g_i*(1 - s_i)),  s = sigmoid(g)         */
-/*   du_i = dA_i * silu(g_i)                                                */
+/*   dg_i = dA_i * u_i * act'(g_i)         (act_grad above)                 */
+/*   du_i = dA_i * act(g_i)                                                 */
 /*   dXr_h = sum_i dg_i*Wg[e,h,i] + du_i*Wu[e,h,i]                          */
 /* SwiGLU is recomputed from g and u ("Permute-Free ...", section 6: "swiglu */
 /* is just an op", recomputed in the backward). fp32, fixed orders.          */
 /* Outputs (any may be NULL): dprob, dxr [H], dg [I], du [I], aw [I] = p'*a. */
 /* ======================================================================== */
-static void bwd_one(int H, int I, float p, const uint16_t* xrow, const uint16_t* dyrow,
+static void bwd_one(int H, int I, int act, float p, const uint16_t* xrow, const uint16_t* dyrow,
                     const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, float* g, float* u,
                     float* da0, float* dprob, float* dxr, float* dg_out, float* du_out,
                     float* aw_out) {
@@ -459,13 +494,12 @@ static void bwd_one(int H, int I, float p, const uint16_t* xrow, const uint16_t*
   }
   float dp = 0.0f;
   for (int i = 0; i < I; ++i) {
-    const float s = 1.0f / (1.0f + expf(-g[i]));
-    const float silu = g[i] * s;
-    const float a = silu * u[i];
+    const float ag = act_fn(act, g[i]);
+    const float a = ag * u[i];
     dp = dp + a * da0[i];
     const float dA = p * da0[i];
-    const float dgi = dA * u[i] * s * (1.0f + g[i] * (1.0f - s));
-    const float dui = dA * silu;
+    const float dgi = dA * u[i] * act_grad(act, g[i]);
+    const float dui = dA * ag;
     if (aw_out) aw_out[i] = p * a;
     da0[i] = dgi; /* reuse: da0 now holds dg */
     u[i] = dui;   /* reuse: u now holds du */
@@ -488,7 +522,7 @@ static void bwd_one(int H, int I, float p, const uint16_t* xrow, const uint16_t*
 /* Backward for a list of n routes (token, expert, p'). Per route outputs as in
  * bwd_one, stored row-wise; NULL skips an output. */
 int oracle_bwd_routes(int n, const int32_t* tokens, const int32_t* experts, const float* probs, int H,
-                      int I, const uint16_t* x, const uint16_t* dy, const uint16_t* const* wg,
+                      int I, int act, const uint16_t* x, const uint16_t* dy, const uint16_t* const* wg,
                       const uint16_t* const* wu, const uint16_t* const* wd, float* dprob,
                       float* dxr, float* dg, float* du, float* aw) {
   int bad = 0;
@@ -505,7 +539,7 @@ int oracle_bwd_routes(int n, const int32_t* tokens, const int32_t* experts, cons
       for (int r = 0; r < n; ++r) {
         const int e = experts[r];
         const int t = tokens[r];
-        bwd_one(H, I, probs[r], x + (size_t)t * H, dy + (size_t)t * H, wg[e], wu[e], wd[e], g, u, d,
+        bwd_one(H, I, act, probs[r], x + (size_t)t * H, dy + (size_t)t * H, wg[e], wu[e], wd[e], g, u, d,
                 dprob ? dprob + r : NULL, dxr ? dxr + (size_t)r * H : NULL,
                 dg ? dg + (size_t)r * I : NULL, du ? du + (size_t)r * I : NULL,
                 aw ? aw + (size_t)r * I : NULL);

@@ -5,6 +5,7 @@ central finite differences in fp64 of the forward written with numpy, for every
 backward output (dX, dW_gate, dW_up, dW_down, dprob), plus an fp64 closed form
 of the weight gradients on tiny inputs. No GPU."""
 import numpy as np
+from scipy.special import erf
 import pytest
 
 import oracle
@@ -86,8 +87,9 @@ def _problem(seed, N=12, H=16, E=3, K=2, I=8):
     return x, dy, wg, wu, wd, ids, p, L, W
 
 
-def _loss64(x, wg, wu, wd, ids, p, dy):
-    """L = sum_t <dY[t], y[t]>, y[t] = sum_k p[t,k] * SwiGLU_{e}(x[t]) in fp64."""
+def _loss64(x, wg, wu, wd, ids, p, dy, act=0):
+    """L = sum_t <dY[t], y[t]>, y[t] = sum_k p[t,k] * FFN_{e}(x[t]) in fp64
+    (act 0: SwiGLU, 1: GeGLU with the erf form of GELU)."""
     N, K = ids.shape
     y = np.zeros((N, x.shape[1]))
     for t in range(N):
@@ -95,17 +97,29 @@ def _loss64(x, wg, wu, wd, ids, p, dy):
             e = ids[t, k]
             g = x[t] @ wg[e]
             u = x[t] @ wu[e]
-            a = g / (1.0 + np.exp(-g)) * u
+            if act == 1:
+                a = 0.5 * g * (1.0 + erf(g / np.sqrt(2.0))) * u
+            else:
+                a = g / (1.0 + np.exp(-g)) * u
             y[t] += p[t, k] * (a @ wd[e])
     return float((dy * y).sum())
 
 
 @pytest.mark.parametrize("seed", range(2))
 def test_backward_matches_central_differences(seed):
+    _central_differences(seed, act=0)
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_backward_matches_central_differences_gelu(seed):
+    _central_differences(10 + seed, act=1)
+
+
+def _central_differences(seed, act):
     x, dy, wg, wu, wd, ids, p, L, W = _problem(seed)
     N, H = x.shape
     E, I = len(wg), wg[0].shape[1]
-    dX, dprob, dW = oracle.backward_all(x, dy, W, H, I, E, ids, p, L.token_routes)
+    dX, dprob, dW = oracle.backward_all(x, dy, W, H, I, E, ids, p, L.token_routes, act=act)
     X = _f(x)
     DY = _f(dy)
     G = {e: _f(wg[e]) for e in range(E)}
@@ -127,8 +141,8 @@ def test_backward_matches_central_differences(seed):
         Xp, Xm = X.copy(), X.copy()
         Xp[t, h] += eps
         Xm[t, h] -= eps
-        check(dX[t, h], num(lambda: _loss64(Xp, G, U, D, ids, P, DY),
-                            lambda: _loss64(Xm, G, U, D, ids, P, DY)), sc)
+        check(dX[t, h], num(lambda: _loss64(Xp, G, U, D, ids, P, DY, act),
+                            lambda: _loss64(Xm, G, U, D, ids, P, DY, act)), sc)
     for name, Wd_ in (("g", G), ("u", U), ("d", D)):
         for _ in range(4):
             e = int(rng.integers(E))
@@ -142,8 +156,8 @@ def test_backward_matches_central_differences(seed):
             args_m = dict(g=G, u=U, d=D)
             args_p[name] = Wp
             args_m[name] = Wm
-            want = num(lambda: _loss64(X, args_p["g"], args_p["u"], args_p["d"], ids, P, DY),
-                       lambda: _loss64(X, args_m["g"], args_m["u"], args_m["d"], ids, P, DY))
+            want = num(lambda: _loss64(X, args_p["g"], args_p["u"], args_p["d"], ids, P, DY, act),
+                       lambda: _loss64(X, args_m["g"], args_m["u"], args_m["d"], ids, P, DY, act))
             got = {"d": dW[e][0], "g": dW[e][1], "u": dW[e][2]}[name][i, j]
             check(got, want, max(np.abs(dW[e][0]).max(), np.abs(dW[e][1]).max()))
     for _ in range(6):
@@ -151,8 +165,8 @@ def test_backward_matches_central_differences(seed):
         Pp, Pm = P.copy(), P.copy()
         Pp[t, k] += eps
         Pm[t, k] -= eps
-        check(dprob[t, k], num(lambda: _loss64(X, G, U, D, ids, Pp, DY),
-                               lambda: _loss64(X, G, U, D, ids, Pm, DY)), np.abs(dprob).max())
+        check(dprob[t, k], num(lambda: _loss64(X, G, U, D, ids, Pp, DY, act),
+                               lambda: _loss64(X, G, U, D, ids, Pm, DY, act)), np.abs(dprob).max())
 
 
 def test_weight_gradients_match_fp64_closed_form():

@@ -26,13 +26,13 @@ MUTATIONS = [
     ("kept tokens laid out in probability order",
      "    qsort(buf, (size_t)kept, sizeof(route_key), cmp_token_asc); /* kept ones in ascending t */\n",
      "", lambda: fp.test_layout_hand_worked("layout_prob_k2.txt")),
-    ("silu without its gate factor", "const float s = g[i] / (1.0f + expf(-g[i]));",
-     "const float s = 1.0f / (1.0f + expf(-g[i]));",
+    ("silu without its gate factor", "return v / (1.0f + expf(-v));",
+     "return 1.0f / (1.0f + expf(-v));",
      lambda: fp.test_single_expert_top1_is_plain_swiglu_mlp()),
     ("renormalisation skipped", "topk_p[(size_t)t * K + k] = topk_p[(size_t)t * K + k] / d;",
      "topk_p[(size_t)t * K + k] = topk_p[(size_t)t * K + k];",
      lambda: fp.test_router_matches_fp64_library_routines(37, 64, 8, 2, False)),
-    ("SwiGLU backward loses the derivative term", "(1.0f + g[i] * (1.0f - s))", "(1.0f)",
+    ("SwiGLU backward loses the derivative term", "(1.0f + v * (1.0f - sg))", "(1.0f)",
      lambda: bp.test_backward_matches_central_differences(0)),
     ("dprob taken from the weighted gradient", "dp = dp + a * da0[i];", "dp = dp + a * p * da0[i];",
      lambda: bp.test_backward_matches_central_differences(1)),
@@ -40,6 +40,10 @@ MUTATIONS = [
      "if (aw_out) aw_out[i] = a;", lambda: bp.test_weight_gradients_match_fp64_closed_form()),
     ("dropless extent ignores the ladder", "    if (count <= rung) return rung;", "",
      lambda: bp.test_dropless_layout_hand_worked()),
+    ("GELU backward without the density term", "return cdf + v * pdf;", "return cdf;",
+     lambda: bp.test_backward_matches_central_differences_gelu(0)),
+    ("GELU with the erf argument unscaled", "erff(v * 0.70710678118654752f));\n  return v",
+     "erff(v));\n  return v", lambda: fp.test_gelu_closed_form_values()),
     ("router backward skips the renormalisation term", "gk[k] = (dp[k] - c) / d;",
      "gk[k] = dp[k] / d;", lambda: rb.test_router_backward_matches_central_differences(0, True)),
     ("router backward skips the softmax normaliser", "dl[ids[k]] = p[ids[k]] * (gk[k] - s);",
