@@ -8,7 +8,8 @@
  *                     -> per-expert counts -> drop-and-pad selection
  *                     -> expert-sorted, block-padded route list
  *   moe_ffn_forward : FC1 gather-GEMM (rows of x gathered by sorted_slot_ids
- *                     inside the tile load) with SwiGLU in its epilogue, then
+ *                     inside the tile load) with the gated activation
+ *                     (SwiGLU or GeGLU) in its epilogue, then
  *                     FC2 grouped GEMM over the same slots
  *   moe_combine     : each token sums its kept routes, weighted by the
  *                     renormalised routing probability
@@ -61,7 +62,7 @@ extern "C" {
  *  hidden    H   model width; multiple of 128
  *  n_experts E   1..256
  *  top_k     K   1..min(E,16) experts per token
- *  inter     I   SwiGLU intermediate width per expert; multiple of 128
+ *  inter     I   gated-activation width per expert; multiple of 128
  *  cap_num/cap_den  capacity factor F = cap_num/cap_den; the source
  *                capacity is cap = ceil(N*K*F/E) ([FC] Design notes).
  *                cap_num = 0 selects the dropless, bucketed layout: no route
@@ -74,7 +75,14 @@ extern "C" {
  *  ladder_len, ladder_den, ladder_num (dropless only; ladder_len 0..16)
  *                rung j = roundup(ceil(ladder_num[j]*N*K / (ladder_den*E)), bm):
  *                multiples ladder_num[j]/ladder_den of the expected rows per
- *                expert; ladder_num is a host array, ascending, positive */
+ *                expert; ladder_num is a host array, ascending, positive
+ *  activation    the experts' gated activation act(gate)*up ([PF] section 3;
+ *                section 8 tests silu and gelu): MOE_ACT_SWIGLU (silu) or
+ *                MOE_ACT_GEGLU (gelu, the exact form v*Phi(v))
+ *  prob_in_act   1 = the routing probability p' multiplies the activation in
+ *                FC1's epilogue (act(gate)*up*p', [PF] section 3) and the
+ *                combine sums the routes with unit weights; 0 = p' weights the
+ *                combine. The same function either way. */
 typedef struct moe_config {
   int32_t n_tokens;
   int32_t hidden;
@@ -88,7 +96,12 @@ typedef struct moe_config {
   int32_t ladder_len;
   int32_t ladder_den;
   const int32_t* ladder_num;
+  int32_t activation;
+  int32_t prob_in_act;
 } moe_config_t;
+
+#define MOE_ACT_SWIGLU 0
+#define MOE_ACT_GEGLU 1
 
 /* Routing metadata written by moe_route_align ([PF] section 4). All device
  * pointers, caller-allocated. With Cpad = roundup(cap, bm) and
@@ -109,6 +122,7 @@ typedef struct moe_config {
  *                             block_start[e]*bm)
  *  num_tokens_post_padded [1] i32  padded extent S, as a device scalar
  *  token_routes    [N,K] i32  inverse map: slot of route (t,k), -1 if dropped
+ *  slot_prob       [S]   f32  p' of the route each slot holds, 0 for padding
  *  gemm_sched      [4]   i32  work counters of the expert GEMMs' tile scheduler;
  *                             zeroed by moe_route_align and left zeroed by every
  *                             GEMM call (a routes object serves one stream at a
@@ -125,6 +139,7 @@ typedef struct moe_routes {
   int32_t* num_tokens_post_padded;
   int32_t* token_routes;
   int32_t* gemm_sched;
+  float* slot_prob;
 } moe_routes_t;
 
 /* Host-side size queries (no GPU work). Negative on an invalid config. */
@@ -152,11 +167,12 @@ int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_route
                     const float* bias, const moe_routes_t* out, void* workspace,
                     size_t ws_bytes, cudaStream_t stream);
 
-/* FC1 gather-GEMM + SwiGLU ([PF] section 2 and 3).
+/* FC1 gather-GEMM + gated activation ([PF] section 2 and 3).
  *  x    [N,H] bf16; row sorted_slot_ids[s] of x feeds slot s
  *  w13  [E,2I,H] bf16 packed expert weights (moe_pack_w13): rows [0,I) of
  *       expert e are W_gate[e]^T, rows [I,2I) are W_up[e]^T
- *  h    [S,I] bf16 output, h[s,:] = silu(x_s W_gate[e]) * (x_s W_up[e]) for
+ *  h    [S,I] bf16 output, h[s,:] = act(x_s W_gate[e]) * (x_s W_up[e]) (times the
+ *       slot's p' when cfg->prob_in_act) for
  *       s in expert e's slots; fp32 accumulation. Rows of slots at or past
  *       roundup(kept_counts[e],16) within an expert are not written; rows of
  *       padding slots below that bound are written as 0. */
@@ -188,8 +204,9 @@ int moe_ffn_forward_train(const moe_config_t* cfg, const moe_routes_t* routes, c
 /* Contention-free gather-combine ([PF] section 2 and 5 "route_gather_combine").
  *  o  [S,H] bf16 expert outputs;  y [N,H] bf16 output:
  *  y[t,:] = sum over k with token_routes[t,k] >= 0 of topk_p[t,k]*o[token_routes[t,k],:]
- *  in fp32, in k order. Dropped routes contribute nothing; a token with every
- *  route dropped gets y = 0. Each output row is written by one CTA; no atomics. */
+ *  in fp32, in k order (unit weights instead of topk_p when cfg->prob_in_act).
+ *  Dropped routes contribute nothing; a token with every route dropped gets
+ *  y = 0. Each output row is written by one CTA; no atomics. */
 int moe_combine(const moe_config_t* cfg, const moe_routes_t* routes, const void* o, void* y,
                 cudaStream_t stream);
 
@@ -219,7 +236,7 @@ int64_t moe_backward_workspace_bytes(const moe_config_t* cfg);
  *         dW_gate[e]^T, rows [I,2I): dW_up[e]^T); zero for an expert with no
  *         kept route
  *  dw2    [E,H,I] f32 output, the gradient of the packed w2 (dW_down[e]^T)
- *  dprob  [N,K] f32 output: dL/dp'[t,k] = <silu(g) u, dY[t] W_down[e]^T> for a
+ *  dprob  [N,K] f32 output: dL/dp'[t,k] = <act(g) u, dY[t] W_down[e]^T> for a
  *         kept route, 0 for a dropped one
  *  workspace/ws_bytes  device scratch of at least moe_backward_workspace_bytes
  * fp32 accumulation everywhere; dPre = [dg | du], p' a and the per-route input

@@ -24,7 +24,7 @@ import os
 from typing import Optional
 
 __all__ = [
-    "Config", "Routes", "MoEError", "lib", "library_path", "alloc_routes", "alloc_workspace",
+    "Config", "Routes", "ACT_SWIGLU", "ACT_GEGLU", "MoEError", "lib", "library_path", "alloc_routes", "alloc_workspace",
     "alloc_buffers", "capacity", "max_slots", "max_blocks", "route_workspace_bytes",
     "route_align", "fc1_forward", "fc2_forward", "ffn_forward", "combine", "pack_w13",
     "pack_w2", "status_string", "launch_count", "device_error", "forward",
@@ -45,27 +45,37 @@ class MoEError(RuntimeError):
         self.status = status
 
 
+ACT_SWIGLU, ACT_GEGLU = 0, 1
+
+
 class Config(ctypes.Structure):
     """Mirror of moe_config_t."""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_tokens", "hidden", "n_experts", "top_k", "inter", "cap_num", "cap_den", "block_m",
-        "renorm", "ladder_len", "ladder_den")] + [("ladder_num", ctypes.POINTER(ctypes.c_int32))]
+        "renorm", "ladder_len", "ladder_den")] + [("ladder_num", ctypes.POINTER(ctypes.c_int32)),
+                                                  ("activation", ctypes.c_int32),
+                                                  ("prob_in_act", ctypes.c_int32)]
 
     def __init__(self, n_tokens, hidden, n_experts, top_k, inter, cap_num=1, cap_den=1,
-                 block_m=32, renorm=1, ladder=None, ladder_den=1):
+                 block_m=32, renorm=1, ladder=None, ladder_den=1, activation=ACT_SWIGLU,
+                 prob_in_act=0):
         """cap_num=0 selects the dropless layout; ladder: rung multipliers
-        (numerators over ladder_den) of the expected rows per expert."""
+        (numerators over ladder_den) of the expected rows per expert;
+        activation: ACT_SWIGLU or ACT_GEGLU; prob_in_act: p' multiplies the
+        activation (unit-weight combine) instead of weighting the combine."""
         lad = list(ladder or [])
         self._ladder = (ctypes.c_int32 * max(len(lad), 1))(*lad)
         super().__init__(n_tokens, hidden, n_experts, top_k, inter, cap_num, cap_den, block_m,
                          renorm, len(lad), ladder_den,
-                         ctypes.cast(self._ladder, ctypes.POINTER(ctypes.c_int32)))
+                         ctypes.cast(self._ladder, ctypes.POINTER(ctypes.c_int32)), activation,
+                         int(bool(prob_in_act)))
 
 
 class _RoutesC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "topk_ids", "topk_p", "keep", "expert_counts", "kept_counts", "sorted_slot_ids",
-        "expert_ids", "block_start", "num_tokens_post_padded", "token_routes", "gemm_sched")]
+        "expert_ids", "block_start", "num_tokens_post_padded", "token_routes", "gemm_sched",
+        "slot_prob")]
 
 
 class Routes:
@@ -180,7 +190,8 @@ def alloc_routes(cfg: Config, device) -> Routes:
         expert_counts=torch.empty(E, **i32), kept_counts=torch.empty(E, **i32),
         sorted_slot_ids=torch.empty(max(S, 1), **i32), expert_ids=torch.empty(max(B, 1), **i32),
         block_start=torch.empty(E, **i32), num_tokens_post_padded=torch.empty(1, **i32),
-        token_routes=torch.empty((N, K), **i32), gemm_sched=torch.zeros(4, **i32))
+        token_routes=torch.empty((N, K), **i32), gemm_sched=torch.zeros(4, **i32),
+        slot_prob=torch.empty(max(S, 1), dtype=torch.float32, device=device))
 
 
 def alloc_workspace(cfg: Config, device):

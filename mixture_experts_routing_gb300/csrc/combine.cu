@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
 #pragma unroll
   for (int k = 0; k < KMAX; ++k) {
     slot[k] = (k < K) ? token_routes[(size_t)t * K + k] : -1;
-    w[k] = (k < K) ? topk_p[(size_t)t * K + k] : 0.0f;
+    w[k] = (k < K) ? (topk_p ? topk_p[(size_t)t * K + k] : 1.0f) : 0.0f;  // null: unit weights
   }
   const int nv = H / 8;
   for (int v = threadIdx.x; v < nv; v += kCombineThreads) {
@@ -114,25 +114,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bwd_kernel(
   }
 }
 
-// slot_prob[s]: the renormalised probability p' of the route (t,k) that slot
-// s holds (token_routes[t,k] == s), 0 for a padding slot. Block 0 also zeroes
-// the backward GEMMs' counters.
-__global__ void slot_prob_kernel(const int32_t* __restrict__ sorted_slot_ids,
-                                 const int32_t* __restrict__ token_routes,
-                                 const float* __restrict__ topk_p, int N, int K, int64_t s_max,
-                                 float* __restrict__ slot_prob, int32_t* __restrict__ sched_zero,
-                                 int n_zero) {
-  if (blockIdx.x == 0 && (int)threadIdx.x < n_zero) sched_zero[threadIdx.x] = 0;
-  const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (s >= s_max) return;
-  const int t = sorted_slot_ids[s];
-  float pr = 0.0f;
-  if (t >= 0 && t < N)
-    for (int k = 0; k < K; ++k)
-      if (token_routes[(size_t)t * K + k] == (int32_t)s) pr = topk_p[(size_t)t * K + k];
-  slot_prob[s] = pr;
-}
-
 __global__ void transpose_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int R,
                                  int C, int64_t in_es, int64_t out_es, int64_t out_off) {
   __shared__ uint16_t tile[32][33];
@@ -183,18 +164,6 @@ int launch_combine_bwd(const uint16_t* dxr, const float* part, int n_part,
   else
     MOE_COMBINE_BWD(16);
 #undef MOE_COMBINE_BWD
-  const cudaError_t err = cudaGetLastError();
-  return err == cudaSuccess ? 1 : -(int)err;
-}
-
-int launch_slot_route(const int32_t* sorted_slot_ids, const int32_t* token_routes,
-                      const float* topk_p, int N, int K, int64_t s_max, float* slot_prob,
-                      int32_t* sched_zero, int n_zero, cudaStream_t s) {
-  if (s_max <= 0) return 0;
-  const int threads = 256;
-  const int64_t blocks = (s_max + threads - 1) / threads;
-  slot_prob_kernel<<<(unsigned)blocks, threads, 0, s>>>(sorted_slot_ids, token_routes, topk_p, N, K,
-                                                        s_max, slot_prob, sched_zero, n_zero);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }

@@ -98,7 +98,10 @@ struct GemmParams {
   uint16_t* out;
   uint16_t* out2;        // FC1: pre-activations [S,2I] or null; FC2 dgrad: p'*a [S,I]
   const uint16_t* aux;   // FC2 dgrad: pre-activations [S,2I]
-  const float* slot_prob;     // FC2 dgrad: p' of each slot's route, 0 for padding
+  const float* slot_prob;     // p' of each slot's route, 0 for padding (FC1 with
+                              // prob_in_act, FC2 dgrad)
+  int activation;             // 0 SwiGLU, 1 GeGLU
+  int prob_in_act;            // FC1: h = act(g) u p'
   float* part;                // FC2 dgrad: dprob partials [S, I/32]
   int inter;                  // I
   uint32_t* err;
@@ -192,6 +195,26 @@ __device__ __forceinline__ void store_rows16(uint32_t stg_u, int lane, const flo
   __syncwarp();
 }
 
+// Gated activation act(gate) of the FFN and its derivative ("Permute-Free
+// Grouped GEMM for MoE (bf16, gfx950)", section 3 act(gate)*up; section 8:
+// silu and gelu): 0 = silu(v) = v sigma(v); 1 = gelu(v) = v Phi(v) (the erf
+// form); act_grad: sigma(v)(1 + v(1 - sigma(v))), Phi(v) + v phi(v).
+template <int act>
+__device__ __forceinline__ float act_fwd(float v) {
+  if (act == 1) return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+  return __fdividef(v, 1.0f + __expf(-v));
+}
+
+template <int act>
+__device__ __forceinline__ float act_grad(float v) {
+  if (act == 1) {
+    const float cdf = 0.5f * (1.0f + erff(v * 0.70710678118654752f));
+    return cdf + v * (__expf(-0.5f * v * v) * 0.39894228040143268f);
+  }
+  const float sg = __fdividef(1.0f, 1.0f + __expf(-v));
+  return sg * (1.0f + v * (1.0f - sg));
+}
+
 // Pre-activations of 16 slots (c0..c0+15 of the tile) for this lane's feature:
 // gate in the low half, up in the high half of each word; 0 past the kept rows.
 __device__ __forceinline__ void load_preact16(const GemmParams& p, const Tile& T, int c0, int f,
@@ -215,11 +238,12 @@ __device__ __forceinline__ float load_slot_prob(const GemmParams& p, const Tile&
 // Epilogue of the FC2 dgrad for 16 slots (registers) x 32 features (lanes).
 // dA0[s,i] = dY[t_s] . W_down[e][i,:] arrives in v; with g, u the saved
 // pre-activations (gu) and p' the slot's routing probability (ps):
-//   a = silu(g) u,  dprob part = sum_i a dA0,  dA = p' dA0,
-//   dg = dA u sigma(g) (1 + g (1 - sigma(g))),  du = dA silu(g),  aw = p' a.
+//   a = act(g) u,  dprob part = sum_i a dA0,  dA = p' dA0,
+//   dg = dA u act'(g),  du = dA act(g),  aw = p' a.
 // dg and du go to dPre (gate columns, then up columns), aw to out2, and the
 // 32-feature partial sum of a dA0 of each slot to part[s, feat0/32]. Padding
 // slots get zeros (their dA0, g, u and p' are 0).
+template <int act>
 __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const Tile& T, int c0,
                                                       int feat0, int lane, uint32_t stg_u,
                                                       const uint32_t (&v)[16],
@@ -232,26 +256,23 @@ __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
     const float da0 = __uint_as_float(v[j]);
-    dp[j] = g * sg * u * da0;
-    o[j] = ps[c0 + j] * da0 * u * sg * (1.0f + g * (1.0f - sg));
+    dp[j] = act_fwd<act>(g) * u * da0;
+    o[j] = ps[c0 + j] * da0 * u * act_grad<act>(g);
   }
   store_rows16(stg_u, lane, o, p.out + row0 * ld2 + feat0, ld2);
   // du
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float g = __uint_as_float(gu[j] << 16);
-    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
-    o[j] = ps[c0 + j] * __uint_as_float(v[j]) * g * sg;
+    o[j] = ps[c0 + j] * __uint_as_float(v[j]) * act_fwd<act>(g);
   }
   store_rows16(stg_u, lane, o, p.out + row0 * ld2 + I + feat0, ld2);
   // aw
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
-    o[j] = ps[c0 + j] * (g * sg * u);
+    o[j] = ps[c0 + j] * (act_fwd<act>(g) * u);
   }
   store_rows16(stg_u, lane, o, p.out2 + row0 * I + feat0, I);
   // sum dp over the 32 lanes for each of the 16 slots, halving the values
@@ -285,8 +306,9 @@ __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const
     p.part[(row0 + m) * (size_t)(I / 32) + feat0 / 32] = dp[0];
 }
 
-// One instantiation per GemmMode, so each carries only its own code path.
-template <int kMode>
+// One instantiation per GemmMode (and per activation for the modes that apply
+// one), so each carries only its own code path.
+template <int kMode, int kAct>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
@@ -527,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           if (lane < 16) ps_w[lane] = p_cur;
           __syncwarp();
-          swiglu_backward_chunk(p, T, c0, feat0 + a * kTileM, lane, stg_u, v, gu, ps_w - c0);
+          swiglu_backward_chunk<kAct>(p, T, c0, feat0 + a * kTileM, lane, stg_u, v, gu, ps_w - c0);
         }
       } else {
         for (int c0 = half * 16; c0 < T.n_eff; c0 += 32) {
@@ -537,11 +559,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           const size_t row0 = (size_t)(T.slot0 + c0);  // slot of register 0
           if constexpr (kMode == kModeFc1) {
+            // p' of the chunk's slots (lane j < 16 holds slot j's) when the
+            // routing probability multiplies the activation
+            const float pl = p.prob_in_act ? load_slot_prob(p, T, c0, lane) : 1.0f;
             float hv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float g = __uint_as_float(v0[i]);
-              hv[i] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[i]);
+              hv[i] = act_fwd<kAct>(g) * __uint_as_float(v1[i]);
+              if (p.prob_in_act) hv[i] *= __shfl_sync(0xFFFFFFFFu, pl, i);
             }
             store_rows16(stg_u, lane, hv, p.out + row0 * p.out_ld + feat0, p.out_ld);
             if (p.out2) {  // pre-activations for the backward: gate, then up
@@ -632,10 +658,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int kMode>
+template <int kMode, int kAct>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(moe_gemm_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kSmemBudget);
+  return cudaFuncSetAttribute(moe_gemm_kernel<kMode, kAct>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
 }
 
 // SM count of the current device, with every instantiation's shared-memory
@@ -648,10 +674,12 @@ int device_sms(cudaError_t* err) {
   int n = 0;
   if ((*err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return 0;
-  if ((*err = set_smem_attr<kModeFc1>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeFc2>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeDgrad2>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeDgrad1>()) != cudaSuccess) {
+  if ((*err = set_smem_attr<kModeFc1, 0>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeFc1, 1>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeFc2, 0>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeDgrad2, 0>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeDgrad2, 1>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeDgrad1, 0>()) != cudaSuccess) {
     cudaGetLastError();  // reported here; do not leave it for a later launch to report
     return 0;
   }
@@ -673,6 +701,8 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   p.out2 = static_cast<uint16_t*>(a.out2);
   p.aux = static_cast<const uint16_t*>(a.aux);
   p.slot_prob = a.slot_prob;
+  p.activation = a.activation;
+  p.prob_in_act = a.prob_in_act;
   p.part = a.part;
   p.inter = a.I;
   p.err = a.err;
@@ -764,11 +794,22 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
   const int grid = (int)(grid_bound < sms ? grid_bound : sms);
   p.sched = a.sched;
+  const bool gelu = a.activation == 1;
   switch (a.mode) {
-    case kModeFc1: moe_gemm_kernel<kModeFc1><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
-    case kModeFc2: moe_gemm_kernel<kModeFc2><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
-    case kModeDgrad2: moe_gemm_kernel<kModeDgrad2><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
-    default: moe_gemm_kernel<kModeDgrad1><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
+    case kModeFc1:
+      if (gelu)
+        moe_gemm_kernel<kModeFc1, 1><<<grid, kThreads, dyn, s>>>(tmA, tmB, p);
+      else
+        moe_gemm_kernel<kModeFc1, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, p);
+      break;
+    case kModeFc2: moe_gemm_kernel<kModeFc2, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
+    case kModeDgrad2:
+      if (gelu)
+        moe_gemm_kernel<kModeDgrad2, 1><<<grid, kThreads, dyn, s>>>(tmA, tmB, p);
+      else
+        moe_gemm_kernel<kModeDgrad2, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, p);
+      break;
+    default: moe_gemm_kernel<kModeDgrad1, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, p); break;
   }
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;

@@ -42,6 +42,9 @@ int check_cfg(const moe_config_t* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->block_m != 16 && c->block_m != 32 && c->block_m != 64 && c->block_m != 128)
     return MOE_ERR_INVALID_ARG;
+  if ((c->activation != MOE_ACT_SWIGLU && c->activation != MOE_ACT_GEGLU) ||
+      (c->prob_in_act != 0 && c->prob_in_act != 1))
+    return MOE_ERR_INVALID_ARG;
   if (c->cap_num == 0) {  // dropless: the ladder must be well formed
     if (c->ladder_len < 0 || c->ladder_len > moe::kMaxLadder) return MOE_ERR_INVALID_ARG;
     if (c->ladder_len > 0) {
@@ -120,10 +123,10 @@ WsLayout ws_layout(const moe_config_t* c) {
   return w;
 }
 
-// Backward scratch: p' of each slot, the backward GEMMs' tile counters, the
+// Backward scratch: the backward GEMMs' tile counters, the
 // dprob partials, dPre = [dg | du], aw = p' a and the per-slot input gradient.
 struct BwdLayout {
-  size_t slot_prob, sched, part, dpre, aw, dxr, total;
+  size_t sched, part, dpre, aw, dxr, total;
 };
 
 BwdLayout bwd_layout(const moe_config_t* c) {
@@ -136,7 +139,6 @@ BwdLayout bwd_layout(const moe_config_t* c) {
     off += (bytes + 255) / 256 * 256;
     return at;
   };
-  w.slot_prob = take((size_t)S * 4);
   w.sched = take(8 * 4);
   w.part = take((size_t)(S * (I / 32)) * 4);
   w.dpre = take((size_t)(S * 2 * I) * 2);
@@ -149,7 +151,7 @@ BwdLayout bwd_layout(const moe_config_t* c) {
 bool routes_complete(const moe_routes_t* r) {
   return r && r->topk_ids && r->topk_p && r->keep && r->expert_counts && r->kept_counts &&
          r->sorted_slot_ids && r->expert_ids && r->block_start && r->num_tokens_post_padded &&
-         r->token_routes && r->gemm_sched;
+         r->token_routes && r->gemm_sched && r->slot_prob;
 }
 
 int finish(int launched) {
@@ -221,6 +223,7 @@ int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_route
   a.ntpp = out->num_tokens_post_padded;
   a.token_routes = out->token_routes;
   a.gemm_sched = out->gemm_sched;
+  a.slot_prob = out->slot_prob;
   a.ws.logits = reinterpret_cast<float*>(ws + w.logits);
   a.ws.chunk_counts = reinterpret_cast<int32_t*>(ws + w.chunk_counts);
   a.ws.chunk_lofs = reinterpret_cast<int32_t*>(ws + w.chunk_lofs);
@@ -249,7 +252,7 @@ static void gemm_base(const moe_config_t* cfg, const moe_routes_t* routes, uint3
 
 static bool gemm_routes_ok(const moe_routes_t* routes) {
   return routes && routes->sorted_slot_ids && routes->kept_counts && routes->block_start &&
-         routes->gemm_sched;
+         routes->gemm_sched && routes->slot_prob;
 }
 
 static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* act,
@@ -270,6 +273,9 @@ static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, const
   a.w = w;
   a.out = out;
   a.out2 = fc1 ? preact : nullptr;
+  a.activation = cfg->activation;
+  a.prob_in_act = fc1 ? cfg->prob_in_act : 0;
+  a.slot_prob = routes->slot_prob;
   a.act_rows = fc1 ? cfg->n_tokens : a.s_max;
   a.sched = routes->gemm_sched + (fc1 ? 0 : 2);
   return finish(moe::launch_gemm(a, stream));
@@ -314,7 +320,7 @@ int moe_combine(const moe_config_t* cfg, const moe_routes_t* routes, const void*
   a.K = cfg->top_k;
   a.o = static_cast<const uint16_t*>(o);
   a.token_routes = routes->token_routes;
-  a.topk_p = routes->topk_p;
+  a.topk_p = cfg->prob_in_act ? nullptr : routes->topk_p;  // unit weights: p' is in h
   a.y = static_cast<uint16_t*>(y);
   return finish(moe::launch_combine(a, stream));
 }
@@ -368,7 +374,6 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
   uint32_t* err = error_word_ptr();
   if (!err) return MOE_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* slot_prob = reinterpret_cast<float*>(ws + L.slot_prob);
   int32_t* sched = reinterpret_cast<int32_t*>(ws + L.sched);
   float* part = reinterpret_cast<float*>(ws + L.part);
   void* dpre = ws + L.dpre;
@@ -383,10 +388,8 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
     launched += l;
     return true;
   };
-  // 1. p' of each slot; zeroes the counters
-  if (!add(moe::launch_slot_route(routes->sorted_slot_ids, routes->token_routes, routes->topk_p,
-                                  N, K, N > 0 ? S : 0, slot_prob, sched, 8, stream)))
-    return finish(-1);
+  // 1. the backward GEMMs' tile counters start at zero
+  if (cudaMemsetAsync(sched, 0, 8 * sizeof(int32_t), stream) != cudaSuccess) return finish(-1);
   if (N > 0) {
     // 2. FC2 dgrad with the SwiGLU backward: dPre, aw = p' a, dprob partials
     moe::GemmArgs g{};
@@ -397,7 +400,8 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
     g.out = dpre;
     g.out2 = aw;
     g.aux = preact;
-    g.slot_prob = slot_prob;
+    g.slot_prob = routes->slot_prob;
+    g.activation = cfg->activation;
     g.part = part;
     g.act_rows = N;
     g.sched = sched + 0;

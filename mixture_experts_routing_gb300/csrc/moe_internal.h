@@ -46,6 +46,7 @@ struct RouteArgs {
   int32_t* ntpp;
   int32_t* token_routes;
   int32_t* gemm_sched;
+  float* slot_prob;      // [S] p' of each slot's route, 0 for padding
   RouteWs ws;
 };
 
@@ -71,7 +72,9 @@ struct GemmArgs {
   void* out;             // FC1: h [S,I]; FC2: o [S,H]; dgrad2: dPre [S,2I]; dgrad1: dXr [S,H]
   void* out2;            // FC1: pre-activations [S,2I] or null; dgrad2: p'*a [S,I]
   const void* aux;       // dgrad2: pre-activations [S,2I]
-  const float* slot_prob;     // dgrad2: p' of each slot's route (0 padding)
+  const float* slot_prob;     // FC1 (prob_in_act), dgrad2: p' of each slot's route (0 padding)
+  int activation;             // FC1, dgrad2: 0 SwiGLU, 1 GeGLU
+  int prob_in_act;            // FC1: multiply the activation by the slot's p'
   float* part;                // dgrad2: dprob partials [S, I/32]
   int64_t act_rows;      // rows of act (N when gathered, else S)
   const int32_t* sorted_slot_ids;
@@ -120,11 +123,6 @@ int router_bwd_splits(int N, int H, int E);
 int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s);
 
 // Backward helpers (combine.cu).
-// slot_prob[s] = topk_p of the route t*K+k held by slot s, 0 for padding;
-// also zeroes sched_zero[0..n_zero).
-int launch_slot_route(const int32_t* sorted_slot_ids, const int32_t* token_routes,
-                      const float* topk_p, int N, int K, int64_t s_max, float* slot_prob,
-                      int32_t* sched_zero, int n_zero, cudaStream_t s);
 // dX[t] = sum_k dXr[token_routes[t,k]] (fp32, k order) and
 // dprob[t,k] = sum_j part[token_routes[t,k], j] (j order; 0 for a dropped route).
 int launch_combine_bwd(const uint16_t* dxr, const float* part, int n_part,

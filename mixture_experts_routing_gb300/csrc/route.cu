@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     int32_t* __restrict__ kept_counts, int32_t* __restrict__ sorted_slot_ids,
     int32_t* __restrict__ expert_ids, int32_t* __restrict__ block_start,
     int32_t* __restrict__ ntpp, int32_t* __restrict__ token_routes,
-    int32_t* __restrict__ gemm_sched) {
+    int32_t* __restrict__ gemm_sched, float* __restrict__ slot_prob) {
   extern __shared__ uint32_t dyn[];
   __shared__ int32_t hist[256];
   __shared__ int32_t warp_tot[32];
@@ -509,6 +509,7 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
       const int slot = base + pos;
       ++pos;
       sorted_slot_ids[slot] = r / K;
+      slot_prob[slot] = __uint_as_float(keys[i]);  // the key is p' (its bits)
       token_routes[r] = slot;
       keep[r] = 1;
     } else {
@@ -517,13 +518,19 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     }
   }
   const int kept_e = select ? cap : n;
-  for (int sl = kept_e + tid; sl < extent; sl += kSelThreads) sorted_slot_ids[base + sl] = N;
+  for (int sl = kept_e + tid; sl < extent; sl += kSelThreads) {
+    sorted_slot_ids[base + sl] = N;
+    slot_prob[base + sl] = 0.0f;
+  }
   const int nb = extent / bm;
   for (int b = tid; b < nb; b += kSelThreads)
     expert_ids[(size_t)base / bm + b] = (b * bm < kept_e) ? e : -1;
   if (dropless && e == E - 1) {
     // slots past the padded total up to the allocated bound: sentinel / -1
-    for (int sl = s_all + tid; sl < s_max; sl += kSelThreads) sorted_slot_ids[sl] = N;
+    for (int sl = s_all + tid; sl < s_max; sl += kSelThreads) {
+      sorted_slot_ids[sl] = N;
+      slot_prob[sl] = 0.0f;
+    }
     for (int b = s_all / bm + tid; b < s_max / bm; b += kSelThreads) expert_ids[b] = -1;
   }
   if (tid == 0) {
@@ -839,7 +846,7 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
       a.ws.chunk_counts, a.ws.chunk_lofs, a.ws.chunk_routes, a.ws.chunk_keys, a.N, a.E, a.K, cap,
       (int)a.cpad, a.bm, a.dropless, a.ladder, (int)a.s_max, a.keep, a.expert_counts,
       a.kept_counts, a.sorted_slot_ids, a.expert_ids,
-      a.block_start, a.ntpp, a.token_routes, a.gemm_sched);
+      a.block_start, a.ntpp, a.token_routes, a.gemm_sched, a.slot_prob);
   ++launched;
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;

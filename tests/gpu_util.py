@@ -55,11 +55,13 @@ class Problem:
 
     def __init__(self, w: synth.Workload, bm: int = 32, dev="cuda:0", host_weights: bool = True,
                  bias: Optional[np.ndarray] = None, renorm: int = 1, x_bits: Optional[np.ndarray] = None,
-                 with_ffn: bool = True):
+                 with_ffn: bool = True, activation: int = 0, prob_in_act: int = 0):
         self.w, self.bm, self.dev = w, bm, torch.device(dev)
         N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
+        self.activation, self.prob_in_act = activation, prob_in_act
         self.cfg = moe.Config(N, H, E, K, I, w.cap_num, w.cap_den, block_m=bm, renorm=renorm,
-                              ladder=list(w.ladder), ladder_den=w.ladder_den)
+                              ladder=list(w.ladder), ladder_den=w.ladder_den,
+                              activation=activation, prob_in_act=prob_in_act)
         self.x_bits = (x_bits if x_bits is not None
                        else synth.normal_bf16_bits(w.seed, synth.STREAM["x"], 0, N * H, w.x_std).reshape(N, H))
         self.wr = synth.normal_f32(w.seed, synth.STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E)
@@ -160,6 +162,7 @@ def assert_routing_equal(P: Problem, R: oracle.Routing) -> None:
     assert np.array_equal(g["block_start"], L.block_start), "block_start"
     assert int(g["num_tokens_post_padded"][0]) == L.num_tokens_post_padded, "num_tokens_post_padded"
     assert np.array_equal(g["token_routes"], L.token_routes), "token_routes"
+    check_slot_prob(P, R)
 
 
 def check_expert_slots(P: Problem, R: oracle.Routing, experts) -> None:
@@ -248,3 +251,15 @@ class Backward:
         I = self.P.w.inter
         d13 = self.dw13[e].cpu().numpy()
         return self.dw2[e].cpu().numpy().T, d13[:I].T, d13[I:].T
+
+
+def check_slot_prob(P: Problem, R: oracle.Routing) -> None:
+    """slot_prob holds, bit for bit, p' of the route each slot holds, and 0 on
+    every padding slot of the allocated bound."""
+    g = P.routes_np()
+    sp = g["slot_prob"][:len(R.layout.sorted_slot_ids)]  # the route list's S slots
+    want = np.zeros(len(sp), np.float32)
+    tr = R.layout.token_routes.ravel()
+    r = np.nonzero(tr >= 0)[0]
+    want[tr[r]] = R.topk_p.ravel()[r]
+    assert np.array_equal(sp.view(np.int32), want.view(np.int32)), "slot_prob"
