@@ -82,7 +82,17 @@ extern "C" {
  *  prob_in_act   1 = the routing probability p' multiplies the activation in
  *                FC1's epilogue (act(gate)*up*p', [PF] section 3) and the
  *                combine sums the routes with unit weights; 0 = p' weights the
- *                combine. The same function either way. */
+ *                combine. The same function either way.
+ *  n_valid       NULL, or a DEVICE pointer to an int32 holding the live token
+ *                count n <= n_tokens, read by the kernels when they run: the
+ *                batch is x[0..n), n_tokens is only the static bound that sizes
+ *                the buffers and grids. Capacity, the ladder and every routing
+ *                result follow n ([PF] section 2: real extents carried as device
+ *                scalars); rows n <= t < n_tokens get topk_ids -1, topk_p 0,
+ *                keep 0, token_routes -1 and y = 0; the sentinel in sorted_slot_ids
+ *                stays n_tokens. This lets one captured CUDA graph serve every
+ *                batch up to its bound (moe_ladder_*). Forward calls only: the
+ *                backward calls reject it (MOE_ERR_UNSUPPORTED_SHAPE). */
 typedef struct moe_config {
   int32_t n_tokens;
   int32_t hidden;
@@ -98,6 +108,7 @@ typedef struct moe_config {
   const int32_t* ladder_num;
   int32_t activation;
   int32_t prob_in_act;
+  const int32_t* n_valid;
 } moe_config_t;
 
 #define MOE_ACT_SWIGLU 0
@@ -273,6 +284,58 @@ int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, con
                         const float* w_router, const float* bias, const float* dprob, void* dx,
                         float* dw_router, float* dbias, void* workspace, size_t ws_bytes,
                         cudaStream_t stream);
+
+/* ---------------------------------------------------------------- graph ladder
+ * Captured CUDA graphs of the forward at a ladder of token-count buckets, for
+ * batches whose size changes from call to call ("[4/5] feat: capture the FFN
+ * experts at bucketed padded shapes", What this adds: an item takes the
+ * smallest bucket that holds it, or runs eager when the bucket would pad it
+ * past a ratio; capture runs largest-bucket-first behind one eager call at the
+ * ceiling). A bucket's graph is moe_route_align + moe_ffn_forward +
+ * moe_combine captured at n_tokens = the bucket with n_valid set, so its
+ * replay on n <= bucket tokens computes what those calls compute on exactly n
+ * tokens (y bit-identical; the sentinel in sorted_slot_ids is the bucket). */
+
+/* Buffers of one layer instance, every one sized for the top bucket. */
+typedef struct moe_layer_buffers {
+  const void* x;           /* [Ntop,H] bf16; a forward of n tokens reads x[0..n) */
+  const float* w_router;   /* [H,E] f32 */
+  const float* bias;       /* [E] f32 or NULL */
+  const void* w13;         /* packed, as moe_ffn_forward */
+  const void* w2;
+  moe_routes_t routes;     /* allocated for the top bucket */
+  void* route_workspace;   /* moe_route_workspace_bytes(top) bytes */
+  size_t route_workspace_bytes;
+  void* h;                 /* [S_top,I] bf16 */
+  void* o;                 /* [S_top,H] bf16 */
+  void* y;                 /* [Ntop,H] bf16; a forward of n tokens writes y[0..n) */
+  int32_t* n_valid;        /* one device int32 the ladder writes the live count to */
+} moe_layer_buffers_t;
+
+typedef struct moe_ladder moe_ladder_t; /* opaque */
+
+/* Host-side bucket choice: the index of the smallest bucket >= n, or -1 when
+ * n exceeds every bucket or the bucket is more than max_pad_ratio * n
+ * (max_pad_ratio <= 0: no limit). buckets ascending. */
+int moe_ladder_pick(const int32_t* buckets, int n_buckets, int32_t n, float max_pad_ratio);
+
+/* Captures one graph per bucket (largest first, after one eager forward at
+ * the ceiling on a private stream; synchronises that stream). top: the layer
+ * config with n_tokens = buckets[n_buckets-1] and n_valid NULL. The buffers'
+ * device memory must stay allocated, and the weights' contents in place, for
+ * the ladder's lifetime (the graphs hold their addresses). *out is NULL on
+ * failure. */
+int moe_ladder_create(const moe_config_t* top, const int32_t* buckets, int n_buckets,
+                      float max_pad_ratio, const moe_layer_buffers_t* bufs, moe_ladder_t** out);
+
+/* One forward of n <= Ntop tokens on `stream`: writes n to n_valid and
+ * replays the chosen bucket's graph, or runs the three calls eagerly with
+ * n_tokens = n. *bucket (optional) receives the bucket index, -1 for eager.
+ * One ladder serves one stream at a time. */
+int moe_ladder_forward(moe_ladder_t* ladder, int32_t n, cudaStream_t stream, int* bucket);
+
+/* Frees the graphs (not the caller's buffers). */
+int moe_ladder_destroy(moe_ladder_t* ladder);
 
 /* Size of the library's built-in route scratch used by moe_route_align_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)

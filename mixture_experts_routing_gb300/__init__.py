@@ -30,6 +30,7 @@ __all__ = [
     "pack_w2", "status_string", "launch_count", "device_error", "forward",
     "ffn_forward_train", "backward_workspace_bytes", "alloc_backward_workspace", "ffn_backward",
     "router_backward_workspace_bytes", "alloc_router_backward_workspace", "router_backward",
+    "Ladder", "ladder_pick",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -54,7 +55,8 @@ class Config(ctypes.Structure):
         "n_tokens", "hidden", "n_experts", "top_k", "inter", "cap_num", "cap_den", "block_m",
         "renorm", "ladder_len", "ladder_den")] + [("ladder_num", ctypes.POINTER(ctypes.c_int32)),
                                                   ("activation", ctypes.c_int32),
-                                                  ("prob_in_act", ctypes.c_int32)]
+                                                  ("prob_in_act", ctypes.c_int32),
+                                                  ("n_valid", ctypes.c_void_p)]
 
     def __init__(self, n_tokens, hidden, n_experts, top_k, inter, cap_num=1, cap_den=1,
                  block_m=32, renorm=1, ladder=None, ladder_den=1, activation=ACT_SWIGLU,
@@ -68,7 +70,7 @@ class Config(ctypes.Structure):
         super().__init__(n_tokens, hidden, n_experts, top_k, inter, cap_num, cap_den, block_m,
                          renorm, len(lad), ladder_den,
                          ctypes.cast(self._ladder, ctypes.POINTER(ctypes.c_int32)), activation,
-                         int(bool(prob_in_act)))
+                         int(bool(prob_in_act)), None)
 
 
 class _RoutesC(ctypes.Structure):
@@ -76,6 +78,14 @@ class _RoutesC(ctypes.Structure):
         "topk_ids", "topk_p", "keep", "expert_counts", "kept_counts", "sorted_slot_ids",
         "expert_ids", "block_start", "num_tokens_post_padded", "token_routes", "gemm_sched",
         "slot_prob")]
+
+
+class _LayerBufsC(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("w_router", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("routes", _RoutesC),
+                ("route_workspace", ctypes.c_void_p), ("route_workspace_bytes", ctypes.c_size_t),
+                ("h", ctypes.c_void_p), ("o", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("n_valid", ctypes.c_void_p)]
 
 
 class Routes:
@@ -117,6 +127,14 @@ def lib():
         L.moe_ffn_forward_train.argtypes = [CP, RP, P, P, P, P, P, P, P]
         L.moe_ffn_backward.argtypes = [CP, RP, P, P, P, P, P, P, P, P, P, P, SZ, P]
         L.moe_router_backward.argtypes = [CP, RP, P, P, P, P, P, P, P, P, SZ, P]
+        L.moe_ladder_pick.argtypes = [P, I32, ctypes.c_int32, ctypes.c_float]
+        L.moe_ladder_pick.restype = I32
+        L.moe_ladder_create.argtypes = [CP, P, I32, ctypes.c_float, ctypes.POINTER(_LayerBufsC),
+                                        ctypes.POINTER(ctypes.c_void_p)]
+        L.moe_ladder_forward.argtypes = [P, ctypes.c_int32, P, ctypes.POINTER(ctypes.c_int)]
+        L.moe_ladder_destroy.argtypes = [P]
+        for name in ("moe_ladder_create", "moe_ladder_forward", "moe_ladder_destroy"):
+            getattr(L, name).restype = I32
         L.moe_pack_w13.argtypes = [CP, P, P, P, P]
         L.moe_pack_w2.argtypes = [CP, P, P, P]
         for name in ("moe_route_align", "moe_fc1_forward", "moe_fc2_forward", "moe_ffn_forward",
@@ -307,3 +325,58 @@ def device_error() -> int:
     v = ctypes.c_uint32(0)
     _check("moe_device_error", lib().moe_device_error(ctypes.byref(v)))
     return int(v.value)
+
+
+def ladder_pick(buckets, n: int, max_pad_ratio: float = 0.0) -> int:
+    """Index of the bucket a batch of n tokens replays, or -1 for eager."""
+    arr = (ctypes.c_int32 * len(buckets))(*buckets)
+    return int(lib().moe_ladder_pick(ctypes.cast(arr, ctypes.c_void_p), len(buckets), int(n),
+                                     float(max_pad_ratio)))
+
+
+class Ladder:
+    """Captured forward graphs at a ladder of token-count buckets (moe_ladder_*).
+    Allocates the layer's buffers for the top bucket (cfg.n_tokens must equal
+    the last bucket); x, y, routes, h, o are torch tensors sized for it. A
+    forward of n tokens reads x[:n] and writes y[:n]."""
+
+    def __init__(self, cfg: Config, buckets, max_pad_ratio, w_router, bias, w13, w2, device):
+        import torch
+        self.cfg, self.buckets = cfg, list(buckets)
+        dev = torch.device(device)
+        N, H = cfg.n_tokens, cfg.hidden
+        self.x = torch.zeros((max(N, 1), H), dtype=torch.bfloat16, device=dev)
+        self.routes = alloc_routes(cfg, dev)
+        self.ws = alloc_workspace(cfg, dev)
+        self.h, self.o, self.y = alloc_buffers(cfg, dev)
+        self.n_valid = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._keep = (w_router, bias, w13, w2)  # the graphs hold their addresses
+        self._bufs = _LayerBufsC(self.x.data_ptr(), w_router.data_ptr(), _ptr(bias), w13.data_ptr(),
+                                 w2.data_ptr(), self.routes.c(), self.ws.data_ptr(),
+                                 self.ws.numel(), self.h.data_ptr(), self.o.data_ptr(),
+                                 self.y.data_ptr(), self.n_valid.data_ptr())
+        arr = (ctypes.c_int32 * len(self.buckets))(*self.buckets)
+        handle = ctypes.c_void_p()
+        _check("moe_ladder_create",
+               lib().moe_ladder_create(ctypes.byref(cfg), ctypes.cast(arr, ctypes.c_void_p),
+                                       len(self.buckets), float(max_pad_ratio),
+                                       ctypes.byref(self._bufs), ctypes.byref(handle)))
+        self._h = handle
+
+    def forward(self, n: int, stream=None) -> int:
+        """One forward of x[:n]; returns the bucket index replayed, -1 for eager."""
+        b = ctypes.c_int(0)
+        _check("moe_ladder_forward", lib().moe_ladder_forward(self._h, int(n), _stream(stream),
+                                                              ctypes.byref(b)))
+        return b.value
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().moe_ladder_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -32,8 +32,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <int KMAX>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const uint16_t* __restrict__ o, const int32_t* __restrict__ token_routes,
-    const float* __restrict__ topk_p, uint16_t* __restrict__ y, int N, int H, int K) {
+    const float* __restrict__ topk_p, uint16_t* __restrict__ y, int N,
+    const int32_t* __restrict__ n_dev, int H, int K) {
   const int t = blockIdx.x;
+  if (n_dev && t >= *n_dev) {  // a token past the live count: zero row
+    for (int v = threadIdx.x; v < H / 8; v += kCombineThreads)
+      reinterpret_cast<uint4*>(y + (size_t)t * H)[v] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
   int slot[KMAX];
   float w[KMAX];
 #pragma unroll
@@ -137,13 +143,13 @@ __global__ void transpose_kernel(const uint16_t* __restrict__ in, uint16_t* __re
 int launch_combine(const CombineArgs& a, cudaStream_t s) {
   if (a.N <= 0) return 0;
   if (a.K <= 2)
-    combine_kernel<2><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
+    combine_kernel<2><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
   else if (a.K <= 4)
-    combine_kernel<4><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
+    combine_kernel<4><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
   else if (a.K <= 8)
-    combine_kernel<8><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
+    combine_kernel<8><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
   else
-    combine_kernel<16><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.H, a.K);
+    combine_kernel<16><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }

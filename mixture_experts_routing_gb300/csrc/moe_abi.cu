@@ -162,6 +162,11 @@ int finish(int launched) {
 
 }  // namespace
 
+namespace moe {
+uint64_t launch_counter() { return g_launches.load(std::memory_order_relaxed); }
+void add_launches(int64_t n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace moe
+
 extern "C" {
 
 int64_t moe_capacity(const moe_config_t* cfg) {
@@ -202,8 +207,9 @@ int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_route
   a.K = cfg->top_k;
   a.renorm = cfg->renorm;
   a.bm = cfg->block_m;
-  a.cap = cap_of(cfg);
-  a.cpad = cpad_of(cfg);
+  a.n_dev = cfg->n_valid;
+  a.cap_num = cfg->cap_num;
+  a.cap_den = cfg->cap_den;
   a.dropless = dropless_of(cfg);
   a.ladder.len = a.dropless ? cfg->ladder_len : 0;
   a.ladder.den = cfg->ladder_den > 0 ? cfg->ladder_den : 1;
@@ -321,6 +327,7 @@ int moe_combine(const moe_config_t* cfg, const moe_routes_t* routes, const void*
   a.o = static_cast<const uint16_t*>(o);
   a.token_routes = routes->token_routes;
   a.topk_p = cfg->prob_in_act ? nullptr : routes->topk_p;  // unit weights: p' is in h
+  a.n_dev = cfg->n_valid;
   a.y = static_cast<uint16_t*>(y);
   return finish(moe::launch_combine(a, stream));
 }
@@ -362,6 +369,7 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
                      size_t ws_bytes, cudaStream_t stream) {
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
+  if (cfg->n_valid) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!routes_complete(routes)) return MOE_ERR_INVALID_ARG;
   if (!dw13 || !dw2 || !aligned16(dw13) || !aligned16(dw2)) return MOE_ERR_INVALID_ARG;
   const BwdLayout L = bwd_layout(cfg);
@@ -479,6 +487,7 @@ int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, con
                         cudaStream_t stream) {
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
+  if (cfg->n_valid) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!routes || !routes->topk_ids || !w_router || !dw_router) return MOE_ERR_INVALID_ARG;
   size_t dl_off, part_off, total;
   router_bwd_layout(cfg, &dl_off, &part_off, &total);

@@ -27,8 +27,9 @@ struct Ladder {  // dropless padding rungs: multiples num[j]/den of the expected
 };
 
 struct RouteArgs {
-  int N, H, E, K, renorm, bm;
-  int64_t cap, cpad;     // capacity mode
+  int N, H, E, K, renorm, bm;   // N: the static token bound (buffers, grids)
+  const int32_t* n_dev;         // live token count on the device, or null for N
+  int cap_num, cap_den;         // capacity factor (the capacity follows the live count)
   int dropless;          // 1: keep every route, extents from the ladder
   Ladder ladder;
   int64_t s_max;         // slots the caller allocated (static bound)
@@ -131,6 +132,7 @@ int launch_combine_bwd(const uint16_t* dxr, const float* part, int n_part,
 
 struct CombineArgs {
   int N, H, K;
+  const int32_t* n_dev;  // live token count (null: N); rows past it are written as 0
   const uint16_t* o;
   const int32_t* token_routes;
   const float* topk_p;
@@ -140,6 +142,11 @@ struct CombineArgs {
 int launch_combine(const CombineArgs& a, cudaStream_t s);
 
 // out[e*out_es + out_off + c*R + r] = in[e*in_es + r*C + c], bf16.
+// The library's launch counter (moe_launch_count): read, and adjusted by the
+// graph ladder (captured launches are not executions; a replay is).
+uint64_t launch_counter();
+void add_launches(int64_t n);
+
 int launch_transpose(const uint16_t* in, uint16_t* out, int E, int R, int C, int64_t in_es,
                      int64_t out_es, int64_t out_off, cudaStream_t s);
 

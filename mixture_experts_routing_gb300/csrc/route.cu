@@ -50,6 +50,15 @@ __device__ __forceinline__ float route_exp(float v) {
   return __fmul_rn(p, scale);
 }
 
+// Live token count: *n_dev clamped to [0, Nmax], or Nmax without a device
+// count. Buffers and grids are sized for Nmax (the static bound a captured
+// graph was built for); tokens at or past the live count are absent.
+__device__ __forceinline__ int live_tokens(const int32_t* n_dev, int Nmax) {
+  if (!n_dev) return Nmax;
+  const int v = *n_dev;
+  return v < 0 ? 0 : (v > Nmax ? Nmax : v);
+}
+
 // ---------------------------------------------------------------- R1
 // CTA tile BM tokens x BN experts, TM x TN outputs per thread (TN = 8 is two
 // groups of 4 columns, BN/2 apart, for conflict-free 16-byte shared loads),
@@ -77,8 +86,11 @@ constexpr size_t router_smem_bytes() {
 template <int BM, int BN, int TM, int TN>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN)) router_logits_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
-    float* __restrict__ logits, int N, int H, int E, int wr_vec4) {
+    float* __restrict__ logits, int Nmax, const int32_t* __restrict__ n_dev, int H, int E,
+    int wr_vec4) {
   constexpr int NT = (BM / TM) * (BN / TN);
+  const int N = live_tokens(n_dev, Nmax);
+  if ((int)blockIdx.y * BM >= N) return;  // the whole tile is past the live tokens
   extern __shared__ __align__(16) uint8_t rsm[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                    // [S][BM][BK] bf16
   float* bs = reinterpret_cast<float*>(rsm + LSTAGES * BM * LBK * 2);  // [S][BK][BN]
@@ -187,7 +199,7 @@ cudaError_t launch_router_logits(const RouteArgs& a, int vec4, cudaStream_t s) {
   }
   dim3 g((a.E + BN - 1) / BN, (a.N + BM - 1) / BM);
   router_logits_kernel<BM, BN, TM, TN><<<g, (BM / TM) * (BN / TN), smem, s>>>(
-      a.x, a.wr, a.bias, a.ws.logits, a.N, a.H, a.E, vec4);
+      a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, vec4);
   return cudaGetLastError();
 }
 
@@ -198,10 +210,11 @@ cudaError_t launch_router_logits(const RouteArgs& a, int vec4, cudaStream_t s) {
 constexpr int kTopkWarps = 32;
 
 __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
-    const float* __restrict__ logits, int N, int E, int K, int renorm, int32_t* __restrict__ topk_ids,
-    float* __restrict__ topk_p, int32_t* __restrict__ chunk_counts,
-    int32_t* __restrict__ chunk_lofs, int32_t* __restrict__ chunk_routes,
-    uint32_t* __restrict__ chunk_keys) {
+    const float* __restrict__ logits, int Nmax, const int32_t* __restrict__ n_dev, int E, int K,
+    int renorm, int32_t* __restrict__ topk_ids, float* __restrict__ topk_p,
+    int32_t* __restrict__ chunk_counts, int32_t* __restrict__ chunk_lofs,
+    int32_t* __restrict__ chunk_routes, uint32_t* __restrict__ chunk_keys,
+    uint8_t* __restrict__ keep, int32_t* __restrict__ token_routes) {
   __shared__ float zbuf[kTopkWarps][kMaxExperts];
   __shared__ int32_t ids_s[kTokensPerChunk * kMaxTopK];
   __shared__ uint32_t pk_s[kTokensPerChunk * kMaxTopK];
@@ -210,7 +223,18 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   const int t0 = c * kTokensPerChunk;
+  const int N = live_tokens(n_dev, Nmax);
   const int nt = min(kTokensPerChunk, N - t0);
+  // routes of tokens past the live count: no expert, no slot
+  for (int i = threadIdx.x; i < kTokensPerChunk * K; i += blockDim.x) {
+    const int t = t0 + i / K;
+    if (t >= N && t < Nmax) {
+      topk_ids[(size_t)t0 * K + i] = -1;
+      topk_p[(size_t)t0 * K + i] = 0.0f;
+      keep[(size_t)t0 * K + i] = 0;
+      token_routes[(size_t)t0 * K + i] = -1;
+    }
+  }
   constexpr int PER = kMaxExperts / 32;
   for (int tl = warp; tl < nt; tl += kTopkWarps) {
     const int t = t0 + tl;
@@ -346,9 +370,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
 // write the expert's part of the route-list layout.
 __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     const int32_t* __restrict__ chunk_counts, const int32_t* __restrict__ chunk_lofs,
-    const int32_t* __restrict__ chunk_routes, const uint32_t* __restrict__ chunk_keys, int N,
-    int E, int K,
-    int cap, int cpad, int bm, int dropless, Ladder ladder, int s_max,
+    const int32_t* __restrict__ chunk_routes, const uint32_t* __restrict__ chunk_keys, int Nmax,
+    const int32_t* __restrict__ n_dev, int E, int K, int cap_num, int cap_den, int bm,
+    int dropless, Ladder ladder, int s_max,
     uint8_t* __restrict__ keep, int32_t* __restrict__ expert_counts,
     int32_t* __restrict__ kept_counts, int32_t* __restrict__ sorted_slot_ids,
     int32_t* __restrict__ expert_ids, int32_t* __restrict__ block_start,
@@ -367,9 +391,19 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
   __shared__ int32_t s_all;       // dropless: total padded extent
   const int e = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int N = live_tokens(n_dev, Nmax);
+  // capacity of the live batch: cap = ceil(N*K*F/E) (capped at N), its region
+  // roundup(cap, bm); dropless keeps every route
+  int cap = N, cpad = 0;
+  if (!dropless) {
+    const long long num = (long long)N * K * cap_num, den = (long long)E * cap_den;
+    const long long cc = (num + den - 1) / den;
+    cpad = (int)((cc + bm - 1) / bm * bm);
+    cap = (int)(cc < N ? cc : N);
+  }
   const int C = (N + kTokensPerChunk - 1) / kTokensPerChunk;
-  uint32_t* keys = dyn;                                  // p' bits, token order
-  int32_t* rids = reinterpret_cast<int32_t*>(dyn + N);   // route index t*K+k
+  uint32_t* keys = dyn;                                     // p' bits, token order
+  int32_t* rids = reinterpret_cast<int32_t*>(dyn + Nmax);  // route index t*K+k
   // column e of the chunk tables -> positions in the expert's list
   const int cnt = (tid < C) ? min(max(chunk_counts[(size_t)tid * E + e], 0), kTokensPerChunk) : 0;
   const int pos0 = block_exclusive_scan(cnt, warp_tot);
@@ -519,19 +553,21 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
   }
   const int kept_e = select ? cap : n;
   for (int sl = kept_e + tid; sl < extent; sl += kSelThreads) {
-    sorted_slot_ids[base + sl] = N;
+    sorted_slot_ids[base + sl] = Nmax;  // sentinel: one past the static token bound
     slot_prob[base + sl] = 0.0f;
   }
   const int nb = extent / bm;
   for (int b = tid; b < nb; b += kSelThreads)
     expert_ids[(size_t)base / bm + b] = (b * bm < kept_e) ? e : -1;
-  if (dropless && e == E - 1) {
-    // slots past the padded total up to the allocated bound: sentinel / -1
-    for (int sl = s_all + tid; sl < s_max; sl += kSelThreads) {
-      sorted_slot_ids[sl] = N;
+  if (e == E - 1) {
+    // slots past the padded total up to the allocated bound (dropless, or a
+    // live batch below the static bound): sentinel / -1
+    const int used = dropless ? s_all : E * cpad;
+    for (int sl = used + tid; sl < s_max; sl += kSelThreads) {
+      sorted_slot_ids[sl] = Nmax;
       slot_prob[sl] = 0.0f;
     }
-    for (int b = s_all / bm + tid; b < s_max / bm; b += kSelThreads) expert_ids[b] = -1;
+    for (int b = used / bm + tid; b < s_max / bm; b += kSelThreads) expert_ids[b] = -1;
   }
   if (tid == 0) {
     block_start[e] = base / bm;
@@ -821,10 +857,10 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
                                       : launch_router_logits<64, 64, 4, 4>(a, vec4, s);
     if (e1 != cudaSuccess) return -(int)e1;
     ++launched;
-    router_topk_kernel<<<C, kTopkWarps * 32, 0, s>>>(a.ws.logits, a.N, a.E, a.K, a.renorm,
+    router_topk_kernel<<<C, kTopkWarps * 32, 0, s>>>(a.ws.logits, a.N, a.n_dev, a.E, a.K, a.renorm,
                                                      a.topk_ids, a.topk_p, a.ws.chunk_counts,
                                                      a.ws.chunk_lofs, a.ws.chunk_routes,
-                                                     a.ws.chunk_keys);
+                                                     a.ws.chunk_keys, a.keep, a.token_routes);
     ++launched;
   }
   const size_t dyn = (size_t)a.N * 8;
@@ -841,10 +877,9 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
       if (dev >= 0 && dev < 64) set_for[dev] = 1;
     }
   }
-  const int cap = (int)(a.cap < a.N ? a.cap : a.N);
   route_select_kernel<<<a.E, kSelThreads, dyn, s>>>(
-      a.ws.chunk_counts, a.ws.chunk_lofs, a.ws.chunk_routes, a.ws.chunk_keys, a.N, a.E, a.K, cap,
-      (int)a.cpad, a.bm, a.dropless, a.ladder, (int)a.s_max, a.keep, a.expert_counts,
+      a.ws.chunk_counts, a.ws.chunk_lofs, a.ws.chunk_routes, a.ws.chunk_keys, a.N, a.n_dev, a.E,
+      a.K, a.cap_num, a.cap_den, a.bm, a.dropless, a.ladder, (int)a.s_max, a.keep, a.expert_counts,
       a.kept_counts, a.sorted_slot_ids, a.expert_ids,
       a.block_start, a.ntpp, a.token_routes, a.gemm_sched, a.slot_prob);
   ++launched;
