@@ -14,6 +14,10 @@ workload that fits one GPU. Its inputs exceed L2, so no flush is needed.
     python bench.py --workload dropless    # training step of the dropless,
                                            # bucketed layer (forward + backward),
                                            # swept over N = 128 .. 16384
+    python bench.py --serve [--workload qwen3_30b]
+                                           # serving: a seeded sequence of
+                                           # variable batch sizes through the
+                                           # graph bucket ladder, and eager
 
 Under torchrun each rank is an independent replica with its own batch (weak
 scaling, no collective on the data path); value = tokens of all ranks / the
@@ -35,6 +39,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer fwd tokens/s on 1 GB300; grouped-GEMM TFLOPS as % of BF16 peak"
+METRIC_SERVE = ("MoE-layer serving tokens/s on 1 GB300: seeded variable batch sizes through the "
+                "graph bucket ladder")
 METRIC_TRAIN = ("MoE-layer fwd+bwd tokens/s on 1 GB300 (dropless bucketed layer, dX/dW backward); "
                 "TFLOPS as % of BF16 peak")
 UNIT = "tokens/s"
@@ -50,6 +56,10 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="dsv3")
     ap.add_argument("--block-m", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serve", action="store_true",
+                    help="variable batch sizes through the graph bucket ladder")
+    ap.add_argument("--serve-batches", type=int, default=64)
+    ap.add_argument("--pad-ratio", type=float, default=0.0)
     ap.add_argument("--cpu-experts", type=int, default=48,
                     help="experts whose FFN the CPU baseline runs (bounded sample)")
     return ap.parse_args(argv)
@@ -715,11 +725,133 @@ def run_ours_train(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- serving (graph ladder)
+def run_ours_serve(args):
+    import numpy as np
+    import torch
+
+    import mixture_experts_routing_gb300 as moe
+    import synth
+    import synth.gpu
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    w = synth.WORKLOADS[args.workload]
+    Ntop, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
+    top = moe.Config(Ntop, H, E, K, I, w.cap_num, w.cap_den, block_m=args.block_m,
+                     ladder=list(w.ladder), ladder_den=w.ladder_den)
+    wr = torch.from_numpy(synth.normal_f32(w.seed, synth.STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E)).to(dev)
+    bias = None if w.zipf_s is None else torch.from_numpy(synth.zipf_bias(w.seed, E, w.zipf_s)).to(dev)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    w13, w2 = torch.empty((E, 2 * I, H), **bf), torch.empty((E, H, I), **bf)
+    tmp, wu = torch.empty((E, H, I), **bf), torch.empty((E, H, I), **bf)
+    synth.gpu.fill(tmp, w.seed, synth.STREAM["wg"], w.w_std)
+    synth.gpu.fill(wu, w.seed, synth.STREAM["wu"], w.w_std)
+    moe.pack_w13(top, tmp, wu, w13)
+    del wu
+    tmp = tmp.view(E, I, H)
+    synth.gpu.fill(tmp, w.seed, synth.STREAM["wd"], w.w_std)
+    moe.pack_w2(top, tmp, w2)
+    del tmp
+    buckets = sorted({b for b in (128 << i for i in range(16)) if b < Ntop} | {Ntop})
+    L = moe.Ladder(top, buckets, args.pad_ratio, wr, bias, w13, w2, dev)
+    x_bits = synth.normal_bf16_bits(w.seed + rank, synth.STREAM["x"], 0, Ntop * H, w.x_std).reshape(Ntop, H)
+    L.x.copy_(torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(dev))
+    # the request sequence: log-uniform batch sizes in [16, Ntop], seeded
+    rng = np.random.default_rng(1234 + rank)
+    sizes = [int(v) for v in np.exp(rng.uniform(np.log(16), np.log(Ntop), args.serve_batches)).round()]
+    stream = torch.cuda.current_stream(dev)
+    # eager: the same three calls on exactly n tokens, configs built up front
+    cfgs = {n: moe.Config(n, H, E, K, I, w.cap_num, w.cap_den, block_m=args.block_m,
+                          ladder=list(w.ladder), ladder_den=w.ladder_den) for n in set(sizes)}
+
+    def eager(n):
+        moe.forward(cfgs[n], L.x, wr, bias, w13, w2, L.routes, L.ws, L.h, L.o, L.y, stream)
+
+    def run(fn, reps=1):
+        barrier(dist, dev)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record(stream)
+        for _ in range(reps):
+            for n in sizes:
+                fn(n)
+        b.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier(dist, dev)
+        return max_over_ranks(a.elapsed_time(b), dist, dev) / reps, wall / reps
+
+    used = [L.forward(n) for n in sizes]  # warm-up (and the bucket of every batch)
+    for _ in range(max(args.warmup - 1, 1)):
+        run(L.forward)
+    for _ in range(max(args.warmup, 2)):
+        run(eager)
+    torch.cuda.synchronize()
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    reps = max(1, args.steps // 10)
+    clocks = ClockSampler(dev.index).start()
+    time.sleep(0.3)
+    launches0 = moe.launch_count()
+    ms_ladder, wall_ladder = run(L.forward, reps)
+    launches = (moe.launch_count() - launches0) // reps
+    ms_eager, wall_eager = run(eager, reps)
+    clk = clocks.stop()
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+    tokens = sum(sizes) * world
+
+    # end to end through the ladder: each batch's x[:n] from pinned host memory in, y[:n] out
+    xh = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((Ntop, H), dtype=torch.bfloat16).pin_memory()
+
+    def e2e(n):
+        L.x[:n].copy_(xh[:n], non_blocking=True)
+        L.forward(n)
+        yh[:n].copy_(L.y[:n], non_blocking=True)
+
+    run(e2e)
+    ms_e2e, _ = run(e2e, reps)
+    out = {
+        "metric": METRIC_SERVE, "value": tokens / (ms_ladder / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": reps, "warmup": args.warmup, "ms_per_step": ms_ladder, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.note, "top_bucket": Ntop, "buckets": buckets,
+                   "max_pad_ratio": args.pad_ratio, "batches": len(sizes), "tokens_per_step": sum(sizes),
+                   "batch_sizes": sizes, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "step": "one pass over the request sequence"},
+        "gpu_launches": launches,
+        "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": sum(sizes) * H * 2, "d2h_bytes_per_step": sum(sizes) * H * 2},
+        "eager": {"value": tokens / (ms_eager / 1e3), "ms_per_step": ms_eager,
+                  "host_wall_ms_per_step": wall_eager * 1e3},
+        "ladder_host_wall_ms_per_step": wall_ladder * 1e3,
+        "speedup_vs_eager": ms_eager / ms_ladder,
+        "replayed_batches": sum(1 for b in used if b >= 0),
+        "roofline": None,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(out))
+    L.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     import synth
+    if args.serve:
+        return run_ours_serve(args)
     if synth.WORKLOADS[args.workload].cap_num == 0:
         return run_ours_train(args)
     return run_ours(args)
