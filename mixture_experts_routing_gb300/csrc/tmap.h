@@ -34,4 +34,21 @@ inline bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t r
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MN-major operand tiles in one copy: a 3-D view of a bf16 [rows, cols]
+// matrix as (64 columns, rows, cols/64 chunks), strides (row pitch, 128 B),
+// box {64, box_rows, box_chunks}: shared memory receives [chunk][row][64],
+// the 128-byte-swizzled MN-major layout with 64-element chunks.
+inline bool make_map_mn3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                          uint32_t box_rows, uint32_t box_chunks) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn || cols % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace moe
