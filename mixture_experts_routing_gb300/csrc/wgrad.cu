@@ -54,6 +54,7 @@ constexpr int kWTileQ = 4;
 struct WgradParams {
   int E, m_total, n_total, m_tiles, n_tiles, bm, stages;
   int tile_n;            // UMMA N: 256, or 128 when n_total is not a multiple of 256
+  int d_full;            // 64-column chunks of the slot-indexed operand in a full tile
   uint32_t buf_stride;   // TMEM columns of one accumulator buffer (2 x tile_n)
   int n_buf;             // accumulator buffers in flight (2 when 2 x buf_stride fits)
   int a_gather;          // 1: A from gathered token rows (dW13: x), B slot rows (dPre)
@@ -84,7 +85,8 @@ __device__ __forceinline__ void wtile_at(const WgradParams& p, int t, WTile& T) 
 }
 
 __global__ void __launch_bounds__(kWThreads, 1)
-    moe_wgrad_kernel(const __grid_constant__ CUtensorMap tmD, const WgradParams p) {
+    moe_wgrad_kernel(const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
+                     const WgradParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kWMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kWMaxStages];
@@ -118,6 +120,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
     mbar_fence_init();
     tma_prefetch_desc(&tmD);
+    tma_prefetch_desc(&tmD2);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), kWTmemCols);
   tc_fence_before();
@@ -171,9 +174,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
           const uint32_t fb = smem_u32(&full_bar[s]);
           const uint32_t st = sbase + (uint32_t)s * kWStageBytes + d_off;
           mbar_arrive_expect_tx(fb, (uint32_t)d_chunks * 8192u);
-          for (int c = 0; c < d_chunks; ++c)
-            tma_load_2d(st + (uint32_t)c * 8192u, &tmD, dcol0 + c * 64, T.slot0 + kt * kWK, fb,
-                        pol);
+          // all 64-column chunks in one 3-D copy ([chunk][slot][64]); tmD2
+          // holds 2 chunks, for the ragged last tile of the A side
+          tma_load_3d(st, d_chunks == p.d_full ? &tmD : &tmD2, 0, T.slot0 + kt * kWK, dcol0 / 64,
+                      fb, pol);
         }
         __syncwarp();
       }
@@ -377,7 +381,8 @@ int launch_wgrad(const WgradArgs& a, cudaStream_t s) {
   p.sched = a.sched;
   p.out = a.out;
   p.err = a.err;
-  CUtensorMap tmD;
+  CUtensorMap tmD, tmD2;
+  const int tile_n = ((a.dw13 ? 2 * a.I : a.H) % kWN == 0) ? kWN : 128;
   if (a.dw13) {
     // M = h (x gathered), N = k over 2I (dPre rows)
     p.a_gather = 1;
@@ -385,7 +390,10 @@ int launch_wgrad(const WgradArgs& a, cudaStream_t s) {
     p.n_total = 2 * a.I;
     p.act = static_cast<const uint16_t*>(a.x);
     p.act_ld = a.H;
-    if (!make_map(&tmD, a.slot_mat, (uint64_t)(2 * a.I), (uint64_t)a.s_max, 64, kWK)) return -1;
+    p.d_full = tile_n / 64;
+    if (!make_map_mn3d(&tmD, a.slot_mat, (uint64_t)(2 * a.I), (uint64_t)a.s_max, kWK, p.d_full) ||
+        !make_map_mn3d(&tmD2, a.slot_mat, (uint64_t)(2 * a.I), (uint64_t)a.s_max, kWK, 2))
+      return -1;
   } else {
     // M = i (aw rows), N = h (dY gathered)
     p.a_gather = 0;
@@ -393,10 +401,13 @@ int launch_wgrad(const WgradArgs& a, cudaStream_t s) {
     p.n_total = a.H;
     p.act = static_cast<const uint16_t*>(a.dy);
     p.act_ld = a.H;
-    if (!make_map(&tmD, a.slot_mat, (uint64_t)a.I, (uint64_t)a.s_max, 64, kWK)) return -1;
+    p.d_full = 4;  // two accumulators of 128 rows
+    if (!make_map_mn3d(&tmD, a.slot_mat, (uint64_t)a.I, (uint64_t)a.s_max, kWK, 4) ||
+        !make_map_mn3d(&tmD2, a.slot_mat, (uint64_t)a.I, (uint64_t)a.s_max, kWK, 2))
+      return -1;
   }
   p.act_rows = a.N;
-  p.tile_n = (p.n_total % kWN == 0) ? kWN : 128;
+  p.tile_n = tile_n;
   if (p.m_total % kWM != 0 || p.n_total % p.tile_n != 0) return -1;
   p.m_tiles = (p.m_total + 2 * kWM - 1) / (2 * kWM);
   p.n_tiles = p.n_total / p.tile_n;
@@ -410,7 +421,7 @@ int launch_wgrad(const WgradArgs& a, cudaStream_t s) {
   if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
   const int64_t tiles = (int64_t)p.E * p.m_tiles * p.n_tiles;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  moe_wgrad_kernel<<<grid, kWThreads, dyn, s>>>(tmD, p);
+  moe_wgrad_kernel<<<grid, kWThreads, dyn, s>>>(tmD, tmD2, p);
   err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }
