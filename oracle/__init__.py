@@ -244,6 +244,14 @@ def _bind_backward(L):
     L.oracle_wgrad_expert.restype = i32
     L.oracle_router_backward.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
     L.oracle_router_backward.restype = i32
+    L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_decode.restype = ctypes.c_float
+    L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    L.oracle_e4m3_encode.restype = ctypes.c_uint8
+    L.oracle_quantize_rows_fp8.argtypes = [i32, i32, P, P, P]
+    L.oracle_quantize_rows_fp8.restype = i32
+    L.oracle_fc1_fp8_routes.argtypes = [i32, P, P, i32, i32, P, P, P, P, i32, P, P]
+    L.oracle_fc1_fp8_routes.restype = i32
     L._bwd_bound = True
     return L
 
@@ -375,3 +383,43 @@ def router_backward(x_bits, wr, bias, K: int, dprob, renorm: bool = True, want_d
     if rc != 0:
         raise RuntimeError("oracle_router_backward failed: %d" % rc)
     return out
+
+
+# ---------------------------------------------------------------- FP8 (E4M3)
+def e4m3_decode(codes) -> np.ndarray:
+    L = _bind_backward(lib())
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([L.oracle_e4m3_decode(int(v)) for v in c.ravel()], np.float32).reshape(c.shape)
+
+
+def e4m3_encode(values) -> np.ndarray:
+    L = _bind_backward(lib())
+    v = np.asarray(values, dtype=np.float32)
+    return np.array([L.oracle_e4m3_encode(float(a)) for a in v.ravel()], np.uint8).reshape(v.shape)
+
+
+def quantize_rows_fp8(m_bits: np.ndarray):
+    """Row-wise E4M3 quantisation of a bf16 matrix: (codes [rows, cols] u8, scales [rows] f32)."""
+    L = _bind_backward(lib())
+    m = np.ascontiguousarray(m_bits, dtype=np.uint16)
+    rows, cols = m.shape
+    q = np.empty((rows, cols), np.uint8)
+    sc = np.empty(rows, np.float32)
+    L.oracle_quantize_rows_fp8(rows, cols, _p(m), _p(q), _p(sc))
+    return q, sc
+
+
+def fc1_fp8_routes(tokens, experts, xq, xs, wq13, ws13, H: int, I: int, act: int = ACT_SILU,
+                   scales=None) -> np.ndarray:
+    """h [n, I] of FC1 in FP8 for (token, expert) routes; wq13 [E,2I,H] u8, ws13 [E,2I] f32."""
+    L = _bind_backward(lib())
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    experts = np.ascontiguousarray(experts, dtype=np.int32)
+    n = len(tokens)
+    h = np.empty((n, I), np.float32)
+    sc = None if scales is None else np.ascontiguousarray(scales, dtype=np.float32)
+    L.oracle_fc1_fp8_routes(n, _p(tokens), _p(experts), H, I, _p(np.ascontiguousarray(xq, np.uint8)),
+                            _p(np.ascontiguousarray(xs, np.float32)),
+                            _p(np.ascontiguousarray(wq13, np.uint8)),
+                            _p(np.ascontiguousarray(ws13, np.float32)), int(act), _p(sc), _p(h))
+    return h

@@ -652,3 +652,77 @@ int oracle_router_backward(int N, int H, int E, int K, int renorm, const uint16_
   }
   return 0;
 }
+
+/* ======================================================================== */
+/* FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no      */
+/* infinities; exponent 15 with mantissa 7 is NaN; max finite 448).          */
+/* Normal code (e >= 1): (1 + m/8) * 2^(e-7); subnormal (e = 0): m/8 * 2^-6. */
+/* ======================================================================== */
+float oracle_e4m3_decode(uint8_t c) {
+  const int e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const float v = (e == 0) ? ldexpf((float)m, -9) : ldexpf((float)(8 + m), e - 10);
+  return (c & 0x80) ? -v : v;
+}
+
+/* Nearest finite E4M3 value, ties to the even code (even mantissa), values at
+ * or beyond 448 in magnitude saturate to +-448; NaN gives 0x7F. Written as a
+ * scan over the 127 finite non-negative codes (ascending in value). */
+uint8_t oracle_e4m3_encode(float v) {
+  if (v != v) return 0x7F;
+  const uint8_t sign = signbit(v) ? 0x80 : 0;
+  const float a = fabsf(v);
+  if (a >= 448.0f) return sign | 0x7E;
+  int best = 0;
+  for (int c = 1; c <= 0x7E; ++c) {
+    const float dc = fabsf(oracle_e4m3_decode((uint8_t)c) - a);
+    const float db = fabsf(oracle_e4m3_decode((uint8_t)best) - a);
+    if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+  }
+  return sign | (uint8_t)best;
+}
+
+/* Row-wise FP8 quantisation of an [rows, cols] bf16 matrix: per row,
+ * scale = max|v| / 448 (1 for an all-zero row), q = E4M3(v / scale) with the
+ * division in fp32. */
+int oracle_quantize_rows_fp8(int rows, int cols, const uint16_t* m, uint8_t* q, float* scale) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    const uint16_t* row = m + (size_t)r * cols;
+    float amax = 0.0f;
+    for (int c = 0; c < cols; ++c) amax = fmaxf(amax, fabsf(bf16_to_f32(row[c])));
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    scale[r] = s;
+    for (int c = 0; c < cols; ++c) q[(size_t)r * cols + c] = oracle_e4m3_encode(bf16_to_f32(row[c]) / s);
+  }
+  return 0;
+}
+
+/* FC1 in FP8 for a list of (token, expert) routes: with x quantised per token
+ * (xq [N,H], xs [N]) and the packed gate/up rows quantised per row
+ * (wq [E,2I,H], ws [E,2I]; rows [0,I) gate, [I,2I) up),
+ *   g_i = sum_h (E4M3(xq[t,h]) xs[t]) (E4M3(wq[e,i,h]) ws[e,i]),  u likewise,
+ *   h_i = act(g_i) u_i (times scales[j] when given),
+ * fp32, ascending h. h_out [n, I]. */
+int oracle_fc1_fp8_routes(int n, const int32_t* tokens, const int32_t* experts, int H, int I,
+                          const uint8_t* xq, const float* xs, const uint8_t* wq, const float* ws,
+                          int act, const float* scales, float* h_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int j = 0; j < n; ++j) {
+    const int t = tokens[j], e = experts[j];
+    const uint8_t* xr = xq + (size_t)t * H;
+    for (int i = 0; i < I; ++i) {
+      const size_t rg = (size_t)e * 2 * I + i, ru = rg + I;
+      const uint8_t* wg = wq + rg * H;
+      const uint8_t* wu = wq + ru * H;
+      float g = 0.0f, u = 0.0f;
+      for (int h = 0; h < H; ++h) {
+        const float xv = oracle_e4m3_decode(xr[h]) * xs[t];
+        g = g + xv * (oracle_e4m3_decode(wg[h]) * ws[rg]);
+        u = u + xv * (oracle_e4m3_decode(wu[h]) * ws[ru]);
+      }
+      h_out[(size_t)j * I + i] = act_fn(act, g) * u * (scales ? scales[j] : 1.0f);
+    }
+  }
+  return 0;
+}
