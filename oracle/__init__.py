@@ -252,6 +252,8 @@ def _bind_backward(L):
     L.oracle_quantize_rows_fp8.restype = i32
     L.oracle_fc1_fp8_routes.argtypes = [i32, P, P, i32, i32, P, P, P, P, i32, P, P]
     L.oracle_fc1_fp8_routes.restype = i32
+    L.oracle_fc2_fp8_routes.argtypes = [i32, P, i32, i32, P, P, P, P, P]
+    L.oracle_fc2_fp8_routes.restype = i32
     L._bwd_bound = True
     return L
 
@@ -423,3 +425,17 @@ def fc1_fp8_routes(tokens, experts, xq, xs, wq13, ws13, H: int, I: int, act: int
                             _p(np.ascontiguousarray(wq13, np.uint8)),
                             _p(np.ascontiguousarray(ws13, np.float32)), int(act), _p(sc), _p(h))
     return h
+
+
+def fc2_fp8_routes(experts, hq, hs, wq2, ws2, H: int, I: int) -> np.ndarray:
+    """o [n, H] of FC2 in FP8 for routes of the given experts; hq [n, I] u8 and
+    hs [n] f32 the routes' quantised h rows, wq2 [E,H,I] u8, ws2 [E,H] f32."""
+    L = _bind_backward(lib())
+    experts = np.ascontiguousarray(experts, dtype=np.int32)
+    n = len(experts)
+    o = np.empty((n, H), np.float32)
+    L.oracle_fc2_fp8_routes(n, _p(experts), H, I, _p(np.ascontiguousarray(hq, np.uint8)),
+                            _p(np.ascontiguousarray(hs, np.float32)),
+                            _p(np.ascontiguousarray(wq2, np.uint8)),
+                            _p(np.ascontiguousarray(ws2, np.float32)), _p(o))
+    return o

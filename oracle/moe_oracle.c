@@ -726,3 +726,26 @@ int oracle_fc1_fp8_routes(int n, const int32_t* tokens, const int32_t* experts, 
   }
   return 0;
 }
+
+/* FC2 in FP8 for n routes: with each route's h row quantised (hq [n,I],
+ * hs [n]) and each w2 row quantised (wq [E,H,I], ws [E,H]; row c of expert e
+ * is the c-th column of W_down[e]),
+ *   o_c = sum_i (E4M3(hq[j,i]) hs[j]) (E4M3(wq[e,c,i]) ws[e,c]),
+ * fp32, ascending i. o_out [n, H]. */
+int oracle_fc2_fp8_routes(int n, const int32_t* experts, int H, int I, const uint8_t* hq,
+                          const float* hs, const uint8_t* wq, const float* ws, float* o_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int j = 0; j < n; ++j) {
+    const int e = experts[j];
+    const uint8_t* hr = hq + (size_t)j * I;
+    for (int c = 0; c < H; ++c) {
+      const size_t r = (size_t)e * H + c;
+      const uint8_t* wr = wq + r * I;
+      float o = 0.0f;
+      for (int i = 0; i < I; ++i)
+        o = o + (oracle_e4m3_decode(hr[i]) * hs[j]) * (oracle_e4m3_decode(wr[i]) * ws[r]);
+      o_out[(size_t)j * H + c] = o;
+    }
+  }
+  return 0;
+}

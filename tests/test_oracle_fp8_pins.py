@@ -80,3 +80,25 @@ def test_fc1_fp8_matches_fp64_dequantised_reference(act):
         a = 0.5 * g * (1 + erf(g / np.sqrt(2))) if act == 1 else g / (1 + np.exp(-g))
         ref = a * u
         assert np.abs(h[j] - ref).max() <= 1e-5 * max(1.0, np.abs(ref).max())
+
+
+def test_fc2_fp8_matches_fp64_dequantised_reference():
+    rng = np.random.default_rng(11)
+    n, H, E, I = 5, 48, 3, 64
+    h = synth.f32_to_bf16_bits(rng.standard_normal((n, I)).astype(np.float32))
+    w2 = synth.f32_to_bf16_bits((rng.standard_normal((E * H, I)) * 0.1).astype(np.float32))
+    hq, hs = oracle.quantize_rows_fp8(h)
+    wq, ws = oracle.quantize_rows_fp8(w2)
+    exps = np.array([2, 0, 1, 2, 0], np.int32)
+    o = oracle.fc2_fp8_routes(exps, hq, hs, wq.reshape(E, H, I), ws.reshape(E, H), H, I)
+    Hd = oracle.e4m3_decode(hq).astype(np.float64) * hs[:, None]
+    W = oracle.e4m3_decode(wq).astype(np.float64) * ws[:, None]
+    for j, e in enumerate(exps):
+        ref = W[e * H:(e + 1) * H] @ Hd[j]
+        assert np.abs(o[j] - ref).max() <= 1e-5 * max(1.0, np.abs(ref).max())
+    # dequantised operands stay within the quantisation error of the bf16 product
+    full = synth.bf16_bits_to_f32(w2).astype(np.float64).reshape(E, H, I)
+    hf = synth.bf16_bits_to_f32(h).astype(np.float64)
+    for j, e in enumerate(exps):
+        exact = full[e] @ hf[j]
+        assert np.abs(o[j] - exact).max() <= 0.15 * np.abs(exact).max()

@@ -49,6 +49,12 @@ MUTATIONS = [
      lambda: [fx.test_e4m3_encode_rounding(v, c) for v, c in ((1.0625, 0x38), (1.1875, 0x3A))]),
     ("E4M3 subnormals with the normal exponent bias", "ldexpf((float)m, -9)", "ldexpf((float)m, -10)",
      lambda: fx.test_e4m3_decode_table(0x01, 2.0 ** -9)),
+    ("FP8 FC2 scales the weight row by the expert's first row", "(oracle_e4m3_decode(wr[i]) * ws[r]);",
+     "(oracle_e4m3_decode(wr[i]) * ws[(size_t)e * H]);",
+     lambda: fx.test_fc2_fp8_matches_fp64_dequantised_reference()),
+    ("FP8 FC1 scales the up row by the gate row's scale", "u = u + xv * (oracle_e4m3_decode(wu[h]) * ws[ru]);",
+     "u = u + xv * (oracle_e4m3_decode(wu[h]) * ws[rg]);",
+     lambda: fx.test_fc1_fp8_matches_fp64_dequantised_reference(0)),
     ("router backward skips the renormalisation term", "gk[k] = (dp[k] - c) / d;",
      "gk[k] = dp[k] / d;", lambda: rb.test_router_backward_matches_central_differences(0, True)),
     ("router backward skips the softmax normaliser", "dl[ids[k]] = p[ids[k]] * (gk[k] - s);",
