@@ -666,19 +666,25 @@ float oracle_e4m3_decode(uint8_t c) {
 }
 
 /* Nearest finite E4M3 value, ties to the even code (even mantissa), values at
- * or beyond 448 in magnitude saturate to +-448; NaN gives 0x7F. Written as a
- * scan over the 127 finite non-negative codes (ascending in value). */
+ * or beyond 448 in magnitude saturate to +-448; NaN gives 0x7F. The 127 finite
+ * non-negative codes ascend in value with the code, so the nearest one is the
+ * smallest code whose value is >= |v| (found by bisection) or the code below
+ * it. */
 uint8_t oracle_e4m3_encode(float v) {
   if (v != v) return 0x7F;
   const uint8_t sign = signbit(v) ? 0x80 : 0;
   const float a = fabsf(v);
   if (a >= 448.0f) return sign | 0x7E;
-  int best = 0;
-  for (int c = 1; c <= 0x7E; ++c) {
-    const float dc = fabsf(oracle_e4m3_decode((uint8_t)c) - a);
-    const float db = fabsf(oracle_e4m3_decode((uint8_t)best) - a);
-    if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+  int lo = 0, hi = 0x7E;  /* decode(0x7E) = 448 > a */
+  while (lo < hi) {
+    const int mid = (lo + hi) / 2;
+    if (oracle_e4m3_decode((uint8_t)mid) >= a) hi = mid;
+    else lo = mid + 1;
   }
+  if (lo == 0) return sign;  /* a == 0 */
+  const float dc = oracle_e4m3_decode((uint8_t)lo) - a;      /* above, >= 0 */
+  const float db = a - oracle_e4m3_decode((uint8_t)(lo - 1)); /* below, > 0 */
+  const int best = (dc < db || (dc == db && (lo & 1) == 0)) ? lo : lo - 1;
   return sign | (uint8_t)best;
 }
 

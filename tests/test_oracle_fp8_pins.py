@@ -40,6 +40,22 @@ def test_e4m3_encode_rounding(value, code):
     assert oracle.e4m3_encode([value])[0] == code
 
 
+def test_e4m3_encode_is_nearest_code_for_every_bf16_value():
+    """Every bf16 value of magnitude up to 450, both signs: the code is the
+    nearest finite value by exhaustive search over the decoded table, ties to
+    the even code, saturation at 448."""
+    vals = synth.bf16_bits_to_f32(np.arange(0, 0x43E1, dtype=np.uint16)).astype(np.float64)
+    table = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8)).astype(np.float64)
+    d = np.abs(table[None, :] - np.minimum(vals, 448.0)[:, None])
+    best = d.min(axis=1, keepdims=True)
+    ties = d == best
+    # the lowest even candidate when two tie, else the only one
+    even = ties & (np.arange(0x7F)[None, :] % 2 == 0)
+    expect = np.where(ties.sum(axis=1) > 1, even.argmax(axis=1), ties.argmax(axis=1)).astype(np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(vals), expect)
+    assert np.array_equal(oracle.e4m3_encode(-vals[1:]), expect[1:] | 0x80)
+
+
 def test_quantize_rows_scale_and_extremes():
     rng = np.random.default_rng(0)
     m = synth.f32_to_bf16_bits(rng.standard_normal((6, 40)).astype(np.float32) * 3)
