@@ -14,6 +14,9 @@ workload that fits one GPU. Its inputs exceed L2, so no flush is needed.
     python bench.py --workload dropless    # training step of the dropless,
                                            # bucketed layer (forward + backward),
                                            # swept over N = 128 .. 16384
+    python bench.py --fp8                  # the same forward with the expert GEMMs
+                                           # on E4M3 operands (row-wise scales): a
+                                           # variant line; the headline is bf16
     python bench.py --serve [--workload qwen3_30b]
                                            # serving: a seeded sequence of
                                            # variable batch sizes through the
@@ -56,6 +59,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="dsv3")
     ap.add_argument("--block-m", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="expert GEMMs on E4M3 operands with row-wise fp32 scales (x and h "
+                         "quantised in the step); prints a variant line, not the bf16 headline")
     ap.add_argument("--serve", action="store_true",
                     help="variable batch sizes through the graph bucket ladder")
     ap.add_argument("--serve-batches", type=int, default=64)
@@ -183,22 +189,30 @@ def ncu_traffic(kernel: str, workload: str, units: float):
 
 
 # ----------------------------------------------------------------------------- work model
-def work_model(w, kept_counts):
+def work_model(w, kept_counts, fp8=False, slots=0):
     """Algorithmic bytes and flops per launch of each kernel, from the
-    per-expert kept counts of this batch."""
+    per-expert kept counts of this batch. fp8: GEMM operands are one byte
+    (plus a 4-byte scale per row), and the two quantisation passes read
+    bf16 x and the `slots` used rows of h."""
     import numpy as np
     N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
     kc = np.asarray(kept_counts, dtype=np.int64)
     kept = int(kc.sum())
     active = int((kc > 0).sum())
     rows = int(((kc + 15) // 16 * 16).sum())  # slots the GEMMs compute (16-row granule)
+    ob = 1.0 if fp8 else 2.0                  # bytes per GEMM operand element
+    sb = 4.0 if fp8 else 0.0                  # bytes of scale per operand row
     m = {}
     m["fc1"] = {"flops": 2.0 * kept * H * 2 * I,
-                "bytes": active * 2.0 * I * H * 2 + N * H * 2 + rows * I * 2,
+                "bytes": active * 2.0 * I * (H * ob + sb) + N * (H * ob + sb) + rows * I * 2,
                 "units": active, "unit": "active expert"}
     m["fc2"] = {"flops": 2.0 * kept * I * H,
-                "bytes": active * 1.0 * H * I * 2 + rows * I * 2 + rows * H * 2,
+                "bytes": active * 1.0 * H * (I * ob + sb) + rows * (I * ob + sb) + rows * H * 2,
                 "units": active, "unit": "active expert"}
+    if fp8:
+        m["quant_x"] = {"flops": 0.0, "bytes": N * H * 3.0 + N * 4, "units": N, "unit": "token"}
+        m["quant_h"] = {"flops": 0.0, "bytes": slots * I * 3.0 + slots * 4, "units": slots,
+                        "unit": "slot"}
     m["combine"] = {"flops": 2.0 * kept * H, "bytes": kept * H * 2.0 + N * H * 2 + N * K * 8,
                     "units": N, "unit": "token"}
     m["route"] = {"flops": 2.0 * N * H * E, "bytes": N * H * 2.0 + H * E * 4 + N * E * 8 + N * K * 24,
@@ -207,12 +221,14 @@ def work_model(w, kept_counts):
     return m
 
 
-def roofline_for(name, model, ms, peaks, workload):
-    """Roofline object of one kernel: bound, achieved, peak, frac, traffic."""
+def roofline_for(name, model, ms, peaks, workload, fp8=False):
+    """Roofline object of one kernel: bound, achieved, peak, frac, traffic.
+    An E4M3 contraction takes the measured bf16 peak times the nominal
+    FP8/BF16 dense ratio (4.5 / 2.25 PFLOP/s)."""
     d = model[name]
     sec = ms / 1e3
     hbm = peaks["hbm_gbs"]
-    tensor = peaks["bf16_tflops"]
+    tensor = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
     alu = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12  # fp32 FMA pipes
     if name == "route":
         t_c, peak_c = d["flops"] / (alu * 1e12), alu
@@ -227,8 +243,10 @@ def roofline_for(name, model, ms, peaks, workload):
     else:
         ach = d["flops"] / sec / 1e12
         r = {"bound": "alu" if name == "route" else "tensor", "achieved": ach, "peak": peak_c,
-             "unit": "TFLOP/s", "frac": ach / peak_c, "peak_source": src}
-    tr = ncu_traffic("moe_gemm_kernel:" + name, workload, d["units"]) if name in ("fc1", "fc2") else None
+             "unit": "TFLOP/s", "frac": ach / peak_c,
+             "peak_source": src + (" x 2 (nominal FP8/BF16 ratio)" if fp8 and name != "route" else "")}
+    tr = (ncu_traffic("moe_gemm_kernel:" + name + ("_fp8" if fp8 else ""), workload, d["units"])
+          if name in ("fc1", "fc2") else None)
     r["traffic"] = tr
     r["kernel"] = name
     r["ms"] = ms
@@ -279,6 +297,53 @@ def time_oracle_sample(w, x_bits, wr, bias, bm, n_experts_sample, seed_experts=0
     return N / t_full, desc, t_route + t_ffn + t_comb, oracle.num_threads()
 
 
+def time_oracle_sample_fp8(w, x_bits, wr, bias, bm, n_experts_sample, seed_experts=0):
+    """The oracle's FP8 chain, as it stands, on a bounded sample of one step:
+    routing and x quantisation of every token; FC1 on E4M3 operands, h
+    rounded to bf16 and quantised, FC2 on E4M3 operands for the kept routes
+    of `n_experts_sample` experts (extrapolated to all kept routes by route
+    count; their weights are quantised once, outside the timing, as the GPU
+    path does); combine of every token."""
+    import numpy as np
+    import oracle
+    import synth
+    N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
+    t0 = time.perf_counter()
+    R = oracle.route(x_bits, wr, bias, E, K, w.cap_num, w.cap_den, bm)
+    xq, xs = oracle.quantize_rows_fp8(x_bits)
+    t_route = time.perf_counter() - t0
+    L = R.layout
+    kept_total = int(L.kept_counts.sum())
+    cand = [e for e in range(E) if L.kept_counts[e] > 0]
+    rng = np.random.default_rng(seed_experts)
+    sample = sorted(rng.choice(cand, size=min(n_experts_sample, len(cand)), replace=False).tolist())
+    t_ffn, n_routes = 0.0, 0
+    for e in sample:
+        wg = synth.normal_bf16_bits(w.seed, synth.STREAM["wg"], e * H * I, H * I, w.w_std).reshape(H, I)
+        wu = synth.normal_bf16_bits(w.seed, synth.STREAM["wu"], e * H * I, H * I, w.w_std).reshape(H, I)
+        wd = synth.normal_bf16_bits(w.seed, synth.STREAM["wd"], e * I * H, I * H, w.w_std).reshape(I, H)
+        w13q, w13s = oracle.quantize_rows_fp8(np.ascontiguousarray(np.concatenate([wg.T, wu.T], 0)))
+        w2q, w2s = oracle.quantize_rows_fp8(np.ascontiguousarray(wd.T))
+        base, k = e * L.cpad, int(L.kept_counts[e])
+        toks = L.sorted_slot_ids[base:base + k]
+        zero = np.zeros(k, np.int32)
+        t0 = time.perf_counter()
+        h = oracle.fc1_fp8_routes(toks, zero, xq, xs, w13q[None], w13s[None], H, I)
+        hq, hs = oracle.quantize_rows_fp8(synth.f32_to_bf16_bits(h))
+        oracle.fc2_fp8_routes(zero, hq, hs, w2q[None], w2s[None], H, I)
+        t_ffn += time.perf_counter() - t0
+        n_routes += k
+    o_zero = np.zeros((N * K, H), dtype=np.float32)
+    t0 = time.perf_counter()
+    oracle.combine(0, N, L.keep, R.topk_p, o_zero)
+    t_comb = time.perf_counter() - t0
+    t_full = t_route + t_ffn * kept_total / max(n_routes, 1) + t_comb
+    desc = ("FP8 chain: routing and x quantisation of all %d tokens + FC1/h quantisation/FC2 on "
+            "E4M3 operands for %d/%d experts (%d of %d kept routes, time extrapolated by route "
+            "count) + combine of all tokens" % (N, len(sample), len(cand), n_routes, kept_total))
+    return N / t_full, desc, t_route + t_ffn + t_comb, oracle.num_threads()
+
+
 def host_inputs(w, rank_seed):
     import synth
     N, H, E = w.n_tokens, w.hidden, w.n_experts
@@ -304,6 +369,9 @@ def run_reference(args):
         def sample(i):
             return time_oracle_train_sample(w, x_bits, dy_bits, wr, bias, args.block_m, n_routes=1024,
                                             seed=i)
+    elif args.fp8:
+        def sample(i):
+            return time_oracle_sample_fp8(w, x_bits, wr, bias, args.block_m, 1, seed_experts=i)
     else:
         n_exp = max(1, min(4, args.cpu_experts))
 
@@ -324,7 +392,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.n_tokens / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": {"workload": w.name, "description": w.note, "block_m": args.block_m,
-                                        "parallelism": "single host, OpenMP"},
+                                        "parallelism": "single host, OpenMP",
+                                        "precision": ("E4M3 GEMM operands, row-wise scales"
+                                                      if args.fp8 and not train else "bf16 inputs")},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "per step: " + desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -379,24 +449,47 @@ def run_ours(args):
     ws = moe.alloc_workspace(cfg, dev)
     h, o, y = moe.alloc_buffers(cfg, dev)
     stream = torch.cuda.current_stream(dev)
+    fp8 = args.fp8
+    weight_bytes = (w13.numel() + w2.numel()) * (1 if fp8 else 2)
+    quant_ms = None
+    if fp8:  # weights quantised once, before any step
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        q0.record(stream)
+        wq = moe.Fp8Weights(cfg, w13, w2, stream)
+        q1.record(stream)
+        torch.cuda.synchronize()
+        quant_ms = q0.elapsed_time(q1)
+        del w13, w2
+        torch.cuda.empty_cache()
+        xq, xs, hq, hs = moe.alloc_fp8_buffers(cfg, dev)
 
-    names = ("route", "fc1", "fc2", "combine")
+    names = (("route", "quant_x", "fc1", "quant_h", "fc2", "combine") if fp8
+             else ("route", "fc1", "fc2", "combine"))
 
     def step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
+        def mark(i):
+            if evs is not None:
+                evs[i].record(stream)
+        mark(0)
         moe.route_align(cfg, x, wr, bias, routes, ws, stream)
-        if evs is not None:
-            evs[1].record(stream)
-        moe.fc1_forward(cfg, routes, x, w13, h, stream)
-        if evs is not None:
-            evs[2].record(stream)
-        moe.fc2_forward(cfg, routes, h, w2, o, stream)
-        if evs is not None:
-            evs[3].record(stream)
+        mark(1)
+        if fp8:
+            moe.quantize_rows_fp8(x, xq, xs, stream)
+            mark(2)
+            moe.fc1_forward_fp8(cfg, routes, xq, xs, wq.w13q, wq.w13_scale, h, stream)
+            mark(3)
+            # only the slots below the padded extent hold routes
+            moe.quantize_rows_fp8(h, hq, hs, stream, rows_dev=routes.num_tokens_post_padded)
+            mark(4)
+            moe.fc2_forward_fp8(cfg, routes, hq, hs, wq.w2q, wq.w2_scale, o, stream)
+            mark(5)
+        else:
+            moe.fc1_forward(cfg, routes, x, w13, h, stream)
+            mark(2)
+            moe.fc2_forward(cfg, routes, h, w2, o, stream)
+            mark(3)
         moe.combine(cfg, routes, o, y, stream)
-        if evs is not None:
-            evs[4].record(stream)
+        mark(len(names))
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -405,7 +498,8 @@ def run_ours(args):
         raise RuntimeError("device error word set during warm-up")
 
     # ---- device-timed region
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+           for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, dev)
     torch.cuda.synchronize()
@@ -426,6 +520,7 @@ def run_ours(args):
     if moe.device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
     kept_counts = routes.kept_counts.cpu().numpy()
+    used_slots = int(routes.num_tokens_post_padded.cpu()[0])
 
     # ---- end to end: pinned host x in, host y out, every step
     x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -447,10 +542,10 @@ def run_ours(args):
     barrier(dist, dev)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
-    model = work_model(w, kept_counts)
-    dom = max(("fc1", "fc2", "combine", "route"), key=lambda n: per_kernel[n])
-    roof = roofline_for(dom, model, per_kernel[dom], peaks, w.name)
-    kernels = {n: roofline_for(n, model, per_kernel[n], peaks, w.name) for n in names}
+    model = work_model(w, kept_counts, fp8=fp8, slots=used_slots)
+    dom = max(names, key=lambda n: per_kernel[n])
+    roof = roofline_for(dom, model, per_kernel[dom], peaks, w.name, fp8=fp8)
+    kernels = {n: roofline_for(n, model, per_kernel[n], peaks, w.name, fp8=fp8) for n in names}
     gemm_ms = per_kernel["fc1"] + per_kernel["fc2"]
     gemm_flops = model["fc1"]["flops"] + model["fc2"]["flops"]
     issued = 2.0 * 3 * H * I * E * moe.capacity(cfg)
@@ -460,18 +555,20 @@ def run_ours(args):
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "data": "synthetic",
         "config": {"workload": w.name, "description": w.note, "tokens_per_step_per_gpu": N,
                    "block_m": args.block_m, "capacity": moe.capacity(cfg),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (%.1f GB of expert weights); no flush"
-                         % ((w13.numel() + w2.numel()) * 2 / 1e9)},
+                         % (weight_bytes / 1e9)},
         "gpu_launches": launches,
         "e2e": {"value": N * world * args.steps / (ms_e2e / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": N * H * 2, "d2h_bytes_per_step": N * H * 2},
         "roofline": roof,
         "grouped_gemm": {"ms": gemm_ms, "tflops_useful": gemm_flops / (gemm_ms / 1e3) / 1e12,
                          "pct_bf16_peak": gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                         "operands": "e4m3" if fp8 else "bf16",
                          "tflops_issued_capacity_shape": issued / (gemm_ms / 1e3) / 1e12,
                          "kept_routes": model["_kept"], "active_experts": model["_active"]},
         "kernels_ms": per_kernel,
@@ -479,8 +576,18 @@ def run_ours(args):
                     for n in names},
         "clocks": clk,
     }
+    if fp8:
+        out["config"]["precision"] = ("E4M3 GEMM operands with one fp32 scale per row (w13, w2 "
+                                      "rows once; x and h rows every step), fp32 accumulation; "
+                                      "x, h, o, y in bf16")
+        out["weight_quantisation_ms"] = quant_ms
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, secs, cores = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m, args.cpu_experts)
+        if fp8:
+            v, desc, secs, cores = time_oracle_sample_fp8(w, x_bits, wr_h, bias_h, args.block_m,
+                                                          min(args.cpu_experts, 2))
+        else:
+            v, desc, secs, cores = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
+                                                      args.cpu_experts)
         out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": desc, "cpu_seconds": secs}
     if rank == 0:

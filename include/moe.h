@@ -228,6 +228,62 @@ int moe_pack_w13(const moe_config_t* cfg, const void* w_gate, const void* w_up, 
                  cudaStream_t stream);
 int moe_pack_w2(const moe_config_t* cfg, const void* w_down, void* w2, cudaStream_t stream);
 
+/* ---- FP8 (E4M3) expert GEMMs ------------------------------------------------
+ * The pages run their experts in bf16 and reject FP8 ([FC] Changelog / Known
+ * limitations: BF16 experts only); this is an extension beyond them, not a
+ * mode they define. Operands are E4M3 codes (1 sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits, largest finite 448, no infinities) with one fp32 scale
+ * per row: value = decode(code) * scale. The GEMMs accumulate the code products
+ * in fp32 on the tensor cores and apply the weight-row scale times the
+ * activation-row scale in the epilogue. */
+
+/* Row-wise quantisation of a bf16 matrix.
+ *  m         [rows, cols] bf16, cols a multiple of 8
+ *  rows_dev  device int32 or NULL: when given, only rows below *rows_dev (read
+ *            on the device when the kernel runs, e.g. num_tokens_post_padded
+ *            for the slot rows of h) are quantised; the others are left as
+ *            they are
+ *  q         [rows, cols] u8 output codes, 16-byte aligned
+ *  scale     [rows] f32 output: amax(|row|)/448 (fp32, correctly rounded), 1
+ *            for an all-zero row
+ * q = E4M3(m / scale): correctly rounded fp32 divide, then round to nearest
+ * even with saturation to +-448. Weights are quantised once (w13 rows as
+ * [E*2I, H], w2 rows as [E*H, I]); activations on each call. */
+int moe_quantize_rows_fp8(const void* m, int64_t rows, const int32_t* rows_dev, int cols, void* q,
+                          float* scale, cudaStream_t stream);
+
+/* FC1 on FP8 operands, otherwise as moe_fc1_forward.
+ *  xq  [N,H] u8, x_scale [N] f32    quantised token rows
+ *  w13q [E,2I,H] u8, w13_scale [E*2I] f32   quantised packed gate/up rows
+ *  h   [S,I] bf16 output, h[s,i] = act(g) u (times p' when cfg->prob_in_act),
+ *      g = x_scale[t] w13_scale[e*2I+i] sum_k xq[t,k] w13q[e,i,k] (decoded codes),
+ *      u likewise from row e*2I+I+i; fp32 accumulation; written-row rule as h
+ *      in moe_fc1_forward. H must be a multiple of 128. */
+int moe_fc1_forward_fp8(const moe_config_t* cfg, const moe_routes_t* routes, const void* xq,
+                        const float* x_scale, const void* w13q, const float* w13_scale, void* h,
+                        cudaStream_t stream);
+
+/* FC2 on FP8 operands, otherwise as moe_fc2_forward.
+ *  hq  [S,I] u8, h_scale [S] f32    quantised slot rows of h
+ *  w2q [E,H,I] u8, w2_scale [E*H] f32   quantised packed w2 rows
+ *  o   [S,H] bf16 output, o[s,c] = h_scale[s] w2_scale[e*H+c] sum_i hq[s,i] w2q[e,c,i]
+ *      for the kept slots s of expert e; o = 0 in padding slots below
+ *      roundup(kept_counts[e],16). I must be a multiple of 128. */
+int moe_fc2_forward_fp8(const moe_config_t* cfg, const moe_routes_t* routes, const void* hq,
+                        const float* h_scale, const void* w2q, const float* w2_scale, void* o,
+                        cudaStream_t stream);
+
+/* FP8 expert path for bf16 input: quantise x into xq/x_scale, FC1 on FP8
+ * into h (bf16), quantise the slot rows of h that lie below
+ * num_tokens_post_padded into hq/h_scale, FC2 on FP8 into o. Four launches on
+ * one stream; the caller owns every buffer:
+ *  x [N,H] bf16;  xq [N,H] u8;  x_scale [N] f32;  h [S,I] bf16;  hq [S,I] u8;
+ *  h_scale [S] f32;  o [S,H] bf16;  weights as above. */
+int moe_ffn_forward_fp8(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                        const void* w13q, const float* w13_scale, const void* w2q,
+                        const float* w2_scale, void* xq, float* x_scale, void* h, void* hq,
+                        float* h_scale, void* o, cudaStream_t stream);
+
 /* Bytes of scratch moe_ffn_backward needs: about S*(2 + 6I + 2H) bytes plus
  * S*I/8 for the dprob partials (S = moe_max_slots). */
 int64_t moe_backward_workspace_bytes(const moe_config_t* cfg);

@@ -137,9 +137,14 @@ def lib():
             getattr(L, name).restype = I32
         L.moe_pack_w13.argtypes = [CP, P, P, P, P]
         L.moe_pack_w2.argtypes = [CP, P, P, P]
+        L.moe_quantize_rows_fp8.argtypes = [P, I64, P, I32, P, P, P]
+        L.moe_fc1_forward_fp8.argtypes = [CP, RP, P, P, P, P, P, P]
+        L.moe_fc2_forward_fp8.argtypes = [CP, RP, P, P, P, P, P, P]
+        L.moe_ffn_forward_fp8.argtypes = [CP, RP, P, P, P, P, P, P, P, P, P, P, P, P]
         for name in ("moe_route_align", "moe_fc1_forward", "moe_fc2_forward", "moe_ffn_forward",
                      "moe_combine", "moe_pack_w13", "moe_pack_w2", "moe_ffn_forward_train",
-                     "moe_ffn_backward", "moe_router_backward"):
+                     "moe_ffn_backward", "moe_router_backward", "moe_quantize_rows_fp8",
+                     "moe_fc1_forward_fp8", "moe_fc2_forward_fp8", "moe_ffn_forward_fp8"):
             getattr(L, name).restype = I32
         L.moe_status_string.argtypes = [I32]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -307,6 +312,66 @@ def pack_w13(cfg: Config, w_gate, w_up, w13, stream=None) -> None:
 def pack_w2(cfg: Config, w_down, w2, stream=None) -> None:
     _check("moe_pack_w2", lib().moe_pack_w2(ctypes.byref(cfg), _ptr(w_down), _ptr(w2),
                                             _stream(stream)))
+
+
+def quantize_rows_fp8(m, q, scale, stream=None, rows_dev=None) -> None:
+    """Row-wise E4M3 codes q [rows, cols] u8 and scales [rows] f32 of a bf16
+    matrix m; rows_dev (a device int32 tensor) bounds the rows quantised."""
+    rows, cols = m.shape
+    _check("moe_quantize_rows_fp8",
+           lib().moe_quantize_rows_fp8(_ptr(m), int(rows), _ptr(rows_dev), int(cols), _ptr(q),
+                                       _ptr(scale), _stream(stream)))
+
+
+def fc1_forward_fp8(cfg: Config, routes: Routes, xq, x_scale, w13q, w13_scale, h,
+                    stream=None) -> None:
+    _check("moe_fc1_forward_fp8",
+           lib().moe_fc1_forward_fp8(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(xq),
+                                     _ptr(x_scale), _ptr(w13q), _ptr(w13_scale), _ptr(h),
+                                     _stream(stream)))
+
+
+def fc2_forward_fp8(cfg: Config, routes: Routes, hq, h_scale, w2q, w2_scale, o,
+                    stream=None) -> None:
+    _check("moe_fc2_forward_fp8",
+           lib().moe_fc2_forward_fp8(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(hq),
+                                     _ptr(h_scale), _ptr(w2q), _ptr(w2_scale), _ptr(o),
+                                     _stream(stream)))
+
+
+class Fp8Weights:
+    """w13 and w2 quantised row-wise once: codes (u8) and fp32 row scales."""
+
+    def __init__(self, cfg: Config, w13, w2, stream=None):
+        import torch
+        E, H, I = cfg.n_experts, cfg.hidden, cfg.inter
+        dev = w13.device
+        self.w13q = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev)
+        self.w13_scale = torch.empty(E * 2 * I, dtype=torch.float32, device=dev)
+        self.w2q = torch.empty((E, H, I), dtype=torch.uint8, device=dev)
+        self.w2_scale = torch.empty(E * H, dtype=torch.float32, device=dev)
+        quantize_rows_fp8(w13.view(E * 2 * I, H), self.w13q, self.w13_scale, stream)
+        quantize_rows_fp8(w2.view(E * H, I), self.w2q, self.w2_scale, stream)
+
+
+def alloc_fp8_buffers(cfg: Config, device):
+    """xq [N,H] u8, x_scale [N] f32, hq [S,I] u8 and h_scale [S] f32 for ffn_forward_fp8."""
+    import torch
+    N, S = max(cfg.n_tokens, 1), max(max_slots(cfg), 1)
+    return (torch.empty((N, cfg.hidden), dtype=torch.uint8, device=device),
+            torch.empty(N, dtype=torch.float32, device=device),
+            torch.empty((S, cfg.inter), dtype=torch.uint8, device=device),
+            torch.empty(S, dtype=torch.float32, device=device))
+
+
+def ffn_forward_fp8(cfg: Config, routes: Routes, x, wq: Fp8Weights, xq, x_scale, h, hq, h_scale, o,
+                    stream=None) -> None:
+    """Quantise x, FC1 on FP8, quantise h, FC2 on FP8 (one C call, four launches)."""
+    _check("moe_ffn_forward_fp8",
+           lib().moe_ffn_forward_fp8(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(x),
+                                     _ptr(wq.w13q), _ptr(wq.w13_scale), _ptr(wq.w2q),
+                                     _ptr(wq.w2_scale), _ptr(xq), _ptr(x_scale), _ptr(h), _ptr(hq),
+                                     _ptr(h_scale), _ptr(o), _stream(stream)))
 
 
 def forward(cfg: Config, x, w_router, bias, w13, w2, routes: Routes, workspace, h, o, y,

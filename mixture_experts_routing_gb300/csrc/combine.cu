@@ -5,6 +5,8 @@
 // routes through the token_routes inverse map and reduces them in registers,
 // instead of expert outputs being scattered with atomics. One CTA per token
 // row; 16-byte vector loads and stores; fp32 accumulation in k order.
+#include <cuda_fp8.h>
+
 #include "moe_internal.h"
 
 namespace moe {
@@ -120,6 +122,53 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bwd_kernel(
   }
 }
 
+// Row-wise FP8 (E4M3) quantisation of a bf16 matrix, one warp per row:
+// scale = max|v| / 448 (1 for an all-zero row, so it encodes to zeros), then
+// q = E4M3(v / scale) rounded to nearest even with saturation at +-448 (the
+// division in fp32). The max is exact in any order, so codes and scales are
+// reproducible.
+constexpr int kQuantWarps = 8;
+
+__global__ void __launch_bounds__(kQuantWarps * 32) quantize_rows_fp8_kernel(
+    const uint16_t* __restrict__ m, int64_t rows, const int32_t* __restrict__ rows_dev, int cols,
+    uint8_t* __restrict__ q, float* __restrict__ scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kQuantWarps + warp;
+  if (rows_dev && r >= (int64_t)*rows_dev) return;  // rows past the live extent
+  if (r >= rows) return;
+  const uint16_t* row = m + (size_t)r * cols;
+  const int nv = cols / 8;  // 16-byte groups of 8 values (cols is a multiple of 8)
+  float amax = 0.0f;
+  for (int v = lane; v < nv; v += 32) {
+    const uint4 w = reinterpret_cast<const uint4*>(row)[v];
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(a[i] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(a[i] & 0xFFFF0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  if (lane == 0) scale[r] = s;
+  uint8_t* qr = q + (size_t)r * cols;
+  for (int v = lane; v < nv; v += 32) {
+    const uint4 w = reinterpret_cast<const uint4*>(row)[v];
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __fdiv_rn(__uint_as_float(a[i] << 16), s);
+      const float hi = __fdiv_rn(__uint_as_float(a[i] & 0xFFFF0000u), s);
+      const uint32_t c0 = __nv_cvt_float_to_fp8(lo, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t c1 = __nv_cvt_float_to_fp8(hi, __NV_SATFINITE, __NV_E4M3);
+      packed[i >> 1] |= (c0 | (c1 << 8)) << ((i & 1) * 16);
+    }
+    reinterpret_cast<uint2*>(qr)[v] = make_uint2(packed[0], packed[1]);
+  }
+}
+
 __global__ void transpose_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int R,
                                  int C, int64_t in_es, int64_t out_es, int64_t out_off) {
   __shared__ uint16_t tile[32][33];
@@ -170,6 +219,16 @@ int launch_combine_bwd(const uint16_t* dxr, const float* part, int n_part,
   else
     MOE_COMBINE_BWD(16);
 #undef MOE_COMBINE_BWD
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? 1 : -(int)err;
+}
+
+int launch_quantize_rows_fp8(const uint16_t* m, int64_t rows, const int32_t* rows_dev, int cols,
+                             uint8_t* q, float* scale, cudaStream_t s) {
+  if (rows <= 0) return 0;
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  quantize_rows_fp8_kernel<<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(m, rows, rows_dev, cols,
+                                                                         q, scale);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }

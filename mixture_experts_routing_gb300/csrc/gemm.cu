@@ -65,6 +65,8 @@ constexpr int kStageRowElems = 32;   // epilogue staging row: 32 features (bf16)
 constexpr uint32_t kEpiStageBytes = kEpiWarps * 16u * kStageRowElems * 2u;  // per warp 16 rows
 constexpr int kTileQ = 4;            // depth of the tile-id queue
 constexpr uint32_t kPsBytes = kEpiWarps * 16 * 4;  // FC2 dgrad: 16 p' values per epilogue warp
+constexpr uint32_t kXsBytes = kEpiWarps * 128 * 4;  // FC1 FP8: the token scales of a warp's
+                                                    // (up to 8) chunks of 16 slots
 
 struct GemmParams {
   int n_acc;             // accumulators per tile: FC1 gate + up; otherwise two 128-feature
@@ -102,6 +104,9 @@ struct GemmParams {
                               // prob_in_act, FC2 dgrad)
   int activation;             // 0 SwiGLU, 1 GeGLU
   int prob_in_act;            // FC1: h = act(g) u p'
+  const float* w_scale;       // FP8: scale of each A (weight) row: FC1 [E*2I], FC2 [E*H]
+  const float* x_scale;       // FP8: scale of each B row: FC1 token [N], FC2 slot [S]
+  uint32_t xs_off;            // FP8: offset of the epilogue warps' B-row scale slices
   float* part;                // FC2 dgrad: dprob partials [S, I/32]
   int inter;                  // I
   uint32_t* err;
@@ -312,7 +317,9 @@ template <int kMode, int kAct>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA2, const GemmParams p) {
-  constexpr bool kGatherB = kMode == kModeFc1 || kMode == kModeDgrad2;
+  constexpr bool kGatherB = kMode == kModeFc1 || kMode == kModeDgrad2 || kMode == kModeFc1Fp8;
+  constexpr bool kFc1 = kMode == kModeFc1 || kMode == kModeFc1Fp8;
+  constexpr bool kFp8 = kMode == kModeFc1Fp8 || kMode == kModeFc2Fp8;
   constexpr bool kAMn = kMode == kModeDgrad2 || kMode == kModeDgrad1;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -462,7 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       tc_fence_after();
       const uint32_t dacc = tmem + ab * p.buf_stride;
-      const uint32_t idesc = idesc_bf16_f32(kTileM, T.n_eff) | (kAMn ? kIdescAMnMajor : 0u);
+      const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kTileM, T.n_eff)
+                                  : (idesc_bf16_f32(kTileM, T.n_eff) | (kAMn ? kIdescAMnMajor : 0u));
       // one UMMA k-step (16 elements) advances 32 bytes along a K-major row,
       // or 16 rows of 128 bytes in an MN-major tile
       constexpr uint32_t a_kstep = kAMn ? 2048u : 32u;
@@ -484,11 +492,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc = (kt | kk) != 0;
             const uint64_t bdesc = sdesc_sw128(st + p.b_off + (uint32_t)kk * 32u);
             const uint32_t a0 = st + (uint32_t)kk * a_kstep;
-            umma_bf16(dacc, kAMn ? sdesc_sw128_mn(a0) : sdesc_sw128(a0), bdesc, idesc, acc);
-            if (T.nacc == 2) {
-              const uint32_t a1 = a0 + kATileBytes;
-              umma_bf16(dacc + p.acc_off, kAMn ? sdesc_sw128_mn(a1) : sdesc_sw128(a1), bdesc,
-                        idesc, acc);
+            if constexpr (kFp8) {  // 32 E4M3 values = the same 32 bytes per k-step
+              umma_fp8(dacc, sdesc_sw128(a0), bdesc, idesc, acc);
+              if (T.nacc == 2) umma_fp8(dacc + p.acc_off, sdesc_sw128(a0 + kATileBytes), bdesc, idesc, acc);
+            } else {
+              umma_bf16(dacc, kAMn ? sdesc_sw128_mn(a0) : sdesc_sw128(a0), bdesc, idesc, acc);
+              if (T.nacc == 2) {
+                const uint32_t a1 = a0 + kATileBytes;
+                umma_bf16(dacc + p.acc_off, kAMn ? sdesc_sw128_mn(a1) : sdesc_sw128(a1), bdesc,
+                          idesc, acc);
+              }
             }
           }
           umma_commit(smem_u32(&empty_bar[s]));
@@ -520,6 +533,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nch = (T.n_eff - half * 16 + 31) / 32;  // this warp's 16-slot chunks
       uint32_t gu_next[16];
       float p_next = 0.0f;
+      float wsg = 1.0f, wsu = 1.0f;
+      if constexpr (kFp8) {
+        // before the accumulator is ready: this lane's row scale of each
+        // accumulator (FC1: gate and up rows; FC2: the two 128-row halves of
+        // the feature tile), and the B-row scale of every slot of the warp's
+        // chunks (slot c0 + j of chunk m at xs_w[16m + j]) into the warp's
+        // own slice; the previous tile's readers of the slice passed the
+        // warp barrier that ends each chunk's stores
+        if constexpr (kMode == kModeFc1Fp8) {
+          const int rg = T.e * 2 * p.inter + feat0 + lane;
+          wsg = p.w_scale[rg];
+          wsu = p.w_scale[rg + p.inter];
+        } else {
+          const int rg = T.e * p.m_total + feat0 + lane;
+          wsg = p.w_scale[rg];
+          if (T.nacc == 2) wsu = p.w_scale[rg + kTileM];
+        }
+        float* xs_w = reinterpret_cast<float*>(smem_raw + (sbase - smem_u32(smem_raw)) + p.xs_off) +
+                      (warp - 2) * 128;
+        for (int i = lane; i < 16 * nch; i += 32) {
+          const int c = half * 16 + 32 * (i >> 4) + (i & 15);
+          float v = 0.0f;
+          if (c < T.rows) {
+            if constexpr (kMode == kModeFc1Fp8) {
+              const int tok = p.sorted_slot_ids[T.slot0 + c];
+              if ((unsigned)tok < (unsigned)p.act_rows) v = p.x_scale[tok];
+            } else {
+              v = p.x_scale[T.slot0 + c];
+            }
+          }
+          xs_w[i] = v;
+        }
+        __syncwarp();
+      }
       if (kMode == kModeDgrad2 && nch > 0) {
         // before the accumulator is ready: the first chunk's pre-activations
         // and p' (lane j < 16 holds slot j's) into registers
@@ -562,15 +609,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (T.nacc == 2) tmem_ld16(ta + p.acc_off + (uint32_t)c0, v1);
           tmem_ld_wait();
           const size_t row0 = (size_t)(T.slot0 + c0);  // slot of register 0
-          if constexpr (kMode == kModeFc1) {
+          if constexpr (kFc1) {
             // p' of the chunk's slots (lane j < 16 holds slot j's) when the
             // routing probability multiplies the activation
             const float pl = p.prob_in_act ? load_slot_prob(p, T, c0, lane) : 1.0f;
+            const float* xs_c =
+                reinterpret_cast<const float*>(smem_raw + (sbase - smem_u32(smem_raw)) + p.xs_off) +
+                (warp - 2) * 128 + 16 * ((c0 - half * 16) >> 5);
             float hv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float g = __uint_as_float(v0[i]);
-              hv[i] = act_fwd<kAct>(g) * __uint_as_float(v1[i]);
+              float g = __uint_as_float(v0[i]), u = __uint_as_float(v1[i]);
+              if constexpr (kFp8) {  // dequantise: row scale x token scale
+                g *= wsg * xs_c[i];
+                u *= wsu * xs_c[i];
+              }
+              hv[i] = act_fwd<kAct>(g) * u;
               if (p.prob_in_act) hv[i] *= __shfl_sync(0xFFFFFFFFu, pl, i);
             }
             store_rows16(stg_u, lane, hv, p.out + row0 * p.out_ld + feat0, p.out_ld);
@@ -586,10 +640,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               store_rows16(stg_u, lane, uv, p.out2 + row0 * ld2 + p.inter + feat0, ld2);
             }
           } else {
+            const float* xs_c =
+                reinterpret_cast<const float*>(smem_raw + (sbase - smem_u32(smem_raw)) + p.xs_off) +
+                (warp - 2) * 128 + 16 * ((c0 - half * 16) >> 5);
             for (int seg = 0; seg < T.nacc; ++seg) {
               float ov[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) ov[i] = __uint_as_float(seg == 0 ? v0[i] : v1[i]);
+              for (int i = 0; i < 16; ++i) {
+                ov[i] = __uint_as_float(seg == 0 ? v0[i] : v1[i]);
+                if constexpr (kFp8) ov[i] *= (seg == 0 ? wsg : wsu) * xs_c[i];
+              }
               store_rows16(stg_u, lane, ov, p.out + row0 * p.out_ld + feat0 + seg * kTileM,
                            p.out_ld);
             }
@@ -680,7 +740,10 @@ int device_sms(cudaError_t* err) {
     return 0;
   if ((*err = set_smem_attr<kModeFc1, 0>()) != cudaSuccess ||
       (*err = set_smem_attr<kModeFc1, 1>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeFc1Fp8, 0>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeFc1Fp8, 1>()) != cudaSuccess ||
       (*err = set_smem_attr<kModeFc2, 0>()) != cudaSuccess ||
+      (*err = set_smem_attr<kModeFc2Fp8, 0>()) != cudaSuccess ||
       (*err = set_smem_attr<kModeDgrad2, 0>()) != cudaSuccess ||
       (*err = set_smem_attr<kModeDgrad2, 1>()) != cudaSuccess ||
       (*err = set_smem_attr<kModeDgrad1, 0>()) != cudaSuccess) {
@@ -696,7 +759,7 @@ int device_sms(cudaError_t* err) {
 int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.max_rows <= 0 || a.N <= 0) return 0;
   GemmParams p{};
-  const bool gather_b = a.mode == kModeFc1 || a.mode == kModeDgrad2;
+  const bool gather_b = a.mode == kModeFc1 || a.mode == kModeDgrad2 || a.mode == kModeFc1Fp8;
   p.bm = a.bm;
   p.sorted_slot_ids = a.sorted_slot_ids;
   p.kept_counts = a.kept_counts;
@@ -706,6 +769,8 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   p.aux = static_cast<const uint16_t*>(a.aux);
   p.slot_prob = a.slot_prob;
   p.activation = a.activation;
+  p.w_scale = a.w_scale;
+  p.x_scale = a.x_scale;
   p.prob_in_act = a.prob_in_act;
   p.part = a.part;
   p.inter = a.I;
@@ -732,6 +797,23 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       tmB = tmA;  // unused: B rows are gathered with cp.async
       tmA2 = tmA;
       break;
+    case kModeFc1Fp8:  // A = quantised w13 rows [E*2I, H] bytes; B gathered from quantised x
+      // bytes addressed as pairs: a 64-element (16-bit) box row is 128 E4M3
+      // values, the same 128-byte swizzled rows as bf16
+      p.n_acc = 2;
+      p.pair_feats = 0;
+      p.m_total = a.I;
+      p.k_tiles = a.H / (2 * kBK);
+      p.a_rows_per_expert = 2 * a.I;
+      p.a_second_off = a.I;
+      p.f_rows = kTileM;
+      p.f_tiles = a.I / kTileM;
+      p.out_ld = a.I;
+      p.act_ld = a.H / 2;
+      if (!make_map(&tmA, a.w, (uint64_t)(a.H / 2), E * 2 * a.I, kBK, kTileM)) return -1;
+      tmB = tmA;
+      tmA2 = tmA;
+      break;
     case kModeFc2:  // A = w2 rows [E*H, I], two 128-row feature tiles; B = h [S, I]
       p.n_acc = 2;
       p.pair_feats = 1;
@@ -745,6 +827,21 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       p.act_ld = a.I;
       if (!make_map(&tmA, a.w, (uint64_t)a.I, E * a.H, kBK, kTileM)) return -1;
       if (!make_map(&tmB, a.act, (uint64_t)a.I, (uint64_t)S, kBK, 16)) return -1;
+      tmA2 = tmA;
+      break;
+    case kModeFc2Fp8:  // FC2 on E4M3 bytes: w2q rows [E*H, I], hq [S, I], addressed as pairs
+      p.n_acc = 2;
+      p.pair_feats = 1;
+      p.m_total = a.H;
+      p.k_tiles = a.I / (2 * kBK);
+      p.a_rows_per_expert = a.H;
+      p.a_second_off = kTileM;
+      p.f_rows = 2 * kTileM;
+      p.f_tiles = (a.H + 2 * kTileM - 1) / (2 * kTileM);
+      p.out_ld = a.H;
+      p.act_ld = a.I / 2;
+      if (!make_map(&tmA, a.w, (uint64_t)(a.I / 2), E * a.H, kBK, kTileM)) return -1;
+      if (!make_map(&tmB, a.act, (uint64_t)(a.I / 2), (uint64_t)S, kBK, 16)) return -1;
       tmA2 = tmA;
       break;
     case kModeDgrad2:  // A[i, h] = w2[e][h][i] (MN-major, K = H); B gathered from dY [N, H]
@@ -788,15 +885,18 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       (int64_t)p.f_tiles * ((a.max_total + p.max_tn - 1) / p.max_tn + a.E);
   p.b_off = (uint32_t)p.n_acc * kATileBytes;
   p.stage_bytes = p.b_off + (((uint32_t)tile_cap * 128u + 1023u) & ~1023u);
-  p.stages = (int)((kSmemBudget - 1024u - kEpiStageBytes - kPsBytes) / p.stage_bytes);
+  // the FP8 modes' epilogue keeps its B-row scales in shared memory
+  const uint32_t xs_bytes = (a.mode == kModeFc1Fp8 || a.mode == kModeFc2Fp8) ? kXsBytes : 0u;
+  p.stages = (int)((kSmemBudget - 1024u - kEpiStageBytes - kPsBytes - xs_bytes) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2) return -1;
   p.epi_off = (uint32_t)p.stages * p.stage_bytes;
   p.ps_off = p.epi_off + kEpiStageBytes;
+  p.xs_off = p.ps_off + kPsBytes;
   p.acc_off = (uint32_t)p.max_tn;
   p.buf_stride = (uint32_t)(p.n_acc * p.max_tn);
   p.n_buf = 2 * p.buf_stride <= kTmemCols ? 2 : 1;
-  const size_t dyn = (size_t)p.ps_off + kPsBytes + 1024;
+  const size_t dyn = (size_t)p.xs_off + xs_bytes + 1024;
   cudaError_t err = cudaSuccess;
   const int sms = device_sms(&err);
   if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
@@ -810,7 +910,16 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       else
         moe_gemm_kernel<kModeFc1, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
       break;
+    case kModeFc1Fp8:
+      if (gelu)
+        moe_gemm_kernel<kModeFc1Fp8, 1><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+      else
+        moe_gemm_kernel<kModeFc1Fp8, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+      break;
     case kModeFc2: moe_gemm_kernel<kModeFc2, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p); break;
+    case kModeFc2Fp8:
+      moe_gemm_kernel<kModeFc2Fp8, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+      break;
     case kModeDgrad2:
       if (gelu)
         moe_gemm_kernel<kModeDgrad2, 1><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);

@@ -261,11 +261,17 @@ static bool gemm_routes_ok(const moe_routes_t* routes) {
          routes->gemm_sched && routes->slot_prob;
 }
 
-static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* act,
-                      const void* w, void* out, void* preact, int fc1, cudaStream_t stream) {
+// One forward expert GEMM: mode kModeFc1/kModeFc2, or their FP8 forms with
+// the weight-row and activation-row scales.
+static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, int mode,
+                      const void* act, const void* w, void* out, void* preact,
+                      const float* w_scale, const float* x_scale, cudaStream_t stream) {
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
   if (!gemm_routes_ok(routes)) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = mode == moe::kModeFc1Fp8 || mode == moe::kModeFc2Fp8;
+  const bool fc1 = mode == moe::kModeFc1 || mode == moe::kModeFc1Fp8;
+  if (fp8 && (!w_scale || !x_scale)) return MOE_ERR_INVALID_ARG;
   if (cfg->n_tokens == 0) return MOE_OK;
   if (!act || !w || !out || !aligned16(act) || !aligned16(w) || !aligned16(out) ||
       !aligned16(preact))
@@ -274,7 +280,7 @@ static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, const
   if (!err) return MOE_ERR_CUDA;
   moe::GemmArgs a{};
   gemm_base(cfg, routes, err, a);
-  a.mode = fc1 ? moe::kModeFc1 : moe::kModeFc2;
+  a.mode = mode;
   a.act = act;
   a.w = w;
   a.out = out;
@@ -282,6 +288,8 @@ static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, const
   a.activation = cfg->activation;
   a.prob_in_act = fc1 ? cfg->prob_in_act : 0;
   a.slot_prob = routes->slot_prob;
+  a.w_scale = w_scale;
+  a.x_scale = x_scale;
   a.act_rows = fc1 ? cfg->n_tokens : a.s_max;
   a.sched = routes->gemm_sched + (fc1 ? 0 : 2);
   return finish(moe::launch_gemm(a, stream));
@@ -289,12 +297,62 @@ static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, const
 
 int moe_fc1_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
                     const void* w13, void* h, cudaStream_t stream) {
-  return fc_forward(cfg, routes, x, w13, h, nullptr, 1, stream);
+  return fc_forward(cfg, routes, moe::kModeFc1, x, w13, h, nullptr, nullptr, nullptr, stream);
 }
 
 int moe_fc2_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* h,
                     const void* w2, void* o, cudaStream_t stream) {
-  return fc_forward(cfg, routes, h, w2, o, nullptr, 0, stream);
+  return fc_forward(cfg, routes, moe::kModeFc2, h, w2, o, nullptr, nullptr, nullptr, stream);
+}
+
+int moe_quantize_rows_fp8(const void* m, int64_t rows, const int32_t* rows_dev, int cols, void* q,
+                          float* scale, cudaStream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 8 != 0 || rows > ((int64_t)1 << 34))
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!m || !q || !scale || !aligned16(m) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return finish(moe::launch_quantize_rows_fp8(static_cast<const uint16_t*>(m), rows, rows_dev, cols,
+                                              static_cast<uint8_t*>(q), scale, stream));
+}
+
+int moe_fc1_forward_fp8(const moe_config_t* cfg, const moe_routes_t* routes, const void* xq,
+                        const float* x_scale, const void* w13q, const float* w13_scale, void* h,
+                        cudaStream_t stream) {
+  return fc_forward(cfg, routes, moe::kModeFc1Fp8, xq, w13q, h, nullptr, w13_scale, x_scale,
+                    stream);
+}
+
+int moe_fc2_forward_fp8(const moe_config_t* cfg, const moe_routes_t* routes, const void* hq,
+                        const float* h_scale, const void* w2q, const float* w2_scale, void* o,
+                        cudaStream_t stream) {
+  return fc_forward(cfg, routes, moe::kModeFc2Fp8, hq, w2q, o, nullptr, w2_scale, h_scale, stream);
+}
+
+int moe_ffn_forward_fp8(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                        const void* w13q, const float* w13_scale, const void* w2q,
+                        const float* w2_scale, void* xq, float* x_scale, void* h, void* hq,
+                        float* h_scale, void* o, cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!gemm_routes_ok(routes) || !routes->num_tokens_post_padded) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_tokens == 0) return MOE_OK;
+  if (!x || !xq || !x_scale || !h || !hq || !h_scale || !aligned16(x) || !aligned16(xq) ||
+      !aligned16(h) || !aligned16(hq))
+    return MOE_ERR_INVALID_ARG;
+  // x rows past a device-side live count are quantised too: FC1 gathers only
+  // live rows, so they are never read
+  rc = finish(moe::launch_quantize_rows_fp8(static_cast<const uint16_t*>(x), cfg->n_tokens, nullptr,
+                                            cfg->hidden, static_cast<uint8_t*>(xq), x_scale,
+                                            stream));
+  if (rc != MOE_OK) return rc;
+  rc = moe_fc1_forward_fp8(cfg, routes, xq, x_scale, w13q, w13_scale, h, stream);
+  if (rc != MOE_OK) return rc;
+  // only the slots below the padded extent hold routes
+  rc = finish(moe::launch_quantize_rows_fp8(static_cast<const uint16_t*>(h), slots_of(cfg),
+                                            routes->num_tokens_post_padded, cfg->inter,
+                                            static_cast<uint8_t*>(hq), h_scale, stream));
+  if (rc != MOE_OK) return rc;
+  return moe_fc2_forward_fp8(cfg, routes, hq, h_scale, w2q, w2_scale, o, stream);
 }
 
 int moe_ffn_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
@@ -308,7 +366,8 @@ int moe_ffn_forward_train(const moe_config_t* cfg, const moe_routes_t* routes, c
                           const void* w13, const void* w2, void* h, void* o, void* preact,
                           cudaStream_t stream) {
   if (cfg && cfg->n_tokens > 0 && !preact) return MOE_ERR_INVALID_ARG;
-  const int rc = fc_forward(cfg, routes, x, w13, h, preact, 1, stream);
+  const int rc =
+      fc_forward(cfg, routes, moe::kModeFc1, x, w13, h, preact, nullptr, nullptr, stream);
   if (rc != MOE_OK) return rc;
   return moe_fc2_forward(cfg, routes, h, w2, o, stream);
 }

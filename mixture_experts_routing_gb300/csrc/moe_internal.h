@@ -60,6 +60,10 @@ enum GemmMode {
   kModeDgrad2 = 2,  // dgrad of FC2: A = w2 read MN-major, B = rows of dY gathered by
                     // slot, SwiGLU-backward epilogue
   kModeDgrad1 = 3,  // dgrad of FC1: A = w13 read MN-major, B = dPre rows by slot (TMA)
+  kModeFc1Fp8 = 4,  // FC1 in FP8 (E4M3): A = quantised w13 rows, B = rows of quantised x
+                    // gathered by slot; epilogue applies the row and token scales
+  kModeFc2Fp8 = 5,  // FC2 in FP8: A = quantised w2 rows, B = quantised h rows (TMA);
+                    // epilogue applies the w2 row and h slot-row scales
 };
 
 struct GemmArgs {
@@ -76,6 +80,8 @@ struct GemmArgs {
   const float* slot_prob;     // FC1 (prob_in_act), dgrad2: p' of each slot's route (0 padding)
   int activation;             // FC1, dgrad2: 0 SwiGLU, 1 GeGLU
   int prob_in_act;            // FC1: multiply the activation by the slot's p'
+  const float* w_scale;       // FP8: scale of each weight row (FC1 [E*2I], FC2 [E*H])
+  const float* x_scale;       // FP8: scale of each B row (FC1: token [N]; FC2: slot [S])
   float* part;                // dgrad2: dprob partials [S, I/32]
   int64_t act_rows;      // rows of act (N when gathered, else S)
   const int32_t* sorted_slot_ids;
@@ -141,12 +147,18 @@ struct CombineArgs {
 
 int launch_combine(const CombineArgs& a, cudaStream_t s);
 
-// out[e*out_es + out_off + c*R + r] = in[e*in_es + r*C + c], bf16.
+// Row-wise E4M3 quantisation of a bf16 [rows, cols] matrix (cols a multiple
+// of 8, rows 16-byte aligned): codes q [rows, cols], scales [rows]. With
+// rows_dev, rows at or past *rows_dev (read on the device) are left as they are.
+int launch_quantize_rows_fp8(const uint16_t* m, int64_t rows, const int32_t* rows_dev, int cols,
+                             uint8_t* q, float* scale, cudaStream_t s);
+
 // The library's launch counter (moe_launch_count): read, and adjusted by the
 // graph ladder (captured launches are not executions; a replay is).
 uint64_t launch_counter();
 void add_launches(int64_t n);
 
+// out[e*out_es + out_off + c*R + r] = in[e*in_es + r*C + c], bf16.
 int launch_transpose(const uint16_t* in, uint16_t* out, int E, int R, int C, int64_t in_es,
                      int64_t out_es, int64_t out_off, cudaStream_t s);
 
