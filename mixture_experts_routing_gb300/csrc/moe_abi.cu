@@ -201,6 +201,8 @@ int moe_route_align(const moe_config_t* cfg, const void* x, const float* w_route
   if (!workspace || ws_bytes < w.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   moe::RouteArgs a{};
+  a.err = error_word_ptr();
+  if (!a.err) return MOE_ERR_CUDA;
   a.N = cfg->n_tokens;
   a.H = cfg->hidden;
   a.E = cfg->n_experts;
@@ -563,6 +565,8 @@ int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, con
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   moe::RouterBwdArgs a{};
+  a.err = error_word_ptr();
+  if (!a.err) return MOE_ERR_CUDA;
   a.N = cfg->n_tokens;
   a.H = cfg->hidden;
   a.E = cfg->n_experts;

@@ -29,6 +29,7 @@ struct Ladder {  // dropless padding rungs: multiples num[j]/den of the expected
 struct RouteArgs {
   int N, H, E, K, renorm, bm;   // N: the static token bound (buffers, grids)
   const int32_t* n_dev;         // live token count on the device, or null for N
+  uint32_t* err;                // device error word (bounded waits)
   int cap_num, cap_den;         // capacity factor (the capacity follows the live count)
   int dropless;          // 1: keep every route, extents from the ladder
   Ladder ladder;
@@ -115,6 +116,7 @@ int launch_wgrad(const WgradArgs& a, cudaStream_t s);
 // dx += dl . W_r^T (bf16 in/out).
 struct RouterBwdArgs {
   int N, H, E, K, renorm;
+  uint32_t* err;                // device error word (bounded waits)
   const uint16_t* x;
   const float* wr;
   const float* bias;

@@ -11,6 +11,7 @@ enum : uint32_t {
   kErrWaitFull = 1u << 0,     // MMA issuer: operand stage never arrived
   kErrWaitEmpty = 1u << 1,    // producer: stage never released
   kErrWaitAccum = 1u << 2,    // epilogue: accumulator never completed
+  kErrWaitRouter = 1u << 3,   // router logits: a stage of x / W_r never arrived
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -22,6 +22,8 @@
 #include <math.h>
 
 #include "moe_internal.h"
+#include "ptx.cuh"
+#include "tmap.h"
 
 namespace moe {
 namespace {
@@ -60,14 +62,21 @@ __device__ __forceinline__ int live_tokens(const int32_t* n_dev, int Nmax) {
 }
 
 // ---------------------------------------------------------------- R1
-// CTA tile BM tokens x BN experts, TM x TN outputs per thread (TN = 8 is two
-// groups of 4 columns, BN/2 apart, for conflict-free 16-byte shared loads),
-// BK = 32 contraction elements per stage, a 4-stage cp.async ring for x (bf16
-// rows, converted once per stage into a transposed fp32 tile) and W_r (fp32).
-// Each output is still one fma chain in ascending h. (Chosen by measurement
-// among 8 tile shapes: 64x128 with 4x8 per thread was fastest on both the
-// Qwen3-30B and DeepSeek-V3 router shapes.)
+// A SIMT SGEMM in which every output is one fp32 fma chain over ascending h.
+// Work split for the whole GPU: the [N, E] logit matrix is cut into one token
+// group per SM (bm = ceil(N / groups) tokens, any integer) by tiles of
+// BN = 4*TX experts, one CTA per block. A CTA has TY x TX threads with 7
+// tokens x 4 experts each (TY = ceil(bm/7) rounded up to 4; rows past bm
+// idle). A warp covers 4 thread rows x 8 thread columns, so each contraction
+// step reads 4 distinct token vectors and 8 distinct expert vectors from
+// shared memory: three conflict-free 16-byte loads per thread for 28 fmas.
+// Stages of BK = 32 contraction elements run in a 4-deep cp.async ring: x
+// rows (bf16, converted once per stage into a transposed fp32 tile whose
+// 7-token vectors are padded to 8) and W_r rows (fp32). (The earlier
+// power-of-two tiling, 64 tokens x 128 experts per CTA, gave the DeepSeek-V3
+// router shape 128 CTAs for 152 SMs and ran at 47 % of the fp32 FMA peak.)
 constexpr int LBK = 32, LSTAGES = 4;
+constexpr int kRTM = 7, kRTN = 4, kRPad = 8, kRMaxThreads = 512;
 
 __device__ __forceinline__ void cpa16(uint32_t dst, const void* src, uint32_t n) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
@@ -78,41 +87,99 @@ __device__ __forceinline__ void cpa4(uint32_t dst, const void* src, uint32_t n) 
                : "memory");
 }
 
-template <int BM, int BN, int TM, int TN>
-constexpr size_t router_smem_bytes() {
-  return (size_t)LSTAGES * BM * LBK * 2 + (size_t)LSTAGES * LBK * BN * 4 + (size_t)LBK * BM * 4;
+// Dynamic shared memory of one CTA: x stages, W_r stages, the fp32 x tile.
+constexpr size_t router_smem_bytes(int bm, int bn, int ty) {
+  return (size_t)LSTAGES * bm * LBK * 2 + (size_t)LSTAGES * LBK * bn * 4 +
+         (size_t)LBK * ty * kRPad * 4;
 }
 
-template <int BM, int BN, int TM, int TN>
-__global__ void __launch_bounds__((BM / TM) * (BN / TN)) router_logits_kernel(
+// Converts stage rows [0, rows) of bf16 x ([row][BK]) into the transposed
+// fp32 tile `as` ([BK][RM], token m at (m/7)*8 + m%7).
+__device__ __forceinline__ void router_convert(const uint16_t* xsl, float* as, int rows, int RM,
+                                               int tid, int NT) {
+  for (int c = tid; c < rows * (LBK / 8); c += NT) {
+    const int m = c % rows, q = c / rows;
+    const int pos = (m / kRTM) * kRPad + m % kRTM;
+    const uint4 v = *reinterpret_cast<const uint4*>(xsl + m * LBK + q * 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      as[(q * 8 + 2 * i) * RM + pos] = __uint_as_float(w[i] << 16);
+      as[(q * 8 + 2 * i + 1) * RM + pos] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+// One stage of the fma chains: acc[i][j] += x[token i][k] * W_r[k][expert j]
+// for k ascending over the stage.
+template <int BN>
+__device__ __forceinline__ void router_fma_stage(float (&acc)[kRTM][kRTN], const float* as,
+                                                 const float* bsl, int RM, int ty, int tx) {
+#pragma unroll
+  for (int kk = 0; kk < LBK; ++kk) {
+    const float4 a0 = *reinterpret_cast<const float4*>(&as[kk * RM + ty * kRPad]);
+    const float4 a1 = *reinterpret_cast<const float4*>(&as[kk * RM + ty * kRPad + 4]);
+    const float4 b = *reinterpret_cast<const float4*>(&bsl[kk * BN + tx * kRTN]);
+    const float av[kRTM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z};
+    const float bv[kRTN] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < kRTM; ++i)
+#pragma unroll
+      for (int j = 0; j < kRTN; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+  }
+}
+
+__device__ __forceinline__ void router_store(const float (&acc)[kRTM][kRTN], float* logits,
+                                             const float* bias, int m0, int rows, int n0, int E,
+                                             int ty, int tx) {
+#pragma unroll
+  for (int i = 0; i < kRTM; ++i) {
+    const int r = ty * kRTM + i;
+    if (r >= rows) continue;
+    float* out = logits + (size_t)(m0 + r) * E;
+#pragma unroll
+    for (int j = 0; j < kRTN; ++j) {
+      const int e = n0 + tx * kRTN + j;
+      if (e < E) out[e] = __fadd_rn(acc[i][j], bias ? bias[e] : 0.0f);
+    }
+  }
+}
+
+// cp.async form: any E (W_r rows read 16 or 4 bytes at a time).
+template <int TX>
+__global__ void __launch_bounds__(kRMaxThreads) router_logits_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
-    float* __restrict__ logits, int Nmax, const int32_t* __restrict__ n_dev, int H, int E,
+    float* __restrict__ logits, int Nmax, const int32_t* __restrict__ n_dev, int H, int E, int bm,
     int wr_vec4) {
-  constexpr int NT = (BM / TM) * (BN / TN);
+  constexpr int BN = TX * kRTN;
+  const int NT = blockDim.x, RM = (NT / TX) * kRPad;
   const int N = live_tokens(n_dev, Nmax);
-  if ((int)blockIdx.y * BM >= N) return;  // the whole tile is past the live tokens
+  const int m0 = blockIdx.y * bm;
+  if (m0 >= N) return;  // the whole group is past the live tokens
+  const int rows = min(bm, N - m0);
   extern __shared__ __align__(16) uint8_t rsm[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                    // [S][BM][BK] bf16
-  float* bs = reinterpret_cast<float*>(rsm + LSTAGES * BM * LBK * 2);  // [S][BK][BN]
-  float* as = bs + LSTAGES * LBK * BN;                                  // [BK][BM]
-  const int tid = threadIdx.x, tx = tid % (BN / TN), ty = tid / (BN / TN);
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-  float acc[TM][TN];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                             // [S][bm][BK] bf16
+  float* bs = reinterpret_cast<float*>(rsm + (size_t)LSTAGES * bm * LBK * 2);   // [S][BK][BN]
+  float* as = bs + LSTAGES * LBK * BN;                                          // [BK][RM]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tx = (warp % (TX / 8)) * 8 + (lane & 7);
+  const int ty = (warp / (TX / 8)) * 4 + (lane >> 3);
+  const int n0 = blockIdx.x * BN;
+  // the pad of each token vector and the rows past `rows` stay zero
+  for (int i = tid; i < LBK * RM; i += NT) as[i] = 0.0f;
+  float acc[kRTM][kRTN];
 #pragma unroll
-  for (int i = 0; i < TM; ++i)
+  for (int i = 0; i < kRTM; ++i)
 #pragma unroll
-    for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+    for (int j = 0; j < kRTN; ++j) acc[i][j] = 0.0f;
   const int KT = H / LBK;
-  auto col_of = [&](int j) { return (j / 4) * (BN / 2) * (TN / 8) + tx * 4 + (j % 4); };
   auto issue = [&](int kt) {
     if (kt < KT) {
       const int slot = kt % LSTAGES, k0 = kt * LBK;
-      for (int c = tid; c < BM * LBK / 8; c += NT) {
+      for (int c = tid; c < rows * (LBK / 8); c += NT) {
         const int row = c / (LBK / 8), q = c % (LBK / 8);
-        const int t = m0 + row;
-        const bool ok = t < N;
-        cpa16((uint32_t)__cvta_generic_to_shared(xs + (size_t)slot * BM * LBK + row * LBK + q * 8),
-              x + (size_t)(ok ? t : 0) * H + k0 + q * 8, ok ? 16u : 0u);
+        cpa16((uint32_t)__cvta_generic_to_shared(xs + ((size_t)slot * bm + row) * LBK + q * 8),
+              x + (size_t)(m0 + row) * H + k0 + q * 8, 16u);
       }
       float* bsl = bs + (size_t)slot * LBK * BN;
       if (wr_vec4) {
@@ -140,67 +207,192 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) router_logits_kernel(
     asm volatile("cp.async.wait_group %0;" ::"n"(LSTAGES - 2) : "memory");
     __syncthreads();  // stage kt landed; every thread is done with stage kt-1 and with `as`
     issue(kt + LSTAGES - 1);
-    const uint16_t* xsl = xs + (size_t)(kt % LSTAGES) * BM * LBK;
-    for (int c = tid; c < BM * LBK / 8; c += NT) {
-      const int m = c % BM, q = c / BM;
-      const uint4 v = *reinterpret_cast<const uint4*>(xsl + m * LBK + q * 8);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        as[(q * 8 + 2 * i) * BM + m] = __uint_as_float(w[i] << 16);
-        as[(q * 8 + 2 * i + 1) * BM + m] = __uint_as_float(w[i] & 0xFFFF0000u);
-      }
-    }
+    router_convert(xs + (size_t)(kt % LSTAGES) * bm * LBK, as, rows, RM, tid, NT);
     __syncthreads();
-    const float* bsl = bs + (size_t)(kt % LSTAGES) * LBK * BN;
-#pragma unroll
-    for (int kk = 0; kk < LBK; ++kk) {
-      float av[TM], bv[TN];
-#pragma unroll
-      for (int i = 0; i < TM; i += 4) {
-        const float4 q = *reinterpret_cast<const float4*>(&as[kk * BM + ty * TM + i]);
-        av[i] = q.x; av[i + 1] = q.y; av[i + 2] = q.z; av[i + 3] = q.w;
-      }
-#pragma unroll
-      for (int j = 0; j < TN; j += 4) {
-        const float4 q = *reinterpret_cast<const float4*>(&bsl[kk * BN + col_of(j)]);
-        bv[j] = q.x; bv[j + 1] = q.y; bv[j + 2] = q.z; bv[j + 3] = q.w;
-      }
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
-    }
+    router_fma_stage<BN>(acc, as, bs + (size_t)(kt % LSTAGES) * LBK * BN, RM, ty, tx);
   }
-#pragma unroll
-  for (int i = 0; i < TM; ++i) {
-    const int t = m0 + ty * TM + i;
-    if (t >= N) continue;
-#pragma unroll
-    for (int j = 0; j < TN; ++j) {
-      const int e = n0 + col_of(j);
-      if (e < E) logits[(size_t)t * E + e] = __fadd_rn(acc[i][j], bias ? bias[e] : 0.0f);
-    }
-  }
+  router_store(acc, logits, bias, m0, rows, n0, E, ty, tx);
 }
 
-template <int BM, int BN, int TM, int TN>
-cudaError_t launch_router_logits(const RouteArgs& a, int vec4, cudaStream_t s) {
-  constexpr size_t smem = router_smem_bytes<BM, BN, TM, TN>();
+// Shared-memory layout of the TMA form: LSTAGES stages of [x tile bm x BK
+// bf16, padded to 128 B | W_r tile BK x BN fp32], two fp32 x tiles, the stage
+// barriers.
+struct RouterTmaLayout {
+  uint32_t xbytes, stage, as_off, bar_off, total;
+};
+__host__ __device__ inline RouterTmaLayout router_tma_layout(int bm, int bn, int ty) {
+  RouterTmaLayout L;
+  L.xbytes = ((uint32_t)bm * LBK * 2 + 127u) & ~127u;
+  L.stage = L.xbytes + (uint32_t)LBK * bn * 4;
+  L.as_off = LSTAGES * L.stage;
+  L.bar_off = L.as_off + 2u * LBK * ty * kRPad * 4;
+  L.total = L.bar_off + LSTAGES * 8 + 128;  // + slack for aligning the base to 128 B
+  return L;
+}
+
+// TMA form (E a multiple of 4, E >= BN): one thread loads each stage with two
+// 2-D tensor copies (x box BK x bm, W_r box BN x BK; rows and experts past
+// the tensor read as zero) completing on the stage's mbarrier. The fp32 x
+// tile is double-buffered, so one CTA barrier per stage orders everything:
+// after it, the tile converted in the previous iteration is visible, and
+// every thread is done with the stage slot the producer refills and with the
+// x tile the next conversion overwrites. Waits are bounded; a CTA that runs
+// out of time records kErrWaitRouter, waits (bounded) for its copies in
+// flight and leaves without writing logits.
+template <int TX>
+__global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
+    const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+    const float* __restrict__ bias, float* __restrict__ logits, int Nmax,
+    const int32_t* __restrict__ n_dev, int H, int E, int bm, uint32_t* __restrict__ err) {
+  constexpr int BN = TX * kRTN;
+  const int NT = blockDim.x, TY = NT / TX, RM = TY * kRPad;
+  const int N = live_tokens(n_dev, Nmax);
+  const int m0 = blockIdx.y * bm;
+  if (m0 >= N) return;
+  const int rows = min(bm, N - m0);
+  const RouterTmaLayout L = router_tma_layout(bm, BN, TY);
+  extern __shared__ __align__(16) uint8_t rsm_raw[];
+  uint8_t* rsm = rsm_raw + ((128u - (smem_u32(rsm_raw) & 127u)) & 127u);
+  const uint32_t sbase = smem_u32(rsm);
+  float* as = reinterpret_cast<float*>(rsm + L.as_off);  // [2][BK][RM]
+  const uint32_t bar0 = sbase + L.bar_off;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tx = (warp % (TX / 8)) * 8 + (lane & 7);
+  const int ty = (warp / (TX / 8)) * 4 + (lane >> 3);
+  const int n0 = blockIdx.x * BN;
+  const int KT = H / LBK;
+  const uint32_t tx_bytes = (uint32_t)bm * LBK * 2 + (uint32_t)LBK * BN * 4;
+  for (int i = tid; i < 2 * LBK * RM; i += NT) as[i] = 0.0f;
+  if (tid == 0) {
+    tma_prefetch_desc(&tmx);
+    tma_prefetch_desc(&tmw);
+    for (int st = 0; st < LSTAGES; ++st) mbar_init(bar0 + 8u * st, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  uint64_t pol_x = 0, pol_w = 0;
+  int issued = 0;
+  auto issue = [&](int kt) {  // thread 0 only
+    const int slot = kt % LSTAGES;
+    const uint32_t st = sbase + (uint32_t)slot * L.stage, bar = bar0 + 8u * slot;
+    mbar_arrive_expect_tx(bar, tx_bytes);
+    tma_load_2d(st, &tmx, kt * LBK, m0, bar, pol_x);
+    tma_load_2d(st + L.xbytes, &tmw, n0, kt * LBK, bar, pol_w);
+    ++issued;
+  };
+  if (tid == 0) {
+    pol_x = policy_evict_first();
+    pol_w = policy_evict_last();
+    for (int kt = 0; kt < LSTAGES - 1 && kt < KT; ++kt) issue(kt);
+  }
+  float acc[kRTM][kRTN];
+#pragma unroll
+  for (int i = 0; i < kRTM; ++i)
+#pragma unroll
+    for (int j = 0; j < kRTN; ++j) acc[i][j] = 0.0f;
+  int waited = 0;  // stages this thread saw arrive
+  bool ok = mbar_wait(bar0, 0u, err, kErrWaitRouter);
+  if (ok) {
+    ++waited;
+    router_convert(reinterpret_cast<const uint16_t*>(rsm), as, rows, RM, tid, NT);
+  }
+  for (int kt = 0; kt < KT; ++kt) {
+    if (!__syncthreads_and(ok)) break;
+    if (tid == 0 && kt + LSTAGES - 1 < KT) issue(kt + LSTAGES - 1);
+    const int slot = kt % LSTAGES;
+    router_fma_stage<BN>(acc, as + (kt & 1) * LBK * RM,
+                         reinterpret_cast<const float*>(rsm + (size_t)slot * L.stage + L.xbytes),
+                         RM, ty, tx);
+    if (kt + 1 < KT) {
+      const int ns = (kt + 1) % LSTAGES;
+      ok = mbar_wait(bar0 + 8u * ns, (uint32_t)((kt + 1) / LSTAGES) & 1u, err, kErrWaitRouter);
+      if (ok) {
+        ++waited;
+        router_convert(reinterpret_cast<const uint16_t*>(rsm + (size_t)ns * L.stage),
+                       as + ((kt + 1) & 1) * LBK * RM, rows, RM, tid, NT);
+      }
+    }
+  }
+  if (!__syncthreads_and(ok)) {
+    // out of time: let this CTA's copies in flight land before leaving
+    if (tid == 0)
+      for (int st = waited; st < issued; ++st)
+        if (!mbar_wait(bar0 + 8u * (st % LSTAGES), (uint32_t)(st / LSTAGES) & 1u, err,
+                       kErrWaitRouter))
+          break;
+    return;
+  }
+  router_store(acc, logits, bias, m0, rows, n0, E, ty, tx);
+}
+
+int router_sm_count(cudaError_t* err) {
+  static int sms[64] = {};
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && sms[dev] > 0) return sms[dev];
+  int n = 0;
+  if ((*err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return 0;
+  if (dev >= 0 && dev < 64) sms[dev] = n;
+  return n;
+}
+
+template <int TX>
+cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaStream_t s) {
+  constexpr int BN = TX * kRTN;
+  constexpr int kTyMax = (kRMaxThreads / TX < 32 ? kRMaxThreads / TX : 32) / 4 * 4;
+  const int gx = (a.E + BN - 1) / BN;
+  const int groups = sms / gx > 0 ? sms / gx : 1;
+  int bm = (a.N + groups - 1) / groups;
+  int ty = ((bm + kRTM - 1) / kRTM + 3) / 4 * 4;
+  if (ty > kTyMax) {  // more tokens than one CTA per SM can hold: several waves
+    ty = kTyMax;
+    bm = ty * kRTM;
+  }
   static int set_for[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || !set_for[dev]) {
-    err = cudaFuncSetAttribute(router_logits_kernel<BM, BN, TM, TN>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    err = cudaFuncSetAttribute(router_logits_kernel<TX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)router_smem_bytes(kTyMax * kRTM, BN, kTyMax));
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(router_logits_tma_kernel<TX>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)router_tma_layout(kTyMax * kRTM, BN, kTyMax).total);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) set_for[dev] = 1;
   }
-  dim3 g((a.E + BN - 1) / BN, (a.N + BM - 1) / BM);
-  router_logits_kernel<BM, BN, TM, TN><<<g, (BM / TM) * (BN / TN), smem, s>>>(
-      a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, vec4);
+  dim3 g(gx, (a.N + bm - 1) / bm);
+  // TMA form: W_r rows a multiple of 16 bytes, boxes inside the tensors
+  const bool tma = vec4 && a.E >= BN && a.err &&
+                   (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0;
+  CUtensorMap tmx, tmw;
+  if (tma &&
+      make_map_plain(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, (uint64_t)a.H, (uint64_t)a.N,
+                     LBK, (uint32_t)bm) &&
+      make_map_plain(&tmw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.wr, (uint64_t)a.E,
+                     (uint64_t)a.H, BN, LBK)) {
+    router_logits_tma_kernel<TX><<<g, ty * TX, router_tma_layout(bm, BN, ty).total, s>>>(
+        tmx, tmw, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, bm, a.err);
+  } else {
+    router_logits_kernel<TX><<<g, ty * TX, router_smem_bytes(bm, BN, ty), s>>>(
+        a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, bm, vec4);
+  }
   return cudaGetLastError();
+}
+
+// Expert tile width from E: the narrowest of 32, 64, 128, 256 experts that
+// holds E (several tiles of 256 above that).
+cudaError_t launch_router_logits(const RouteArgs& a, cudaStream_t s) {
+  const int vec4 = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 15u) == 0);
+  cudaError_t err = cudaSuccess;
+  const int sms = router_sm_count(&err);
+  if (sms <= 0) return err != cudaSuccess ? err : cudaErrorUnknown;
+  if (a.E <= 32) return launch_router_logits_tx<8>(a, vec4, sms, s);
+  if (a.E <= 64) return launch_router_logits_tx<16>(a, vec4, sms, s);
+  if (a.E <= 128) return launch_router_logits_tx<32>(a, vec4, sms, s);
+  return launch_router_logits_tx<64>(a, vec4, sms, s);
 }
 
 // ---------------------------------------------------------------- R2
@@ -852,9 +1044,7 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   int launched = 0;
   const int C = (a.N + kTokensPerChunk - 1) / kTokensPerChunk;
   if (a.N > 0) {
-    const int vec4 = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 15u) == 0);
-    const cudaError_t e1 = (a.E > 64) ? launch_router_logits<64, 128, 4, 8>(a, vec4, s)
-                                      : launch_router_logits<64, 64, 4, 4>(a, vec4, s);
+    const cudaError_t e1 = launch_router_logits(a, s);
     if (e1 != cudaSuccess) return -(int)e1;
     ++launched;
     router_topk_kernel<<<C, kTopkWarps * 32, 0, s>>>(a.ws.logits, a.N, a.n_dev, a.E, a.K, a.renorm,
@@ -908,9 +1098,8 @@ int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
   r.wr = a.wr;
   r.bias = a.bias;
   r.ws.logits = a.dl;
-  const int vec4 = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 15u) == 0);
-  cudaError_t err = (a.E > 64) ? launch_router_logits<64, 128, 4, 8>(r, vec4, s)
-                               : launch_router_logits<64, 64, 4, 4>(r, vec4, s);
+  r.err = a.err;
+  cudaError_t err = launch_router_logits(r, s);
   if (err != cudaSuccess) return -(int)err;
   ++launched;
   router_dlogits_kernel<<<(a.N + kDlWarps - 1) / kDlWarps, kDlWarps * 32, 0, s>>>(
@@ -931,6 +1120,7 @@ int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
     ++launched;
   }
   dim3 g2((a.H + kRbTile - 1) / kRbTile, (a.N + kRbTile - 1) / kRbTile);
+  const int vec4 = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 15u) == 0);
   router_dx_kernel<<<g2, 256, 0, s>>>(a.dl, a.wr, a.N, a.H, a.E, vec4, a.dx);
   ++launched;
   err = cudaGetLastError();

@@ -250,6 +250,15 @@ WORKLOADS = {
     # each expert sees the same ~128 routes; 1.4 GB of weights (above L2)
     "dsv3_e16": Workload("dsv3_e16", 256, 7168, 16, 8, 2048, 5, 4, w_std=0.006,
                          note="DeepSeek-V3 shapes with 16 experts, N=256 (ncu profiling case)"),
+    # profiling case: the DeepSeek-V3 router shape (N=4096, H=7168, E=256,
+    # top-8) with I=128 experts, so the whole problem holds 1.4 GB on the device
+    "dsv3_route": Workload("dsv3_route", 4096, 7168, 256, 8, 128, 5, 4, w_std=0.006,
+                           note="DeepSeek-V3 router shape with I=128 experts (ncu profiling case)"),
+    # profiling case: the dropless per-expert shapes (H=4096, I=1408, ~1536
+    # routes per expert) with 16 experts and N=4096, about 3 GB on the device
+    "dropless_e16": Workload("dropless_e16", 4096, 4096, 16, 6, 1408, 0, 1, zipf_s=0.8,
+                             note="dropless per-expert shapes with 16 experts, N=4096 (ncu profiling case)",
+                             ladder=(2, 3, 4, 5, 6, 8), ladder_den=4),
     "dropless": Workload("dropless", 16384, 4096, 64, 6, 1408, 0, 1, zipf_s=0.8,
                          note="dropless bucketed layer: H=4096, E=64, top-6, I=1408, N swept 128..16384, Zipf(0.8)",
                          sweep=tuple(2 ** k for k in range(7, 15)),
