@@ -466,15 +466,18 @@ def run_ours(args):
     names = (("route", "quant_x", "fc1", "quant_h", "fc2", "combine") if fp8
              else ("route", "fc1", "fc2", "combine"))
 
-    def step(evs=None):
+    def step(evs=None, xb=None, yb=None):
+        xb = x if xb is None else xb
+        yb = y if yb is None else yb
+
         def mark(i):
             if evs is not None:
                 evs[i].record(stream)
         mark(0)
-        moe.route_align(cfg, x, wr, bias, routes, ws, stream)
+        moe.route_align(cfg, xb, wr, bias, routes, ws, stream)
         mark(1)
         if fp8:
-            moe.quantize_rows_fp8(x, xq, xs, stream)
+            moe.quantize_rows_fp8(xb, xq, xs, stream)
             mark(2)
             moe.fc1_forward_fp8(cfg, routes, xq, xs, wq.w13q, wq.w13_scale, h, stream)
             mark(3)
@@ -484,11 +487,11 @@ def run_ours(args):
             moe.fc2_forward_fp8(cfg, routes, hq, hs, wq.w2q, wq.w2_scale, o, stream)
             mark(5)
         else:
-            moe.fc1_forward(cfg, routes, x, w13, h, stream)
+            moe.fc1_forward(cfg, routes, xb, w13, h, stream)
             mark(2)
             moe.fc2_forward(cfg, routes, h, w2, o, stream)
             mark(3)
-        moe.combine(cfg, routes, o, y, stream)
+        moe.combine(cfg, routes, o, yb, stream)
         mark(len(names))
 
     for _ in range(max(args.warmup, 3)):
@@ -522,21 +525,45 @@ def run_ours(args):
     kept_counts = routes.kept_counts.cpu().numpy()
     used_slots = int(routes.num_tokens_post_padded.cpu()[0])
 
-    # ---- end to end: pinned host x in, host y out, every step
+    # ---- end to end: every step copies its x in from pinned host memory and
+    # its y out to pinned host memory. Two device buffers of each and a copy
+    # stream: step i+2's x copy and step i's y copy run under the compute of
+    # the steps between (the first two x copies and the last y copies are
+    # inside the timed region too).
     x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    y_host = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
-    for _ in range(2):
-        x.copy_(x_host, non_blocking=True)
-        step()
-        y_host.copy_(y[:N], non_blocking=True)
+    y_host = [torch.empty((N, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_dev, y_dev = [x, torch.empty_like(x)], [y, torch.empty_like(y)]
+    cstream = torch.cuda.Stream(dev)
+    h2d = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_run(steps, start_evt):
+        cstream.wait_event(start_evt)
+        with torch.cuda.stream(cstream):
+            for b in range(min(2, steps)):
+                x_dev[b].copy_(x_host, non_blocking=True)
+                h2d[b].record(cstream)
+        for i in range(steps):
+            b = i % 2
+            stream.wait_event(h2d[b])
+            step(xb=x_dev[b], yb=y_dev[b])
+            done[b].record(stream)
+            cstream.wait_event(done[b])
+            with torch.cuda.stream(cstream):
+                y_host[b].copy_(y_dev[b][:N], non_blocking=True)
+                if i + 2 < steps:
+                    x_dev[b].copy_(x_host, non_blocking=True)
+                h2d[b].record(cstream)
+        stream.wait_stream(cstream)
+
+    w0 = torch.cuda.Event()
+    w0.record(stream)
+    e2e_run(2, w0)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, dev)
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(args.steps):
-        x.copy_(x_host, non_blocking=True)
-        step()
-        y_host.copy_(y[:N], non_blocking=True)
+    e2e_run(args.steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(dist, dev)
@@ -564,7 +591,9 @@ def run_ours(args):
                          % (weight_bytes / 1e9)},
         "gpu_launches": launches,
         "e2e": {"value": N * world * args.steps / (ms_e2e / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": N * H * 2, "d2h_bytes_per_step": N * H * 2},
+                "h2d_bytes_per_step": N * H * 2, "d2h_bytes_per_step": N * H * 2,
+                "copies": "pinned host x in and y out every step, on a second stream with two "
+                          "device buffers each, overlapping the compute of neighbouring steps"},
         "roofline": roof,
         "grouped_gemm": {"ms": gemm_ms, "tflops_useful": gemm_flops / (gemm_ms / 1e3) / 1e12,
                          "pct_bf16_peak": gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
@@ -764,29 +793,53 @@ def run_ours_train(args):
                      "fwd_ms": per["route"] + per["ffn_forward"] + per["combine"],
                      "bwd_ms": per["ffn_backward"] + per["router_backward"]}
 
-    # ---- end to end: x and dY in from pinned host memory, y, dX and dprob out
+    # ---- end to end: every step copies x and dY in from pinned host memory
+    # and y, dX and dprob out to it. Two sets of these device buffers and a
+    # copy stream: a step's copies run under the compute of its neighbours
+    # (the first inputs and the last outputs are inside the timed region).
     xh = torch.from_numpy(st["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
     dyh = torch.from_numpy(st["dy_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    yh = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
-    dxh = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
-    dph = torch.empty((N, K), dtype=torch.float32).pin_memory()
+    yh = [torch.empty((N, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dxh = [torch.empty((N, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dph = [torch.empty((N, K), dtype=torch.float32).pin_memory() for _ in range(2)]
+    io = [st, dict(st, x=torch.empty_like(st["x"]), dy=torch.empty_like(st["dy"]),
+                   y=torch.empty_like(st["y"]), dx=torch.empty_like(st["dx"]),
+                   dprob=torch.empty_like(st["dprob"]))]
+    cstream = torch.cuda.Stream(dev)
+    h2d = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        st["x"].copy_(xh, non_blocking=True)
-        st["dy"].copy_(dyh, non_blocking=True)
-        step(st)
-        yh.copy_(st["y"][:N], non_blocking=True)
-        dxh.copy_(st["dx"], non_blocking=True)
-        dph.copy_(st["dprob"], non_blocking=True)
+    def e2e_run(steps, start_evt):
+        cstream.wait_event(start_evt)
+        with torch.cuda.stream(cstream):
+            for b in range(min(2, steps)):
+                io[b]["x"].copy_(xh, non_blocking=True)
+                io[b]["dy"].copy_(dyh, non_blocking=True)
+                h2d[b].record(cstream)
+        for i in range(steps):
+            b = i % 2
+            stream.wait_event(h2d[b])
+            step(io[b])
+            done[b].record(stream)
+            cstream.wait_event(done[b])
+            with torch.cuda.stream(cstream):
+                yh[b].copy_(io[b]["y"][:N], non_blocking=True)
+                dxh[b].copy_(io[b]["dx"], non_blocking=True)
+                dph[b].copy_(io[b]["dprob"], non_blocking=True)
+                if i + 2 < steps:
+                    io[b]["x"].copy_(xh, non_blocking=True)
+                    io[b]["dy"].copy_(dyh, non_blocking=True)
+                h2d[b].record(cstream)
+        stream.wait_stream(cstream)
 
-    for _ in range(2):
-        e2e_step()
+    w0 = torch.cuda.Event()
+    w0.record(stream)
+    e2e_run(2, w0)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, dev)
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(dist, dev)
@@ -812,7 +865,9 @@ def run_ours_train(args):
                                                    (dw13.numel() + dw2.numel()) * 4 / 1e9)},
         "gpu_launches": launches,
         "e2e": {"value": N * world / (ms_e2e / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2 + N * K * 4},
+                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2 + N * K * 4,
+                "copies": "pinned host x, dY in and y, dX, dprob out every step, on a second "
+                          "stream with two device buffer sets, overlapping neighbouring steps"},
         "roofline": roof,
         "tflops_fwd_bwd": 18.0 * R * H * I / (ms / 1e3) / 1e12,
         "pct_bf16_peak_fwd_bwd": 18.0 * R * H * I / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
