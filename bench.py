@@ -239,7 +239,7 @@ def roofline_for(name, model, ms, peaks, workload, fp8=False):
     if t_m >= t_c:
         ach = d["bytes"] / sec / 1e9
         r = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-             "peak_source": src}
+             "peak_source": src, "frac_of_spec_8000_gbs": ach / 8000.0}
     else:
         ach = d["flops"] / sec / 1e12
         r = {"bound": "alu" if name == "route" else "tensor", "achieved": ach, "peak": peak_c,
@@ -466,32 +466,33 @@ def run_ours(args):
     names = (("route", "quant_x", "fc1", "quant_h", "fc2", "combine") if fp8
              else ("route", "fc1", "fc2", "combine"))
 
-    def step(evs=None, xb=None, yb=None):
+    def step(evs=None, xb=None, yb=None, strm=None):
         xb = x if xb is None else xb
         yb = y if yb is None else yb
+        s = stream if strm is None else strm
 
         def mark(i):
             if evs is not None:
-                evs[i].record(stream)
+                evs[i].record(s)
         mark(0)
-        moe.route_align(cfg, xb, wr, bias, routes, ws, stream)
+        moe.route_align(cfg, xb, wr, bias, routes, ws, s)
         mark(1)
         if fp8:
-            moe.quantize_rows_fp8(xb, xq, xs, stream)
+            moe.quantize_rows_fp8(xb, xq, xs, s)
             mark(2)
-            moe.fc1_forward_fp8(cfg, routes, xq, xs, wq.w13q, wq.w13_scale, h, stream)
+            moe.fc1_forward_fp8(cfg, routes, xq, xs, wq.w13q, wq.w13_scale, h, s)
             mark(3)
             # only the slots below the padded extent hold routes
-            moe.quantize_rows_fp8(h, hq, hs, stream, rows_dev=routes.num_tokens_post_padded)
+            moe.quantize_rows_fp8(h, hq, hs, s, rows_dev=routes.num_tokens_post_padded)
             mark(4)
-            moe.fc2_forward_fp8(cfg, routes, hq, hs, wq.w2q, wq.w2_scale, o, stream)
+            moe.fc2_forward_fp8(cfg, routes, hq, hs, wq.w2q, wq.w2_scale, o, s)
             mark(5)
         else:
-            moe.fc1_forward(cfg, routes, xb, w13, h, stream)
+            moe.fc1_forward(cfg, routes, xb, w13, h, s)
             mark(2)
-            moe.fc2_forward(cfg, routes, h, w2, o, stream)
+            moe.fc2_forward(cfg, routes, h, w2, o, s)
             mark(3)
-        moe.combine(cfg, routes, o, yb, stream)
+        moe.combine(cfg, routes, o, yb, s)
         mark(len(names))
 
     for _ in range(max(args.warmup, 3)):
@@ -524,6 +525,32 @@ def run_ours(args):
         raise RuntimeError("device error word set during the timed region")
     kept_counts = routes.kept_counts.cpu().numpy()
     used_slots = int(routes.num_tokens_post_padded.cpu()[0])
+
+    # ---- the whole forward captured as one CUDA graph: 10 warm-up replays,
+    # then each replay timed on its own (median and minimum)
+    graph = torch.cuda.CUDAGraph()
+    gstream = torch.cuda.Stream(dev)
+    gstream.wait_stream(stream)
+    n0 = moe.launch_count()
+    with torch.cuda.graph(graph, stream=gstream):
+        step(strm=gstream)
+    graph_kernels = moe.launch_count() - n0  # launches recorded into the graph
+    stream.wait_stream(gstream)
+    for _ in range(10):
+        graph.replay()
+    reps = max(20, min(args.steps, 50))
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, b in gev:
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during the graph replays")
+    g_ms = sorted(a.elapsed_time(b) for a, b in gev)
+    g_med = statistics.median(g_ms)
 
     # ---- end to end: every step copies its x in from pinned host memory and
     # its y out to pinned host memory. Two device buffers of each and a copy
@@ -600,6 +627,9 @@ def run_ours(args):
                          "operands": "e4m3" if fp8 else "bf16",
                          "tflops_issued_capacity_shape": issued / (gemm_ms / 1e3) / 1e12,
                          "kept_routes": model["_kept"], "active_experts": model["_active"]},
+        "graph": {"replays": reps, "warmup_replays": 10, "kernels_per_replay": graph_kernels,
+                  "median_ms": g_med, "min_ms": g_ms[0],
+                  "tokens_per_s_median": N / (g_med / 1e3), "tokens_per_s_min_ms": N / (g_ms[0] / 1e3)},
         "kernels_ms": per_kernel,
         "kernels": {n: {k: v for k, v in kernels[n].items() if k in ("bound", "achieved", "unit", "frac")}
                     for n in names},
@@ -618,7 +648,18 @@ def run_ours(args):
             v, desc, secs, cores = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
                                                       args.cpu_experts)
         out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                               "sample": desc, "cpu_seconds": secs}
+                               "sample": desc, "cpu_seconds": secs, "host_cpus": os.cpu_count()}
+        if N * H <= 1024 * 512 and not fp8:  # the small layers: also on one thread
+            import oracle
+            threads = oracle.num_threads()
+            oracle.set_num_threads(1)
+            try:
+                v1, desc1, secs1, _ = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
+                                                         args.cpu_experts)
+            finally:
+                oracle.set_num_threads(threads)
+            out["cpu_baseline"]["single_thread"] = {"value": v1, "unit": UNIT, "cores": 1,
+                                                    "sample": desc1, "cpu_seconds": secs1}
     if rank == 0:
         print(json.dumps(out))
     if dist is not None:
