@@ -238,7 +238,7 @@ int moe_pack_w2(const moe_config_t* cfg, const void* w_down, void* w2, cudaStrea
  * activation-row scale in the epilogue. */
 
 /* Row-wise quantisation of a bf16 matrix.
- *  m         [rows, cols] bf16, cols a multiple of 8
+ *  m         [rows, cols] bf16, rows <= INT32_MAX, cols a multiple of 8
  *  rows_dev  device int32 or NULL: when given, only rows below *rows_dev (read
  *            on the device when the kernel runs, e.g. num_tokens_post_padded
  *            for the slot rows of h) are quantised; the others are left as

@@ -129,6 +129,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bwd_kernel(
 // reproducible.
 constexpr int kQuantWarps = 8;
 
+// Eight bf16 values (one 16-byte group) to eight E4M3 codes, lowest first.
+__device__ __forceinline__ uint2 quantize8_e4m3(const uint4 w, float s) {
+  const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+  uint32_t packed[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __fdiv_rn(__uint_as_float(a[i] << 16), s);
+    const float hi = __fdiv_rn(__uint_as_float(a[i] & 0xFFFF0000u), s);
+    const uint32_t pair =
+        __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);  // lo: low byte
+    if (i & 1)
+      packed[i >> 1] |= pair << 16;
+    else
+      packed[i >> 1] = pair;
+  }
+  return make_uint2(packed[0], packed[1]);
+}
+
 __global__ void __launch_bounds__(kQuantWarps * 32) quantize_rows_fp8_kernel(
     const uint16_t* __restrict__ m, int64_t rows, const int32_t* __restrict__ rows_dev, int cols,
     uint8_t* __restrict__ q, float* __restrict__ scale) {
@@ -153,19 +171,62 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_rows_fp8_kernel(
   const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   if (lane == 0) scale[r] = s;
   uint8_t* qr = q + (size_t)r * cols;
-  for (int v = lane; v < nv; v += 32) {
-    const uint4 w = reinterpret_cast<const uint4*>(row)[v];
-    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
-    uint32_t packed[2] = {0u, 0u};
+  for (int v = lane; v < nv; v += 32)
+    reinterpret_cast<uint2*>(qr)[v] = quantize8_e4m3(reinterpret_cast<const uint4*>(row)[v], s);
+}
+
+// The same quantisation with the whole row held in registers: WPR warps per
+// row, and lane l of the row's warps loads 16-byte groups l, l + 32*WPR, ...
+// (at most NV of them, all issued before any is used), so each row is read
+// from memory once. The row's warps combine their maxima through shared
+// memory; warps of rows past the bound skip the work but reach the barrier.
+template <int NV, int WPR>
+__global__ void __launch_bounds__(kQuantWarps * 32) quantize_rows_fp8_reg_kernel(
+    const uint16_t* __restrict__ m, int64_t rows, const int32_t* __restrict__ rows_dev, int cols,
+    uint8_t* __restrict__ q, float* __restrict__ scale) {
+  __shared__ float part[kQuantWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * (kQuantWarps / WPR) + warp / WPR;
+  const int64_t live = rows_dev ? min(rows, (int64_t)*rows_dev) : rows;
+  const bool active = r < live;
+  const int li = (warp % WPR) * 32 + lane;  // lane within the row's warps
+  const int nv = cols / 8;
+  uint4 w[NV];
+  float amax = 0.0f;
+  if (active) {
+    const uint4* row = reinterpret_cast<const uint4*>(m + (size_t)r * cols);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = __fdiv_rn(__uint_as_float(a[i] << 16), s);
-      const float hi = __fdiv_rn(__uint_as_float(a[i] & 0xFFFF0000u), s);
-      const uint32_t c0 = __nv_cvt_float_to_fp8(lo, __NV_SATFINITE, __NV_E4M3);
-      const uint32_t c1 = __nv_cvt_float_to_fp8(hi, __NV_SATFINITE, __NV_E4M3);
-      packed[i >> 1] |= (c0 | (c1 << 8)) << ((i & 1) * 16);
+    for (int j = 0; j < NV; ++j) {
+      const int v = li + 32 * WPR * j;
+      w[j] = v < nv ? row[v] : make_uint4(0u, 0u, 0u, 0u);
     }
-    reinterpret_cast<uint2*>(qr)[v] = make_uint2(packed[0], packed[1]);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const uint32_t a[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(a[i] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(a[i] & 0xFFFF0000u)));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  if (WPR > 1) {
+    if (lane == 0) part[warp] = amax;
+    __syncthreads();
+    const int w0 = warp - warp % WPR;
+#pragma unroll
+    for (int k = 0; k < WPR; ++k) amax = fmaxf(amax, part[w0 + k]);
+  }
+  if (!active) return;
+  const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  if (li == 0) scale[r] = s;
+  uint2* qr = reinterpret_cast<uint2*>(q + (size_t)r * cols);
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int v = li + 32 * WPR * j;
+    if (v < nv) qr[v] = quantize8_e4m3(w[j], s);
   }
 }
 
@@ -227,8 +288,26 @@ int launch_quantize_rows_fp8(const uint16_t* m, int64_t rows, const int32_t* row
                              uint8_t* q, float* scale, cudaStream_t s) {
   if (rows <= 0) return 0;
   const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
-  quantize_rows_fp8_kernel<<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(m, rows, rows_dev, cols,
-                                                                         q, scale);
+  const int nv = cols / 8;  // 16-byte groups per row
+  const dim3 b(kQuantWarps * 32);
+  const unsigned g1 = (unsigned)blocks;                                        // 8 rows per CTA
+  const unsigned g2 = (unsigned)((rows + kQuantWarps / 2 - 1) / (kQuantWarps / 2));  // 4 rows
+  const unsigned g4 = (unsigned)((rows + kQuantWarps / 4 - 1) / (kQuantWarps / 4));  // 2 rows
+  const unsigned g8 = (unsigned)rows;                                          // 1 row
+  if (nv <= 64)
+    quantize_rows_fp8_reg_kernel<2, 1><<<g1, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+  else if (nv <= 128)
+    quantize_rows_fp8_reg_kernel<4, 1><<<g1, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+  else if (nv <= 256)
+    quantize_rows_fp8_reg_kernel<8, 1><<<g1, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+  else if (nv <= 512)
+    quantize_rows_fp8_reg_kernel<8, 2><<<g2, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+  else if (nv <= 1024)
+    quantize_rows_fp8_reg_kernel<8, 4><<<g4, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+  else if (nv <= 2048)
+    quantize_rows_fp8_reg_kernel<8, 8><<<g8, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+  else  // rows wider than 16384 values: two passes over the row
+    quantize_rows_fp8_kernel<<<g1, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }

@@ -309,7 +309,7 @@ int moe_fc2_forward(const moe_config_t* cfg, const moe_routes_t* routes, const v
 
 int moe_quantize_rows_fp8(const void* m, int64_t rows, const int32_t* rows_dev, int cols, void* q,
                           float* scale, cudaStream_t stream) {
-  if (rows < 0 || cols <= 0 || cols % 8 != 0 || rows > ((int64_t)1 << 34))
+  if (rows < 0 || cols <= 0 || cols % 8 != 0 || rows > (int64_t)INT32_MAX)
     return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (!m || !q || !scale || !aligned16(m) || !aligned16(q)) return MOE_ERR_INVALID_ARG;

@@ -53,8 +53,11 @@ def test_quantize_rows_tie_saturation_and_subnormal_rows():
     _assert_same_codes(synth.f32_to_bf16_bits(rows), torch.device("cuda:0"), "hand rows")
 
 
+# widths that take each form of the quantiser: one warp per row holding 2, 4
+# or 8 groups per lane, 2, 4 or 8 warps per row, and two passes above 16384
 @pytest.mark.parametrize("rows,cols,std", [(37, 256, 1.0), (1000, 7168, 0.02), (8, 8, 50.0),
-                                           (300, 1408, 3.0)])
+                                           (300, 1408, 3.0), (5, 1024, 1.0), (17, 2048, 1.0),
+                                           (40, 4096, 1.0), (9, 12288, 0.5), (3, 16392, 2.0)])
 def test_quantize_rows_random_bit_exact(rows, cols, std):
     rng = np.random.default_rng(rows + cols)
     m = (rng.standard_normal((rows, cols)) * std).astype(np.float32)
@@ -62,22 +65,24 @@ def test_quantize_rows_random_bit_exact(rows, cols, std):
     _assert_same_codes(synth.f32_to_bf16_bits(m), torch.device("cuda:0"), "%dx%d" % (rows, cols))
 
 
-def test_quantize_rows_device_row_bound():
+@pytest.mark.parametrize("cols,bound", [(128, 6), (4096, 5), (12288, 3)])
+def test_quantize_rows_device_row_bound(cols, bound):
     """Rows at or past the device-side bound keep their contents; the rows
-    below it equal the oracle's codes."""
+    below it equal the oracle's codes (also when the bound falls inside a CTA
+    whose rows span several warps)."""
     dev = torch.device("cuda:0")
     rng = np.random.default_rng(9)
-    bits = synth.f32_to_bf16_bits(rng.standard_normal((10, 128)).astype(np.float32))
+    bits = synth.f32_to_bf16_bits(rng.standard_normal((10, cols)).astype(np.float32))
     m = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-    q = torch.full((10, 128), 0xAB, dtype=torch.uint8, device=dev)
+    q = torch.full((10, cols), 0xAB, dtype=torch.uint8, device=dev)
     s = torch.full((10,), -1.0, dtype=torch.float32, device=dev)
-    bound = torch.tensor([6], dtype=torch.int32, device=dev)
-    moe.quantize_rows_fp8(m, q, s, rows_dev=bound)
+    bd = torch.tensor([bound], dtype=torch.int32, device=dev)
+    moe.quantize_rows_fp8(m, q, s, rows_dev=bd)
     torch.cuda.synchronize()
-    qo, so = oracle.quantize_rows_fp8(bits[:6])
-    assert np.array_equal(q[:6].cpu().numpy(), qo)
-    assert np.array_equal(s[:6].cpu().numpy().view(np.uint32), so.view(np.uint32))
-    assert bool((q[6:] == 0xAB).all()) and bool((s[6:] == -1.0).all())
+    qo, so = oracle.quantize_rows_fp8(bits[:bound])
+    assert np.array_equal(q[:bound].cpu().numpy(), qo)
+    assert np.array_equal(s[:bound].cpu().numpy().view(np.uint32), so.view(np.uint32))
+    assert bool((q[bound:] == 0xAB).all()) and bool((s[bound:] == -1.0).all())
 
 
 def test_quantize_rows_rejects_bad_arguments():
