@@ -325,6 +325,66 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
   router_store(acc, logits, bias, m0, rows, n0, E, ty, tx);
 }
 
+// Few chains (small N*E, where the tiled kernels leave most lanes idle and
+// walk H/32 pipelined stages): one thread per token and 2 consecutive
+// experts, the whole contraction in registers, x rows and W_r rows read from
+// global memory (shared between threads through L1), the next 8 values of h
+// loaded while the current 8 are multiplied. Same chains: ascending h, one
+// fma per term, bias last.
+constexpr int kRSmallThreads = 128;
+
+template <bool kVec2>
+__global__ void __launch_bounds__(kRSmallThreads) router_logits_small_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
+    float* __restrict__ logits, int Nmax, const int32_t* __restrict__ n_dev, int H, int E) {
+  const int eg = (E + 1) / 2;  // pairs of experts
+  const int64_t gid = (int64_t)blockIdx.x * kRSmallThreads + threadIdx.x;
+  const int N = live_tokens(n_dev, Nmax);
+  const int t = (int)(gid / eg), e0 = (int)(gid % eg) * 2;
+  if (t >= N) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  auto load = [&](int h8, uint4& xv, float (&w)[8][2]) {
+    xv = __ldg(xr + h8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float* wrow = wr + (size_t)(h8 * 8 + i) * E + e0;
+      if (kVec2) {
+        const float2 q = __ldg(reinterpret_cast<const float2*>(wrow));
+        w[i][0] = q.x;
+        w[i][1] = q.y;
+      } else {
+        w[i][0] = __ldg(wrow);
+        w[i][1] = (e0 + 1 < E) ? __ldg(wrow + 1) : 0.0f;
+      }
+    }
+  };
+  float acc0 = 0.0f, acc1 = 0.0f;
+  uint4 xv;
+  float w[8][2];
+  load(0, xv, w);
+  for (int h8 = 0; h8 < H / 8; ++h8) {
+    uint4 xn = xv;
+    float wn[8][2];
+    if (h8 + 1 < H / 8) load(h8 + 1, xn, wn);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float xf = __uint_as_float((i & 1) ? (xw[i >> 1] & 0xFFFF0000u) : (xw[i >> 1] << 16));
+      acc0 = __fmaf_rn(xf, w[i][0], acc0);
+      acc1 = __fmaf_rn(xf, w[i][1], acc1);
+    }
+    xv = xn;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      w[i][0] = wn[i][0];
+      w[i][1] = wn[i][1];
+    }
+  }
+  float* out = logits + (size_t)t * E;
+  out[e0] = __fadd_rn(acc0, bias ? bias[e0] : 0.0f);
+  if (e0 + 1 < E) out[e0 + 1] = __fadd_rn(acc1, bias ? bias[e0 + 1] : 0.0f);
+}
+
 int router_sm_count(cudaError_t* err) {
   static int sms[64] = {};
   int dev = 0;
@@ -389,6 +449,18 @@ cudaError_t launch_router_logits(const RouteArgs& a, cudaStream_t s) {
   cudaError_t err = cudaSuccess;
   const int sms = router_sm_count(&err);
   if (sms <= 0) return err != cudaSuccess ? err : cudaErrorUnknown;
+  const int64_t threads = (int64_t)a.N * ((a.E + 1) / 2);
+  if (threads <= (int64_t)sms * 64) {  // at most 4 chains per fp32 lane of the GPU
+    const unsigned blocks = (unsigned)((threads + kRSmallThreads - 1) / kRSmallThreads);
+    const bool vec2 = (a.E % 2 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 7u) == 0);
+    if (vec2)
+      router_logits_small_kernel<true><<<blocks, kRSmallThreads, 0, s>>>(
+          a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E);
+    else
+      router_logits_small_kernel<false><<<blocks, kRSmallThreads, 0, s>>>(
+          a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E);
+    return cudaGetLastError();
+  }
   if (a.E <= 32) return launch_router_logits_tx<8>(a, vec4, sms, s);
   if (a.E <= 64) return launch_router_logits_tx<16>(a, vec4, sms, s);
   if (a.E <= 128) return launch_router_logits_tx<32>(a, vec4, sms, s);
