@@ -169,10 +169,6 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
-  return __uint_as_float((uint32_t)b << 16);
-}
-
 // Writes a 16-slot x 32-feature block to a bf16 row-major matrix: lane l holds
 // feature l of slots 0..15 in v; dst points at (slot 0, feature 0), ld is the
 // row stride in elements. Staged through this warp's 1 KiB buffer so that each
