@@ -757,6 +757,7 @@ def run_ours_train(args):
                   dwr=torch.empty((H, E), dtype=torch.float32, device=dev),
                   dbias=torch.empty(E, dtype=torch.float32, device=dev))
         st["h"], st["o"], st["y"] = moe.alloc_buffers(cfg, dev)
+        st["logits"] = moe.route_workspace_logits(cfg, st["ws"])
         return st
 
     def step(st, evs=None):
@@ -776,8 +777,9 @@ def run_ours_train(args):
                          st["dprob"], st["bws"], stream)
         if evs is not None:
             evs[4].record(stream)
+        # the logits the forward's route_align left in its workspace
         moe.router_backward(c, r, st["x"], st["wr"], st["bias"], st["dprob"], st["dx"], st["dwr"],
-                            st["dbias"], st["rws"], stream)
+                            st["dbias"], st["rws"], stream, logits=st["logits"])
         if evs is not None:
             evs[5].record(stream)
 

@@ -330,6 +330,9 @@ int64_t moe_router_backward_workspace_bytes(const moe_config_t* cfg);
  *   else:   g_k = dprob_k;   s = sum_k g_k p[e_k]
  *   dl[e] = p[e] (g[e] - s)   (g = 0 for the experts not chosen)
  *  x, w_router, bias   the forward's inputs (bias may be NULL)
+ *  logits     [N,E] f32: the logits moe_route_align left in its workspace
+ *             (moe_route_workspace_logits), valid while that workspace is
+ *             untouched; or NULL to recompute them (bit-identical either way)
  *  dprob      [N,K] f32 d loss / d p'
  *  dx         [N,H] bf16, in/out: dx += dl . W_r^T, summed in fp32 and rounded
  *             to bf16 once (add the router's path to the experts' dX)
@@ -337,9 +340,14 @@ int64_t moe_router_backward_workspace_bytes(const moe_config_t* cfg);
  *  dbias      [E] f32 output sum_t dl[t,:], or NULL
  * Outputs other than dx are overwritten. fp32 throughout; deterministic. */
 int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
-                        const float* w_router, const float* bias, const float* dprob, void* dx,
-                        float* dw_router, float* dbias, void* workspace, size_t ws_bytes,
-                        cudaStream_t stream);
+                        const float* w_router, const float* bias, const float* logits,
+                        const float* dprob, void* dx, float* dw_router, float* dbias,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Where moe_route_align leaves the router logits l [N,E] f32 (before the
+ * softmax, bias included) inside its workspace; NULL for an invalid config or
+ * workspace. Host-side pointer arithmetic only. */
+const float* moe_route_workspace_logits(const moe_config_t* cfg, const void* workspace);
 
 /* ---------------------------------------------------------------- graph ladder
  * Captured CUDA graphs of the forward at a ladder of token-count buckets, for

@@ -38,6 +38,7 @@ _LIB_PATH = os.path.join(_PKG, "libmoe.so")
 _lib = None
 
 MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
 
 
 class MoEError(RuntimeError):
@@ -126,7 +127,9 @@ def lib():
         L.moe_combine.argtypes = [CP, RP, P, P, P]
         L.moe_ffn_forward_train.argtypes = [CP, RP, P, P, P, P, P, P, P]
         L.moe_ffn_backward.argtypes = [CP, RP, P, P, P, P, P, P, P, P, P, P, SZ, P]
-        L.moe_router_backward.argtypes = [CP, RP, P, P, P, P, P, P, P, P, SZ, P]
+        L.moe_router_backward.argtypes = [CP, RP, P, P, P, P, P, P, P, P, P, SZ, P]
+        L.moe_route_workspace_logits.argtypes = [CP, P]
+        L.moe_route_workspace_logits.restype = P
         L.moe_ladder_pick.argtypes = [P, I32, ctypes.c_int32, ctypes.c_float]
         L.moe_ladder_pick.restype = I32
         L.moe_ladder_create.argtypes = [CP, P, I32, ctypes.c_float, ctypes.POINTER(_LayerBufsC),
@@ -288,15 +291,28 @@ def alloc_router_backward_workspace(cfg: Config, device):
 
 
 def router_backward(cfg: Config, routes: Routes, x, w_router, bias, dprob, dx, dw_router, dbias,
-                    workspace, stream=None) -> None:
+                    workspace, stream=None, logits=None) -> None:
     """Router backward: dx += dl . W_r^T (bf16, in place), dw_router [H,E] f32 and
-    dbias [E] f32 (or None) overwritten."""
+    dbias [E] f32 (or None) overwritten. logits: the forward's [N,E] logits
+    (route_workspace_logits), or None to recompute them."""
     _check("moe_router_backward",
            lib().moe_router_backward(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(x),
-                                     _ptr(w_router), _ptr(bias), _ptr(dprob), _ptr(dx),
-                                     _ptr(dw_router), _ptr(dbias), _ptr(workspace),
+                                     _ptr(w_router), _ptr(bias), _ptr(logits), _ptr(dprob),
+                                     _ptr(dx), _ptr(dw_router), _ptr(dbias), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(),
                                      _stream(stream)))
+
+
+def route_workspace_logits(cfg: Config, workspace):
+    """The [N,E] fp32 router logits moe_route_align left in its workspace, as a
+    view of that workspace tensor."""
+    import torch
+    p = lib().moe_route_workspace_logits(ctypes.byref(cfg), _ptr(workspace))
+    if not p:
+        raise MoEError("moe_route_workspace_logits", MOE_ERR_INVALID_ARG)
+    off = p - workspace.data_ptr()
+    n = cfg.n_tokens * cfg.n_experts
+    return workspace.view(-1)[off:off + 4 * n].view(torch.float32).view(cfg.n_tokens, cfg.n_experts)
 
 
 def combine(cfg: Config, routes: Routes, o, y, stream=None) -> None:

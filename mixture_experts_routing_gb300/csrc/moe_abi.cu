@@ -542,10 +542,16 @@ int64_t moe_router_backward_workspace_bytes(const moe_config_t* cfg) {
   return (int64_t)t;
 }
 
+const float* moe_route_workspace_logits(const moe_config_t* cfg, const void* workspace) {
+  if (check_cfg(cfg) != MOE_OK || !workspace) return nullptr;
+  return reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) +
+                                        ws_layout(cfg).logits);
+}
+
 int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
-                        const float* w_router, const float* bias, const float* dprob, void* dx,
-                        float* dw_router, float* dbias, void* workspace, size_t ws_bytes,
-                        cudaStream_t stream) {
+                        const float* w_router, const float* bias, const float* logits,
+                        const float* dprob, void* dx, float* dw_router, float* dbias,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream) {
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
   if (cfg->n_valid) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -577,6 +583,7 @@ int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, con
   a.bias = bias;
   a.topk_ids = routes->topk_ids;
   a.dprob = dprob;
+  a.logits = logits;
   a.dl = reinterpret_cast<float*>(ws + dl_off);
   a.part = reinterpret_cast<float*>(ws + part_off);
   a.dwr = dw_router;

@@ -117,6 +117,7 @@ int launch_wgrad(const WgradArgs& a, cudaStream_t s);
 struct RouterBwdArgs {
   int N, H, E, K, renorm;
   uint32_t* err;                // device error word (bounded waits)
+  const float* logits;          // the forward's logits [N,E], or null to recompute them
   const uint16_t* x;
   const float* wr;
   const float* bias;

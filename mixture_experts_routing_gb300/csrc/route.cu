@@ -858,9 +858,11 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
 // dl overwrites the logits.
 constexpr int kDlWarps = 8;
 
+// Reads the logits from `lg` and writes dl to `ld`, which may be the same
+// buffer (each lane reads its entries before it writes them).
 __global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
-    float* __restrict__ ld, int N, int E, int K, int renorm, const int32_t* __restrict__ topk_ids,
-    const float* __restrict__ dprob) {
+    const float* lg, float* ld, int N, int E, int K, int renorm,
+    const int32_t* __restrict__ topk_ids, const float* __restrict__ dprob) {
   __shared__ float pbuf[kDlWarps][kMaxExperts];
   __shared__ float gk_s[kDlWarps][kMaxTopK];
   __shared__ int32_t id_s[kDlWarps][kMaxTopK];
@@ -869,7 +871,7 @@ __global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
   const int t = blockIdx.x * kDlWarps + warp;
   if (t >= N) return;
   constexpr int PER = kMaxExperts / 32;
-  float* l = ld + (size_t)t * E;
+  const float* l = lg + (size_t)t * E;
   float v[PER];
   float m = -INFINITY;
 #pragma unroll
@@ -926,7 +928,7 @@ __global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
     float g = 0.0f;
     for (int k = 0; k < K; ++k)
       if (id_s[warp][k] == e) g = gk_s[warp][k];
-    l[e] = __fmul_rn(v[j], __fsub_rn(g, sg));
+    ld[(size_t)t * E + e] = __fmul_rn(v[j], __fsub_rn(g, sg));
   }
 }
 
@@ -1161,7 +1163,8 @@ int router_bwd_splits(int N, int H, int E) {
 int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
   if (a.N <= 0) return 0;
   int launched = 0;
-  // logits recomputed exactly as the forward (into the dl buffer)
+  // the forward's logits, or recomputed exactly as the forward (into the dl
+  // buffer)
   RouteArgs r{};
   r.N = a.N;
   r.H = a.H;
@@ -1171,11 +1174,14 @@ int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
   r.bias = a.bias;
   r.ws.logits = a.dl;
   r.err = a.err;
-  cudaError_t err = launch_router_logits(r, s);
-  if (err != cudaSuccess) return -(int)err;
-  ++launched;
+  cudaError_t err = cudaSuccess;
+  if (!a.logits) {
+    err = launch_router_logits(r, s);
+    if (err != cudaSuccess) return -(int)err;
+    ++launched;
+  }
   router_dlogits_kernel<<<(a.N + kDlWarps - 1) / kDlWarps, kDlWarps * 32, 0, s>>>(
-      a.dl, a.N, a.E, a.K, a.renorm, a.topk_ids, a.dprob);
+      a.logits ? a.logits : a.dl, a.dl, a.N, a.E, a.K, a.renorm, a.topk_ids, a.dprob);
   ++launched;
   const int splits = router_bwd_splits(a.N, a.H, a.E);
   const int tps = ((a.N + splits - 1) / splits + kDwK - 1) / kDwK * kDwK;

@@ -89,3 +89,29 @@ def test_router_backward_empty_batch():
     P = Problem(w, bm=32, with_ffn=False)
     _, dwr, dbias = _run(P, np.zeros((0, 2), np.float32))
     assert np.all(dwr == 0) and np.all(dbias == 0)
+
+
+@pytest.mark.parametrize("w", [SMALL[2][0], synth.WORKLOADS["qwen3_30b"]], ids=["e64", "qwen3_30b"])
+def test_router_backward_with_forward_logits_is_bit_identical(w):
+    """The logits route_align left in its workspace give exactly the outputs
+    of the recomputed ones."""
+    P = Problem(w, bm=32, host_weights=True, with_ffn=False)
+    N, H, E, K = w.n_tokens, w.hidden, w.n_experts, w.top_k
+    dev = P.dev
+    moe.route_align(P.cfg, P.x, P.wr_d, P.bias_d, P.routes, P.ws)
+    rng = np.random.default_rng(4)
+    dp = torch.from_numpy(rng.standard_normal((N, K)).astype(np.float32)).to(dev)
+    ws = moe.alloc_router_backward_workspace(P.cfg, dev)
+    outs = []
+    for logits in (None, moe.route_workspace_logits(P.cfg, P.ws)):
+        dx = torch.zeros((N, H), dtype=torch.bfloat16, device=dev)
+        dwr = torch.full((H, E), float("nan"), dtype=torch.float32, device=dev)
+        dbias = torch.full((E,), float("nan"), dtype=torch.float32, device=dev)
+        moe.router_backward(P.cfg, P.routes, P.x, P.wr_d, P.bias_d, dp, dx, dwr, dbias, ws,
+                            logits=logits)
+        torch.cuda.synchronize()
+        outs.append((dx.view(torch.int16).cpu(), dwr.view(torch.int32).cpu(),
+                     dbias.view(torch.int32).cpu()))
+    assert moe.device_error() == 0
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
