@@ -8,6 +8,7 @@
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -36,6 +37,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const uint16_t* __restrict__ o, const int32_t* __restrict__ token_routes,
     const float* __restrict__ topk_p, uint16_t* __restrict__ y, int N,
     const int32_t* __restrict__ n_dev, int H, int K) {
+  griddep_wait();  // launched after the kernel that writes this one's inputs
+  griddep_launch_dependents();
   const int t = blockIdx.x;
   if (n_dev && t >= *n_dev) {  // a token past the live count: zero row
     for (int v = threadIdx.x; v < H / 8; v += kCombineThreads)
@@ -150,6 +153,8 @@ __device__ __forceinline__ uint2 quantize8_e4m3(const uint4 w, float s) {
 __global__ void __launch_bounds__(kQuantWarps * 32) quantize_rows_fp8_kernel(
     const uint16_t* __restrict__ m, int64_t rows, const int32_t* __restrict__ rows_dev, int cols,
     uint8_t* __restrict__ q, float* __restrict__ scale) {
+  griddep_wait();  // launched after the kernel that writes this one's inputs
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * kQuantWarps + warp;
   if (rows_dev && r >= (int64_t)*rows_dev) return;  // rows past the live extent
@@ -184,6 +189,8 @@ template <int NV, int WPR>
 __global__ void __launch_bounds__(kQuantWarps * 32) quantize_rows_fp8_reg_kernel(
     const uint16_t* __restrict__ m, int64_t rows, const int32_t* __restrict__ rows_dev, int cols,
     uint8_t* __restrict__ q, float* __restrict__ scale) {
+  griddep_wait();  // launched after the kernel that writes this one's inputs
+  griddep_launch_dependents();
   __shared__ float part[kQuantWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * (kQuantWarps / WPR) + warp / WPR;
@@ -253,13 +260,13 @@ __global__ void transpose_kernel(const uint16_t* __restrict__ in, uint16_t* __re
 int launch_combine(const CombineArgs& a, cudaStream_t s) {
   if (a.N <= 0) return 0;
   if (a.K <= 2)
-    combine_kernel<2><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
+    launch_pdl(combine_kernel<2>, dim3(a.N), dim3(kCombineThreads), 0, s, a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
   else if (a.K <= 4)
-    combine_kernel<4><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
+    launch_pdl(combine_kernel<4>, dim3(a.N), dim3(kCombineThreads), 0, s, a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
   else if (a.K <= 8)
-    combine_kernel<8><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
+    launch_pdl(combine_kernel<8>, dim3(a.N), dim3(kCombineThreads), 0, s, a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
   else
-    combine_kernel<16><<<a.N, kCombineThreads, 0, s>>>(a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
+    launch_pdl(combine_kernel<16>, dim3(a.N), dim3(kCombineThreads), 0, s, a.o, a.token_routes, a.topk_p, a.y, a.N, a.n_dev, a.H, a.K);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }
@@ -295,19 +302,19 @@ int launch_quantize_rows_fp8(const uint16_t* m, int64_t rows, const int32_t* row
   const unsigned g4 = (unsigned)((rows + kQuantWarps / 4 - 1) / (kQuantWarps / 4));  // 2 rows
   const unsigned g8 = (unsigned)rows;                                          // 1 row
   if (nv <= 64)
-    quantize_rows_fp8_reg_kernel<2, 1><<<g1, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+    launch_pdl(quantize_rows_fp8_reg_kernel<2, 1>, dim3(g1), dim3(b), 0, s, m, rows, rows_dev, cols, q, scale);
   else if (nv <= 128)
-    quantize_rows_fp8_reg_kernel<4, 1><<<g1, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+    launch_pdl(quantize_rows_fp8_reg_kernel<4, 1>, dim3(g1), dim3(b), 0, s, m, rows, rows_dev, cols, q, scale);
   else if (nv <= 256)
-    quantize_rows_fp8_reg_kernel<8, 1><<<g1, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+    launch_pdl(quantize_rows_fp8_reg_kernel<8, 1>, dim3(g1), dim3(b), 0, s, m, rows, rows_dev, cols, q, scale);
   else if (nv <= 512)
-    quantize_rows_fp8_reg_kernel<8, 2><<<g2, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+    launch_pdl(quantize_rows_fp8_reg_kernel<8, 2>, dim3(g2), dim3(b), 0, s, m, rows, rows_dev, cols, q, scale);
   else if (nv <= 1024)
-    quantize_rows_fp8_reg_kernel<8, 4><<<g4, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+    launch_pdl(quantize_rows_fp8_reg_kernel<8, 4>, dim3(g4), dim3(b), 0, s, m, rows, rows_dev, cols, q, scale);
   else if (nv <= 2048)
-    quantize_rows_fp8_reg_kernel<8, 8><<<g8, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+    launch_pdl(quantize_rows_fp8_reg_kernel<8, 8>, dim3(g8), dim3(b), 0, s, m, rows, rows_dev, cols, q, scale);
   else  // rows wider than 16384 values: two passes over the row
-    quantize_rows_fp8_kernel<<<g1, b, 0, s>>>(m, rows, rows_dev, cols, q, scale);
+    launch_pdl(quantize_rows_fp8_kernel, dim3(g1), dim3(b), 0, s, m, rows, rows_dev, cols, q, scale);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }

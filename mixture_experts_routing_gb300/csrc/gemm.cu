@@ -353,6 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kAMn) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+  // the setup above touches no global memory; the tile list reads the counts
+  // the previous kernel wrote
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 0) build_tile_list(p, tpre, ttn, lane);
   tc_fence_before();
   __syncthreads();
@@ -906,27 +910,27 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   switch (a.mode) {
     case kModeFc1:
       if (gelu)
-        moe_gemm_kernel<kModeFc1, 1><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+        launch_pdl(moe_gemm_kernel<kModeFc1, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
       else
-        moe_gemm_kernel<kModeFc1, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+        launch_pdl(moe_gemm_kernel<kModeFc1, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
       break;
     case kModeFc1Fp8:
       if (gelu)
-        moe_gemm_kernel<kModeFc1Fp8, 1><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+        launch_pdl(moe_gemm_kernel<kModeFc1Fp8, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
       else
-        moe_gemm_kernel<kModeFc1Fp8, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+        launch_pdl(moe_gemm_kernel<kModeFc1Fp8, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
       break;
-    case kModeFc2: moe_gemm_kernel<kModeFc2, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p); break;
+    case kModeFc2: launch_pdl(moe_gemm_kernel<kModeFc2, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p); break;
     case kModeFc2Fp8:
-      moe_gemm_kernel<kModeFc2Fp8, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+      launch_pdl(moe_gemm_kernel<kModeFc2Fp8, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
       break;
     case kModeDgrad2:
       if (gelu)
-        moe_gemm_kernel<kModeDgrad2, 1><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+        launch_pdl(moe_gemm_kernel<kModeDgrad2, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
       else
-        moe_gemm_kernel<kModeDgrad2, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p);
+        launch_pdl(moe_gemm_kernel<kModeDgrad2, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
       break;
-    default: moe_gemm_kernel<kModeDgrad1, 0><<<grid, kThreads, dyn, s>>>(tmA, tmB, tmA2, p); break;
+    default: launch_pdl(moe_gemm_kernel<kModeDgrad1, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p); break;
   }
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;

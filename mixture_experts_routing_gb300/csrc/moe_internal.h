@@ -6,6 +6,26 @@
 
 namespace moe {
 
+// Launch of a forward-path kernel with programmatic stream serialization: it
+// may start (setup, then griddep_wait) while the previous kernel in the
+// stream finishes, which hides the launch gap between the six kernels of a
+// forward. Captured into CUDA graphs as programmatic edges.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kTokensPerChunk = 64;   // tokens per router CTA = one scan chunk
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 16;

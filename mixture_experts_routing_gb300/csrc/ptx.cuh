@@ -24,6 +24,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- programmatic launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel in the stream is still running. griddep_wait() blocks
+// until that kernel has completed and its memory is visible; every kernel of
+// this library that is launched so calls it before its first global-memory
+// access (in every CTA, also in CTAs that leave early). It is a no-op for an
+// ordinary launch. griddep_launch_dependents() lets the next such kernel
+// launch; a dependent grid starts only after every CTA of this one has
+// issued it or exited.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

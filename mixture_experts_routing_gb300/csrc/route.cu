@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
     float* __restrict__ logits, int Nmax, const int32_t* __restrict__ n_dev, int H, int E, int bm,
     int wr_vec4) {
+  griddep_wait();  // launched after the kernel that writes this one's inputs
+  griddep_launch_dependents();
   constexpr int BN = TX * kRTN;
   const int NT = blockDim.x, RM = (NT / TX) * kRPad;
   const int N = live_tokens(n_dev, Nmax);
@@ -244,6 +246,8 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
     const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
     const float* __restrict__ bias, float* __restrict__ logits, int Nmax,
     const int32_t* __restrict__ n_dev, int H, int E, int bm, uint32_t* __restrict__ err) {
+  griddep_wait();  // launched after the kernel that writes this one's inputs
+  griddep_launch_dependents();
   constexpr int BN = TX * kRTN;
   const int NT = blockDim.x, TY = NT / TX, RM = TY * kRPad;
   const int N = live_tokens(n_dev, Nmax);
@@ -337,6 +341,8 @@ template <bool kVec2>
 __global__ void __launch_bounds__(kRSmallThreads) router_logits_small_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
     float* __restrict__ logits, int Nmax, const int32_t* __restrict__ n_dev, int H, int E) {
+  griddep_wait();  // launched after the kernel that writes this one's inputs
+  griddep_launch_dependents();
   const int eg = (E + 1) / 2;  // pairs of experts
   const int64_t gid = (int64_t)blockIdx.x * kRSmallThreads + threadIdx.x;
   const int N = live_tokens(n_dev, Nmax);
@@ -433,10 +439,10 @@ cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaS
                      LBK, (uint32_t)bm) &&
       make_map_plain(&tmw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.wr, (uint64_t)a.E,
                      (uint64_t)a.H, BN, LBK)) {
-    router_logits_tma_kernel<TX><<<g, ty * TX, router_tma_layout(bm, BN, ty).total, s>>>(
+    launch_pdl(router_logits_tma_kernel<TX>, dim3(g), dim3(ty * TX), router_tma_layout(bm, BN, ty).total, s, 
         tmx, tmw, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, bm, a.err);
   } else {
-    router_logits_kernel<TX><<<g, ty * TX, router_smem_bytes(bm, BN, ty), s>>>(
+    launch_pdl(router_logits_kernel<TX>, dim3(g), dim3(ty * TX), router_smem_bytes(bm, BN, ty), s, 
         a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, bm, vec4);
   }
   return cudaGetLastError();
@@ -454,10 +460,10 @@ cudaError_t launch_router_logits(const RouteArgs& a, cudaStream_t s) {
     const unsigned blocks = (unsigned)((threads + kRSmallThreads - 1) / kRSmallThreads);
     const bool vec2 = (a.E % 2 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 7u) == 0);
     if (vec2)
-      router_logits_small_kernel<true><<<blocks, kRSmallThreads, 0, s>>>(
+      launch_pdl(router_logits_small_kernel<true>, dim3(blocks), dim3(kRSmallThreads), 0, s, 
           a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E);
     else
-      router_logits_small_kernel<false><<<blocks, kRSmallThreads, 0, s>>>(
+      launch_pdl(router_logits_small_kernel<false>, dim3(blocks), dim3(kRSmallThreads), 0, s, 
           a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E);
     return cudaGetLastError();
   }
@@ -479,6 +485,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
     int32_t* __restrict__ chunk_counts, int32_t* __restrict__ chunk_lofs,
     int32_t* __restrict__ chunk_routes, uint32_t* __restrict__ chunk_keys,
     uint8_t* __restrict__ keep, int32_t* __restrict__ token_routes) {
+  griddep_wait();  // launched after the kernel that writes this one's inputs
+  griddep_launch_dependents();
   __shared__ float zbuf[kTopkWarps][kMaxExperts];
   __shared__ int32_t ids_s[kTokensPerChunk * kMaxTopK];
   __shared__ uint32_t pk_s[kTokensPerChunk * kMaxTopK];
@@ -642,6 +650,8 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     int32_t* __restrict__ expert_ids, int32_t* __restrict__ block_start,
     int32_t* __restrict__ ntpp, int32_t* __restrict__ token_routes,
     int32_t* __restrict__ gemm_sched, float* __restrict__ slot_prob) {
+  griddep_wait();  // launched after the kernel that writes this one's inputs
+  griddep_launch_dependents();
   extern __shared__ uint32_t dyn[];
   __shared__ int32_t hist[256];
   __shared__ int32_t warp_tot[32];
@@ -1121,7 +1131,7 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
     const cudaError_t e1 = launch_router_logits(a, s);
     if (e1 != cudaSuccess) return -(int)e1;
     ++launched;
-    router_topk_kernel<<<C, kTopkWarps * 32, 0, s>>>(a.ws.logits, a.N, a.n_dev, a.E, a.K, a.renorm,
+    launch_pdl(router_topk_kernel, dim3(C), dim3(kTopkWarps * 32), 0, s, a.ws.logits, a.N, a.n_dev, a.E, a.K, a.renorm,
                                                      a.topk_ids, a.topk_p, a.ws.chunk_counts,
                                                      a.ws.chunk_lofs, a.ws.chunk_routes,
                                                      a.ws.chunk_keys, a.keep, a.token_routes);
@@ -1141,7 +1151,7 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
       if (dev >= 0 && dev < 64) set_for[dev] = 1;
     }
   }
-  route_select_kernel<<<a.E, kSelThreads, dyn, s>>>(
+  launch_pdl(route_select_kernel, dim3(a.E), dim3(kSelThreads), dyn, s, 
       a.ws.chunk_counts, a.ws.chunk_lofs, a.ws.chunk_routes, a.ws.chunk_keys, a.N, a.n_dev, a.E,
       a.K, a.cap_num, a.cap_den, a.bm, a.dropless, a.ladder, (int)a.s_max, a.keep, a.expert_counts,
       a.kept_counts, a.sorted_slot_ids, a.expert_ids,
