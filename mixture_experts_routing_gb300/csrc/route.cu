@@ -1051,59 +1051,82 @@ __global__ void __launch_bounds__(256) router_dbias_kernel(const float* __restri
   if (threadIdx.x == 0) dbias[e] = red[0];
 }
 
-// dx[t,h] += sum_e dl[t,e] W_r[h,e] (fp32, rounded to bf16 once). 64 tokens x
-// 64 rows of W_r per CTA; both operands are staged 64 experts at a time as
-// rows (e contiguous, padded to 68 floats), and a thread takes 4 tokens x 4
-// rows of W_r (tx + 16j: the 8 threads of a quarter-warp hit 8 different
-// 16-byte bank groups), reading 16 bytes (4 experts) of each row per step:
-// 8 loads per 64 fma.
-constexpr int kDxE = 64, kDxPad = kDxE + 4;
+// dx[t,h] += sum_e dl[t,e] W_r[h,e] (an fp32 fma chain over ascending e, then
+// added to dx in fp32 and rounded to bf16 once). 64 tokens x 128 rows of W_r
+// per step, 256 threads: a warp covers 4 x 8 threads, a thread 4 tokens x 8
+// rows of W_r (two groups of 4 rows, 64 apart). Both operands are staged
+// transposed, 64 experts at a time (ds[e][t], ws[e][h]), so each step is
+// three conflict-free 16-byte shared loads for 32 fmas; dx is read and written
+// 8 bytes (4 values) at a time. A CTA keeps one 128-row slice of W_r and walks
+// `tiles` consecutive 64-token tiles; with E <= 64 its W_r tile is staged
+// once. H is a multiple of 128.
+constexpr int kDxE = 64, kDxT = 64, kDxH = 128;
 
 __global__ void __launch_bounds__(256) router_dx_kernel(const float* __restrict__ dl,
                                                         const float* __restrict__ wr, int N, int H,
-                                                        int E, int vec4, uint16_t* __restrict__ dx) {
-  __shared__ __align__(16) float ds[kRbTile][kDxPad];
-  __shared__ __align__(16) float ws_[kRbTile][kDxPad];
-  const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
-  const int h0 = blockIdx.x * kRbTile, t0 = blockIdx.y * kRbTile;
-  float acc[4][4] = {};
+                                                        int E, int vec4, int tiles,
+                                                        uint16_t* __restrict__ dx) {
+  __shared__ __align__(16) float ds[kDxE][kDxT];
+  __shared__ __align__(16) float ws_[kDxE][kDxH];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ty = (warp >> 1) * 4 + (lane >> 3);  // tokens 4ty .. 4ty+3
+  const int tx = (warp & 1) * 8 + (lane & 7);    // rows 4tx .. +3 and 64 + 4tx .. +3
+  const int h0 = blockIdx.x * kDxH;
+  for (int tt = 0; tt < tiles; ++tt) {
+  const int t0 = (blockIdx.y * tiles + tt) * kDxT;
+  if (t0 >= N) break;
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
   for (int k0 = 0; k0 < E; k0 += kDxE) {
     const int ke = min(kDxE, E - k0);
-    for (int i = tid; i < kRbTile * (kDxE / 4); i += 256) {
-      const int r = i / (kDxE / 4), q = (i % (kDxE / 4)) * 4;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-      if (vec4) {  // E a multiple of 4, 16-byte rows
-        if (q < ke && t0 + r < N) a = *reinterpret_cast<const float4*>(dl + (size_t)(t0 + r) * E + k0 + q);
-        if (q < ke && h0 + r < H) b = *reinterpret_cast<const float4*>(wr + (size_t)(h0 + r) * E + k0 + q);
-      } else {
-        float av[4] = {0.f, 0.f, 0.f, 0.f}, bv[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < 4; ++j) {
-          if (q + j >= ke) break;
-          if (t0 + r < N) av[j] = dl[(size_t)(t0 + r) * E + k0 + q + j];
-          if (h0 + r < H) bv[j] = wr[(size_t)(h0 + r) * E + k0 + q + j];
+    // 4 experts of one row per thread and step, written transposed; with
+    // vec4 (E a multiple of 4, 16-byte rows) ke is a multiple of 4 too
+    for (int c = tid; c < kDxT * (kDxE / 4); c += 256) {
+      const int t = c % kDxT, q = (c / kDxT) * 4;
+      float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (t0 + t < N && q < ke) {
+        const float* src = dl + (size_t)(t0 + t) * E + k0 + q;
+        if (vec4) {
+          const float4 f = *reinterpret_cast<const float4*>(src);
+          v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = (q + j < ke) ? src[j] : 0.0f;
         }
-        a = make_float4(av[0], av[1], av[2], av[3]);
-        b = make_float4(bv[0], bv[1], bv[2], bv[3]);
       }
-      *reinterpret_cast<float4*>(&ds[r][q]) = a;
-      *reinterpret_cast<float4*>(&ws_[r][q]) = b;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ds[q + j][t] = v[j];
+    }
+    for (int c = tid; c < kDxH * (kDxE / 4) && (tt == 0 || E > kDxE); c += 256) {
+      const int h = c % kDxH, q = (c / kDxH) * 4;
+      float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (q < ke) {
+        const float* src = wr + (size_t)(h0 + h) * E + k0 + q;
+        if (vec4) {
+          const float4 f = *reinterpret_cast<const float4*>(src);
+          v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = (q + j < ke) ? src[j] : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ws_[q + j][h] = v[j];
     }
     __syncthreads();
-    for (int k = 0; k < ke; k += 4) {
-      float4 a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(&ds[ty * 4 + i][k]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = *reinterpret_cast<const float4*>(&ws_[tx + 16 * j][k]);
+    for (int k = 0; k < ke; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(&ds[k][ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&ws_[k][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&ws_[k][64 + tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[i][j] = __fmaf_rn(a[i].x, b[j].x, acc[i][j]);
-          acc[i][j] = __fmaf_rn(a[i].y, b[j].y, acc[i][j]);
-          acc[i][j] = __fmaf_rn(a[i].z, b[j].z, acc[i][j]);
-          acc[i][j] = __fmaf_rn(a[i].w, b[j].w, acc[i][j]);
-        }
+        for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
@@ -1112,13 +1135,21 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const float* __restrict_
     const int t = t0 + ty * 4 + i;
     if (t >= N) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int h = h0 + tx + 16 * j;
-      if (h >= H) continue;
-      uint16_t* q = dx + (size_t)t * H + h;
-      const float v = __fadd_rn(__uint_as_float((uint32_t)*q << 16), acc[i][j]);
-      *q = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    for (int g = 0; g < 2; ++g) {
+      uint2* q = reinterpret_cast<uint2*>(dx + (size_t)t * H + h0 + g * 64 + tx * 4);
+      const uint2 old = *q;
+      const uint32_t w[2] = {old.x, old.y};
+      uint32_t out[2];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const float lo = __fadd_rn(__uint_as_float(w[m] << 16), acc[i][g * 4 + 2 * m]);
+        const float hi = __fadd_rn(__uint_as_float(w[m] & 0xFFFF0000u), acc[i][g * 4 + 2 * m + 1]);
+        out[m] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+      }
+      *q = make_uint2(out[0], out[1]);
     }
+  }
   }
 }
 
@@ -1207,9 +1238,19 @@ int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
     router_dbias_kernel<<<a.E, 256, 0, s>>>(a.dl, a.N, a.E, a.dbias);
     ++launched;
   }
-  dim3 g2((a.H + kRbTile - 1) / kRbTile, (a.N + kRbTile - 1) / kRbTile);
+  // about four CTAs per SM, each walking consecutive token tiles
+  int sms_dx = 0;
+  {
+    cudaError_t e2 = cudaSuccess;
+    sms_dx = router_sm_count(&e2);
+    if (sms_dx <= 0) return -(int)(e2 != cudaSuccess ? e2 : cudaErrorUnknown);
+  }
+  const int t_tiles = (a.N + kDxT - 1) / kDxT;
+  const int want_y = (4 * sms_dx + a.H / kDxH - 1) / (a.H / kDxH);
+  const int dx_tiles = (t_tiles + want_y - 1) / want_y;
+  dim3 g2(a.H / kDxH, (t_tiles + dx_tiles - 1) / dx_tiles);
   const int vec4 = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 15u) == 0);
-  router_dx_kernel<<<g2, 256, 0, s>>>(a.dl, a.wr, a.N, a.H, a.E, vec4, a.dx);
+  router_dx_kernel<<<g2, 256, 0, s>>>(a.dl, a.wr, a.N, a.H, a.E, vec4, dx_tiles, a.dx);
   ++launched;
   err = cudaGetLastError();
   return err == cudaSuccess ? launched : -(int)err;
