@@ -942,84 +942,98 @@ __global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
   }
 }
 
-// dW_r[h,e] = sum_t x[t,h] dl[t,e] over the tokens of one split (64 x 64 CTA
-// tile, 4 x 4 per thread, 32 tokens per stage, the next stage's loads held in
-// registers while this stage is computed); partial sums of split z go to
-// part + z*H*E, each a sequential sum over ascending t within the split.
-// (vec: H a multiple of 4 and E a multiple of 4, so a thread's 4 columns are
-// one 8-byte x load and one 16-byte dl load.)
-constexpr int kRbTile = 64, kDwK = 32;
+// dW_r[h,e] = sum_t x[t,h] dl[t,e] over the tokens of one split: 128 rows of
+// h x 64 experts per CTA, 256 threads, a warp covering 4 x 8 threads and a
+// thread 8 rows x 4 experts (three conflict-free 16-byte shared loads per 32
+// fmas); 32 tokens per stage, the next stage's loads held in registers while
+// this stage is computed. Partial sums of split z go to part + z*H*E, each a
+// sequential sum over ascending t within the split. H is a multiple of 128;
+// vec: E a multiple of 4 (16-byte dl loads and partial stores).
+constexpr int kDwH = 128, kDwE = 64, kDwK = 32;
 
 __global__ void __launch_bounds__(256) router_dwr_kernel(const uint16_t* __restrict__ x,
                                                          const float* __restrict__ dl, int N, int H,
                                                          int E, int t_per_split, int vec,
                                                          float* __restrict__ part) {
-  __shared__ __align__(16) float as[2][kDwK][kRbTile];
-  __shared__ __align__(16) float bs[2][kDwK][kRbTile];
-  const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
-  const int e0 = blockIdx.x * kRbTile, h0 = blockIdx.y * kRbTile;
+  __shared__ __align__(16) float as[2][kDwK][kDwH];
+  __shared__ __align__(16) float bs[2][kDwK][kDwE];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ty = (warp >> 1) * 4 + (lane >> 3);  // rows h0 + 8ty .. +7
+  const int tx = (warp & 1) * 8 + (lane & 7);    // experts e0 + 4tx .. +3
+  const int e0 = blockIdx.x * kDwE, h0 = blockIdx.y * kDwH;
   const int ta = blockIdx.z * t_per_split, tb = min(N, ta + t_per_split);
-  // this thread's loads of each 32 x 64 stage tile: rows lk and lk + 16, 4 columns
-  const int lk = tid / 16, lc = (tid % 16) * 4;
-  float ra[2][4], rb[2][4];
+  // this thread's loads of each stage: token rows lk and lk + 16; 8 values of
+  // h from column xc, 4 experts from column dc
+  const int lk = tid / 16, xc = (tid % 16) * 8, dc = (tid % 16) * 4;
+  float ra[2][8], rb[2][4];
   auto fetch = [&](int t0) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int t = t0 + lk + 16 * r;
       const bool ok = t < tb;
+      uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+      if (ok) xv = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h0 + xc);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ra[r][2 * i] = __uint_as_float(xw[i] << 16);
+        ra[r][2 * i + 1] = __uint_as_float(xw[i] & 0xFFFF0000u);
+      }
       if (vec) {
-        uint2 xv = make_uint2(0u, 0u);
         float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ok && h0 + lc < H) xv = *reinterpret_cast<const uint2*>(x + (size_t)t * H + h0 + lc);
-        if (ok && e0 + lc < E) dv = *reinterpret_cast<const float4*>(dl + (size_t)t * E + e0 + lc);
-        ra[r][0] = __uint_as_float(xv.x << 16);
-        ra[r][1] = __uint_as_float(xv.x & 0xFFFF0000u);
-        ra[r][2] = __uint_as_float(xv.y << 16);
-        ra[r][3] = __uint_as_float(xv.y & 0xFFFF0000u);
+        if (ok && e0 + dc < E) dv = *reinterpret_cast<const float4*>(dl + (size_t)t * E + e0 + dc);
         rb[r][0] = dv.x; rb[r][1] = dv.y; rb[r][2] = dv.z; rb[r][3] = dv.w;
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          ra[r][j] = (ok && h0 + lc + j < H)
-                         ? __uint_as_float((uint32_t)x[(size_t)t * H + h0 + lc + j] << 16) : 0.0f;
-          rb[r][j] = (ok && e0 + lc + j < E) ? dl[(size_t)t * E + e0 + lc + j] : 0.0f;
-        }
+        for (int j = 0; j < 4; ++j)
+          rb[r][j] = (ok && e0 + dc + j < E) ? dl[(size_t)t * E + e0 + dc + j] : 0.0f;
       }
     }
   };
-  float acc[4][4] = {};
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
   if (ta < tb) fetch(ta);
   int buf = 0;
   for (int t0 = ta; t0 < tb; t0 += kDwK, buf ^= 1) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      *reinterpret_cast<float4*>(&as[buf][lk + 16 * r][lc]) =
+      *reinterpret_cast<float4*>(&as[buf][lk + 16 * r][xc]) =
           make_float4(ra[r][0], ra[r][1], ra[r][2], ra[r][3]);
-      *reinterpret_cast<float4*>(&bs[buf][lk + 16 * r][lc]) =
+      *reinterpret_cast<float4*>(&as[buf][lk + 16 * r][xc + 4]) =
+          make_float4(ra[r][4], ra[r][5], ra[r][6], ra[r][7]);
+      *reinterpret_cast<float4*>(&bs[buf][lk + 16 * r][dc]) =
           make_float4(rb[r][0], rb[r][1], rb[r][2], rb[r][3]);
     }
     __syncthreads();
     if (t0 + kDwK < tb) fetch(t0 + kDwK);  // next stage's loads overlap this stage's math
 #pragma unroll
     for (int k = 0; k < kDwK; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(&as[buf][k][ty * 4]);
+      const float4 a0 = *reinterpret_cast<const float4*>(&as[buf][k][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&as[buf][k][ty * 8 + 4]);
       const float4 b = *reinterpret_cast<const float4*>(&bs[buf][k][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
     }
   }
   float* out = part + (size_t)blockIdx.z * H * E;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int h = h0 + ty * 4 + i;
-    if (h >= H) continue;
+  for (int i = 0; i < 8; ++i) {
+    const int h = h0 + ty * 8 + i;
+    const int e = e0 + tx * 4;
+    float* o = out + (size_t)h * E + e;
+    if (vec && e + 3 < E) {
+      *reinterpret_cast<float4*>(o) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
-      if (e < E) out[(size_t)h * E + e] = acc[i][j];
+      for (int j = 0; j < 4; ++j)
+        if (e + j < E) o[j] = acc[i][j];
     }
   }
 }
@@ -1194,7 +1208,7 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
 }
 
 int router_bwd_splits(int N, int H, int E) {
-  const int tiles = ((E + kRbTile - 1) / kRbTile) * ((H + kRbTile - 1) / kRbTile);
+  const int tiles = ((E + kDwE - 1) / kDwE) * (H / kDwH);
   int splits = (2 * 152 + tiles - 1) / tiles;  // about two CTAs per SM
   const int max_splits = (N + 255) / 256;      // at least 256 tokens per split
   if (splits > max_splits) splits = max_splits;
@@ -1226,7 +1240,7 @@ int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
   ++launched;
   const int splits = router_bwd_splits(a.N, a.H, a.E);
   const int tps = ((a.N + splits - 1) / splits + kDwK - 1) / kDwK * kDwK;
-  dim3 g1((a.E + kRbTile - 1) / kRbTile, (a.H + kRbTile - 1) / kRbTile, splits);
+  dim3 g1((a.E + kDwE - 1) / kDwE, a.H / kDwH, splits);
   const int dw_vec = (a.H % 4 == 0) && (a.E % 4 == 0) &&
                      ((reinterpret_cast<uintptr_t>(a.x) & 7u) == 0);
   router_dwr_kernel<<<g1, 256, 0, s>>>(a.x, a.dl, a.N, a.H, a.E, tps, dw_vec, a.part);
