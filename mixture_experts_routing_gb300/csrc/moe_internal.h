@@ -26,7 +26,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-constexpr int kTokensPerChunk = 64;   // tokens per router CTA = one scan chunk
+constexpr int kTokensPerChunk = 32;   // tokens per router CTA = one scan chunk
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 16;
 constexpr int kMaxTokens = 24576;     // select kernel stages one expert's routes in smem

@@ -7,7 +7,7 @@
 //  R2 router_topk   : one warp per token: softmax with our own fp32 exp, K rounds
 //                     of warp argmax (max of the p bits, then min of the expert
 //                     ids at that max), renormalise; then the CTA sorts its
-//                     64-token chunk's routes by expert (stable) and records
+//                     32-token chunk's routes by expert (stable) and records
 //                     per-expert counts and offsets (the scan's first level).
 //  R3+R4 route_select: one CTA per expert: exclusive scan of the expert's chunk
 //                     counts, gather of its routes in token order, radix select
@@ -474,7 +474,7 @@ cudaError_t launch_router_logits(const RouteArgs& a, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------- R2
-// One warp per token (32 warps, 64 tokens per CTA = one chunk). After the
+// One warp per token (32 warps, 32 tokens per CTA = one chunk). After the
 // chunk's top-K, the CTA sorts its routes by expert (stable, so each expert's
 // routes stay in token order) and records per-expert counts and offsets.
 constexpr int kTopkWarps = 32;
