@@ -72,6 +72,11 @@ def test_invalid_configs_fail_closed(L):
         c = moe.Config(**dict(good, **{k: v}, top_k=2))
         assert L.moe_max_slots(ctypes.byref(c)) == -2, (k, v)
     assert L.moe_max_slots(None) == -1
+    # the token bound of the route kernels: 24576 is accepted, one more is not
+    c = moe.Config(**dict(good, n_tokens=24576))
+    assert L.moe_max_slots(ctypes.byref(c)) > 0
+    c = moe.Config(**dict(good, n_tokens=24577))
+    assert L.moe_max_slots(ctypes.byref(c)) == -2
 
 
 def test_entry_points_reject_bad_arguments_before_launch(L):

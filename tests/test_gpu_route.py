@@ -24,13 +24,17 @@ def _w(N, H, E, K, I=128, cn=1, cd=1, **kw):
 
 @pytest.mark.parametrize("w,bm", [
     (_w(1, 128, 8, 2), 16),            # one token
-    (_w(63, 128, 8, 2), 16),           # ragged chunk
-    (_w(65, 256, 16, 4, cn=1, cd=2), 32),  # two chunks, second holds one token; heavy drops
+    (_w(31, 128, 8, 2), 16),           # one ragged 32-token chunk
+    (_w(33, 128, 8, 2), 32),           # the second chunk holds one token
+    (_w(63, 128, 8, 2), 16),           # ragged second chunk
+    (_w(65, 256, 16, 4, cn=1, cd=2), 32),  # three chunks, the last holds one token; heavy drops
     (_w(130, 128, 1, 1), 16),          # one expert
     (_w(97, 128, 5, 5), 64),           # K = E: every expert picked
     (_w(200, 128, 256, 16), 16),       # widest supported router
     (_w(300, 384, 12, 3, cn=7, cd=1), 128),  # capacity above N: nothing dropped
     (_w(0, 128, 8, 2), 16),            # empty batch
+    (_w(24576, 128, 8, 2), 32),        # the largest supported token count
+    (_w(24576, 128, 64, 6, cn=0, cd=1, zipf_s=0.8, ladder=(2, 4), ladder_den=2), 32),  # dropless
 ])
 def test_route_align_edge_shapes(w, bm):
     P = Problem(w, bm=bm, host_weights=False, with_ffn=False)
