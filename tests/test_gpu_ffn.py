@@ -136,3 +136,29 @@ def test_graph_replay_equals_eager_with_new_inputs():
         assert torch.equal(o_graph[kept], P.o[kept])
         assert torch.equal(y_graph, P.y)
         assert S == moe.max_slots(P.cfg)
+
+
+@pytest.mark.parametrize("cn", [1, 0], ids=["capacity", "dropless"])
+def test_forward_largest_token_count(cn):
+    """The largest supported token count (24576) through the whole forward:
+    routing bit-exact, every kept slot of the busiest and the emptiest
+    non-empty expert against the oracle, y of every token as the combine of
+    the library's o, and whole tokens (first, last, middle) end to end."""
+    kw = dict(zipf_s=0.8, ladder=(2, 4), ladder_den=2) if cn == 0 else dict(zipf_s=0.8)
+    w = synth.Workload("max_tokens", 24576, 256, 16, 4, 256, cn, 1, **kw)
+    P = Problem(w, bm=32, host_weights=True)
+    P.run()
+    R = P.oracle_routing()
+    assert_routing_equal(P, R)
+    kc = R.layout.kept_counts
+    order = np.argsort(kc, kind="stable")
+    nonzero = [e for e in order if kc[e] > 0]
+    check_expert_slots(P, R, sorted({int(order[-1]), int(nonzero[0])}))
+    check_combine_property(P, R)
+    toks = [0, w.n_tokens // 2, w.n_tokens - 1]
+    W = P.expert_weights(range(w.n_experts))
+    y = P.y.float().cpu().numpy()
+    for t in toks:
+        y_ref = oracle.forward_tokens(t, t + 1, P.x_bits, W, w.hidden, w.inter, R.topk_ids,
+                                      R.topk_p, R.layout.keep)
+        assert_close(y[t:t + 1], y_ref, "y of token %d" % t)
