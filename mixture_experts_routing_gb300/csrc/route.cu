@@ -93,14 +93,15 @@ constexpr size_t router_smem_bytes(int bm, int bn, int ty) {
          (size_t)LBK * ty * kRPad * 4;
 }
 
-// Converts stage rows [0, rows) of bf16 x ([row][BK]) into the transposed
-// fp32 tile `as` ([BK][RM], token m at (m/7)*8 + m%7).
+// Converts stage rows [0, rows) of bf16 x ([row][KB]) into the transposed
+// fp32 tile `as` ([KB][RM], token m at (m/7)*8 + m%7).
+template <int KB>
 __device__ __forceinline__ void router_convert(const uint16_t* xsl, float* as, int rows, int RM,
                                                int tid, int NT) {
-  for (int c = tid; c < rows * (LBK / 8); c += NT) {
+  for (int c = tid; c < rows * (KB / 8); c += NT) {
     const int m = c % rows, q = c / rows;
     const int pos = (m / kRTM) * kRPad + m % kRTM;
-    const uint4 v = *reinterpret_cast<const uint4*>(xsl + m * LBK + q * 8);
+    const uint4 v = *reinterpret_cast<const uint4*>(xsl + m * KB + q * 8);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -111,12 +112,12 @@ __device__ __forceinline__ void router_convert(const uint16_t* xsl, float* as, i
 }
 
 // One stage of the fma chains: acc[i][j] += x[token i][k] * W_r[k][expert j]
-// for k ascending over the stage.
-template <int BN>
+// for k ascending over the KB values of the stage.
+template <int BN, int KB>
 __device__ __forceinline__ void router_fma_stage(float (&acc)[kRTM][kRTN], const float* as,
                                                  const float* bsl, int RM, int ty, int tx) {
 #pragma unroll
-  for (int kk = 0; kk < LBK; ++kk) {
+  for (int kk = 0; kk < KB; ++kk) {
     const float4 a0 = *reinterpret_cast<const float4*>(&as[kk * RM + ty * kRPad]);
     const float4 a1 = *reinterpret_cast<const float4*>(&as[kk * RM + ty * kRPad + 4]);
     const float4 b = *reinterpret_cast<const float4*>(&bsl[kk * BN + tx * kRTN]);
@@ -209,26 +210,27 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_kernel(
     asm volatile("cp.async.wait_group %0;" ::"n"(LSTAGES - 2) : "memory");
     __syncthreads();  // stage kt landed; every thread is done with stage kt-1 and with `as`
     issue(kt + LSTAGES - 1);
-    router_convert(xs + (size_t)(kt % LSTAGES) * bm * LBK, as, rows, RM, tid, NT);
+    router_convert<LBK>(xs + (size_t)(kt % LSTAGES) * bm * LBK, as, rows, RM, tid, NT);
     __syncthreads();
-    router_fma_stage<BN>(acc, as, bs + (size_t)(kt % LSTAGES) * LBK * BN, RM, ty, tx);
+    router_fma_stage<BN, LBK>(acc, as, bs + (size_t)(kt % LSTAGES) * LBK * BN, RM, ty, tx);
   }
   router_store(acc, logits, bias, m0, rows, n0, E, ty, tx);
 }
 
-// Shared-memory layout of the TMA form: LSTAGES stages of [x tile bm x BK
+// Shared-memory layout of the TMA form: NS stages of [x tile bm x KB
 // bf16, padded to 128 B | W_r tile BK x BN fp32], two fp32 x tiles, the stage
 // barriers.
 struct RouterTmaLayout {
   uint32_t xbytes, stage, as_off, bar_off, total;
 };
+template <int KB, int NS>
 __host__ __device__ inline RouterTmaLayout router_tma_layout(int bm, int bn, int ty) {
   RouterTmaLayout L;
-  L.xbytes = ((uint32_t)bm * LBK * 2 + 127u) & ~127u;
-  L.stage = L.xbytes + (uint32_t)LBK * bn * 4;
-  L.as_off = LSTAGES * L.stage;
-  L.bar_off = L.as_off + 2u * LBK * ty * kRPad * 4;
-  L.total = L.bar_off + LSTAGES * 8 + 128;  // + slack for aligning the base to 128 B
+  L.xbytes = ((uint32_t)bm * KB * 2 + 127u) & ~127u;
+  L.stage = L.xbytes + (uint32_t)KB * bn * 4;
+  L.as_off = NS * L.stage;
+  L.bar_off = L.as_off + 2u * KB * ty * kRPad * 4;
+  L.total = L.bar_off + NS * 8 + 128;  // + slack for aligning the base to 128 B
   return L;
 }
 
@@ -241,7 +243,7 @@ __host__ __device__ inline RouterTmaLayout router_tma_layout(int bm, int bn, int
 // x tile the next conversion overwrites. Waits are bounded; a CTA that runs
 // out of time records kErrWaitRouter, waits (bounded) for its copies in
 // flight and leaves without writing logits.
-template <int TX>
+template <int TX, int KB, int NS>
 __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
     const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
     const float* __restrict__ bias, float* __restrict__ logits, int Nmax,
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
   const int m0 = blockIdx.y * bm;
   if (m0 >= N) return;
   const int rows = min(bm, N - m0);
-  const RouterTmaLayout L = router_tma_layout(bm, BN, TY);
+  const RouterTmaLayout L = router_tma_layout<KB, NS>(bm, BN, TY);
   extern __shared__ __align__(16) uint8_t rsm_raw[];
   uint8_t* rsm = rsm_raw + ((128u - (smem_u32(rsm_raw) & 127u)) & 127u);
   const uint32_t sbase = smem_u32(rsm);
@@ -264,30 +266,30 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
   const int tx = (warp % (TX / 8)) * 8 + (lane & 7);
   const int ty = (warp / (TX / 8)) * 4 + (lane >> 3);
   const int n0 = blockIdx.x * BN;
-  const int KT = H / LBK;
-  const uint32_t tx_bytes = (uint32_t)bm * LBK * 2 + (uint32_t)LBK * BN * 4;
-  for (int i = tid; i < 2 * LBK * RM; i += NT) as[i] = 0.0f;
+  const int KT = H / KB;
+  const uint32_t tx_bytes = (uint32_t)bm * KB * 2 + (uint32_t)KB * BN * 4;
+  for (int i = tid; i < 2 * KB * RM; i += NT) as[i] = 0.0f;
   if (tid == 0) {
     tma_prefetch_desc(&tmx);
     tma_prefetch_desc(&tmw);
-    for (int st = 0; st < LSTAGES; ++st) mbar_init(bar0 + 8u * st, 1);
+    for (int st = 0; st < NS; ++st) mbar_init(bar0 + 8u * st, 1);
     mbar_fence_init();
   }
   __syncthreads();
   uint64_t pol_x = 0, pol_w = 0;
   int issued = 0;
   auto issue = [&](int kt) {  // thread 0 only
-    const int slot = kt % LSTAGES;
+    const int slot = kt % NS;
     const uint32_t st = sbase + (uint32_t)slot * L.stage, bar = bar0 + 8u * slot;
     mbar_arrive_expect_tx(bar, tx_bytes);
-    tma_load_2d(st, &tmx, kt * LBK, m0, bar, pol_x);
-    tma_load_2d(st + L.xbytes, &tmw, n0, kt * LBK, bar, pol_w);
+    tma_load_2d(st, &tmx, kt * KB, m0, bar, pol_x);
+    tma_load_2d(st + L.xbytes, &tmw, n0, kt * KB, bar, pol_w);
     ++issued;
   };
   if (tid == 0) {
     pol_x = policy_evict_first();
     pol_w = policy_evict_last();
-    for (int kt = 0; kt < LSTAGES - 1 && kt < KT; ++kt) issue(kt);
+    for (int kt = 0; kt < NS - 1 && kt < KT; ++kt) issue(kt);
   }
   float acc[kRTM][kRTN];
 #pragma unroll
@@ -298,22 +300,22 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
   bool ok = mbar_wait(bar0, 0u, err, kErrWaitRouter);
   if (ok) {
     ++waited;
-    router_convert(reinterpret_cast<const uint16_t*>(rsm), as, rows, RM, tid, NT);
+    router_convert<KB>(reinterpret_cast<const uint16_t*>(rsm), as, rows, RM, tid, NT);
   }
   for (int kt = 0; kt < KT; ++kt) {
     if (!__syncthreads_and(ok)) break;
-    if (tid == 0 && kt + LSTAGES - 1 < KT) issue(kt + LSTAGES - 1);
-    const int slot = kt % LSTAGES;
-    router_fma_stage<BN>(acc, as + (kt & 1) * LBK * RM,
+    if (tid == 0 && kt + NS - 1 < KT) issue(kt + NS - 1);
+    const int slot = kt % NS;
+    router_fma_stage<BN, KB>(acc, as + (kt & 1) * KB * RM,
                          reinterpret_cast<const float*>(rsm + (size_t)slot * L.stage + L.xbytes),
                          RM, ty, tx);
     if (kt + 1 < KT) {
-      const int ns = (kt + 1) % LSTAGES;
-      ok = mbar_wait(bar0 + 8u * ns, (uint32_t)((kt + 1) / LSTAGES) & 1u, err, kErrWaitRouter);
+      const int ns = (kt + 1) % NS;
+      ok = mbar_wait(bar0 + 8u * ns, (uint32_t)((kt + 1) / NS) & 1u, err, kErrWaitRouter);
       if (ok) {
         ++waited;
-        router_convert(reinterpret_cast<const uint16_t*>(rsm + (size_t)ns * L.stage),
-                       as + ((kt + 1) & 1) * LBK * RM, rows, RM, tid, NT);
+        router_convert<KB>(reinterpret_cast<const uint16_t*>(rsm + (size_t)ns * L.stage),
+                       as + ((kt + 1) & 1) * KB * RM, rows, RM, tid, NT);
       }
     }
   }
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
     // out of time: let this CTA's copies in flight land before leaving
     if (tid == 0)
       for (int st = waited; st < issued; ++st)
-        if (!mbar_wait(bar0 + 8u * (st % LSTAGES), (uint32_t)(st / LSTAGES) & 1u, err,
+        if (!mbar_wait(bar0 + 8u * (st % NS), (uint32_t)(st / NS) & 1u, err,
                        kErrWaitRouter))
           break;
     return;
@@ -423,9 +425,13 @@ cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaS
     err = cudaFuncSetAttribute(router_logits_kernel<TX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)router_smem_bytes(kTyMax * kRTM, BN, kTyMax));
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(router_logits_tma_kernel<TX>,
+    err = cudaFuncSetAttribute(router_logits_tma_kernel<TX, 32, 4>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)router_tma_layout(kTyMax * kRTM, BN, kTyMax).total);
+                               (int)router_tma_layout<32, 4>(kTyMax * kRTM, BN, kTyMax).total);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(router_logits_tma_kernel<TX, 64, 2>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)router_tma_layout<64, 2>(kTyMax * kRTM, BN, kTyMax).total);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) set_for[dev] = 1;
   }
@@ -433,14 +439,25 @@ cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaS
   // TMA form: W_r rows a multiple of 16 bytes, boxes inside the tensors
   const bool tma = vec4 && a.E >= BN && a.err &&
                    (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0;
+  // stages of 64 contraction elements, two deep, for long rows (measured:
+  // dsv3's router 0.40 -> 0.37 ms); 32 x 4 for shorter ones (H = 2048:
+  // 0.167 vs 0.188 ms)
+  const bool wide = a.H >= 4096;
+  const uint32_t kb = wide ? 64u : 32u;
   CUtensorMap tmx, tmw;
   if (tma &&
       make_map_plain(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, (uint64_t)a.H, (uint64_t)a.N,
-                     LBK, (uint32_t)bm) &&
+                     kb, (uint32_t)bm) &&
       make_map_plain(&tmw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.wr, (uint64_t)a.E,
-                     (uint64_t)a.H, BN, LBK)) {
-    launch_pdl(router_logits_tma_kernel<TX>, dim3(g), dim3(ty * TX), router_tma_layout(bm, BN, ty).total, s, 
-        tmx, tmw, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, bm, a.err);
+                     (uint64_t)a.H, BN, kb)) {
+    if (wide)
+      launch_pdl(router_logits_tma_kernel<TX, 64, 2>, dim3(g), dim3(ty * TX),
+                 router_tma_layout<64, 2>(bm, BN, ty).total, s, tmx, tmw, a.bias, a.ws.logits, a.N,
+                 a.n_dev, a.H, a.E, bm, a.err);
+    else
+      launch_pdl(router_logits_tma_kernel<TX, 32, 4>, dim3(g), dim3(ty * TX),
+                 router_tma_layout<32, 4>(bm, BN, ty).total, s, tmx, tmw, a.bias, a.ws.logits, a.N,
+                 a.n_dev, a.H, a.E, bm, a.err);
   } else {
     launch_pdl(router_logits_kernel<TX>, dim3(g), dim3(ty * TX), router_smem_bytes(bm, BN, ty), s, 
         a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, bm, vec4);
