@@ -362,29 +362,49 @@ def run_reference(args):
     w = synth.WORKLOADS[args.workload]
     x_bits, wr, bias = host_inputs(w, w.seed)
     train = w.cap_num == 0
-    if train:  # dropless training step: routing + expert-path backward on a route sample
+    dy_bits = None
+    if train:
         dy_bits = synth.normal_bf16_bits(w.seed, synth.STREAM["dy"], 0, w.n_tokens * w.hidden,
                                          1.0).reshape(w.n_tokens, w.hidden)
 
-        def sample(i):
-            return time_oracle_train_sample(w, x_bits, dy_bits, wr, bias, args.block_m, n_routes=1024,
-                                            seed=i)
-    elif args.fp8:
-        def sample(i):
-            return time_oracle_sample_fp8(w, x_bits, wr, bias, args.block_m, 1, seed_experts=i)
-    else:
-        n_exp = max(1, min(4, args.cpu_experts))
+    def sample(i, n):
+        """One bounded sample on the first n tokens of the batch, taken as a
+        batch of their own (per-token oracle work does not depend on N)."""
+        wn, xn = w.with_tokens(n), x_bits[:n]
+        if train:  # dropless training step: routing + expert-path backward on a route sample
+            return time_oracle_train_sample(wn, xn, dy_bits[:n], wr, bias, args.block_m,
+                                            n_routes=1024, seed=i)
+        if args.fp8:
+            return time_oracle_sample_fp8(wn, xn, wr, bias, args.block_m, 1, seed_experts=i)
+        return time_oracle_sample(wn, xn, wr, bias, args.block_m, max(1, min(4, args.cpu_experts)),
+                                  seed_experts=i)
 
-        def sample(i):
-            return time_oracle_sample(w, x_bits, wr, bias, args.block_m, n_exp, seed_experts=i)
+    # the whole run stays near two minutes of oracle work: a sample that takes
+    # longer than its share shrinks the token count of the following ones
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_tok = w.n_tokens
+
+    def run_one(i):
+        nonlocal n_tok
+        out = sample(i, n_tok)
+        if out[2] > budget and n_tok > 64:
+            n_tok = max(64, int(n_tok * budget / out[2]) // 64 * 64)
+        return out
+
     for i in range(args.warmup):
-        sample(i)
-    vals, secs = [], 0.0
+        run_one(i)
+    vals, secs, descs = [], 0.0, []
     t_start = time.perf_counter()
     for i in range(args.steps):
-        v, desc, s, cores = sample(i)
+        n_used = n_tok
+        v, desc, s, cores = run_one(i)
         vals.append(v)
         secs += s
+        descs.append((n_used, desc))
+    desc = descs[-1][1]
+    if descs[-1][0] < w.n_tokens:
+        desc = ("first %d of the %d tokens as a batch of their own (work per token does not "
+                "depend on N): %s" % (descs[-1][0], w.n_tokens, desc))
     wall = time.perf_counter() - t_start
     value = len(vals) / sum(1.0 / v for v in vals)  # tokens over total extrapolated time
     out = {
