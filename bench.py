@@ -1032,17 +1032,55 @@ def run_ours_serve(args):
         raise RuntimeError("device error word set during the timed region")
     tokens = sum(sizes) * world
 
-    # end to end through the ladder: each batch's x[:n] from pinned host memory in, y[:n] out
+    # end to end through the ladder: each batch's x[:n] comes from pinned host
+    # memory and its y[:n] goes back to it. The ladder's graphs are bound to its
+    # own x and y buffers, so the host copies go through two staging buffers on
+    # a copy stream (batch i+2's x and batch i's y move under the forwards in
+    # between) and device copies on the compute stream move the rows in and out.
     xh = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    yh = torch.empty((Ntop, H), dtype=torch.bfloat16).pin_memory()
+    yh = [torch.empty((Ntop, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    bfd = dict(dtype=torch.bfloat16, device=dev)
+    xs = [torch.empty((Ntop, H), **bfd) for _ in range(2)]
+    ys = [torch.empty((Ntop, H), **bfd) for _ in range(2)]
+    cstream = torch.cuda.Stream(dev)
+    h2d = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e(n):
-        L.x[:n].copy_(xh[:n], non_blocking=True)
-        L.forward(n)
-        yh[:n].copy_(L.y[:n], non_blocking=True)
+    def e2e_pass(start_evt):
+        cstream.wait_event(start_evt)
+        with torch.cuda.stream(cstream):
+            for b in range(min(2, len(sizes))):
+                xs[b][:sizes[b]].copy_(xh[:sizes[b]], non_blocking=True)
+                h2d[b].record(cstream)
+        for i, n in enumerate(sizes):
+            b = i % 2
+            stream.wait_event(h2d[b])
+            L.x[:n].copy_(xs[b][:n], non_blocking=True)
+            L.forward(n)
+            ys[b][:n].copy_(L.y[:n], non_blocking=True)
+            done[b].record(stream)
+            cstream.wait_event(done[b])
+            with torch.cuda.stream(cstream):
+                yh[b][:n].copy_(ys[b][:n], non_blocking=True)
+                if i + 2 < len(sizes):
+                    m = sizes[i + 2]
+                    xs[b][:m].copy_(xh[:m], non_blocking=True)
+                h2d[b].record(cstream)
+        stream.wait_stream(cstream)
 
-    run(e2e)
-    ms_e2e, _ = run(e2e, reps)
+    w0 = torch.cuda.Event()
+    w0.record(stream)
+    e2e_pass(w0)
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(reps):
+        e2e_pass(ea)
+    eb.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    ms_e2e = max_over_ranks(ea.elapsed_time(eb), dist, dev) / reps
     out = {
         "metric": METRIC_SERVE, "value": tokens / (ms_ladder / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": reps, "warmup": args.warmup, "ms_per_step": ms_ladder, "higher_is_better": True,
@@ -1053,7 +1091,10 @@ def run_ours_serve(args):
                    "step": "one pass over the request sequence"},
         "gpu_launches": launches,
         "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": sum(sizes) * H * 2, "d2h_bytes_per_step": sum(sizes) * H * 2},
+                "h2d_bytes_per_step": sum(sizes) * H * 2, "d2h_bytes_per_step": sum(sizes) * H * 2,
+                "copies": "pinned host x in and y out for every batch through two staging buffers on "
+                          "a second stream (overlapping the neighbouring batches), device copies "
+                          "into and out of the ladder's buffers"},
         "eager": {"value": tokens / (ms_eager / 1e3), "ms_per_step": ms_eager,
                   "host_wall_ms_per_step": wall_eager * 1e3},
         "ladder_host_wall_ms_per_step": wall_ladder * 1e3,
