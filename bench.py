@@ -1088,7 +1088,9 @@ def run_ours_serve(args):
         "config": {"workload": w.name, "description": w.note, "top_bucket": Ntop, "buckets": buckets,
                    "max_pad_ratio": args.pad_ratio, "batches": len(sizes), "tokens_per_step": sum(sizes),
                    "batch_sizes": sizes, "parallelism": "replicas" if world > 1 else "single GPU",
-                   "step": "one pass over the request sequence"},
+                   "step": "one pass over the request sequence",
+                   "l2": "inputs larger than L2 (%.2f GB of expert weights); no flush"
+                         % ((w13.numel() + w2.numel()) * 2 / 1e9)},
         "gpu_launches": launches,
         "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": sum(sizes) * H * 2, "d2h_bytes_per_step": sum(sizes) * H * 2,
