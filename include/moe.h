@@ -38,6 +38,11 @@
  *    arguments are rejected before any launch; unsupported shapes fail closed
  *    (never a silent fallback), as [FC] Changelog / Known limitations does.
  *  - `stream` is the CUDA stream all work is queued on (0 = legacy default).
+ *  - The forward-path kernels are launched with programmatic stream
+ *    serialization: each may start its on-chip setup while the previous
+ *    kernel in the stream drains, and waits for that kernel to complete
+ *    before its first global-memory access, so stream order semantics hold.
+ *    Stream capture records these as programmatic edges.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
