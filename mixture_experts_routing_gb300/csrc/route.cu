@@ -94,14 +94,18 @@ constexpr size_t router_smem_bytes(int bm, int bn, int ty) {
 }
 
 // Converts stage rows [0, rows) of bf16 x ([row][KB]) into the transposed
-// fp32 tile `as` ([KB][RM], token m at (m/7)*8 + m%7).
-template <int KB>
+// fp32 tile `as` ([KB][RM], token m at (m/7)*8 + m%7). With kSw128 the rows
+// (KB = 64: 128 bytes) are 128-byte swizzled, 16-byte chunk q of row m at
+// m*128 + ((q ^ (m % 8)) * 16), so the consecutive rows a warp reads fall on
+// distinct banks.
+template <int KB, bool kSw128 = false>
 __device__ __forceinline__ void router_convert(const uint16_t* xsl, float* as, int rows, int RM,
                                                int tid, int NT) {
   for (int c = tid; c < rows * (KB / 8); c += NT) {
     const int m = c % rows, q = c / rows;
     const int pos = (m / kRTM) * kRPad + m % kRTM;
-    const uint4 v = *reinterpret_cast<const uint4*>(xsl + m * KB + q * 8);
+    const int qs = kSw128 ? (q ^ (m & 7)) : q;
+    const uint4 v = *reinterpret_cast<const uint4*>(xsl + m * KB + qs * 8);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -226,11 +230,13 @@ struct RouterTmaLayout {
 template <int KB, int NS>
 __host__ __device__ inline RouterTmaLayout router_tma_layout(int bm, int bn, int ty) {
   RouterTmaLayout L;
-  L.xbytes = ((uint32_t)bm * KB * 2 + 127u) & ~127u;
+  // a 128-byte-swizzled x tile (KB = 64) starts on a 1024-byte boundary
+  constexpr uint32_t kAlign = KB == 64 ? 1024u : 128u;
+  L.xbytes = ((uint32_t)bm * KB * 2 + kAlign - 1u) & ~(kAlign - 1u);
   L.stage = L.xbytes + (uint32_t)KB * bn * 4;
   L.as_off = NS * L.stage;
   L.bar_off = L.as_off + 2u * KB * ty * kRPad * 4;
-  L.total = L.bar_off + NS * 8 + 128;  // + slack for aligning the base to 128 B
+  L.total = L.bar_off + NS * 8 + kAlign;  // + slack for aligning the base
   return L;
 }
 
@@ -258,7 +264,8 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
   const int rows = min(bm, N - m0);
   const RouterTmaLayout L = router_tma_layout<KB, NS>(bm, BN, TY);
   extern __shared__ __align__(16) uint8_t rsm_raw[];
-  uint8_t* rsm = rsm_raw + ((128u - (smem_u32(rsm_raw) & 127u)) & 127u);
+  constexpr uint32_t kAlign = KB == 64 ? 1024u : 128u;
+  uint8_t* rsm = rsm_raw + ((kAlign - (smem_u32(rsm_raw) & (kAlign - 1u))) & (kAlign - 1u));
   const uint32_t sbase = smem_u32(rsm);
   float* as = reinterpret_cast<float*>(rsm + L.as_off);  // [2][BK][RM]
   const uint32_t bar0 = sbase + L.bar_off;
@@ -300,7 +307,7 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
   bool ok = mbar_wait(bar0, 0u, err, kErrWaitRouter);
   if (ok) {
     ++waited;
-    router_convert<KB>(reinterpret_cast<const uint16_t*>(rsm), as, rows, RM, tid, NT);
+    router_convert<KB, KB == 64>(reinterpret_cast<const uint16_t*>(rsm), as, rows, RM, tid, NT);
   }
   for (int kt = 0; kt < KT; ++kt) {
     if (!__syncthreads_and(ok)) break;
@@ -314,7 +321,7 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
       ok = mbar_wait(bar0 + 8u * ns, (uint32_t)((kt + 1) / NS) & 1u, err, kErrWaitRouter);
       if (ok) {
         ++waited;
-        router_convert<KB>(reinterpret_cast<const uint16_t*>(rsm + (size_t)ns * L.stage),
+        router_convert<KB, KB == 64>(reinterpret_cast<const uint16_t*>(rsm + (size_t)ns * L.stage),
                        as + ((kt + 1) & 1) * KB * RM, rows, RM, tid, NT);
       }
     }
@@ -447,7 +454,8 @@ cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaS
   CUtensorMap tmx, tmw;
   if (tma &&
       make_map_plain(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, (uint64_t)a.H, (uint64_t)a.N,
-                     kb, (uint32_t)bm) &&
+                     kb, (uint32_t)bm,
+                     wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE) &&
       make_map_plain(&tmw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.wr, (uint64_t)a.E,
                      (uint64_t)a.H, BN, kb)) {
     if (wide)

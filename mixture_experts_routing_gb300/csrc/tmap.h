@@ -34,12 +34,15 @@ inline bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t r
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D tensor [rows, cols] row-major of `dtype` (elem_bytes each), plain
-// (unswizzled) boxes of box_cols x box_rows; out-of-bounds elements read as
-// zero. The row pitch cols*elem_bytes must be a multiple of 16.
+// 2-D tensor [rows, cols] row-major of `dtype` (elem_bytes each), boxes of
+// box_cols x box_rows, unswizzled unless `swizzle` says otherwise (128-byte
+// swizzle: box rows of 128 bytes, 16-byte chunk q of row r at
+// r*128 + ((q ^ (r % 8)) * 16)); out-of-bounds elements read as zero. The row
+// pitch cols*elem_bytes must be a multiple of 16.
 inline bool make_map_plain(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t elem_bytes,
                            const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                           uint32_t box_rows) {
+                           uint32_t box_rows,
+                           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn || (cols * elem_bytes) % 16 != 0) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -47,8 +50,8 @@ inline bool make_map_plain(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t e
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // MN-major operand tiles in one copy: a 3-D view of a bf16 [rows, cols]
