@@ -318,8 +318,9 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
                      void* dx, float* dw13, float* dw2, float* dprob, void* workspace,
                      size_t ws_bytes, cudaStream_t stream);
 
-/* Bytes of scratch moe_router_backward needs: N*E*4 for the logit gradient
- * plus the per-split partial sums of dW_r (about two CTA tiles per SM). */
+/* Bytes of scratch moe_router_backward needs: the logit gradient (N*E*4), its
+ * bf16 split copy (N*C*2) and W_r's (H*C*2), C = 2*E rounded up to 128, and
+ * the per-split partial sums of dW_r (one wave of CTA tiles). */
 int64_t moe_router_backward_workspace_bytes(const moe_config_t* cfg);
 
 /* Router backward: the gradient of the routing probabilities p' (dprob, e.g.
@@ -339,11 +340,17 @@ int64_t moe_router_backward_workspace_bytes(const moe_config_t* cfg);
  *             (moe_route_workspace_logits), valid while that workspace is
  *             untouched; or NULL to recompute them (bit-identical either way)
  *  dprob      [N,K] f32 d loss / d p'
- *  dx         [N,H] bf16, in/out: dx += dl . W_r^T, summed in fp32 and rounded
- *             to bf16 once (add the router's path to the experts' dX)
+ *  dx         [N,H] bf16, in/out, 16-byte aligned: dx += dl . W_r^T, summed in
+ *             fp32 and rounded to bf16 once (add the router's path to the
+ *             experts' dX)
  *  dw_router  [H,E] f32 output: sum_t x[t,:]^T dl[t,:]
  *  dbias      [E] f32 output sum_t dl[t,:], or NULL
- * Outputs other than dx are overwritten. fp32 throughout; deterministic. */
+ * Outputs other than dx are overwritten. dl is computed in fp32; the two
+ * contractions run on the tensor cores with dl and W_r each carried as a pair
+ * of bf16 values (hi = bf16(v), lo = bf16(v - hi), 16 significant bits) and
+ * fp32 accumulation, so they match fp32 sums up to accumulation order
+ * (dx: hi.hi + lo.hi + hi.lo; dW_r: x.hi + x.lo, x being bf16); dbias is an
+ * fp32 sum. Deterministic. x and dx misaligned: MOE_ERR_INVALID_ARG. */
 int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
                         const float* w_router, const float* bias, const float* logits,
                         const float* dprob, void* dx, float* dw_router, float* dbias,

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ["route.cu", "gemm.cu", "wgrad.cu", "combine.cu", "moe_abi.cu", "ladder.cu"]
+SOURCES = ["route.cu", "router_mma.cu", "gemm.cu", "wgrad.cu", "combine.cu", "moe_abi.cu",
+           "ladder.cu"]
 HEADERS = ["ptx.cuh", "moe_internal.h", "tmap.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

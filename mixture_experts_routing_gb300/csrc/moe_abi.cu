@@ -525,21 +525,30 @@ int moe_ffn_backward(const moe_config_t* cfg, const moe_routes_t* routes, const 
   return finish(launched);
 }
 
-static void router_bwd_layout(const moe_config_t* c, size_t* dl_off, size_t* part_off,
-                              size_t* total) {
+// Router-backward workspace: dl [N,E] f32, its split copy [N,C] bf16, W_r's
+// split copy [H,C] bf16 (C = moe::router_split_cols(E)), the dW_r partials
+// [splits,H,E] f32; each region 256-byte aligned.
+struct RouterBwdLayout {
+  size_t dl, dls, wrs, part, total;
+};
+
+static RouterBwdLayout router_bwd_layout(const moe_config_t* c) {
   const int64_t N = c->n_tokens, H = c->hidden, E = c->n_experts;
-  const int splits = N > 0 ? moe::router_bwd_splits((int)N, (int)H, (int)E) : 0;
-  *dl_off = 0;
-  *part_off = (size_t)((N * E * 4 + 255) / 256 * 256);
-  *total = *part_off + (size_t)((splits * H * E * 4 + 255) / 256 * 256);
+  const int64_t C = moe::router_split_cols((int)E);
+  const int64_t splits = N > 0 ? moe::router_bwd_splits((int)N, (int)H, (int)E) : 0;
+  RouterBwdLayout L{};
+  L.dl = 0;
+  L.dls = L.dl + (size_t)roundup(N * E * 4, 256);
+  L.wrs = L.dls + (size_t)roundup(N * C * 2, 256);
+  L.part = L.wrs + (size_t)roundup(H * C * 2, 256);
+  L.total = L.part + (size_t)roundup(splits * H * E * 4, 256);
+  return L;
 }
 
 int64_t moe_router_backward_workspace_bytes(const moe_config_t* cfg) {
   const int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
-  size_t a, b, t;
-  router_bwd_layout(cfg, &a, &b, &t);
-  return (int64_t)t;
+  return (int64_t)router_bwd_layout(cfg).total;
 }
 
 const float* moe_route_workspace_logits(const moe_config_t* cfg, const void* workspace) {
@@ -556,11 +565,10 @@ int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, con
   if (rc != MOE_OK) return rc;
   if (cfg->n_valid) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!routes || !routes->topk_ids || !w_router || !dw_router) return MOE_ERR_INVALID_ARG;
-  size_t dl_off, part_off, total;
-  router_bwd_layout(cfg, &dl_off, &part_off, &total);
-  if (cfg->n_tokens > 0 && (!workspace || ws_bytes < total || !aligned16(workspace)))
+  const RouterBwdLayout L = router_bwd_layout(cfg);
+  if (cfg->n_tokens > 0 && (!workspace || ws_bytes < L.total || !aligned16(workspace)))
     return MOE_ERR_WORKSPACE;
-  if (cfg->n_tokens > 0 && (!x || !dprob || !dx || !aligned16(x)))
+  if (cfg->n_tokens > 0 && (!x || !dprob || !dx || !aligned16(x) || !aligned16(dx)))
     return MOE_ERR_INVALID_ARG;
   if (cfg->n_tokens == 0) {  // no token: zero gradients
     if (cudaMemsetAsync(dw_router, 0, (size_t)cfg->hidden * cfg->n_experts * 4, stream) !=
@@ -584,8 +592,10 @@ int moe_router_backward(const moe_config_t* cfg, const moe_routes_t* routes, con
   a.topk_ids = routes->topk_ids;
   a.dprob = dprob;
   a.logits = logits;
-  a.dl = reinterpret_cast<float*>(ws + dl_off);
-  a.part = reinterpret_cast<float*>(ws + part_off);
+  a.dl = reinterpret_cast<float*>(ws + L.dl);
+  a.dls = reinterpret_cast<uint16_t*>(ws + L.dls);
+  a.wrs = reinterpret_cast<uint16_t*>(ws + L.wrs);
+  a.part = reinterpret_cast<float*>(ws + L.part);
   a.dwr = dw_router;
   a.dbias = dbias;
   a.dx = static_cast<uint16_t*>(dx);

@@ -131,9 +131,11 @@ struct WgradArgs {
 
 int launch_wgrad(const WgradArgs& a, cudaStream_t s);
 
-// Router backward (route.cu): logits recomputed into dl, dl = d loss / d logits
-// from dprob, then dW_r (split over tokens, partials in part), dbias, and
-// dx += dl . W_r^T (bf16 in/out).
+// Router backward (route.cu, router_mma.cu): logits recomputed into dl,
+// dl = d loss / d logits from dprob (fp32, plus its bf16 hi/lo split copy dls),
+// then dW_r on the tensor cores (split over tokens, partials in part), dbias,
+// and dx += dl . W_r^T on the tensor cores (W_r's split copy in wrs; bf16
+// in/out).
 struct RouterBwdArgs {
   int N, H, E, K, renorm;
   uint32_t* err;                // device error word (bounded waits)
@@ -144,13 +146,23 @@ struct RouterBwdArgs {
   const int32_t* topk_ids;
   const float* dprob;
   float* dl;        // [N,E] workspace
+  uint16_t* dls;    // [N, router_split_cols(E)] workspace: bf16 hi | lo of dl
+  uint16_t* wrs;    // [H, router_split_cols(E)] workspace: bf16 hi | lo of W_r
   float* part;      // [splits,H,E] workspace
   float* dwr;       // [H,E]
   float* dbias;     // [E] or null
   uint16_t* dx;     // [N,H] bf16, accumulated
 };
-int router_bwd_splits(int N, int H, int E);
 int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s);
+// router_mma.cu: columns of a split copy (2 * E rounded up to 64), the token
+// splits of dW_r (a function of the shape only), and the launches
+int router_split_cols(int E);
+int router_bwd_splits(int N, int H, int E);
+int launch_router_split_w(const float* wr, int H, int E, uint16_t* wrs, cudaStream_t s);
+int launch_router_dwr_mma(const uint16_t* x, const uint16_t* dls, int N, int H, int E,
+                          float* part, uint32_t* err, cudaStream_t s);
+int launch_router_dx_mma(const uint16_t* dls, const uint16_t* wrs, int N, int H, int E,
+                         uint16_t* dx, uint32_t* err, cudaStream_t s);
 
 // Backward helpers (combine.cu).
 // dX[t] = sum_k dXr[token_routes[t,k]] (fp32, k order) and

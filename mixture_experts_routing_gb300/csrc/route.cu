@@ -890,14 +890,17 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
 //   renorm: d = sum_k p[e_k], c = sum_k dprob_k p[e_k]/d, g_k = (dprob_k - c)/d
 //   else:   g_k = dprob_k
 //   s = sum_k g_k p[e_k];  dl[e] = p[e] (g[e] - s), g[e] = 0 for the others.
-// dl overwrites the logits.
+// Besides dl it writes the bf16 split copy dls [N, 2*Ep] (Ep = E rounded up to
+// 64): dls[t,e] = hi = bf16(dl), dls[t,Ep+e] = bf16(dl - hi), zero for
+// E <= e < Ep; the tensor-core contractions of the router backward read it.
 constexpr int kDlWarps = 8;
 
 // Reads the logits from `lg` and writes dl to `ld`, which may be the same
 // buffer (each lane reads its entries before it writes them).
 __global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
     const float* lg, float* ld, int N, int E, int K, int renorm,
-    const int32_t* __restrict__ topk_ids, const float* __restrict__ dprob) {
+    const int32_t* __restrict__ topk_ids, const float* __restrict__ dprob,
+    uint16_t* __restrict__ dls, int Ep) {
   __shared__ float pbuf[kDlWarps][kMaxExperts];
   __shared__ float gk_s[kDlWarps][kMaxTopK];
   __shared__ int32_t id_s[kDlWarps][kMaxTopK];
@@ -956,110 +959,24 @@ __global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
   }
   __syncwarp();
   const float sg = s_s[warp];
+  uint16_t* split = dls + (size_t)t * 2 * Ep;
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     const int e = lane + 32 * j;
-    if (e >= E) continue;
-    float g = 0.0f;
-    for (int k = 0; k < K; ++k)
-      if (id_s[warp][k] == e) g = gk_s[warp][k];
-    ld[(size_t)t * E + e] = __fmul_rn(v[j], __fsub_rn(g, sg));
-  }
-}
-
-// dW_r[h,e] = sum_t x[t,h] dl[t,e] over the tokens of one split: 128 rows of
-// h x 64 experts per CTA, 256 threads, a warp covering 4 x 8 threads and a
-// thread 8 rows x 4 experts (three conflict-free 16-byte shared loads per 32
-// fmas); 32 tokens per stage, the next stage's loads held in registers while
-// this stage is computed. Partial sums of split z go to part + z*H*E, each a
-// sequential sum over ascending t within the split. H is a multiple of 128;
-// vec: E a multiple of 4 (16-byte dl loads and partial stores).
-constexpr int kDwH = 128, kDwE = 64, kDwK = 32;
-
-__global__ void __launch_bounds__(256) router_dwr_kernel(const uint16_t* __restrict__ x,
-                                                         const float* __restrict__ dl, int N, int H,
-                                                         int E, int t_per_split, int vec,
-                                                         float* __restrict__ part) {
-  __shared__ __align__(16) float as[2][kDwK][kDwH];
-  __shared__ __align__(16) float bs[2][kDwK][kDwE];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ty = (warp >> 1) * 4 + (lane >> 3);  // rows h0 + 8ty .. +7
-  const int tx = (warp & 1) * 8 + (lane & 7);    // experts e0 + 4tx .. +3
-  const int e0 = blockIdx.x * kDwE, h0 = blockIdx.y * kDwH;
-  const int ta = blockIdx.z * t_per_split, tb = min(N, ta + t_per_split);
-  // this thread's loads of each stage: token rows lk and lk + 16; 8 values of
-  // h from column xc, 4 experts from column dc
-  const int lk = tid / 16, xc = (tid % 16) * 8, dc = (tid % 16) * 4;
-  float ra[2][8], rb[2][4];
-  auto fetch = [&](int t0) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int t = t0 + lk + 16 * r;
-      const bool ok = t < tb;
-      uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-      if (ok) xv = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h0 + xc);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        ra[r][2 * i] = __uint_as_float(xw[i] << 16);
-        ra[r][2 * i + 1] = __uint_as_float(xw[i] & 0xFFFF0000u);
-      }
-      if (vec) {
-        float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ok && e0 + dc < E) dv = *reinterpret_cast<const float4*>(dl + (size_t)t * E + e0 + dc);
-        rb[r][0] = dv.x; rb[r][1] = dv.y; rb[r][2] = dv.z; rb[r][3] = dv.w;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          rb[r][j] = (ok && e0 + dc + j < E) ? dl[(size_t)t * E + e0 + dc + j] : 0.0f;
-      }
+    if (e >= Ep) continue;
+    uint16_t hi = 0, lo = 0;
+    if (e < E) {
+      float g = 0.0f;
+      for (int k = 0; k < K; ++k)
+        if (id_s[warp][k] == e) g = gk_s[warp][k];
+      const float d = __fmul_rn(v[j], __fsub_rn(g, sg));
+      ld[(size_t)t * E + e] = d;
+      const __nv_bfloat16 bh = __float2bfloat16_rn(d);
+      hi = __bfloat16_as_ushort(bh);
+      lo = __bfloat16_as_ushort(__float2bfloat16_rn(__fsub_rn(d, __bfloat162float(bh))));
     }
-  };
-  float acc[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-  if (ta < tb) fetch(ta);
-  int buf = 0;
-  for (int t0 = ta; t0 < tb; t0 += kDwK, buf ^= 1) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      *reinterpret_cast<float4*>(&as[buf][lk + 16 * r][xc]) =
-          make_float4(ra[r][0], ra[r][1], ra[r][2], ra[r][3]);
-      *reinterpret_cast<float4*>(&as[buf][lk + 16 * r][xc + 4]) =
-          make_float4(ra[r][4], ra[r][5], ra[r][6], ra[r][7]);
-      *reinterpret_cast<float4*>(&bs[buf][lk + 16 * r][dc]) =
-          make_float4(rb[r][0], rb[r][1], rb[r][2], rb[r][3]);
-    }
-    __syncthreads();
-    if (t0 + kDwK < tb) fetch(t0 + kDwK);  // next stage's loads overlap this stage's math
-#pragma unroll
-    for (int k = 0; k < kDwK; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&as[buf][k][ty * 8]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&as[buf][k][ty * 8 + 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&bs[buf][k][tx * 4]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
-    }
-  }
-  float* out = part + (size_t)blockIdx.z * H * E;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int h = h0 + ty * 8 + i;
-    const int e = e0 + tx * 4;
-    float* o = out + (size_t)h * E + e;
-    if (vec && e + 3 < E) {
-      *reinterpret_cast<float4*>(o) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (e + j < E) o[j] = acc[i][j];
-    }
+    split[e] = hi;
+    split[Ep + e] = lo;
   }
 }
 
@@ -1088,108 +1005,6 @@ __global__ void __launch_bounds__(256) router_dbias_kernel(const float* __restri
     __syncthreads();
   }
   if (threadIdx.x == 0) dbias[e] = red[0];
-}
-
-// dx[t,h] += sum_e dl[t,e] W_r[h,e] (an fp32 fma chain over ascending e, then
-// added to dx in fp32 and rounded to bf16 once). 64 tokens x 128 rows of W_r
-// per step, 256 threads: a warp covers 4 x 8 threads, a thread 4 tokens x 8
-// rows of W_r (two groups of 4 rows, 64 apart). Both operands are staged
-// transposed, 64 experts at a time (ds[e][t], ws[e][h]), so each step is
-// three conflict-free 16-byte shared loads for 32 fmas; dx is read and written
-// 8 bytes (4 values) at a time. A CTA keeps one 128-row slice of W_r and walks
-// `tiles` consecutive 64-token tiles; with E <= 64 its W_r tile is staged
-// once. H is a multiple of 128.
-constexpr int kDxE = 64, kDxT = 64, kDxH = 128;
-
-__global__ void __launch_bounds__(256) router_dx_kernel(const float* __restrict__ dl,
-                                                        const float* __restrict__ wr, int N, int H,
-                                                        int E, int vec4, int tiles,
-                                                        uint16_t* __restrict__ dx) {
-  __shared__ __align__(16) float ds[kDxE][kDxT];
-  __shared__ __align__(16) float ws_[kDxE][kDxH];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ty = (warp >> 1) * 4 + (lane >> 3);  // tokens 4ty .. 4ty+3
-  const int tx = (warp & 1) * 8 + (lane & 7);    // rows 4tx .. +3 and 64 + 4tx .. +3
-  const int h0 = blockIdx.x * kDxH;
-  for (int tt = 0; tt < tiles; ++tt) {
-  const int t0 = (blockIdx.y * tiles + tt) * kDxT;
-  if (t0 >= N) break;
-  float acc[4][8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-  for (int k0 = 0; k0 < E; k0 += kDxE) {
-    const int ke = min(kDxE, E - k0);
-    // 4 experts of one row per thread and step, written transposed; with
-    // vec4 (E a multiple of 4, 16-byte rows) ke is a multiple of 4 too
-    for (int c = tid; c < kDxT * (kDxE / 4); c += 256) {
-      const int t = c % kDxT, q = (c / kDxT) * 4;
-      float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (t0 + t < N && q < ke) {
-        const float* src = dl + (size_t)(t0 + t) * E + k0 + q;
-        if (vec4) {
-          const float4 f = *reinterpret_cast<const float4*>(src);
-          v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = (q + j < ke) ? src[j] : 0.0f;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) ds[q + j][t] = v[j];
-    }
-    for (int c = tid; c < kDxH * (kDxE / 4) && (tt == 0 || E > kDxE); c += 256) {
-      const int h = c % kDxH, q = (c / kDxH) * 4;
-      float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (q < ke) {
-        const float* src = wr + (size_t)(h0 + h) * E + k0 + q;
-        if (vec4) {
-          const float4 f = *reinterpret_cast<const float4*>(src);
-          v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = (q + j < ke) ? src[j] : 0.0f;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) ws_[q + j][h] = v[j];
-    }
-    __syncthreads();
-    for (int k = 0; k < ke; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(&ds[k][ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&ws_[k][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&ws_[k][64 + tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
-    if (t >= N) continue;
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      uint2* q = reinterpret_cast<uint2*>(dx + (size_t)t * H + h0 + g * 64 + tx * 4);
-      const uint2 old = *q;
-      const uint32_t w[2] = {old.x, old.y};
-      uint32_t out[2];
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const float lo = __fadd_rn(__uint_as_float(w[m] << 16), acc[i][g * 4 + 2 * m]);
-        const float hi = __fadd_rn(__uint_as_float(w[m] & 0xFFFF0000u), acc[i][g * 4 + 2 * m + 1]);
-        out[m] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
-      }
-      *q = make_uint2(out[0], out[1]);
-    }
-  }
-  }
 }
 
 }  // namespace
@@ -1232,14 +1047,6 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   return launched;
 }
 
-int router_bwd_splits(int N, int H, int E) {
-  const int tiles = ((E + kDwE - 1) / kDwE) * (H / kDwH);
-  int splits = (2 * 152 + tiles - 1) / tiles;  // about two CTAs per SM
-  const int max_splits = (N + 255) / 256;      // at least 256 tokens per split
-  if (splits > max_splits) splits = max_splits;
-  return splits < 1 ? 1 : splits;
-}
-
 int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
   if (a.N <= 0) return 0;
   int launched = 0;
@@ -1260,16 +1067,18 @@ int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
     if (err != cudaSuccess) return -(int)err;
     ++launched;
   }
+  // W_r's split copy does not depend on dl
+  int rc = launch_router_split_w(a.wr, a.H, a.E, a.wrs, s);
+  if (rc < 0) return rc;
+  launched += rc;
   router_dlogits_kernel<<<(a.N + kDlWarps - 1) / kDlWarps, kDlWarps * 32, 0, s>>>(
-      a.logits ? a.logits : a.dl, a.dl, a.N, a.E, a.K, a.renorm, a.topk_ids, a.dprob);
+      a.logits ? a.logits : a.dl, a.dl, a.N, a.E, a.K, a.renorm, a.topk_ids, a.dprob, a.dls,
+      router_split_cols(a.E) / 2);
   ++launched;
+  rc = launch_router_dwr_mma(a.x, a.dls, a.N, a.H, a.E, a.part, a.err, s);
+  if (rc < 0) return rc;
+  launched += rc;
   const int splits = router_bwd_splits(a.N, a.H, a.E);
-  const int tps = ((a.N + splits - 1) / splits + kDwK - 1) / kDwK * kDwK;
-  dim3 g1((a.E + kDwE - 1) / kDwE, a.H / kDwH, splits);
-  const int dw_vec = (a.H % 4 == 0) && (a.E % 4 == 0) &&
-                     ((reinterpret_cast<uintptr_t>(a.x) & 7u) == 0);
-  router_dwr_kernel<<<g1, 256, 0, s>>>(a.x, a.dl, a.N, a.H, a.E, tps, dw_vec, a.part);
-  ++launched;
   const int64_t n = (int64_t)a.H * a.E;
   router_dwr_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.part, splits, n, a.dwr);
   ++launched;
@@ -1277,20 +1086,9 @@ int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
     router_dbias_kernel<<<a.E, 256, 0, s>>>(a.dl, a.N, a.E, a.dbias);
     ++launched;
   }
-  // about four CTAs per SM, each walking consecutive token tiles
-  int sms_dx = 0;
-  {
-    cudaError_t e2 = cudaSuccess;
-    sms_dx = router_sm_count(&e2);
-    if (sms_dx <= 0) return -(int)(e2 != cudaSuccess ? e2 : cudaErrorUnknown);
-  }
-  const int t_tiles = (a.N + kDxT - 1) / kDxT;
-  const int want_y = (4 * sms_dx + a.H / kDxH - 1) / (a.H / kDxH);
-  const int dx_tiles = (t_tiles + want_y - 1) / want_y;
-  dim3 g2(a.H / kDxH, (t_tiles + dx_tiles - 1) / dx_tiles);
-  const int vec4 = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 15u) == 0);
-  router_dx_kernel<<<g2, 256, 0, s>>>(a.dl, a.wr, a.N, a.H, a.E, vec4, dx_tiles, a.dx);
-  ++launched;
+  rc = launch_router_dx_mma(a.dls, a.wrs, a.N, a.H, a.E, a.dx, a.err, s);
+  if (rc < 0) return rc;
+  launched += rc;
   err = cudaGetLastError();
   return err == cudaSuccess ? launched : -(int)err;
 }
