@@ -38,6 +38,11 @@ SMALL = [
     (synth.Workload("rb_e256", 333, 384, 256, 8, 128, 5, 4), 1),
     # E not a multiple of 4: W_r rows are not 16-byte multiples
     (synth.Workload("rb_e6", 200, 128, 6, 2, 128, 1, 1, zipf_s=0.5), 1),
+    # experts padded to 128 and to 192 split columns (three 64-wide chunks)
+    (synth.Workload("rb_e100", 257, 256, 100, 4, 128, 1, 1), 1),
+    (synth.Workload("rb_e160", 190, 128, 160, 6, 128, 5, 4), 1),
+    # many token splits of dW_r, the last one 8 tokens long
+    (synth.Workload("rb_splits", 5000, 512, 64, 6, 128, 0, 1), 1),
 ]
 
 
