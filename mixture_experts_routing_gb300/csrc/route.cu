@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
   __shared__ float zbuf[kTopkWarps][kMaxExperts];
   __shared__ int32_t ids_s[kTokensPerChunk * kMaxTopK];
   __shared__ uint32_t pk_s[kTokensPerChunk * kMaxTopK];
-  __shared__ int32_t hist[kMaxExperts];
+  __shared__ uint32_t emask[kMaxExperts];  // bit tl: token tl of the chunk chose e
   __shared__ int32_t offs[kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -596,17 +596,21 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
       pk_s[tl * K + lane] = __float_as_uint(pr);
     }
   }
-  // stable counting sort of the chunk's routes by expert
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  // stable counting sort of the chunk's routes by expert. A token picks an
+  // expert at most once, so expert e's routes are its tokens in the mask
+  // (32 tokens per chunk), and a route's rank among them is the number of
+  // earlier tokens in the mask.
+  static_assert(kTokensPerChunk == 32, "one mask bit per token of a chunk");
+  for (int e = threadIdx.x; e < E; e += blockDim.x) emask[e] = 0u;
   __syncthreads();
   const int nr = nt * K;
-  for (int r = threadIdx.x; r < nr; r += blockDim.x) atomicAdd(&hist[ids_s[r]], 1);
+  for (int r = threadIdx.x; r < nr; r += blockDim.x) atomicOr(&emask[ids_s[r]], 1u << (r / K));
   __syncthreads();
   if (warp == 0) {
     int run = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
-      const int h = (e < E) ? hist[e] : 0;
+      const int h = (e < E) ? __popc(emask[e]) : 0;
       int incl = h;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -621,13 +625,12 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
   for (int r = threadIdx.x; r < nr; r += blockDim.x) {
     const int e = ids_s[r];
     const int tl = r / K;
-    int rank = 0;
-    for (int r2 = 0; r2 < tl * K; ++r2) rank += (ids_s[r2] == e);  // earlier tokens only
+    const int rank = __popc(emask[e] & ((1u << tl) - 1u));  // earlier tokens only
     chunk_routes[(size_t)t0 * K + offs[e] + rank] = t0 * K + r;
     chunk_keys[(size_t)t0 * K + offs[e] + rank] = pk_s[r];
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    chunk_counts[(size_t)c * E + e] = hist[e];
+    chunk_counts[(size_t)c * E + e] = __popc(emask[e]);
     chunk_lofs[(size_t)c * E + e] = offs[e];
   }
 }
@@ -665,7 +668,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
 // One CTA per expert: assemble the expert's routes in token order from the
 // chunk tables, select the `cap` highest p' (ties to the lower token) and
 // write the expert's part of the route-list layout.
-__global__ void __launch_bounds__(kSelThreads) route_select_kernel(
+// (at most 32 registers a thread, so two CTAs share an SM: dsv3's 256 experts
+// fit in one wave on 152 SMs)
+__global__ void __launch_bounds__(kSelThreads, 2) route_select_kernel(
     const int32_t* __restrict__ chunk_counts, const int32_t* __restrict__ chunk_lofs,
     const int32_t* __restrict__ chunk_routes, const uint32_t* __restrict__ chunk_keys, int Nmax,
     const int32_t* __restrict__ n_dev, int E, int K, int cap_num, int cap_den, int bm,
