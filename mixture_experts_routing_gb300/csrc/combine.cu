@@ -132,14 +132,46 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bwd_kernel(
 // reproducible.
 constexpr int kQuantWarps = 8;
 
+// The quotient v / s that the codes encode. A row whose scale s lies in
+// [2^-100, FLT_MAX] takes y = RN(1/s) once and, per value, q = RN(v y), the
+// exact residual r = v - s q (one fma) and RN(q + r y): Markstein's division
+// step (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990), which gives the
+// correctly rounded quotient when nothing underflows. An exhaustive check over
+// the quantiser's whole domain in that range (every bf16 row maximum amax with
+// s = RN(amax/448), every bf16 value up to it; tests/test_quantize_division.py)
+// finds it equal to RN(v/s) wherever |v/s| >= 2^-12 and of the same sign
+// below that, where both encode as a zero code. Other rows divide directly.
+struct RowDivisor {
+  float s, y;
+  bool fast;
+};
+
+__device__ __forceinline__ RowDivisor row_divisor(float s) {
+  RowDivisor d;
+  d.s = s;
+  d.fast = s >= 0x1p-100f && s <= 3.40282347e38f;
+  d.y = d.fast ? __frcp_rn(s) : 0.0f;
+  return d;
+}
+
+__device__ __forceinline__ float row_div(float v, const RowDivisor& d) {
+  if (!d.fast) return __fdiv_rn(v, d.s);
+  const float q = __fmul_rn(v, d.y);
+  const float r = __fmaf_rn(-d.s, q, v);
+  // the quotient has v's sign; the sign restores it for v = -0, where the
+  // residual sum gives +0
+  return copysignf(__fmaf_rn(r, d.y, q), v);
+}
+
 // Eight bf16 values (one 16-byte group) to eight E4M3 codes, lowest first.
-__device__ __forceinline__ uint2 quantize8_e4m3(const uint4 w, float s) {
+__device__ __forceinline__ uint2 quantize8_e4m3(const uint4 w, const RowDivisor& d) {
   const uint32_t a[4] = {w.x, w.y, w.z, w.w};
   uint32_t packed[2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float lo = __fdiv_rn(__uint_as_float(a[i] << 16), s);
-    const float hi = __fdiv_rn(__uint_as_float(a[i] & 0xFFFF0000u), s);
+    const float lo = row_div(__uint_as_float(a[i] << 16), d);
+    const float hi = row_div(__uint_as_float(a[i] & 0xFFFF0000u), d);
     const uint32_t pair =
         __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);  // lo: low byte
     if (i & 1)
@@ -176,8 +208,9 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_rows_fp8_kernel(
   const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   if (lane == 0) scale[r] = s;
   uint8_t* qr = q + (size_t)r * cols;
+  const RowDivisor dv = row_divisor(s);
   for (int v = lane; v < nv; v += 32)
-    reinterpret_cast<uint2*>(qr)[v] = quantize8_e4m3(reinterpret_cast<const uint4*>(row)[v], s);
+    reinterpret_cast<uint2*>(qr)[v] = quantize8_e4m3(reinterpret_cast<const uint4*>(row)[v], dv);
 }
 
 // The same quantisation with the whole row held in registers: WPR warps per
@@ -230,10 +263,11 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_rows_fp8_reg_kernel
   const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   if (li == 0) scale[r] = s;
   uint2* qr = reinterpret_cast<uint2*>(q + (size_t)r * cols);
+  const RowDivisor dv = row_divisor(s);
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     const int v = li + 32 * WPR * j;
-    if (v < nv) qr[v] = quantize8_e4m3(w[j], s);
+    if (v < nv) qr[v] = quantize8_e4m3(w[j], dv);
   }
 }
 
