@@ -23,9 +23,9 @@
 // over a split of the tokens in stages of 64; each split writes its partial
 // sum, and a separate pass adds the splits in split order (deterministic).
 // dx: tiles of 128 tokens (M) x 128 rows of h (N), K = Ep in stages of 64
-// experts, both operands K-major; the tile of dx is fetched by TMA with the
-// first stage and read back from shared memory by the epilogue, which adds
-// the accumulator and stores the rounded sum.
+// experts, both operands K-major; persistent CTAs walk the tiles, each tile
+// of dx fetched by TMA ahead of its epilogue, which reads it back from shared
+// memory, adds the accumulator and stores the rounded sum.
 //
 // Warp roles (192 threads): warp 0 issues the TMA copies, warp 1 owns TMEM and
 // issues the MMAs (one lane), warps 2-5 drain TMEM (warp w reads lanes
@@ -191,9 +191,15 @@ __global__ void __launch_bounds__(kRbThreads, 1)
 }
 
 // ---------------------------------------------------------------- dx
+// Persistent: one CTA per SM walks the (h slice, token tile) items
+// w = blockIdx.x, blockIdx.x + gridDim.x, ... (item w: rows h0 = 128 (w % h
+// tiles), tokens t0 = 128 (w / h tiles)). Per item the producer loads the dx
+// tile into one of two tile buffers and the Ep/64 operand stages into a ring
+// of two; the MMA warp accumulates into one of two TMEM accumulators; so the
+// epilogue of one item overlaps the loads and MMAs of the next.
 struct DxMmaParams {
   int N, H, Ep;
-  int stages;
+  int h_tiles, items;
   uint16_t* dx;
   uint32_t* err;
 };
@@ -201,36 +207,43 @@ struct DxMmaParams {
 constexpr uint32_t kDxOpBytes = 128u * 128u;        // one 128-row x 64-column bf16 box
 constexpr uint32_t kDxStageBytes = 4u * kDxOpBytes;  // A hi, A lo, B hi, B lo
 constexpr uint32_t kDxTileBytes = 2u * kDxOpBytes;   // dx: 128 tokens x 128 h
+constexpr int kDxStages = 2;
+constexpr uint32_t kDxSmemBytes = kDxStages * kDxStageBytes + 2u * kDxTileBytes + 1024u;
 
 __global__ void __launch_bounds__(kRbThreads, 1)
     router_dx_mma_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmD, const DxMmaParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kRbMaxStages];
-  __shared__ __align__(8) uint64_t empty_bar[kRbMaxStages];
-  __shared__ __align__(8) uint64_t dx_bar;
-  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ __align__(8) uint64_t full_bar[kDxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kDxStages];
+  __shared__ __align__(8) uint64_t dx_full[2];
+  __shared__ __align__(8) uint64_t dx_empty[2];
+  __shared__ __align__(8) uint64_t acc_full[2];
+  __shared__ __align__(8) uint64_t acc_empty[2];
   __shared__ uint32_t tmem_base_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t dxs = sbase + (uint32_t)p.stages * kDxStageBytes;
-  const int h0 = blockIdx.x * 128, t0 = blockIdx.y * 128;
+  const uint32_t dxs0 = sbase + (uint32_t)kDxStages * kDxStageBytes;
   const int kb_n = p.Ep / kRbK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
+    for (int s = 0; s < kDxStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
-    mbar_init(smem_u32(&dx_bar), 1);
-    mbar_init(smem_u32(&acc_bar), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&dx_full[b]), 1);
+      mbar_init(smem_u32(&dx_empty[b]), 4);   // one arrival per epilogue warp
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 4);
+    }
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmD);
   }
-  if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), 128u);
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), 256u);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -239,56 +252,83 @@ __global__ void __launch_bounds__(kRbThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     const uint64_t pol_d = policy_evict_first(), pol_w = policy_evict_last();
-    if (lane == 0) {
-      const uint32_t db = smem_u32(&dx_bar);
-      mbar_arrive_expect_tx(db, kDxTileBytes);
-      tma_load_2d(dxs, &tmD, h0, t0, db, pol_d);
-      tma_load_2d(dxs + kDxOpBytes, &tmD, h0 + 64, t0, db, pol_d);
-    }
-    for (int kb = 0; kb < kb_n; ++kb) {
-      const int s = kb % p.stages;
-      const uint32_t u = (uint32_t)(kb / p.stages);
-      if (kb >= p.stages &&
-          !mbar_wait_warp(smem_u32(&empty_bar[s]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty))
+    uint32_t g = 0;  // operand stages issued
+    bool ok = true;
+    for (int i = 0, w = blockIdx.x; ok && w < p.items; ++i, w += gridDim.x) {
+      const int h0 = (w % p.h_tiles) * 128, t0 = (w / p.h_tiles) * 128;
+      const int b = i & 1;
+      const uint32_t u = (uint32_t)(i >> 1);
+      if (i >= 2 && !mbar_wait_warp(smem_u32(&dx_empty[b]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty))
         break;
       if (lane == 0) {
-        const uint32_t fb = smem_u32(&full_bar[s]);
-        const uint32_t st = sbase + (uint32_t)s * kDxStageBytes;
-        const int k = kb * kRbK;
-        mbar_arrive_expect_tx(fb, kDxStageBytes);
-        tma_load_2d(st, &tmA, k, t0, fb, pol_w);                                // dl hi
-        tma_load_2d(st + kDxOpBytes, &tmA, p.Ep + k, t0, fb, pol_w);            // dl lo
-        tma_load_2d(st + 2u * kDxOpBytes, &tmB, k, h0, fb, pol_w);              // W_r hi
-        tma_load_2d(st + 3u * kDxOpBytes, &tmB, p.Ep + k, h0, fb, pol_w);       // W_r lo
+        const uint32_t db = smem_u32(&dx_full[b]);
+        const uint32_t dst = dxs0 + (uint32_t)b * kDxTileBytes;
+        mbar_arrive_expect_tx(db, kDxTileBytes);
+        tma_load_2d(dst, &tmD, h0, t0, db, pol_d);
+        tma_load_2d(dst + kDxOpBytes, &tmD, h0 + 64, t0, db, pol_d);
       }
       __syncwarp();
+      for (int kb = 0; kb < kb_n; ++kb, ++g) {
+        const int s = (int)(g % kDxStages);
+        const uint32_t us = g / kDxStages;
+        if (g >= (uint32_t)kDxStages &&
+            !mbar_wait_warp(smem_u32(&empty_bar[s]), (us & 1u) ^ 1u, p.err, kErrWaitEmpty)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&full_bar[s]);
+          const uint32_t st = sbase + (uint32_t)s * kDxStageBytes;
+          const int k = kb * kRbK;
+          mbar_arrive_expect_tx(fb, kDxStageBytes);
+          tma_load_2d(st, &tmA, k, t0, fb, pol_w);                           // dl hi
+          tma_load_2d(st + kDxOpBytes, &tmA, p.Ep + k, t0, fb, pol_w);       // dl lo
+          tma_load_2d(st + 2u * kDxOpBytes, &tmB, k, h0, fb, pol_w);         // W_r hi
+          tma_load_2d(st + 3u * kDxOpBytes, &tmB, p.Ep + k, h0, fb, pol_w);  // W_r lo
+        }
+        __syncwarp();
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, 128);
-    for (int kb = 0; kb < kb_n; ++kb) {
-      const int s = kb % p.stages;
-      const uint32_t u = (uint32_t)(kb / p.stages);
-      if (!mbar_wait_warp(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) break;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int i = 0, w = blockIdx.x; ok && w < p.items; ++i, w += gridDim.x) {
+      const int a = i & 1;
+      const uint32_t u = (uint32_t)(i >> 1);
+      if (i >= 2 &&
+          !mbar_wait_warp(smem_u32(&acc_empty[a]), (u & 1u) ^ 1u, p.err, kErrWaitAccum))
+        break;
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t st = sbase + (uint32_t)s * kDxStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < kRbK / 16; ++kk) {  // 16 experts = 32 bytes of a row
-          const uint32_t o = (uint32_t)kk * 32u;
-          const uint64_t ahi = sdesc_sw128(st + o), alo = sdesc_sw128(st + kDxOpBytes + o);
-          const uint64_t bhi = sdesc_sw128(st + 2u * kDxOpBytes + o);
-          const uint64_t blo = sdesc_sw128(st + 3u * kDxOpBytes + o);
-          umma_bf16(tmem, ahi, bhi, idesc, (kb | kk) != 0);
-          umma_bf16(tmem, alo, bhi, idesc, 1u);
-          umma_bf16(tmem, ahi, blo, idesc, 1u);
+      const uint32_t d = tmem + (uint32_t)a * 128u;
+      for (int kb = 0; kb < kb_n; ++kb, ++g) {
+        const int s = (int)(g % kDxStages);
+        const uint32_t us = g / kDxStages;
+        if (!mbar_wait_warp(smem_u32(&full_bar[s]), us & 1u, p.err, kErrWaitFull)) {
+          ok = false;
+          break;
         }
-        umma_commit(smem_u32(&empty_bar[s]));
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t st = sbase + (uint32_t)s * kDxStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < kRbK / 16; ++kk) {  // 16 experts = 32 bytes of a row
+            const uint32_t o = (uint32_t)kk * 32u;
+            const uint64_t ahi = sdesc_sw128(st + o), alo = sdesc_sw128(st + kDxOpBytes + o);
+            const uint64_t bhi = sdesc_sw128(st + 2u * kDxOpBytes + o);
+            const uint64_t blo = sdesc_sw128(st + 3u * kDxOpBytes + o);
+            umma_bf16(d, ahi, bhi, idesc, (kb | kk) != 0);
+            umma_bf16(d, alo, bhi, idesc, 1u);
+            umma_bf16(d, ahi, blo, idesc, 1u);
+          }
+          umma_commit(smem_u32(&empty_bar[s]));
+        }
+        __syncwarp();
       }
+      if (lane == 0) umma_commit(smem_u32(&acc_full[a]));  // also after an abort
       __syncwarp();
     }
-    if (lane == 0) umma_commit(smem_u32(&acc_bar));  // also after an abort
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     // lane = token row r of the tile; 16 columns of h at a time: the old dx
@@ -297,13 +337,18 @@ __global__ void __launch_bounds__(kRbThreads, 1)
     // accumulator, rounded once, stored 32 bytes per lane
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    const int t = t0 + r;
-    const bool ok = mbar_wait_warp(smem_u32(&dx_bar), 0u, p.err, kErrWaitFull) &&
-                    mbar_wait_warp(smem_u32(&acc_bar), 0u, p.err, kErrWaitAccum);
-    if (ok) {
+    for (int i = 0, w = blockIdx.x; w < p.items; ++i, w += gridDim.x) {
+      const int h0 = (w % p.h_tiles) * 128, t0 = (w / p.h_tiles) * 128;
+      const int a = i & 1;
+      const uint32_t u = (uint32_t)(i >> 1);
+      if (!mbar_wait_warp(smem_u32(&acc_full[a]), u & 1u, p.err, kErrWaitAccum) ||
+          !mbar_wait_warp(smem_u32(&dx_full[a]), u & 1u, p.err, kErrWaitFull))
+        break;
       tc_fence_after();
-      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-      const uint8_t* tile = smem_raw + (dxs - smem_u32(smem_raw));
+      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)a * 128u;
+      const uint8_t* tile =
+          smem_raw + (dxs0 + (uint32_t)a * kDxTileBytes - smem_u32(smem_raw));
+      const int t = t0 + r;
       uint16_t* out = p.dx + (size_t)t * p.H + h0;
       for (int c = 0; c < 8; ++c) {
         uint32_t v[16];
@@ -313,13 +358,13 @@ __global__ void __launch_bounds__(kRbThreads, 1)
         const int j0 = (c & 3) * 2;
         const uint4 o0 = *reinterpret_cast<const uint4*>(row + ((j0 ^ (r & 7)) << 4));
         const uint4 o1 = *reinterpret_cast<const uint4*>(row + (((j0 + 1) ^ (r & 7)) << 4));
-        const uint32_t w[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+        const uint32_t wv[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
         uint32_t res[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-          const float lo = __fadd_rn(__uint_as_float(w[m] << 16), __uint_as_float(v[2 * m]));
+          const float lo = __fadd_rn(__uint_as_float(wv[m] << 16), __uint_as_float(v[2 * m]));
           const float hi =
-              __fadd_rn(__uint_as_float(w[m] & 0xFFFF0000u), __uint_as_float(v[2 * m + 1]));
+              __fadd_rn(__uint_as_float(wv[m] & 0xFFFF0000u), __uint_as_float(v[2 * m + 1]));
           res[m] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
         }
@@ -328,13 +373,19 @@ __global__ void __launch_bounds__(kRbThreads, 1)
           *reinterpret_cast<uint4*>(out + c * 16 + 8) = make_uint4(res[4], res[5], res[6], res[7]);
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&acc_empty[a]));
+        mbar_arrive(smem_u32(&dx_empty[a]));
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128u);
+    tmem_dealloc(tmem, 256u);
   }
 }
 
@@ -361,8 +412,8 @@ bool set_smem_limits(cudaError_t* err) {
   int dev = 0;
   if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return false;
   if (dev >= 0 && dev < 64 && done[dev]) return true;
-  // the largest request below is 2 stages of 80 KiB + 1 KiB (dW_r, Ep = 256)
-  // or 2 x 64 KiB + 32 KiB + 1 KiB (dx); static shared memory comes on top
+  // the largest requests: 2 stages of 80 KiB + 1 KiB (dW_r, Ep = 256) and
+  // 2 x 64 KiB + 2 x 32 KiB + 1 KiB (dx); static shared memory comes on top
   const int lim = 200 * 1024;
   if ((*err = cudaFuncSetAttribute(router_dwr_mma_kernel,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) !=
@@ -434,11 +485,16 @@ int launch_router_dx_mma(const uint16_t* dls, const uint16_t* wrs, int N, int H,
   if (N <= 0) return 0;
   cudaError_t err = cudaSuccess;
   if (!set_smem_limits(&err)) return -(int)err;
+  int sms = 0, dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return -(int)err;
   DxMmaParams p{};
   p.N = N;
   p.H = H;
   p.Ep = round64(E);
-  p.stages = p.Ep / kRbK >= 2 ? 2 : 1;
+  p.h_tiles = H / 128;
+  p.items = p.h_tiles * ((N + 127) / 128);
   p.dx = dx;
   p.err = errw;
   CUtensorMap tmA, tmB, tmD;
@@ -446,9 +502,8 @@ int launch_router_dx_mma(const uint16_t* dls, const uint16_t* wrs, int N, int H,
       !make_map(&tmB, wrs, (uint64_t)(2 * p.Ep), (uint64_t)H, 64, 128) ||
       !make_map(&tmD, dx, (uint64_t)H, (uint64_t)N, 64, 128))
     return -1;
-  const size_t dyn = (size_t)p.stages * kDxStageBytes + kDxTileBytes + 1024;
-  router_dx_mma_kernel<<<dim3(H / 128, (N + 127) / 128), kRbThreads, dyn, s>>>(tmA, tmB, tmD,
-                                                                                p);
+  const int grid = p.items < sms ? p.items : sms;
+  router_dx_mma_kernel<<<grid, kRbThreads, kDxSmemBytes, s>>>(tmA, tmB, tmD, p);
   err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }
