@@ -341,10 +341,12 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
 // Few chains (small N*E, where the tiled kernels leave most lanes idle and
 // walk H/32 pipelined stages): one thread per token and 2 consecutive
 // experts, the whole contraction in registers, x rows and W_r rows read from
-// global memory (shared between threads through L1), the next 8 values of h
-// loaded while the current 8 are multiplied. Same chains: ascending h, one
-// fma per term, bias last.
+// global memory (shared between threads through L1), the next 16 values of h
+// loaded while the current 16 are multiplied (8 at a time measured 9.0 us on
+// a 256-token, H = 128, E = 8 router: one load round trip per 8 values).
+// Same chains: ascending h, one fma per term, bias last.
 constexpr int kRSmallThreads = 128;
+constexpr int kRSmallG = 16;  // values of h per load step (H is a multiple of 128)
 
 template <bool kVec2>
 __global__ void __launch_bounds__(kRSmallThreads) router_logits_small_kernel(
@@ -352,17 +354,19 @@ __global__ void __launch_bounds__(kRSmallThreads) router_logits_small_kernel(
     float* __restrict__ logits, int Nmax, const int32_t* __restrict__ n_dev, int H, int E) {
   griddep_wait();  // launched after the kernel that writes this one's inputs
   griddep_launch_dependents();
-  const int eg = (E + 1) / 2;  // pairs of experts
+  constexpr int XV = kRSmallG / 8;  // 16-byte x loads per step
+  const int eg = (E + 1) / 2;       // pairs of experts
   const int64_t gid = (int64_t)blockIdx.x * kRSmallThreads + threadIdx.x;
   const int N = live_tokens(n_dev, Nmax);
   const int t = (int)(gid / eg), e0 = (int)(gid % eg) * 2;
   if (t >= N) return;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  auto load = [&](int h8, uint4& xv, float (&w)[8][2]) {
-    xv = __ldg(xr + h8);
+  auto load = [&](int hg, uint4 (&xv)[XV], float (&w)[kRSmallG][2]) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float* wrow = wr + (size_t)(h8 * 8 + i) * E + e0;
+    for (int v = 0; v < XV; ++v) xv[v] = __ldg(xr + hg * XV + v);
+#pragma unroll
+    for (int i = 0; i < kRSmallG; ++i) {
+      const float* wrow = wr + (size_t)(hg * kRSmallG + i) * E + e0;
       if (kVec2) {
         const float2 q = __ldg(reinterpret_cast<const float2*>(wrow));
         w[i][0] = q.x;
@@ -374,23 +378,29 @@ __global__ void __launch_bounds__(kRSmallThreads) router_logits_small_kernel(
     }
   };
   float acc0 = 0.0f, acc1 = 0.0f;
-  uint4 xv;
-  float w[8][2];
+  uint4 xv[XV];
+  float w[kRSmallG][2];
   load(0, xv, w);
-  for (int h8 = 0; h8 < H / 8; ++h8) {
-    uint4 xn = xv;
-    float wn[8][2];
-    if (h8 + 1 < H / 8) load(h8 + 1, xn, wn);
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+  const int steps = H / kRSmallG;
+  for (int hg = 0; hg < steps; ++hg) {
+    uint4 xn[XV];
+    float wn[kRSmallG][2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float xf = __uint_as_float((i & 1) ? (xw[i >> 1] & 0xFFFF0000u) : (xw[i >> 1] << 16));
+    for (int v = 0; v < XV; ++v) xn[v] = xv[v];
+    if (hg + 1 < steps) load(hg + 1, xn, wn);
+#pragma unroll
+    for (int i = 0; i < kRSmallG; ++i) {
+      const uint4 q = xv[i >> 3];
+      const uint32_t xw[4] = {q.x, q.y, q.z, q.w};
+      const int k = i & 7;
+      const float xf = __uint_as_float((k & 1) ? (xw[k >> 1] & 0xFFFF0000u) : (xw[k >> 1] << 16));
       acc0 = __fmaf_rn(xf, w[i][0], acc0);
       acc1 = __fmaf_rn(xf, w[i][1], acc1);
     }
-    xv = xn;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int v = 0; v < XV; ++v) xv[v] = xn[v];
+#pragma unroll
+    for (int i = 0; i < kRSmallG; ++i) {
       w[i][0] = wn[i][0];
       w[i][1] = wn[i][1];
     }
@@ -636,10 +646,12 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
 }
 
 // ---------------------------------------------------------------- R4
-constexpr int kSelThreads = 1024;
 constexpr int kMaxChunks = kMaxTokens / kTokensPerChunk;
+constexpr int kSelSmallThreads = 256;     // select CTA size for small batches
+constexpr int kSelSmallMaxTokens = 2048;  // (one thread per chunk needs <= 8192)
 
-// Exclusive scan of v over the CTA (kSelThreads threads, all must call).
+// Exclusive scan of v over the CTA (THREADS threads, all must call).
+template <int THREADS>
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __syncthreads();
@@ -652,7 +664,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
   if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int w = (lane < (kSelThreads >> 5)) ? warp_tot[lane] : 0;
+    const int w = (lane < (THREADS >> 5)) ? warp_tot[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -667,10 +679,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
 
 // One CTA per expert: assemble the expert's routes in token order from the
 // chunk tables, select the `cap` highest p' (ties to the lower token) and
-// write the expert's part of the route-list layout.
-// (at most 32 registers a thread, so two CTAs share an SM: dsv3's 256 experts
-// fit in one wave on 152 SMs)
-__global__ void __launch_bounds__(kSelThreads, 2) route_select_kernel(
+// write the expert's part of the route-list layout. A thread owns one chunk
+// column, so THREADS >= the chunk count: 256 threads for batches of up to
+// 2048 tokens (fewer CTA-wide barriers to wait on), 1024 above (at most 32
+// registers a thread, so two such CTAs share an SM).
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select_kernel(
     const int32_t* __restrict__ chunk_counts, const int32_t* __restrict__ chunk_lofs,
     const int32_t* __restrict__ chunk_routes, const uint32_t* __restrict__ chunk_keys, int Nmax,
     const int32_t* __restrict__ n_dev, int E, int K, int cap_num, int cap_den, int bm,
@@ -710,7 +724,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) route_select_kernel(
   int32_t* rids = reinterpret_cast<int32_t*>(dyn + Nmax);  // route index t*K+k
   // column e of the chunk tables -> positions in the expert's list
   const int cnt = (tid < C) ? min(max(chunk_counts[(size_t)tid * E + e], 0), kTokensPerChunk) : 0;
-  const int pos0 = block_exclusive_scan(cnt, warp_tot);
+  const int pos0 = block_exclusive_scan<THREADS>(cnt, warp_tot);
   if (tid < C) { s_cnt[tid] = cnt; s_pos[tid] = pos0; }
   if (tid == C - 1) s_total = pos0 + cnt;
   if (C == 0 && tid == 0) s_total = 0;
@@ -735,7 +749,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) route_select_kernel(
       }
       if (ext < 0) ext = (cnt_e + bm - 1) / bm * bm;
     }
-    const int before = block_exclusive_scan(ext, warp_tot);
+    const int before = block_exclusive_scan<THREADS>(ext, warp_tot);
     if (tid == e) {
       s_base = before;
       s_extent = ext;
@@ -745,7 +759,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) route_select_kernel(
     base = s_base;
     extent = s_extent;
   }
-  for (int cc = warp; cc < C; cc += kSelThreads / 32) {
+  for (int cc = warp; cc < C; cc += THREADS / 32) {
     const int lo = min(max(chunk_lofs[(size_t)cc * E + e], 0), kTokensPerChunk * K);
     const int64_t chunk_base = (int64_t)cc * kTokensPerChunk * K;
     const int m = (int)min((int64_t)min(s_cnt[cc], kTokensPerChunk * K - lo),
@@ -770,9 +784,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) route_select_kernel(
     uint32_t prefix = 0, mask = 0;
     int remaining = cap;
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+      for (int i = tid; i < 256; i += THREADS) hist[i] = 0;
       __syncthreads();
-      for (int base = warp * 32; base < n; base += kSelThreads) {
+      for (int base = warp * 32; base < n; base += THREADS) {
         const int i = base + lane;
         const uint32_t k = (i < n) ? keys[i] : 0u;
         const bool cand = (i < n) && ((k & mask) == prefix);
@@ -815,12 +829,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) route_select_kernel(
     needed = remaining;  // how many keys equal to thr are kept (lowest tokens first)
   }
   // each thread owns a contiguous run of the list, so scans follow token order
-  const int ipt = (n + kSelThreads - 1) / kSelThreads;
+  const int ipt = (n + THREADS - 1) / THREADS;
   const int i0 = min(n, tid * ipt), i1 = min(n, i0 + ipt);
   int ties = 0;
   if (select)
     for (int i = i0; i < i1; ++i) ties += (keys[i] == thr);
-  const int tie_base = block_exclusive_scan(ties, warp_tot);
+  const int tie_base = block_exclusive_scan<THREADS>(ties, warp_tot);
   int tie_rank = tie_base;
   int kept_local = 0;
   for (int i = i0; i < i1; ++i) {
@@ -832,7 +846,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) route_select_kernel(
     }
     kept_local += kp;
   }
-  int pos = block_exclusive_scan(kept_local, warp_tot);
+  int pos = block_exclusive_scan<THREADS>(kept_local, warp_tot);
   // second pass: same keep decisions, now writing the layout
   tie_rank = tie_base;
   for (int i = i0; i < i1; ++i) {
@@ -856,22 +870,22 @@ __global__ void __launch_bounds__(kSelThreads, 2) route_select_kernel(
     }
   }
   const int kept_e = select ? cap : n;
-  for (int sl = kept_e + tid; sl < extent; sl += kSelThreads) {
+  for (int sl = kept_e + tid; sl < extent; sl += THREADS) {
     sorted_slot_ids[base + sl] = Nmax;  // sentinel: one past the static token bound
     slot_prob[base + sl] = 0.0f;
   }
   const int nb = extent / bm;
-  for (int b = tid; b < nb; b += kSelThreads)
+  for (int b = tid; b < nb; b += THREADS)
     expert_ids[(size_t)base / bm + b] = (b * bm < kept_e) ? e : -1;
   if (e == E - 1) {
     // slots past the padded total up to the allocated bound (dropless, or a
     // live batch below the static bound): sentinel / -1
     const int used = dropless ? s_all : E * cpad;
-    for (int sl = used + tid; sl < s_max; sl += kSelThreads) {
+    for (int sl = used + tid; sl < s_max; sl += THREADS) {
       sorted_slot_ids[sl] = Nmax;
       slot_prob[sl] = 0.0f;
     }
-    for (int b = used / bm + tid; b < s_max / bm; b += kSelThreads) expert_ids[b] = -1;
+    for (int b = used / bm + tid; b < s_max / bm; b += THREADS) expert_ids[b] = -1;
   }
   if (tid == 0) {
     block_start[e] = base / bm;
@@ -1035,17 +1049,26 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return -(int)err;
     if (dev < 0 || dev >= 64 || !set_for[dev]) {
-      err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMaxTokens * 8);
+      err = cudaFuncSetAttribute(route_select_kernel<1024>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxTokens * 8);
+      if (err != cudaSuccess) return -(int)err;
+      err = cudaFuncSetAttribute(route_select_kernel<kSelSmallThreads>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSelSmallThreads * kTokensPerChunk * 8);
       if (err != cudaSuccess) return -(int)err;
       if (dev >= 0 && dev < 64) set_for[dev] = 1;
     }
   }
-  launch_pdl(route_select_kernel, dim3(a.E), dim3(kSelThreads), dyn, s, 
-      a.ws.chunk_counts, a.ws.chunk_lofs, a.ws.chunk_routes, a.ws.chunk_keys, a.N, a.n_dev, a.E,
-      a.K, a.cap_num, a.cap_den, a.bm, a.dropless, a.ladder, (int)a.s_max, a.keep, a.expert_counts,
-      a.kept_counts, a.sorted_slot_ids, a.expert_ids,
-      a.block_start, a.ntpp, a.token_routes, a.gemm_sched, a.slot_prob);
+  // the narrow CTA for batches of at most 2048 tokens: an expert can hold every
+  // token, and above that many keys per thread (a Zipf-skewed 8192-token batch:
+  // route_align 0.168 -> 0.195 ms) cost more than the barriers save
+  const bool small = a.N <= kSelSmallMaxTokens;
+  launch_pdl(small ? route_select_kernel<kSelSmallThreads> : route_select_kernel<1024>,
+             dim3(a.E), dim3(small ? kSelSmallThreads : 1024), dyn, s, a.ws.chunk_counts,
+             a.ws.chunk_lofs, a.ws.chunk_routes, a.ws.chunk_keys, a.N, a.n_dev, a.E, a.K,
+             a.cap_num, a.cap_den, a.bm, a.dropless, a.ladder, (int)a.s_max, a.keep,
+             a.expert_counts, a.kept_counts, a.sorted_slot_ids, a.expert_ids, a.block_start,
+             a.ntpp, a.token_routes, a.gemm_sched, a.slot_prob);
   ++launched;
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;
