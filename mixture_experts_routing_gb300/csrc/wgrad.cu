@@ -18,9 +18,12 @@
 //
 // The UMMA M dimension is always the output's contiguous dimension (i for dW2,
 // h for dW13), so TMEM lane = output column and every epilogue store of one
-// accumulator column is 32 consecutive floats. Tiles are 128 x 256 with two
-// TMEM accumulators (512 columns), so the epilogue of one tile overlaps the
-// MMAs of the next. An expert's last k-chunk issues only the 16-slot k-steps
+// accumulator column is 32 consecutive floats. A tile is two 128-row
+// accumulators x tile_n columns sharing each B stage; with tile_n = 256 they
+// fill the 512 TMEM columns, so a tile's MMAs wait for the previous tile's
+// epilogue (two buffers, and so overlap, only with tile_n = 128, which moves
+// more operand bytes per flop and measured slower). An expert's last k-chunk
+// issues only the 16-slot k-steps
 // that hold kept slots (rows up to roundup(kept,16) are written by the FC2
 // dgrad, zeros for padding); an expert with no kept slot gets zero tiles
 // written without any MMA.
