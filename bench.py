@@ -68,7 +68,29 @@ def parse_args(argv=None):
     ap.add_argument("--pad-ratio", type=float, default=0.0)
     ap.add_argument("--cpu-experts", type=int, default=48,
                     help="experts whose FFN the CPU baseline runs (bounded sample)")
-    return ap.parse_args(argv)
+    ap.add_argument("--activation", choices=["swiglu", "geglu"], default="swiglu",
+                    help="gated activation of FC1 (forward and training steps)")
+    ap.add_argument("--prob-in-act", action="store_true",
+                    help="p' multiplies FC1's activation; the combine sums with unit weights")
+    args = ap.parse_args(argv)
+    if args.fp8 and (args.activation != "swiglu" or args.prob_in_act):
+        ap.error("--fp8 runs the SwiGLU layer with p' in the combine")
+    return args
+
+
+def act_code(args) -> int:
+    """moe_config_t.activation (and the oracle's act): 0 SwiGLU, 1 GeGLU."""
+    return 1 if args.activation == "geglu" else 0
+
+
+def variant_config(args) -> dict:
+    """Config keys of the activation variant (none for the default layer)."""
+    d = {}
+    if args.activation != "swiglu":
+        d["activation"] = args.activation
+    if args.prob_in_act:
+        d["prob_in_act"] = True
+    return d
 
 
 def dist_env():
@@ -256,11 +278,14 @@ def roofline_for(name, model, ms, peaks, workload, fp8=False):
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
-def time_oracle_sample(w, x_bits, wr, bias, bm, n_experts_sample, seed_experts=0):
+def time_oracle_sample(w, x_bits, wr, bias, bm, n_experts_sample, seed_experts=0, act=0,
+                       prob_in_act=False):
     """The oracle, as it stands, on a bounded sample of one step: routing of
     every token, expert FFN of `n_experts_sample` experts' kept routes
-    (extrapolated to all kept routes by route count), combine of every token.
-    Returns (tokens/s, description, seconds of CPU work, threads)."""
+    (extrapolated to all kept routes by route count), combine of every token;
+    act 0 SwiGLU / 1 GeGLU, prob_in_act: p' scales the activation and the
+    combine has unit weights. Returns (tokens/s, description, seconds of CPU
+    work, threads)."""
     import numpy as np
     import oracle
     import synth
@@ -283,12 +308,17 @@ def time_oracle_sample(w, x_bits, wr, bias, bm, n_experts_sample, seed_experts=0
         k = int(L.kept_counts[e])
         toks += L.sorted_slot_ids[base:base + k].tolist()
         exps += [e] * k
+    scales = None
+    if prob_in_act:  # each route's p'
+        ids = np.asarray(R.topk_ids)
+        pk = np.asarray(R.topk_p)
+        scales = np.array([pk[t][list(ids[t]).index(e)] for t, e in zip(toks, exps)], np.float32)
     t0 = time.perf_counter()
-    oracle.ffn_routes(toks, exps, x_bits, W, H, I)
+    oracle.ffn_routes(toks, exps, x_bits, W, H, I, act=act, scales=scales)
     t_ffn = time.perf_counter() - t0
     o_zero = np.zeros((N * K, H), dtype=np.float32)
     t0 = time.perf_counter()
-    oracle.combine(0, N, L.keep, R.topk_p, o_zero)
+    oracle.combine(0, N, L.keep, None if prob_in_act else R.topk_p, o_zero)
     t_comb = time.perf_counter() - t0
     t_full = t_route + t_ffn * kept_total / max(len(toks), 1) + t_comb
     desc = ("routing of all %d tokens + expert FFN of %d/%d experts (%d of %d kept routes, "
@@ -373,11 +403,12 @@ def run_reference(args):
         wn, xn = w.with_tokens(n), x_bits[:n]
         if train:  # dropless training step: routing + expert-path backward on a route sample
             return time_oracle_train_sample(wn, xn, dy_bits[:n], wr, bias, args.block_m,
-                                            n_routes=1024, seed=i)
+                                            n_routes=1024, seed=i, act=act_code(args))
         if args.fp8:
             return time_oracle_sample_fp8(wn, xn, wr, bias, args.block_m, 1, seed_experts=i)
         return time_oracle_sample(wn, xn, wr, bias, args.block_m, max(1, min(4, args.cpu_experts)),
-                                  seed_experts=i)
+                                  seed_experts=i, act=act_code(args),
+                                  prob_in_act=args.prob_in_act)
 
     # the whole run stays near two minutes of oracle work: a sample that takes
     # longer than its share shrinks the token count of the following ones
@@ -441,7 +472,8 @@ def run_ours(args):
     dist = init_dist(world, "nccl")
     w = synth.WORKLOADS[args.workload]
     N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
-    cfg = moe.Config(N, H, E, K, I, w.cap_num, w.cap_den, block_m=args.block_m)
+    cfg = moe.Config(N, H, E, K, I, w.cap_num, w.cap_den, block_m=args.block_m,
+                     activation=act_code(args), prob_in_act=args.prob_in_act)
     peaks = load_peaks()
 
     # inputs: this rank's batch (seed = rank), shared weights
@@ -635,7 +667,7 @@ def run_ours(args):
                    "block_m": args.block_m, "capacity": moe.capacity(cfg),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (%.1f GB of expert weights); no flush"
-                         % (weight_bytes / 1e9)},
+                         % (weight_bytes / 1e9), **variant_config(args)},
         "gpu_launches": launches,
         "e2e": {"value": N * world * args.steps / (ms_e2e / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": N * H * 2, "d2h_bytes_per_step": N * H * 2,
@@ -666,7 +698,8 @@ def run_ours(args):
                                                           min(args.cpu_experts, 2))
         else:
             v, desc, secs, cores = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
-                                                      args.cpu_experts)
+                                                      args.cpu_experts, act=act_code(args),
+                                                      prob_in_act=args.prob_in_act)
         out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": desc, "cpu_seconds": secs, "host_cpus": os.cpu_count()}
         if N * H <= 1024 * 512 and not fp8:  # the small layers: also on one thread
@@ -675,7 +708,8 @@ def run_ours(args):
             oracle.set_num_threads(1)
             try:
                 v1, desc1, secs1, _ = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
-                                                         args.cpu_experts)
+                                                         args.cpu_experts, act=act_code(args),
+                                                         prob_in_act=args.prob_in_act)
             finally:
                 oracle.set_num_threads(threads)
             out["cpu_baseline"]["single_thread"] = {"value": v1, "unit": UNIT, "cores": 1,
@@ -688,7 +722,7 @@ def run_ours(args):
 
 
 # ----------------------------------------------------------------------------- training step (dropless)
-def time_oracle_train_sample(w, x_bits, dy_bits, wr, bias, bm, n_routes=4096, seed=0):
+def time_oracle_train_sample(w, x_bits, dy_bits, wr, bias, bm, n_routes=4096, seed=0, act=0):
     """The oracle's routing of every token plus the expert-path backward of a
     bounded sample of routes (forward recompute, dX row, dW contributions),
     extrapolated to all routes by route count."""
@@ -709,7 +743,7 @@ def time_oracle_train_sample(w, x_bits, dy_bits, wr, bias, bm, n_routes=4096, se
     wd = {e: synth.normal_bf16_bits(w.seed, synth.STREAM["wd"], e * I * H, I * H, w.w_std).reshape(I, H) for e in exps}
     W = oracle.ExpertWeights(E, wg, wu, wd)
     t0 = time.perf_counter()
-    out = oracle.bwd_routes(tok, ex, pr, x_bits, dy_bits, W, H, I)
+    out = oracle.bwd_routes(tok, ex, pr, x_bits, dy_bits, W, H, I, act=act)
     e0 = exps[0]
     sel = ex == e0
     oracle.wgrad_expert(tok[sel], x_bits, dy_bits, out["aw"][sel], out["dg"][sel], out["du"][sel], H, I)
@@ -740,7 +774,8 @@ def run_ours_train(args):
     bf = dict(dtype=torch.bfloat16, device=dev)
     # weights, packed once (random-init, the layer's shapes)
     cfg0 = moe.Config(base.n_tokens, H, E, K, I, 0, 1, block_m=args.block_m, ladder=list(base.ladder),
-                      ladder_den=base.ladder_den)
+                      ladder_den=base.ladder_den, activation=act_code(args),
+                      prob_in_act=args.prob_in_act)
     w13 = torch.empty((E, 2 * I, H), **bf)
     w2 = torch.empty((E, H, I), **bf)
     tmp = torch.empty((E, H, I), **bf)
@@ -760,7 +795,8 @@ def run_ours_train(args):
     def setup(N):
         w = base.with_tokens(N)
         cfg = moe.Config(N, H, E, K, I, 0, 1, block_m=args.block_m, ladder=list(base.ladder),
-                         ladder_den=base.ladder_den)
+                         ladder_den=base.ladder_den, activation=act_code(args),
+                         prob_in_act=args.prob_in_act)
         x_bits, wr_h, bias_h = host_inputs(w, w.seed + rank)
         dy_bits = synth.normal_bf16_bits(w.seed + rank, synth.STREAM["dy"], 0, N * H, 1.0).reshape(N, H)
         S = moe.max_slots(cfg)
@@ -925,7 +961,8 @@ def run_ours_train(args):
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (%.2f GB of expert weights, %.2f GB of fp32 weight "
                          "gradients); no flush" % ((w13.numel() + w2.numel()) * 2 / 1e9,
-                                                   (dw13.numel() + dw2.numel()) * 4 / 1e9)},
+                                                   (dw13.numel() + dw2.numel()) * 4 / 1e9),
+                   **variant_config(args)},
         "gpu_launches": launches,
         "e2e": {"value": N * world / (ms_e2e / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2 + N * K * 4,
@@ -940,7 +977,8 @@ def run_ours_train(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, desc, secs, cores = time_oracle_train_sample(st["w"], st["x_bits"], st["dy_bits"],
-                                                        st["wr_h"], st["bias_h"], args.block_m)
+                                                        st["wr_h"], st["bias_h"], args.block_m,
+                                                        act=act_code(args))
         out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": desc, "cpu_seconds": secs}
     if rank == 0:
