@@ -206,14 +206,19 @@ __device__ __forceinline__ float act_fwd(float v) {
   return __fdividef(v, 1.0f + __expf(-v));
 }
 
+// The factor both share: act(v) = v c(v) with c = sigma (silu) or Phi (gelu),
+// and act'(v) from c: c (1 + v (1 - c)) for silu, c + v phi(v) for gelu. The
+// backward evaluates c once per element and derives both from it.
 template <int act>
-__device__ __forceinline__ float act_grad(float v) {
-  if (act == 1) {
-    const float cdf = 0.5f * (1.0f + erff(v * 0.70710678118654752f));
-    return cdf + v * (__expf(-0.5f * v * v) * 0.39894228040143268f);
-  }
-  const float sg = __fdividef(1.0f, 1.0f + __expf(-v));
-  return sg * (1.0f + v * (1.0f - sg));
+__device__ __forceinline__ float act_core(float v) {
+  if (act == 1) return 0.5f * (1.0f + erff(v * 0.70710678118654752f));
+  return __fdividef(1.0f, 1.0f + __expf(-v));
+}
+
+template <int act>
+__device__ __forceinline__ float act_grad_core(float v, float c) {
+  if (act == 1) return c + v * (__expf(-0.5f * v * v) * 0.39894228040143268f);
+  return c * (1.0f + v * (1.0f - c));
 }
 
 // Pre-activations of 16 slots (c0..c0+15 of the tile) for this lane's feature:
@@ -253,29 +258,60 @@ __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const
   const int ld2 = 2 * I;
   const size_t row0 = (size_t)(T.slot0 + c0);
   float o[16], dp[16];
-  // dg
+  if constexpr (act == 1) {
+    // gelu: Phi(g) (one erf) evaluated once per element and kept for all
+    // three outputs; du (and the dprob terms) with act(g) = g Phi(g)
+    float cr[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-    const float da0 = __uint_as_float(v[j]);
-    dp[j] = act_fwd<act>(g) * u * da0;
-    o[j] = ps[c0 + j] * da0 * u * act_grad<act>(g);
-  }
-  store_rows16(stg_u, lane, o, p.out + row0 * ld2 + feat0, ld2);
-  // du
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
+      const float da0 = __uint_as_float(v[j]);
+      cr[j] = act_core<act>(g);
+      const float a = g * cr[j];
+      dp[j] = a * u * da0;
+      o[j] = ps[c0 + j] * da0 * a;
+    }
+    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + I + feat0, ld2);
+    // aw
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float g = __uint_as_float(gu[j] << 16);
-    o[j] = ps[c0 + j] * __uint_as_float(v[j]) * act_fwd<act>(g);
-  }
-  store_rows16(stg_u, lane, o, p.out + row0 * ld2 + I + feat0, ld2);
-  // aw
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
+      o[j] = ps[c0 + j] * ((g * cr[j]) * u);
+    }
+    store_rows16(stg_u, lane, o, p.out2 + row0 * I + feat0, I);
+    // dg
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-    o[j] = ps[c0 + j] * (act_fwd<act>(g) * u);
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
+      o[j] = ps[c0 + j] * __uint_as_float(v[j]) * u * act_grad_core<act>(g, cr[j]);
+    }
+    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + feat0, ld2);
+  } else {
+    // silu: sigma is cheap, so each output recomputes it (no extra live array)
+    // dg
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
+      const float da0 = __uint_as_float(v[j]);
+      dp[j] = act_fwd<act>(g) * u * da0;
+      o[j] = ps[c0 + j] * da0 * u * act_grad_core<act>(g, act_core<act>(g));
+    }
+    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + feat0, ld2);
+    // du
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16);
+      o[j] = ps[c0 + j] * __uint_as_float(v[j]) * act_fwd<act>(g);
+    }
+    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + I + feat0, ld2);
+    // aw
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
+      o[j] = ps[c0 + j] * (act_fwd<act>(g) * u);
+    }
+    store_rows16(stg_u, lane, o, p.out2 + row0 * I + feat0, I);
   }
-  store_rows16(stg_u, lane, o, p.out2 + row0 * I + feat0, I);
   // sum dp over the 32 lanes for each of the 16 slots, halving the values
   // held per lane at each exchange: afterwards lanes 2m and 2m+1 hold slot m
 #pragma unroll
