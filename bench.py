@@ -677,7 +677,12 @@ def run_ours(args):
         "grouped_gemm": {"ms": gemm_ms, "tflops_useful": gemm_flops / (gemm_ms / 1e3) / 1e12,
                          "pct_bf16_peak": gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
                          "operands": "e4m3" if fp8 else "bf16",
-                         "tflops_issued_capacity_shape": issued / (gemm_ms / 1e3) / 1e12,
+                         # the flops a fixed-capacity layer would issue (every slot of
+                         # E x cap, empty ones included) over the same time: an
+                         # equivalent rate, above the peak when many slots are empty,
+                         # since the kernels skip slots past each expert's kept count
+                         "tflops_capacity_equivalent": issued / (gemm_ms / 1e3) / 1e12,
+                         "capacity_slots_used": model["_kept"] / max(1, E * moe.capacity(cfg)),
                          "kept_routes": model["_kept"], "active_experts": model["_active"]},
         "graph": {"replays": reps, "warmup_replays": 10, "kernels_per_replay": graph_kernels,
                   "median_ms": g_med, "min_ms": g_ms[0],
