@@ -69,3 +69,17 @@ def test_roofline_picks_the_binding_resource():
     model["fc1"]["flops"] = 4e12                                 # tensor binds
     r = bench.roofline_for("fc1", model, 8.0, peaks, "x")
     assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-12
+
+
+def test_activation_variant_options():
+    """--activation / --prob-in-act reach the layer config and the JSON config
+    keys; the FP8 line keeps the default layer, so combining them is refused."""
+    a = bench.parse_args([])
+    assert bench.act_code(a) == 0 and bench.variant_config(a) == {}
+    a = bench.parse_args(["--activation", "geglu", "--prob-in-act"])
+    assert bench.act_code(a) == 1
+    assert bench.variant_config(a) == {"activation": "geglu", "prob_in_act": True}
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--fp8", "--activation", "geglu"])
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--fp8", "--prob-in-act"])
