@@ -134,3 +134,25 @@ def test_dropless_ladder_validation(L):
         assert L.moe_max_slots(ctypes.byref(c)) == -1, (lad, den)
     no_ladder = moe.Config(**base)
     assert moe.max_slots(no_ladder) == 64 * 2 + 8 * 32
+
+
+def test_router_backward_rejects_bad_arguments_before_launch(L):
+    """Argument checks of moe_router_backward run on the host before any
+    device work: routes, operands, 16-byte alignment of x and dx, workspace."""
+    cfg = moe.Config(64, 128, 8, 2, 128, 1, 1, block_m=32)
+    full = moe._RoutesC(*([256] * len(moe._RoutesC._fields_)))
+    need = L.moe_router_backward_workspace_bytes(ctypes.byref(cfg))
+    assert need > 0
+
+    def call(routes=ctypes.byref(full), x=256, wr=256, dprob=256, dx=256, dwr=256, ws=256,
+             nbytes=None):
+        return L.moe_router_backward(ctypes.byref(cfg), routes, x, wr, None, None, dprob, dx, dwr,
+                                     None, ws, need if nbytes is None else nbytes, None)
+
+    assert call(routes=None) == -1
+    assert call(wr=None) == -1
+    assert call(dwr=None) == -1
+    assert call(dprob=None) == -1
+    assert call(x=264) == -1 and call(x=258) == -1   # x not 16-byte aligned
+    assert call(dx=264) == -1                        # dx not 16-byte aligned
+    assert call(ws=None) == -3 and call(nbytes=need - 1) == -3 and call(ws=264) == -3
