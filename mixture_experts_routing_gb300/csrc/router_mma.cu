@@ -194,9 +194,9 @@ __global__ void __launch_bounds__(kRbThreads, 1)
 // Persistent: one CTA per SM walks the (h slice, token tile) items
 // w = blockIdx.x, blockIdx.x + gridDim.x, ... (item w: rows h0 = 128 (w % h
 // tiles), tokens t0 = 128 (w / h tiles)). Per item the producer loads the dx
-// tile into one of two tile buffers and the Ep/64 operand stages into a ring
-// of two; the MMA warp accumulates into one of two TMEM accumulators; so the
-// epilogue of one item overlaps the loads and MMAs of the next.
+// tile into one of three tile buffers and the Ep/64 operand stages into a
+// ring of two; the MMA warp accumulates into one of two TMEM accumulators; so
+// the epilogue of one item overlaps the loads and MMAs of the next ones.
 struct DxMmaParams {
   int N, H, Ep;
   int h_tiles, items;
@@ -208,7 +208,8 @@ constexpr uint32_t kDxOpBytes = 128u * 128u;        // one 128-row x 64-column b
 constexpr uint32_t kDxStageBytes = 4u * kDxOpBytes;  // A hi, A lo, B hi, B lo
 constexpr uint32_t kDxTileBytes = 2u * kDxOpBytes;   // dx: 128 tokens x 128 h
 constexpr int kDxStages = 2;
-constexpr uint32_t kDxSmemBytes = kDxStages * kDxStageBytes + 2u * kDxTileBytes + 1024u;
+constexpr int kDxTiles = 3;  // dx tiles in flight (loaded ahead of their epilogue)
+constexpr uint32_t kDxSmemBytes = kDxStages * kDxStageBytes + kDxTiles * kDxTileBytes + 1024u;
 
 __global__ void __launch_bounds__(kRbThreads, 1)
     router_dx_mma_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -217,8 +218,8 @@ __global__ void __launch_bounds__(kRbThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kDxStages];
   __shared__ __align__(8) uint64_t empty_bar[kDxStages];
-  __shared__ __align__(8) uint64_t dx_full[2];
-  __shared__ __align__(8) uint64_t dx_empty[2];
+  __shared__ __align__(8) uint64_t dx_full[kDxTiles];
+  __shared__ __align__(8) uint64_t dx_empty[kDxTiles];
   __shared__ __align__(8) uint64_t acc_full[2];
   __shared__ __align__(8) uint64_t acc_empty[2];
   __shared__ uint32_t tmem_base_s;
@@ -232,9 +233,11 @@ __global__ void __launch_bounds__(kRbThreads, 1)
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kDxTiles; ++b) {
       mbar_init(smem_u32(&dx_full[b]), 1);
       mbar_init(smem_u32(&dx_empty[b]), 4);   // one arrival per epilogue warp
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
       mbar_init(smem_u32(&acc_empty[b]), 4);
     }
@@ -256,9 +259,10 @@ __global__ void __launch_bounds__(kRbThreads, 1)
     bool ok = true;
     for (int i = 0, w = blockIdx.x; ok && w < p.items; ++i, w += gridDim.x) {
       const int h0 = (w % p.h_tiles) * 128, t0 = (w / p.h_tiles) * 128;
-      const int b = i & 1;
-      const uint32_t u = (uint32_t)(i >> 1);
-      if (i >= 2 && !mbar_wait_warp(smem_u32(&dx_empty[b]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty))
+      const int b = i % kDxTiles;
+      const uint32_t u = (uint32_t)(i / kDxTiles);
+      if (i >= kDxTiles &&
+          !mbar_wait_warp(smem_u32(&dx_empty[b]), (u & 1u) ^ 1u, p.err, kErrWaitEmpty))
         break;
       if (lane == 0) {
         const uint32_t db = smem_u32(&dx_full[b]);
@@ -341,13 +345,15 @@ __global__ void __launch_bounds__(kRbThreads, 1)
       const int h0 = (w % p.h_tiles) * 128, t0 = (w / p.h_tiles) * 128;
       const int a = i & 1;
       const uint32_t u = (uint32_t)(i >> 1);
+      const int b = i % kDxTiles;
+      const uint32_t ub = (uint32_t)(i / kDxTiles);
       if (!mbar_wait_warp(smem_u32(&acc_full[a]), u & 1u, p.err, kErrWaitAccum) ||
-          !mbar_wait_warp(smem_u32(&dx_full[a]), u & 1u, p.err, kErrWaitFull))
+          !mbar_wait_warp(smem_u32(&dx_full[b]), ub & 1u, p.err, kErrWaitFull))
         break;
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)a * 128u;
       const uint8_t* tile =
-          smem_raw + (dxs0 + (uint32_t)a * kDxTileBytes - smem_u32(smem_raw));
+          smem_raw + (dxs0 + (uint32_t)b * kDxTileBytes - smem_u32(smem_raw));
       const int t = t0 + r;
       uint16_t* out = p.dx + (size_t)t * p.H + h0;
       for (int c = 0; c < 8; ++c) {
@@ -377,7 +383,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&acc_empty[a]));
-        mbar_arrive(smem_u32(&dx_empty[a]));
+        mbar_arrive(smem_u32(&dx_empty[b]));
       }
     }
   }
@@ -412,15 +418,14 @@ bool set_smem_limits(cudaError_t* err) {
   int dev = 0;
   if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return false;
   if (dev >= 0 && dev < 64 && done[dev]) return true;
-  // the largest requests: 2 stages of 80 KiB + 1 KiB (dW_r, Ep = 256) and
-  // 2 x 64 KiB + 2 x 32 KiB + 1 KiB (dx); static shared memory comes on top
-  const int lim = 200 * 1024;
+  // dW_r asks for at most 2 stages of 80 KiB + 1 KiB (Ep = 256), dx for its
+  // fixed layout; static shared memory comes on top of either
   if ((*err = cudaFuncSetAttribute(router_dwr_mma_kernel,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) !=
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) !=
           cudaSuccess ||
       (*err = cudaFuncSetAttribute(router_dx_mma_kernel,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) !=
-          cudaSuccess)
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kDxSmemBytes)) != cudaSuccess)
     return false;
   if (dev >= 0 && dev < 64) done[dev] = 1;
   return true;
