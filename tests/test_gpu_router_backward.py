@@ -43,6 +43,9 @@ SMALL = [
     (synth.Workload("rb_e160", 190, 128, 160, 6, 128, 5, 4), 1),
     # many token splits of dW_r, the last one 8 tokens long
     (synth.Workload("rb_splits", 5000, 512, 64, 6, 128, 0, 1), 1),
+    # fewer tokens than one tensor-map box (64 rows for dW_r, 128 for dx)
+    (synth.Workload("rb_n5", 5, 128, 8, 2, 128, 1, 1), 1),
+    (synth.Workload("rb_n40", 40, 256, 64, 4, 128, 1, 1), 1),
 ]
 
 
