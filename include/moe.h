@@ -364,10 +364,11 @@ const float* moe_route_workspace_logits(const moe_config_t* cfg, const void* wor
 /* ---------------------------------------------------------------- graph ladder
  * Captured CUDA graphs of the forward at a ladder of token-count buckets, for
  * batches whose size changes from call to call ("[4/5] feat: capture the FFN
- * experts at bucketed padded shapes", What this adds: an item takes the
- * smallest bucket that holds it, or runs eager when the bucket would pad it
- * past a ratio; capture runs largest-bucket-first behind one eager call at the
- * ceiling). A bucket's graph is moe_route_align + moe_ffn_forward +
+ * experts at bucketed padded shapes", What this adds). A batch of n tokens
+ * replays the first bucket >= n, or runs eagerly when n is above the top
+ * bucket or that bucket exceeds max_pad_ratio * n; graphs are captured from
+ * the top bucket down after one warm-up call at the top size. A bucket's
+ * graph is moe_route_align + moe_ffn_forward +
  * moe_combine captured at n_tokens = the bucket with n_valid set, so its
  * replay on n <= bucket tokens computes what those calls compute on exactly n
  * tokens (y bit-identical; the sentinel in sorted_slot_ids is the bucket). */
@@ -395,8 +396,8 @@ typedef struct moe_ladder moe_ladder_t; /* opaque */
  * (max_pad_ratio <= 0: no limit). buckets ascending. */
 int moe_ladder_pick(const int32_t* buckets, int n_buckets, int32_t n, float max_pad_ratio);
 
-/* Captures one graph per bucket (largest first, after one eager forward at
- * the ceiling on a private stream; synchronises that stream). top: the layer
+/* Captures one graph per bucket (from the top bucket down, after one warm-up
+ * forward at the top size on a private stream; synchronises that stream). top: the layer
  * config with n_tokens = buckets[n_buckets-1] and n_valid NULL. The buffers'
  * device memory must stay allocated, and the weights' contents in place, for
  * the ladder's lifetime (the graphs hold their addresses). *out is NULL on

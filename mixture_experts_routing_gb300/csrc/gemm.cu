@@ -767,27 +767,24 @@ cudaError_t set_smem_attr() {
 // SM count of the current device, with every instantiation's shared-memory
 // opt-in set up once per device.
 int device_sms(cudaError_t* err) {
-  static int sms[64] = {};
-  int dev = 0;
-  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && sms[dev] > 0) return sms[dev];
+  static DeviceOnce sms;
   int n = 0;
-  if ((*err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return 0;
-  if ((*err = set_smem_attr<kModeFc1, 0>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeFc1, 1>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeFc1Fp8, 0>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeFc1Fp8, 1>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeFc2, 0>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeFc2Fp8, 0>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeDgrad2, 0>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeDgrad2, 1>()) != cudaSuccess ||
-      (*err = set_smem_attr<kModeDgrad1, 0>()) != cudaSuccess) {
-    cudaGetLastError();  // reported here; do not leave it for a later launch to report
-    return 0;
-  }
-  if (dev >= 0 && dev < 64) sms[dev] = n;
-  return n;
+  *err = once_per_device(sms, &n, [](int dev, int* v) {
+    cudaError_t e = cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if ((e = set_smem_attr<kModeFc1, 0>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc1, 1>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc1Fp8, 0>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc1Fp8, 1>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc2, 0>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc2Fp8, 0>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeDgrad2, 0>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeDgrad2, 1>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeDgrad1, 0>()) != cudaSuccess)
+      cudaGetLastError();  // reported here; do not leave it for a later launch to report
+    return e;
+  });
+  return *err == cudaSuccess ? n : 0;
 }
 
 }  // namespace

@@ -1,9 +1,10 @@
 // Graph bucket ladder: captured CUDA graphs of the layer forward at a ladder
 // of token-count buckets, for batches whose size changes from call to call
 // ("[4/5] feat: capture the FFN experts at bucketed padded shapes", What this
-// adds: a ladder of buckets, an item takes the smallest bucket that holds it or
-// runs eager when the bucket would pad it past a ratio; capture runs
-// largest-bucket-first behind one eager call at the ceiling).
+// adds). A batch of n tokens replays the first bucket >= n; it runs eagerly
+// when n is above the top bucket or that bucket exceeds max_pad_ratio * n.
+// Capture goes from the top bucket down, after one warm-up call at the top
+// size.
 //
 // A bucket's graph is the three forward calls (route_align, ffn_forward,
 // combine) captured with n_tokens = the bucket and n_valid pointing at one
@@ -50,7 +51,7 @@ int moe_ladder_pick(const int32_t* buckets, int n_buckets, int32_t n, float max_
   if (!buckets || n_buckets <= 0 || n < 0) return -1;
   for (int b = 0; b < n_buckets; ++b) {
     if (buckets[b] < n) continue;
-    // a replay pays for its whole bucket: too much padding runs eager instead
+    // a replay costs the bucket's full size, so a batch far below it goes eager
     if (max_pad_ratio > 0.0f && n > 0 && (double)buckets[b] > (double)max_pad_ratio * n)
       return -1;
     return b;
@@ -80,7 +81,7 @@ int moe_ladder_create(const moe_config_t* top, const int32_t* buckets, int n_buc
   cudaStream_t cs = nullptr;
   int rc = MOE_OK;
   if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) rc = MOE_ERR_CUDA;
-  // one eager call at the ceiling first: every lazily set kernel attribute and
+  // one warm-up call at the top size first: every lazily set kernel attribute and
   // looked-up symbol is in place before any capture
   if (rc == MOE_OK) rc = forward_calls(&L->top, &L->bufs, cs);
   if (rc == MOE_OK && cudaStreamSynchronize(cs) != cudaSuccess) rc = MOE_ERR_CUDA;

@@ -4,7 +4,42 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace moe {
+
+constexpr int kMaxDevices = 64;
+
+// One-time, per-device set-up (shared-memory opt-ins, SM counts): `fn(dev,
+// &v)` runs for the current device under a lock until it succeeds with v > 0;
+// later calls read v without locking. Safe when several host threads make
+// their first call on a device at the same time.
+struct DeviceOnce {
+  std::mutex mu;
+  std::atomic<int> value[kMaxDevices];
+};
+
+template <class Fn>
+inline cudaError_t once_per_device(DeviceOnce& o, int* value, Fn fn) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int v = o.value[dev].load(std::memory_order_acquire);
+  if (v <= 0) {
+    std::lock_guard<std::mutex> lock(o.mu);
+    v = o.value[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+      err = fn(dev, &v);
+      if (err != cudaSuccess) return err;
+      if (v <= 0) v = 1;
+      o.value[dev].store(v, std::memory_order_release);
+    }
+  }
+  if (value) *value = v;
+  return cudaSuccess;
+}
 
 // Launch of a forward-path kernel with programmatic stream serialization: it
 // may start (setup, then griddep_wait) while the previous kernel in the

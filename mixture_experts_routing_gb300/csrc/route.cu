@@ -434,24 +434,21 @@ cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaS
     ty = kTyMax;
     bm = ty * kRTM;
   }
-  static int set_for[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static DeviceOnce smem_set;
+  cudaError_t err = once_per_device(smem_set, nullptr, [&](int, int*) {
+    cudaError_t e = cudaFuncSetAttribute(router_logits_kernel<TX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)router_smem_bytes(kTyMax * kRTM, BN, kTyMax));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(router_logits_tma_kernel<TX, 32, 4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)router_tma_layout<32, 4>(kTyMax * kRTM, BN, kTyMax).total);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(router_logits_tma_kernel<TX, 64, 2>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)router_tma_layout<64, 2>(kTyMax * kRTM, BN, kTyMax).total);
+  });
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64 || !set_for[dev]) {
-    err = cudaFuncSetAttribute(router_logits_kernel<TX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)router_smem_bytes(kTyMax * kRTM, BN, kTyMax));
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(router_logits_tma_kernel<TX, 32, 4>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)router_tma_layout<32, 4>(kTyMax * kRTM, BN, kTyMax).total);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(router_logits_tma_kernel<TX, 64, 2>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)router_tma_layout<64, 2>(kTyMax * kRTM, BN, kTyMax).total);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) set_for[dev] = 1;
-  }
   dim3 g(gx, (a.N + bm - 1) / bm);
   // TMA form: W_r rows a multiple of 16 bytes, boxes inside the tensors
   const bool tma = vec4 && a.E >= BN && a.err &&
@@ -1045,19 +1042,17 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   cudaError_t err = cudaSuccess;
   {
     // raise the kernel's dynamic shared-memory limit once per device
-    static int set_for[64] = {};
-    int dev = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return -(int)err;
-    if (dev < 0 || dev >= 64 || !set_for[dev]) {
-      err = cudaFuncSetAttribute(route_select_kernel<1024>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxTokens * 8);
-      if (err != cudaSuccess) return -(int)err;
-      err = cudaFuncSetAttribute(route_select_kernel<kSelSmallThreads>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSelSmallThreads * kTokensPerChunk * 8);
-      if (err != cudaSuccess) return -(int)err;
-      if (dev >= 0 && dev < 64) set_for[dev] = 1;
-    }
+    static DeviceOnce smem_set;
+    err = once_per_device(smem_set, nullptr, [](int, int*) {
+      cudaError_t e = cudaFuncSetAttribute(route_select_kernel<1024>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kMaxTokens * 8);
+      if (e != cudaSuccess) return e;
+      return cudaFuncSetAttribute(route_select_kernel<kSelSmallThreads>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSelSmallThreads * kTokensPerChunk * 8);
+    });
+    if (err != cudaSuccess) return -(int)err;
   }
   // the narrow CTA for batches of at most 2048 tokens: an expert can hold every
   // token, and above that many keys per thread (a Zipf-skewed 8192-token batch:

@@ -414,21 +414,17 @@ __global__ void router_split_w_kernel(const float* __restrict__ wr, int H, int E
 }
 
 bool set_smem_limits(cudaError_t* err) {
-  static int done[64] = {};
-  int dev = 0;
-  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return false;
-  if (dev >= 0 && dev < 64 && done[dev]) return true;
-  // dW_r asks for at most 2 stages of 80 KiB + 1 KiB (Ep = 256), dx for its
-  // fixed layout; static shared memory comes on top of either
-  if ((*err = cudaFuncSetAttribute(router_dwr_mma_kernel,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) !=
-          cudaSuccess ||
-      (*err = cudaFuncSetAttribute(router_dx_mma_kernel,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kDxSmemBytes)) != cudaSuccess)
-    return false;
-  if (dev >= 0 && dev < 64) done[dev] = 1;
-  return true;
+  static DeviceOnce done;
+  *err = once_per_device(done, nullptr, [](int, int*) {
+    // dW_r asks for at most 2 stages of 80 KiB + 1 KiB (Ep = 256), dx for its
+    // fixed layout; static shared memory comes on top of either
+    cudaError_t e = cudaFuncSetAttribute(router_dwr_mma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(router_dx_mma_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmemBytes);
+  });
+  return *err == cudaSuccess;
 }
 
 }  // namespace

@@ -355,20 +355,17 @@ __global__ void __launch_bounds__(kWThreads, 1)
 }
 
 int wgrad_sms(cudaError_t* err) {
-  static int sms[64] = {};
-  int dev = 0;
-  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && sms[dev] > 0) return sms[dev];
+  static DeviceOnce sms;
   int n = 0;
-  if ((*err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return 0;
-  if ((*err = cudaFuncSetAttribute(moe_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kWSmemBudget)) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  if (dev >= 0 && dev < 64) sms[dev] = n;
-  return n;
+  *err = once_per_device(sms, &n, [](int dev, int* v) {
+    cudaError_t e = cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(moe_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kWSmemBudget);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
+  });
+  return *err == cudaSuccess ? n : 0;
 }
 
 }  // namespace

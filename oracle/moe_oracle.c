@@ -403,9 +403,9 @@ int oracle_forward_tokens(int t0, int t1, int K, int H, int I, const uint16_t* x
 
 /* ======================================================================== */
 /* Dropless, bucketed variant ("[4/5] feat: capture the FFN experts at      */
-/* bucketed padded shapes", What this adds: a ladder of buckets built as    */
-/* multiples of the expected item size; an item takes the smallest bucket   */
-/* that holds it, and runs unpadded when none does).                        */
+/* bucketed padded shapes", What this adds): the rungs are multiples of the */
+/* expected rows per expert; an expert's extent is the first rung at or     */
+/* above its count, or its count rounded to the block when no rung fits.   */
 /* Per expert: rung_j = roundup(ceil(num_j*R / (den*E)), bm) with R = N*K;  */
 /* extent_e = the smallest rung >= count_e, else roundup(count_e, bm).      */
 /* Nothing is dropped. Expert e's slots start at the exclusive scan of the  */

@@ -1,5 +1,5 @@
-"""Bucket choice of the graph ladder (host logic, no GPU): the smallest bucket
-that holds the batch, eager above the top bucket or past the padding ratio
+"""Bucket choice of the graph ladder (host logic, no GPU): the first bucket at
+or above the batch size, eager above the top bucket or past the padding ratio
 ("[4/5] feat: capture the FFN experts at bucketed padded shapes", What this
 adds)."""
 import pytest
