@@ -379,7 +379,7 @@ def host_inputs(w, rank_seed):
     N, H, E = w.n_tokens, w.hidden, w.n_experts
     x_bits = synth.normal_bf16_bits(rank_seed, synth.STREAM["x"], 0, N * H, w.x_std).reshape(N, H)
     wr = synth.normal_f32(w.seed, synth.STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E)
-    bias = synth.zipf_bias(w.seed, E, w.zipf_s) if w.zipf_s is not None else None
+    bias = synth.router_bias(w)
     return x_bits, wr, bias
 
 
@@ -1013,7 +1013,8 @@ def run_ours_serve(args):
     top = moe.Config(Ntop, H, E, K, I, w.cap_num, w.cap_den, block_m=args.block_m,
                      ladder=list(w.ladder), ladder_den=w.ladder_den)
     wr = torch.from_numpy(synth.normal_f32(w.seed, synth.STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E)).to(dev)
-    bias = None if w.zipf_s is None else torch.from_numpy(synth.zipf_bias(w.seed, E, w.zipf_s)).to(dev)
+    bias = synth.router_bias(w)
+    bias = None if bias is None else torch.from_numpy(bias).to(dev)
     bf = dict(dtype=torch.bfloat16, device=dev)
     w13, w2 = torch.empty((E, 2 * I, H), **bf), torch.empty((E, H, I), **bf)
     tmp, wu = torch.empty((E, H, I), **bf), torch.empty((E, H, I), **bf)

@@ -20,7 +20,7 @@ must give the same bits):
    round-to-nearest-even.
 
 Streams per tensor: x=0, W_r=1, W_gate=2, W_up=3, W_down=4, bias/permutation=5,
-dY=6. Expert weight tensors are indexed in their logical layout
+dY=6, calibration tokens (used only to fit a stored router bias)=7. Expert weight tensors are indexed in their logical layout
 (``W_gate[e,h,i]`` at ``(e*H + h)*I + i``), so any slice can be regenerated
 without the rest.
 """
@@ -34,10 +34,11 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "STREAM", "normal_f32", "normal_bf16_bits",
-    "bf16_bits_to_f32", "f32_to_bf16_bits", "zipf_bias", "make_host_inputs",
+    "bf16_bits_to_f32", "f32_to_bf16_bits", "zipf_bias", "zipf_ranks", "zipf_target_shares",
+    "router_bias", "load_router_bias", "make_host_inputs",
 ]
 
-STREAM = {"x": 0, "wr": 1, "wg": 2, "wu": 3, "wd": 4, "bias": 5, "dy": 6}
+STREAM = {"x": 0, "wr": 1, "wg": 2, "wu": 3, "wd": 4, "bias": 5, "dy": 6, "xcal": 7}
 
 _G = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
@@ -196,18 +197,87 @@ def normal_bf16_bits(seed: int, stream: int, start: int, count: int, std: float 
     return out
 
 
-def zipf_bias(seed: int, n_experts: int, s: float) -> np.ndarray:
-    """Per-expert router bias ``b_e = -s * ln(rank_e)``.
-
-    ``rank_e`` (1-based) comes from a seeded permutation: experts ordered by
-    the SplitMix64 output of stream 5 at index e. Adding ``b`` to the logits
-    scales each expert's softmax weight by ``rank^-s``, a Zipf(s) popularity.
-    """
+def zipf_ranks(seed: int, n_experts: int) -> np.ndarray:
+    """Popularity rank of each expert (1 = most popular): experts ordered by
+    the SplitMix64 output of stream 5 at index e."""
     h = _hash(seed, STREAM["bias"], np.arange(n_experts, dtype=np.uint64))
     order = np.argsort(h, kind="stable")
     rank = np.empty(n_experts, dtype=np.int64)
     rank[order] = np.arange(1, n_experts + 1)
+    return rank
+
+
+def zipf_bias(seed: int, n_experts: int, s: float) -> np.ndarray:
+    """Per-expert router bias ``b_e = -s * ln(rank_e)`` (ranks from
+    ``zipf_ranks``). Adding ``b`` to the logits scales each expert's softmax
+    weight by ``rank^-s``; the route shares that top-K selection then gives
+    are steeper than Zipf(s) at the head, so the named workloads use a
+    calibrated bias instead (``router_bias``)."""
+    rank = zipf_ranks(seed, n_experts)
     return (-s * np.log(rank.astype(np.float64))).astype(np.float32)
+
+
+def zipf_target_shares(n_experts: int, top_k: int, s: float) -> np.ndarray:
+    """Target route share of each popularity rank (index r-1 for rank r):
+    Zipf(s), ``share_r`` proportional to ``r^-s``, summing to 1, with no share
+    above 1/K (a token picks an expert at most once, so an expert can hold at
+    most N of the N*K routes). Shares over the cap are set to 1/K and the
+    others scaled up to keep the sum at 1, repeated until none exceeds it."""
+    w = np.arange(1, n_experts + 1, dtype=np.float64) ** (-float(s))
+    cap = 1.0 / top_k
+    clipped = np.zeros(n_experts, dtype=bool)
+    while True:
+        free = 1.0 - cap * clipped.sum()
+        share = np.where(clipped, cap, w * free / w[~clipped].sum())
+        over = (share > cap * (1 + 1e-12)) & ~clipped
+        if not over.any():
+            return share
+        clipped |= over
+
+
+_BIAS_DIR = __import__("os").path.join(_HERE, "data")
+
+
+def router_bias_path(name: str) -> str:
+    return __import__("os").path.join(_BIAS_DIR, "router_bias_%s.txt" % name)
+
+
+def load_router_bias(name: str, n_experts: int) -> Optional[np.ndarray]:
+    """The stored, calibrated router bias of workload ``name`` (fp32 [E]), or
+    None when the workload has none. File format: '#' comments, then one line
+    per expert: ``e bits`` with ``bits`` the fp32 bit pattern in hex."""
+    import os
+    path = router_bias_path(name)
+    if not os.path.exists(path):
+        return None
+    bits = np.zeros(n_experts, dtype=np.uint32)
+    seen = np.zeros(n_experts, dtype=bool)
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if not line:
+                continue
+            e = int(line[0])
+            bits[e] = int(line[1], 16)
+            seen[e] = True
+    if not seen.all():
+        raise ValueError("%s: %d of %d experts missing" % (path, int((~seen).sum()), n_experts))
+    return bits.view(np.float32).copy()
+
+
+def router_bias(w: "Workload") -> Optional[np.ndarray]:
+    """Router bias of a workload: none for a balanced router; for a Zipf(s)
+    workload the stored bias calibrated so that route shares follow Zipf(s)
+    (capped at 1/K) when one exists for its name and expert count, else
+    ``zipf_bias`` (the small test layers)."""
+    if w.zipf_s is None:
+        return None
+    if w.calibrated_bias:
+        b = load_router_bias(w.calibrated_bias, w.n_experts)
+        if b is None:
+            raise FileNotFoundError(router_bias_path(w.calibrated_bias))
+        return b
+    return zipf_bias(w.seed, w.n_experts, w.zipf_s)
 
 
 @dataclass(frozen=True)
@@ -230,6 +300,7 @@ class Workload:
     sweep: tuple = field(default=())
     ladder: tuple = field(default=())   # dropless: rung multipliers (numerators)
     ladder_den: int = 1
+    calibrated_bias: str = ""           # name of the stored calibrated router bias, if any
 
     def with_tokens(self, n: int) -> "Workload":
         d = dict(self.__dict__)
@@ -243,6 +314,7 @@ WORKLOADS = {
     "qwen3_small": Workload("qwen3_small", 1024, 512, 8, 2, 1024, 5, 4,
                             note="small Qwen3-MoE-style layer: N=1024 (2x512), H=512, E=8, top-2, I=1024, F=1.25"),
     "qwen3_30b": Workload("qwen3_30b", 8192, 2048, 128, 8, 768, 1, 1, zipf_s=1.0,
+                          calibrated_bias="qwen3_30b",
                           note="Qwen3-30B-A3B-shaped layer: N=8192, H=2048, E=128, top-8, I=768, F=1.0, Zipf(1.0) router bias"),
     "dsv3": Workload("dsv3", 4096, 7168, 256, 8, 2048, 5, 4, w_std=0.006,
                      note="DeepSeek-V3-shaped layer: N=4096, H=7168, E=256, top-8, I=2048, F=1.25, balanced router"),
@@ -258,11 +330,11 @@ WORKLOADS = {
     # routes per expert) with 16 experts and N=4096, about 3 GB on the device
     "dropless_e16": Workload("dropless_e16", 4096, 4096, 16, 6, 1408, 0, 1, zipf_s=0.8,
                              note="dropless per-expert shapes with 16 experts, N=4096 (ncu profiling case)",
-                             ladder=(2, 3, 4, 5, 6, 8), ladder_den=4),
+                             ladder=(2, 3, 4, 5, 6, 8), ladder_den=4, calibrated_bias="dropless_e16"),
     "dropless": Workload("dropless", 16384, 4096, 64, 6, 1408, 0, 1, zipf_s=0.8,
                          note="dropless bucketed layer: H=4096, E=64, top-6, I=1408, N swept 128..16384, Zipf(0.8)",
                          sweep=tuple(2 ** k for k in range(7, 15)),
-                         ladder=(2, 3, 4, 5, 6, 8), ladder_den=4),
+                         ladder=(2, 3, 4, 5, 6, 8), ladder_den=4, calibrated_bias="dropless"),
 }
 
 
@@ -276,7 +348,7 @@ def make_host_inputs(w: Workload, experts: Optional[list] = None) -> dict:
     out = {
         "x": normal_bf16_bits(w.seed, STREAM["x"], 0, N * H, w.x_std).reshape(N, H),
         "wr": normal_f32(w.seed, STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E),
-        "bias": (zipf_bias(w.seed, E, w.zipf_s) if w.zipf_s is not None else None),
+        "bias": router_bias(w),
     }
     ids = range(E) if experts is None else experts
     for name in ("wg", "wu"):

@@ -65,8 +65,8 @@ class Problem:
         self.x_bits = (x_bits if x_bits is not None
                        else synth.normal_bf16_bits(w.seed, synth.STREAM["x"], 0, N * H, w.x_std).reshape(N, H))
         self.wr = synth.normal_f32(w.seed, synth.STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E)
-        if bias is None and w.zipf_s is not None:
-            bias = synth.zipf_bias(w.seed, E, w.zipf_s)
+        if bias is None:
+            bias = synth.router_bias(w)
         self.bias = bias
         self.x = bf16_dev(self.x_bits, self.dev) if N > 0 else torch.empty((1, H), dtype=torch.bfloat16, device=self.dev)
         self.wr_d = torch.from_numpy(self.wr).to(self.dev)
