@@ -72,6 +72,9 @@ def parse_args(argv=None):
                     help="gated activation of FC1 (forward and training steps)")
     ap.add_argument("--prob-in-act", action="store_true",
                     help="p' multiplies FC1's activation; the combine sums with unit weights")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default run only: skip the Qwen3-30B-shaped forward and the dropless "
+                         "training step reported beside the headline")
     args = ap.parse_args(argv)
     if args.fp8 and (args.activation != "swiglu" or args.prob_in_act):
         ap.error("--fp8 runs the SwiGLU layer with p' in the combine")
@@ -151,7 +154,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -440,7 +443,11 @@ def run_reference(args):
     value = len(vals) / sum(1.0 / v for v in vals)  # tokens over total extrapolated time
     out = {
         "impl": "reference", "metric": METRIC_TRAIN if train else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.n_tokens / value * 1e3,
+        "steps": args.steps, "warmup": args.warmup,
+        # the host time each timed step actually took (its bounded sample), and
+        # the time the oracle would need for the whole step at the same rate
+        "ms_per_step": wall / max(1, args.steps) * 1e3,
+        "ms_per_step_extrapolated": w.n_tokens / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": {"workload": w.name, "description": w.note, "block_m": args.block_m,
                                         "parallelism": "single host, OpenMP",
@@ -456,7 +463,88 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- our arm
+class GpuCtx:
+    """This rank's device and process group."""
+
+    def __init__(self):
+        import torch
+        self.world, self.rank, self.local = dist_env()
+        if not torch.cuda.is_available():
+            raise RuntimeError("bench.py needs a CUDA device")
+        self.dev = torch.device("cuda", self.local)
+        torch.cuda.set_device(self.dev)
+        self.dist = init_dist(self.world, "nccl")
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+def steps_for(ms_per_step: float, target_ms: float = 1500.0, lo: int = 100, hi: int = 5000) -> int:
+    """Steps that make a timed region of about target_ms (long enough for
+    several clock samples)."""
+    return int(min(hi, max(lo, -(-target_ms // max(ms_per_step, 1e-3)))))
+
+
+def routing_summary(w, expert_counts, kept_counts, cap):
+    """Realised routing of one batch: kept and dropped routes, experts at
+    capacity and, for a Zipf workload, route shares against the target by
+    popularity rank."""
+    import numpy as np
+    import synth
+    ec = np.asarray(expert_counts, np.int64)
+    kc = np.asarray(kept_counts, np.int64)
+    R = w.n_tokens * w.top_k
+    d = {"routes": R, "kept_routes": int(kc.sum()), "dropped_routes": int(R - kc.sum()),
+         "experts_at_capacity": int((ec >= cap).sum()) if cap else 0,
+         "experts_without_routes": int((ec == 0).sum())}
+    if w.zipf_s is not None:
+        ranks = synth.zipf_ranks(w.seed, w.n_experts)
+        target = synth.zipf_target_shares(w.n_experts, w.top_k, w.zipf_s)
+        share = np.empty(w.n_experts)
+        share[ranks - 1] = ec / max(1, R)
+        rel = share / target - 1.0
+        n64 = min(64, w.n_experts)
+        d.update({"zipf_s": w.zipf_s,
+                  "share_by_rank_top8": [round(float(v), 5) for v in share[:8]],
+                  "target_by_rank_top8": [round(float(v), 5) for v in target[:8]],
+                  "ranks_within_10pct_of_target": "%d of ranks 1-%d" % (
+                      int((np.abs(rel[:n64]) <= 0.10).sum()), n64),
+                  "max_rel_dev_ranks_1_64": float(np.abs(rel[:n64]).max())})
+    return d
+
+
 def run_ours(args):
+    ctx = GpuCtx()
+    out = forward_bench(args, ctx, args.workload, args.steps, args.warmup, full=True)
+    extras = (not args.no_extras and ctx.world == 1 and args.workload == "dsv3" and not args.fp8
+              and args.activation == "swiglu" and not args.prob_in_act)
+    if extras:
+        import torch
+        torch.cuda.empty_cache()
+        q = forward_bench(args, ctx, "qwen3_30b", None, 10, full=False)
+        out["qwen3_30b_forward"] = {k: q[k] for k in (
+            "value", "unit", "steps", "ms_per_step", "config", "roofline", "grouped_gemm",
+            "graph", "kernels_ms", "kernels", "routing", "clocks", "gpu_launches")}
+        torch.cuda.empty_cache()
+        t = train_bench(args, ctx, "dropless", None, 5, sweep=False, full=False)
+        out["dropless_train"] = {k: t[k] for k in (
+            "metric", "value", "unit", "steps", "ms_per_step", "config", "roofline",
+            "tflops_fwd_bwd", "pct_bf16_peak_fwd_bwd", "calls_ms", "routing", "clocks",
+            "gpu_launches")}
+        out["extra_lines"] = ("qwen3_30b_forward and dropless_train: the Qwen3-30B-A3B-shaped "
+                              "forward and the dropless N=16384 training step, each timed in a "
+                              "region of its own (about 1.5 s) with its own clock record")
+    if ctx.rank == 0:
+        print(json.dumps(out))
+    ctx.close()
+    return 0
+
+
+def forward_bench(args, ctx, wname, steps, warmup, full=True):
+    """One forward workload timed on this rank. steps None: enough steps for
+    about 1.5 s of timed work. full: also the end-to-end leg with host copies
+    and the CPU baseline. Returns the JSON object (printed by the caller)."""
     import numpy as np
     import torch
 
@@ -464,13 +552,8 @@ def run_ours(args):
     import synth
     import synth.gpu
 
-    world, rank, local = dist_env()
-    if not torch.cuda.is_available():
-        raise RuntimeError("bench.py needs a CUDA device")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist = init_dist(world, "nccl")
-    w = synth.WORKLOADS[args.workload]
+    world, rank, dev, dist = ctx.world, ctx.rank, ctx.dev, ctx.dist
+    w = synth.WORKLOADS[wname]
     N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
     cfg = moe.Config(N, H, E, K, I, w.cap_num, w.cap_den, block_m=args.block_m,
                      activation=act_code(args), prob_in_act=args.prob_in_act)
@@ -547,15 +630,23 @@ def run_ours(args):
         moe.combine(cfg, routes, o, yb, s)
         mark(len(names))
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step()
     torch.cuda.synchronize()
     if moe.device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
+    if steps is None:  # size the timed region from a short untimed probe
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for _ in range(10):
+            step()
+        p1.record(stream)
+        torch.cuda.synchronize()
+        steps = steps_for(p0.elapsed_time(p1) / 10)
 
     # ---- device-timed region
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
-           for _ in range(args.steps)]
+           for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, dev)
     torch.cuda.synchronize()
@@ -563,7 +654,7 @@ def run_ours(args):
     time.sleep(0.3)  # let the sampler start before the timed work
     launches0 = moe.launch_count()
     start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         step(evs[i])
     end.record(stream)
     torch.cuda.synchronize()
@@ -571,11 +662,12 @@ def run_ours(args):
     barrier(dist, dev)
     clk = clocks.stop()
     ms_total = max_over_ranks(start.elapsed_time(end), dist, dev)
-    per_kernel = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+    per_kernel = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
                   for j, n in enumerate(names)}
     if moe.device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
     kept_counts = routes.kept_counts.cpu().numpy()
+    expert_counts = routes.expert_counts.cpu().numpy()
     used_slots = int(routes.num_tokens_post_padded.cpu()[0])
 
     # ---- the whole forward captured as one CUDA graph: 10 warm-up replays,
@@ -590,7 +682,7 @@ def run_ours(args):
     stream.wait_stream(gstream)
     for _ in range(10):
         graph.replay()
-    reps = max(20, min(args.steps, 50))
+    reps = max(20, min(steps, 50))
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
     torch.cuda.synchronize()
@@ -609,6 +701,97 @@ def run_ours(args):
     # stream: step i+2's x copy and step i's y copy run under the compute of
     # the steps between (the first two x copies and the last y copies are
     # inside the timed region too).
+    ms_e2e = e2e_forward(ctx, stream, step, x, y, x_bits, N, H, steps) if full else None
+
+    model = work_model(w, kept_counts, fp8=fp8, slots=used_slots)
+    dom = max(names, key=lambda n: per_kernel[n])
+    roof = roofline_for(dom, model, per_kernel[dom], peaks, w.name, fp8=fp8)
+    kernels = {n: roofline_for(n, model, per_kernel[n], peaks, w.name, fp8=fp8) for n in names}
+    gemm_ms = per_kernel["fc1"] + per_kernel["fc2"]
+    gemm_flops = model["fc1"]["flops"] + model["fc2"]["flops"]
+    issued = 2.0 * 3 * H * I * E * moe.capacity(cfg)
+    # the GEMMs' own bound: the weights of the active experts streamed once at
+    # the measured HBM rate, or the useful flops at the bf16 peak
+    gemm_bound_ms = max((model["fc1"]["bytes"] + model["fc2"]["bytes"]) / (peaks["hbm_gbs"] * 1e9),
+                        gemm_flops / (peaks["bf16_tflops"] * (2 if fp8 else 1) * 1e12)) * 1e3
+
+    tokens = N * world * steps
+    value = tokens / (ms_total / 1e3)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_total / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "description": w.note, "tokens_per_step_per_gpu": N,
+                   "block_m": args.block_m, "capacity": moe.capacity(cfg),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": ("inputs larger than L2 (%.1f GB of expert weights); no flush"
+                          % (weight_bytes / 1e9)) if weight_bytes > 129e6 else
+                         "expert weights (%.1f MB) fit in L2; no flush" % (weight_bytes / 1e6),
+                   **variant_config(args)},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "grouped_gemm": {"ms": gemm_ms, "tflops_useful": gemm_flops / (gemm_ms / 1e3) / 1e12,
+                         "pct_bf16_peak": gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                         "operands": "e4m3" if fp8 else "bf16",
+                         "bound_ms": gemm_bound_ms, "frac_of_bound": gemm_bound_ms / gemm_ms,
+                         # the flops a fixed-capacity layer would issue (every slot of
+                         # E x cap, empty ones included) over the same time: an
+                         # equivalent rate, above the peak when many slots are empty,
+                         # since the kernels skip slots past each expert's kept count
+                         "tflops_capacity_equivalent": issued / (gemm_ms / 1e3) / 1e12,
+                         "capacity_slots_used": model["_kept"] / max(1, E * moe.capacity(cfg)),
+                         "kept_routes": model["_kept"], "active_experts": model["_active"]},
+        "graph": {"replays": reps, "warmup_replays": 10, "kernels_per_replay": graph_kernels,
+                  "median_ms": g_med, "min_ms": g_ms[0],
+                  "tokens_per_s_median": N / (g_med / 1e3), "tokens_per_s_min_ms": N / (g_ms[0] / 1e3)},
+        "kernels_ms": per_kernel,
+        "kernels": {n: {k: v for k, v in kernels[n].items() if k in ("bound", "achieved", "unit", "frac")}
+                    for n in names},
+        "routing": routing_summary(w, expert_counts, kept_counts, moe.capacity(cfg)),
+        "clocks": clk,
+    }
+    if full:
+        out["e2e"] = {"value": N * world * steps / (ms_e2e / 1e3), "unit": UNIT,
+                      "h2d_bytes_per_step": N * H * 2, "d2h_bytes_per_step": N * H * 2,
+                      "copies": "pinned host x in and y out every step, on a second stream with two "
+                                "device buffers each, overlapping the compute of neighbouring steps"}
+    if fp8:
+        out["config"]["precision"] = ("E4M3 GEMM operands with one fp32 scale per row (w13, w2 "
+                                      "rows once; x and h rows every step), fp32 accumulation; "
+                                      "x, h, o, y in bf16")
+        out["weight_quantisation_ms"] = quant_ms
+    if full and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if fp8:
+            v, desc, secs, cores = time_oracle_sample_fp8(w, x_bits, wr_h, bias_h, args.block_m,
+                                                          min(args.cpu_experts, 2))
+        else:
+            v, desc, secs, cores = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
+                                                      args.cpu_experts, act=act_code(args),
+                                                      prob_in_act=args.prob_in_act)
+        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": desc, "cpu_seconds": secs, "host_cpus": os.cpu_count()}
+        if N * H <= 1024 * 512 and not fp8:  # the small layers: also on one thread
+            import oracle
+            threads = oracle.num_threads()
+            oracle.set_num_threads(1)
+            try:
+                v1, desc1, secs1, _ = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
+                                                         args.cpu_experts, act=act_code(args),
+                                                         prob_in_act=args.prob_in_act)
+            finally:
+                oracle.set_num_threads(threads)
+            out["cpu_baseline"]["single_thread"] = {"value": v1, "unit": UNIT, "cores": 1,
+                                                    "sample": desc1, "cpu_seconds": secs1}
+    return out
+
+
+def e2e_forward(ctx, stream, step, x, y, x_bits, N, H, steps):
+    """Milliseconds (max over ranks) of `steps` forwards, each copying its x in
+    from pinned host memory and its y out to pinned host memory."""
+    import numpy as np
+    import torch
+    dev, dist = ctx.dev, ctx.dist
     x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     y_host = [torch.empty((N, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     x_dev, y_dev = [x, torch.empty_like(x)], [y, torch.empty_like(y)]
@@ -642,88 +825,11 @@ def run_ours(args):
     barrier(dist, dev)
     torch.cuda.synchronize()
     e0.record(stream)
-    e2e_run(args.steps, e0)
+    e2e_run(steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(dist, dev)
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist, dev)
-
-    model = work_model(w, kept_counts, fp8=fp8, slots=used_slots)
-    dom = max(names, key=lambda n: per_kernel[n])
-    roof = roofline_for(dom, model, per_kernel[dom], peaks, w.name, fp8=fp8)
-    kernels = {n: roofline_for(n, model, per_kernel[n], peaks, w.name, fp8=fp8) for n in names}
-    gemm_ms = per_kernel["fc1"] + per_kernel["fc2"]
-    gemm_flops = model["fc1"]["flops"] + model["fc2"]["flops"]
-    issued = 2.0 * 3 * H * I * E * moe.capacity(cfg)
-
-    tokens = N * world * args.steps
-    value = tokens / (ms_total / 1e3)
-    out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
-        "data": "synthetic",
-        "config": {"workload": w.name, "description": w.note, "tokens_per_step_per_gpu": N,
-                   "block_m": args.block_m, "capacity": moe.capacity(cfg),
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (%.1f GB of expert weights); no flush"
-                         % (weight_bytes / 1e9), **variant_config(args)},
-        "gpu_launches": launches,
-        "e2e": {"value": N * world * args.steps / (ms_e2e / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": N * H * 2, "d2h_bytes_per_step": N * H * 2,
-                "copies": "pinned host x in and y out every step, on a second stream with two "
-                          "device buffers each, overlapping the compute of neighbouring steps"},
-        "roofline": roof,
-        "grouped_gemm": {"ms": gemm_ms, "tflops_useful": gemm_flops / (gemm_ms / 1e3) / 1e12,
-                         "pct_bf16_peak": gemm_flops / (gemm_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
-                         "operands": "e4m3" if fp8 else "bf16",
-                         # the flops a fixed-capacity layer would issue (every slot of
-                         # E x cap, empty ones included) over the same time: an
-                         # equivalent rate, above the peak when many slots are empty,
-                         # since the kernels skip slots past each expert's kept count
-                         "tflops_capacity_equivalent": issued / (gemm_ms / 1e3) / 1e12,
-                         "capacity_slots_used": model["_kept"] / max(1, E * moe.capacity(cfg)),
-                         "kept_routes": model["_kept"], "active_experts": model["_active"]},
-        "graph": {"replays": reps, "warmup_replays": 10, "kernels_per_replay": graph_kernels,
-                  "median_ms": g_med, "min_ms": g_ms[0],
-                  "tokens_per_s_median": N / (g_med / 1e3), "tokens_per_s_min_ms": N / (g_ms[0] / 1e3)},
-        "kernels_ms": per_kernel,
-        "kernels": {n: {k: v for k, v in kernels[n].items() if k in ("bound", "achieved", "unit", "frac")}
-                    for n in names},
-        "clocks": clk,
-    }
-    if fp8:
-        out["config"]["precision"] = ("E4M3 GEMM operands with one fp32 scale per row (w13, w2 "
-                                      "rows once; x and h rows every step), fp32 accumulation; "
-                                      "x, h, o, y in bf16")
-        out["weight_quantisation_ms"] = quant_ms
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        if fp8:
-            v, desc, secs, cores = time_oracle_sample_fp8(w, x_bits, wr_h, bias_h, args.block_m,
-                                                          min(args.cpu_experts, 2))
-        else:
-            v, desc, secs, cores = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
-                                                      args.cpu_experts, act=act_code(args),
-                                                      prob_in_act=args.prob_in_act)
-        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                               "sample": desc, "cpu_seconds": secs, "host_cpus": os.cpu_count()}
-        if N * H <= 1024 * 512 and not fp8:  # the small layers: also on one thread
-            import oracle
-            threads = oracle.num_threads()
-            oracle.set_num_threads(1)
-            try:
-                v1, desc1, secs1, _ = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
-                                                         args.cpu_experts, act=act_code(args),
-                                                         prob_in_act=args.prob_in_act)
-            finally:
-                oracle.set_num_threads(threads)
-            out["cpu_baseline"]["single_thread"] = {"value": v1, "unit": UNIT, "cores": 1,
-                                                    "sample": desc1, "cpu_seconds": secs1}
-    if rank == 0:
-        print(json.dumps(out))
-    if dist is not None:
-        dist.destroy_process_group()
-    return 0
+    return max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
 
 # ----------------------------------------------------------------------------- training step (dropless)
@@ -760,6 +866,19 @@ def time_oracle_train_sample(w, x_bits, dy_bits, wr, bias, bm, n_routes=4096, se
 
 
 def run_ours_train(args):
+    ctx = GpuCtx()
+    out = train_bench(args, ctx, args.workload, args.steps, args.warmup, sweep=True, full=True)
+    if ctx.rank == 0:
+        print(json.dumps(out))
+    ctx.close()
+    return 0
+
+
+def train_bench(args, ctx, wname, steps, warmup, sweep=True, full=True):
+    """Training step of the dropless layer timed on this rank at its full
+    token count (and, with sweep, over the N sweep). steps None: enough steps
+    for about 1.5 s of timed work. full: also the end-to-end leg with host
+    copies and the CPU baseline. Returns the JSON object."""
     import numpy as np
     import torch
 
@@ -767,13 +886,9 @@ def run_ours_train(args):
     import synth
     import synth.gpu
 
-    world, rank, local = dist_env()
-    if not torch.cuda.is_available():
-        raise RuntimeError("bench.py needs a CUDA device")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist = init_dist(world, "nccl")
-    base = synth.WORKLOADS[args.workload]
+    world, rank, dev, dist = ctx.world, ctx.rank, ctx.dev, ctx.dist
+    do_sweep = sweep
+    base = synth.WORKLOADS[wname]
     peaks = load_peaks()
     H, E, K, I = base.hidden, base.n_experts, base.top_k, base.inter
     bf = dict(dtype=torch.bfloat16, device=dev)
@@ -862,13 +977,13 @@ def run_ours_train(args):
 
     # ---- sweep over N (the curve), then the headline at N = base.n_tokens
     sweep = {}
-    for N in base.sweep:
+    for N in (base.sweep if do_sweep else ()):
         if N == base.n_tokens:
             continue
         st = setup(N)
-        for _ in range(max(args.warmup, 3)):
+        for _ in range(max(warmup, 3)):
             step(st)
-        ms, per = time_steps(st, max(3, min(args.steps, 10)))
+        ms, per = time_steps(st, max(3, min(steps or 10, 10)))
         R = N * K
         sweep[str(N)] = {"ms_per_step": ms, "tokens_per_s": N * world / (ms / 1e3),
                          "tflops": 18.0 * R * H * I / (ms / 1e3) / 1e12,
@@ -878,15 +993,18 @@ def run_ours_train(args):
         torch.cuda.empty_cache()
     st = setup(base.n_tokens)
     N = base.n_tokens
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step(st)
     torch.cuda.synchronize()
     if moe.device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
+    if steps is None:  # size the timed region from a short untimed probe
+        probe_ms, _ = time_steps(st, 5)
+        steps = steps_for(probe_ms, lo=20, hi=1000)
     clocks = ClockSampler(dev.index).start()
     time.sleep(0.3)
     launches0 = moe.launch_count()
-    ms, per = time_steps(st, args.steps)
+    ms, per = time_steps(st, steps)
     launches = moe.launch_count() - launches0
     clk = clocks.stop()
     if moe.device_error() != 0:
@@ -901,6 +1019,61 @@ def run_ours_train(args):
     # and y, dX and dprob out to it. Two sets of these device buffers and a
     # copy stream: a step's copies run under the compute of its neighbours
     # (the first inputs and the last outputs are inside the timed region).
+    routing = routing_summary(st["w"], st["routes"].expert_counts.cpu().numpy(),
+                              st["routes"].kept_counts.cpu().numpy(), 0)
+    ms_e2e = e2e_train(ctx, stream, step, st, N, H, K, steps) if full else None
+
+    bwd_flops = 12.0 * R * H * I
+    ach = bwd_flops / (per["ffn_backward"] / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"], "traffic": None, "peak_source": peaks["_source"],
+            "kernel": "ffn_backward (FC2 dgrad + SwiGLU backward, FC1 dgrad, dX/dprob "
+                      "gather-combine, dW2 and dW13 weight gradients)",
+            "ms": per["ffn_backward"], "algorithmic_flops": bwd_flops}
+    value = N * world / (ms / 1e3)
+    out = {
+        "metric": METRIC_TRAIN, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": base.name, "description": base.note, "tokens_per_step_per_gpu": N,
+                   "block_m": args.block_m, "ladder": [list(base.ladder), base.ladder_den],
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (%.2f GB of expert weights, %.2f GB of fp32 weight "
+                         "gradients); no flush" % ((w13.numel() + w2.numel()) * 2 / 1e9,
+                                                   (dw13.numel() + dw2.numel()) * 4 / 1e9),
+                   **variant_config(args)},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "tflops_fwd_bwd": 18.0 * R * H * I / (ms / 1e3) / 1e12,
+        "pct_bf16_peak_fwd_bwd": 18.0 * R * H * I / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+        "calls_ms": per,
+        "routing": routing,
+        "clocks": clk,
+    }
+    if do_sweep:
+        out["sweep"] = sweep
+    if full:
+        out["e2e"] = {"value": N * world / (ms_e2e / 1e3), "unit": UNIT,
+                      "h2d_bytes_per_step": 2 * N * H * 2,
+                      "d2h_bytes_per_step": 2 * N * H * 2 + N * K * 4,
+                      "copies": "pinned host x, dY in and y, dX, dprob out every step, on a "
+                                "second stream with two device buffer sets, overlapping "
+                                "neighbouring steps"}
+    if full and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, secs, cores = time_oracle_train_sample(st["w"], st["x_bits"], st["dy_bits"],
+                                                        st["wr_h"], st["bias_h"], args.block_m,
+                                                        act=act_code(args))
+        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": desc, "cpu_seconds": secs}
+    return out
+
+
+def e2e_train(ctx, stream, step, st, N, H, K, steps):
+    """Milliseconds per step (max over ranks) of training steps that each copy
+    x and dY in from pinned host memory and y, dX and dprob out to it."""
+    import numpy as np
+    import torch
+    dev, dist = ctx.dev, ctx.dist
     xh = torch.from_numpy(st["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
     dyh = torch.from_numpy(st["dy_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
     yh = [torch.empty((N, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
@@ -943,54 +1116,11 @@ def run_ours_train(args):
     barrier(dist, dev)
     torch.cuda.synchronize()
     e0.record(stream)
-    e2e_run(args.steps, e0)
+    e2e_run(steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(dist, dev)
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
-
-    bwd_flops = 12.0 * R * H * I
-    ach = bwd_flops / (per["ffn_backward"] / 1e3) / 1e12
-    roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": ach / peaks["bf16_tflops"], "traffic": None, "peak_source": peaks["_source"],
-            "kernel": "ffn_backward (FC2 dgrad + SwiGLU backward, FC1 dgrad, dX/dprob "
-                      "gather-combine, dW2 and dW13 weight gradients)",
-            "ms": per["ffn_backward"], "algorithmic_flops": bwd_flops}
-    value = N * world / (ms / 1e3)
-    out = {
-        "metric": METRIC_TRAIN, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": base.name, "description": base.note, "tokens_per_step_per_gpu": N,
-                   "block_m": args.block_m, "ladder": [list(base.ladder), base.ladder_den],
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (%.2f GB of expert weights, %.2f GB of fp32 weight "
-                         "gradients); no flush" % ((w13.numel() + w2.numel()) * 2 / 1e9,
-                                                   (dw13.numel() + dw2.numel()) * 4 / 1e9),
-                   **variant_config(args)},
-        "gpu_launches": launches,
-        "e2e": {"value": N * world / (ms_e2e / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2 + N * K * 4,
-                "copies": "pinned host x, dY in and y, dX, dprob out every step, on a second "
-                          "stream with two device buffer sets, overlapping neighbouring steps"},
-        "roofline": roof,
-        "tflops_fwd_bwd": 18.0 * R * H * I / (ms / 1e3) / 1e12,
-        "pct_bf16_peak_fwd_bwd": 18.0 * R * H * I / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
-        "calls_ms": per,
-        "sweep": sweep,
-        "clocks": clk,
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, secs, cores = time_oracle_train_sample(st["w"], st["x_bits"], st["dy_bits"],
-                                                        st["wr_h"], st["bias_h"], args.block_m,
-                                                        act=act_code(args))
-        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                               "sample": desc, "cpu_seconds": secs}
-    if rank == 0:
-        print(json.dumps(out))
-    if dist is not None:
-        dist.destroy_process_group()
-    return 0
+    return max_over_ranks(e0.elapsed_time(e1), dist, dev) / steps
 
 
 # ----------------------------------------------------------------------------- serving (graph ladder)

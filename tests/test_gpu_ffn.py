@@ -88,6 +88,32 @@ def test_forward_qwen3_30b_sampled_tokens_end_to_end():
         assert_close(y[t:t + 1], y_ref, "y of token %d" % t)
 
 
+def test_forward_dsv3_whole_tokens_and_spread_experts():
+    """DeepSeek-V3-shaped layer at full size: whole tokens through the oracle
+    layer (the first, the last, and tokens that lost a route to the capacity
+    limit), and h and o of every kept slot of eight experts spread over the id
+    range, so a wrong weight slice of any of them at H = 7168 shows."""
+    w = synth.WORKLOADS["dsv3"]
+    P = Problem(w, bm=32, host_weights=False)
+    P.run()
+    R = P.oracle_routing()
+    assert_routing_equal(P, R)
+    E = w.n_experts
+    spread = sorted({int(e) for e in np.linspace(0, E - 1, 8).round()})
+    check_expert_slots(P, R, spread)
+    keep = R.layout.keep
+    partly = np.nonzero((keep.sum(1) > 0) & (keep.sum(1) < w.top_k))[0]
+    assert len(partly) > 0, "the workload is expected to drop some routes"
+    toks = sorted({0, w.n_tokens - 1, int(partly[0]), int(partly[-1])})
+    experts = sorted({int(e) for t in toks for e in R.topk_ids[t]})
+    W = P.expert_weights(experts)
+    y = P.y.float().cpu().numpy()
+    for t in toks:
+        y_ref = oracle.forward_tokens(t, t + 1, P.x_bits, W, w.hidden, w.inter, R.topk_ids,
+                                      R.topk_p, keep)
+        assert_close(y[t:t + 1], y_ref, "y of token %d" % t)
+
+
 def test_empty_batch_is_a_no_op():
     P = Problem(_w(0, 128, 8, 2, 128), bm=16, host_weights=True)
     P.run()

@@ -1,15 +1,19 @@
 """Graph bucket ladder on the GPU: a replay of a bucket's captured forward on
-n tokens equals an eager forward on exactly those n tokens (y bit-identical,
-routing identical up to the sentinel value), for capacity and dropless
-layouts; eager fallback past the padding ratio; new inputs between replays."""
+n tokens computes the oracle's layer on those n tokens (routing bit-exact up
+to the sentinel value, y within the stated tolerance) and equals an eager
+forward on exactly those n tokens (y bit-identical), for capacity and
+dropless layouts; eager fallback past the padding ratio; new inputs between
+replays ("[4/5] feat: capture the FFN experts at bucketed padded shapes",
+What this adds and Testing)."""
 import numpy as np
 import pytest
 import torch
 
 import mixture_experts_routing_gb300 as moe
+import oracle
 import synth
 import synth.gpu
-from gpu_util import bf16_dev
+from gpu_util import assert_close, bf16_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -20,7 +24,8 @@ def _layer(w, seed=0):
     cfg = moe.Config(N, H, E, K, I, w.cap_num, w.cap_den, block_m=32, ladder=list(w.ladder),
                      ladder_den=w.ladder_den)
     wr = torch.from_numpy(synth.normal_f32(seed, synth.STREAM["wr"], 0, H * E, w.wr_std).reshape(H, E)).to(dev)
-    bias = None if w.zipf_s is None else torch.from_numpy(synth.zipf_bias(seed, E, w.zipf_s)).to(dev)
+    b = synth.router_bias(w) if seed == w.seed else synth.zipf_bias(seed, E, w.zipf_s)
+    bias = None if b is None else torch.from_numpy(b).to(dev)
     bf = dict(dtype=torch.bfloat16, device=dev)
     wg, wu, wd = torch.empty((E, H, I), **bf), torch.empty((E, H, I), **bf), torch.empty((E, I, H), **bf)
     synth.gpu.fill(wg, seed, synth.STREAM["wg"], w.w_std)
@@ -83,6 +88,81 @@ def test_ladder_replay_equals_eager(w):
         assert b == next(i for i, v in enumerate(buckets) if v >= n)
         y_e, r_e, s_e = _eager(w, n, L.x, wr, bias, w13, w2)
         _check_equal(L, n, w, y_e, r_e, s_e, buckets[b])
+    assert moe.device_error() == 0
+    L.close()
+
+
+def _host_weights(w):
+    H, I = w.hidden, w.inter
+    wg, wu, wd = {}, {}, {}
+    for e in range(w.n_experts):
+        wg[e] = synth.normal_bf16_bits(w.seed, synth.STREAM["wg"], e * H * I, H * I, w.w_std).reshape(H, I)
+        wu[e] = synth.normal_bf16_bits(w.seed, synth.STREAM["wu"], e * H * I, H * I, w.w_std).reshape(H, I)
+        wd[e] = synth.normal_bf16_bits(w.seed, synth.STREAM["wd"], e * I * H, I * H, w.w_std).reshape(I, H)
+    return oracle.ExpertWeights(w.n_experts, wg, wu, wd)
+
+
+def _oracle_layer(w, xb, wr, bias, n, bm=32):
+    """The oracle's routing (fields in the library's naming) and y for the
+    first n tokens as one batch."""
+    E, K = w.n_experts, w.top_k
+    xs = xb[:n]
+    if w.cap_num == 0:
+        ids, p, _, _ = oracle.router(xs, wr, bias, K)
+        D = oracle.dropless_layout(ids, E, bm, list(w.ladder), w.ladder_den)
+        keep = np.ones(ids.shape, np.uint8)
+        lay = dict(expert_counts=D.expert_counts, kept_counts=D.expert_counts,
+                   block_start=D.block_start, sorted_slot_ids=D.sorted_slot_ids,
+                   expert_ids=D.expert_ids, ntpp=D.num_tokens_post_padded,
+                   token_routes=D.token_routes)
+    else:
+        R = oracle.route(xs, wr, bias, E, K, w.cap_num, w.cap_den, bm)
+        ids, p, keep, L = R.topk_ids, R.topk_p, R.layout.keep, R.layout
+        lay = dict(expert_counts=L.expert_counts, kept_counts=L.kept_counts,
+                   block_start=L.block_start, sorted_slot_ids=L.sorted_slot_ids,
+                   expert_ids=L.expert_ids, ntpp=L.num_tokens_post_padded,
+                   token_routes=L.token_routes)
+    lay.update(topk_ids=ids, topk_p=p, keep=keep)
+    return lay
+
+
+@pytest.mark.parametrize("w", [CAP, DL], ids=["capacity", "dropless"])
+def test_ladder_replay_matches_oracle(w):
+    """Each replay's routing bit for bit, and y elementwise, against the
+    oracle run on the n live tokens alone (capacity and ladder extents
+    follow n)."""
+    cfg, wr, bias, w13, w2 = _layer(w)
+    buckets = [128, 256, 512, 1024, 2048]
+    L = moe.Ladder(cfg, buckets, 0.0, wr, bias, w13, w2, "cuda:0")
+    xb = synth.normal_bf16_bits(11, synth.STREAM["x"], 0, w.n_tokens * w.hidden, 1.0).reshape(w.n_tokens, w.hidden)
+    L.x.copy_(bf16_dev(xb, L.x.device))
+    wr_h = wr.cpu().numpy()
+    bias_h = None if bias is None else bias.cpu().numpy()
+    W = _host_weights(w)
+    bm = 32
+    for n in (1, 100, 129, 1500, 2048):
+        b = L.forward(n)
+        torch.cuda.synchronize()
+        bucket = buckets[b]
+        ref = _oracle_layer(w, xb, wr_h, bias_h, n, bm)
+        g = {k: getattr(L.routes, k).cpu().numpy() for k, _ in moe.Routes.FIELDS}
+        for k in ("topk_ids", "keep", "token_routes"):
+            assert np.array_equal(g[k][:n], ref[k]), "%s (n=%d)" % (k, n)
+        assert np.array_equal(g["topk_p"][:n].view(np.int32), ref["topk_p"].view(np.int32)), n
+        for k in ("expert_counts", "kept_counts", "block_start"):
+            assert np.array_equal(g[k], ref[k]), "%s (n=%d)" % (k, n)
+        ntpp = int(g["num_tokens_post_padded"][0])
+        assert ntpp == ref["ntpp"], n
+        ssi = g["sorted_slot_ids"][:ntpp].copy()
+        ssi_ref = ref["sorted_slot_ids"][:ntpp].copy()
+        # the sentinel is the bucket in a replay, n in the oracle
+        assert np.array_equal(ssi == bucket, ssi_ref == n), "sentinel slots (n=%d)" % n
+        live = ssi_ref != n
+        assert np.array_equal(ssi[live], ssi_ref[live]), "sorted_slot_ids (n=%d)" % n
+        assert np.array_equal(g["expert_ids"][:ntpp // bm], ref["expert_ids"][:ntpp // bm]), n
+        y_ref = oracle.forward_tokens(0, n, xb[:n], W, w.hidden, w.inter, ref["topk_ids"],
+                                      ref["topk_p"], ref["keep"])
+        assert_close(L.y[:n].float().cpu().numpy(), y_ref, "y (n=%d, bucket %d)" % (n, bucket))
     assert moe.device_error() == 0
     L.close()
 
