@@ -254,6 +254,14 @@ def _bind_backward(L):
     L.oracle_fc1_fp8_routes.restype = i32
     L.oracle_fc2_fp8_routes.argtypes = [i32, P, i32, i32, P, P, P, P, P]
     L.oracle_fc2_fp8_routes.restype = i32
+    L.oracle_e8m0_decode.argtypes = [ctypes.c_uint8]
+    L.oracle_e8m0_decode.restype = ctypes.c_float
+    L.oracle_quantize_mx_fp8.argtypes = [i32, i32, P, P, P]
+    L.oracle_quantize_mx_fp8.restype = i32
+    L.oracle_fc1_mx_routes.argtypes = [i32, P, P, i32, i32, P, P, P, P, i32, P, P]
+    L.oracle_fc1_mx_routes.restype = i32
+    L.oracle_fc2_mx_routes.argtypes = [i32, P, i32, i32, P, P, P, P, P]
+    L.oracle_fc2_mx_routes.restype = i32
     L._bwd_bound = True
     return L
 
@@ -438,4 +446,59 @@ def fc2_fp8_routes(experts, hq, hs, wq2, ws2, H: int, I: int) -> np.ndarray:
                             _p(np.ascontiguousarray(hs, np.float32)),
                             _p(np.ascontiguousarray(wq2, np.uint8)),
                             _p(np.ascontiguousarray(ws2, np.float32)), _p(o))
+    return o
+
+
+# ---------------------------------------------------------------- MX block-scaled FP8
+def e8m0_decode(codes) -> np.ndarray:
+    L = _bind_backward(lib())
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([L.oracle_e8m0_decode(int(v)) for v in c.ravel()], np.float32).reshape(c.shape)
+
+
+def quantize_mx_fp8(m_bits: np.ndarray):
+    """MX quantisation of a bf16 matrix along its rows in blocks of 32:
+    (E4M3 codes [rows, cols] u8, E8M0 scale codes [rows, cols/32] u8)."""
+    L = _bind_backward(lib())
+    m = np.ascontiguousarray(m_bits, dtype=np.uint16)
+    rows, cols = m.shape
+    q = np.empty((rows, cols), np.uint8)
+    sc = np.empty((rows, cols // 32), np.uint8)
+    if L.oracle_quantize_mx_fp8(rows, cols, _p(m), _p(q), _p(sc)) != 0:
+        raise ValueError("columns must be a multiple of 32")
+    return q, sc
+
+
+def fc1_mx_routes(tokens, experts, xq, xs, wq13, ws13, H: int, I: int, act: int = ACT_SILU,
+                  scales=None) -> np.ndarray:
+    """h [n, I] of FC1 on MX operands; xq [N,H] u8, xs [N,H/32] u8 (E8M0),
+    wq13 [E,2I,H] u8, ws13 [E*2I, H/32] u8."""
+    L = _bind_backward(lib())
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    experts = np.ascontiguousarray(experts, dtype=np.int32)
+    n = len(tokens)
+    h = np.empty((n, I), np.float32)
+    sc = None if scales is None else np.ascontiguousarray(scales, dtype=np.float32)
+    rc = L.oracle_fc1_mx_routes(n, _p(tokens), _p(experts), H, I, _p(np.ascontiguousarray(xq, np.uint8)),
+                                _p(np.ascontiguousarray(xs, np.uint8)),
+                                _p(np.ascontiguousarray(wq13, np.uint8)),
+                                _p(np.ascontiguousarray(ws13, np.uint8)), int(act), _p(sc), _p(h))
+    if rc != 0:
+        raise ValueError("H must be a multiple of 32")
+    return h
+
+
+def fc2_mx_routes(experts, hq, hs, wq2, ws2, H: int, I: int) -> np.ndarray:
+    """o [n, H] of FC2 on MX operands; hq [n, I] u8 and hs [n, I/32] u8 the
+    routes' quantised h rows, wq2 [E,H,I] u8, ws2 [E*H, I/32] u8."""
+    L = _bind_backward(lib())
+    experts = np.ascontiguousarray(experts, dtype=np.int32)
+    n = len(experts)
+    o = np.empty((n, H), np.float32)
+    rc = L.oracle_fc2_mx_routes(n, _p(experts), H, I, _p(np.ascontiguousarray(hq, np.uint8)),
+                                _p(np.ascontiguousarray(hs, np.uint8)),
+                                _p(np.ascontiguousarray(wq2, np.uint8)),
+                                _p(np.ascontiguousarray(ws2, np.uint8)), _p(o))
+    if rc != 0:
+        raise ValueError("I must be a multiple of 32")
     return o

@@ -755,3 +755,115 @@ int oracle_fc2_fp8_routes(int n, const int32_t* experts, int H, int I, const uin
   }
   return 0;
 }
+
+/* ======================================================================== */
+/* MX block-scaled FP8 (MXFP8 E4M3). No page defines a block-scaled format; */
+/* the definition is the OCP Microscaling Formats (MX) v1.0 specification,  */
+/* the format tcgen05's kind::mxf8f6f4 consumes: a block of 32 consecutive  */
+/* values along the contraction shares one scale X = 2^s, stored as an E8M0 */
+/* byte (code c encodes 2^(c-127); 255 is NaN), and each value is an E4M3   */
+/* code P_i, the value being P_i * X.                                       */
+/* Quantisation of one block (the specification's conversion):             */
+/*   s = floor(log2(max_i |v_i|)) - 8, 8 being the exponent of the largest  */
+/*       power of two E4M3 holds (256 <= 448 < 512); s clamped to           */
+/*       [-127, 127]; an all-zero block takes s = -127 (code 0);            */
+/*   P_i = E4M3(v_i / 2^s), round to nearest even, saturating at +-448 (a   */
+/*       block maximum in [448, 512) * 2^s saturates).                      */
+/* The division by 2^s is exact (a power of two).                           */
+/* ======================================================================== */
+float oracle_e8m0_decode(uint8_t c) {
+  if (c == 255) return NAN;
+  return ldexpf(1.0f, (int)c - 127);
+}
+
+static int mx_block_exponent(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  int e;
+  frexpf(amax, &e);  /* amax = f * 2^e with f in [0.5, 1): floor(log2 amax) = e - 1 */
+  int s = (e - 1) - 8;
+  if (s < -127) s = -127;
+  if (s > 127) s = 127;
+  return s;
+}
+
+/* MX quantisation of an [rows, cols] bf16 matrix along its rows (cols a
+ * multiple of 32): codes q [rows, cols], scale codes sc [rows, cols / 32]. */
+int oracle_quantize_mx_fp8(int rows, int cols, const uint16_t* m, uint8_t* q, uint8_t* sc) {
+  if (cols % 32 != 0) return -1;
+  const int nb = cols / 32;
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    for (int b = 0; b < nb; ++b) {
+      const uint16_t* blk = m + (size_t)r * cols + (size_t)b * 32;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(bf16_to_f32(blk[i])));
+      const int s = mx_block_exponent(amax);
+      sc[(size_t)r * nb + b] = (uint8_t)(s + 127);
+      for (int i = 0; i < 32; ++i)
+        q[(size_t)r * cols + (size_t)b * 32 + i] = oracle_e4m3_encode(ldexpf(bf16_to_f32(blk[i]), -s));
+    }
+  }
+  return 0;
+}
+
+/* FC1 on MX operands for a list of (token, expert) routes: x quantised along
+ * H per token (xq [N,H], xs [N,H/32]), the packed gate/up rows along H
+ * (wq [E,2I,H], ws [E*2I, H/32]; rows [0,I) gate, [I,2I) up):
+ *   g_i = sum_h (E4M3(xq[t,h]) X(xs[t,h/32])) (E4M3(wq[e,i,h]) X(ws[e,i,h/32])),
+ *   u likewise, h_i = act(g_i) u_i (times scales[j] when given),
+ * fp32, ascending h. h_out [n, I]. */
+int oracle_fc1_mx_routes(int n, const int32_t* tokens, const int32_t* experts, int H, int I,
+                         const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws,
+                         int act, const float* scales, float* h_out) {
+  if (H % 32 != 0) return -1;
+  const int nb = H / 32;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int j = 0; j < n; ++j) {
+    const int t = tokens[j], e = experts[j];
+    const uint8_t* xr = xq + (size_t)t * H;
+    const uint8_t* xsr = xs + (size_t)t * nb;
+    for (int i = 0; i < I; ++i) {
+      const size_t rg = (size_t)e * 2 * I + i, ru = rg + I;
+      const uint8_t* wg = wq + rg * H;
+      const uint8_t* wu = wq + ru * H;
+      float g = 0.0f, u = 0.0f;
+      for (int h = 0; h < H; ++h) {
+        const int b = h / 32;
+        const float xv = oracle_e4m3_decode(xr[h]) * oracle_e8m0_decode(xsr[b]);
+        g = g + xv * (oracle_e4m3_decode(wg[h]) * oracle_e8m0_decode(ws[rg * nb + b]));
+        u = u + xv * (oracle_e4m3_decode(wu[h]) * oracle_e8m0_decode(ws[ru * nb + b]));
+      }
+      h_out[(size_t)j * I + i] = act_fn(act, g) * u * (scales ? scales[j] : 1.0f);
+    }
+  }
+  return 0;
+}
+
+/* FC2 on MX operands for n routes: each route's h row quantised along I
+ * (hq [n,I], hs [n,I/32]) and each w2 row along I (wq [E,H,I],
+ * ws [E*H, I/32]):
+ *   o_c = sum_i (E4M3(hq[j,i]) X(hs[j,i/32])) (E4M3(wq[e,c,i]) X(ws[e,c,i/32])),
+ * fp32, ascending i. o_out [n, H]. */
+int oracle_fc2_mx_routes(int n, const int32_t* experts, int H, int I, const uint8_t* hq,
+                         const uint8_t* hs, const uint8_t* wq, const uint8_t* ws, float* o_out) {
+  if (I % 32 != 0) return -1;
+  const int nb = I / 32;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int j = 0; j < n; ++j) {
+    const int e = experts[j];
+    const uint8_t* hr = hq + (size_t)j * I;
+    const uint8_t* hsr = hs + (size_t)j * nb;
+    for (int c = 0; c < H; ++c) {
+      const size_t r = (size_t)e * H + c;
+      const uint8_t* wr = wq + r * I;
+      float o = 0.0f;
+      for (int i = 0; i < I; ++i) {
+        const int b = i / 32;
+        o = o + (oracle_e4m3_decode(hr[i]) * oracle_e8m0_decode(hsr[b])) *
+                    (oracle_e4m3_decode(wr[i]) * oracle_e8m0_decode(ws[r * nb + b]));
+      }
+      o_out[(size_t)j * H + c] = o;
+    }
+  }
+  return 0;
+}

@@ -13,6 +13,7 @@ import oracle
 import test_oracle_backward_pins as bp
 import test_oracle_pins as fp
 import test_oracle_fp8_pins as fx
+import test_oracle_mx_pins as mx
 import test_oracle_router_backward_pins as rb
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
@@ -59,6 +60,14 @@ MUTATIONS = [
      "gk[k] = dp[k] / d;", lambda: rb.test_router_backward_matches_central_differences(0, True)),
     ("router backward skips the softmax normaliser", "dl[ids[k]] = p[ids[k]] * (gk[k] - s);",
      "dl[ids[k]] = p[ids[k]] * gk[k];", lambda: rb.test_router_backward_matches_central_differences(1, False)),
+    ("MX block exponent with the wrong element emax", "int s = (e - 1) - 8;", "int s = (e - 1) - 7;",
+     lambda: mx.test_block_scale_exponent_worked_values(1.0, 119)),
+    ("E8M0 decoded with bias 128", "return ldexpf(1.0f, (int)c - 127);", "return ldexpf(1.0f, (int)c - 128);",
+     lambda: mx.test_e8m0_decode(127, 1.0)),
+    ("MX FC1 gate weight scaled by its first block", "oracle_e8m0_decode(ws[rg * nb + b])",
+     "oracle_e8m0_decode(ws[rg * nb])", lambda: mx.test_fc1_mx_matches_fp64_dequantised_reference(0)),
+    ("MX FC2 h scaled by its first block", "oracle_e8m0_decode(hsr[b])", "oracle_e8m0_decode(hsr[0])",
+     lambda: mx.test_fc2_mx_matches_fp64_dequantised_reference()),
     ("router dx with the weight transposed", "acc = acc + dlogits[(size_t)t * E + e] * wr[(size_t)h * E + e];",
      "acc = acc + dlogits[(size_t)t * E + e] * wr[(size_t)e * H + h];",
      lambda: rb.test_router_backward_matches_central_differences(2, True)),
