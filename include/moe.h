@@ -289,6 +289,66 @@ int moe_ffn_forward_fp8(const moe_config_t* cfg, const moe_routes_t* routes, con
                         const float* w2_scale, void* xq, float* x_scale, void* h, void* hq,
                         float* h_scale, void* o, cudaStream_t stream);
 
+/* ---- MX block-scaled FP8 (MXFP8 E4M3) expert GEMMs --------------------------
+ * An extension beyond the pages as well (they run bf16 experts and reject FP8:
+ * [FC] Changelog / Known limitations); the format is the OCP Microscaling
+ * Formats (MX) v1.0 MXFP8: each block of 32 consecutive values along the
+ * contraction shares one scale 2^s stored as an E8M0 byte (s + 127), each
+ * value an E4M3 code; value = decode(code) * 2^s. Quantisation of a block:
+ * s = floor(log2(max |v|)) - 8 clamped to [-127, 127] (-127 for an all-zero
+ * block), code = E4M3(v * 2^-s) rounded to nearest even, saturating at +-448.
+ * The tensor cores (tcgen05.mma kind::mxf8f6f4) apply both operands' block
+ * scales inside the contraction, fp32 accumulation. */
+
+/* MX quantisation of a bf16 matrix along its rows.
+ *  m         [rows, cols] bf16, cols a multiple of 32, 16-byte aligned
+ *  rows_dev  device int32 or NULL: only rows below *rows_dev (read on the
+ *            device) are quantised; the others are left as they are
+ *  q         [rows, cols] u8 output E4M3 codes, 16-byte aligned
+ *  scale     [rows, cols/32] u8 output E8M0 codes, row-major
+ * Used for the activations (x per token, h per slot) on each call. */
+int moe_quantize_mx_fp8(const void* m, int64_t rows, const int32_t* rows_dev, int cols, void* q,
+                        void* scale, cudaStream_t stream);
+
+/* MX quantisation of packed weights (w13 rows as [E*2I, H], w2 rows as
+ * [E*H, I]); rows and cols multiples of 128. Codes as above; the
+ * rows*cols/32 scale bytes go in the layout the MX GEMMs copy to tensor
+ * memory: 512-byte atoms, atom (rt, kt) = rows 128rt.., blocks 4kt..4kt+3 at
+ * byte (rt * cols/128 + kt) * 512, row r's block b inside it at
+ * (r%32)*16 + ((r%128)/32)*4 + b%4. Done once, before any forward. */
+int moe_quantize_mx_fp8_weights(const void* m, int64_t rows, int cols, void* q, void* scale_atoms,
+                                cudaStream_t stream);
+
+/* FC1 on MX operands, otherwise as moe_fc1_forward.
+ *  xq [N,H] u8, x_sf [N,H/32] u8    MX-quantised token rows (moe_quantize_mx_fp8)
+ *  w13q [E,2I,H] u8, w13_sf         MX-quantised packed gate/up rows, scale atoms
+ *                                   (moe_quantize_mx_fp8_weights)
+ *  h [S,I] bf16 output: h = act(g) u (times p' with cfg->prob_in_act),
+ *      g[s,i] = sum_k xq[t,k] 2^(x_sf[t,k/32]-127) w13q[e,i,k] 2^(sf(e*2I+i,k/32)-127)
+ *      (decoded codes), u from row e*2I+I+i; fp32 accumulation. All scale
+ *      buffers 16-byte aligned. */
+int moe_fc1_forward_mx(const moe_config_t* cfg, const moe_routes_t* routes, const void* xq,
+                       const void* x_sf, const void* w13q, const void* w13_sf, void* h,
+                       cudaStream_t stream);
+
+/* FC2 on MX operands, otherwise as moe_fc2_forward.
+ *  hq [S,I] u8, h_sf [S,I/32] u8    MX-quantised slot rows of h
+ *  w2q [E,H,I] u8, w2_sf            MX-quantised w2 rows, scale atoms
+ *  o [S,H] bf16 output, o = 0 in padding slots below roundup(kept_counts[e],16). */
+int moe_fc2_forward_mx(const moe_config_t* cfg, const moe_routes_t* routes, const void* hq,
+                       const void* h_sf, const void* w2q, const void* w2_sf, void* o,
+                       cudaStream_t stream);
+
+/* MX expert path for bf16 input: quantise x into xq/x_sf, FC1 into h (bf16),
+ * quantise the slot rows of h below num_tokens_post_padded into hq/h_sf, FC2
+ * into o. Four launches on one stream; the caller owns every buffer:
+ *  x [N,H] bf16; xq [N,H] u8; x_sf [N,H/32] u8; h [S,I] bf16; hq [S,I] u8;
+ *  h_sf [S,I/32] u8; o [S,H] bf16; weights as above. */
+int moe_ffn_forward_mx(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                       const void* w13q, const void* w13_sf, const void* w2q, const void* w2_sf,
+                       void* xq, void* x_sf, void* h, void* hq, void* h_sf, void* o,
+                       cudaStream_t stream);
+
 /* Bytes of scratch moe_ffn_backward needs: about S*(2 + 6I + 2H) bytes plus
  * S*I/8 for the dprob partials (S = moe_max_slots). */
 int64_t moe_backward_workspace_bytes(const moe_config_t* cfg);

@@ -144,10 +144,17 @@ def lib():
         L.moe_fc1_forward_fp8.argtypes = [CP, RP, P, P, P, P, P, P]
         L.moe_fc2_forward_fp8.argtypes = [CP, RP, P, P, P, P, P, P]
         L.moe_ffn_forward_fp8.argtypes = [CP, RP, P, P, P, P, P, P, P, P, P, P, P, P]
+        L.moe_quantize_mx_fp8.argtypes = [P, I64, P, I32, P, P, P]
+        L.moe_quantize_mx_fp8_weights.argtypes = [P, I64, I32, P, P, P]
+        L.moe_fc1_forward_mx.argtypes = [CP, RP, P, P, P, P, P, P]
+        L.moe_fc2_forward_mx.argtypes = [CP, RP, P, P, P, P, P, P]
+        L.moe_ffn_forward_mx.argtypes = [CP, RP, P, P, P, P, P, P, P, P, P, P, P, P]
         for name in ("moe_route_align", "moe_fc1_forward", "moe_fc2_forward", "moe_ffn_forward",
                      "moe_combine", "moe_pack_w13", "moe_pack_w2", "moe_ffn_forward_train",
                      "moe_ffn_backward", "moe_router_backward", "moe_quantize_rows_fp8",
-                     "moe_fc1_forward_fp8", "moe_fc2_forward_fp8", "moe_ffn_forward_fp8"):
+                     "moe_fc1_forward_fp8", "moe_fc2_forward_fp8", "moe_ffn_forward_fp8",
+                     "moe_quantize_mx_fp8", "moe_quantize_mx_fp8_weights", "moe_fc1_forward_mx",
+                     "moe_fc2_forward_mx", "moe_ffn_forward_mx"):
             getattr(L, name).restype = I32
         L.moe_status_string.argtypes = [I32]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -388,6 +395,72 @@ def ffn_forward_fp8(cfg: Config, routes: Routes, x, wq: Fp8Weights, xq, x_scale,
                                      _ptr(wq.w13q), _ptr(wq.w13_scale), _ptr(wq.w2q),
                                      _ptr(wq.w2_scale), _ptr(xq), _ptr(x_scale), _ptr(h), _ptr(hq),
                                      _ptr(h_scale), _ptr(o), _stream(stream)))
+
+
+def quantize_mx_fp8(m, q, scale, stream=None, rows_dev=None) -> None:
+    """MX (block-scaled) E4M3 codes q [rows, cols] u8 and E8M0 scale codes
+    [rows, cols/32] u8 of a bf16 matrix m; rows_dev bounds the rows quantised."""
+    rows, cols = m.shape
+    _check("moe_quantize_mx_fp8",
+           lib().moe_quantize_mx_fp8(_ptr(m), int(rows), _ptr(rows_dev), int(cols), _ptr(q),
+                                     _ptr(scale), _stream(stream)))
+
+
+def quantize_mx_fp8_weights(m, q, scale_atoms, stream=None) -> None:
+    """MX codes of packed weight rows m [rows, cols] (multiples of 128) with
+    the scale bytes in the GEMMs' 512-byte atom layout."""
+    rows, cols = m.shape
+    _check("moe_quantize_mx_fp8_weights",
+           lib().moe_quantize_mx_fp8_weights(_ptr(m), int(rows), int(cols), _ptr(q),
+                                             _ptr(scale_atoms), _stream(stream)))
+
+
+def fc1_forward_mx(cfg: Config, routes: Routes, xq, x_sf, w13q, w13_sf, h, stream=None) -> None:
+    _check("moe_fc1_forward_mx",
+           lib().moe_fc1_forward_mx(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(xq),
+                                    _ptr(x_sf), _ptr(w13q), _ptr(w13_sf), _ptr(h),
+                                    _stream(stream)))
+
+
+def fc2_forward_mx(cfg: Config, routes: Routes, hq, h_sf, w2q, w2_sf, o, stream=None) -> None:
+    _check("moe_fc2_forward_mx",
+           lib().moe_fc2_forward_mx(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(hq),
+                                    _ptr(h_sf), _ptr(w2q), _ptr(w2_sf), _ptr(o), _stream(stream)))
+
+
+class MxWeights:
+    """w13 and w2 MX-quantised once: E4M3 codes and E8M0 block scales in the
+    GEMMs' atom layout."""
+
+    def __init__(self, cfg: Config, w13, w2, stream=None):
+        import torch
+        E, H, I = cfg.n_experts, cfg.hidden, cfg.inter
+        dev = w13.device
+        self.w13q = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev)
+        self.w13_sf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device=dev)
+        self.w2q = torch.empty((E, H, I), dtype=torch.uint8, device=dev)
+        self.w2_sf = torch.empty(E * H * I // 32, dtype=torch.uint8, device=dev)
+        quantize_mx_fp8_weights(w13.view(E * 2 * I, H), self.w13q, self.w13_sf, stream)
+        quantize_mx_fp8_weights(w2.view(E * H, I), self.w2q, self.w2_sf, stream)
+
+
+def alloc_mx_buffers(cfg: Config, device):
+    """xq [N,H] u8, x_sf [N,H/32] u8, hq [S,I] u8 and h_sf [S,I/32] u8 for ffn_forward_mx."""
+    import torch
+    N, S = max(cfg.n_tokens, 1), max(max_slots(cfg), 1)
+    u8 = dict(dtype=torch.uint8, device=device)
+    return (torch.empty((N, cfg.hidden), **u8), torch.empty((N, cfg.hidden // 32), **u8),
+            torch.empty((S, cfg.inter), **u8), torch.empty((S, cfg.inter // 32), **u8))
+
+
+def ffn_forward_mx(cfg: Config, routes: Routes, x, wq: MxWeights, xq, x_sf, h, hq, h_sf, o,
+                   stream=None) -> None:
+    """Quantise x, FC1 on MX operands, quantise h, FC2 on MX (one C call, four launches)."""
+    _check("moe_ffn_forward_mx",
+           lib().moe_ffn_forward_mx(ctypes.byref(cfg), ctypes.byref(routes.c()), _ptr(x),
+                                    _ptr(wq.w13q), _ptr(wq.w13_sf), _ptr(wq.w2q), _ptr(wq.w2_sf),
+                                    _ptr(xq), _ptr(x_sf), _ptr(h), _ptr(hq), _ptr(h_sf), _ptr(o),
+                                    _stream(stream)))
 
 
 def forward(cfg: Config, x, w_router, bias, w13, w2, routes: Routes, workspace, h, o, y,

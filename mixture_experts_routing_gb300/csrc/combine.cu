@@ -271,6 +271,87 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_rows_fp8_reg_kernel
   }
 }
 
+// MX block-scaled FP8 (MXFP8 E4M3, the OCP Microscaling Formats v1.0
+// conversion): each block of 32 consecutive values of a row shares the scale
+// 2^s, s = floor(log2(amax of the block)) - 8 clamped to [-127, 127] (-127 for
+// an all-zero block), stored as the E8M0 byte s + 127; each value becomes
+// E4M3(v * 2^-s), round to nearest even, saturating at +-448. The scaling is by
+// a power of two, so it is exact and the codes do not depend on the order of
+// anything. One warp takes 256 consecutive values of a row (8 blocks): lanes
+// 4b..4b+3 hold block b's 32 values (one 16-byte group each) and combine their
+// maxima with two shuffles.
+constexpr int kMxWarps = 8;
+
+// 2^-s for s in [-127, 127], from its bits (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float pow2_neg(int s) {
+  const int e = 127 - s;
+  return e > 0 ? __int_as_float(e << 23) : __int_as_float(0x00400000);
+}
+
+// floor(log2(a)) - 8 clamped to [-127, 127] for a finite a >= 0; -127 for a = 0.
+__device__ __forceinline__ int mx_block_exponent(float a) {
+  const uint32_t b = __float_as_uint(a);
+  if (b == 0u) return -127;
+  const int ef = (int)(b >> 23);
+  const int fl = ef > 0 ? ef - 127 : (31 - __clz((int)(b & 0x7FFFFFu))) - 149;
+  return min(127, max(-127, fl - 8));
+}
+
+// atoms: scale bytes in the layout the GEMM's tensor-core copies read (rows and
+// columns multiples of 128): for a row tile rt = r/128 and a k tile kt = b/4,
+// a 512-byte atom at (rt * (nb/4) + kt) * 512 holding row r's block b at
+// (r%32)*16 + ((r%128)/32)*4 + b%4. Otherwise scale[r * nb + b].
+__global__ void __launch_bounds__(kMxWarps * 32) quantize_mx_fp8_kernel(
+    const uint16_t* __restrict__ m, int64_t rows, const int32_t* __restrict__ rows_dev, int cols,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ scale, int atoms) {
+  griddep_wait();  // launched after the kernel that writes this one's inputs
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = cols / 32;
+  const int groups = (nb + 7) / 8;
+  const int64_t item = (int64_t)blockIdx.x * kMxWarps + warp;
+  const int64_t r = item / groups;
+  if (r >= rows || (rows_dev && r >= (int64_t)*rows_dev)) return;
+  const int b = (int)(item - r * groups) * 8 + (lane >> 2);
+  const bool valid = b < nb;
+  uint4 w = make_uint4(0u, 0u, 0u, 0u);
+  if (valid) w = reinterpret_cast<const uint4*>(m + (size_t)r * cols + (size_t)b * 32)[lane & 3];
+  const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    amax = fmaxf(amax, fabsf(__uint_as_float(a[i] << 16)));
+    amax = fmaxf(amax, fabsf(__uint_as_float(a[i] & 0xFFFF0000u)));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  if (!valid) return;
+  const int sx = mx_block_exponent(amax);
+  const float f = pow2_neg(sx);
+  uint32_t packed[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __fmul_rn(__uint_as_float(a[i] << 16), f);
+    const float hi = __fmul_rn(__uint_as_float(a[i] & 0xFFFF0000u), f);
+    const uint32_t pair =
+        __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);  // lo: low byte
+    if (i & 1)
+      packed[i >> 1] |= pair << 16;
+    else
+      packed[i >> 1] = pair;
+  }
+  reinterpret_cast<uint2*>(q + (size_t)r * cols + (size_t)b * 32)[lane & 3] =
+      make_uint2(packed[0], packed[1]);
+  if ((lane & 3) == 0) {
+    const uint8_t code = (uint8_t)(sx + 127);
+    if (atoms)
+      scale[((size_t)(r / 128) * (nb / 4) + b / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 +
+            b % 4] = code;
+    else
+      scale[(size_t)r * nb + b] = code;
+  }
+}
+
 __global__ void transpose_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int R,
                                  int C, int64_t in_es, int64_t out_es, int64_t out_off) {
   __shared__ uint16_t tile[32][33];
@@ -290,6 +371,17 @@ __global__ void transpose_kernel(const uint16_t* __restrict__ in, uint16_t* __re
 }
 
 }  // namespace
+
+int launch_quantize_mx_fp8(const uint16_t* m, int64_t rows, const int32_t* rows_dev, int cols,
+                           uint8_t* q, uint8_t* scale, int atoms, cudaStream_t s) {
+  if (rows <= 0) return 0;
+  const int64_t items = rows * ((cols / 32 + 7) / 8);
+  const int64_t blocks = (items + kMxWarps - 1) / kMxWarps;
+  launch_pdl(quantize_mx_fp8_kernel, dim3((unsigned)blocks), dim3(kMxWarps * 32), 0, s, m, rows,
+             rows_dev, cols, q, scale, atoms);
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? 1 : -(int)err;
+}
 
 int launch_combine(const CombineArgs& a, cudaStream_t s) {
   if (a.N <= 0) return 0;

@@ -51,6 +51,7 @@ namespace {
 constexpr int kBK = 64;           // contraction elements per stage (128 B of bf16)
 constexpr int kTileM = 128;       // weight rows per accumulator (UMMA M)
 constexpr int kMaxTileN = 256;    // slots per tile (UMMA N), at most
+constexpr int kMxMaxTileN = 224;  // the same for the MX modes (TMEM also holds the scales)
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 448;
 constexpr int kEpiWarps = 8;         // warps 2-9
@@ -110,6 +111,11 @@ struct GemmParams {
   float* part;                // FC2 dgrad: dprob partials [S, I/32]
   int inter;                  // I
   uint32_t* err;
+  const uint8_t* sfa;         // MX: E8M0 scales of the weight rows, 512-byte atoms
+  const uint8_t* sfb;         // MX: E8M0 scales of the B rows, [rows, sfb_ld]
+  int sfb_ld;                 // MX: scale bytes per B row (K / 32)
+  uint32_t sf_off;            // MX: offset in a stage of its scale atoms (2 of A, 2 of B)
+  uint32_t sf_tmem;           // MX: first TMEM column of the scale ring (16 per stage)
 };
 
 struct Tile {
@@ -349,8 +355,13 @@ template <int kMode, int kAct>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA2, const GemmParams p) {
-  constexpr bool kGatherB = kMode == kModeFc1 || kMode == kModeDgrad2 || kMode == kModeFc1Fp8;
-  constexpr bool kFc1 = kMode == kModeFc1 || kMode == kModeFc1Fp8;
+  constexpr bool kGatherB = kMode == kModeFc1 || kMode == kModeDgrad2 || kMode == kModeFc1Fp8 ||
+                            kMode == kModeFc1Mx;
+  constexpr bool kMx = kMode == kModeFc1Mx || kMode == kModeFc2Mx;
+  // warps 10-13 copy B rows (gathered modes) and, in the MX modes, the B rows'
+  // scale bytes
+  constexpr bool kGatherWarps = kGatherB || kMx;
+  constexpr bool kFc1 = kMode == kModeFc1 || kMode == kModeFc1Fp8 || kMode == kModeFc1Mx;
   constexpr bool kFp8 = kMode == kModeFc1Fp8 || kMode == kModeFc2Fp8;
   constexpr bool kAMn = kMode == kModeDgrad2 || kMode == kModeDgrad1;
   extern __shared__ uint8_t smem_raw[];
@@ -371,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), kGatherB ? 1 + kGatherThreads : 1);
+      mbar_init(smem_u32(&full_bar[s]), kGatherWarps ? 1 + kGatherThreads : 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -381,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kTileQ; ++i) {
       mbar_init(smem_u32(&tq_full[i]), 1);
       // consumers: the UMMA thread, the epilogue warps, the 4 gather warps (FC1)
-      mbar_init(smem_u32(&tq_empty[i]), 1 + kEpiWarps + (kGatherB ? 4 : 0));
+      mbar_init(smem_u32(&tq_empty[i]), 1 + kEpiWarps + (kGatherWarps ? 4 : 0));
     }
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
@@ -442,8 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the dropless shape).
       const int a_row0 = T.e * p.a_rows_per_expert + (kAMn ? 0 : T.f * p.f_rows);
       const int a_col0 = T.f * p.f_rows;
-      const uint32_t tx =
-          (uint32_t)T.nacc * kATileBytes + (kGatherB ? 0u : (uint32_t)T.n_eff * 128u);
+      const uint32_t tx = (uint32_t)T.nacc * kATileBytes +
+                          (kGatherB ? 0u : (uint32_t)T.n_eff * 128u) +
+                          (kMx ? (uint32_t)T.nacc * 512u : 0u);
       bool ok = true;
       for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
         const int s = (int)(gk % (uint32_t)p.stages);
@@ -468,6 +480,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st, &tmA, kx, a_row0, fb, pol_w);
             if (T.nacc == 2)
               tma_load_2d(st + kATileBytes, &tmA, kx, a_row0 + p.a_second_off, fb, pol_w);
+          }
+          if constexpr (kMx) {
+            // the weight rows' scale atom of this k tile, one per accumulator
+            for (int a2 = 0; a2 < T.nacc; ++a2) {
+              const int row = a_row0 + a2 * p.a_second_off;
+              bulk_load(st + p.sf_off + 512u * (uint32_t)a2,
+                        p.sfa + ((size_t)(row / kTileM) * p.k_tiles + kt) * 512u, 512u, fb);
+            }
           }
         }
         __syncwarp();
@@ -521,10 +541,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (lane == 0) {
           // B rows written by cp.async (generic proxy) are read by the tensor core
-          if (kGatherB) fence_proxy_async_smem();
+          if (kGatherWarps) fence_proxy_async_smem();
           const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
+          if constexpr (kMx) {
+            // this stage's scales into its TMEM columns: A atoms at +0 / +4, B
+            // atoms (128 rows each) at +8 / +12; the copies run before this
+            // thread's MMAs below
+            const uint32_t sft = tmem + p.sf_tmem + 16u * (uint32_t)s;
+            for (int a2 = 0; a2 < T.nacc; ++a2)
+              tmem_cp_32x128b_x4(sft + 4u * (uint32_t)a2,
+                                 sdesc_rows16(st + p.sf_off + 512u * (uint32_t)a2));
+            for (int g = 0; g * kTileM < T.n_eff; ++g)
+              tmem_cp_32x128b_x4(sft + 8u + 4u * (uint32_t)g,
+                                 sdesc_rows16(st + p.sf_off + 1024u + 512u * (uint32_t)g));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
+            for (int kk = 0; kk < 4; ++kk) {  // one 32-value scale block per k-step
+              const uint32_t acc = (kt | kk) != 0;
+              const uint32_t id = idesc_mx_e4m3(kTileM, T.n_eff, kk, kk);
+              const uint64_t bdesc = sdesc_sw128(st + p.b_off + (uint32_t)kk * 32u);
+              const uint32_t a0 = st + (uint32_t)kk * 32u;
+              umma_mx(dacc, sdesc_sw128(a0), bdesc, id, sft, sft + 8u, acc);
+              if (T.nacc == 2)
+                umma_mx(dacc + p.acc_off, sdesc_sw128(a0 + kATileBytes), bdesc, id, sft + 4u,
+                        sft + 8u, acc);
+            }
+          }
+#pragma unroll
+          for (int kk = 0; kk < (kMx ? 0 : kBK / 16); ++kk) {
             const uint32_t acc = (kt | kk) != 0;
             const uint64_t bdesc = sdesc_sw128(st + p.b_off + (uint32_t)kk * 32u);
             const uint32_t a0 = st + (uint32_t)kk * a_kstep;
@@ -695,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar[ab]));
     }
-  } else if (kGatherB) {
+  } else if (kGatherWarps) {
     // ---------------------------------------------------------------- B row gather
     // Row r of a stage holds act[sorted_slot_ids[slot0 + r], kx .. kx+63]:
     // 16-byte chunk c at r*128 + ((c ^ (r%8)) * 16), the 128-byte swizzle the
@@ -724,10 +767,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         off[i] = 0;
-        if (i < n_i) {
+        if (kGatherB && i < n_i) {
           const int tok = p.sorted_slot_ids[T.slot0 + rb + 16 * i];
           if ((unsigned)tok < (unsigned)p.act_rows) {
-            off[i] = (uint32_t)tok * (uint32_t)p.act_ld + (uint32_t)(c * 8);
+            // MX: the token itself (its scale row); otherwise its element offset
+            off[i] = kMx ? (uint32_t)tok : (uint32_t)tok * (uint32_t)p.act_ld + (uint32_t)(c * 8);
             vmask |= 1u << i;
           }
         }
@@ -740,11 +784,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t b = sbase + (uint32_t)s * p.stage_bytes + p.b_off + dst0;
-        const uint16_t* src = p.act + kt * kBK;
+        const uint32_t stb = sbase + (uint32_t)s * p.stage_bytes;
+        if constexpr (kGatherB) {
+          const uint32_t b = stb + p.b_off + dst0;
+          const uint16_t* src = p.act + kt * kBK;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (i < n_i) cp_async_16(b + (uint32_t)i * 2048u, src + off[i], ((vmask >> i) & 1u) << 4);
+          for (int i = 0; i < 16; ++i) {
+            if (i < n_i) {
+              const uint32_t eo = kMx ? off[i] * (uint32_t)p.act_ld + (uint32_t)(c * 8) : off[i];
+              cp_async_16(b + (uint32_t)i * 2048u, src + eo, ((vmask >> i) & 1u) << 4);
+            }
+          }
+        }
+        if constexpr (kMx) {
+          // the B rows' scale bytes of this k tile (4 blocks of 32) into the
+          // stage's B atoms: row r at (r/128)*512 + (r%32)*16 + ((r%128)/32)*4;
+          // rows past the tile's routes (or sentinel tokens) get zero scales
+          const uint32_t sfb_s = stb + p.sf_off + 1024u;
+          if constexpr (kMode == kModeFc1Mx) {
+            if (c == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                if (i < n_i) {
+                  const int r = rb + 16 * i;
+                  const uint32_t d = sfb_s + (uint32_t)((r >> 7) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4);
+                  cp_async_4(d, p.sfb + (size_t)off[i] * p.sfb_ld + kt * 4, ((vmask >> i) & 1u) << 2);
+                }
+              }
+            }
+          } else {
+            for (int r = gt; r < T.n_eff; r += kGatherThreads) {
+              const uint32_t d = sfb_s + (uint32_t)((r >> 7) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4);
+              cp_async_4(d, p.sfb + (size_t)(T.slot0 + r) * p.sfb_ld + kt * 4, r < T.rows ? 4u : 0u);
+            }
+          }
+        }
         cp_async_mbar_arrive_noinc(smem_u32(&full_bar[s]));
       }
     }
@@ -780,7 +854,10 @@ int device_sms(cudaError_t* err) {
         (e = set_smem_attr<kModeFc2Fp8, 0>()) != cudaSuccess ||
         (e = set_smem_attr<kModeDgrad2, 0>()) != cudaSuccess ||
         (e = set_smem_attr<kModeDgrad2, 1>()) != cudaSuccess ||
-        (e = set_smem_attr<kModeDgrad1, 0>()) != cudaSuccess)
+        (e = set_smem_attr<kModeDgrad1, 0>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc1Mx, 0>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc1Mx, 1>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc2Mx, 0>()) != cudaSuccess)
       cudaGetLastError();  // reported here; do not leave it for a later launch to report
     return e;
   });
@@ -792,7 +869,9 @@ int device_sms(cudaError_t* err) {
 int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.max_rows <= 0 || a.N <= 0) return 0;
   GemmParams p{};
-  const bool gather_b = a.mode == kModeFc1 || a.mode == kModeDgrad2 || a.mode == kModeFc1Fp8;
+  const bool gather_b = a.mode == kModeFc1 || a.mode == kModeDgrad2 || a.mode == kModeFc1Fp8 ||
+                        a.mode == kModeFc1Mx;
+  const bool mx = a.mode == kModeFc1Mx || a.mode == kModeFc2Mx;
   p.bm = a.bm;
   p.sorted_slot_ids = a.sorted_slot_ids;
   p.kept_counts = a.kept_counts;
@@ -813,7 +892,11 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   const int64_t S = a.s_max;
   const uint64_t E = (uint64_t)a.E;
   CUtensorMap tmA, tmB, tmA2;
-  p.max_tn = kMaxTileN;
+  // MX: the scale ring needs TMEM columns beside the two accumulators, so a
+  // slot tile holds at most 224 slots (2 x 224 + 4 stages x 16 <= 512)
+  p.max_tn = mx ? kMxMaxTileN : kMaxTileN;
+  p.sfa = a.w_sf;
+  p.sfb = a.b_sf;
   switch (a.mode) {
     case kModeFc1:  // A = w13 rows [E*2I, H] (gate and up accumulators); B gathered from x
       p.n_acc = 2;
@@ -845,6 +928,40 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       p.act_ld = a.H / 2;
       if (!make_map(&tmA, a.w, (uint64_t)(a.H / 2), E * 2 * a.I, kBK, kTileM)) return -1;
       tmB = tmA;
+      tmA2 = tmA;
+      break;
+    case kModeFc1Mx:  // as kModeFc1Fp8; the block scales travel with the operands
+      p.n_acc = 2;
+      p.pair_feats = 0;
+      p.m_total = a.I;
+      p.k_tiles = a.H / (2 * kBK);
+      p.a_rows_per_expert = 2 * a.I;
+      p.a_second_off = a.I;
+      p.f_rows = kTileM;
+      p.f_tiles = a.I / kTileM;
+      p.out_ld = a.I;
+      p.act_ld = a.H / 2;
+      p.sfb_ld = a.H / 32;
+      if (!a.w_sf || !a.b_sf) return -1;
+      if (!make_map(&tmA, a.w, (uint64_t)(a.H / 2), E * 2 * a.I, kBK, kTileM)) return -1;
+      tmB = tmA;
+      tmA2 = tmA;
+      break;
+    case kModeFc2Mx:  // as kModeFc2Fp8; the h rows' scale bytes gathered by warps 10-13
+      p.n_acc = 2;
+      p.pair_feats = 1;
+      p.m_total = a.H;
+      p.k_tiles = a.I / (2 * kBK);
+      p.a_rows_per_expert = a.H;
+      p.a_second_off = kTileM;
+      p.f_rows = 2 * kTileM;
+      p.f_tiles = (a.H + 2 * kTileM - 1) / (2 * kTileM);
+      p.out_ld = a.H;
+      p.act_ld = a.I / 2;
+      p.sfb_ld = a.I / 32;
+      if (!a.w_sf || !a.b_sf) return -1;
+      if (!make_map(&tmA, a.w, (uint64_t)(a.I / 2), E * a.H, kBK, kTileM)) return -1;
+      if (!make_map(&tmB, a.act, (uint64_t)(a.I / 2), (uint64_t)S, kBK, 16)) return -1;
       tmA2 = tmA;
       break;
     case kModeFc2:  // A = w2 rows [E*H, I], two 128-row feature tiles; B = h [S, I]
@@ -921,11 +1038,14 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   const int64_t grid_bound =
       (int64_t)p.f_tiles * ((a.max_total + p.max_tn - 1) / p.max_tn + a.E);
   p.b_off = (uint32_t)p.n_acc * kATileBytes;
-  p.stage_bytes = p.b_off + (((uint32_t)tile_cap * 128u + 1023u) & ~1023u);
+  p.sf_off = p.b_off + (((uint32_t)tile_cap * 128u + 1023u) & ~1023u);
+  p.stage_bytes = p.sf_off + (mx ? 2048u : 0u);  // MX: 2 A and 2 B scale atoms
   // the FP8 modes' epilogue keeps its B-row scales in shared memory
   const uint32_t xs_bytes = (a.mode == kModeFc1Fp8 || a.mode == kModeFc2Fp8) ? kXsBytes : 0u;
   p.stages = (int)((kSmemBudget - 1024u - kEpiStageBytes - kPsBytes - xs_bytes) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
+  p.sf_tmem = (uint32_t)(2 * p.max_tn);
+  if (mx && p.stages > (int)((kTmemCols - p.sf_tmem) / 16)) p.stages = (int)((kTmemCols - p.sf_tmem) / 16);
   if (p.stages < 2) return -1;
   p.epi_off = (uint32_t)p.stages * p.stage_bytes;
   p.ps_off = p.epi_off + kEpiStageBytes;
@@ -954,6 +1074,15 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
         launch_pdl(moe_gemm_kernel<kModeFc1Fp8, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
       break;
     case kModeFc2: launch_pdl(moe_gemm_kernel<kModeFc2, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p); break;
+    case kModeFc1Mx:
+      if (gelu)
+        launch_pdl(moe_gemm_kernel<kModeFc1Mx, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
+      else
+        launch_pdl(moe_gemm_kernel<kModeFc1Mx, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
+      break;
+    case kModeFc2Mx:
+      launch_pdl(moe_gemm_kernel<kModeFc2Mx, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
+      break;
     case kModeFc2Fp8:
       launch_pdl(moe_gemm_kernel<kModeFc2Fp8, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
       break;

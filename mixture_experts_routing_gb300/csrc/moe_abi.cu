@@ -267,13 +267,16 @@ static bool gemm_routes_ok(const moe_routes_t* routes) {
 // the weight-row and activation-row scales.
 static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, int mode,
                       const void* act, const void* w, void* out, void* preact,
-                      const float* w_scale, const float* x_scale, cudaStream_t stream) {
+                      const float* w_scale, const float* x_scale, cudaStream_t stream,
+                      const void* w_sf = nullptr, const void* b_sf = nullptr) {
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
   if (!gemm_routes_ok(routes)) return MOE_ERR_INVALID_ARG;
   const bool fp8 = mode == moe::kModeFc1Fp8 || mode == moe::kModeFc2Fp8;
-  const bool fc1 = mode == moe::kModeFc1 || mode == moe::kModeFc1Fp8;
+  const bool mx = mode == moe::kModeFc1Mx || mode == moe::kModeFc2Mx;
+  const bool fc1 = mode == moe::kModeFc1 || mode == moe::kModeFc1Fp8 || mode == moe::kModeFc1Mx;
   if (fp8 && (!w_scale || !x_scale)) return MOE_ERR_INVALID_ARG;
+  if (mx && (!w_sf || !b_sf || !aligned16(w_sf) || !aligned16(b_sf))) return MOE_ERR_INVALID_ARG;
   if (cfg->n_tokens == 0) return MOE_OK;
   if (!act || !w || !out || !aligned16(act) || !aligned16(w) || !aligned16(out) ||
       !aligned16(preact))
@@ -292,6 +295,8 @@ static int fc_forward(const moe_config_t* cfg, const moe_routes_t* routes, int m
   a.slot_prob = routes->slot_prob;
   a.w_scale = w_scale;
   a.x_scale = x_scale;
+  a.w_sf = static_cast<const uint8_t*>(w_sf);
+  a.b_sf = static_cast<const uint8_t*>(b_sf);
   a.act_rows = fc1 ? cfg->n_tokens : a.s_max;
   a.sched = routes->gemm_sched + (fc1 ? 0 : 2);
   return finish(moe::launch_gemm(a, stream));
@@ -355,6 +360,69 @@ int moe_ffn_forward_fp8(const moe_config_t* cfg, const moe_routes_t* routes, con
                                             static_cast<uint8_t*>(hq), h_scale, stream));
   if (rc != MOE_OK) return rc;
   return moe_fc2_forward_fp8(cfg, routes, hq, h_scale, w2q, w2_scale, o, stream);
+}
+
+int moe_quantize_mx_fp8(const void* m, int64_t rows, const int32_t* rows_dev, int cols, void* q,
+                        void* scale, cudaStream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 32 != 0 || rows > (int64_t)INT32_MAX)
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!m || !q || !scale || !aligned16(m) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return finish(moe::launch_quantize_mx_fp8(static_cast<const uint16_t*>(m), rows, rows_dev, cols,
+                                            static_cast<uint8_t*>(q),
+                                            static_cast<uint8_t*>(scale), 0, stream));
+}
+
+int moe_quantize_mx_fp8_weights(const void* m, int64_t rows, int cols, void* q, void* scale_atoms,
+                                cudaStream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 128 != 0 || rows % 128 != 0 || rows > (int64_t)INT32_MAX)
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!m || !q || !scale_atoms || !aligned16(m) || !aligned16(q) || !aligned16(scale_atoms))
+    return MOE_ERR_INVALID_ARG;
+  return finish(moe::launch_quantize_mx_fp8(static_cast<const uint16_t*>(m), rows, nullptr, cols,
+                                            static_cast<uint8_t*>(q),
+                                            static_cast<uint8_t*>(scale_atoms), 1, stream));
+}
+
+int moe_fc1_forward_mx(const moe_config_t* cfg, const moe_routes_t* routes, const void* xq,
+                       const void* x_sf, const void* w13q, const void* w13_sf, void* h,
+                       cudaStream_t stream) {
+  return fc_forward(cfg, routes, moe::kModeFc1Mx, xq, w13q, h, nullptr, nullptr, nullptr, stream,
+                    w13_sf, x_sf);
+}
+
+int moe_fc2_forward_mx(const moe_config_t* cfg, const moe_routes_t* routes, const void* hq,
+                       const void* h_sf, const void* w2q, const void* w2_sf, void* o,
+                       cudaStream_t stream) {
+  return fc_forward(cfg, routes, moe::kModeFc2Mx, hq, w2q, o, nullptr, nullptr, nullptr, stream,
+                    w2_sf, h_sf);
+}
+
+int moe_ffn_forward_mx(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,
+                       const void* w13q, const void* w13_sf, const void* w2q, const void* w2_sf,
+                       void* xq, void* x_sf, void* h, void* hq, void* h_sf, void* o,
+                       cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!gemm_routes_ok(routes) || !routes->num_tokens_post_padded) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_tokens == 0) return MOE_OK;
+  if (!x || !xq || !x_sf || !h || !hq || !h_sf || !aligned16(x) || !aligned16(xq) ||
+      !aligned16(x_sf) || !aligned16(h) || !aligned16(hq) || !aligned16(h_sf))
+    return MOE_ERR_INVALID_ARG;
+  rc = finish(moe::launch_quantize_mx_fp8(static_cast<const uint16_t*>(x), cfg->n_tokens, nullptr,
+                                          cfg->hidden, static_cast<uint8_t*>(xq),
+                                          static_cast<uint8_t*>(x_sf), 0, stream));
+  if (rc != MOE_OK) return rc;
+  rc = moe_fc1_forward_mx(cfg, routes, xq, x_sf, w13q, w13_sf, h, stream);
+  if (rc != MOE_OK) return rc;
+  // only the slots below the padded extent hold routes
+  rc = finish(moe::launch_quantize_mx_fp8(static_cast<const uint16_t*>(h), slots_of(cfg),
+                                          routes->num_tokens_post_padded, cfg->inter,
+                                          static_cast<uint8_t*>(hq), static_cast<uint8_t*>(h_sf), 0,
+                                          stream));
+  if (rc != MOE_OK) return rc;
+  return moe_fc2_forward_mx(cfg, routes, hq, h_sf, w2q, w2_sf, o, stream);
 }
 
 int moe_ffn_forward(const moe_config_t* cfg, const moe_routes_t* routes, const void* x,

@@ -120,6 +120,9 @@ enum GemmMode {
                     // gathered by slot; epilogue applies the row and token scales
   kModeFc2Fp8 = 5,  // FC2 in FP8: A = quantised w2 rows, B = quantised h rows (TMA);
                     // epilogue applies the w2 row and h slot-row scales
+  kModeFc1Mx = 6,   // FC1 on MX (block-scaled E4M3) operands: B rows of x gathered with
+                    // their scale bytes; the tensor cores apply the block scales
+  kModeFc2Mx = 7,   // FC2 on MX operands: B = h rows (TMA), their scale bytes gathered
 };
 
 struct GemmArgs {
@@ -139,6 +142,8 @@ struct GemmArgs {
   const float* w_scale;       // FP8: scale of each weight row (FC1 [E*2I], FC2 [E*H])
   const float* x_scale;       // FP8: scale of each B row (FC1: token [N]; FC2: slot [S])
   float* part;                // dgrad2: dprob partials [S, I/32]
+  const uint8_t* w_sf;        // MX: E8M0 scales of the weight rows in 512-byte atoms
+  const uint8_t* b_sf;        // MX: E8M0 scales of the B rows, [rows, K/32]
   int64_t act_rows;      // rows of act (N when gathered, else S)
   const int32_t* sorted_slot_ids;
   const int32_t* kept_counts;
@@ -222,6 +227,14 @@ int launch_combine(const CombineArgs& a, cudaStream_t s);
 // rows_dev, rows at or past *rows_dev (read on the device) are left as they are.
 int launch_quantize_rows_fp8(const uint16_t* m, int64_t rows, const int32_t* rows_dev, int cols,
                              uint8_t* q, float* scale, cudaStream_t s);
+
+// MX (block-scaled) E4M3 quantisation of a bf16 [rows, cols] matrix along its
+// rows (cols a multiple of 32; with atoms, rows and cols multiples of 128):
+// codes q [rows, cols] and one E8M0 scale byte per 32 values, plain
+// [rows, cols/32] or, with atoms, in the 512-byte atoms the MX GEMMs copy to
+// tensor memory. With rows_dev, rows at or past *rows_dev are left as they are.
+int launch_quantize_mx_fp8(const uint16_t* m, int64_t rows, const int32_t* rows_dev, int cols,
+                           uint8_t* q, uint8_t* scale, int atoms, cudaStream_t s);
 
 // The library's launch counter (moe_launch_count): read, and adjusted by the
 // graph ladder (captured launches are not executions; a replay is).

@@ -249,6 +249,67 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// ---- MX block-scaled E4M3 (tcgen05.mma kind::mxf8f6f4 with E8M0 scales)
+// Instruction descriptor: E4M3 A and B (format 0), scale format E8M0 (bit 23),
+// N >> 3 at bit 17, M >> 4 at bit 24, and which byte of each 32-bit scale
+// element this instruction uses: B's at bits 4-5, A's at bits 29-30.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n, int a_sf_id, int b_sf_id) {
+  return ((uint32_t)b_sf_id << 4) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(m >> 4) << 24) | ((uint32_t)a_sf_id << 29);
+}
+
+// D (+)= (A x scale_A) (B x scale_B)^T, M x N x 32, one E8M0 scale per 32
+// contraction values: row m of A takes the byte a_sf_id of TMEM lane m, column
+// sfa + m/32; column n of B the byte b_sf_id of lane n%32 (in the lane quarter
+// of the output row), column sfb + n/32 (measured on this hardware).
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of a plain (unswizzled) K-major matrix of 16-byte
+// rows stored back to back: 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128u >> 4) << 16;
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Copies 32 rows of 16 bytes from shared memory into TMEM columns col..col+3
+// of all four lane quarters (row r to lanes r, 32+r, 64+r, 96+r; bytes 4j..4j+3
+// of a row to column col+j). Asynchronous, ordered with the same thread's
+// later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared (addresses 16-byte aligned, bytes a multiple
+// of 16) completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// 4-byte global -> shared copy; src_bytes = 0 writes 4 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
