@@ -14,6 +14,8 @@ workload that fits one GPU. Its inputs exceed L2, so no flush is needed.
     python bench.py --workload dropless    # training step of the dropless,
                                            # bucketed layer (forward + backward),
                                            # swept over N = 128 .. 16384
+    python bench.py --mx                   # the same forward with MX block-scaled E4M3
+                                           # expert GEMMs (E8M0 scale per 32 values)
     python bench.py --fp8                  # the same forward with the expert GEMMs
                                            # on E4M3 operands (row-wise scales): a
                                            # variant line; the headline is bf16
@@ -62,6 +64,9 @@ def parse_args(argv=None):
     ap.add_argument("--fp8", action="store_true",
                     help="expert GEMMs on E4M3 operands with row-wise fp32 scales (x and h "
                          "quantised in the step); prints a variant line, not the bf16 headline")
+    ap.add_argument("--mx", action="store_true",
+                    help="expert GEMMs on MX block-scaled E4M3 operands (an E8M0 scale per 32 "
+                         "values along the contraction); prints a variant line")
     ap.add_argument("--serve", action="store_true",
                     help="variable batch sizes through the graph bucket ladder")
     ap.add_argument("--serve-batches", type=int, default=64)
@@ -76,8 +81,10 @@ def parse_args(argv=None):
                     help="default run only: skip the Qwen3-30B-shaped forward and the dropless "
                          "training step reported beside the headline")
     args = ap.parse_args(argv)
-    if args.fp8 and (args.activation != "swiglu" or args.prob_in_act):
-        ap.error("--fp8 runs the SwiGLU layer with p' in the combine")
+    if (args.fp8 or args.mx) and (args.activation != "swiglu" or args.prob_in_act):
+        ap.error("--fp8 and --mx run the SwiGLU layer with p' in the combine")
+    if args.fp8 and args.mx:
+        ap.error("--fp8 (row scales) and --mx (block scales) are separate variants")
     return args
 
 
@@ -214,19 +221,20 @@ def ncu_traffic(kernel: str, workload: str, units: float):
 
 
 # ----------------------------------------------------------------------------- work model
-def work_model(w, kept_counts, fp8=False, slots=0):
+def work_model(w, kept_counts, fp8=False, slots=0, mx=False):
     """Algorithmic bytes and flops per launch of each kernel, from the
     per-expert kept counts of this batch. fp8: GEMM operands are one byte
-    (plus a 4-byte scale per row), and the two quantisation passes read
-    bf16 x and the `slots` used rows of h."""
+    (plus a 4-byte scale per row; with mx a one-byte scale per 32 values),
+    and the two quantisation passes read bf16 x and the `slots` used rows of
+    h."""
     import numpy as np
     N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
     kc = np.asarray(kept_counts, dtype=np.int64)
     kept = int(kc.sum())
     active = int((kc > 0).sum())
     rows = int(((kc + 15) // 16 * 16).sum())  # slots the GEMMs compute (16-row granule)
-    ob = 1.0 if fp8 else 2.0                  # bytes per GEMM operand element
-    sb = 4.0 if fp8 else 0.0                  # bytes of scale per operand row
+    ob = (1.0 + 1.0 / 32 if mx else 1.0) if fp8 else 2.0  # bytes per GEMM operand element
+    sb = 4.0 if fp8 and not mx else 0.0                    # bytes of scale per operand row
     m = {}
     m["fc1"] = {"flops": 2.0 * kept * H * 2 * I,
                 "bytes": active * 2.0 * I * (H * ob + sb) + N * (H * ob + sb) + rows * I * 2,
@@ -235,8 +243,9 @@ def work_model(w, kept_counts, fp8=False, slots=0):
                 "bytes": active * 1.0 * H * (I * ob + sb) + rows * (I * ob + sb) + rows * H * 2,
                 "units": active, "unit": "active expert"}
     if fp8:
-        m["quant_x"] = {"flops": 0.0, "bytes": N * H * 3.0 + N * 4, "units": N, "unit": "token"}
-        m["quant_h"] = {"flops": 0.0, "bytes": slots * I * 3.0 + slots * 4, "units": slots,
+        m["quant_x"] = {"flops": 0.0, "bytes": N * H * (2.0 + ob) + N * sb, "units": N,
+                        "unit": "token"}
+        m["quant_h"] = {"flops": 0.0, "bytes": slots * I * (2.0 + ob) + slots * sb, "units": slots,
                         "unit": "slot"}
     m["combine"] = {"flops": 2.0 * kept * H, "bytes": kept * H * 2.0 + N * H * 2 + N * K * 8,
                     "units": N, "unit": "token"}
@@ -246,7 +255,7 @@ def work_model(w, kept_counts, fp8=False, slots=0):
     return m
 
 
-def roofline_for(name, model, ms, peaks, workload, fp8=False):
+def roofline_for(name, model, ms, peaks, workload, fp8=False, mx=False):
     """Roofline object of one kernel: bound, achieved, peak, frac, traffic.
     An E4M3 contraction takes the measured bf16 peak times the nominal
     FP8/BF16 dense ratio (4.5 / 2.25 PFLOP/s)."""
@@ -270,7 +279,8 @@ def roofline_for(name, model, ms, peaks, workload, fp8=False):
         r = {"bound": "alu" if name == "route" else "tensor", "achieved": ach, "peak": peak_c,
              "unit": "TFLOP/s", "frac": ach / peak_c,
              "peak_source": src + (" x 2 (nominal FP8/BF16 ratio)" if fp8 and name != "route" else "")}
-    tr = (ncu_traffic("moe_gemm_kernel:" + name + ("_fp8" if fp8 else ""), workload, d["units"])
+    tr = (ncu_traffic("moe_gemm_kernel:" + name + (("_mx" if mx else "_fp8") if fp8 else ""),
+                      workload, d["units"])
           if name in ("fc1", "fc2") else None)
     r["traffic"] = tr
     r["kernel"] = name
@@ -330,8 +340,9 @@ def time_oracle_sample(w, x_bits, wr, bias, bm, n_experts_sample, seed_experts=0
     return N / t_full, desc, t_route + t_ffn + t_comb, oracle.num_threads()
 
 
-def time_oracle_sample_fp8(w, x_bits, wr, bias, bm, n_experts_sample, seed_experts=0):
-    """The oracle's FP8 chain, as it stands, on a bounded sample of one step:
+def time_oracle_sample_fp8(w, x_bits, wr, bias, bm, n_experts_sample, seed_experts=0, mx=False):
+    """The oracle's FP8 chain (row scales; with mx block scales), as it
+    stands, on a bounded sample of one step:
     routing and x quantisation of every token; FC1 on E4M3 operands, h
     rounded to bf16 and quantised, FC2 on E4M3 operands for the kept routes
     of `n_experts_sample` experts (extrapolated to all kept routes by route
@@ -343,7 +354,8 @@ def time_oracle_sample_fp8(w, x_bits, wr, bias, bm, n_experts_sample, seed_exper
     N, H, E, K, I = w.n_tokens, w.hidden, w.n_experts, w.top_k, w.inter
     t0 = time.perf_counter()
     R = oracle.route(x_bits, wr, bias, E, K, w.cap_num, w.cap_den, bm)
-    xq, xs = oracle.quantize_rows_fp8(x_bits)
+    quant = oracle.quantize_mx_fp8 if mx else oracle.quantize_rows_fp8
+    xq, xs = quant(x_bits)
     t_route = time.perf_counter() - t0
     L = R.layout
     kept_total = int(L.kept_counts.sum())
@@ -355,15 +367,20 @@ def time_oracle_sample_fp8(w, x_bits, wr, bias, bm, n_experts_sample, seed_exper
         wg = synth.normal_bf16_bits(w.seed, synth.STREAM["wg"], e * H * I, H * I, w.w_std).reshape(H, I)
         wu = synth.normal_bf16_bits(w.seed, synth.STREAM["wu"], e * H * I, H * I, w.w_std).reshape(H, I)
         wd = synth.normal_bf16_bits(w.seed, synth.STREAM["wd"], e * I * H, I * H, w.w_std).reshape(I, H)
-        w13q, w13s = oracle.quantize_rows_fp8(np.ascontiguousarray(np.concatenate([wg.T, wu.T], 0)))
-        w2q, w2s = oracle.quantize_rows_fp8(np.ascontiguousarray(wd.T))
+        w13q, w13s = quant(np.ascontiguousarray(np.concatenate([wg.T, wu.T], 0)))
+        w2q, w2s = quant(np.ascontiguousarray(wd.T))
         base, k = e * L.cpad, int(L.kept_counts[e])
         toks = L.sorted_slot_ids[base:base + k]
         zero = np.zeros(k, np.int32)
         t0 = time.perf_counter()
-        h = oracle.fc1_fp8_routes(toks, zero, xq, xs, w13q[None], w13s[None], H, I)
-        hq, hs = oracle.quantize_rows_fp8(synth.f32_to_bf16_bits(h))
-        oracle.fc2_fp8_routes(zero, hq, hs, w2q[None], w2s[None], H, I)
+        if mx:
+            h = oracle.fc1_mx_routes(toks, zero, xq, xs, w13q[None], w13s, H, I)
+            hq, hs = quant(synth.f32_to_bf16_bits(h))
+            oracle.fc2_mx_routes(zero, hq, hs, w2q[None], w2s, H, I)
+        else:
+            h = oracle.fc1_fp8_routes(toks, zero, xq, xs, w13q[None], w13s[None], H, I)
+            hq, hs = quant(synth.f32_to_bf16_bits(h))
+            oracle.fc2_fp8_routes(zero, hq, hs, w2q[None], w2s[None], H, I)
         t_ffn += time.perf_counter() - t0
         n_routes += k
     o_zero = np.zeros((N * K, H), dtype=np.float32)
@@ -371,9 +388,10 @@ def time_oracle_sample_fp8(w, x_bits, wr, bias, bm, n_experts_sample, seed_exper
     oracle.combine(0, N, L.keep, R.topk_p, o_zero)
     t_comb = time.perf_counter() - t0
     t_full = t_route + t_ffn * kept_total / max(n_routes, 1) + t_comb
-    desc = ("FP8 chain: routing and x quantisation of all %d tokens + FC1/h quantisation/FC2 on "
+    desc = ("%s chain: routing and x quantisation of all %d tokens + FC1/h quantisation/FC2 on "
             "E4M3 operands for %d/%d experts (%d of %d kept routes, time extrapolated by route "
-            "count) + combine of all tokens" % (N, len(sample), len(cand), n_routes, kept_total))
+            "count) + combine of all tokens" % ("MX" if mx else "FP8", N, len(sample), len(cand),
+                                                n_routes, kept_total))
     return N / t_full, desc, t_route + t_ffn + t_comb, oracle.num_threads()
 
 
@@ -407,8 +425,9 @@ def run_reference(args):
         if train:  # dropless training step: routing + expert-path backward on a route sample
             return time_oracle_train_sample(wn, xn, dy_bits[:n], wr, bias, args.block_m,
                                             n_routes=1024, seed=i, act=act_code(args))
-        if args.fp8:
-            return time_oracle_sample_fp8(wn, xn, wr, bias, args.block_m, 1, seed_experts=i)
+        if args.fp8 or args.mx:
+            return time_oracle_sample_fp8(wn, xn, wr, bias, args.block_m, 1, seed_experts=i,
+                                          mx=args.mx)
         return time_oracle_sample(wn, xn, wr, bias, args.block_m, max(1, min(4, args.cpu_experts)),
                                   seed_experts=i, act=act_code(args),
                                   prob_in_act=args.prob_in_act)
@@ -452,7 +471,9 @@ def run_reference(args):
         "data": "synthetic", "config": {"workload": w.name, "description": w.note, "block_m": args.block_m,
                                         "parallelism": "single host, OpenMP",
                                         "precision": ("E4M3 GEMM operands, row-wise scales"
-                                                      if args.fp8 and not train else "bf16 inputs")},
+                                                      if args.fp8 and not train else
+                                                      "MX E4M3 GEMM operands, E8M0 scale per 32 values"
+                                                      if args.mx and not train else "bf16 inputs")},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "per step: " + desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -518,6 +539,7 @@ def run_ours(args):
     ctx = GpuCtx()
     out = forward_bench(args, ctx, args.workload, args.steps, args.warmup, full=True)
     extras = (not args.no_extras and ctx.world == 1 and args.workload == "dsv3" and not args.fp8
+              and not args.mx
               and args.activation == "swiglu" and not args.prob_in_act)
     if extras:
         import torch
@@ -584,19 +606,20 @@ def forward_bench(args, ctx, wname, steps, warmup, full=True):
     ws = moe.alloc_workspace(cfg, dev)
     h, o, y = moe.alloc_buffers(cfg, dev)
     stream = torch.cuda.current_stream(dev)
-    fp8 = args.fp8
+    mx = args.mx
+    fp8 = args.fp8 or mx  # one-byte GEMM operands (row scales, or MX block scales)
     weight_bytes = (w13.numel() + w2.numel()) * (1 if fp8 else 2)
     quant_ms = None
     if fp8:  # weights quantised once, before any step
         q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         q0.record(stream)
-        wq = moe.Fp8Weights(cfg, w13, w2, stream)
+        wq = moe.MxWeights(cfg, w13, w2, stream) if mx else moe.Fp8Weights(cfg, w13, w2, stream)
         q1.record(stream)
         torch.cuda.synchronize()
         quant_ms = q0.elapsed_time(q1)
         del w13, w2
         torch.cuda.empty_cache()
-        xq, xs, hq, hs = moe.alloc_fp8_buffers(cfg, dev)
+        xq, xs, hq, hs = (moe.alloc_mx_buffers if mx else moe.alloc_fp8_buffers)(cfg, dev)
 
     names = (("route", "quant_x", "fc1", "quant_h", "fc2", "combine") if fp8
              else ("route", "fc1", "fc2", "combine"))
@@ -612,7 +635,17 @@ def forward_bench(args, ctx, wname, steps, warmup, full=True):
         mark(0)
         moe.route_align(cfg, xb, wr, bias, routes, ws, s)
         mark(1)
-        if fp8:
+        if mx:
+            moe.quantize_mx_fp8(xb, xq, xs, s)
+            mark(2)
+            moe.fc1_forward_mx(cfg, routes, xq, xs, wq.w13q, wq.w13_sf, h, s)
+            mark(3)
+            # only the slots below the padded extent hold routes
+            moe.quantize_mx_fp8(h, hq, hs, s, rows_dev=routes.num_tokens_post_padded)
+            mark(4)
+            moe.fc2_forward_mx(cfg, routes, hq, hs, wq.w2q, wq.w2_sf, o, s)
+            mark(5)
+        elif fp8:
             moe.quantize_rows_fp8(xb, xq, xs, s)
             mark(2)
             moe.fc1_forward_fp8(cfg, routes, xq, xs, wq.w13q, wq.w13_scale, h, s)
@@ -703,10 +736,11 @@ def forward_bench(args, ctx, wname, steps, warmup, full=True):
     # inside the timed region too).
     ms_e2e = e2e_forward(ctx, stream, step, x, y, x_bits, N, H, steps) if full else None
 
-    model = work_model(w, kept_counts, fp8=fp8, slots=used_slots)
+    model = work_model(w, kept_counts, fp8=fp8, slots=used_slots, mx=mx)
     dom = max(names, key=lambda n: per_kernel[n])
-    roof = roofline_for(dom, model, per_kernel[dom], peaks, w.name, fp8=fp8)
-    kernels = {n: roofline_for(n, model, per_kernel[n], peaks, w.name, fp8=fp8) for n in names}
+    roof = roofline_for(dom, model, per_kernel[dom], peaks, w.name, fp8=fp8, mx=mx)
+    kernels = {n: roofline_for(n, model, per_kernel[n], peaks, w.name, fp8=fp8, mx=mx)
+               for n in names}
     gemm_ms = per_kernel["fc1"] + per_kernel["fc2"]
     gemm_flops = model["fc1"]["flops"] + model["fc2"]["flops"]
     issued = 2.0 * 3 * H * I * E * moe.capacity(cfg)
@@ -757,14 +791,17 @@ def forward_bench(args, ctx, wname, steps, warmup, full=True):
                       "copies": "pinned host x in and y out every step, on a second stream with two "
                                 "device buffers each, overlapping the compute of neighbouring steps"}
     if fp8:
-        out["config"]["precision"] = ("E4M3 GEMM operands with one fp32 scale per row (w13, w2 "
-                                      "rows once; x and h rows every step), fp32 accumulation; "
+        out["config"]["precision"] = (("MX E4M3 GEMM operands with an E8M0 scale per 32 values "
+                                       "along the contraction, applied by the tensor cores"
+                                       if mx else
+                                       "E4M3 GEMM operands with one fp32 scale per row") +
+                                      " (w13, w2 once; x and h every step), fp32 accumulation; "
                                       "x, h, o, y in bf16")
         out["weight_quantisation_ms"] = quant_ms
     if full and rank == 0 and world == 1 and not args.no_cpu_baseline:
         if fp8:
             v, desc, secs, cores = time_oracle_sample_fp8(w, x_bits, wr_h, bias_h, args.block_m,
-                                                          min(args.cpu_experts, 2))
+                                                          min(args.cpu_experts, 2), mx=mx)
         else:
             v, desc, secs, cores = time_oracle_sample(w, x_bits, wr_h, bias_h, args.block_m,
                                                       args.cpu_experts, act=act_code(args),

@@ -58,12 +58,12 @@ constexpr int kEpiWarps = 8;         // warps 2-9
 constexpr int kGatherWarp0 = 10;     // warps 10-13
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;  // 16 KiB
-// dynamic shared memory opt-in; with the kernel's ~3.3 KB of static shared
+// dynamic shared memory opt-in; with the kernel's 2.25 KB of static shared
 // memory the CTA stays under the 227 KB per-block limit
-constexpr uint32_t kSmemBudget = 223 * 1024;
+constexpr uint32_t kSmemBudget = 224 * 1024;
 constexpr int kGatherThreads = 128;  // warps 10-13
 constexpr int kStageRowElems = 32;   // epilogue staging row: 32 features (bf16)
-constexpr uint32_t kEpiStageBytes = kEpiWarps * 16u * kStageRowElems * 2u;  // per warp 16 rows
+constexpr uint32_t kEpiStageBytes = kEpiWarps * 8u * kStageRowElems * 2u;  // per warp 8 rows
 constexpr int kTileQ = 4;            // depth of the tile-id queue
 constexpr uint32_t kPsBytes = kEpiWarps * 16 * 4;  // FC2 dgrad: 16 p' values per epilogue warp
 constexpr uint32_t kXsBytes = kEpiWarps * 128 * 4;  // FC1 FP8: the token scales of a warp's
@@ -177,29 +177,28 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
 
 // Writes a 16-slot x 32-feature block to a bf16 row-major matrix: lane l holds
 // feature l of slots 0..15 in v; dst points at (slot 0, feature 0), ld is the
-// row stride in elements. Staged through this warp's 1 KiB buffer so that each
-// row goes out as four 16-byte stores.
+// row stride in elements. Staged through this warp's 512-byte buffer, eight
+// rows at a time, so that each row goes out as four 16-byte stores.
 __device__ __forceinline__ void store_rows16(uint32_t stg_u, int lane, const float (&v)[16],
                                              uint16_t* dst, int ld) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint32_t at = stg_u + (uint32_t)(i * kStageRowElems + lane) * 2u;
-    asm volatile("st.shared.b16 [%0], %1;" ::"r"(at), "h"((unsigned short)bf16_bits(v[i]))
-                 : "memory");
-  }
-  __syncwarp();
+  for (int h8 = 0; h8 < 2; ++h8) {
 #pragma unroll
-  for (int it = 0; it < 2; ++it) {  // 16 rows x 4 chunks of 16 bytes
-    const int ch = lane + it * 32;
-    const int row = ch >> 2, part = ch & 3;
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t at = stg_u + (uint32_t)(i * kStageRowElems + lane) * 2u;
+      asm volatile("st.shared.b16 [%0], %1;" ::"r"(at), "h"((unsigned short)bf16_bits(v[h8 * 8 + i]))
+                   : "memory");
+    }
+    __syncwarp();
+    const int row = lane >> 2, part = lane & 3;  // 8 rows x 4 chunks of 16 bytes
     uint4 val;
     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
                  : "r"(stg_u + (uint32_t)(row * kStageRowElems + part * 8) * 2u)
                  : "memory");
-    *reinterpret_cast<uint4*>(dst + (size_t)row * ld + part * 8) = val;
+    *reinterpret_cast<uint4*>(dst + (size_t)(h8 * 8 + row) * ld + part * 8) = val;
+    __syncwarp();
   }
-  __syncwarp();
 }
 
 // Gated activation act(gate) of the FFN and its derivative ("Permute-Free
@@ -597,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;  // which of the two warps of this lane quarter
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    const uint32_t stg_u = sbase + p.epi_off + (uint32_t)(warp - 2) * 16u * kStageRowElems * 2u;
+    const uint32_t stg_u = sbase + p.epi_off + (uint32_t)(warp - 2) * 8u * kStageRowElems * 2u;
     // FC2 dgrad: this warp's 16 p' values of the current chunk
     float* ps_w = reinterpret_cast<float*>(smem_raw + (sbase - smem_u32(smem_raw)) + p.ps_off) +
                   (warp - 2) * 16;
@@ -762,6 +761,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       Tile T;
       tile_at(p, tpre, ttn, t, T);
       const int n_i = T.n_eff >> 4;
+      // MX: the scale rows this thread copies (rows gt and gt + 128 of the
+      // tile), looked up once per tile; -1 for a row past the tile's routes or
+      // a sentinel token (zero scale bytes)
+      int sf_row[2] = {-1, -1};
+      if constexpr (kMx) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int r = gt + j * kGatherThreads;
+          if (r < T.rows) {
+            if constexpr (kMode == kModeFc1Mx) {
+              const int tok = p.sorted_slot_ids[T.slot0 + r];
+              sf_row[j] = (unsigned)tok < (unsigned)p.act_rows ? tok : -1;
+            } else {
+              sf_row[j] = T.slot0 + r;
+            }
+          }
+        }
+      }
       uint32_t off[16];
       uint32_t vmask = 0;
 #pragma unroll
@@ -799,23 +816,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kMx) {
           // the B rows' scale bytes of this k tile (4 blocks of 32) into the
           // stage's B atoms: row r at (r/128)*512 + (r%32)*16 + ((r%128)/32)*4;
-          // rows past the tile's routes (or sentinel tokens) get zero scales
+          // every gather thread copies at most two rows, so a stage's scales
+          // take one 4-byte copy per thread
           const uint32_t sfb_s = stb + p.sf_off + 1024u;
-          if constexpr (kMode == kModeFc1Mx) {
-            if (c == 0) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                if (i < n_i) {
-                  const int r = rb + 16 * i;
-                  const uint32_t d = sfb_s + (uint32_t)((r >> 7) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4);
-                  cp_async_4(d, p.sfb + (size_t)off[i] * p.sfb_ld + kt * 4, ((vmask >> i) & 1u) << 2);
-                }
-              }
-            }
-          } else {
-            for (int r = gt; r < T.n_eff; r += kGatherThreads) {
+          for (int j = 0; j < 2; ++j) {
+            const int r = gt + j * kGatherThreads;
+            if (r < T.n_eff) {
               const uint32_t d = sfb_s + (uint32_t)((r >> 7) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4);
-              cp_async_4(d, p.sfb + (size_t)(T.slot0 + r) * p.sfb_ld + kt * 4, r < T.rows ? 4u : 0u);
+              const int row = sf_row[j] < 0 ? 0 : sf_row[j];
+              cp_async_4(d, p.sfb + (size_t)row * p.sfb_ld + kt * 4, sf_row[j] < 0 ? 0u : 4u);
             }
           }
         }
