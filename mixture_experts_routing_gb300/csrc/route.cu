@@ -519,7 +519,10 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
     uint8_t* __restrict__ keep, int32_t* __restrict__ token_routes) {
   griddep_wait();  // launched after the kernel that writes this one's inputs
   griddep_launch_dependents();
-  __shared__ float zbuf[kTopkWarps][kMaxExperts];
+  // exp(l - max) of every token of the chunk, one row per token (padded so
+  // that lane l reading row l, column e, hits bank (l + e) % 32)
+  __shared__ float zbuf[kTokensPerChunk][kMaxExperts + 1];
+  __shared__ float ssum[kTokensPerChunk];
   __shared__ int32_t ids_s[kTokensPerChunk * kMaxTopK];
   __shared__ uint32_t pk_s[kTokensPerChunk * kMaxTopK];
   __shared__ uint32_t emask[kMaxExperts];  // bit tl: token tl of the chunk chose e
@@ -540,10 +543,12 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
     }
   }
   constexpr int PER = kMaxExperts / 32;
-  for (int tl = warp; tl < nt; tl += kTopkWarps) {
-    const int t = t0 + tl;
-    const float* l = logits + (size_t)t * E;
-    float v[PER];
+  static_assert(kTopkWarps == kTokensPerChunk, "one token of the chunk per warp");
+  // one token per warp: z = exp(l - max) kept in registers and in zbuf
+  const int tl = warp;
+  float v[PER];
+  if (tl < nt) {
+    const float* l = logits + (size_t)(t0 + tl) * E;
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
@@ -558,15 +563,22 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
       const int e = lane + 32 * j;
       if (e < E) {
         v[j] = route_exp(__fsub_rn(v[j], m));
-        zbuf[warp][e] = v[j];
+        zbuf[tl][e] = v[j];
       }
     }
-    __syncwarp();
-    float s = 0.0f;
-    if (lane == 0)
-      for (int e = 0; e < E; ++e) s = __fadd_rn(s, zbuf[warp][e]);  // ascending e
-    s = __shfl_sync(0xFFFFFFFFu, s, 0);
-    __syncwarp();
+  }
+  __syncthreads();
+  // the softmax denominators, each the sequential fp32 sum over ascending e:
+  // lane l of warp 0 sums token l's row, so one warp does all 32 sums at once
+  if (warp == 0 && lane < nt) {
+    float sacc = 0.0f;
+    for (int e = 0; e < E; ++e) sacc = __fadd_rn(sacc, zbuf[lane][e]);
+    ssum[lane] = sacc;
+  }
+  __syncthreads();
+  if (tl < nt) {
+    const int t = t0 + tl;
+    const float s = ssum[tl];
 #pragma unroll
     for (int j = 0; j < PER; ++j) v[j] = __fdiv_rn(v[j], s);
     // K picks of the largest p, ties to the lower e: warp max of the p bit
@@ -698,6 +710,7 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t s_cnt[kMaxChunks];
   __shared__ int32_t s_pos[kMaxChunks];
+  __shared__ int32_t s_lo[kMaxChunks];
   __shared__ uint32_t s_prefix;
   __shared__ int32_t s_remaining;
   __shared__ int32_t s_total;
@@ -720,9 +733,12 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
   uint32_t* keys = dyn;                                     // p' bits, token order
   int32_t* rids = reinterpret_cast<int32_t*>(dyn + Nmax);  // route index t*K+k
   // column e of the chunk tables -> positions in the expert's list
+  // this thread's chunk: the expert's route count in it and where they start
+  // in the chunk's sorted list (both read here, before any barrier)
   const int cnt = (tid < C) ? min(max(chunk_counts[(size_t)tid * E + e], 0), kTokensPerChunk) : 0;
+  const int lo0 = (tid < C) ? min(max(chunk_lofs[(size_t)tid * E + e], 0), kTokensPerChunk * K) : 0;
   const int pos0 = block_exclusive_scan<THREADS>(cnt, warp_tot);
-  if (tid < C) { s_cnt[tid] = cnt; s_pos[tid] = pos0; }
+  if (tid < C) { s_cnt[tid] = cnt; s_pos[tid] = pos0; s_lo[tid] = lo0; }
   if (tid == C - 1) s_total = pos0 + cnt;
   if (C == 0 && tid == 0) s_total = 0;
   __syncthreads();
@@ -757,7 +773,7 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
     extent = s_extent;
   }
   for (int cc = warp; cc < C; cc += THREADS / 32) {
-    const int lo = min(max(chunk_lofs[(size_t)cc * E + e], 0), kTokensPerChunk * K);
+    const int lo = s_lo[cc];
     const int64_t chunk_base = (int64_t)cc * kTokensPerChunk * K;
     const int m = (int)min((int64_t)min(s_cnt[cc], kTokensPerChunk * K - lo),
                            (int64_t)N * K - chunk_base - lo);
