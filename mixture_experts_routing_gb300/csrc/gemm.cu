@@ -116,6 +116,7 @@ struct GemmParams {
   int sfb_ld;                 // MX: scale bytes per B row (K / 32)
   uint32_t sf_off;            // MX: offset in a stage of its scale atoms (2 of A, 2 of B)
   uint32_t sf_tmem;           // MX: first TMEM column of the scale ring (16 per stage)
+  int f_cta;                  // pair mode: features of a pair tile that each CTA holds
 };
 
 struct Tile {
@@ -350,10 +351,23 @@ __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const
 
 // One instantiation per GemmMode (and per activation for the modes that apply
 // one), so each carries only its own code path.
-template <int kMode, int kAct>
+//
+// kPair = 1: the CTAs run as pairs (clusters of two) on one tile. Each CTA
+// loads its own 128 rows of every accumulator's weights and half of the
+// tile's B rows (slots [r*N/2, (r+1)*N/2) for CTA r), and holds its 128
+// accumulator rows in its TMEM; the even CTA issues the pair's M = 256 MMAs
+// (tcgen05 cta_group::2), which read both CTAs' shared memory. So a stage
+// holds half the B rows a one-CTA tile would, and each CTA's epilogue works on
+// its own features. Roles beyond the one-CTA ones: the even CTA's scheduler
+// publishes each tile to both CTAs; the odd CTA's warp 0 is only its producer
+// and its warp 1 relays "stage full" to the even CTA's barrier; the MMA
+// commits multicast their arrivals to both CTAs; the odd CTA's epilogue warps
+// release the accumulator on the even CTA's barrier.
+template <int kMode, int kAct, int kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA2, const GemmParams p) {
+  constexpr bool kP = kPair != 0;
   constexpr bool kGatherB = kMode == kModeFc1 || kMode == kModeDgrad2 || kMode == kModeFc1Fp8 ||
                             kMode == kModeFc1Mx;
   constexpr bool kMx = kMode == kModeFc1Mx || kMode == kModeFc2Mx;
@@ -378,27 +392,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
+  const uint32_t crank = kP ? cluster_ctarank() : 0u;
+  const bool lead = crank == 0u;  // the CTA that schedules and issues the MMAs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), kGatherWarps ? 1 + kGatherThreads : 1);
+      // pair mode, even CTA: one more arrival per phase, the odd CTA's relay
+      mbar_init(smem_u32(&full_bar[s]),
+                (kGatherWarps ? 1 + kGatherThreads : 1) + (kP && lead ? 1 : 0));
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tmem_full_bar[b]), 1);
-      mbar_init(smem_u32(&tmem_empty_bar[b]), kEpiWarps);  // one arrive per epilogue warp
+      // one arrive per epilogue warp (pair mode: of both CTAs, on the even one's)
+      mbar_init(smem_u32(&tmem_empty_bar[b]), kEpiWarps * (kP ? 2 : 1));
     }
     for (int i = 0; i < kTileQ; ++i) {
       mbar_init(smem_u32(&tq_full[i]), 1);
-      // consumers: the UMMA thread, the epilogue warps, the 4 gather warps (FC1)
-      mbar_init(smem_u32(&tq_empty[i]), 1 + kEpiWarps + (kGatherWarps ? 4 : 0));
+      // consumers: the UMMA thread, the epilogue warps, the 4 gather warps (FC1);
+      // pair mode adds the odd CTA's producer, relay, epilogue and gather warps
+      mbar_init(smem_u32(&tq_empty[i]), 1 + kEpiWarps + (kGatherWarps ? 4 : 0) +
+                                            (kP ? 2 + kEpiWarps + (kGatherWarps ? 4 : 0) : 0));
     }
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     if (!kGatherB) tma_prefetch_desc(&tmB);
     if (kAMn) tma_prefetch_desc(&tmA2);
   }
-  if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+  if (warp == 1) {
+    if constexpr (kP)
+      tmem_alloc_pair(smem_u32(&tmem_base_s), kTmemCols);
+    else
+      tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+  }
   // the setup above touches no global memory; the tile list reads the counts
   // the previous kernel wrote
   griddep_wait();
@@ -406,20 +432,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) build_tile_list(p, tpre, ttn, lane);
   tc_fence_before();
   __syncthreads();
+  // pair mode: both CTAs' barriers are initialised before either signals the other
+  if constexpr (kP) cluster_sync_all();
   const int n_tiles = tpre[p.E];
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  // pair mode: a barrier of this CTA at the same offset in the even CTA
+  auto at_lead = [&](const void* local) -> uint32_t {
+    return kP ? mapa_shared(smem_u32(local), 0u) : smem_u32(local);
+  };
+  // waits on barriers that the other CTA of a pair signals take cluster scope
+  auto wait_warp = [&](uint32_t bar, uint32_t parity, uint32_t code) -> bool {
+    if constexpr (kP)
+      return mbar_wait_cluster_warp(bar, parity, p.err, code);
+    else
+      return mbar_wait_warp(bar, parity, p.err, code);
+  };
 
   // Pops the next tile id (lane 0 waits, the warp gets the value); -1 ends.
   auto pop_tile = [&](uint32_t& qi, uint32_t code) -> int {
     const int slot = (int)(qi % kTileQ);
-    const bool ok = mbar_wait_warp(smem_u32(&tq_full[slot]), (qi / kTileQ) & 1u, p.err, code);
+    const bool ok = wait_warp(smem_u32(&tq_full[slot]), (qi / kTileQ) & 1u, code);
     const int t = ok ? tile_q[slot] : -1;
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&tq_empty[slot]));
+    if (lane == 0) {
+      if (kP && !lead)
+        mbar_arrive_remote_relaxed(at_lead(&tq_empty[slot]));
+      else
+        mbar_arrive(smem_u32(&tq_empty[slot]));
+    }
     ++qi;
     return t;
   };
+  // this CTA's first feature of tile T, and its share of the tile's B rows
+  auto feat_base = [&](const Tile& T) -> int { return T.f * p.f_rows + (int)crank * p.f_cta; };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -428,19 +474,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     uint32_t gk = 0;  // k-steps issued by this CTA, across tiles
+    uint32_t pq = 0;  // pair mode, odd CTA: tiles popped
     for (uint32_t qi = 0;; ++qi) {
-      const int slot = (int)(qi % kTileQ);
-      const bool free_ok =
-          qi < (uint32_t)kTileQ ||
-          mbar_wait_warp(smem_u32(&tq_empty[slot]), ((qi / kTileQ) - 1u) & 1u, p.err, kErrWaitEmpty);
       int t = -1;
-      if (lane == 0) {
-        if (free_ok) t = atomicAdd(&p.sched[0], 1);
-        if (t >= n_tiles) t = -1;
-        tile_q[slot] = t;
-        mbar_arrive(smem_u32(&tq_full[slot]));
+      if (kP && !lead) {
+        t = pop_tile(pq, kErrWaitFull);  // the odd CTA takes the even CTA's tile
+      } else {
+        const int slot = (int)(qi % kTileQ);
+        const bool free_ok =
+            qi < (uint32_t)kTileQ ||
+            wait_warp(smem_u32(&tq_empty[slot]), ((qi / kTileQ) - 1u) & 1u, kErrWaitEmpty);
+        if (lane == 0) {
+          if (free_ok) t = atomicAdd(&p.sched[0], 1);
+          if (t >= n_tiles) t = -1;
+          tile_q[slot] = t;
+          if constexpr (kP) {  // publish to the odd CTA too
+            st_shared_remote_u32(mapa_shared(smem_u32(&tile_q[slot]), 1u), (uint32_t)t);
+            mbar_arrive_remote(mapa_shared(smem_u32(&tq_full[slot]), 1u));
+          }
+          mbar_arrive(smem_u32(&tq_full[slot]));
+        }
+        t = __shfl_sync(0xFFFFFFFFu, t, 0);
       }
-      t = __shfl_sync(0xFFFFFFFFu, t, 0);
       if (t < 0) break;
       Tile T;
       tile_at(p, tpre, ttn, t, T);
@@ -450,10 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // chunks, all of them fetched by one 3-D copy ([chunk][row][64]; one copy
       // instead of one per chunk took the FC1 dgrad from 1.93 to 1.70 ms on
       // the dropless shape).
-      const int a_row0 = T.e * p.a_rows_per_expert + (kAMn ? 0 : T.f * p.f_rows);
-      const int a_col0 = T.f * p.f_rows;
+      const int fb0 = feat_base(T);
+      const int a_row0 = T.e * p.a_rows_per_expert + (kAMn ? 0 : fb0);
+      const int a_col0 = fb0;
+      // pair mode: this CTA's B rows, in 8-row boxes
+      const int b_rows = kP ? T.n_eff / 2 : T.n_eff;
+      const int b_row0 = T.slot0 + (int)crank * b_rows;
       const uint32_t tx = (uint32_t)T.nacc * kATileBytes +
-                          (kGatherB ? 0u : (uint32_t)T.n_eff * 128u) +
+                          (kGatherB ? 0u : (uint32_t)b_rows * 128u) +
                           (kMx ? (uint32_t)T.nacc * 512u : 0u);
       bool ok = true;
       for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
@@ -492,8 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (!kGatherB) {
           const uint32_t b = st + p.b_off;
-          for (int q = lane * 16; q < T.n_eff; q += 512)
-            tma_load_2d(b + (uint32_t)q * 128u, &tmB, kx, T.slot0 + q, fb, pol_x);
+          constexpr int kBox = kP ? 8 : 16;  // rows per B box
+          for (int q = lane * kBox; q < b_rows; q += 32 * kBox)
+            tma_load_2d(b + (uint32_t)q * 128u, &tmB, kx, b_row0 + q, fb, pol_x);
         }
       }
       if (!ok) break;
@@ -508,9 +568,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
       }
     }
+  } else if (kP && !lead && warp == 1) {
+    // ---------------------------------------------------------------- pair relay
+    // The odd CTA issues no MMAs: this warp tells the even CTA's MMA thread
+    // when each of this CTA's stages is full (its TMA bytes and its gathered
+    // rows have landed), ordering the gathered rows' generic-proxy writes
+    // before the tensor core's reads.
+    uint32_t gk = 0, qi = 0;
+    for (bool ok = true; ok;) {
+      const int t = pop_tile(qi, kErrWaitFull);
+      if (t < 0) break;
+      for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
+        const int s = (int)(gk % (uint32_t)p.stages);
+        const uint32_t u = gk / (uint32_t)p.stages;
+        if (!mbar_wait_warp(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          if (kGatherWarps) fence_proxy_async_smem();
+          mbar_arrive_remote_relaxed(at_lead(&full_bar[s]));
+        }
+        __syncwarp();
+      }
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- UMMA issuer
     // The whole warp walks the tiles and takes the waits; lane 0 issues.
+    // Pair mode (even CTA): the MMAs are the pair's (M = 256), the waits take
+    // cluster scope, and the commits arrive on both CTAs' barriers.
     uint32_t gk = 0, tc = 0, qi = 0;
     for (;;) {
       const int t = pop_tile(qi, kErrWaitFull);
@@ -519,13 +605,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_at(p, tpre, ttn, t, T);
       // accumulator buffer: two in flight when one tile uses 256 columns
       const uint32_t ab = tc % (uint32_t)p.n_buf, au = tc / (uint32_t)p.n_buf;
-      if (au > 0 &&
-          !mbar_wait_warp(smem_u32(&tmem_empty_bar[ab]), (au - 1) & 1u, p.err, kErrWaitAccum))
+      if (au > 0 && !wait_warp(smem_u32(&tmem_empty_bar[ab]), (au - 1) & 1u, kErrWaitAccum))
         break;
       tc_fence_after();
       const uint32_t dacc = tmem + ab * p.buf_stride;
-      const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kTileM, T.n_eff)
-                                  : (idesc_bf16_f32(kTileM, T.n_eff) | (kAMn ? kIdescAMnMajor : 0u));
+      const uint32_t idesc =
+          kFp8 ? idesc_e4m3_f32(kTileM, T.n_eff)
+               : (idesc_bf16_f32(kP ? 2 * kTileM : kTileM, T.n_eff) | (kAMn ? kIdescAMnMajor : 0u));
       // one UMMA k-step (16 elements) advances 32 bytes along a K-major row,
       // or 16 rows of 128 bytes in an MN-major tile
       constexpr uint32_t a_kstep = kAMn ? 2048u : 32u;
@@ -533,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kt = 0; kt < p.k_tiles; ++kt, ++gk) {
         const int s = (int)(gk % (uint32_t)p.stages);
         const uint32_t u = gk / (uint32_t)p.stages;
-        if (!mbar_wait_warp(smem_u32(&full_bar[s]), u & 1u, p.err, kErrWaitFull)) {
+        if (!wait_warp(smem_u32(&full_bar[s]), u & 1u, kErrWaitFull)) {
           ok = false;
           break;
         }
@@ -573,6 +659,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kFp8) {  // 32 E4M3 values = the same 32 bytes per k-step
               umma_fp8(dacc, sdesc_sw128(a0), bdesc, idesc, acc);
               if (T.nacc == 2) umma_fp8(dacc + p.acc_off, sdesc_sw128(a0 + kATileBytes), bdesc, idesc, acc);
+            } else if constexpr (kP) {
+              umma_bf16_pair(dacc, kAMn ? sdesc_sw128_mn(a0) : sdesc_sw128(a0), bdesc, idesc, acc);
+              if (T.nacc == 2) {
+                const uint32_t a1 = a0 + kATileBytes;
+                umma_bf16_pair(dacc + p.acc_off, kAMn ? sdesc_sw128_mn(a1) : sdesc_sw128(a1),
+                               bdesc, idesc, acc);
+              }
             } else {
               umma_bf16(dacc, kAMn ? sdesc_sw128_mn(a0) : sdesc_sw128(a0), bdesc, idesc, acc);
               if (T.nacc == 2) {
@@ -582,11 +675,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          umma_commit(smem_u32(&empty_bar[s]));
+          if constexpr (kP)
+            umma_commit_pair(smem_u32(&empty_bar[s]), 3);
+          else
+            umma_commit(smem_u32(&empty_bar[s]));
         }
         __syncwarp();
       }
-      if (lane == 0) umma_commit(smem_u32(&tmem_full_bar[ab]));  // also after an abort
+      if (lane == 0) {  // also after an abort
+        if constexpr (kP)
+          umma_commit_pair(smem_u32(&tmem_full_bar[ab]), 3);
+        else
+          umma_commit(smem_u32(&tmem_full_bar[ab]));
+      }
       __syncwarp();
       ++tc;
       if (!ok) break;
@@ -607,8 +708,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       Tile T;
       tile_at(p, tpre, ttn, t, T);
       const uint32_t ab = tc % (uint32_t)p.n_buf, au = tc / (uint32_t)p.n_buf;
-      const int feat0 = T.f * p.f_rows + q * 32;  // first feature of this lane quarter
-      const int nch = (T.n_eff - half * 16 + 31) / 32;  // this warp's 16-slot chunks
+      const int fbt = feat_base(T);
+      const int feat0 = fbt + q * 32;  // first feature of this lane quarter
+      // accumulators whose features this CTA writes: all of the tile's, except
+      // in a pair whose last feature tile is ragged (the odd CTA's 128-row
+      // halves past the last feature are computed but not stored)
+      int na = T.nacc;
+      if constexpr (kP) {
+        if (p.pair_feats)
+          na = (fbt >= p.m_total) ? 0 : (fbt + kTileM >= p.m_total ? min(T.nacc, 1) : T.nacc);
+        else
+          na = fbt < p.m_total ? T.nacc : 0;
+      }
+      const int nch = na > 0 ? (T.n_eff - half * 16 + 31) / 32 : 0;  // this warp's 16-slot chunks
       uint32_t gu_next[16];
       float p_next = 0.0f;
       float wsg = 1.0f, wsu = 1.0f;
@@ -653,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // the warp's vote: the warp-collective TMEM loads below are reached by
       // all lanes or by none
-      const bool w = mbar_wait_warp(smem_u32(&tmem_full_bar[ab]), au & 1u, p.err, kErrWaitAccum);
+      const bool w = wait_warp(smem_u32(&tmem_full_bar[ab]), au & 1u, kErrWaitAccum);
       ++tc;
       if (!w) break;
       tc_fence_after();
@@ -661,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kMode == kModeDgrad2) {
         // chunks of accumulator 0, then of accumulator 1; the next chunk's
         // operands load under this chunk's math
-        const int total = T.nacc * nch;
+        const int total = na * nch;
         for (int it = 0; it < total; ++it) {
           const int a = it / nch, c0 = half * 16 + 32 * (it - a * nch);
           uint32_t gu[16];
@@ -681,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           swiglu_backward_chunk<kAct>(p, T, c0, feat0 + a * kTileM, lane, stg_u, v, gu, ps_w - c0);
         }
       } else {
-        for (int c0 = half * 16; c0 < T.n_eff; c0 += 32) {
+        for (int c0 = half * 16; c0 < (na > 0 ? T.n_eff : 0); c0 += 32) {
           uint32_t v0[16], v1[16];
           tmem_ld16(ta + (uint32_t)c0, v0);
           if (T.nacc == 2) tmem_ld16(ta + p.acc_off + (uint32_t)c0, v1);
@@ -721,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* xs_c =
                 reinterpret_cast<const float*>(smem_raw + (sbase - smem_u32(smem_raw)) + p.xs_off) +
                 (warp - 2) * 128 + 16 * ((c0 - half * 16) >> 5);
-            for (int seg = 0; seg < T.nacc; ++seg) {
+            for (int seg = 0; seg < na; ++seg) {
               float ov[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
@@ -735,7 +847,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar[ab]));
+      if (lane == 0) {
+        if (kP && !lead)
+          mbar_arrive_remote_relaxed(at_lead(&tmem_empty_bar[ab]));
+        else
+          mbar_arrive(smem_u32(&tmem_empty_bar[ab]));
+      }
     }
   } else if (kGatherWarps) {
     // ---------------------------------------------------------------- B row gather
@@ -760,7 +877,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t < 0) break;
       Tile T;
       tile_at(p, tpre, ttn, t, T);
-      const int n_i = T.n_eff >> 4;
+      // this CTA's B rows: all of the tile's, or in a pair the half
+      // [crank*N/2, (crank+1)*N/2), in 16-row passes
+      const int g_rows = kP ? T.n_eff / 2 : T.n_eff;
+      const int g_off = kP ? (int)crank * g_rows : 0;
+      const int n_i = (g_rows - rb + 15) >> 4;  // rows rb + 16i below g_rows
       // MX: the scale rows this thread copies (rows gt and gt + 128 of the
       // tile), looked up once per tile; -1 for a row past the tile's routes or
       // a sentinel token (zero scale bytes)
@@ -785,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 16; ++i) {
         off[i] = 0;
         if (kGatherB && i < n_i) {
-          const int tok = p.sorted_slot_ids[T.slot0 + rb + 16 * i];
+          const int tok = p.sorted_slot_ids[T.slot0 + g_off + rb + 16 * i];
           if ((unsigned)tok < (unsigned)p.act_rows) {
             // MX: the token itself (its scale row); otherwise its element offset
             off[i] = kMx ? (uint32_t)tok : (uint32_t)tok * (uint32_t)p.act_ld + (uint32_t)(c * 8);
@@ -836,16 +957,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // pair mode: neither CTA leaves (or frees its TMEM) while the other may still
+  // signal its barriers or have MMAs write its accumulators
+  if constexpr (kP) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (kP)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-template <int kMode, int kAct>
+template <int kMode, int kAct, int kPair = 0>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(moe_gemm_kernel<kMode, kAct>,
+  return cudaFuncSetAttribute(moe_gemm_kernel<kMode, kAct, kPair>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+}
+
+// Whether a GEMM runs as CTA pairs (cta_group::2 tiles): the bf16 forward
+// GEMMs with a short contraction, where each tile's fixed costs weigh most and
+// halving the B rows each CTA stages pays (Qwen3-30B-shaped layer, H = 2048,
+// I = 768: FC1 0.217 -> 0.211 ms, FC2 0.136 -> 0.134 ms). With longer
+// contractions pairs measured slower (DeepSeek-V3-shaped FC1 2.39 -> 2.40,
+// FC2 1.26 -> 1.29 ms; the dropless layer's forward 2.63 -> 2.76 ms, its
+// dgrads as pairs 7.03 -> 7.08 ms).
+bool pair_mode(int mode, int H, int I) {
+  return (mode == kModeFc1 && H <= 2048) || (mode == kModeFc2 && I <= 1024);
 }
 
 // SM count of the current device, with every instantiation's shared-memory
@@ -867,7 +1005,10 @@ int device_sms(cudaError_t* err) {
         (e = set_smem_attr<kModeDgrad1, 0>()) != cudaSuccess ||
         (e = set_smem_attr<kModeFc1Mx, 0>()) != cudaSuccess ||
         (e = set_smem_attr<kModeFc1Mx, 1>()) != cudaSuccess ||
-        (e = set_smem_attr<kModeFc2Mx, 0>()) != cudaSuccess)
+        (e = set_smem_attr<kModeFc2Mx, 0>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc1, 0, 1>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc1, 1, 1>()) != cudaSuccess ||
+        (e = set_smem_attr<kModeFc2, 0, 1>()) != cudaSuccess)
       cudaGetLastError();  // reported here; do not leave it for a later launch to report
     return e;
   });
@@ -1042,13 +1183,23 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       return -1;
   }
   p.E = a.E;
+  const bool pair = pair_mode(a.mode, a.H, a.I);
+  if (pair) {
+    // a pair tile covers twice the features, each CTA f_cta of them; the B
+    // rows of a slot tile are split between the CTAs, fetched in 8-row boxes
+    p.f_cta = p.f_rows;
+    p.f_rows = 2 * p.f_rows;
+    p.f_tiles = (p.m_total + p.f_rows - 1) / p.f_rows;
+    if (!gather_b && !make_map(&tmB, a.act, (uint64_t)p.act_ld, (uint64_t)S, kBK, 8)) return -1;
+  }
   // stage size for the largest slot tile any expert can have
   const int64_t rows_cap = a.max_rows < p.max_tn ? a.max_rows : p.max_tn;
   const int tile_cap = (int)((rows_cap + 15) / 16 * 16);
+  const int b_rows_cap = pair ? tile_cap / 2 : tile_cap;  // B rows of a stage in one CTA
   const int64_t grid_bound =
-      (int64_t)p.f_tiles * ((a.max_total + p.max_tn - 1) / p.max_tn + a.E);
+      (int64_t)p.f_tiles * ((a.max_total + p.max_tn - 1) / p.max_tn + a.E) * (pair ? 2 : 1);
   p.b_off = (uint32_t)p.n_acc * kATileBytes;
-  p.sf_off = p.b_off + (((uint32_t)tile_cap * 128u + 1023u) & ~1023u);
+  p.sf_off = p.b_off + (((uint32_t)b_rows_cap * 128u + 1023u) & ~1023u);
   p.stage_bytes = p.sf_off + (mx ? 2048u : 0u);  // MX: 2 A and 2 B scale atoms
   // the FP8 modes' epilogue keeps its B-row scales in shared memory
   const uint32_t xs_bytes = (a.mode == kModeFc1Fp8 || a.mode == kModeFc2Fp8) ? kXsBytes : 0u;
@@ -1067,43 +1218,40 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   cudaError_t err = cudaSuccess;
   const int sms = device_sms(&err);
   if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
-  const int grid = (int)(grid_bound < sms ? grid_bound : sms);
+  int grid = (int)(grid_bound < sms ? grid_bound : sms);
+  if (pair) grid &= ~1;  // whole pairs
+  if (grid <= 0) return -1;
   p.sched = a.sched;
   const bool gelu = a.activation == 1;
+  // a mode's kernel, as CTA pairs or single CTAs
+#define MOE_LAUNCH_GEMM(MODE, ACT)                                                                  \
+  (pair ? launch_pdl_pairs(moe_gemm_kernel<MODE, ACT, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, \
+                           tmB, tmA2, p)                                                           \
+        : launch_pdl(moe_gemm_kernel<MODE, ACT, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB,  \
+                     tmA2, p))
+#define MOE_LAUNCH_GEMM1(MODE, ACT)                                                                 \
+  launch_pdl(moe_gemm_kernel<MODE, ACT, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p)
   switch (a.mode) {
     case kModeFc1:
-      if (gelu)
-        launch_pdl(moe_gemm_kernel<kModeFc1, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
-      else
-        launch_pdl(moe_gemm_kernel<kModeFc1, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
+      if (gelu) MOE_LAUNCH_GEMM(kModeFc1, 1); else MOE_LAUNCH_GEMM(kModeFc1, 0);
       break;
-    case kModeFc1Fp8:
-      if (gelu)
-        launch_pdl(moe_gemm_kernel<kModeFc1Fp8, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
-      else
-        launch_pdl(moe_gemm_kernel<kModeFc1Fp8, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
-      break;
-    case kModeFc2: launch_pdl(moe_gemm_kernel<kModeFc2, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p); break;
-    case kModeFc1Mx:
-      if (gelu)
-        launch_pdl(moe_gemm_kernel<kModeFc1Mx, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
-      else
-        launch_pdl(moe_gemm_kernel<kModeFc1Mx, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
-      break;
-    case kModeFc2Mx:
-      launch_pdl(moe_gemm_kernel<kModeFc2Mx, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
-      break;
-    case kModeFc2Fp8:
-      launch_pdl(moe_gemm_kernel<kModeFc2Fp8, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
-      break;
+    case kModeFc2: MOE_LAUNCH_GEMM(kModeFc2, 0); break;
     case kModeDgrad2:
-      if (gelu)
-        launch_pdl(moe_gemm_kernel<kModeDgrad2, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
-      else
-        launch_pdl(moe_gemm_kernel<kModeDgrad2, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p);
+      if (gelu) MOE_LAUNCH_GEMM1(kModeDgrad2, 1); else MOE_LAUNCH_GEMM1(kModeDgrad2, 0);
       break;
-    default: launch_pdl(moe_gemm_kernel<kModeDgrad1, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p); break;
+    case kModeDgrad1: MOE_LAUNCH_GEMM1(kModeDgrad1, 0); break;
+    case kModeFc1Fp8:
+      if (gelu) MOE_LAUNCH_GEMM1(kModeFc1Fp8, 1); else MOE_LAUNCH_GEMM1(kModeFc1Fp8, 0);
+      break;
+    case kModeFc2Fp8: MOE_LAUNCH_GEMM1(kModeFc2Fp8, 0); break;
+    case kModeFc1Mx:
+      if (gelu) MOE_LAUNCH_GEMM1(kModeFc1Mx, 1); else MOE_LAUNCH_GEMM1(kModeFc1Mx, 0);
+      break;
+    case kModeFc2Mx: MOE_LAUNCH_GEMM1(kModeFc2Mx, 0); break;
+    default: return -1;
   }
+#undef MOE_LAUNCH_GEMM
+#undef MOE_LAUNCH_GEMM1
   err = cudaGetLastError();
   if (err != cudaSuccess) return -(int)err;
   return 1;
