@@ -53,6 +53,16 @@ constexpr int kTileM = 128;       // weight rows per accumulator (UMMA M)
 constexpr int kMaxTileN = 256;    // slots per tile (UMMA N), at most
 constexpr int kMxMaxTileN = 224;  // the same for the MX modes (TMEM also holds the scales)
 constexpr int kMaxStages = 8;
+// Rows per TMA box of a slot-indexed B operand (one CTA; one CTA of a pair):
+// whole large boxes for the bulk of a tile's rows, small ones (a multiple of
+// which every tile's row count is) for the rest. Fewer, larger boxes took the
+// Qwen3-30B-shaped FC2 from 0.135 to 0.132 ms (pair: 0.132 -> 0.128 ms);
+// large boxes alone, reading past a tile's rows, cost the DeepSeek-V3-shaped
+// FC2 6 % (slot tiles of at most 160 rows).
+constexpr int kBBoxRows = 64;
+constexpr int kBBoxRowsPair = 32;
+constexpr int kBBoxRowsSmall = 16;
+constexpr int kBBoxRowsPairSmall = 8;
 constexpr int kThreads = 448;
 constexpr int kEpiWarps = 8;         // warps 2-9
 constexpr int kGatherWarp0 = 10;     // warps 10-13
@@ -366,7 +376,8 @@ __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const
 template <int kMode, int kAct, int kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmA2, const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmA2,
+                    const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   constexpr bool kP = kPair != 0;
   constexpr bool kGatherB = kMode == kModeFc1 || kMode == kModeDgrad2 || kMode == kModeFc1Fp8 ||
                             kMode == kModeFc1Mx;
@@ -416,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
-    if (!kGatherB) tma_prefetch_desc(&tmB);
+    if (!kGatherB) {
+      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmB2);
+    }
     if (kAMn) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) {
@@ -508,9 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int fb0 = feat_base(T);
       const int a_row0 = T.e * p.a_rows_per_expert + (kAMn ? 0 : fb0);
       const int a_col0 = fb0;
-      // pair mode: this CTA's B rows, in 8-row boxes
+      // pair mode: this CTA's B rows (half of the tile's)
       const int b_rows = kP ? T.n_eff / 2 : T.n_eff;
       const int b_row0 = T.slot0 + (int)crank * b_rows;
+      constexpr int kBox = kP ? kBBoxRowsPair : kBBoxRows;
+      constexpr int kBoxS = kP ? kBBoxRowsPairSmall : kBBoxRowsSmall;
+      const int b_big = b_rows / kBox * kBox;  // rows in whole large boxes
       const uint32_t tx = (uint32_t)T.nacc * kATileBytes +
                           (kGatherB ? 0u : (uint32_t)b_rows * 128u) +
                           (kMx ? (uint32_t)T.nacc * 512u : 0u);
@@ -551,9 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (!kGatherB) {
           const uint32_t b = st + p.b_off;
-          constexpr int kBox = kP ? 8 : 16;  // rows per B box
-          for (int q = lane * kBox; q < b_rows; q += 32 * kBox)
+          for (int q = lane * kBox; q < b_big; q += 32 * kBox)
             tma_load_2d(b + (uint32_t)q * 128u, &tmB, kx, b_row0 + q, fb, pol_x);
+          for (int q = b_big + lane * kBoxS; q < b_rows; q += 32 * kBoxS)
+            tma_load_2d(b + (uint32_t)q * 128u, &tmB2, kx, b_row0 + q, fb, pol_x);
         }
       }
       if (!ok) break;
@@ -1042,7 +1060,12 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   p.act_rows = gather_b ? a.N : 0;
   const int64_t S = a.s_max;
   const uint64_t E = (uint64_t)a.E;
-  CUtensorMap tmA, tmB, tmA2;
+  CUtensorMap tmA{}, tmB{}, tmA2{}, tmB2{};
+  // a slot-indexed B operand [S, cols]: large and small boxes
+  auto make_b = [&](const void* base, uint64_t cols) -> bool {
+    return make_map(&tmB, base, cols, (uint64_t)S, kBK, kBBoxRows) &&
+           make_map(&tmB2, base, cols, (uint64_t)S, kBK, kBBoxRowsSmall);
+  };
   // MX: the scale ring needs TMEM columns beside the two accumulators, so a
   // slot tile holds at most 224 slots (2 x 224 + 4 stages x 16 <= 512)
   p.max_tn = mx ? kMxMaxTileN : kMaxTileN;
@@ -1112,7 +1135,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       p.sfb_ld = a.I / 32;
       if (!a.w_sf || !a.b_sf) return -1;
       if (!make_map(&tmA, a.w, (uint64_t)(a.I / 2), E * a.H, kBK, kTileM)) return -1;
-      if (!make_map(&tmB, a.act, (uint64_t)(a.I / 2), (uint64_t)S, kBK, 16)) return -1;
+      if (!make_b(a.act, (uint64_t)(a.I / 2))) return -1;
       tmA2 = tmA;
       break;
     case kModeFc2:  // A = w2 rows [E*H, I], two 128-row feature tiles; B = h [S, I]
@@ -1127,7 +1150,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       p.out_ld = a.H;
       p.act_ld = a.I;
       if (!make_map(&tmA, a.w, (uint64_t)a.I, E * a.H, kBK, kTileM)) return -1;
-      if (!make_map(&tmB, a.act, (uint64_t)a.I, (uint64_t)S, kBK, 16)) return -1;
+      if (!make_b(a.act, (uint64_t)a.I)) return -1;
       tmA2 = tmA;
       break;
     case kModeFc2Fp8:  // FC2 on E4M3 bytes: w2q rows [E*H, I], hq [S, I], addressed as pairs
@@ -1142,7 +1165,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       p.out_ld = a.H;
       p.act_ld = a.I / 2;
       if (!make_map(&tmA, a.w, (uint64_t)(a.I / 2), E * a.H, kBK, kTileM)) return -1;
-      if (!make_map(&tmB, a.act, (uint64_t)(a.I / 2), (uint64_t)S, kBK, 16)) return -1;
+      if (!make_b(a.act, (uint64_t)(a.I / 2))) return -1;
       tmA2 = tmA;
       break;
     case kModeDgrad2:  // A[i, h] = w2[e][h][i] (MN-major, K = H); B gathered from dY [N, H]
@@ -1177,7 +1200,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
       p.act_ld = 2 * a.I;
       if (!make_map_mn3d(&tmA, a.w, (uint64_t)a.H, E * 2 * a.I, kBK, 4)) return -1;
       if (!make_map_mn3d(&tmA2, a.w, (uint64_t)a.H, E * 2 * a.I, kBK, 2)) return -1;
-      if (!make_map(&tmB, a.act, (uint64_t)(2 * a.I), (uint64_t)S, kBK, 16)) return -1;
+      if (!make_b(a.act, (uint64_t)(2 * a.I))) return -1;
       break;
     default:
       return -1;
@@ -1186,11 +1209,14 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   const bool pair = pair_mode(a.mode, a.H, a.I);
   if (pair) {
     // a pair tile covers twice the features, each CTA f_cta of them; the B
-    // rows of a slot tile are split between the CTAs, fetched in 8-row boxes
+    // rows of a slot tile are split between the CTAs, fetched in 32-row boxes
     p.f_cta = p.f_rows;
     p.f_rows = 2 * p.f_rows;
     p.f_tiles = (p.m_total + p.f_rows - 1) / p.f_rows;
-    if (!gather_b && !make_map(&tmB, a.act, (uint64_t)p.act_ld, (uint64_t)S, kBK, 8)) return -1;
+    if (!gather_b &&
+        !(make_map(&tmB, a.act, (uint64_t)p.act_ld, (uint64_t)S, kBK, kBBoxRowsPair) &&
+          make_map(&tmB2, a.act, (uint64_t)p.act_ld, (uint64_t)S, kBK, kBBoxRowsPairSmall)))
+      return -1;
   }
   // stage size for the largest slot tile any expert can have
   const int64_t rows_cap = a.max_rows < p.max_tn ? a.max_rows : p.max_tn;
@@ -1226,11 +1252,12 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   // a mode's kernel, as CTA pairs or single CTAs
 #define MOE_LAUNCH_GEMM(MODE, ACT)                                                                  \
   (pair ? launch_pdl_pairs(moe_gemm_kernel<MODE, ACT, 1>, dim3(grid), dim3(kThreads), dyn, s, tmA, \
-                           tmB, tmA2, p)                                                           \
+                           tmB, tmA2, tmB2, p)                                                     \
         : launch_pdl(moe_gemm_kernel<MODE, ACT, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB,  \
-                     tmA2, p))
+                     tmA2, tmB2, p))
 #define MOE_LAUNCH_GEMM1(MODE, ACT)                                                                 \
-  launch_pdl(moe_gemm_kernel<MODE, ACT, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, p)
+  launch_pdl(moe_gemm_kernel<MODE, ACT, 0>, dim3(grid), dim3(kThreads), dyn, s, tmA, tmB, tmA2, \
+             tmB2, p)
   switch (a.mode) {
     case kModeFc1:
       if (gelu) MOE_LAUNCH_GEMM(kModeFc1, 1); else MOE_LAUNCH_GEMM(kModeFc1, 0);
