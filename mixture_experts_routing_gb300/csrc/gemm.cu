@@ -76,6 +76,8 @@ constexpr int kStageRowElems = 32;   // epilogue staging row: 32 features (bf16)
 constexpr uint32_t kEpiStageBytes = kEpiWarps * 8u * kStageRowElems * 2u;  // per warp 8 rows
 constexpr int kTileQ = 4;            // depth of the tile-id queue
 constexpr uint32_t kPsBytes = kEpiWarps * 16 * 4;  // FC2 dgrad: 16 p' values per epilogue warp
+constexpr uint32_t kPreBufBytes = kEpiWarps * 2048;  // FC2 dgrad: a warp's next 16 x 2 x 32
+                                                      // pre-activations (bf16)
 constexpr uint32_t kXsBytes = kEpiWarps * 128 * 4;  // FC1 FP8: the token scales of a warp's
                                                     // (up to 8) chunks of 16 slots
 
@@ -187,17 +189,21 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
 }
 
 // Writes a 16-slot x 32-feature block to a bf16 row-major matrix: lane l holds
-// feature l of slots 0..15 in v; dst points at (slot 0, feature 0), ld is the
-// row stride in elements. Staged through this warp's 512-byte buffer, eight
-// rows at a time, so that each row goes out as four 16-byte stores.
-__device__ __forceinline__ void store_rows16(uint32_t stg_u, int lane, const float (&v)[16],
-                                             uint16_t* dst, int ld) {
+// feature l of slot j in value_of(j) (evaluated as the block is written, so
+// the 16 values need not be live together); dst points at (slot 0, feature 0),
+// ld is the row stride in elements. Staged through this warp's 512-byte
+// buffer, eight rows at a time, so that each row goes out as four 16-byte
+// stores.
+template <class F>
+__device__ __forceinline__ void store_rows16_of(uint32_t stg_u, int lane, F value_of,
+                                                uint16_t* dst, int ld) {
 #pragma unroll
   for (int h8 = 0; h8 < 2; ++h8) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t at = stg_u + (uint32_t)(i * kStageRowElems + lane) * 2u;
-      asm volatile("st.shared.b16 [%0], %1;" ::"r"(at), "h"((unsigned short)bf16_bits(v[h8 * 8 + i]))
+      asm volatile("st.shared.b16 [%0], %1;" ::"r"(at),
+                   "h"((unsigned short)bf16_bits(value_of(h8 * 8 + i)))
                    : "memory");
     }
     __syncwarp();
@@ -210,6 +216,12 @@ __device__ __forceinline__ void store_rows16(uint32_t stg_u, int lane, const flo
     *reinterpret_cast<uint4*>(dst + (size_t)(h8 * 8 + row) * ld + part * 8) = val;
     __syncwarp();
   }
+}
+
+// The same with the 16 values in registers: v[j] is slot j's.
+__device__ __forceinline__ void store_rows16(uint32_t stg_u, int lane, const float (&v)[16],
+                                             uint16_t* dst, int ld) {
+  store_rows16_of(stg_u, lane, [&](int j) { return v[j]; }, dst, ld);
 }
 
 // Gated activation act(gate) of the FFN and its derivative ("Permute-Free
@@ -237,99 +249,18 @@ __device__ __forceinline__ float act_grad_core(float v, float c) {
   return c * (1.0f + v * (1.0f - c));
 }
 
-// Pre-activations of 16 slots (c0..c0+15 of the tile) for this lane's feature:
-// gate in the low half, up in the high half of each word; 0 past the kept rows.
-__device__ __forceinline__ void load_preact16(const GemmParams& p, const Tile& T, int c0, int f,
-                                              uint32_t (&gu)[16]) {
-  const int ld2 = 2 * p.inter;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    gu[j] = 0u;
-    if (c0 + j < T.rows) {
-      const uint16_t* r = p.aux + (size_t)(T.slot0 + c0 + j) * ld2 + f;
-      gu[j] = (uint32_t)r[0] | ((uint32_t)r[p.inter] << 16);
-    }
-  }
-}
-
 // p' of slot c0 + lane of the tile for lanes 0..15 (0 past the kept rows).
 __device__ __forceinline__ float load_slot_prob(const GemmParams& p, const Tile& T, int c0, int lane) {
   return (lane < 16 && c0 + lane < T.rows) ? p.slot_prob[T.slot0 + c0 + lane] : 0.0f;
 }
 
-// Epilogue of the FC2 dgrad for 16 slots (registers) x 32 features (lanes).
-// dA0[s,i] = dY[t_s] . W_down[e][i,:] arrives in v; with g, u the saved
-// pre-activations (gu) and p' the slot's routing probability (ps):
-//   a = act(g) u,  dprob part = sum_i a dA0,  dA = p' dA0,
-//   dg = dA u act'(g),  du = dA act(g),  aw = p' a.
-// dg and du go to dPre (gate columns, then up columns), aw to out2, and the
-// 32-feature partial sum of a dA0 of each slot to part[s, feat0/32]. Padding
-// slots get zeros (their dA0, g, u and p' are 0).
-template <int act>
-__device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const Tile& T, int c0,
-                                                      int feat0, int lane, uint32_t stg_u,
-                                                      const uint32_t (&v)[16],
-                                                      const uint32_t (&gu)[16], const float* ps) {
-  const int I = p.inter;
-  const int ld2 = 2 * I;
+// The 32-feature partial sums of the dprob terms: dp[j] (slot j's term of
+// this lane's feature) summed over the warp's 32 lanes for each of the 16
+// slots, halving the values held per lane at each exchange (afterwards lanes
+// 2m and 2m+1 hold slot m), written to part[slot, feat0/32].
+__device__ __forceinline__ void dprob_part16(const GemmParams& p, const Tile& T, int c0, int feat0,
+                                             int lane, float (&dp)[16]) {
   const size_t row0 = (size_t)(T.slot0 + c0);
-  float o[16], dp[16];
-  if constexpr (act == 1) {
-    // gelu: Phi(g) (one erf) evaluated once per element and kept for all
-    // three outputs; du (and the dprob terms) with act(g) = g Phi(g)
-    float cr[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-      const float da0 = __uint_as_float(v[j]);
-      cr[j] = act_core<act>(g);
-      const float a = g * cr[j];
-      dp[j] = a * u * da0;
-      o[j] = ps[c0 + j] * da0 * a;
-    }
-    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + I + feat0, ld2);
-    // aw
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-      o[j] = ps[c0 + j] * ((g * cr[j]) * u);
-    }
-    store_rows16(stg_u, lane, o, p.out2 + row0 * I + feat0, I);
-    // dg
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-      o[j] = ps[c0 + j] * __uint_as_float(v[j]) * u * act_grad_core<act>(g, cr[j]);
-    }
-    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + feat0, ld2);
-  } else {
-    // silu: sigma is cheap, so each output recomputes it (no extra live array)
-    // dg
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-      const float da0 = __uint_as_float(v[j]);
-      dp[j] = act_fwd<act>(g) * u * da0;
-      o[j] = ps[c0 + j] * da0 * u * act_grad_core<act>(g, act_core<act>(g));
-    }
-    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + feat0, ld2);
-    // du
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = __uint_as_float(gu[j] << 16);
-      o[j] = ps[c0 + j] * __uint_as_float(v[j]) * act_fwd<act>(g);
-    }
-    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + I + feat0, ld2);
-    // aw
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-      o[j] = ps[c0 + j] * (act_fwd<act>(g) * u);
-    }
-    store_rows16(stg_u, lane, o, p.out2 + row0 * I + feat0, I);
-  }
-  // sum dp over the 32 lanes for each of the 16 slots, halving the values
-  // held per lane at each exchange: afterwards lanes 2m and 2m+1 hold slot m
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const bool hi = lane & 16;
@@ -356,7 +287,83 @@ __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const
   dp[0] += __shfl_xor_sync(0xFFFFFFFFu, dp[0], 1);
   const int m = lane >> 1;
   if ((lane & 1) == 0 && c0 + m < T.rows)
-    p.part[(row0 + m) * (size_t)(I / 32) + feat0 / 32] = dp[0];
+    p.part[(row0 + m) * (size_t)(p.inter / 32) + feat0 / 32] = dp[0];
+}
+
+// Epilogue of the FC2 dgrad for 16 slots (registers) x 32 features (lanes).
+// dA0[s,i] = dY[t_s] . W_down[e][i,:] arrives in v; with g, u the saved
+// pre-activations (gu) and p' the slot's routing probability (ps):
+//   a = act(g) u,  dprob part = sum_i a dA0,  dA = p' dA0,
+//   dg = dA u act'(g),  du = dA act(g),  aw = p' a.
+// dg and du go to dPre (gate columns, then up columns), aw to out2, and the
+// 32-feature partial sum of a dA0 of each slot to part[s, feat0/32]. Padding
+// slots get zeros (their dA0, g, u and p' are 0).
+template <int act>
+__device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const Tile& T, int c0,
+                                                      int feat0, int lane, uint32_t stg_u,
+                                                      const uint32_t (&v)[16],
+                                                      const uint32_t (&gu)[16], const float* ps) {
+  const int I = p.inter;
+  const int ld2 = 2 * I;
+  const size_t row0 = (size_t)(T.slot0 + c0);
+  float o[16], dp[16];
+  if constexpr (act == 1) {
+    // gelu: Phi(g) (one erf) evaluated once per element and kept for all
+    // three outputs; du (and the dprob terms) with act(g) = g Phi(g). The
+    // outputs are computed as they are staged, so no 16-value output array
+    // is live beside Phi (with one, this instantiation spilled past its 128
+    // registers).
+    float cr[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
+      cr[j] = act_core<act>(g);
+      dp[j] = g * cr[j] * u * __uint_as_float(v[j]);
+    }
+    dprob_part16(p, T, c0, feat0, lane, dp);  // before the stores: dp is dead after it
+    auto g_of = [&](int j) { return __uint_as_float(gu[j] << 16); };
+    auto u_of = [&](int j) { return __uint_as_float(gu[j] & 0xFFFF0000u); };
+    store_rows16_of(
+        stg_u, lane, [&](int j) { return ps[c0 + j] * __uint_as_float(v[j]) * (g_of(j) * cr[j]); },
+        p.out + row0 * ld2 + I + feat0, ld2);
+    // aw
+    store_rows16_of(
+        stg_u, lane, [&](int j) { return ps[c0 + j] * ((g_of(j) * cr[j]) * u_of(j)); },
+        p.out2 + row0 * I + feat0, I);
+    // dg
+    store_rows16_of(
+        stg_u, lane,
+        [&](int j) {
+          return ps[c0 + j] * __uint_as_float(v[j]) * u_of(j) * act_grad_core<act>(g_of(j), cr[j]);
+        },
+        p.out + row0 * ld2 + feat0, ld2);
+  } else {
+    // silu: sigma is cheap, so each output recomputes it (no extra live array)
+    // dg
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
+      const float da0 = __uint_as_float(v[j]);
+      dp[j] = act_fwd<act>(g) * u * da0;
+      o[j] = ps[c0 + j] * da0 * u * act_grad_core<act>(g, act_core<act>(g));
+    }
+    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + feat0, ld2);
+    // du
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16);
+      o[j] = ps[c0 + j] * __uint_as_float(v[j]) * act_fwd<act>(g);
+    }
+    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + I + feat0, ld2);
+    // aw
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
+      o[j] = ps[c0 + j] * (act_fwd<act>(g) * u);
+    }
+    store_rows16(stg_u, lane, o, p.out2 + row0 * I + feat0, I);
+  }
+  if constexpr (act != 1) dprob_part16(p, T, c0, feat0, lane, dp);
 }
 
 // One instantiation per GemmMode (and per activation for the modes that apply
@@ -719,6 +726,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // FC2 dgrad: this warp's 16 p' values of the current chunk
     float* ps_w = reinterpret_cast<float*>(smem_raw + (sbase - smem_u32(smem_raw)) + p.ps_off) +
                   (warp - 2) * 16;
+    // FC2 dgrad: the next chunk's pre-activations wait in this warp's 2 KB of
+    // shared memory (row r: gate features at r*128, up at r*128 + 64),
+    // fetched with 16-byte cp.async copies, instead of in 16 registers
+    // filled by 2-byte loads (with gelu, whose backward keeps Phi of 16
+    // values live, the register form spilled past the 128 registers)
+    const uint32_t pre_u = sbase + p.xs_off + (uint32_t)(warp - 2) * 2048u;
+    auto prefetch_preact = [&](const Tile& T, int c, int f0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int pi = lane + 32 * k;  // 16 rows x (4 gate + 4 up) 16-byte pieces
+        const int r = pi >> 3, gsel = (pi >> 2) & 1, qq = pi & 3;
+        const bool ok = c + r < T.rows;
+        const uint16_t* src = p.aux + (size_t)(T.slot0 + (ok ? c + r : 0)) * (2 * p.inter) +
+                              (gsel ? p.inter : 0) + f0 + qq * 8;
+        cp_async_16(pre_u + (uint32_t)(r * 128 + gsel * 64 + qq * 16), src, ok ? 16u : 0u);
+      }
+      cp_async_commit();
+    };
+    auto read_preact = [&](uint32_t (&gu)[16]) {
+      cp_async_wait_all();
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        uint16_t g, u;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(g) : "r"(pre_u + (uint32_t)(j * 128 + lane * 2)));
+        asm volatile("ld.shared.u16 %0, [%1];"
+                     : "=h"(u)
+                     : "r"(pre_u + (uint32_t)(j * 128 + 64 + lane * 2)));
+        gu[j] = (uint32_t)g | ((uint32_t)u << 16);
+      }
+      __syncwarp();  // every lane has its values before the buffer is refilled
+    };
     uint32_t tc = 0, qi = 0;
     for (;;) {
       const int t = pop_tile(qi, kErrWaitAccum);
@@ -739,7 +778,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           na = fbt < p.m_total ? T.nacc : 0;
       }
       const int nch = na > 0 ? (T.n_eff - half * 16 + 31) / 32 : 0;  // this warp's 16-slot chunks
-      uint32_t gu_next[16];
       float p_next = 0.0f;
       float wsg = 1.0f, wsu = 1.0f;
       if constexpr (kFp8) {
@@ -777,8 +815,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (kMode == kModeDgrad2 && nch > 0) {
         // before the accumulator is ready: the first chunk's pre-activations
-        // and p' (lane j < 16 holds slot j's) into registers
-        load_preact16(p, T, half * 16, feat0 + lane, gu_next);
+        // and p' (lane j < 16 holds slot j's)
+        prefetch_preact(T, half * 16, feat0);
         p_next = load_slot_prob(p, T, half * 16, lane);
       }
       // the warp's vote: the warp-collective TMEM loads below are reached by
@@ -794,13 +832,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int total = na * nch;
         for (int it = 0; it < total; ++it) {
           const int a = it / nch, c0 = half * 16 + 32 * (it - a * nch);
-          uint32_t gu[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) gu[j] = gu_next[j];
+          uint32_t gu[16];  // gate in the low half, up in the high half of each word
+          read_preact(gu);
           const float p_cur = p_next;
           if (it + 1 < total) {
             const int a2 = (it + 1) / nch, c2 = half * 16 + 32 * (it + 1 - a2 * nch);
-            load_preact16(p, T, c2, feat0 + a2 * kTileM + lane, gu_next);
+            prefetch_preact(T, c2, feat0 + a2 * kTileM);
             p_next = load_slot_prob(p, T, c2, lane);
           }
           uint32_t v[16];
@@ -1227,8 +1264,11 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   p.b_off = (uint32_t)p.n_acc * kATileBytes;
   p.sf_off = p.b_off + (((uint32_t)b_rows_cap * 128u + 1023u) & ~1023u);
   p.stage_bytes = p.sf_off + (mx ? 2048u : 0u);  // MX: 2 A and 2 B scale atoms
-  // the FP8 modes' epilogue keeps its B-row scales in shared memory
-  const uint32_t xs_bytes = (a.mode == kModeFc1Fp8 || a.mode == kModeFc2Fp8) ? kXsBytes : 0u;
+  // the FP8 modes' epilogue keeps its B-row scales in shared memory, the FC2
+  // dgrad its next pre-activations (the same region)
+  const uint32_t xs_bytes = (a.mode == kModeFc1Fp8 || a.mode == kModeFc2Fp8) ? kXsBytes
+                            : a.mode == kModeDgrad2                        ? kPreBufBytes
+                                                                           : 0u;
   p.stages = (int)((kSmemBudget - 1024u - kEpiStageBytes - kPsBytes - xs_bytes) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   p.sf_tmem = (uint32_t)(2 * p.max_tn);

@@ -411,15 +411,12 @@ __global__ void __launch_bounds__(kRSmallThreads) router_logits_small_kernel(
 }
 
 int router_sm_count(cudaError_t* err) {
-  static int sms[64] = {};
-  int dev = 0;
-  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && sms[dev] > 0) return sms[dev];
+  static DeviceOnce sms;
   int n = 0;
-  if ((*err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return 0;
-  if (dev >= 0 && dev < 64) sms[dev] = n;
-  return n;
+  *err = once_per_device(sms, &n, [](int dev, int* v) {
+    return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+  });
+  return *err == cudaSuccess ? n : 0;
 }
 
 template <int TX>
