@@ -288,15 +288,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // Stage row r (slot slot0 + 64kt + r) of 64-feature chunk c holds
     // act[t, col0 + 64c .. +63] for t = sorted_slot_ids[slot]: 16-byte unit j
     // at c*8192 + r*128 + ((j ^ (r%8)) * 16). Slots past the kept count and
-    // sentinel tokens are zero-filled. A warp copies whole rows (lane = 16-byte
-    // unit; rpi = 32/units rows per instruction): warp g owns rows
-    // rpi*g + sub + 4*rpi*i, and lane j < 16 holds the token of the warp's j-th
-    // row, loaded one stage ahead and broadcast with a shuffle. The full
-    // barrier receives each thread's arrival when its copies complete
-    // (cp.async.mbarrier.arrive.noinc); the UMMA thread fences them against
-    // its async-proxy reads. Waits end in a warp vote, so a warp leaves
-    // together when one runs out.
+    // sentinel tokens are zero-filled. One warp instruction copies one chunk
+    // (128 bytes) of four consecutive rows, 512 contiguous bytes of shared
+    // memory (lane l: row 4i + l/8, unit l%8); with four chunks warp g takes
+    // chunk g of all 64 rows (16 instructions a stage), with two chunk g%2 of
+    // rows 32*(g/2) .. +31 (8). (Copying a whole 512-byte token row per
+    // instruction into four chunks 8 KB apart issued 1.5x slower.) Lane l
+    // holds the tokens of stage rows l and l + 32, loaded one stage ahead and
+    // broadcast with a shuffle. The full barrier receives each thread's
+    // arrival when its copies complete (cp.async.mbarrier.arrive.noinc); the
+    // UMMA thread fences them against its async-proxy reads. Waits end in a
+    // warp vote, so a warp leaves together when one runs out.
     const int gw = warp - kWGatherWarp0;
+    const int jj = lane & 7, rsub = lane >> 3;
     uint32_t gk = 0, qi = 0;
     bool ok = true;
     while (ok) {
@@ -304,24 +308,21 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (t < 0) break;
       WTile T;
       wtile_at(p, t, T);
-      const int g_chunks = p.a_gather ? 2 * T.nacc : p.tile_n / 64;
-      const int units = g_chunks * 8;     // 16-byte units per row: 16 or 32
-      const int rpi = 32 / units;         // rows per warp instruction: 2 or 1
-      const int sub = lane / units;
-      const int uc = lane % units;
-      const int c = uc >> 3, jj = uc & 7;
-      const int n_ins = 16 / rpi;         // instructions per stage
-      const int my_row = rpi * gw + (lane % rpi) + 4 * rpi * (lane / rpi);  // lane < 16
-      const int gcol0 = (p.a_gather ? T.m0 : T.n0) + c * 64 + jj * 8;
+      const int g_chunks = p.a_gather ? 2 * T.nacc : p.tile_n / 64;  // 4 or 2
+      const int cw = g_chunks == 4 ? gw : (gw & 1);
+      const int row_lo = g_chunks == 4 ? 0 : 32 * (gw >> 1);
+      const int n_ins = g_chunks == 4 ? 16 : 8;
+      const int gcol0 = (p.a_gather ? T.m0 : T.n0) + cw * 64 + jj * 8;
       const int chunks = (T.kept + kWK - 1) / kWK;
-      auto token_of = [&](int kt) -> int {
-        const int ks = kt * kWK + my_row;
-        return (lane < 16 && kt < chunks && ks < T.kept) ? p.sorted_slot_ids[T.slot0 + ks] : -1;
+      auto token_of = [&](int kt, int r) -> int {
+        const int ks = kt * kWK + r;
+        return (kt < chunks && ks < T.kept) ? p.sorted_slot_ids[T.slot0 + ks] : -1;
       };
-      int nxt = token_of(0);
+      int nxt0 = token_of(0, lane), nxt1 = token_of(0, lane + 32);
       for (int kt = 0; kt < chunks; ++kt, ++gk) {
-        const int cur = nxt;
-        nxt = token_of(kt + 1);
+        const int cur0 = nxt0, cur1 = nxt1;
+        nxt0 = token_of(kt + 1, lane);
+        nxt1 = token_of(kt + 1, lane + 32);
         const int s = (int)(gk % (uint32_t)p.stages);
         const uint32_t u = gk / (uint32_t)p.stages;
         if (gk >= (uint32_t)p.stages &&
@@ -329,12 +330,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t g = sbase + (uint32_t)s * kWStageBytes + g_off + (uint32_t)c * 8192u;
+        const uint32_t g = sbase + (uint32_t)s * kWStageBytes + g_off + (uint32_t)cw * 8192u;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (i < n_ins) {
-            const int tok = __shfl_sync(0xFFFFFFFFu, cur, i * rpi + sub);
-            const int r = rpi * gw + sub + 4 * rpi * i;
+            const int r0 = row_lo + 4 * i;  // the instruction's first row (warp-uniform)
+            const int r = r0 + rsub;
+            const int tok = __shfl_sync(0xFFFFFFFFu, r0 < 32 ? cur0 : cur1, r & 31);
             const bool valid = (unsigned)tok < (unsigned)p.act_rows;
             const uint16_t* src = p.act + (size_t)(valid ? tok : 0) * p.act_ld + gcol0;
             cp_async_16(g + (uint32_t)r * 128u + ((uint32_t)(jj ^ (r & 7)) << 4), src,
