@@ -51,6 +51,8 @@ constexpr uint32_t kWABytes = 2 * kWM * kWK * 2;  // 32 KiB: two accumulators' A
 constexpr uint32_t kWBBytes = kWN * kWK * 2;      // 32 KiB: 4 chunks
 constexpr uint32_t kWStageBytes = kWABytes + kWBBytes;
 constexpr uint32_t kWSmemBudget = 223 * 1024;
+// the epilogue's output staging: per warp one 16-column x 32-row fp32 block
+constexpr uint32_t kWOutStgBytes = kWEpiWarps * 16 * 32 * 4;
 constexpr uint32_t kWTmemCols = 512;
 constexpr int kWTileQ = 4;
 
@@ -89,7 +91,7 @@ __device__ __forceinline__ void wtile_at(const WgradParams& p, int t, WTile& T) 
 
 __global__ void __launch_bounds__(kWThreads, 1)
     moe_wgrad_kernel(const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
-                     const WgradParams p) {
+                     const __grid_constant__ CUtensorMap tmO, const WgradParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kWMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kWMaxStages];
@@ -245,10 +247,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
   } else if (warp < 2 + kWEpiWarps) {
     // ------------------------------------------------------------ epilogue
     // warp w reads TMEM lanes 32*(w%4)..+31 (output rows m0+32q..+31) and the
-    // 16-column chunks c0 = 16*half, +32, ...; each column store is 32
-    // consecutive floats.
+    // 16-column chunks c0 = 16*half, +32, ...
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
+    // this warp's output staging block [16 columns][32 rows] fp32; each
+    // 16-column chunk goes out as one TMA store of a 32 x 16 box (dW rows
+    // e*n_total + n, m contiguous), so the epilogue's writes leave through the
+    // TMA engine rather than the load/store pipe the row gather uses
+    const uint32_t ostg = sbase + (uint32_t)p.stages * kWStageBytes + (uint32_t)(warp - 2) * 2048u;
     uint32_t tc = 0, qi = 0;
     for (;;) {
       const int t = pop_tile(qi, kErrWaitAccum);
@@ -275,14 +281,26 @@ __global__ void __launch_bounds__(kWThreads, 1)
           uint32_t v[16];
           tmem_ld16(tl + (uint32_t)(a * p.tile_n + c), v);
           tmem_ld_wait();
+          // the warp's previous block has left the staging buffer
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            dst[(size_t)(c + j) * p.m_total + a * kWM] = __uint_as_float(v[j]);
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(ostg + (uint32_t)(j * 128 + lane * 4)),
+                         "f"(__uint_as_float(v[j]))
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmO, ostg, T.m0 + a * kWM + q * 32, T.e * p.n_total + T.n0 + c);
+            bulk_commit();
+          }
         }
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(smem_u32(&tmem_empty_bar[b]));
     }
+    if (lane == 0) bulk_wait_all();  // the last stores have read their staging and landed
   } else {
     // ------------------------------------------------------------ token-row gather
     // Stage row r (slot slot0 + 64kt + r) of 64-feature chunk c holds
@@ -383,7 +401,7 @@ int launch_wgrad(const WgradArgs& a, cudaStream_t s) {
   p.sched = a.sched;
   p.out = a.out;
   p.err = a.err;
-  CUtensorMap tmD, tmD2;
+  CUtensorMap tmD, tmD2, tmO;
   const int tile_n = ((a.dw13 ? 2 * a.I : a.H) % kWN == 0) ? kWN : 128;
   if (a.dw13) {
     // M = h (x gathered), N = k over 2I (dPre rows)
@@ -415,15 +433,19 @@ int launch_wgrad(const WgradArgs& a, cudaStream_t s) {
   p.n_tiles = p.n_total / p.tile_n;
   p.buf_stride = (uint32_t)(2 * p.tile_n);
   p.n_buf = 2 * p.buf_stride <= kWTmemCols ? 2 : 1;
-  p.stages = (int)((kWSmemBudget - 1024u) / kWStageBytes);
+  // dW as a 2-D fp32 matrix [E * n_total rows, m_total], stored in 32 x 16 boxes
+  if (!make_map_plain(&tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.out, (uint64_t)p.m_total,
+                      (uint64_t)p.E * p.n_total, 32, 16))
+    return -1;
+  p.stages = (int)((kWSmemBudget - 1024u - kWOutStgBytes) / kWStageBytes);
   if (p.stages > kWMaxStages) p.stages = kWMaxStages;
-  const size_t dyn = (size_t)p.stages * kWStageBytes + 1024;
+  const size_t dyn = (size_t)p.stages * kWStageBytes + kWOutStgBytes + 1024;
   cudaError_t err = cudaSuccess;
   const int sms = wgrad_sms(&err);
   if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
   const int64_t tiles = (int64_t)p.E * p.m_tiles * p.n_tiles;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  moe_wgrad_kernel<<<grid, kWThreads, dyn, s>>>(tmD, tmD2, p);
+  moe_wgrad_kernel<<<grid, kWThreads, dyn, s>>>(tmD, tmD2, tmO, p);
   err = cudaGetLastError();
   return err == cudaSuccess ? 1 : -(int)err;
 }
