@@ -224,13 +224,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 
 // Instruction descriptor, kind::f16: bf16 x bf16 -> f32, both operands K-major.
 // MN-major operand in 128-byte-swizzled tiles of 64 MN elements x 8 K rows:
-// the leading byte offset steps between 64-element MN chunks (each chunk holds
-// 64 K rows of 128 bytes: 8192 bytes), the stride byte offset between 8-row K
-// groups (1024 bytes).
-__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
+// the leading byte offset `lbo` steps between 64-element MN chunks (a chunk
+// holds its K rows of 128 bytes: 64 rows, 8192 bytes, unless the stage holds
+// fewer), the stride byte offset between 8-row K groups (1024 bytes).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo = 8192u) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)(8192u >> 4) << 16;
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)(1024u >> 4) << 32;
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;

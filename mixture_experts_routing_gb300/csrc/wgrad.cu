@@ -41,14 +41,17 @@ namespace {
 
 constexpr int kWM = 128;              // UMMA M: output-contiguous features per accumulator
 constexpr int kWN = 256;              // UMMA N
-constexpr int kWK = 64;               // slots per stage
+// slots per stage: 3 stages of 64 KB (48 slots in 4 stages, 32 in 6 measured
+// slower: dropless ffn_backward 5.62 ms, against 5.85 and 6.33)
+constexpr int kWK = 64;
 constexpr int kWThreads = 448;
 constexpr int kWEpiWarps = 8;         // warps 2-9
 constexpr int kWGatherWarp0 = 10;     // warps 10-13
 constexpr int kWGatherThreads = 128;
 constexpr int kWMaxStages = 8;
-constexpr uint32_t kWABytes = 2 * kWM * kWK * 2;  // 32 KiB: two accumulators' A, 4 chunks
-constexpr uint32_t kWBBytes = kWN * kWK * 2;      // 32 KiB: 4 chunks
+constexpr uint32_t kWChunk = kWK * 128u;          // one 64-feature chunk of a stage
+constexpr uint32_t kWABytes = 2 * kWM * kWK * 2;  // two accumulators' A, 4 chunks
+constexpr uint32_t kWBBytes = kWN * kWK * 2;      // 4 chunks
 constexpr uint32_t kWStageBytes = kWABytes + kWBBytes;
 constexpr uint32_t kWSmemBudget = 223 * 1024;
 // the epilogue's output staging: per warp one 16-column x 32-row fp32 block
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         if (lane == 0) {
           const uint32_t fb = smem_u32(&full_bar[s]);
           const uint32_t st = sbase + (uint32_t)s * kWStageBytes + d_off;
-          mbar_arrive_expect_tx(fb, (uint32_t)d_chunks * 8192u);
+          mbar_arrive_expect_tx(fb, (uint32_t)d_chunks * kWChunk);
           // all 64-column chunks in one 3-D copy ([chunk][slot][64]); tmD2
           // holds 2 chunks, for the ragged last tile of the A side
           tma_load_3d(st, d_chunks == p.d_full ? &tmD : &tmD2, 0, T.slot0 + kt * kWK, dcol0 / 64,
@@ -229,10 +232,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
           const int rem = T.kept - kt * kWK;
           const int ksub = rem >= kWK ? kWK / 16 : (rem + 15) / 16;
           for (int kk = 0; kk < ksub; ++kk) {
-            const uint64_t bdesc = sdesc_sw128_mn(st + kWABytes + (uint32_t)kk * 2048u);
+            const uint64_t bdesc = sdesc_sw128_mn(st + kWABytes + (uint32_t)kk * 2048u, kWChunk);
             for (int a = 0; a < T.nacc; ++a)
               umma_bf16(d + (uint32_t)(a * p.tile_n),
-                        sdesc_sw128_mn(st + (uint32_t)a * 16384u + (uint32_t)kk * 2048u), bdesc,
+                        sdesc_sw128_mn(st + (uint32_t)a * 2u * kWChunk + (uint32_t)kk * 2048u, kWChunk), bdesc,
                         idesc, (kt | kk) != 0);
           }
           umma_commit(smem_u32(&empty_bar[s]));
@@ -328,13 +331,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
       wtile_at(p, t, T);
       const int g_chunks = p.a_gather ? 2 * T.nacc : p.tile_n / 64;  // 4 or 2
       const int cw = g_chunks == 4 ? gw : (gw & 1);
-      const int row_lo = g_chunks == 4 ? 0 : 32 * (gw >> 1);
-      const int n_ins = g_chunks == 4 ? 16 : 8;
+      const int row_lo = g_chunks == 4 ? 0 : (kWK / 2) * (gw >> 1);
+      const int n_ins = (g_chunks == 4 ? kWK : kWK / 2) / 4;
       const int gcol0 = (p.a_gather ? T.m0 : T.n0) + cw * 64 + jj * 8;
       const int chunks = (T.kept + kWK - 1) / kWK;
       auto token_of = [&](int kt, int r) -> int {
         const int ks = kt * kWK + r;
-        return (kt < chunks && ks < T.kept) ? p.sorted_slot_ids[T.slot0 + ks] : -1;
+        return (r < kWK && kt < chunks && ks < T.kept) ? p.sorted_slot_ids[T.slot0 + ks] : -1;
       };
       int nxt0 = token_of(0, lane), nxt1 = token_of(0, lane + 32);
       for (int kt = 0; kt < chunks; ++kt, ++gk) {
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t g = sbase + (uint32_t)s * kWStageBytes + g_off + (uint32_t)cw * 8192u;
+        const uint32_t g = sbase + (uint32_t)s * kWStageBytes + g_off + (uint32_t)cw * kWChunk;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (i < n_ins) {
