@@ -703,7 +703,11 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
   griddep_wait();  // launched after the kernel that writes this one's inputs
   griddep_launch_dependents();
   extern __shared__ uint32_t dyn[];
-  __shared__ int32_t hist[256];
+  // radix histograms: kHistReps copies, warp w counting into copy w % kHistReps
+  // (a hot expert's keys crowd a few bins, and one copy serialised every warp
+  // on the same shared-memory words)
+  constexpr int kHistReps = 8;
+  __shared__ int32_t hist[kHistReps][256];
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t s_cnt[kMaxChunks];
   __shared__ int32_t s_pos[kMaxChunks];
@@ -769,18 +773,40 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
     base = s_base;
     extent = s_extent;
   }
-  for (int cc = warp; cc < C; cc += THREADS / 32) {
-    const int lo = s_lo[cc];
-    const int64_t chunk_base = (int64_t)cc * kTokensPerChunk * K;
-    const int m = (int)min((int64_t)min(s_cnt[cc], kTokensPerChunk * K - lo),
-                           (int64_t)N * K - chunk_base - lo);
-    const int at = s_pos[cc];
-    for (int i = lane; i < m; i += 32) {
-      if (at + i >= n) break;
-      int r = chunk_routes[chunk_base + lo + i];
-      if ((unsigned)r >= (unsigned)(N * K)) r = 0;  // never taken when the tables agree
-      rids[at + i] = r;
-      keys[at + i] = chunk_keys[chunk_base + lo + i];
+  // the expert's routes of chunk cc are lanes 0..m-1 (at most one per token
+  // of the chunk); a warp loads four of its chunks before storing any, so
+  // their load round trips overlap
+  {
+    constexpr int kG = 4;
+    for (int cc0 = warp; cc0 < C; cc0 += kG * (THREADS / 32)) {
+      int rv[kG], at_[kG];
+      uint32_t kv[kG];
+#pragma unroll
+      for (int g = 0; g < kG; ++g) {
+        const int cc = cc0 + g * (THREADS / 32);
+        at_[g] = -1;
+        if (cc < C) {
+          const int lo = s_lo[cc];
+          const int64_t chunk_base = (int64_t)cc * kTokensPerChunk * K;
+          const int m = (int)min((int64_t)min(s_cnt[cc], kTokensPerChunk * K - lo),
+                                 (int64_t)N * K - chunk_base - lo);
+          const int at = s_pos[cc] + lane;
+          if (lane < m && at < n) {
+            rv[g] = chunk_routes[chunk_base + lo + lane];
+            kv[g] = chunk_keys[chunk_base + lo + lane];
+            at_[g] = at;
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kG; ++g) {
+        if (at_[g] >= 0) {
+          int r = rv[g];
+          if ((unsigned)r >= (unsigned)(N * K)) r = 0;  // never taken when the tables agree
+          rids[at_[g]] = r;
+          keys[at_[g]] = kv[g];
+        }
+      }
     }
   }
   __syncthreads();
@@ -788,21 +814,28 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
   uint32_t thr = 0;
   int needed = 0;
   if (select) {
-    // the cap-th largest key, 8 bits at a time from the top; histogram bins
-    // are filled with warp-aggregated atomics (a hot expert's keys crowd a
-    // few bins)
+    // the cap-th largest key, 8 bits at a time from the top
     uint32_t prefix = 0, mask = 0;
     int remaining = cap;
+    int32_t* my_hist = hist[warp % kHistReps];
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += THREADS) hist[i] = 0;
+      for (int i = tid; i < kHistReps * 256; i += THREADS) (&hist[0][0])[i] = 0;
       __syncthreads();
       for (int base = warp * 32; base < n; base += THREADS) {
         const int i = base + lane;
         const uint32_t k = (i < n) ? keys[i] : 0u;
         const bool cand = (i < n) && ((k & mask) == prefix);
         const int bin = cand ? (int)((k >> shift) & 255u) : -1;
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
-        if (cand && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+        if (shift == 24) {
+          // the top byte (sign and high exponent bits) of probabilities takes
+          // one or two values: aggregate the lanes of each bin first
+          const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
+          if (cand && lane == __ffs(peers) - 1) atomicAdd(&my_hist[bin], __popc(peers));
+        } else if (cand) {
+          // lower digits spread over many bins: one atomic per lane (grouping
+          // lanes first measured 3x slower on a hot expert's 8174 keys)
+          atomicAdd(&my_hist[bin], 1);
+        }
       }
       __syncthreads();
       if (warp == 0) {
@@ -811,7 +844,12 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
         // the lane, a short walk finds the bin
         int h[8], sum = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) { h[j] = hist[255 - 8 * lane - j]; sum += h[j]; }
+        for (int j = 0; j < 8; ++j) {
+          h[j] = 0;
+#pragma unroll
+          for (int rr = 0; rr < kHistReps; ++rr) h[j] += hist[rr][255 - 8 * lane - j];
+          sum += h[j];
+        }
         int incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -838,45 +876,62 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
     thr = prefix;
     needed = remaining;  // how many keys equal to thr are kept (lowest tokens first)
   }
-  // each thread owns a contiguous run of the list, so scans follow token order
-  const int ipt = (n + THREADS - 1) / THREADS;
-  const int i0 = min(n, tid * ipt), i1 = min(n, i0 + ipt);
-  int ties = 0;
+  // Warp w owns the contiguous segment [s0, s1) of the list (token order) and
+  // visits it 32 elements at a time, lane l the l-th: shared-memory reads
+  // fall on distinct banks and the kept slots of a step are consecutive.
+  // Ties with the threshold are kept lowest token first: a tie's rank is the
+  // ties before it (the warps before, then ballots within the segment).
+  constexpr int kWarps = THREADS / 32;
+  const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
+  const uint32_t lt = (1u << lane) - 1u;  // lanes below this one
+  // One scan gives both prefixes a warp needs: ties before it (tie_base) and
+  // keys above the threshold before it (gt_base), packed as ties | gt << 16
+  // (each at most 24576). The kept routes before warp w are gt_base +
+  // min(needed, tie_base): every key above the threshold, and the lowest
+  // tokens' ties up to the `needed` the select left.
+  int ties = 0, gt = 0;
   if (select)
-    for (int i = i0; i < i1; ++i) ties += (keys[i] == thr);
-  const int tie_base = block_exclusive_scan<THREADS>(ties, warp_tot);
-  int tie_rank = tie_base;
-  int kept_local = 0;
-  for (int i = i0; i < i1; ++i) {
-    bool kp = true;
-    if (select) {
+    for (int i = s0 + lane; i < s1; i += 32) {
       const uint32_t k = keys[i];
-      kp = k > thr || (k == thr && tie_rank < needed);
-      tie_rank += (k == thr);
+      ties += (k == thr);
+      gt += (k > thr);
     }
-    kept_local += kp;
-  }
-  int pos = block_exclusive_scan<THREADS>(kept_local, warp_tot);
-  // second pass: same keep decisions, now writing the layout
-  tie_rank = tie_base;
-  for (int i = i0; i < i1; ++i) {
-    bool kp = true;
-    if (select) {
-      const uint32_t k = keys[i];
-      kp = k > thr || (k == thr && tie_rank < needed);
-      tie_rank += (k == thr);
-    }
-    const int r = rids[i];
-    if (kp) {
-      const int slot = base + pos;
-      ++pos;
-      sorted_slot_ids[slot] = r / K;
-      slot_prob[slot] = __uint_as_float(keys[i]);  // the key is p' (its bits)
-      token_routes[r] = slot;
-      keep[r] = 1;
-    } else {
-      token_routes[r] = -1;
-      keep[r] = 0;
+  const int packed = __reduce_add_sync(0xFFFFFFFFu, ties | (gt << 16));
+  const int before = __shfl_sync(
+      0xFFFFFFFFu, block_exclusive_scan<THREADS>(lane == 0 ? packed : 0, warp_tot), 0);
+  const int tie_base = before & 0xFFFF;
+  int pos = select ? (before >> 16) + min(needed, tie_base) : s0;
+  // the keep decision of element i (all lanes of the warp take the step)
+  auto keep_step = [&](int i, int& tie_rank) -> bool {
+    if (!select) return i < s1;
+    const uint32_t k = i < s1 ? keys[i] : 0u;
+    const bool tie = i < s1 && k == thr;
+    const uint32_t tb = __ballot_sync(0xFFFFFFFFu, tie);
+    const bool kp = i < s1 && (k > thr || (tie && tie_rank + __popc(tb & lt) < needed));
+    tie_rank += __popc(tb);
+    return kp;
+  };
+  // second walk: same decisions, now writing the layout
+  {
+    int tie_rank = tie_base;
+    for (int i = s0 + lane; i - lane < s1; i += 32) {
+      const bool kp = keep_step(i, tie_rank);
+      const uint32_t kb = __ballot_sync(0xFFFFFFFFu, kp);
+      if (i < s1) {
+        const int r = rids[i];
+        if (kp) {
+          const int slot = base + pos + __popc(kb & lt);
+          sorted_slot_ids[slot] = r / K;
+          slot_prob[slot] = __uint_as_float(keys[i]);  // the key is p' (its bits)
+          token_routes[r] = slot;
+          keep[r] = 1;
+        } else {
+          token_routes[r] = -1;
+          keep[r] = 0;
+        }
+      }
+      pos += __popc(kb);
     }
   }
   const int kept_e = select ? cap : n;
