@@ -301,69 +301,59 @@ __device__ __forceinline__ void dprob_part16(const GemmParams& p, const Tile& T,
 template <int act>
 __device__ __forceinline__ void swiglu_backward_chunk(const GemmParams& p, const Tile& T, int c0,
                                                       int feat0, int lane, uint32_t stg_u,
-                                                      const uint32_t (&v)[16],
+                                                      uint32_t stg2_u, const uint32_t (&v)[16],
                                                       const uint32_t (&gu)[16], const float* ps) {
   const int I = p.inter;
   const int ld2 = 2 * I;
   const size_t row0 = (size_t)(T.slot0 + c0);
-  float o[16], dp[16];
-  if constexpr (act == 1) {
-    // gelu: Phi(g) (one erf) evaluated once per element and kept for all
-    // three outputs; du (and the dprob terms) with act(g) = g Phi(g). The
-    // outputs are computed as they are staged, so no 16-value output array
-    // is live beside Phi (with one, this instantiation spilled past its 128
-    // registers).
-    float cr[16];
+  // One pass over each half of 8 slots: act's factor c (sigma or Phi) once
+  // per element, all three outputs staged as bf16 in the warp's three
+  // 512-byte buffers (dg in stg_u, du and aw in stg2_u), then each lane
+  // copies 16 bytes of each output row. (One pass per output, recomputing c,
+  // made this epilogue instruction-bound: ~1 us a chunk, ~24 us a tile.)
+  const uint32_t st_dg = stg_u, st_du = stg2_u, st_aw = stg2_u + 512u;
+  float dp[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+  for (int h8 = 0; h8 < 2; ++h8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = h8 * 8 + i;
       const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-      cr[j] = act_core<act>(g);
-      dp[j] = g * cr[j] * u * __uint_as_float(v[j]);
+      const float da0 = __uint_as_float(v[j]), pj = ps[c0 + j];
+      const float c = act_core<act>(g);
+      const float a = g * c;  // act(g)
+      const float au = a * u;
+      dp[j] = au * da0;
+      const float dA = pj * da0;
+      const uint32_t at = (uint32_t)(i * kStageRowElems + lane) * 2u;
+      asm volatile("st.shared.b16 [%0], %1;" ::"r"(st_dg + at),
+                   "h"((unsigned short)bf16_bits(dA * u * act_grad_core<act>(g, c)))
+                   : "memory");
+      asm volatile("st.shared.b16 [%0], %1;" ::"r"(st_du + at),
+                   "h"((unsigned short)bf16_bits(dA * a))
+                   : "memory");
+      asm volatile("st.shared.b16 [%0], %1;" ::"r"(st_aw + at),
+                   "h"((unsigned short)bf16_bits(pj * au))
+                   : "memory");
     }
-    dprob_part16(p, T, c0, feat0, lane, dp);  // before the stores: dp is dead after it
-    auto g_of = [&](int j) { return __uint_as_float(gu[j] << 16); };
-    auto u_of = [&](int j) { return __uint_as_float(gu[j] & 0xFFFF0000u); };
-    store_rows16_of(
-        stg_u, lane, [&](int j) { return ps[c0 + j] * __uint_as_float(v[j]) * (g_of(j) * cr[j]); },
-        p.out + row0 * ld2 + I + feat0, ld2);
-    // aw
-    store_rows16_of(
-        stg_u, lane, [&](int j) { return ps[c0 + j] * ((g_of(j) * cr[j]) * u_of(j)); },
-        p.out2 + row0 * I + feat0, I);
-    // dg
-    store_rows16_of(
-        stg_u, lane,
-        [&](int j) {
-          return ps[c0 + j] * __uint_as_float(v[j]) * u_of(j) * act_grad_core<act>(g_of(j), cr[j]);
-        },
-        p.out + row0 * ld2 + feat0, ld2);
-  } else {
-    // silu: sigma is cheap, so each output recomputes it (no extra live array)
-    // dg
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-      const float da0 = __uint_as_float(v[j]);
-      dp[j] = act_fwd<act>(g) * u * da0;
-      o[j] = ps[c0 + j] * da0 * u * act_grad_core<act>(g, act_core<act>(g));
-    }
-    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + feat0, ld2);
-    // du
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = __uint_as_float(gu[j] << 16);
-      o[j] = ps[c0 + j] * __uint_as_float(v[j]) * act_fwd<act>(g);
-    }
-    store_rows16(stg_u, lane, o, p.out + row0 * ld2 + I + feat0, ld2);
-    // aw
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = __uint_as_float(gu[j] << 16), u = __uint_as_float(gu[j] & 0xFFFF0000u);
-      o[j] = ps[c0 + j] * (act_fwd<act>(g) * u);
-    }
-    store_rows16(stg_u, lane, o, p.out2 + row0 * I + feat0, I);
+    __syncwarp();
+    const int row = lane >> 2, part = lane & 3;  // 8 rows x 4 chunks of 16 bytes
+    const uint32_t rd = (uint32_t)(row * kStageRowElems + part * 8) * 2u;
+    const size_t r = row0 + (size_t)(h8 * 8 + row);
+    auto copy16 = [&](uint32_t src, uint16_t* dst) {
+      uint4 val;
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                   : "r"(src)
+                   : "memory");
+      *reinterpret_cast<uint4*>(dst) = val;
+    };
+    copy16(st_dg + rd, p.out + r * ld2 + feat0 + part * 8);
+    copy16(st_du + rd, p.out + r * ld2 + I + feat0 + part * 8);
+    copy16(st_aw + rd, p.out2 + r * I + feat0 + part * 8);
+    __syncwarp();
   }
-  if constexpr (act != 1) dprob_part16(p, T, c0, feat0, lane, dp);
+  dprob_part16(p, T, c0, feat0, lane, dp);
 }
 
 // One instantiation per GemmMode (and per activation for the modes that apply
@@ -732,6 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // filled by 2-byte loads (with gelu, whose backward keeps Phi of 16
     // values live, the register form spilled past the 128 registers)
     const uint32_t pre_u = sbase + p.xs_off + (uint32_t)(warp - 2) * 2048u;
+    // FC2 dgrad: this warp's two more 512-byte output staging buffers
+    const uint32_t stg2_u = sbase + p.xs_off + kPreBufBytes + (uint32_t)(warp - 2) * 1024u;
     auto prefetch_preact = [&](const Tile& T, int c, int f0) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -845,7 +837,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           if (lane < 16) ps_w[lane] = p_cur;
           __syncwarp();
-          swiglu_backward_chunk<kAct>(p, T, c0, feat0 + a * kTileM, lane, stg_u, v, gu, ps_w - c0);
+          swiglu_backward_chunk<kAct>(p, T, c0, feat0 + a * kTileM, lane, stg_u, stg2_u, v, gu,
+                                      ps_w - c0);
         }
       } else {
         for (int c0 = half * 16; c0 < (na > 0 ? T.n_eff : 0); c0 += 32) {
@@ -1265,10 +1258,11 @@ int launch_gemm(const GemmArgs& a, cudaStream_t s) {
   p.sf_off = p.b_off + (((uint32_t)b_rows_cap * 128u + 1023u) & ~1023u);
   p.stage_bytes = p.sf_off + (mx ? 2048u : 0u);  // MX: 2 A and 2 B scale atoms
   // the FP8 modes' epilogue keeps its B-row scales in shared memory, the FC2
-  // dgrad its next pre-activations (the same region)
+  // dgrad its next pre-activations and two more output staging buffers (the
+  // same region)
   const uint32_t xs_bytes = (a.mode == kModeFc1Fp8 || a.mode == kModeFc2Fp8) ? kXsBytes
-                            : a.mode == kModeDgrad2                        ? kPreBufBytes
-                                                                           : 0u;
+                            : a.mode == kModeDgrad2 ? kPreBufBytes + kEpiWarps * 1024u
+                                                    : 0u;
   p.stages = (int)((kSmemBudget - 1024u - kEpiStageBytes - kPsBytes - xs_bytes) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   p.sf_tmem = (uint32_t)(2 * p.max_tn);
