@@ -529,14 +529,18 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(
   const int t0 = c * kTokensPerChunk;
   const int N = live_tokens(n_dev, Nmax);
   const int nt = min(kTokensPerChunk, N - t0);
-  // routes of tokens past the live count: no expert, no slot
+  // every route starts dropped (no slot); the select kernel, which runs
+  // after this grid, marks the kept ones. Routes of tokens past the live
+  // count also get no expert.
   for (int i = threadIdx.x; i < kTokensPerChunk * K; i += blockDim.x) {
     const int t = t0 + i / K;
-    if (t >= N && t < Nmax) {
-      topk_ids[(size_t)t0 * K + i] = -1;
-      topk_p[(size_t)t0 * K + i] = 0.0f;
+    if (t < Nmax) {
       keep[(size_t)t0 * K + i] = 0;
       token_routes[(size_t)t0 * K + i] = -1;
+      if (t >= N) {
+        topk_ids[(size_t)t0 * K + i] = -1;
+        topk_p[(size_t)t0 * K + i] = 0.0f;
+      }
     }
   }
   constexpr int PER = kMaxExperts / 32;
@@ -918,18 +922,13 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
     for (int i = s0 + lane; i - lane < s1; i += 32) {
       const bool kp = keep_step(i, tie_rank);
       const uint32_t kb = __ballot_sync(0xFFFFFFFFu, kp);
-      if (i < s1) {
+      if (kp) {  // a dropped route keeps the top-K kernel's keep = 0, no slot
         const int r = rids[i];
-        if (kp) {
-          const int slot = base + pos + __popc(kb & lt);
-          sorted_slot_ids[slot] = r / K;
-          slot_prob[slot] = __uint_as_float(keys[i]);  // the key is p' (its bits)
-          token_routes[r] = slot;
-          keep[r] = 1;
-        } else {
-          token_routes[r] = -1;
-          keep[r] = 0;
-        }
+        const int slot = base + pos + __popc(kb & lt);
+        sorted_slot_ids[slot] = r / K;
+        slot_prob[slot] = __uint_as_float(keys[i]);  // the key is p' (its bits)
+        token_routes[r] = slot;
+        keep[r] = 1;
       }
       pos += __popc(kb);
     }
