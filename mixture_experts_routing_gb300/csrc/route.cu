@@ -995,6 +995,8 @@ constexpr int kDlWarps = 8;
 
 // Reads the logits from `lg` and writes dl to `ld`, which may be the same
 // buffer (each lane reads its entries before it writes them).
+// PER: values per lane, Ep <= 32 * PER (the split copy's padded width)
+template <int PER>
 __global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
     const float* lg, float* ld, int N, int E, int K, int renorm,
     const int32_t* __restrict__ topk_ids, const float* __restrict__ dprob,
@@ -1006,7 +1008,7 @@ __global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kDlWarps + warp;
   if (t >= N) return;
-  constexpr int PER = kMaxExperts / 32;
+  static_assert(PER * 32 <= kMaxExperts, "pbuf holds kMaxExperts values a token");
   const float* l = lg + (size_t)t * E;
   float v[PER];
   float m = -INFINITY;
@@ -1028,8 +1030,17 @@ __global__ void __launch_bounds__(kDlWarps * 32) router_dlogits_kernel(
   }
   __syncwarp();
   float sum = 0.0f;
-  if (lane == 0)
-    for (int e = 0; e < E; ++e) sum = __fadd_rn(sum, pbuf[warp][e]);  // ascending e
+  if (lane == 0) {  // ascending e; eight terms loaded ahead of their adds
+    int e = 0;
+    for (; e + 8 <= E; e += 8) {
+      float z8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) z8[i] = pbuf[warp][e + i];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum = __fadd_rn(sum, z8[i]);
+    }
+    for (; e < E; ++e) sum = __fadd_rn(sum, pbuf[warp][e]);
+  }
   sum = __shfl_sync(0xFFFFFFFFu, sum, 0);
   __syncwarp();
 #pragma unroll
@@ -1179,9 +1190,11 @@ int launch_router_backward(const RouterBwdArgs& a, cudaStream_t s) {
   int rc = launch_router_split_w(a.wr, a.H, a.E, a.wrs, s);
   if (rc < 0) return rc;
   launched += rc;
-  router_dlogits_kernel<<<(a.N + kDlWarps - 1) / kDlWarps, kDlWarps * 32, 0, s>>>(
-      a.logits ? a.logits : a.dl, a.dl, a.N, a.E, a.K, a.renorm, a.topk_ids, a.dprob, a.dls,
-      router_split_cols(a.E) / 2);
+  const int ep = router_split_cols(a.E) / 2;  // E rounded up to 64
+  auto dlogits = ep <= 64 ? router_dlogits_kernel<2> : ep <= 128 ? router_dlogits_kernel<4>
+                                                                 : router_dlogits_kernel<8>;
+  dlogits<<<(a.N + kDlWarps - 1) / kDlWarps, kDlWarps * 32, 0, s>>>(
+      a.logits ? a.logits : a.dl, a.dl, a.N, a.E, a.K, a.renorm, a.topk_ids, a.dprob, a.dls, ep);
   ++launched;
   rc = launch_router_dwr_mma(a.x, a.dls, a.N, a.H, a.E, a.part, a.err, s);
   if (rc < 0) return rc;
