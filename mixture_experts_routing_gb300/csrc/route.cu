@@ -115,6 +115,81 @@ __device__ __forceinline__ void router_convert(const uint16_t* xsl, float* as, i
   }
 }
 
+// Thread rows of a CTA at most: 512 threads, 32 rows, a multiple of 4.
+template <int TX>
+__host__ __device__ constexpr int router_ty_max() {
+  return (kRMaxThreads / TX < 32 ? kRMaxThreads / TX : 32) / 4 * 4;
+}
+
+// The conversion above with each thread's (row, chunk) pairs worked out once
+// per CTA: the same pairs recur every stage, and the division by the
+// runtime row count and the position arithmetic then leave the stage loop.
+// The fp32 tile has the compile-time token stride RMS.
+template <int KB, bool kSw128, int RMS, int CMAX>
+struct RouterConvertPlan {
+  // per chunk: bf16 offset in the stage's x tile << 16 | float offset of its
+  // first value in the fp32 tile (both below 2^15); -1 for no chunk
+  int item[CMAX];
+  static_assert(7 * 32 * KB < (1 << 15) && KB * RMS < (1 << 15), "offsets fit 15 bits");
+  __device__ __forceinline__ RouterConvertPlan(int rows, int tid, int NT) {
+#pragma unroll
+    for (int i = 0; i < CMAX; ++i) {
+      const int c = tid + i * NT;
+      item[i] = -1;
+      if (c < rows * (KB / 8)) {
+        const int m = c % rows, q = c / rows;
+        const int src = m * KB + (kSw128 ? (q ^ (m & 7)) : q) * 8;
+        item[i] = (src << 16) | (q * 8 * RMS + (m / kRTM) * kRPad + m % kRTM);
+      }
+    }
+  }
+  __device__ __forceinline__ void run(const uint16_t* xsl, float* as) const {
+#pragma unroll
+    for (int i = 0; i < CMAX; ++i) {
+      if (item[i] < 0) continue;
+      const uint4 v = *reinterpret_cast<const uint4*>(xsl + (item[i] >> 16));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float* d = as + (item[i] & 0xFFFF);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        d[(2 * j) * RMS] = __uint_as_float(w[j] << 16);
+        d[(2 * j + 1) * RMS] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+  }
+};
+
+// One stage of the fma chains with the compile-time token stride RMS: the
+// operand loads of step k+1 are issued before the fmas of step k, so their
+// shared-memory latency overlaps the 28 fmas (the chains are unchanged).
+template <int BN, int KB, int RMS>
+__device__ __forceinline__ void router_fma_stage_c(float (&acc)[kRTM][kRTN], const float* as,
+                                                   const float* bsl, int ty, int tx) {
+  const float* ap = as + ty * kRPad;
+  const float* bp = bsl + tx * kRTN;
+  float4 a0 = *reinterpret_cast<const float4*>(ap);
+  float4 a1 = *reinterpret_cast<const float4*>(ap + 4);
+  float4 b = *reinterpret_cast<const float4*>(bp);
+#pragma unroll
+  for (int kk = 0; kk < KB; ++kk) {
+    float4 a0n = a0, a1n = a1, bn = b;
+    if (kk + 1 < KB) {
+      a0n = *reinterpret_cast<const float4*>(ap + (kk + 1) * RMS);
+      a1n = *reinterpret_cast<const float4*>(ap + (kk + 1) * RMS + 4);
+      bn = *reinterpret_cast<const float4*>(bp + (kk + 1) * BN);
+    }
+    const float av[kRTM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z};
+    const float bv[kRTN] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < kRTM; ++i)
+#pragma unroll
+      for (int j = 0; j < kRTN; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+    a0 = a0n;
+    a1 = a1n;
+    b = bn;
+  }
+}
+
 // One stage of the fma chains: acc[i][j] += x[token i][k] * W_r[k][expert j]
 // for k ascending over the KB values of the stage.
 template <int BN, int KB>
@@ -149,6 +224,7 @@ __device__ __forceinline__ void router_store(const float (&acc)[kRTM][kRTN], flo
     }
   }
 }
+
 
 // cp.async form: any E (W_r rows read 16 or 4 bytes at a time).
 template <int TX>
@@ -228,14 +304,14 @@ struct RouterTmaLayout {
   uint32_t xbytes, stage, as_off, bar_off, total;
 };
 template <int KB, int NS>
-__host__ __device__ inline RouterTmaLayout router_tma_layout(int bm, int bn, int ty) {
+__host__ __device__ inline RouterTmaLayout router_tma_layout(int bm, int bn, int rms) {
   RouterTmaLayout L;
   // a 128-byte-swizzled x tile (KB = 64) starts on a 1024-byte boundary
   constexpr uint32_t kAlign = KB == 64 ? 1024u : 128u;
   L.xbytes = ((uint32_t)bm * KB * 2 + kAlign - 1u) & ~(kAlign - 1u);
   L.stage = L.xbytes + (uint32_t)KB * bn * 4;
   L.as_off = NS * L.stage;
-  L.bar_off = L.as_off + 2u * KB * ty * kRPad * 4;
+  L.bar_off = L.as_off + 2u * KB * rms * 4;
   L.total = L.bar_off + NS * 8 + kAlign;  // + slack for aligning the base
   return L;
 }
@@ -257,12 +333,14 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
   griddep_wait();  // launched after the kernel that writes this one's inputs
   griddep_launch_dependents();
   constexpr int BN = TX * kRTN;
-  const int NT = blockDim.x, TY = NT / TX, RM = TY * kRPad;
+  constexpr int RMS = router_ty_max<TX>() * kRPad;            // token stride of the fp32 x tile
+  constexpr int CMAX = (kRTM * KB + 8 * TX - 1) / (8 * TX);   // conversion chunks a thread takes
+  const int NT = blockDim.x;
   const int N = live_tokens(n_dev, Nmax);
   const int m0 = blockIdx.y * bm;
   if (m0 >= N) return;
   const int rows = min(bm, N - m0);
-  const RouterTmaLayout L = router_tma_layout<KB, NS>(bm, BN, TY);
+  const RouterTmaLayout L = router_tma_layout<KB, NS>(bm, BN, RMS);
   extern __shared__ __align__(16) uint8_t rsm_raw[];
   constexpr uint32_t kAlign = KB == 64 ? 1024u : 128u;
   uint8_t* rsm = rsm_raw + ((kAlign - (smem_u32(rsm_raw) & (kAlign - 1u))) & (kAlign - 1u));
@@ -275,7 +353,8 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
   const int n0 = blockIdx.x * BN;
   const int KT = H / KB;
   const uint32_t tx_bytes = (uint32_t)bm * KB * 2 + (uint32_t)KB * BN * 4;
-  for (int i = tid; i < 2 * KB * RM; i += NT) as[i] = 0.0f;
+  for (int i = tid; i < 2 * KB * RMS; i += NT) as[i] = 0.0f;
+  const RouterConvertPlan<KB, KB == 64, RMS, CMAX> plan(rows, tid, NT);
   if (tid == 0) {
     tma_prefetch_desc(&tmx);
     tma_prefetch_desc(&tmw);
@@ -307,22 +386,22 @@ __global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
   bool ok = mbar_wait(bar0, 0u, err, kErrWaitRouter);
   if (ok) {
     ++waited;
-    router_convert<KB, KB == 64>(reinterpret_cast<const uint16_t*>(rsm), as, rows, RM, tid, NT);
+    plan.run(reinterpret_cast<const uint16_t*>(rsm), as);
   }
   for (int kt = 0; kt < KT; ++kt) {
     if (!__syncthreads_and(ok)) break;
     if (tid == 0 && kt + NS - 1 < KT) issue(kt + NS - 1);
     const int slot = kt % NS;
-    router_fma_stage<BN, KB>(acc, as + (kt & 1) * KB * RM,
-                         reinterpret_cast<const float*>(rsm + (size_t)slot * L.stage + L.xbytes),
-                         RM, ty, tx);
+    router_fma_stage_c<BN, KB, RMS>(
+        acc, as + (kt & 1) * KB * RMS,
+        reinterpret_cast<const float*>(rsm + (size_t)slot * L.stage + L.xbytes), ty, tx);
     if (kt + 1 < KT) {
       const int ns = (kt + 1) % NS;
       ok = mbar_wait(bar0 + 8u * ns, (uint32_t)((kt + 1) / NS) & 1u, err, kErrWaitRouter);
       if (ok) {
         ++waited;
-        router_convert<KB, KB == 64>(reinterpret_cast<const uint16_t*>(rsm + (size_t)ns * L.stage),
-                       as + ((kt + 1) & 1) * KB * RM, rows, RM, tid, NT);
+        plan.run(reinterpret_cast<const uint16_t*>(rsm + (size_t)ns * L.stage),
+                 as + ((kt + 1) & 1) * KB * RMS);
       }
     }
   }
@@ -419,10 +498,19 @@ int router_sm_count(cudaError_t* err) {
   return *err == cudaSuccess ? n : 0;
 }
 
+// Dynamic shared memory of a TMA-form CTA, at least kRouterOneCta: the work
+// split gives each SM one token group, and two CTAs of less than half the
+// SM's 228 KB may share an SM while another idles (measured with the kernel
+// launched while the previous launch's route-list kernels still held SMs:
+// qwen3_30b route_align 0.200 ms per call in back-to-back graph replays,
+// 0.130 ms with the floor).
+constexpr uint32_t kRouterOneCta = 116u * 1024u;
+inline uint32_t lg_smem(uint32_t b) { return b < kRouterOneCta ? kRouterOneCta : b; }
+
 template <int TX>
 cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaStream_t s) {
   constexpr int BN = TX * kRTN;
-  constexpr int kTyMax = (kRMaxThreads / TX < 32 ? kRMaxThreads / TX : 32) / 4 * 4;
+  constexpr int kTyMax = router_ty_max<TX>();
   const int gx = (a.E + BN - 1) / BN;
   const int groups = sms / gx > 0 ? sms / gx : 1;
   int bm = (a.N + groups - 1) / groups;
@@ -439,11 +527,11 @@ cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaS
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(router_logits_tma_kernel<TX, 32, 4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)router_tma_layout<32, 4>(kTyMax * kRTM, BN, kTyMax).total);
+                             (int)lg_smem(router_tma_layout<32, 4>(kTyMax * kRTM, BN, kTyMax * kRPad).total));
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(router_logits_tma_kernel<TX, 64, 2>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)router_tma_layout<64, 2>(kTyMax * kRTM, BN, kTyMax).total);
+                                (int)lg_smem(router_tma_layout<64, 2>(kTyMax * kRTM, BN, kTyMax * kRPad).total));
   });
   if (err != cudaSuccess) return err;
   dim3 g(gx, (a.N + bm - 1) / bm);
@@ -464,11 +552,11 @@ cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaS
                      (uint64_t)a.H, BN, kb)) {
     if (wide)
       launch_pdl(router_logits_tma_kernel<TX, 64, 2>, dim3(g), dim3(ty * TX),
-                 router_tma_layout<64, 2>(bm, BN, ty).total, s, tmx, tmw, a.bias, a.ws.logits, a.N,
+                 lg_smem(router_tma_layout<64, 2>(bm, BN, kTyMax * kRPad).total), s, tmx, tmw, a.bias, a.ws.logits, a.N,
                  a.n_dev, a.H, a.E, bm, a.err);
     else
       launch_pdl(router_logits_tma_kernel<TX, 32, 4>, dim3(g), dim3(ty * TX),
-                 router_tma_layout<32, 4>(bm, BN, ty).total, s, tmx, tmw, a.bias, a.ws.logits, a.N,
+                 lg_smem(router_tma_layout<32, 4>(bm, BN, kTyMax * kRPad).total), s, tmx, tmw, a.bias, a.ws.logits, a.N,
                  a.n_dev, a.H, a.E, bm, a.err);
   } else {
     launch_pdl(router_logits_kernel<TX>, dim3(g), dim3(ty * TX), router_smem_bytes(bm, BN, ty), s, 
