@@ -326,7 +326,10 @@ __host__ __device__ inline RouterTmaLayout router_tma_layout(int bm, int bn, int
 // out of time records kErrWaitRouter, waits (bounded) for its copies in
 // flight and leaves without writing logits.
 template <int TX, int KB, int NS>
-__global__ void __launch_bounds__(kRMaxThreads) router_logits_tma_kernel(
+// (At most one CTA per SM is resident, and saying so lets the compiler keep
+// more operand loads in flight: 64 -> 79..107 registers, qwen3_30b's
+// route_align 0.130 -> 0.125 ms, dropless N=16384's 0.236 -> 0.229 ms.)
+__global__ void __launch_bounds__(kRMaxThreads, 1) router_logits_tma_kernel(
     const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
     const float* __restrict__ bias, float* __restrict__ logits, int Nmax,
     const int32_t* __restrict__ n_dev, int H, int E, int bm, uint32_t* __restrict__ err) {
@@ -573,7 +576,11 @@ cudaError_t launch_router_logits(const RouteArgs& a, cudaStream_t s) {
   const int sms = router_sm_count(&err);
   if (sms <= 0) return err != cudaSuccess ? err : cudaErrorUnknown;
   const int64_t threads = (int64_t)a.N * ((a.E + 1) / 2);
-  if (threads <= (int64_t)sms * 64) {  // at most 4 chains per fp32 lane of the GPU
+  // Fewer than 32 experts: always (the tiled forms would run a 32-expert
+  // tile, and without TMA: E = 16, N = 4096, H = 4096 took 0.238 ms of
+  // route_align tiled, 0.101 ms here; E = 8, N = 16384, H = 2048 0.179 ->
+  // 0.086 ms; E = 16, N = 16384, H = 4096 0.334 -> 0.244 ms).
+  if (a.E < 32 || threads <= (int64_t)sms * 64) {
     const unsigned blocks = (unsigned)((threads + kRSmallThreads - 1) / kRSmallThreads);
     const bool vec2 = (a.E % 2 == 0) && ((reinterpret_cast<uintptr_t>(a.wr) & 7u) == 0);
     if (vec2)
@@ -794,10 +801,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
 // chunk tables, select the `cap` highest p' (ties to the lower token) and
 // write the expert's part of the route-list layout. A thread owns one chunk
 // column, so THREADS >= the chunk count: 256 threads for batches of up to
-// 2048 tokens (fewer CTA-wide barriers to wait on), 1024 above (at most 32
-// registers a thread, so two such CTAs share an SM).
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select_kernel(
+// 2048 tokens (fewer CTA-wide barriers to wait on), 1024 above: MINB = 2
+// (at most 32 registers a thread, so two such CTAs share an SM) when there
+// are more experts than SMs, else MINB = 1 (64 registers: no spills, and the
+// gather keeps eight chunk loads of a warp in flight instead of four).
+template <int THREADS, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB) route_select_kernel(
     const int32_t* __restrict__ chunk_counts, const int32_t* __restrict__ chunk_lofs,
     const int32_t* __restrict__ chunk_routes, const uint32_t* __restrict__ chunk_keys, int Nmax,
     const int32_t* __restrict__ n_dev, int E, int K, int cap_num, int cap_den, int bm,
@@ -815,6 +824,12 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
   // on the same shared-memory words)
   constexpr int kHistReps = 8;
   __shared__ int32_t hist[kHistReps][256];
+  // the keys still in the running after the top 16 bits are fixed, gathered
+  // during the third pass so the last pass reads only them (a hot expert's
+  // 8174 keys leave a few hundred); kept only when they fit
+  constexpr int kCBuf = 2048;
+  __shared__ uint32_t cbuf[kCBuf];
+  __shared__ int32_t s_nc;
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t s_cnt[kMaxChunks];
   __shared__ int32_t s_pos[kMaxChunks];
@@ -884,7 +899,7 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
   // of the chunk); a warp loads four of its chunks before storing any, so
   // their load round trips overlap
   {
-    constexpr int kG = 4;
+    constexpr int kG = (THREADS >= 1024 && MINB == 1) ? 8 : 4;
     for (int cc0 = warp; cc0 < C; cc0 += kG * (THREADS / 32)) {
       int rv[kG], at_[kG];
       uint32_t kv[kG];
@@ -924,15 +939,27 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
     // the cap-th largest key, 8 bits at a time from the top
     uint32_t prefix = 0, mask = 0;
     int remaining = cap;
+    int nc = -1;  // keys in cbuf (the last pass's source), -1: read them all
+    if (tid == 0) s_nc = 0;  // (the first pass's barriers order this before any append)
     int32_t* my_hist = hist[warp % kHistReps];
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < kHistReps * 256; i += THREADS) (&hist[0][0])[i] = 0;
       __syncthreads();
-      for (int base = warp * 32; base < n; base += THREADS) {
+      const uint32_t* src = nc >= 0 ? cbuf : keys;
+      const int ns = nc >= 0 ? nc : n;
+      for (int base = warp * 32; base < ns; base += THREADS) {
         const int i = base + lane;
-        const uint32_t k = (i < n) ? keys[i] : 0u;
-        const bool cand = (i < n) && ((k & mask) == prefix);
+        const uint32_t k = (i < ns) ? src[i] : 0u;
+        const bool cand = (i < ns) && ((k & mask) == prefix);
         const int bin = cand ? (int)((k >> shift) & 255u) : -1;
+        if (MINB == 1 && shift == 8) {  // (the 32-register form would spill)
+          // keep the candidates (top 16 bits fixed) for the last pass
+          const uint32_t cb = __ballot_sync(0xFFFFFFFFu, cand);
+          int at = 0;
+          if (lane == 0 && cb != 0u) at = atomicAdd(&s_nc, __popc(cb));
+          at = __shfl_sync(0xFFFFFFFFu, at, 0) + __popc(cb & ((1u << lane) - 1u));
+          if (cand && at < kCBuf) cbuf[at] = k;
+        }
         if (shift == 24) {
           // the top byte (sign and high exponent bits) of probabilities takes
           // one or two values: aggregate the lanes of each bin first
@@ -979,6 +1006,7 @@ __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 2 : 1) route_select
       remaining = s_remaining;
       prefix = s_prefix;
       mask |= 0xFFu << shift;
+      if (MINB == 1 && shift == 8) nc = s_nc <= kCBuf ? s_nc : -1;
     }
     thr = prefix;
     needed = remaining;  // how many keys equal to thr are kept (lowest tokens first)
@@ -1228,11 +1256,14 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
     // raise the kernel's dynamic shared-memory limit once per device
     static DeviceOnce smem_set;
     err = once_per_device(smem_set, nullptr, [](int, int*) {
-      cudaError_t e = cudaFuncSetAttribute(route_select_kernel<1024>,
+      cudaError_t e = cudaFuncSetAttribute(route_select_kernel<1024, 2>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kMaxTokens * 8);
       if (e != cudaSuccess) return e;
-      return cudaFuncSetAttribute(route_select_kernel<kSelSmallThreads>,
+      e = cudaFuncSetAttribute(route_select_kernel<1024, 1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxTokens * 8);
+      if (e != cudaSuccess) return e;
+      return cudaFuncSetAttribute(route_select_kernel<kSelSmallThreads, 1>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kSelSmallThreads * kTokensPerChunk * 8);
     });
@@ -1242,7 +1273,10 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   // token, and above that many keys per thread (a Zipf-skewed 8192-token batch:
   // route_align 0.168 -> 0.195 ms) cost more than the barriers save
   const bool small = a.N <= kSelSmallMaxTokens;
-  launch_pdl(small ? route_select_kernel<kSelSmallThreads> : route_select_kernel<1024>,
+  const int sms = router_sm_count(&err);
+  if (sms <= 0) return -(int)(err != cudaSuccess ? err : cudaErrorUnknown);
+  launch_pdl(small ? route_select_kernel<kSelSmallThreads, 1>
+                   : (a.E <= sms ? route_select_kernel<1024, 1> : route_select_kernel<1024, 2>),
              dim3(a.E), dim3(small ? kSelSmallThreads : 1024), dyn, s, a.ws.chunk_counts,
              a.ws.chunk_lofs, a.ws.chunk_routes, a.ws.chunk_keys, a.N, a.n_dev, a.E, a.K,
              a.cap_num, a.cap_den, a.bm, a.dropless, a.ladder, (int)a.s_max, a.keep,

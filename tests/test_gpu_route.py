@@ -35,6 +35,13 @@ def _w(N, H, E, K, I=128, cn=1, cd=1, **kw):
     (_w(0, 128, 8, 2), 16),            # empty batch
     (_w(24576, 128, 8, 2), 32),        # the largest supported token count
     (_w(24576, 128, 64, 6, cn=0, cd=1, zipf_s=0.8, ladder=(2, 4), ladder_den=2), 32),  # dropless
+    # each form of the logits kernel at a size past the few-chains bound:
+    (_w(4096, 1024, 16, 4, cn=5, cd=4), 32),   # E < 32: one thread per token and expert pair
+    (_w(2048, 256, 31, 3), 16),                # odd E: the same, scalar W_r loads
+    (_w(4096, 2048, 32, 4), 32),               # 32-expert tiles, TMA stages of 32
+    (_w(3000, 4096, 64, 6, cn=5, cd=4), 64),   # 64-expert tiles, TMA stages of 64
+    (_w(3000, 512, 48, 4), 32),                # E below the 64-wide tile: cp.async form
+    (_w(2500, 256, 130, 6), 32),               # E not a multiple of 4: cp.async form, 4-byte W_r loads
 ])
 def test_route_align_edge_shapes(w, bm):
     P = Problem(w, bm=bm, host_weights=False, with_ffn=False)
