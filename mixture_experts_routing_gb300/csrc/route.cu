@@ -225,7 +225,6 @@ __device__ __forceinline__ void router_store(const float (&acc)[kRTM][kRTN], flo
   }
 }
 
-
 // cp.async form: any E (W_r rows read 16 or 4 bytes at a time).
 template <int TX>
 __global__ void __launch_bounds__(kRMaxThreads) router_logits_kernel(
@@ -324,11 +323,12 @@ __host__ __device__ inline RouterTmaLayout router_tma_layout(int bm, int bn, int
 // every thread is done with the stage slot the producer refills and with the
 // x tile the next conversion overwrites. Waits are bounded; a CTA that runs
 // out of time records kErrWaitRouter, waits (bounded) for its copies in
-// flight and leaves without writing logits.
+// flight and leaves without writing logits. At most one CTA per SM is
+// resident (the shared-memory floor below), and declaring it lets the
+// compiler keep more operand loads in flight: 64 -> 79..107 registers,
+// qwen3_30b's route_align 0.130 -> 0.125 ms, dropless N=16384's 0.236 ->
+// 0.229 ms.
 template <int TX, int KB, int NS>
-// (At most one CTA per SM is resident, and saying so lets the compiler keep
-// more operand loads in flight: 64 -> 79..107 registers, qwen3_30b's
-// route_align 0.130 -> 0.125 ms, dropless N=16384's 0.236 -> 0.229 ms.)
 __global__ void __launch_bounds__(kRMaxThreads, 1) router_logits_tma_kernel(
     const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
     const float* __restrict__ bias, float* __restrict__ logits, int Nmax,
@@ -528,13 +528,13 @@ cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaS
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)router_smem_bytes(kTyMax * kRTM, BN, kTyMax));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(router_logits_tma_kernel<TX, 32, 4>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)lg_smem(router_tma_layout<32, 4>(kTyMax * kRTM, BN, kTyMax * kRPad).total));
+    e = cudaFuncSetAttribute(
+        router_logits_tma_kernel<TX, 32, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)lg_smem(router_tma_layout<32, 4>(kTyMax * kRTM, BN, kTyMax * kRPad).total));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(router_logits_tma_kernel<TX, 64, 2>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)lg_smem(router_tma_layout<64, 2>(kTyMax * kRTM, BN, kTyMax * kRPad).total));
+    return cudaFuncSetAttribute(
+        router_logits_tma_kernel<TX, 64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)lg_smem(router_tma_layout<64, 2>(kTyMax * kRTM, BN, kTyMax * kRPad).total));
   });
   if (err != cudaSuccess) return err;
   dim3 g(gx, (a.N + bm - 1) / bm);
@@ -555,12 +555,12 @@ cudaError_t launch_router_logits_tx(const RouteArgs& a, int vec4, int sms, cudaS
                      (uint64_t)a.H, BN, kb)) {
     if (wide)
       launch_pdl(router_logits_tma_kernel<TX, 64, 2>, dim3(g), dim3(ty * TX),
-                 lg_smem(router_tma_layout<64, 2>(bm, BN, kTyMax * kRPad).total), s, tmx, tmw, a.bias, a.ws.logits, a.N,
-                 a.n_dev, a.H, a.E, bm, a.err);
+                 lg_smem(router_tma_layout<64, 2>(bm, BN, kTyMax * kRPad).total), s, tmx, tmw,
+                 a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, bm, a.err);
     else
       launch_pdl(router_logits_tma_kernel<TX, 32, 4>, dim3(g), dim3(ty * TX),
-                 lg_smem(router_tma_layout<32, 4>(bm, BN, kTyMax * kRPad).total), s, tmx, tmw, a.bias, a.ws.logits, a.N,
-                 a.n_dev, a.H, a.E, bm, a.err);
+                 lg_smem(router_tma_layout<32, 4>(bm, BN, kTyMax * kRPad).total), s, tmx, tmw,
+                 a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, bm, a.err);
   } else {
     launch_pdl(router_logits_kernel<TX>, dim3(g), dim3(ty * TX), router_smem_bytes(bm, BN, ty), s, 
         a.x, a.wr, a.bias, a.ws.logits, a.N, a.n_dev, a.H, a.E, bm, vec4);
