@@ -68,6 +68,17 @@ MUTATIONS = [
      "oracle_e8m0_decode(ws[rg * nb])", lambda: mx.test_fc1_mx_matches_fp64_dequantised_reference(0)),
     ("MX FC2 h scaled by its first block", "oracle_e8m0_decode(hsr[b])", "oracle_e8m0_decode(hsr[0])",
      lambda: mx.test_fc2_mx_matches_fp64_dequantised_reference()),
+    ("router logits with a rounded product before each add",
+     "acc = fmaf(bf16_to_f32(x[(size_t)t * H + h]), wr[(size_t)h * E + e], acc);",
+     "acc = acc + bf16_to_f32(x[(size_t)t * H + h]) * wr[(size_t)h * E + e];",
+     lambda: fp.test_router_is_the_exact_fp32_chain()),
+    ("router logits summed over descending h",
+     "for (int h = 0; h < H; ++h) acc = fmaf(bf16_to_f32(x",
+     "for (int h = H - 1; h >= 0; --h) acc = fmaf(bf16_to_f32(x",
+     lambda: fp.test_router_is_the_exact_fp32_chain()),
+    ("router bias added before the chain", "      float acc = 0.0f;\n      for (int h = 0; h < H; ++h) acc = fmaf(",
+     "      float acc = bias ? bias[e] : 0.0f;\n      for (int h = 0; h < H; ++h) acc = fmaf(",
+     lambda: fp.test_router_is_the_exact_fp32_chain()),
     ("router dx with the weight transposed", "acc = acc + dlogits[(size_t)t * E + e] * wr[(size_t)h * E + e];",
      "acc = acc + dlogits[(size_t)t * E + e] * wr[(size_t)e * H + h];",
      lambda: rb.test_router_backward_matches_central_differences(2, True)),

@@ -85,6 +85,100 @@ def test_router_matches_fp64_library_routines(N, H, E, K, use_bias):
     assert np.all(p[:, :-1] >= p[:, 1:])
 
 
+# Exact fp32 arithmetic: each operation is the exact rational result rounded
+# once to the nearest fp32 value, ties to the even significand (IEEE 754
+# round-to-nearest-even; normal and subnormal range, no overflow here).
+def _rn32(q):
+    from fractions import Fraction
+    if q == 0:
+        return np.float32(0.0)
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    elif Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, -126) - 23)
+    scaled = a / quantum
+    m = scaled.numerator // scaled.denominator
+    rem = scaled - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    v = float(m * quantum)
+    return np.float32(v if q > 0 else -v)
+
+
+def _q(v):
+    from fractions import Fraction
+    return Fraction(float(v))
+
+
+def _exact_router(x, wr, bias, K, *, fused=True, ascending=True):
+    """The router step by step in exact fp32 arithmetic: each logit the
+    sequential chain l = fma(x[h], W_r[h,e], l) over ascending h, then + b[e];
+    z = exp(l - max) with the oracle's exp (pinned to libm above); the
+    denominator summed in ascending e; p = z / sum; K picks of the largest p
+    (the lower e on ties); p' = p / (the picked p summed in pick order).
+    fused=False / ascending=False give the plausible wrong forms the pin must
+    tell apart (a rounded product before each add; descending h)."""
+    xf = _f(x)
+    N, H = xf.shape
+    E = wr.shape[1]
+    logits = np.empty((N, E), np.float32)
+    probs = np.empty((N, E), np.float32)
+    ids = np.empty((N, K), np.int32)
+    pk = np.empty((N, K), np.float32)
+    hs = range(H) if ascending else range(H - 1, -1, -1)
+    for t in range(N):
+        for e in range(E):
+            acc = np.float32(0.0)
+            for h in hs:
+                if fused:
+                    acc = _rn32(_q(xf[t, h]) * _q(wr[h, e]) + _q(acc))
+                else:
+                    acc = _rn32(_q(_rn32(_q(xf[t, h]) * _q(wr[h, e]))) + _q(acc))
+            logits[t, e] = _rn32(_q(acc) + _q(0.0 if bias is None else bias[e]))
+        m = max(logits[t])
+        z = [oracle.exp_f32(np.array([_rn32(_q(logits[t, e]) - _q(m))], np.float32))[0]
+             for e in range(E)]
+        s = np.float32(0.0)
+        for e in range(E):
+            s = _rn32(_q(s) + _q(z[e]))
+        for e in range(E):
+            probs[t, e] = _rn32(_q(z[e]) / _q(s))
+        taken, d = set(), np.float32(0.0)
+        for k in range(K):
+            best = max((e for e in range(E) if e not in taken), key=lambda e: (probs[t, e], -e))
+            taken.add(best)
+            ids[t, k] = best
+            d = _rn32(_q(d) + _q(probs[t, best]))
+        for k in range(K):
+            pk[t, k] = _rn32(_q(probs[t, ids[t, k]]) / _q(d))
+    return ids, pk, probs, logits
+
+
+def test_router_is_the_exact_fp32_chain():
+    """Bit for bit against the step-by-step definition in exact arithmetic:
+    logits, softmax probabilities, picks and renormalised p'. The wrong
+    forms of the logit chain (unfused, descending h) give other bits on
+    these inputs, so the pin tells them apart."""
+    rng = np.random.default_rng(11)
+    N, H, E, K = 6, 24, 7, 3
+    x = _bf16(rng.standard_normal((N, H)))
+    wr = (rng.standard_normal((H, E)) * rng.choice([0.003, 0.05, 0.7], size=(H, E))).astype(np.float32)
+    bias = (rng.standard_normal(E) * 0.3).astype(np.float32)
+    ids, p, probs, logits = oracle.router(x, wr, bias, K, renorm=True, want_probs=True,
+                                          want_logits=True)
+    r_ids, r_p, r_probs, r_logits = _exact_router(x, wr, bias, K)
+    assert np.array_equal(logits.view(np.uint32), r_logits.view(np.uint32))
+    assert np.array_equal(probs.view(np.uint32), r_probs.view(np.uint32))
+    assert np.array_equal(ids, r_ids)
+    assert np.array_equal(p.view(np.uint32), r_p.view(np.uint32))
+    for wrong in ({"fused": False}, {"ascending": False}):
+        w_logits = _exact_router(x, wr, bias, K, **wrong)[3]
+        assert not np.array_equal(w_logits.view(np.uint32), r_logits.view(np.uint32)), wrong
+
+
 def test_router_without_renorm_returns_softmax_probs():
     rng = np.random.default_rng(3)
     x = _bf16(rng.standard_normal((20, 64)))
