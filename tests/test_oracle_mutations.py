@@ -68,6 +68,10 @@ MUTATIONS = [
      "oracle_e8m0_decode(ws[rg * nb])", lambda: mx.test_fc1_mx_matches_fp64_dequantised_reference(0)),
     ("MX FC2 h scaled by its first block", "oracle_e8m0_decode(hsr[b])", "oracle_e8m0_decode(hsr[0])",
      lambda: mx.test_fc2_mx_matches_fp64_dequantised_reference()),
+    ("exp's sixth-order coefficient off", "p = fmaf(p, r, (float)(1.0 / 720.0));",
+     "p = fmaf(p, r, (float)(1.0 / 700.0));", lambda: fp.test_exp_is_the_stated_method_step_by_step()),
+    ("exp reduction without the low part of ln 2", "  r = fmaf(-n, ln2_lo, r);\n", "",
+     lambda: fp.test_exp_is_the_stated_method_step_by_step()),
     ("router logits with a rounded product before each add",
      "acc = fmaf(bf16_to_f32(x[(size_t)t * H + h]), wr[(size_t)h * E + e], acc);",
      "acc = acc + bf16_to_f32(x[(size_t)t * H + h]) * wr[(size_t)h * E + e];",

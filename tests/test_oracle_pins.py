@@ -179,6 +179,44 @@ def test_router_is_the_exact_fp32_chain():
         assert not np.array_equal(w_logits.view(np.uint32), r_logits.view(np.uint32)), wrong
 
 
+def _exact_exp_steps(v):
+    """exp(v) by the stated method, each fp32 operation exact then rounded
+    once: n = rint(v·log2 e); r = v − n·ln2_hi − n·ln2_lo (two fused steps);
+    the degree-7 Taylor polynomial of e^r in Horner form (fused steps,
+    coefficients 1/k! rounded from double); times 2^n. The constants follow
+    their definitions: log2 e and ln 2 rounded from double to fp32, ln2_lo the
+    double remainder ln 2 − ln2_hi rounded to fp32."""
+    import math
+    from fractions import Fraction
+    if v < -87.0:
+        return np.float32(0.0)
+    f32 = lambda d: _rn32(Fraction(d))
+    log2e, ln2_hi = f32(1.0 / math.log(2.0)), f32(math.log(2.0))
+    ln2_lo = f32(math.log(2.0) - float(ln2_hi))
+    y = _rn32(_q(v) * _q(log2e))
+    fl = math.floor(float(y))
+    n = fl + 1 if (float(y) - fl > 0.5 or (float(y) - fl == 0.5 and fl % 2 == 1)) else fl
+    r = _rn32(-n * _q(ln2_hi) + _q(v))
+    r = _rn32(-n * _q(ln2_lo) + _q(r))
+    p = f32(1.0 / 5040.0)
+    for c in (1.0 / 720.0, 1.0 / 120.0, 1.0 / 24.0, 1.0 / 6.0, 0.5, 1.0, 1.0):
+        p = _rn32(_q(p) * _q(r) + _q(f32(c)))
+    return _rn32(_q(p) * Fraction(2) ** n)
+
+
+def test_exp_is_the_stated_method_step_by_step():
+    """Bit for bit against the method evaluated in exact arithmetic (a
+    coefficient or a reduction term off by a fraction of an ulp passes the
+    libm bound above but not this)."""
+    rng = np.random.default_rng(5)
+    v = np.concatenate([-rng.uniform(0.0, 87.0, 1500), -rng.exponential(1.0, 500),
+                        [0.0, -0.5, -1.0, -0.34657359, -0.34657362, -86.99, -87.0, -88.0]])
+    v = v.astype(np.float32)
+    got = oracle.exp_f32(v)
+    want = np.array([_exact_exp_steps(float(a)) for a in v], np.float32)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
 def test_router_without_renorm_returns_softmax_probs():
     rng = np.random.default_rng(3)
     x = _bf16(rng.standard_normal((20, 64)))
