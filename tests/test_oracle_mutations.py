@@ -72,6 +72,8 @@ MUTATIONS = [
      "p = fmaf(p, r, (float)(1.0 / 700.0));", lambda: fp.test_exp_is_the_stated_method_step_by_step()),
     ("exp reduction without the low part of ln 2", "  r = fmaf(-n, ln2_lo, r);\n", "",
      lambda: fp.test_exp_is_the_stated_method_step_by_step()),
+    ("softmax without the max subtraction", "p[e] = oracle_exp(l[e] - m);", "p[e] = oracle_exp(l[e]);",
+     lambda: fp.test_router_is_the_exact_fp32_chain()),
     ("router logits with a rounded product before each add",
      "acc = fmaf(bf16_to_f32(x[(size_t)t * H + h]), wr[(size_t)h * E + e], acc);",
      "acc = acc + bf16_to_f32(x[(size_t)t * H + h]) * wr[(size_t)h * E + e];",
