@@ -421,7 +421,8 @@ __global__ void __launch_bounds__(kRMaxThreads, 1) router_logits_tma_kernel(
 }
 
 // Few chains (small N*E, where the tiled kernels leave most lanes idle and
-// walk H/32 pipelined stages): one thread per token and 2 consecutive
+// walk H/32 pipelined stages), and every router with fewer than 32 experts
+// (see launch_router_logits): one thread per token and 2 consecutive
 // experts, the whole contraction in registers, x rows and W_r rows read from
 // global memory (shared between threads through L1), the next 16 values of h
 // loaded while the current 16 are multiplied (8 at a time measured 9.0 us on
